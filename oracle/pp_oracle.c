@@ -1,0 +1,540 @@
+/*
+ * ORACLE — test infrastructure only.
+ *
+ * A plain, slow, single-threaded CPU statement of what the parser computes,
+ * used to check the GPU library.  Only the tests, the smoke check and the
+ * benchmark's CPU-baseline leg may load it; the product path never does.
+ * It shares no code, header or table with the CUDA library.
+ *
+ * Source: "ParPaRaw: Massively Parallel Parsing of Delimiter-Separated Raw
+ * Data" (Sections 3.1-3.4 and 4, Figures 2-5).  The method is only a fast
+ * route to the result of sequential DFA parsing (Section 3.1: "A sequential
+ * approach would simply set the starting state of its DFA and read the
+ * symbols of the input beginning to end"), so the oracle *is* that
+ * sequential walk:
+ *   - walk the DFA from the start state byte by byte,
+ *   - classify each byte from (state before, symbol),
+ *   - append value bytes to the current field,
+ *   - close the field at every field/record delimiter, close the record at
+ *     every record delimiter.
+ * The DFA tables are written as switch statements from the state names
+ * EOR/FLD/ENC/ESC/INV (Section 3.1, Figure 3 and its caption about the
+ * invalid state, "reading quotes in FLD state").
+ *
+ * The method's own steps (multi-instance DFA -> state-transition vector,
+ * composite operation, exclusive scan; absolute/relative column offsets) are
+ * stated separately below (or_stv_*, or_colofs_*) so the tests can check
+ * them against the sequential walk on every short input.
+ *
+ * The JSON-like lexer DFA (16 states) follows the prefix-scan lexing scheme
+ * of "Lexing on the GPU: the scan is the easy part" (section "A lexer is a
+ * prefix scan"): one transition function per input symbol; a token begins
+ * where the automaton leaves a finished token for a new one.
+ *
+ * Floats: glibc strtod (correctly rounded, round-half-even).
+ */
+#include <errno.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------ codes */
+/* error bits (a bitmask); the same values are part of the library's ABI   */
+#define E_INVALID_INPUT 1
+#define E_BAD_END_STATE 2
+#define E_COLCOUNT 4
+#define E_NUM_SYNTAX 8
+#define E_NUM_OVERFLOW 16
+#define E_CAPACITY 32
+
+enum { T_DATA = 0, T_FD = 1, T_RD = 2, T_CTRL = 3, T_INVALID = 4, T_BEGIN = 5 };
+enum { C_STR = 0, C_I8 = 1, C_I32 = 2, C_I64 = 3, C_F64 = 4, C_SKIP = 5 };
+
+typedef struct {
+  int32_t error;
+  int32_t pad;
+  uint64_t first_error_offset;
+  uint64_t n_records;
+  uint64_t n_tokens;
+  uint64_t chars_len[64];
+} or_status;
+
+static void flag(or_status* st, int bit, uint64_t off, int with_offset) {
+  st->error |= bit;
+  if (with_offset && off < st->first_error_offset) st->first_error_offset = off;
+}
+
+/* ------------------------------------------------------------ CSV DFA */
+enum { EOR = 0, FLD = 1, ENC = 2, ESC = 3, INV = 4 };
+
+typedef struct { uint8_t fd, rd, q; } csv_syms;
+
+/* One transition of the quoted-CSV DFA.  Returns the next state and writes
+ * the symbol's tag.  Cells (state, symbol) -> (next, tag):
+ *   EOR: quote -> ENC ctrl | fd -> EOR fd | rd -> EOR rd | other -> FLD data
+ *   FLD: quote -> INV      | fd -> EOR fd | rd -> EOR rd | other -> FLD data
+ *   ENC: quote -> ESC ctrl | anything else -> ENC data
+ *   ESC: quote -> ENC data (second quote of a doubled pair)
+ *        fd -> EOR fd | rd -> EOR rd | other -> INV
+ *   INV: everything -> INV                                               */
+static int csv_step(const csv_syms* y, int s, uint8_t b, int* tag) {
+  int is_q = b == y->q, is_fd = b == y->fd, is_rd = b == y->rd;
+  switch (s) {
+    case EOR:
+      if (is_q) { *tag = T_CTRL; return ENC; }
+      if (is_fd) { *tag = T_FD; return EOR; }
+      if (is_rd) { *tag = T_RD; return EOR; }
+      *tag = T_DATA; return FLD;
+    case FLD:
+      if (is_q) { *tag = T_INVALID; return INV; }
+      if (is_fd) { *tag = T_FD; return EOR; }
+      if (is_rd) { *tag = T_RD; return EOR; }
+      *tag = T_DATA; return FLD;
+    case ENC:
+      if (is_q) { *tag = T_CTRL; return ESC; }
+      *tag = T_DATA; return ENC;
+    case ESC:
+      if (is_q) { *tag = T_DATA; return ENC; }
+      if (is_fd) { *tag = T_FD; return EOR; }
+      if (is_rd) { *tag = T_RD; return EOR; }
+      *tag = T_INVALID; return INV;
+    default:
+      *tag = T_INVALID; return INV;
+  }
+}
+static int csv_accepting(int s) { return s == EOR || s == FLD || s == ESC; }
+
+/* ------------------------------------------------------------ lexer DFA */
+enum { L_START = 0, L_WS, L_PUNCT, L_STR_OPEN, L_STR, L_STR_BSL, L_STR_END, L_NEG,
+       L_ZERO, L_INT, L_DOT, L_FRAC, L_EXP_E, L_EXP_SIGN, L_EXP, L_INV };
+enum { G_WS = 0, G_PUNCT, G_QUOTE, G_BSL, G_MINUS, G_PLUS, G_ZERO, G_D19, G_DOT,
+       G_E, G_OTHER };
+
+static int lex_group(uint8_t b) {
+  switch (b) {
+    case ' ': case '\t': case '\n': case '\r': return G_WS;
+    case '{': case '}': case '[': case ']': case ',': case ':': return G_PUNCT;
+    case '"': return G_QUOTE;
+    case '\\': return G_BSL;
+    case '-': return G_MINUS;
+    case '+': return G_PLUS;
+    case '0': return G_ZERO;
+    case '.': return G_DOT;
+    case 'e': case 'E': return G_E;
+    default: return (b >= '1' && b <= '9') ? G_D19 : G_OTHER;
+  }
+}
+/* the state that starts a new token on symbol group g (INV if none) */
+static int lex_begin(int g) {
+  switch (g) {
+    case G_WS: return L_WS;
+    case G_PUNCT: return L_PUNCT;
+    case G_QUOTE: return L_STR_OPEN;
+    case G_MINUS: return L_NEG;
+    case G_ZERO: return L_ZERO;
+    case G_D19: return L_INT;
+    default: return L_INV;
+  }
+}
+static int ends_number(int g) { return g == G_WS || g == G_PUNCT || g == G_QUOTE || g == G_MINUS; }
+
+/* One lexer transition; *begin = 1 when a new token starts at this byte. */
+static int lex_step(int s, uint8_t b, int* begin) {
+  int g = lex_group(b), n;
+  *begin = 0;
+  switch (s) {
+    case L_START: case L_WS: case L_PUNCT: case L_STR_END:
+      n = lex_begin(g);
+      *begin = (n != L_INV) && !(s == L_WS && g == G_WS);
+      return n;
+    case L_STR_OPEN: case L_STR:
+      return g == G_QUOTE ? L_STR_END : g == G_BSL ? L_STR_BSL : L_STR;
+    case L_STR_BSL:
+      return L_STR;
+    case L_NEG:
+      return g == G_ZERO ? L_ZERO : g == G_D19 ? L_INT : L_INV;
+    case L_ZERO:
+      if (g == G_DOT) return L_DOT;
+      if (g == G_E) return L_EXP_E;
+      if (ends_number(g)) { *begin = 1; return lex_begin(g); }
+      return L_INV;
+    case L_INT:
+      if (g == G_ZERO || g == G_D19) return L_INT;
+      if (g == G_DOT) return L_DOT;
+      if (g == G_E) return L_EXP_E;
+      if (ends_number(g)) { *begin = 1; return lex_begin(g); }
+      return L_INV;
+    case L_DOT:
+      return (g == G_ZERO || g == G_D19) ? L_FRAC : L_INV;
+    case L_FRAC:
+      if (g == G_ZERO || g == G_D19) return L_FRAC;
+      if (g == G_E) return L_EXP_E;
+      if (ends_number(g)) { *begin = 1; return lex_begin(g); }
+      return L_INV;
+    case L_EXP_E:
+      if (g == G_PLUS || g == G_MINUS) return L_EXP_SIGN;
+      return (g == G_ZERO || g == G_D19) ? L_EXP : L_INV;
+    case L_EXP_SIGN:
+      return (g == G_ZERO || g == G_D19) ? L_EXP : L_INV;
+    case L_EXP:
+      if (g == G_ZERO || g == G_D19) return L_EXP;
+      if (ends_number(g)) { *begin = 1; return lex_begin(g); }
+      return L_INV;
+    default:
+      return L_INV;
+  }
+}
+static int lex_accepting(int s) {
+  return s == L_START || s == L_WS || s == L_PUNCT || s == L_STR_END || s == L_ZERO ||
+         s == L_INT || s == L_FRAC || s == L_EXP;
+}
+/* token id from the state after the token's last byte */
+static int lex_token_id(int s, uint8_t first_byte) {
+  switch (s) {
+    case L_WS: return 9;
+    case L_PUNCT:
+      switch (first_byte) {
+        case '{': return 0; case '}': return 1; case '[': return 2;
+        case ']': return 3; case ',': return 4; default: return 5;
+      }
+    case L_STR_END: return 6;
+    case L_ZERO: case L_INT: return 7;
+    case L_FRAC: case L_EXP: return 8;
+    default: return 255;
+  }
+}
+
+/* ------------------------------------------------- generic step by kind */
+/* kind 0 = quoted CSV (syms from y), kind 1 = JSON-like lexer             */
+static int step_any(int kind, const csv_syms* y, int s, uint8_t b, int* tag) {
+  if (kind == 0) return csv_step(y, s, b, tag);
+  int begin, n = lex_step(s, b, &begin);
+  *tag = n == L_INV ? T_INVALID : begin ? T_BEGIN : T_DATA;
+  return n;
+}
+static int nstates(int kind) { return kind == 0 ? 5 : 16; }
+
+/* Per-byte state before and tag (the test hook's definition). */
+int or_tags(int kind, uint8_t fd, uint8_t rd, uint8_t q, const uint8_t* in, uint64_t n,
+            uint8_t* state_before, uint8_t* tag) {
+  csv_syms y = {fd, rd, q};
+  int s = kind == 0 ? EOR : L_START;
+  for (uint64_t i = 0; i < n; i++) {
+    int t;
+    state_before[i] = (uint8_t)s;
+    s = step_any(kind, &y, s, in[i], &t);
+    tag[i] = (uint8_t)t;
+  }
+  return s;
+}
+
+/* ------------------------------------------------------ numeric fields */
+/* Integer grammar [+-]?[0-9]+ over the field's value bytes.  Returns 0 ok,
+ * E_NUM_SYNTAX or E_NUM_OVERFLOW; the value is 0 on error and for "".     */
+static int conv_int(const uint8_t* v, size_t n, int64_t lo, int64_t hi, int64_t* out) {
+  *out = 0;
+  if (n == 0) return 0;
+  size_t i = 0;
+  int neg = 0;
+  if (v[0] == '+' || v[0] == '-') { neg = v[0] == '-'; i = 1; }
+  if (i == n) return E_NUM_SYNTAX;
+  for (size_t k = i; k < n; k++)
+    if (v[k] < '0' || v[k] > '9') return E_NUM_SYNTAX;
+  /* magnitude with saturation above 2^63 */
+  unsigned __int128 mag = 0;
+  const unsigned __int128 CAP = ((unsigned __int128)1) << 64;
+  for (; i < n; i++) {
+    mag = mag * 10 + (unsigned)(v[i] - '0');
+    if (mag > CAP) mag = CAP;
+  }
+  __int128 val = neg ? -(__int128)mag : (__int128)mag;
+  if (val < lo || val > hi) return E_NUM_OVERFLOW;
+  *out = (int64_t)val;
+  return 0;
+}
+
+/* Float grammar [+-]?([0-9]+(\.[0-9]*)?|\.[0-9]+)([eE][+-]?[0-9]+)?; the
+ * value is strtod's (correctly rounded).  "" -> 0.0.                      */
+static int conv_f64(const uint8_t* v, size_t n, double* out) {
+  *out = 0.0;
+  if (n == 0) return 0;
+  size_t i = 0, d0 = 0, d1 = 0;
+  if (v[i] == '+' || v[i] == '-') i++;
+  while (i < n && v[i] >= '0' && v[i] <= '9') { i++; d0++; }
+  if (i < n && v[i] == '.') {
+    i++;
+    while (i < n && v[i] >= '0' && v[i] <= '9') { i++; d1++; }
+  }
+  if (d0 + d1 == 0) return E_NUM_SYNTAX;
+  if (i < n && (v[i] == 'e' || v[i] == 'E')) {
+    i++;
+    if (i < n && (v[i] == '+' || v[i] == '-')) i++;
+    size_t de = 0;
+    while (i < n && v[i] >= '0' && v[i] <= '9') { i++; de++; }
+    if (de == 0) return E_NUM_SYNTAX;
+  }
+  if (i != n) return E_NUM_SYNTAX;
+  char stackbuf[128];
+  char* s = n < sizeof stackbuf ? stackbuf : (char*)malloc(n + 1);
+  memcpy(s, v, n);
+  s[n] = 0;
+  *out = strtod(s, NULL);
+  if (s != stackbuf) free(s);
+  return 0;
+}
+
+/* ------------------------------------------------------------ CSV parse */
+typedef struct {
+  /* outputs */
+  int n_cols;
+  const int32_t* types;
+  int32_t** offsets;
+  uint8_t** chars;
+  void** typed;
+  uint64_t rec_cap;
+  const uint64_t* chars_cap;
+  or_status* st;
+  /* current field */
+  uint8_t* val;
+  size_t val_len, val_cap;
+} csv_out;
+
+static void field_value_push(csv_out* o, uint8_t b) {
+  if (o->val_len == o->val_cap) {
+    o->val_cap = o->val_cap ? 2 * o->val_cap : 256;
+    o->val = (uint8_t*)realloc(o->val, o->val_cap);
+  }
+  o->val[o->val_len++] = b;
+}
+
+/* Close field `col` of record `rec`; the value is o->val. */
+static void close_field(csv_out* o, uint64_t rec, int col, uint64_t field_start) {
+  if (col >= o->n_cols) return;                 /* extra field: dropped */
+  int t = o->types[col];
+  if (t == C_SKIP) return;
+  if (rec >= o->rec_cap) { flag(o->st, E_CAPACITY, 0, 0); return; }
+  if (t == C_STR) {
+    uint64_t len = o->st->chars_len[col];
+    if (len + o->val_len > o->chars_cap[col] || len + o->val_len > 0x7FFFFFFFull) {
+      flag(o->st, E_CAPACITY, 0, 0);
+      return;
+    }
+    memcpy(o->chars[col] + len, o->val, o->val_len);
+    len += o->val_len;
+    o->st->chars_len[col] = len;
+    o->offsets[col][rec + 1] = (int32_t)len;
+    return;
+  }
+  int rc;
+  if (t == C_F64) {
+    double d;
+    rc = conv_f64(o->val, o->val_len, &d);
+    ((double*)o->typed[col])[rec] = d;
+  } else {
+    int64_t lo = t == C_I8 ? -128 : t == C_I32 ? INT32_MIN : INT64_MIN;
+    int64_t hi = t == C_I8 ? 127 : t == C_I32 ? INT32_MAX : INT64_MAX;
+    int64_t x;
+    rc = conv_int(o->val, o->val_len, lo, hi, &x);
+    if (t == C_I8) ((int8_t*)o->typed[col])[rec] = (int8_t)x;
+    else if (t == C_I32) ((int32_t*)o->typed[col])[rec] = (int32_t)x;
+    else ((int64_t*)o->typed[col])[rec] = x;
+  }
+  if (rc) flag(o->st, rc, field_start, 1);
+}
+
+/* Close record `rec` whose last field was column `col` (terminator at off). */
+static void close_record(csv_out* o, uint64_t rec, int col, uint64_t off) {
+  if (col != o->n_cols - 1) flag(o->st, E_COLCOUNT, off, 1);
+  o->val_len = 0;
+  for (int c = col + 1; c < o->n_cols; c++) close_field(o, rec, c, off);  /* defaults */
+}
+
+int or_csv_parse(const uint8_t* in, uint64_t n, uint8_t fd, uint8_t rd, uint8_t q,
+                 int n_cols, const int32_t* col_types, int32_t** out_offsets,
+                 uint8_t** out_chars, void** out_typed, uint64_t records_capacity,
+                 const uint64_t* chars_capacity, or_status* st) {
+  memset(st, 0, sizeof *st);
+  st->first_error_offset = UINT64_MAX;
+  csv_out o = {n_cols, col_types, out_offsets, out_chars, out_typed, records_capacity,
+               chars_capacity, st, NULL, 0, 0};
+  for (int c = 0; c < n_cols; c++)
+    if (col_types[c] == C_STR && out_offsets[c]) out_offsets[c][0] = 0;
+  csv_syms y = {fd, rd, q};
+  int s = EOR, tag = T_RD;
+  uint64_t rec = 0, field_start = 0;
+  int col = 0;
+  for (uint64_t i = 0; i < n; i++) {
+    s = csv_step(&y, s, in[i], &tag);
+    switch (tag) {
+      case T_DATA: field_value_push(&o, in[i]); break;
+      case T_CTRL: break;
+      case T_FD:
+        close_field(&o, rec, col, field_start);
+        o.val_len = 0; col++; field_start = i + 1;
+        break;
+      case T_RD:
+        close_field(&o, rec, col, field_start);
+        close_record(&o, rec, col, i);
+        rec++; col = 0; field_start = i + 1;
+        break;
+      default:
+        flag(st, E_INVALID_INPUT, i, 1);
+        break;
+    }
+  }
+  if (s == INV) {
+    /* the automaton died; nothing after the invalid byte forms a field */
+  } else if (!csv_accepting(s)) {
+    flag(st, E_BAD_END_STATE, n, 1);
+  } else if (n > 0 && tag != T_RD) {            /* unterminated last record */
+    close_field(&o, rec, col, field_start);
+    close_record(&o, rec, col, n);
+    rec++;
+  }
+  st->n_records = rec;
+  free(o.val);
+  return 0;
+}
+
+/* ------------------------------------------------------------ tokenize */
+int or_tokenize(const uint8_t* in, uint64_t n, uint8_t* out_id, uint64_t* out_start,
+                uint32_t* out_len, uint64_t cap, or_status* st) {
+  memset(st, 0, sizeof *st);
+  st->first_error_offset = UINT64_MAX;
+  int s = L_START;
+  uint64_t k = 0, cur_start = 0;
+  for (uint64_t i = 0; i < n; i++) {
+    int begin, before = s;
+    s = lex_step(s, in[i], &begin);
+    if (s == L_INV && before != L_INV) flag(st, E_INVALID_INPUT, i, 1);
+    if (i == 0 || begin) {
+      if (i > 0) {               /* close the previous token */
+        if (k - 1 < cap) {
+          out_id[k - 1] = (uint8_t)lex_token_id(before, in[cur_start]);
+          out_len[k - 1] = (uint32_t)(i - cur_start);
+        }
+      }
+      if (k < cap) out_start[k] = i;
+      else flag(st, E_CAPACITY, 0, 0);
+      k++;
+      cur_start = i;
+    }
+  }
+  if (n > 0 && k - 1 < cap) {
+    out_id[k - 1] = (uint8_t)lex_token_id(s, in[cur_start]);
+    out_len[k - 1] = (uint32_t)(n - cur_start);
+  }
+  if (s != L_INV && !lex_accepting(s)) flag(st, E_BAD_END_STATE, n, 1);
+  st->n_tokens = k;
+  return 0;
+}
+
+/* ------------------------------------------- the method's own steps */
+/* These restate ParPaRaw Section 3.1 (multi-instance DFA, state-transition
+ * vectors, composite operation, exclusive scan) and Section 3.2 (absolute /
+ * relative column offsets) directly, for the tests to compare with the
+ * sequential walk above.                                                  */
+
+/* State-transition vector of one chunk: entry i = the final state of the
+ * DFA instance that started the chunk in state i (Figure 2).              */
+void or_stv(int kind, uint8_t fd, uint8_t rd, uint8_t q, const uint8_t* chunk,
+            uint64_t len, uint8_t* stv) {
+  csv_syms y = {fd, rd, q};
+  for (int i = 0; i < nstates(kind); i++) {
+    int s = i, t;
+    for (uint64_t j = 0; j < len; j++) s = step_any(kind, &y, s, chunk[j], &t);
+    stv[i] = (uint8_t)s;
+  }
+}
+
+/* Composite operation: (a o b)[i] = b[a[i]] with a the earlier chunk —
+ * running a's chunk from state i and then b's chunk from where it ended.   */
+void or_compose(int ns, const uint8_t* a, const uint8_t* b, uint8_t* out) {
+  for (int i = 0; i < ns; i++) out[i] = b[a[i]];
+}
+
+/* Chunk start states by the scan: STVs per chunk, exclusive composite scan
+ * seeded with the identity vector, start state = prefix[start state].      */
+void or_chunk_start_states(int kind, uint8_t fd, uint8_t rd, uint8_t q,
+                           const uint8_t* in, uint64_t n, uint64_t chunk, uint8_t* out) {
+  int ns = nstates(kind), s0 = 0;
+  uint8_t pre[16], stv[16], tmp[16];
+  for (int i = 0; i < ns; i++) pre[i] = (uint8_t)i;   /* identity */
+  uint64_t c = 0;
+  for (uint64_t off = 0; off < n; off += chunk, c++) {
+    out[c] = pre[s0];
+    uint64_t len = n - off < chunk ? n - off : chunk;
+    or_stv(kind, fd, rd, q, in + off, len, stv);
+    or_compose(ns, pre, stv, tmp);
+    memcpy(pre, tmp, (size_t)ns);
+  }
+}
+
+/* Column offset of one chunk (Section 3.2, Figure 4): absolute when the
+ * chunk holds a record delimiter (then the number of field delimiters after
+ * the last record delimiter), else relative (the number of field
+ * delimiters).  Tags come from running the DFA from the chunk's start. */
+void or_colofs_chunk(const uint8_t* tags, uint64_t len, int* is_abs, uint64_t* o) {
+  *is_abs = 0; *o = 0;
+  for (uint64_t j = 0; j < len; j++) {
+    if (tags[j] == T_RD) { *is_abs = 1; *o = 0; }
+    else if (tags[j] == T_FD) (*o)++;
+  }
+}
+/* Column-offset operator: b absolute wins; b relative adds to a. */
+void or_colofs_combine(int a_abs, uint64_t a_o, int b_abs, uint64_t b_o, int* abs_out,
+                       uint64_t* o_out) {
+  if (b_abs) { *abs_out = 1; *o_out = b_o; }
+  else { *abs_out = a_abs; *o_out = a_o + b_o; }
+}
+
+/* Brute force over every string of length 1..max_len on `alpha`: for every
+ * chunk size 1..max_len, the scan-derived chunk start states must equal the
+ * sequential walk's state at each chunk start, and the scanned column
+ * offsets must equal the sequential column index.  Returns the number of
+ * mismatches; *checked = strings visited.                                 */
+uint64_t or_bruteforce(int kind, uint8_t fd, uint8_t rd, uint8_t q, const uint8_t* alpha,
+                       int n_alpha, int max_len, uint64_t* checked) {
+  uint64_t bad = 0;
+  *checked = 0;
+  uint8_t str[16], seq_state[17], tags[16], starts[16];
+  int idx[16];
+  csv_syms y = {fd, rd, q};
+  for (int len = 1; len <= max_len; len++) {
+    for (int i = 0; i < len; i++) idx[i] = 0;
+    for (;;) {
+      for (int i = 0; i < len; i++) str[i] = alpha[idx[i]];
+      /* sequential walk */
+      int s = 0, t;
+      uint64_t col_seq[17];
+      uint64_t col = 0;
+      for (int i = 0; i < len; i++) {
+        seq_state[i] = (uint8_t)s;
+        col_seq[i] = col;
+        s = step_any(kind, &y, s, str[i], &t);
+        tags[i] = (uint8_t)t;
+        if (kind == 0) { if (t == T_RD) col = 0; else if (t == T_FD) col++; }
+      }
+      (*checked)++;
+      for (int ch = 1; ch <= max_len; ch++) {
+        or_chunk_start_states(kind, fd, rd, q, str, (uint64_t)len, (uint64_t)ch, starts);
+        int nch = (len + ch - 1) / ch;
+        int a_abs = 1; uint64_t a_o = 0;         /* seed: absolute column 0 */
+        for (int c = 0; c < nch; c++) {
+          if (starts[c] != seq_state[c * ch]) bad++;
+          if (kind == 0) {
+            if (!a_abs || a_o != col_seq[c * ch]) bad++;
+            int b_abs; uint64_t b_o;
+            int clen = len - c * ch < ch ? len - c * ch : ch;
+            or_colofs_chunk(tags + c * ch, (uint64_t)clen, &b_abs, &b_o);
+            or_colofs_combine(a_abs, a_o, b_abs, b_o, &a_abs, &a_o);
+          }
+        }
+      }
+      int p = len - 1;
+      while (p >= 0 && ++idx[p] == n_alpha) { idx[p] = 0; p--; }
+      if (p < 0) break;
+    }
+  }
+  return bad;
+}
