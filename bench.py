@@ -1,0 +1,379 @@
+"""Benchmark: raw-input parse throughput of libpp on one GB300 and its HBM
+roofline fraction.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference]
+
+A step is one pass of the whole parse hot path (pp_parse: context
+identification, tagging, record/column indexing, columnar output, numeric
+conversion; or pp_tokenize for the token-stream workload) over one
+synthetic input already resident in device memory.  Inputs are larger than
+the 129 MB L2, so no flush is needed between steps.  For N > 1 (one process
+per GPU, launched by torch.distributed.run) every rank parses its own
+replica of the input: the path does not shard, so the scaling is weak and
+no data-path collective exists.  Rank 0 prints one JSON line.
+
+--impl reference times the CPU oracle (the plain sequential parser) on this
+host's cores, on a bounded sample of the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import datagen  # noqa: E402
+
+METRIC = "raw-input parse GB/s on 1 GB300 and % of HBM-bandwidth roofline"
+DEFAULT_WORKLOAD = "csv18_2gib"
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, torch copy)"
+    return 6800.0, "fallback (6.8 TB/s earlier GB300 measurement)"
+
+
+def _traffic(workload):
+    """DRAM bytes per launch of the dominant kernel from a committed ncu
+    capture (profiles/ncu_traffic.json), or None."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("stale"):
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class Clocks:
+    """Sample nvidia-smi clocks and throttle reasons while the timed region runs."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _barrier(ws):
+    if ws > 1:
+        torch.distributed.barrier()
+
+
+def _max_over_ranks(x, ws, dev):
+    if ws == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _generate_pinned(workload, target=None, record_offsets=False):
+    w = datagen.WORKLOADS[workload]
+    cap = w["target"] if target is None else target
+    h = torch.empty(cap, dtype=torch.uint8, pin_memory=True)
+    data, info, _ = datagen.generate(workload, target=cap, out_ptr=h.data_ptr(), out_cap=cap,
+                                     record_offsets=record_offsets)
+    return h[: info["n_bytes"]], info
+
+
+def _cpu_baseline(workload, h_in, info, seconds=10.0):
+    """Time the oracle on a bounded prefix of the workload (whole records)."""
+    import oracle
+    w = datagen.WORKLOADS[workload]
+    arr = h_in.numpy()
+    cores = 1
+
+    def run(nb):
+        sample = arr[:nb]
+        if w["kind"] == "csv":
+            (_, st), dt = oracle.timed_csv_parse(sample, w["cols"])
+        else:
+            (_, st), dt = oracle.timed_tokenize(sample)
+        return dt
+
+    # cut samples at record starts so the sample is whole records
+    probe = min(arr.size, 16 << 20)
+    dt = run(probe)
+    rate = probe / max(dt, 1e-9)
+    nb = int(min(arr.size, rate * seconds))
+    if w["kind"] == "csv":
+        nl = np.flatnonzero(arr[:nb] == 10)
+        nb = int(nl[-1]) + 1 if nl.size else nb
+    dt = run(nb)
+    return {"value": nb / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {nb} bytes of {workload} (whole records), single-threaded "
+                      f"sequential DFA walk, parse only, input in RAM",
+            "seconds": dt, "host": _cpu_model()}
+
+
+def _cpu_model():
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith(("model name", "cpu part", "hardware")):
+                    return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return None
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    w = datagen.WORKLOADS[args.workload]
+    h_in, info = _generate_pinned(args.workload)
+    import oracle
+    arr = h_in.numpy()
+    # one bounded sample per step, sized for a few seconds of CPU work
+    probe = min(arr.size, 8 << 20)
+    t0 = time.perf_counter()
+    if w["kind"] == "csv":
+        oracle.csv_parse(arr[:probe], w["cols"])
+    else:
+        oracle.tokenize(arr[:probe])
+    rate = probe / max(time.perf_counter() - t0, 1e-9)
+    nb = int(min(arr.size, rate * 4.0))
+    if w["kind"] == "csv":
+        nl = np.flatnonzero(arr[:nb] == 10)
+        nb = int(nl[-1]) + 1 if nl.size else nb
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        if w["kind"] == "csv":
+            oracle.csv_parse(arr[:nb], w["cols"])
+        else:
+            oracle.tokenize(arr[:nb])
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    tot = sum(times)
+    value = nb * len(times) / tot / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": tot / len(times) * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+        "config": {"workload": args.workload, "n_bytes_sample": nb},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"first {nb} bytes of {args.workload} per step",
+                         "host": _cpu_model()},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import dfa_parsing_delimiter_gb300 as pp
+    ws, rank, local = _dist()
+    if ws > 1:
+        torch.distributed.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = datagen.WORKLOADS[args.workload]
+    h_in, info = _generate_pinned(args.workload)
+    n = int(h_in.numel())
+    d_in = torch.empty(n + 16, dtype=torch.uint8, device=dev)[:n]
+    d_in.copy_(h_in)
+    stream = torch.cuda.current_stream(dev)
+    csv = w["kind"] == "csv"
+
+    if csv:
+        desc = pp.desc_csv()
+        R = info["n_records"]
+        chars_cap = [info["col_value_bytes"][c] if t == "str" else 0
+                     for c, t in enumerate(w["cols"])]
+        out = pp.CsvOutputs(w["cols"], R, chars_cap, device=dev)
+
+        def step():
+            out.run(d_in, n, desc, stream)
+        launches_per_step = 2
+    else:
+        desc = pp.desc_json_lexer()
+        T = info["n_tokens"]
+        ids = torch.empty(T, dtype=torch.uint8, device=dev)
+        starts = torch.empty(T, dtype=torch.int64, device=dev)
+        lens = torch.empty(T, dtype=torch.int32, device=dev)
+        status = pp.new_status(dev)
+
+        def step():
+            pp.pp_tokenize(d_in, n, desc, ids, starts, lens, T, status, stream)
+        launches_per_step = 2
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    # correctness of the measured run: status must be clean and complete
+    if csv:
+        st = pp.read_status(out.status, len(w["cols"]))
+        assert st["error"] == 0 and st["n_records"] == info["n_records"], st
+        out_bytes = out.output_bytes(st["n_records"], st["chars_len"])
+    else:
+        st = pp.read_status(status)
+        assert st["error"] == 0 and st["n_tokens"] == info["n_tokens"], st
+        out_bytes = 13 * st["n_tokens"]
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    with Clocks(local) as clk:
+        _barrier(ws)
+        torch.cuda.synchronize()
+        t_start = time.perf_counter()
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        _barrier(ws)
+        wall = time.perf_counter() - t_start
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    tot_ms = _max_over_ranks(sum(step_ms), ws, dev)
+    ms_per_step = tot_ms / args.steps
+    value = n * ws * args.steps / (tot_ms / 1e3) / 1e9
+    peak, peak_src = _peaks()
+    kern_s = float(np.mean(step_ms)) / 1e3
+    achieved = (n + out_bytes) / kern_s / 1e9
+
+    # end to end through the public API with host buffers
+    e2e_steps = max(1, min(args.steps, 3))
+    e2e_t = []
+    h2d = d2h = 0
+    for i in range(e2e_steps + 1):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        if csv:
+            _, est, h2d, d2h = pp.parse_csv_host(h_in, w["cols"])
+        else:
+            _, est, h2d, d2h = pp.tokenize_host(h_in)
+        dt = time.perf_counter() - t0
+        assert est["error"] == 0, est
+        if i > 0:
+            e2e_t.append(dt)
+    e2e_value = n * ws / _max_over_ranks(float(np.mean(e2e_t)), ws, dev) / 1e9
+
+    if rank != 0:
+        return
+    cpu = _cpu_baseline(args.workload, h_in, info) if not args.no_cpu_baseline else None
+    traffic = _traffic(args.workload)
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+        "data": "synthetic (seeded generator, see datagen)",
+        "config": {"workload": args.workload, "n_bytes": n,
+                   "n_records": info["n_records"] if csv else None,
+                   "n_tokens": info["n_tokens"] if not csv else None,
+                   "columns": w["cols"], "output_bytes": out_bytes,
+                   "l2": "input (and output) larger than the 129 MB L2; no flush",
+                   "parallelism": "replicas" if ws > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": peak_src,
+                     "algorithmic_bytes_per_launch": n + out_bytes,
+                     "kernel": "parse_kernel" if csv else "tokenize_kernel",
+                     "timing": "CUDA events per call on the launching stream (includes the "
+                               "small scratch-init kernel)"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h,
+                "api": "parse_csv_host" if csv else "tokenize_host"},
+        "clocks": clk.summary(),
+        "gpu_launches": launches_per_step * args.steps,
+        "wall_s_timed_region": wall,
+        "step_ms_min": min(step_ms), "step_ms_median": float(np.median(step_ms)),
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(datagen.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,87 @@
+// Host/device shared definitions of libpp (not part of the public ABI).
+#pragma once
+#include <cstdint>
+#include <cuda_runtime_api.h>
+#include "pp.h"
+
+namespace ppi {
+
+constexpr int MAX_STR_COLS = 16;  // string columns per pp_parse call
+
+// Cross-block scratch of one pp_parse call (device memory, zeroed per call).
+struct ParseScratch {
+  unsigned long long* lb1;  // [n_tiles] flag|STV
+  uint32_t* lb2_flag;       // [n_tiles]
+  uint64_t* lb2_agg;        // [n_tiles][4]
+  uint64_t* lb2_inc;        // [n_tiles][4]
+  uint32_t* lb3_flag;       // [n_tiles]
+  uint64_t* lb3_agg;        // [n_tiles][ns]
+  uint64_t* lb3_inc;        // [n_tiles][ns]
+  uint32_t* tile_counter;   // [1]
+};
+
+struct ParseParams {
+  const uint8_t* in;
+  uint64_t n;
+  uint32_t n_tiles;
+  uint32_t spin_limit;
+  uint32_t lut[256];      // per byte: STV selector, next-state/tag fields, special bit
+  uint32_t bg_next;       // nibble s = delta[background][s], s = 0..4
+  uint16_t accept_mask;
+  uint8_t start_state;
+  uint8_t has_inv;        // state 4 is the absorbing invalid state
+  int32_t n_cols;
+  int32_t n_str;
+  int32_t has_out;
+  int8_t stridx[PP_MAX_COLS];   // column -> string index, or -1
+  uint8_t strcol[MAX_STR_COLS]; // string index -> column
+  uint8_t coltype[PP_MAX_COLS];
+  int32_t* offsets[MAX_STR_COLS];
+  uint8_t* chars[MAX_STR_COLS];
+  uint64_t chars_cap[MAX_STR_COLS];
+  void* typed[PP_MAX_COLS];
+  uint64_t rec_cap;
+  pp_status* st;
+  ParseScratch s;
+};
+
+// bytes of scratch for n_tiles tiles and ns string columns (ns rounded to the
+// kernel's instantiation width)
+size_t parse_scratch_bytes(uint32_t n_tiles, int ns);
+void parse_scratch_carve(void* base, uint32_t n_tiles, int ns, ParseScratch* out);
+int parse_ns_width(int n_str);
+
+cudaError_t launch_parse_init(const ParseParams& p, size_t scratch_bytes, void* scratch,
+                              cudaStream_t stream);
+cudaError_t launch_parse(const ParseParams& p, cudaStream_t stream);
+size_t parse_tile_bytes();
+
+// ---------------------------------------------------------- pp_tags / tokenize
+struct GenericDfa {
+  uint8_t n_states;
+  uint8_t start_state;
+  uint8_t invalid_state;
+  uint8_t pad;
+  uint16_t accept_mask;
+  uint8_t byte_to_group[256];
+  uint8_t delta[PP_MAX_GROUPS][PP_MAX_STATES];
+  uint8_t tag[PP_MAX_STATES][PP_MAX_GROUPS];
+  uint8_t token_id[PP_MAX_STATES];
+  uint8_t byte_token_id[256];
+};
+
+cudaError_t launch_tags(const uint8_t* in, uint64_t n, const GenericDfa& dfa,
+                        uint8_t* state_before, uint8_t* tag, pp_status* st, void* scratch,
+                        size_t scratch_bytes, cudaStream_t stream);
+size_t tags_scratch_bytes(uint64_t n);
+
+cudaError_t launch_tokenize(const uint8_t* in, uint64_t n, const GenericDfa& dfa,
+                            uint8_t* out_id, uint64_t* out_start, uint32_t* out_len,
+                            uint64_t cap, pp_status* st, void* scratch, size_t scratch_bytes,
+                            cudaStream_t stream);
+size_t tokenize_scratch_bytes(uint64_t n);
+
+cudaError_t launch_count_byte(const uint8_t* in, uint64_t n, uint8_t value, uint64_t* d_count,
+                              cudaStream_t stream);
+
+}  // namespace ppi

@@ -1,0 +1,228 @@
+/*
+ * pp.h — C ABI of libpp, a GB300 (sm_103a) library for massively parallel
+ * parsing of delimiter-separated raw data with a DFA, after "ParPaRaw:
+ * Massively Parallel Parsing of Delimiter-Separated Raw Data".
+ *
+ * What is computed (ParPaRaw, Section 3): every chunk of the input runs one
+ * DFA instance per state, giving a state-transition vector (Section 3.1,
+ * Figure 2); an exclusive scan with the composite operation gives each
+ * chunk its true start state; a single DFA run then tags each byte as field
+ * delimiter, record delimiter, control symbol or value (Section 3.1, the
+ * three bitmap indexes); record counts and absolute/relative column offsets
+ * are scanned (Section 3.2, Figure 4); values are emitted per column
+ * (Section 3.3, Figure 5) — here directly as Arrow-style int32 offsets plus
+ * chars for string columns (the Arrow layout as described in the libcudf
+ * string-column article: offsets[0] = 0, offsets[i+1] - offsets[i] = size
+ * of row i, last offset = chars size) and as dense arrays for numeric
+ * columns (type conversion, Section 3.3; empty field = default value 0,
+ * Section 4.3).
+ *
+ * Conventions for every entry point:
+ *  - Pointers named d_* and out_* are DEVICE pointers; everything else
+ *    (descriptors, column-type arrays, capacity arrays, pointer arrays) is
+ *    HOST memory, read during the call only.
+ *  - The caller owns all input and output buffers.  Scratch for the
+ *    cross-block scan is allocated stream-ordered on `stream`
+ *    (cudaMallocAsync) and released stream-ordered before return.
+ *  - All device work is enqueued on `stream`; no call synchronises the
+ *    host except where stated.
+ *  - The return code covers argument checks and CUDA launch/allocation
+ *    errors only.  Errors found in the data are reported in the device-side
+ *    pp_status (error bitmask + the minimum byte offset of any data error).
+ *  - Outputs are defined only when pp_status.error holds none of the fatal
+ *    bits (PP_ERR_FATAL).  Every store is bounds-checked against the given
+ *    capacities whatever the input.
+ */
+#ifndef PP_H
+#define PP_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PP_MAX_COLS 64
+#define PP_MAX_STATES 16
+#define PP_MAX_GROUPS 16
+
+/* host return codes */
+typedef enum { PP_OK = 0, PP_EINVAL = 1, PP_ECUDA = 2, PP_ENOMEM = 3 } pp_rc;
+
+/* column kinds for pp_parse */
+typedef enum {
+  PP_COL_STRING = 0, /* Arrow int32 offsets[R+1] + uint8 chars          */
+  PP_COL_INT8 = 1,   /* int8[R],  grammar [+-]?[0-9]+                   */
+  PP_COL_INT32 = 2,  /* int32[R]                                        */
+  PP_COL_INT64 = 3,  /* int64[R]                                        */
+  PP_COL_FLOAT64 = 4,/* double[R], decimal grammar, within 1 ulp of the
+                        correctly rounded value                          */
+  PP_COL_SKIP = 5    /* parsed for structure, not emitted               */
+} pp_coltype;
+
+/* per-byte tags (ParPaRaw Section 3.1: record delimiter, field delimiter,
+ * control symbol vs. value; plus "invalid" for transitions into the error
+ * state, Section 4.3 "Validating format", and "begin" for lexers)         */
+typedef enum {
+  PP_TAG_DATA = 0,    /* part of a value                                 */
+  PP_TAG_FD = 1,      /* field delimiter                                 */
+  PP_TAG_RD = 2,      /* record delimiter                                */
+  PP_TAG_CTRL = 3,    /* control symbol (quote, escape) — not a value    */
+  PP_TAG_INVALID = 4, /* transition into / inside the invalid state      */
+  PP_TAG_BEGIN = 5    /* first byte of a token (pp_tokenize DFAs)        */
+} pp_tag;
+
+/* pp_status.error bits */
+#define PP_ERR_INVALID_INPUT 1    /* a transition into the invalid state    */
+#define PP_ERR_BAD_END_STATE 2    /* input ends in a non-accepting state    */
+#define PP_ERR_COLCOUNT 4         /* a record with != n_cols fields         */
+#define PP_ERR_NUM_SYNTAX 8       /* numeric field does not match grammar   */
+#define PP_ERR_NUM_OVERFLOW 16    /* integer out of range for its column    */
+#define PP_ERR_CAPACITY 32        /* an output capacity was too small       */
+#define PP_ERR_LOOKBACK_TIMEOUT 64/* a cross-block wait gave up (bounded)   */
+#define PP_ERR_FATAL (PP_ERR_INVALID_INPUT | PP_ERR_BAD_END_STATE | \
+                      PP_ERR_CAPACITY | PP_ERR_LOOKBACK_TIMEOUT)
+
+/* Description of a DFA over bytes (ParPaRaw Section 5, Table 1: symbols
+ * with identical transitions are collapsed into symbol groups, and the
+ * transition table is stored with one row per symbol group).             */
+typedef struct {
+  uint8_t n_states;       /* |S|, 1..16                                    */
+  uint8_t n_groups;       /* symbol groups, 1..16                          */
+  uint8_t start_state;    /* state of the sequential DFA at byte 0         */
+  uint8_t invalid_state;  /* absorbing error state, or 0xFF for none       */
+  uint16_t accept_mask;   /* bit s set: s is an accepting end state        */
+  uint8_t background_group; /* a group whose transition is idempotent and
+                               whose bytes are never delimiters/controls, or
+                               0xFF; lets the tagger skip runs of it        */
+  uint8_t reserved;
+  uint8_t byte_to_group[256];
+  uint8_t delta[PP_MAX_GROUPS][PP_MAX_STATES]; /* delta[group][state]       */
+  uint8_t tag[PP_MAX_STATES][PP_MAX_GROUPS];   /* tag[state_before][group]  */
+  /* pp_tokenize only: token id from the state after the token's last byte;
+   * 0xFE means "take byte_token_id[first byte of the token]"             */
+  uint8_t token_id[PP_MAX_STATES];
+  uint8_t byte_token_id[256];
+} pp_dfa_desc;
+
+/* Device-resident result status.  The caller allocates it; every call
+ * initialises it on `stream` before any other device work.               */
+typedef struct {
+  int32_t error;                 /* 0 or PP_ERR_* bitmask                  */
+  int32_t reserved;
+  uint64_t first_error_offset;   /* min byte offset over all data errors
+                                    (INVALID_INPUT at the offending byte,
+                                    BAD_END_STATE at n_bytes, COLCOUNT at
+                                    the record's terminator, NUM_* at the
+                                    field's first byte); UINT64_MAX if none */
+  uint64_t n_records;            /* pp_parse                               */
+  uint64_t n_tokens;             /* pp_tokenize                            */
+  uint64_t chars_len[PP_MAX_COLS]; /* pp_parse: chars of column c (string
+                                    columns; 0 for the others)             */
+} pp_status;
+
+/*
+ * pp_parse — parse delimiter-separated input into columns.
+ *   d_in            device, n_bytes bytes of raw input (any alignment).
+ *   dfa             host; a DFA with at most 4 live states plus (optionally)
+ *                   one absorbing invalid state with index 4, tags FD/RD/
+ *                   CTRL/DATA/INVALID (e.g. built by pp_desc_csv).
+ *   n_cols          1..PP_MAX_COLS; col_types[n_cols] host.
+ *   out_offsets[c]  device int32[records_capacity+1] for PP_COL_STRING
+ *                   columns, else ignored (may be NULL).
+ *   out_chars[c]    device uint8[chars_capacity[c]] for string columns.
+ *   out_typed[c]    device array of records_capacity elements of the
+ *                   column's type for numeric columns.
+ *   chars_capacity  host array of n_cols sizes (string columns only).
+ *   d_status        device pp_status.
+ * Passing NULL for every out_offsets/out_chars/out_typed pointer is allowed
+ * (a sizing pass): nothing is written except d_status, whose n_records and
+ * chars_len then give exact sizes.
+ * Semantics (ParPaRaw Sections 3-4): a record ends at every record
+ * delimiter; a non-empty tail without one is one more record; an empty line
+ * is a record with one empty field; records with != n_cols fields set
+ * PP_ERR_COLCOUNT, extra fields are dropped and missing ones take the
+ * default (empty string / 0).  String values are the value bytes only
+ * (enclosing quotes dropped, a doubled quote yields one quote).
+ * Returns PP_EINVAL for bad arguments, PP_ENOMEM / PP_ECUDA on CUDA errors.
+ */
+pp_rc pp_parse(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa, int n_cols,
+               const pp_coltype* col_types, int32_t* const out_offsets[],
+               uint8_t* const out_chars[], void* const out_typed[],
+               size_t records_capacity, const size_t chars_capacity[],
+               pp_status* d_status, cudaStream_t stream);
+
+/*
+ * pp_tokenize — run a general DFA (|S| <= 16) over the input and emit one
+ * (token_id, start, len) triple per token, as struct-of-arrays.  A token
+ * starts at byte 0 and at every byte whose tag is PP_TAG_BEGIN; its length
+ * runs to the next token start (or n_bytes); its id is token_id[state after
+ * its last byte] (the prefix-scan lexer of "Lexing on the GPU: the scan is
+ * the easy part", section "A lexer is a prefix scan").
+ *   out_token_id   device uint8[tokens_capacity]
+ *   out_start      device uint64[tokens_capacity]
+ *   out_len        device uint32[tokens_capacity]
+ * NULL outputs with tokens_capacity 0 make a counting pass (n_tokens only).
+ * Tokens beyond tokens_capacity are counted, not written (PP_ERR_CAPACITY).
+ */
+pp_rc pp_tokenize(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa,
+                  uint8_t* out_token_id, uint64_t* out_start, uint32_t* out_len,
+                  size_t tokens_capacity, pp_status* d_status, cudaStream_t stream);
+
+/*
+ * pp_tags — test hook: per byte, the state of the sequential DFA before the
+ * byte and the byte's tag (tag[state_before][group]), computed by the same
+ * multi-instance DFA + composite scan as the parsers (ParPaRaw Section
+ * 3.1).  d_state_before and d_tag are device uint8[n_bytes].  d_status gets
+ * error/first_error_offset for INVALID_INPUT and BAD_END_STATE.
+ */
+pp_rc pp_tags(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa,
+              uint8_t* d_state_before, uint8_t* d_tag, pp_status* d_status,
+              cudaStream_t stream);
+
+/*
+ * pp_count_byte — *d_count = number of bytes equal to `value` in d_in
+ * (uint64, device).  With value = the record delimiter, *d_count + 1 bounds
+ * the record count of any input, which is how callers size pp_parse
+ * outputs without a sizing pass.
+ */
+pp_rc pp_count_byte(const uint8_t* d_in, size_t n_bytes, uint8_t value, uint64_t* d_count,
+                    cudaStream_t stream);
+
+/*
+ * pp_desc_csv — build the quoted-CSV DFA (RFC-4180 style quoting) with
+ * states EOR=0 (at a field/record boundary, the start state), FLD=1 (inside
+ * an unquoted field), ENC=2 (inside quotes), ESC=3 (a quote seen inside
+ * quotes), INV=4 (invalid, absorbing; ParPaRaw Section 3.1 names reading a
+ * quote in FLD as invalid).  fd, rd and quote must be distinct.
+ * Accepting end states: EOR, FLD, ESC.  Host only.
+ */
+pp_rc pp_desc_csv(pp_dfa_desc* out, uint8_t fd, uint8_t rd, uint8_t quote);
+
+/*
+ * pp_desc_json_lexer — build the 16-state JSON-like lexer DFA used by
+ * pp_tokenize (whitespace runs, punctuation {}[],:, strings with backslash
+ * escapes, integers, fractions and exponents).  Token ids: '{'0 '}'1 '['2
+ * ']'3 ','4 ':'5 string 6 integer 7 float 8 whitespace 9, 255 invalid.
+ * Host only.
+ */
+pp_rc pp_desc_json_lexer(pp_dfa_desc* out);
+
+/* Human-readable text for a pp_rc value. */
+const char* pp_strerror(int code);
+
+/* Tile size in bytes used by the cross-block scan (for tests that place
+ * adversarial inputs at tile boundaries). */
+size_t pp_tile_bytes(void);
+
+/* Test/debug hook: number of polls a cross-block wait makes before it gives
+ * up and reports PP_ERR_LOOKBACK_TIMEOUT (0 restores the default, about one
+ * second of polling).  Process-wide; affects calls made afterwards. */
+void pp_debug_set_spin_limit(uint32_t polls);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PP_H */

@@ -1,0 +1,256 @@
+"""GPU parity: libpp (through its C ABI) against the CPU oracle, element by
+element, on seeded inputs spanning many tiles and ragged tails, plus the
+edge cases of the method (empty input, tails without a delimiter, fields
+crossing tiles, invalid input, column-count errors, capacity limits)."""
+import random
+
+import numpy as np
+import pytest
+import torch
+
+import datagen
+import dfa_parsing_delimiter_gb300 as pp
+import oracle as O
+from gpu_util import compare_csv, compare_tags, compare_tokens, run_gpu_csv, to_dev
+
+pytestmark = pytest.mark.gpu
+TILE = 16384
+
+
+@pytest.fixture(autouse=True, scope="module")
+def _device():
+    assert torch.cuda.is_available(), "GPU tests need CUDA"
+    torch.cuda.set_device(0)
+    assert pp.tile_bytes() == TILE
+
+
+def _rand_csv(rng, n, alpha=b'",\nab'):
+    return bytes(rng.choice(alpha) for _ in range(n))
+
+
+# ------------------------------------------------------------------ tags
+@pytest.mark.parametrize("n", [0, 1, 31, 32, 33, 1000, TILE - 1, TILE, TILE + 1, 3 * TILE + 777])
+def test_tags_csv_random(n):
+    rng = random.Random(n)
+    data = _rand_csv(rng, n, alpha=b'"' + b",\naaaaaaa")
+    compare_tags(data)
+
+
+@pytest.mark.parametrize("name", ["csv4_1mib", "csv3_1gib"])
+def test_tags_csv_generated(name):
+    data, _, _ = datagen.generate(name, target=5 * TILE + 123)
+    compare_tags(data)
+    compare_tags(data, offset=3)
+
+
+@pytest.mark.parametrize("n", [0, 5, 4 * TILE + 9])
+def test_tags_lexer(n):
+    data, _, _ = datagen.generate("json_2gib", target=max(n, 1))
+    compare_tags(data[:n], kind=O.KIND_LEX)
+    rng = random.Random(n)
+    junk = bytes(rng.choice(b' {"\\-+01.exa]:,') for _ in range(n))
+    compare_tags(junk, kind=O.KIND_LEX)
+
+
+# ---------------------------------------------------------------- parse
+@pytest.mark.parametrize("name,target", [
+    ("csv4_1mib", None),                 # the full 1 MiB workload
+    ("csv4_1mib", 3 * TILE + 101),
+    ("csv16_256mib", 2 << 20),
+    ("csv16_256mib", 5 * TILE + 3),
+    ("csv3_1gib", 4 << 20),
+    ("csv3_1gib", 2 * TILE + 17),
+    ("csv18_2gib", 2 << 20),
+    ("csv18_2gib", TILE + 1),
+])
+def test_parse_workloads(name, target):
+    data, info, _ = datagen.generate(name, target=target)
+    st = compare_csv(data, datagen.WORKLOADS[name]["cols"])
+    assert st["error"] == 0 and st["n_records"] == info["n_records"]
+
+
+@pytest.mark.parametrize("offset", [1, 7])
+def test_parse_misaligned_input(offset):
+    data, _, _ = datagen.generate("csv16_256mib", target=3 * TILE + 5)
+    compare_csv(data, datagen.WORKLOADS["csv16_256mib"]["cols"], offset=offset)
+
+
+def test_parse_empty_and_tiny():
+    for data in [b"", b"a", b"\n", b",", b'"', b'""', b'"a"', b"a\n", b"a,b", b"\n\n\n", b",\n,,\n"]:
+        compare_csv(data, ["str", "str"])
+
+
+def test_parse_no_trailing_newline():
+    data, _, _ = datagen.generate("csv18_2gib", target=3 * TILE)
+    cols = datagen.WORKLOADS["csv18_2gib"]["cols"]
+    compare_csv(bytes(data[:-1]), cols)          # last record unterminated
+    compare_csv(bytes(data[:-7]), cols)
+
+
+def test_parse_field_spanning_many_tiles():
+    rng = random.Random(5)
+    body = bytes(rng.choice(b"abc,\n\"") for _ in range(5 * TILE + 333))
+    quoted = b'"' + body.replace(b'"', b'""') + b'"'
+    data = b"1," + quoted + b",2\n3,x,4\n" + b"5," + quoted + b",6\n"
+    compare_csv(data, ["i32", "str", "i32"])
+    compare_csv(data, ["i32", "skip", "i8"])
+
+
+@pytest.mark.parametrize("k", range(-6, 7))
+def test_parse_tile_boundary_patterns(k):
+    """Place quotes, doubled quotes and delimiters at every offset around the
+    first tile boundary (and a numeric field straddling it)."""
+    for pat in [b'"a,""b\nc"', b'""', b'"x"', b',\n', b'12345.678']:
+        fill = TILE + k - 2
+        head = (b"q" * (fill - 1)) + b","
+        data = head + b'1,' + pat + b"\n7,8,9\n"
+        if pat == b'12345.678':
+            compare_csv(data, ["str", "i32", "f64"])
+        else:
+            compare_csv(data, ["str", "i32", "str"])
+
+
+@pytest.mark.parametrize("pos", [0, 5, 31, 32, TILE - 1, TILE, TILE + 40, 2 * TILE + 3])
+def test_parse_invalid_quote(pos):
+    data, _, _ = datagen.generate("csv18_2gib", target=3 * TILE)
+    b = bytearray(data)
+    # put a quote right after an unquoted data byte -> invalid at that byte
+    while b[pos - 1:pos] in (b",", b"\n") or pos == 0:
+        pos += 1
+    b[pos] = ord('"')
+    st = compare_csv(bytes(b), datagen.WORKLOADS["csv18_2gib"]["cols"])
+    assert st["error"] & pp.ERR_INVALID_INPUT and st["first_error_offset"] == pos
+
+
+def test_parse_bad_end_state():
+    data, _, _ = datagen.generate("csv4_1mib", target=2 * TILE)
+    st = compare_csv(bytes(data) + b'a,"unterminated,\n', ["str"] * 4)
+    assert st["error"] & pp.ERR_BAD_END_STATE
+
+
+def test_parse_colcount_defaults():
+    rows = [b"1,a,2.5", b"2", b"3,b", b"4,c,1e3,extra,more", b"", b"5,d,-0"]
+    data = b"\n".join(rows) * 700 + b"\n"
+    st = compare_csv(data, ["i64", "str", "f64"])
+    assert st["error"] == pp.ERR_COLCOUNT
+
+
+def test_parse_numeric_errors():
+    rows = [b"1,2.5", b"x,1", b"99999999999,3", b"+,4", b"5,1.2.3", b'"6","7.5"', b"7,", b",8e1"]
+    data = (b"\n".join(rows) + b"\n") * 900
+    st = compare_csv(data, ["i32", "f64"])
+    assert st["error"] == pp.ERR_NUM_SYNTAX | pp.ERR_NUM_OVERFLOW
+    compare_csv(data, ["i8", "f64"])
+    compare_csv(data, ["i64", "str"])
+
+
+def test_parse_float_hard_cases():
+    rng = random.Random(17)
+    vals = ["0", "-0", "1e308", "1e309", "-1e400", "4.9406564584124654e-324",
+            "2.4703282292062328e-324", "9007199254740993", "123456789012345678901234567890",
+            "179769313486231580793728971405301e276", "1.7976931348623159e308",
+            "0.000000000000000000000000000001", "2.2250738585072011e-308"]
+    for _ in range(30000):
+        mant = "".join(rng.choice("0123456789") for _ in range(rng.randint(1, 25)))
+        if rng.random() < 0.5:
+            k = rng.randint(0, len(mant))
+            mant = mant[:k] + "." + mant[k:]
+            if mant == ".":
+                mant = "0."
+        s = ("-" if rng.random() < 0.3 else "") + mant
+        if rng.random() < 0.6:
+            s += rng.choice("eE") + rng.choice(["", "+", "-"]) + str(rng.randint(0, 340))
+        vals.append(s)
+    data = ("\n".join(vals) + "\n").encode()
+    compare_csv(data, ["f64"])
+
+
+def test_parse_custom_delimiters():
+    data, _, _ = datagen.generate("csv16_256mib", target=3 * TILE)
+    b = bytes(data).replace(b",", b"|").replace(b"\n", b";")
+    compare_csv(b, datagen.WORKLOADS["csv16_256mib"]["cols"], fd=b"|", rd=b";", quote=b'"')
+
+
+def test_parse_random_small_inputs():
+    rng = random.Random(99)
+    for trial in range(300):
+        n = rng.randint(0, 200)
+        data = _rand_csv(rng, n, alpha=b'",\n1a-.')
+        compare_csv(data, ["str", "i32", "f64"])
+
+
+def test_parse_capacity_too_small():
+    data, info, _ = datagen.generate("csv18_2gib", target=2 * TILE)
+    cols = datagen.WORKLOADS["csv18_2gib"]["cols"]
+    out, st = run_gpu_csv(data, cols, records_capacity=info["n_records"] - 3)
+    assert st["error"] & pp.ERR_CAPACITY
+    out, st = run_gpu_csv(data, cols, chars_capacity=[100] * len(cols))
+    assert st["error"] & pp.ERR_CAPACITY
+
+
+def test_parse_sizing_pass():
+    data, info, _ = datagen.generate("csv4_1mib", target=4 * TILE + 11)
+    d_in = to_dev(data)
+    st = pp.new_status()
+    pp.pp_parse(d_in, data.size, pp.desc_csv(), ["str"] * 4, None, None, None, 0, None, st)
+    s = pp.read_status(st, 4)
+    _, rst = O.csv_parse(data, ["str"] * 4)
+    assert s["error"] == 0 and s["n_records"] == rst["n_records"]
+    assert s["chars_len"] == rst["chars_len"]
+
+
+def test_parse_repeat_calls_identical():
+    data, _, _ = datagen.generate("csv3_1gib", target=8 * TILE)
+    cols = datagen.WORKLOADS["csv3_1gib"]["cols"]
+    a, sa = run_gpu_csv(data, cols)
+    b, sb = run_gpu_csv(data, cols)
+    assert sa == sb
+    for x, y in zip(a.results(sa), b.results(sb)):
+        if isinstance(x, tuple):
+            assert torch.equal(x[0], y[0]) and torch.equal(x[1], y[1])
+        else:
+            assert torch.equal(x, y)
+
+
+def test_count_byte():
+    data, _, _ = datagen.generate("csv3_1gib", target=3 * TILE + 5)
+    for off in (0, 1):
+        d = to_dev(data, off)
+        assert pp.count_byte(d, 10) == int(np.count_nonzero(data == 10))
+
+
+# -------------------------------------------------------------- tokenize
+@pytest.mark.parametrize("target", [1, 100, TILE - 3, 6 * TILE + 71, 1 << 20])
+def test_tokenize_generated(target):
+    data, info, _ = datagen.generate("json_2gib", target=target)
+    st = compare_tokens(data)
+    assert st["n_tokens"] == info["n_tokens"]
+
+
+def test_tokenize_misaligned_and_edges():
+    data, _, _ = datagen.generate("json_2gib", target=2 * TILE)
+    compare_tokens(data, offset=5)
+    for s in [b"", b" ", b"1", b"-", b'"abc', b"1.", b"1e", b"[1,2]", b'"\\u00E9"', b"\x7f", b"00"]:
+        compare_tokens(s)
+
+
+def test_tokenize_random_including_invalid():
+    rng = random.Random(4)
+    for _ in range(200):
+        n = rng.randint(0, 300)
+        compare_tokens(bytes(rng.choice(b' {"\\-+01.exa]:,E\t') for _ in range(n)))
+
+
+def test_tokenize_capacity():
+    data, info, _ = datagen.generate("json_2gib", target=3 * TILE)
+    d_in = to_dev(data)
+    cap = info["n_tokens"] // 2
+    ids = torch.empty(cap, dtype=torch.uint8, device="cuda")
+    starts = torch.empty(cap, dtype=torch.int64, device="cuda")
+    lens = torch.empty(cap, dtype=torch.int32, device="cuda")
+    st = pp.new_status()
+    pp.pp_tokenize(d_in, data.size, pp.desc_json_lexer(), ids, starts, lens, cap, st)
+    s = pp.read_status(st)
+    assert s["error"] & pp.ERR_CAPACITY and s["n_tokens"] == info["n_tokens"]
+    (rids, rstarts, rlens), _ = O.tokenize(data)
+    assert np.array_equal(starts.cpu().numpy().astype(np.uint64), rstarts[:cap])
