@@ -242,7 +242,7 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     w = datagen.WORKLOADS[args.workload]
-    h_in, info = _generate_pinned(args.workload)
+    h_in, info = _generate_pinned(args.workload, target=args.target)
     n = int(h_in.numel())
     d_in = torch.empty(n + 16, dtype=torch.uint8, device=dev)[:n]
     d_in.copy_(h_in)
@@ -306,10 +306,10 @@ def run_ours(args):
     achieved = (n + out_bytes) / kern_s / 1e9
 
     # end to end through the public API with host buffers
-    e2e_steps = max(1, min(args.steps, 3))
+    e2e_steps = 0 if args.no_e2e else max(1, min(args.steps, 3))
     e2e_t = []
     h2d = d2h = 0
-    for i in range(e2e_steps + 1):
+    for i in range(e2e_steps + 1 if e2e_steps else 0):
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         if csv:
@@ -320,7 +320,7 @@ def run_ours(args):
         assert est["error"] == 0, est
         if i > 0:
             e2e_t.append(dt)
-    e2e_value = n * ws / _max_over_ranks(float(np.mean(e2e_t)), ws, dev) / 1e9
+    e2e_value = (n * ws / _max_over_ranks(float(np.mean(e2e_t)), ws, dev) / 1e9) if e2e_t else None
 
     if rank != 0:
         return
@@ -366,6 +366,10 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(datagen.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--target", type=int, default=None,
+                    help="input byte target (default: the workload's size); smaller "
+                         "values give the small case used for ncu captures")
+    ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -34,7 +34,7 @@ def _stale(target: str, deps: list[str]) -> bool:
 
 def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(BUILD, exist_ok=True)
-    table = os.path.join(CSRC, "pow10_table.inc")
+    table = os.path.join(CSRC, "pow5_table.inc")
     gen = os.path.join(CSRC, "gen_pow10.py")
     if force or _stale(table, [gen]):
         subprocess.check_call([sys.executable, gen, table])

@@ -4,52 +4,105 @@
 //
 // Integers: grammar [+-]?[0-9]+, exact, range-checked per column type.
 // Floats: grammar [+-]?([0-9]+(\.[0-9]*)?|\.[0-9]+)([eE][+-]?[0-9]+)?.
-//   Fast path (Clinger, "How to read floating point numbers accurately",
-//   PLDI 1990): a significand of at most 2^53 and |e10| <= 22 gives the
-//   correctly rounded result with one exact-operand multiply or divide.
-//   Otherwise the first 19 significant digits are scaled by 10^e10 in
-//   double-double arithmetic (Dekker's exact product via FMA, fast two-sum)
-//   against a table of 10^k computed exactly, and rounded once: the result
-//   is within 1 ulp of the correctly rounded value.
+//
+// The float conversion uses integer arithmetic only (GB300's FP64 rate is
+// a small fraction of its integer rate).  With w the first 19 significant
+// digits and q the decimal exponent, w * 10^q = w * 5^q * 2^q: the
+// normalised w is multiplied by a 128-bit normalised power of five (the
+// scheme of Lemire, "Number Parsing at a Gigabyte per Second", 2021), the
+// top 54 bits of the exact 192-bit product give the significand and the
+// rounding bit, the lower bits the sticky bit, and the binary64 bits are
+// assembled directly (ties to even, subnormals, overflow to infinity).
+// Powers 5^q with 0 <= q <= 55 are exact in the table, so every input with
+// at most 19 digits and such a q converts exactly; for the other q the
+// truncated table entry (relative error < 2^-127) can only matter within
+// 2^-120 of a rounding tie, and dropped digits beyond the 19th only within
+// 10^-18: the result is then at most 1 ulp from the correctly rounded one.
 #pragma once
 #include <cstdint>
 #include "pp.h"
-#include "pow10_table.inc"
+
+#if defined(__CUDACC__)
+#define PP_FN __device__ __forceinline__
+#define PP_MFN __device__ __forceinline__
+#define PP_TABLE_QUAL __device__ const
+#define PP_LDG(p) __ldg(p)
+#else
+#define PP_FN static inline
+#define PP_MFN inline
+#define PP_TABLE_QUAL static const
+#define PP_LDG(p) (*(p))
+#endif
+
+#include "pow5_table.inc"
 
 namespace ppn {
 
-// 1e0 .. 1e22 are exactly representable in binary64
-__device__ __forceinline__ double exact_pow10(int k) {
-  constexpr double T[23] = {1e0,  1e1,  1e2,  1e3,  1e4,  1e5,  1e6,  1e7,
-                            1e8,  1e9,  1e10, 1e11, 1e12, 1e13, 1e14, 1e15,
-                            1e16, 1e17, 1e18, 1e19, 1e20, 1e21, 1e22};
-  return T[k];
+PP_FN void mul64x64(uint64_t a, uint64_t b, uint64_t* hi, uint64_t* lo) {
+#if defined(__CUDA_ARCH__)
+  *hi = __umul64hi(a, b);
+  *lo = a * b;
+#else
+  const unsigned __int128 p = (unsigned __int128)a * b;
+  *hi = (uint64_t)(p >> 64);
+  *lo = (uint64_t)p;
+#endif
 }
 
-struct DD { double hi, lo; };
-__device__ __forceinline__ DD dd_mul(DD a, DD b) {
-  double p = a.hi * b.hi;
-  double e = fma(a.hi, b.hi, -p);          // exact low part of a.hi*b.hi
-  e = fma(a.hi, b.lo, e);
-  e = fma(a.lo, b.hi, e);
-  double s = p + e;                        // fast two-sum (|p| >= |e|)
-  return {s, e - (s - p)};
+PP_FN int clz64(uint64_t x) {
+#if defined(__CUDA_ARCH__)
+  return __clzll((long long)x);
+#else
+  return __builtin_clzll(x);
+#endif
 }
 
-// mant * 10^e10, mant != 0, `inexact` when digits were dropped
-__device__ __noinline__ double scale_pow10_slow(uint64_t mant, int e10) {
-  if (e10 > PP_P10_MAX) return __longlong_as_double(0x7FF0000000000000ll);  // +inf
-  if (e10 < PP_P10_MIN) return 0.0;
-  const int k = e10 - PP_P10_MIN;
-  DD p = {__ldg(&pp_p10_hi[k]), __ldg(&pp_p10_lo[k])};
-  const int e2 = __ldg(&pp_p10_e2[k]);
-  // mant as a double-double: hi = RN(mant), lo = mant - hi (exact, |lo| < 2^11)
-  double mh = double(mant);
-  double ml = double(int64_t(mant - uint64_t(mh)));
-  DD r = dd_mul({mh, ml}, p);
-  // r in [1, 2^65) * 2^e2; round once to binary64 and scale
-  double v = r.hi + r.lo;
-  return scalbn(v, e2);
+// Bits of the binary64 nearest to w * 10^q (w > 0), see the file comment.
+PP_FN uint64_t decimal_to_binary64(uint64_t w, int q) {
+  if (q > PP_P5_MAX) return 0x7FF0000000000000ull;  // >= 10^309
+  if (q < PP_P5_MIN) return 0;                      // < 2^-1075
+  const int k = q - PP_P5_MIN;
+  const uint64_t th = PP_LDG(&pp_p5_hi[k]);
+  const uint64_t tl = PP_LDG(&pp_p5_lo[k]);
+  const int e5 = PP_LDG(&pp_p5_e2[k]);
+  const int lz = clz64(w);
+  const uint64_t W = w << lz;
+  // P = W * (th:tl) = p2:p1:p0
+  uint64_t ah, al, bh, bl;
+  mul64x64(W, tl, &ah, &al);
+  mul64x64(W, th, &bh, &bl);
+  const uint64_t p0 = al;
+  uint64_t p1 = bl + ah;
+  const uint64_t p2 = bh + (p1 < bl ? 1u : 0u);
+  // w*10^q = P * 2^(q + e5 - 127 - lz) = p2 * 2^(1 + q + e5 - lz) + lower
+  const int ub = int(p2 >> 63);             // MSB of p2 at bit 63 (1) or 62 (0)
+  const int drop = 9 + ub;                  // bits of p2 below the 54 kept
+  const int scale = 1 + q + e5 - lz;        // value = p2 * 2^scale
+  // binary exponent of the 53-bit significand m53 (value = m53 * 2^e)
+  int e = scale + drop + 1;
+  const int biased = e + 1075;              // IEEE exponent field if normal
+  int shift = drop + 1;                     // bits of p2 below the significand
+  if (biased <= 0) {                        // subnormal: drop more bits
+    shift += 1 - biased;
+    if (shift > 64) return 0;               // below half the least subnormal
+  }
+  // m54 = significand plus one rounding bit; sticky = anything below it
+  uint64_t m54, below;
+  if (shift == 64) {
+    m54 = p2 >> 63;
+    below = p2 & ~(1ull << 63);
+  } else {
+    m54 = p2 >> (shift - 1);
+    below = p2 & ((1ull << (shift - 1)) - 1);
+  }
+  const bool sticky = below != 0 || p1 != 0 || p0 != 0;
+  uint64_t m = m54 >> 1;
+  if ((m54 & 1) && (sticky || (m & 1))) ++m;  // round to nearest, ties to even
+  if (biased <= 0) return m;                   // subnormal (m may reach 2^52: fine)
+  if (m == (1ull << 53)) { m >>= 1; ++e; }
+  const int be = e + 1075;
+  if (be >= 2047) return 0x7FF0000000000000ull;
+  return (uint64_t(be) << 52) | (m & ((1ull << 52) - 1));
 }
 
 struct FloatAcc {
@@ -59,16 +112,15 @@ struct FloatAcc {
   uint16_t nsig = 0;   // digits accumulated into mant
   uint16_t ndig = 0;   // digits in int + frac parts
   uint8_t phase = 0;   // 0 start, 1 int, 2 frac, 3 'e' seen, 4 exp sign, 5 exp digits, 6 error
-  bool neg = false, eneg = false, inexact = false;
+  bool neg = false, eneg = false;
 
-  __device__ __forceinline__ void digit(uint32_t d, bool frac) {
+  PP_MFN void digit(uint32_t d, bool frac) {
     ++ndig;
     if (nsig == 0 && d == 0) { if (frac) --d10; return; }
     if (nsig < 19) { mant = mant * 10 + d; ++nsig; if (frac) --d10; return; }
     if (!frac) ++d10;
-    if (d) inexact = true;
   }
-  __device__ __forceinline__ void feed(uint32_t c) {
+  PP_MFN void feed(uint32_t c) {
     const uint32_t d = c - '0';
     switch (phase) {
       case 0:
@@ -104,23 +156,12 @@ struct FloatAcc {
         break;
     }
   }
-  // returns 0 or PP_ERR_NUM_SYNTAX; *out gets the value (0 on error)
-  __device__ __forceinline__ int finish(double* out) const {
-    *out = 0.0;
+  // returns 0 or PP_ERR_NUM_SYNTAX; *bits gets the binary64 bits (0 on error)
+  PP_MFN int finish(uint64_t* bits) const {
+    *bits = 0;
     if (phase == 6 || phase == 3 || phase == 4 || ndig == 0) return PP_ERR_NUM_SYNTAX;
-    double v;
-    if (mant == 0) {
-      v = 0.0;
-    } else {
-      const int e10 = d10 + (eneg ? -ex : ex);
-      if (!inexact && mant <= (1ull << 53) && e10 >= -22 && e10 <= 22) {
-        const double m = double(mant);  // exact
-        v = e10 >= 0 ? m * exact_pow10(e10) : m / exact_pow10(-e10);
-      } else {
-        v = scale_pow10_slow(mant, e10);
-      }
-    }
-    *out = neg ? -v : v;
+    const uint64_t mag = mant == 0 ? 0 : decimal_to_binary64(mant, d10 + (eneg ? -ex : ex));
+    *bits = mag | (neg ? (1ull << 63) : 0);
     return 0;
   }
 };
@@ -130,7 +171,7 @@ struct IntAcc {
   uint8_t phase = 0;  // 0 start, 1 after sign, 2 digits, 3 error
   bool neg = false, ovf = false;
 
-  __device__ __forceinline__ void feed(uint32_t c) {
+  PP_MFN void feed(uint32_t c) {
     if (phase == 0 && (c == '+' || c == '-')) { neg = c == '-'; phase = 1; return; }
     const uint32_t d = c - '0';
     if (d > 9 || phase == 3) { phase = 3; return; }
@@ -138,12 +179,12 @@ struct IntAcc {
     if (mag > 1844674407370955161ull || (mag == 1844674407370955161ull && d > 5)) ovf = true;
     else mag = mag * 10 + d;
   }
-  // lo_mag: magnitude allowed when negative, hi: when positive
-  __device__ __forceinline__ int finish(uint64_t neg_max, uint64_t pos_max, int64_t* out) const {
+  // neg_max: magnitude allowed when negative, pos_max: when positive
+  PP_MFN int finish(uint64_t neg_max, uint64_t pos_max, int64_t* out) const {
     *out = 0;
     if (phase != 2) return PP_ERR_NUM_SYNTAX;
     if (ovf || mag > (neg ? neg_max : pos_max)) return PP_ERR_NUM_OVERFLOW;
-    *out = neg ? int64_t(0) - int64_t(mag) : int64_t(mag);
+    *out = neg ? int64_t(~mag + 1) : int64_t(mag);
     return 0;
   }
 };

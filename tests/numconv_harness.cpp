@@ -1,0 +1,21 @@
+// Host build of the library's numeric field conversion (pp_numeric.cuh) so
+// that its arithmetic can be checked on the CPU against an independent,
+// correctly rounded conversion.  Not part of the library.
+#include <cstddef>
+#include <cstdint>
+#include "pp_numeric.cuh"
+
+extern "C" {
+// `buf` holds n strings, each terminated by one 0x00 byte.  For each:
+// bits[i] = binary64 bits, err[i] = 0 / PP_ERR_NUM_SYNTAX.
+void h_parse_floats(const unsigned char* buf, size_t n, uint64_t* bits, int* err) {
+  size_t p = 0;
+  for (size_t i = 0; i < n; ++i) {
+    ppn::FloatAcc a;
+    while (buf[p]) a.feed(buf[p++]);
+    ++p;
+    err[i] = a.finish(&bits[i]);
+  }
+}
+uint64_t h_decimal_to_binary64(uint64_t w, int q) { return ppn::decimal_to_binary64(w, q); }
+}

