@@ -64,8 +64,10 @@ GenericDfa to_generic(const pp_dfa_desc* d) {
 //   bits 16..19  4: the invalid state maps to itself
 //   bits 20..27  2-bit tag of (s, g), s = 0..3: DATA 0, FD 1, RD 2, CTRL 3
 //   bits 28..29  3: the invalid state's bytes are treated as control
+//   bit  30      the group is not inert in the sticky state X: it changes
+//                X or tags a byte of X other than DATA
 //   bit  31      the group is not the background group
-uint32_t parse_lut_entry(const pp_dfa_desc* d, int g) {
+uint32_t parse_lut_entry(const pp_dfa_desc* d, int g, int x) {
   uint32_t e = 4u << 16 | 3u << 28;
   for (int s = 0; s < 4; ++s) {
     const uint32_t nx = s < d->n_states ? d->delta[g][s] : uint32_t(s);
@@ -82,7 +84,23 @@ uint32_t parse_lut_entry(const pp_dfa_desc* d, int g) {
     e |= tg << (20 + 2 * s);
   }
   if (g != d->background_group) e |= 1u << 31;
+  if (x < 4 && (d->delta[g][x] != x || d->tag[x][g] != PP_TAG_DATA)) e |= 1u << 30;
   return e;
+}
+
+// The live state with the fewest non-inert symbol groups (a group is inert
+// in s if it keeps s and tags the byte DATA); runs of inert bytes in that
+// state need no DFA steps.  4 when no state has an inert group.
+int sticky_state(const pp_dfa_desc* d) {
+  const int live = d->n_states == 5 ? 4 : d->n_states;
+  int best = 4, best_n = d->n_groups;
+  for (int s = 0; s < live; ++s) {
+    int n = 0;
+    for (int g = 0; g < d->n_groups; ++g)
+      if (d->delta[g][s] != s || d->tag[s][g] != PP_TAG_DATA) ++n;
+    if (n < best_n) { best = s; best_n = n; }
+  }
+  return best;
 }
 
 // pp_parse's extra constraints: at most 4 live states plus an absorbing
@@ -294,7 +312,9 @@ pp_rc pp_parse(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa, int 
   if (nt > 0xFFFFFFF0ull) return PP_EINVAL;
   p.n_tiles = uint32_t(nt);
   p.spin_limit = ppi::g_spin_limit;
-  for (int b = 0; b < 256; ++b) p.lut[b] = parse_lut_entry(dfa, dfa->byte_to_group[b]);
+  const int x = sticky_state(dfa);
+  p.sticky = uint32_t(x);
+  for (int b = 0; b < 256; ++b) p.lut[b] = parse_lut_entry(dfa, dfa->byte_to_group[b], x);
   p.bg_next = 0;
   if (dfa->background_group != 0xFF) {
     for (int s = 0; s < 4; ++s)
@@ -311,13 +331,12 @@ pp_rc pp_parse(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa, int 
   p.st = d_status;
 
   const int ns = ppi::parse_ns_width(n_str);
-  const size_t sb = ppi::parse_scratch_bytes(p.n_tiles, ns);
+  const size_t sb = ppi::parse_scratch_bytes(p.n_tiles, ns, n_cols);
   void* scratch = nullptr;
   cudaError_t e = cudaMallocAsync(&scratch, sb, stream);
   if (e != cudaSuccess) return cuda_rc(e);
-  ppi::parse_scratch_carve(scratch, p.n_tiles, ns, &p.s);
-  e = ppi::launch_parse_init(p, sb, scratch, stream);
-  if (e == cudaSuccess) e = ppi::launch_parse(p, stream);
+  ppi::parse_scratch_carve(scratch, p.n_tiles, ns, n_cols, &p.s);
+  e = ppi::launch_parse(p, stream);
   const cudaError_t ef = cudaFreeAsync(scratch, stream);
   if (e == cudaSuccess) e = ef;
   return cuda_rc(e);

@@ -8,16 +8,26 @@ namespace ppi {
 
 constexpr int MAX_STR_COLS = 16;  // string columns per pp_parse call
 
-// Cross-block scratch of one pp_parse call (device memory, zeroed per call).
+// Scratch of one pp_parse call (device memory).
+//   ctx:  per tile, written by the context pass: transition vector and, for
+//         each of the 4 live start states, record count, column offset,
+//         last terminator, value bytes per string column (absolute
+//         columns) and per relative field of the first partial record.
+//   pre:  per tile, written by the scan: start state, record index, column,
+//         last terminator before the tile, chars base per string column.
+//   scan_*: cross-block look-back state of the scan kernel.
 struct ParseScratch {
-  unsigned long long* lb1;  // [n_tiles] flag|STV
-  uint32_t* lb2_flag;       // [n_tiles]
-  uint64_t* lb2_agg;        // [n_tiles][4]
-  uint64_t* lb2_inc;        // [n_tiles][4]
-  uint32_t* lb3_flag;       // [n_tiles]
-  uint64_t* lb3_agg;        // [n_tiles][ns]
-  uint64_t* lb3_inc;        // [n_tiles][ns]
-  uint32_t* tile_counter;   // [1]
+  uint8_t* ctx;
+  uint8_t* pre;
+  uint32_t ctx_stride, pre_stride;
+  uint32_t* counters;       // [0] context pass, [1] main pass, [2] scan tickets
+  uint32_t* scan_flag_a;    // [n_scan_blocks]
+  uint64_t* scan_agg_a;     // [n_scan_blocks][13]
+  uint64_t* scan_inc_a;
+  uint32_t* scan_flag_c;    // [n_scan_blocks]
+  uint64_t* scan_agg_c;     // [n_scan_blocks][ns]
+  uint64_t* scan_inc_c;
+  uint32_t n_scan_blocks;
 };
 
 struct ParseParams {
@@ -27,6 +37,7 @@ struct ParseParams {
   uint32_t spin_limit;
   uint32_t lut[256];      // per byte: STV selector, next-state/tag fields, special bit
   uint32_t bg_next;       // nibble s = delta[background][s], s = 0..4
+  uint32_t sticky;        // state whose non-inert groups set LUT bit 30 (4: none)
   uint16_t accept_mask;
   uint8_t start_state;
   uint8_t has_inv;        // state 4 is the absorbing invalid state
@@ -47,12 +58,11 @@ struct ParseParams {
 
 // bytes of scratch for n_tiles tiles and ns string columns (ns rounded to the
 // kernel's instantiation width)
-size_t parse_scratch_bytes(uint32_t n_tiles, int ns);
-void parse_scratch_carve(void* base, uint32_t n_tiles, int ns, ParseScratch* out);
+size_t parse_scratch_bytes(uint32_t n_tiles, int ns, int n_cols);
+void parse_scratch_carve(void* base, uint32_t n_tiles, int ns, int n_cols, ParseScratch* out);
 int parse_ns_width(int n_str);
 
-cudaError_t launch_parse_init(const ParseParams& p, size_t scratch_bytes, void* scratch,
-                              cudaStream_t stream);
+// init (counters, scan flags, status), context pass, scan, main pass
 cudaError_t launch_parse(const ParseParams& p, cudaStream_t stream);
 size_t parse_tile_bytes();
 

@@ -69,6 +69,43 @@ def test_parse_workloads(name, target):
     assert st["error"] == 0 and st["n_records"] == info["n_records"]
 
 
+@pytest.mark.parametrize("name", ["csv16_256mib", "csv18_2gib"])
+def test_parse_many_tiles(name):
+    """About 40 MB: more than 2048 tiles, so the tile scan runs in several
+    blocks chained by look-back and every warp of a scan block holds tiles."""
+    data, info, _ = datagen.generate(name, target=40 << 20)
+    st = compare_csv(data, datagen.WORKLOADS[name]["cols"])
+    assert st["error"] == 0 and st["n_records"] == info["n_records"]
+
+
+@pytest.mark.parametrize("shift", [0, 1, 13, 31])
+def test_parse_quoted_newlines_everywhere(shift):
+    """Quoted fields holding record delimiters, field delimiters and doubled
+    quotes, with lengths that walk them across every chunk and tile offset."""
+    rng = random.Random(shift)
+    parts = [b'0,"' + b"p" * shift + b'",0.5\n']
+    size = len(parts[0])
+    while size < 3 * TILE + 500:
+        k = rng.randrange(0, 70)
+        body = bytes(rng.choice(b'ab\n,"') for _ in range(k)).replace(b'"', b'""')
+        rec = b"%d,\"%s\",%d.5\n" % (rng.randrange(-99, 99), body, rng.randrange(1000))
+        parts.append(rec)
+        size += len(rec)
+    data = b"".join(parts)
+    compare_csv(data, ["i32", "str", "f64"])
+    compare_csv(data, ["i32", "skip", "f64"])
+    compare_csv(data, ["str", "str", "str"])
+
+
+def test_parse_tiny_records():
+    """Tiles with more fields than the per-tile field list holds."""
+    data = b"".join(b"%d,%d\n" % (i % 10, i % 7) for i in range(3 * TILE // 4 + 9))
+    compare_csv(data, ["i32", "i8"])
+    compare_csv(data, ["str", "i64"])
+    compare_csv(b"\n" * (2 * TILE + 3), ["str"])
+    compare_csv(b",\n" * (2 * TILE + 3), ["str", "i32"])
+
+
 @pytest.mark.parametrize("offset", [1, 7])
 def test_parse_misaligned_input(offset):
     data, _, _ = datagen.generate("csv16_256mib", target=3 * TILE + 5)
