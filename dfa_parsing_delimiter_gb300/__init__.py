@@ -8,6 +8,7 @@ fallback: if ``libpp.so`` is missing, loading fails with an error.
 Names follow the C ABI in ``include/pp.h``:
 
   pp_parse / parse_csv          delimiter-separated input -> columns
+  pp_parse_noalloc              pp_parse with a fixed, compiled-in scratch buffer
   pp_tokenize / tokenize        general DFA lexer -> (token_id, start, len)
   pp_tags / tags                per-byte state and tag (test hook)
   pp_count_byte / count_byte    byte count (record-capacity bound)
@@ -23,7 +24,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libpp.so")
 
-PP_OK, PP_EINVAL, PP_ECUDA, PP_ENOMEM = 0, 1, 2, 3
+PP_OK, PP_EINVAL, PP_ECUDA, PP_ENOMEM, PP_ETOOLARGE = 0, 1, 2, 3, 4
 COL = {"str": 0, "i8": 1, "i32": 2, "i64": 3, "f64": 4, "skip": 5}
 DTYPE = {"i8": torch.int8, "i32": torch.int32, "i64": torch.int64, "f64": torch.float64}
 ERR_INVALID_INPUT, ERR_BAD_END_STATE, ERR_COLCOUNT = 1, 2, 4
@@ -65,6 +66,8 @@ def lib() -> ctypes.CDLL:
         L.pp_parse.restype = ctypes.c_int
         L.pp_parse.argtypes = [_vp, _sz, ctypes.POINTER(DfaDesc), ctypes.c_int, _vp, _vp, _vp, _vp,
                                _sz, _vp, _vp, _vp]
+        L.pp_parse_noalloc.restype = ctypes.c_int
+        L.pp_parse_noalloc.argtypes = L.pp_parse.argtypes
         L.pp_tokenize.restype = ctypes.c_int
         L.pp_tokenize.argtypes = [_vp, _sz, ctypes.POINTER(DfaDesc), _vp, _vp, _vp, _sz, _vp, _vp]
         L.pp_tags.restype = ctypes.c_int
@@ -152,6 +155,24 @@ def pp_parse(d_in: torch.Tensor, n_bytes: int, desc: DfaDesc, col_types, out_off
     _check(rc, "pp_parse")
 
 
+def pp_parse_noalloc(d_in: torch.Tensor, n_bytes: int, desc: DfaDesc, col_types, out_offsets,
+                     out_chars, out_typed, records_capacity: int, chars_capacity,
+                     status: torch.Tensor, stream=None) -> None:
+    """Direct pp_parse_noalloc call: pp_parse's arguments; the library
+    allocates nothing; calls must not overlap on one device."""
+    n = len(col_types)
+    ct = (ctypes.c_int * n)(*[COL[c] if isinstance(c, str) else int(c) for c in col_types])
+    arrs = [None if a is None else (_vp * n)(*[_ptr(x) for x in a])
+            for a in (out_offsets, out_chars, out_typed)]
+    cc = (_sz * n)(*[int(x) for x in chars_capacity]) if chars_capacity is not None else None
+    rc = lib().pp_parse_noalloc(
+        _ptr(d_in), int(n_bytes), ctypes.byref(desc), n, ctypes.addressof(ct),
+        *[ctypes.addressof(a) if a is not None else None for a in arrs],
+        int(records_capacity), ctypes.addressof(cc) if cc is not None else None,
+        _ptr(status), _stream(stream))
+    _check(rc, "pp_parse_noalloc")
+
+
 def pp_tokenize(d_in, n_bytes, desc, out_id, out_start, out_len, capacity, status,
                 stream=None) -> None:
     rc = lib().pp_tokenize(_ptr(d_in), int(n_bytes), ctypes.byref(desc), _ptr(out_id),
@@ -199,6 +220,11 @@ class CsvOutputs:
     def run(self, d_in: torch.Tensor, n_bytes: int, desc: DfaDesc, stream=None) -> None:
         pp_parse(d_in, n_bytes, desc, self.col_types, self.offsets, self.chars, self.typed,
                  self.records_capacity, self.chars_capacity, self.status, stream)
+
+    def run_noalloc(self, d_in: torch.Tensor, n_bytes: int, desc: DfaDesc, stream=None) -> None:
+        pp_parse_noalloc(d_in, n_bytes, desc, self.col_types, self.offsets, self.chars,
+                         self.typed, self.records_capacity, self.chars_capacity, self.status,
+                         stream)
 
     def output_bytes(self, n_records: int, chars_len) -> int:
         """Bytes the parse writes: offsets, chars and typed values."""

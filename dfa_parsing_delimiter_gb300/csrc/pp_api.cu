@@ -135,6 +135,85 @@ bool parse_dfa_ok(const pp_dfa_desc* d) {
 
 }  // namespace
 
+namespace ppi {
+
+// Host half of pp_parse: checks the arguments and fills the kernel
+// parameters (everything but the scratch carve).
+pp_rc parse_prepare(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa, int n_cols,
+                    const pp_coltype* col_types, int32_t* const out_offsets[],
+                    uint8_t* const out_chars[], void* const out_typed[],
+                    size_t records_capacity, const size_t chars_capacity[],
+                    pp_status* d_status, ParseParams* out) {
+  ParseParams& p = *out;
+  if (!d_status || (n_bytes && !d_in) || !parse_dfa_ok(dfa)) return PP_EINVAL;
+  if (n_cols < 1 || n_cols > PP_MAX_COLS || !col_types) return PP_EINVAL;
+  std::memset(&p, 0, sizeof p);
+  int n_str = 0;
+  bool any_out = false;
+  for (int c = 0; c < n_cols; ++c) {
+    const int ty = col_types[c];
+    if (ty < PP_COL_STRING || ty > PP_COL_SKIP) return PP_EINVAL;
+    p.coltype[c] = uint8_t(ty);
+    p.stridx[c] = -1;
+    if (ty == PP_COL_STRING) {
+      if (n_str >= ppi::MAX_STR_COLS) return PP_EINVAL;
+      p.stridx[c] = int8_t(n_str);
+      p.strcol[n_str] = uint8_t(c);
+      ++n_str;
+    }
+    if ((out_offsets && out_offsets[c]) || (out_chars && out_chars[c]) ||
+        (out_typed && out_typed[c]))
+      any_out = true;
+  }
+  for (int c = n_cols; c < PP_MAX_COLS; ++c) { p.coltype[c] = PP_COL_SKIP; p.stridx[c] = -1; }
+  if (any_out) {
+    for (int c = 0; c < n_cols; ++c) {
+      const int ty = col_types[c], si = p.stridx[c];
+      if (ty == PP_COL_STRING) {
+        if (!out_offsets || !out_chars || !out_offsets[c] || !chars_capacity) return PP_EINVAL;
+        if (!out_chars[c] && chars_capacity[c]) return PP_EINVAL;
+        p.offsets[si] = out_offsets[c];
+        p.chars[si] = out_chars[c];
+        p.chars_cap[si] = chars_capacity[c];
+      } else if (ty != PP_COL_SKIP) {
+        if (!out_typed || (!out_typed[c] && records_capacity)) return PP_EINVAL;
+        p.typed[c] = out_typed[c];
+      }
+    }
+    p.rec_cap = records_capacity;
+  } else {
+    p.rec_cap = ~0ull;
+    for (int c = 0; c < n_str; ++c) p.chars_cap[c] = ~0ull;
+  }
+  p.in = d_in;
+  p.n = n_bytes;
+  const uint64_t tile = ppi::parse_tile_bytes();
+  const uint64_t nt = (uint64_t(n_bytes) + tile - 1) / tile;
+  if (nt > 0xFFFFFFF0ull) return PP_EINVAL;
+  p.n_tiles = uint32_t(nt);
+  p.spin_limit = ppi::g_spin_limit;
+  const int x = sticky_state(dfa);
+  p.sticky = uint32_t(x);
+  for (int b = 0; b < 256; ++b) p.lut[b] = parse_lut_entry(dfa, dfa->byte_to_group[b], x);
+  p.bg_next = 0;
+  if (dfa->background_group != 0xFF) {
+    for (int s = 0; s < 4; ++s)
+      p.bg_next |= uint32_t(s < dfa->n_states ? dfa->delta[dfa->background_group][s] : s)
+                   << (4 * s);
+    p.bg_next |= 4u << 16;
+  }
+  p.accept_mask = dfa->accept_mask;
+  p.start_state = dfa->start_state;
+  p.has_inv = dfa->invalid_state == 4;
+  p.n_cols = n_cols;
+  p.n_str = n_str;
+  p.has_out = any_out ? 1 : 0;
+  p.st = d_status;
+  return PP_OK;
+}
+
+}  // namespace ppi
+
 extern "C" {
 
 const char* pp_strerror(int code) {
@@ -143,6 +222,7 @@ const char* pp_strerror(int code) {
     case PP_EINVAL: return "invalid argument";
     case PP_ECUDA: return "CUDA error";
     case PP_ENOMEM: return "out of device memory";
+    case PP_ETOOLARGE: return "input needs more scratch than the fixed buffer holds";
     default: return "unknown error";
   }
 }
@@ -264,73 +344,12 @@ pp_rc pp_parse(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa, int 
                const pp_coltype* col_types, int32_t* const out_offsets[],
                uint8_t* const out_chars[], void* const out_typed[], size_t records_capacity,
                const size_t chars_capacity[], pp_status* d_status, cudaStream_t stream) {
-  if (!d_status || (n_bytes && !d_in) || !parse_dfa_ok(dfa)) return PP_EINVAL;
-  if (n_cols < 1 || n_cols > PP_MAX_COLS || !col_types) return PP_EINVAL;
   ppi::ParseParams p;
-  std::memset(&p, 0, sizeof p);
-  int n_str = 0;
-  bool any_out = false;
-  for (int c = 0; c < n_cols; ++c) {
-    const int ty = col_types[c];
-    if (ty < PP_COL_STRING || ty > PP_COL_SKIP) return PP_EINVAL;
-    p.coltype[c] = uint8_t(ty);
-    p.stridx[c] = -1;
-    if (ty == PP_COL_STRING) {
-      if (n_str >= ppi::MAX_STR_COLS) return PP_EINVAL;
-      p.stridx[c] = int8_t(n_str);
-      p.strcol[n_str] = uint8_t(c);
-      ++n_str;
-    }
-    if ((out_offsets && out_offsets[c]) || (out_chars && out_chars[c]) ||
-        (out_typed && out_typed[c]))
-      any_out = true;
-  }
-  for (int c = n_cols; c < PP_MAX_COLS; ++c) { p.coltype[c] = PP_COL_SKIP; p.stridx[c] = -1; }
-  if (any_out) {
-    for (int c = 0; c < n_cols; ++c) {
-      const int ty = col_types[c], si = p.stridx[c];
-      if (ty == PP_COL_STRING) {
-        if (!out_offsets || !out_chars || !out_offsets[c] || !chars_capacity) return PP_EINVAL;
-        if (!out_chars[c] && chars_capacity[c]) return PP_EINVAL;
-        p.offsets[si] = out_offsets[c];
-        p.chars[si] = out_chars[c];
-        p.chars_cap[si] = chars_capacity[c];
-      } else if (ty != PP_COL_SKIP) {
-        if (!out_typed || (!out_typed[c] && records_capacity)) return PP_EINVAL;
-        p.typed[c] = out_typed[c];
-      }
-    }
-    p.rec_cap = records_capacity;
-  } else {
-    p.rec_cap = ~0ull;
-    for (int c = 0; c < n_str; ++c) p.chars_cap[c] = ~0ull;
-  }
-  p.in = d_in;
-  p.n = n_bytes;
-  const uint64_t tile = ppi::parse_tile_bytes();
-  const uint64_t nt = (uint64_t(n_bytes) + tile - 1) / tile;
-  if (nt > 0xFFFFFFF0ull) return PP_EINVAL;
-  p.n_tiles = uint32_t(nt);
-  p.spin_limit = ppi::g_spin_limit;
-  const int x = sticky_state(dfa);
-  p.sticky = uint32_t(x);
-  for (int b = 0; b < 256; ++b) p.lut[b] = parse_lut_entry(dfa, dfa->byte_to_group[b], x);
-  p.bg_next = 0;
-  if (dfa->background_group != 0xFF) {
-    for (int s = 0; s < 4; ++s)
-      p.bg_next |= uint32_t(s < dfa->n_states ? dfa->delta[dfa->background_group][s] : s)
-                   << (4 * s);
-    p.bg_next |= 4u << 16;
-  }
-  p.accept_mask = dfa->accept_mask;
-  p.start_state = dfa->start_state;
-  p.has_inv = dfa->invalid_state == 4;
-  p.n_cols = n_cols;
-  p.n_str = n_str;
-  p.has_out = any_out ? 1 : 0;
-  p.st = d_status;
-
-  const int ns = ppi::parse_ns_width(n_str);
+  const pp_rc rc = ppi::parse_prepare(d_in, n_bytes, dfa, n_cols, col_types, out_offsets,
+                                      out_chars, out_typed, records_capacity, chars_capacity,
+                                      d_status, &p);
+  if (rc != PP_OK) return rc;
+  const int ns = ppi::parse_ns_width(p.n_str);
   const size_t sb = ppi::parse_scratch_bytes(p.n_tiles, ns, n_cols);
   void* scratch = nullptr;
   cudaError_t e = cudaMallocAsync(&scratch, sb, stream);

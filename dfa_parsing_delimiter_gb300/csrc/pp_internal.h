@@ -64,6 +64,12 @@ int parse_ns_width(int n_str);
 
 // init (counters, scan flags, status), context pass, scan, main pass
 cudaError_t launch_parse(const ParseParams& p, cudaStream_t stream);
+// pp_parse's argument checks and kernel parameters (all but the scratch)
+pp_rc parse_prepare(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa, int n_cols,
+                    const pp_coltype* col_types, int32_t* const out_offsets[],
+                    uint8_t* const out_chars[], void* const out_typed[],
+                    size_t records_capacity, const size_t chars_capacity[],
+                    pp_status* d_status, ParseParams* out);
 size_t parse_tile_bytes();
 
 // ---------------------------------------------------------- pp_tags / tokenize

@@ -49,7 +49,7 @@ extern "C" {
 #define PP_MAX_GROUPS 16
 
 /* host return codes */
-typedef enum { PP_OK = 0, PP_EINVAL = 1, PP_ECUDA = 2, PP_ENOMEM = 3 } pp_rc;
+typedef enum { PP_OK = 0, PP_EINVAL = 1, PP_ECUDA = 2, PP_ENOMEM = 3, PP_ETOOLARGE = 4 } pp_rc;
 
 /* column kinds for pp_parse */
 typedef enum {
@@ -153,6 +153,41 @@ pp_rc pp_parse(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa, int 
                uint8_t* const out_chars[], void* const out_typed[],
                size_t records_capacity, const size_t chars_capacity[],
                pp_status* d_status, cudaStream_t stream);
+
+/* Size of pp_parse_noalloc's fixed scratch buffer (per device). */
+#define PP_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/*
+ * pp_parse_noalloc — pp_parse without allocation: its cross-tile scratch
+ * (tile contexts, scan flags and aggregates) lives in a buffer of
+ * PP_NOALLOC_SCRATCH_BYTES compiled into the library, one per device.  The
+ * ParPaRaw paper has no counterpart; this is an integration entry point
+ * for callers that cannot allocate device memory per call (devices or
+ * driver set-ups without stream-ordered memory pools, where pp_parse's
+ * cudaMallocAsync fails; services whose device memory is fixed at
+ * start-up).
+ *   Arguments, semantics, outputs and d_status: exactly those of pp_parse.
+ *   Limit: the scratch needed is about 88 bytes per 16 KiB tile of input
+ *   with no string column, rising with the string and column counts to
+ *   about 856 bytes per tile with 16 string columns of 64; so 4 MiB holds
+ *   inputs up to about 740 MiB in the first case and about 76 MiB in the
+ *   last.  A larger input returns PP_ETOOLARGE before any CUDA call.
+ *   First call on each device: it looks up the buffer's address
+ *   (cudaGetSymbolAddress; this can load the library's device code) and
+ *   sets kernel attributes.  Make that first call before any stream
+ *   capture starts on the device.
+ *   Calls share the buffer: two calls in flight on one device at the same
+ *   time (on different streams, or from host threads with no ordering
+ *   between them) race on it and corrupt each other's results.  Issue the
+ *   calls on one stream, or order them by events or synchronisation.
+ * Returns PP_EINVAL for bad arguments, PP_ETOOLARGE as above, PP_ECUDA on
+ * CUDA errors.
+ */
+pp_rc pp_parse_noalloc(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa, int n_cols,
+                       const pp_coltype* col_types, int32_t* const out_offsets[],
+                       uint8_t* const out_chars[], void* const out_typed[],
+                       size_t records_capacity, const size_t chars_capacity[],
+                       pp_status* d_status, cudaStream_t stream);
 
 /*
  * pp_tokenize — run a general DFA (|S| <= 16) over the input and emit one
