@@ -159,6 +159,7 @@ pp_rc parse_prepare(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa,
       if (n_str >= ppi::MAX_STR_COLS) return PP_EINVAL;
       p.stridx[c] = int8_t(n_str);
       p.strcol[n_str] = uint8_t(c);
+      p.strmask |= 1ull << c;
       ++n_str;
     }
     if ((out_offsets && out_offsets[c]) || (out_chars && out_chars[c]) ||

@@ -142,31 +142,39 @@ __device__ uint32_t lookback_word(unsigned long long* words, uint32_t tile, uint
 // tile's own aggregate and its inclusive prefix), each K x uint64.  The
 // payload is written with L2-only stores before a release store of the
 // flag; readers acquire the flag, then read the payload from L2.
-// Executed by one full warp; `agg`, `seed`, `identity`, result are K words
-// replicated in every lane.
+//
+// lb_publish_vec posts the tile's aggregate (tile 0: its inclusive prefix)
+// and returns at once; lb_resolve_vec later walks back over predecessors
+// and posts the inclusive prefix.  Splitting the two lets a block do other
+// work while its predecessors finish.  Both are executed by one full warp;
+// `agg`, `seed`, `identity` and the result are K words replicated in every
+// lane.
 template <int K, class Op>
-__device__ void lookback_vec(uint32_t* flags, uint64_t* agg_arr, uint64_t* inc_arr,
-                             uint32_t tile, const uint64_t (&agg)[K], const uint64_t (&seed)[K],
-                             const uint64_t (&identity)[K], Op op, const LookbackCfg& cfg,
-                             uint64_t (&out_excl)[K]) {
+__device__ __forceinline__ void lb_publish_vec(uint32_t* flags, uint64_t* agg_arr,
+                                               uint64_t* inc_arr, uint32_t tile,
+                                               const uint64_t (&agg)[K],
+                                               const uint64_t (&seed)[K], Op op) {
+  if ((threadIdx.x & 31) != 0) return;
+  uint64_t v[K];
+  op(seed, agg, v);
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    uint64_t* dst = (tile == 0 ? inc_arr : agg_arr) + size_t(tile) * K + k;
+    __stcg(reinterpret_cast<unsigned long long*>(dst), tile == 0 ? v[k] : agg[k]);
+  }
+  st_release(&flags[tile], tile == 0 ? LB_INC : LB_AGG);
+}
+
+template <int K, class Op>
+__device__ void lb_resolve_vec(uint32_t* flags, uint64_t* agg_arr, uint64_t* inc_arr,
+                               uint32_t tile, const uint64_t (&agg)[K],
+                               const uint64_t (&seed)[K], const uint64_t (&identity)[K], Op op,
+                               const LookbackCfg& cfg, uint64_t (&out_excl)[K]) {
   const int lane = threadIdx.x & 31;
   if (tile == 0) {
-    uint64_t inc[K];
-    op(seed, agg, inc);
-    if (lane == 0) {
-#pragma unroll
-      for (int k = 0; k < K; ++k) __stcg(reinterpret_cast<unsigned long long*>(&inc_arr[k]), inc[k]);
-      st_release(&flags[0], LB_INC);
-    }
 #pragma unroll
     for (int k = 0; k < K; ++k) out_excl[k] = seed[k];
     return;
-  }
-  if (lane == 0) {
-#pragma unroll
-    for (int k = 0; k < K; ++k)
-      __stcg(reinterpret_cast<unsigned long long*>(&agg_arr[size_t(tile) * K + k]), agg[k]);
-    st_release(&flags[tile], LB_AGG);
   }
   uint64_t acc[K];
 #pragma unroll
@@ -202,6 +210,7 @@ __device__ void lookback_vec(uint32_t* flags, uint64_t* agg_arr, uint64_t* inc_a
 #pragma unroll
       for (int k = 0; k < K; ++k) v[k] = identity[k];
     }
+    // lane L combines with lane L+d, which holds an EARLIER tile
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
       uint64_t o[K], t[K];
@@ -233,6 +242,17 @@ __device__ void lookback_vec(uint32_t* flags, uint64_t* agg_arr, uint64_t* inc_a
   }
 #pragma unroll
   for (int k = 0; k < K; ++k) out_excl[k] = acc[k];
+}
+
+// Publish and resolve in one go.
+template <int K, class Op>
+__device__ void lookback_vec(uint32_t* flags, uint64_t* agg_arr, uint64_t* inc_arr,
+                             uint32_t tile, const uint64_t (&agg)[K], const uint64_t (&seed)[K],
+                             const uint64_t (&identity)[K], Op op, const LookbackCfg& cfg,
+                             uint64_t (&out_excl)[K]) {
+  lb_publish_vec<K>(flags, agg_arr, inc_arr, tile, agg, seed, op);
+  __syncwarp();
+  lb_resolve_vec<K>(flags, agg_arr, inc_arr, tile, agg, seed, identity, op, cfg, out_excl);
 }
 
 // ------------------------------------------------ 1-D bulk copy (TMA engine)

@@ -14,8 +14,9 @@ constexpr int MAX_STR_COLS = 16;  // string columns per pp_parse call
 //         last terminator, value bytes per string column (absolute
 //         columns) and per relative field of the first partial record.
 //   pre:  per tile, written by the scan: start state, record index, column,
-//         last terminator before the tile, chars base per string column.
-//   scan_*: cross-block look-back state of the scan kernel.
+//         last terminator before the tile, chars offset per string column.
+//   scan_*: cross-block look-back state of the scan kernel (a: contexts,
+//         c: chars offsets).
 struct ParseScratch {
   uint8_t* ctx;
   uint8_t* pre;
@@ -44,6 +45,7 @@ struct ParseParams {
   int32_t n_cols;
   int32_t n_str;
   int32_t has_out;
+  uint64_t strmask;             // bit c: column c is a string column
   int8_t stridx[PP_MAX_COLS];   // column -> string index, or -1
   uint8_t strcol[MAX_STR_COLS]; // string index -> column
   uint8_t coltype[PP_MAX_COLS];

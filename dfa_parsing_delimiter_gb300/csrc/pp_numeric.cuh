@@ -105,6 +105,36 @@ PP_FN uint64_t decimal_to_binary64(uint64_t w, int q) {
   return (uint64_t(be) << 52) | (m & ((1ull << 52) - 1));
 }
 
+// Bits of the binary64 nearest to w * 10^q for a short significand:
+// 0 < w < 2^32 and -22 <= q <= 0 (a plain decimal such as "463.86"), with
+// q == 0 the exact integer conversion.  w times the 128-bit table entry,
+// truncated to its top 96 bits, carries a relative error below 2^-94; the
+// value w / 10^-q is a rational whose distance from any rounding tie is
+// at least 2^-86 relative (its numerator against a 54-bit dyadic differs
+// by a nonzero integer), so the top 54 bits round correctly.
+PP_FN uint64_t short_decimal_to_binary64(uint32_t w, int q) {
+  const int lzw = clz64(uint64_t(w)) - 32;  // w != 0
+  if (q == 0)
+    return (uint64_t(1054 - lzw) << 52) | ((uint64_t(w) << (lzw + 21)) & ((1ull << 52) - 1));
+  const int k = q - PP_P5_MIN;
+  const uint64_t th = PP_LDG(&pp_p5_hi[k]);
+  const uint64_t tl = PP_LDG(&pp_p5_lo[k]);
+  const int e5 = PP_LDG(&pp_p5_e2[k]);
+  // (w * (th:tl)) >> 64 = hi * 2^32 + lo32, with hi >= 2^31
+  const uint64_t c1 = uint64_t(w) * uint32_t(tl);
+  const uint64_t c2 = uint64_t(w) * uint32_t(tl >> 32) + (c1 >> 32);
+  const uint64_t plo = uint64_t(w) * uint32_t(th) + (c2 >> 32);
+  const uint64_t hi = uint64_t(w) * uint32_t(th >> 32) + (plo >> 32);
+  const uint32_t lo32 = uint32_t(plo);
+  const int L = clz64(hi);                   // 0..32
+  const uint64_t top = L ? ((hi << L) | (uint64_t(lo32) >> (32 - L))) : hi;  // in [2^63, 2^64)
+  // w * 10^q ~= (hi * 2^32 + lo32) * 2^(q + e5 - 63) = top * 2^(32 - L + q + e5 - 63)
+  uint64_t m = (top >> 11) + ((top >> 10) & 1u);
+  int be = 32 - L + q + e5 - 63 + 11 + 52 + 1023;
+  if (m == (1ull << 53)) { m >>= 1; ++be; }
+  return (uint64_t(be) << 52) | (m & ((1ull << 52) - 1));
+}
+
 struct FloatAcc {
   uint64_t mant = 0;
   int32_t d10 = 0;     // decimal exponent adjustment from digit positions

@@ -59,13 +59,11 @@ constexpr int STAGE_BYTES = TILE + 16 * (ppi::MAX_STR_COLS + 1);
 constexpr int LUT_BYTES = 256 * 32 * 4;
 constexpr int SLOT_CAP = 4096;         // (column, record) slots per pass
 constexpr uint32_t ABS32 = 1u << 31;
-constexpr uint32_t SLOT_ABSENT = 0xFFFFFFFEu;  // field not closed in this tile
 constexpr uint32_t SLOT_DEFAULT = 0xFFFFFFFDu; // missing field: column default
 constexpr uint32_t WAIT_LIMIT = 1u << 24;      // bounded mbarrier polls
 constexpr int SCAN_NT = 256;           // scan kernel threads
 constexpr int SCAN_TPT = 8;            // tiles per scan thread
 constexpr int SCAN_TILES = SCAN_NT * SCAN_TPT;
-constexpr int CTX_HDR = 52;            // stv + rec[4] + col[4] + last[4]
 
 // ------------------------------------------------------------ helpers
 // (record count, column offset, last terminator) of a byte range; column
@@ -122,9 +120,19 @@ __device__ __forceinline__ uint32_t popc_range(const uint32_t* m, uint32_t a, ui
   return n;
 }
 
+// control bytes before tile position p (p <= tile length)
+__device__ __forceinline__ uint32_t ctrl_before(const uint32_t* ctrl_s, const uint16_t* cpre,
+                                                uint32_t p) {
+  const uint32_t w = p >> 5, b = p & 31u;
+  return cpre[w] + (b ? uint32_t(__popc(ctrl_s[w] & ((1u << b) - 1u))) : 0u);
+}
+
 // ------------------------------------------------- tile feeding (TMA)
-// Two linear landing buffers: while a tile is processed from one, the next
-// tile's bulk copy lands in the other.
+// Two linear landing buffers.  A block takes its first tile at start; when
+// it starts processing a tile it takes the next ticket and starts that
+// tile's bulk copy into the other buffer, which the previous tile has
+// released.  Tickets are thus taken in the order tiles start, and a tile's
+// predecessors have all started before it.
 struct Feed {
   uint64_t bar[2];
   uint32_t tile[2], issued[2], parity[2];
@@ -148,20 +156,24 @@ __device__ __forceinline__ void feed_start(const ParseParams& P, Feed& F, uint32
     for (int b = 0; b < 2; ++b) {
       mbar_init(&F.bar[b], 1);
       F.parity[b] = 0;
-      F.tile[b] = atomicAdd(counter, 1u);
-      F.issued[b] = issue_tile(P, F.tile[b], aligned_in, lin0 + b * TILE, &F.bar[b]);
+      F.issued[b] = 0;
     }
+    F.tile[0] = atomicAdd(counter, 1u);
+    F.issued[0] = issue_tile(P, F.tile[0], aligned_in, lin0, &F.bar[0]);
     F.cur = 0;
   }
   __syncthreads();
 }
 
 // Wait until the current tile is in its landing buffer (plain loads for a
-// ragged tail or unaligned input) and load this thread's chunk words.
-__device__ __forceinline__ void feed_tile(const ParseParams& P, Feed& F, uint8_t* lin_s,
-                                          uint64_t tile_base, uint32_t tile_len, uint32_t (&w)[8]) {
+// ragged tail or unaligned input), start the next tile's copy into the
+// other buffer, and load this thread's chunk words.
+__device__ __forceinline__ void feed_tile(const ParseParams& P, Feed& F, uint32_t* counter,
+                                          bool aligned_in, uint8_t* lin0, uint64_t tile_base,
+                                          uint32_t tile_len, uint32_t (&w)[8]) {
   const int t = threadIdx.x;
   const uint32_t b = F.cur;
+  uint8_t* lin_s = lin0 + b * TILE;
   const uint32_t bulk = F.issued[b] ? (tile_len & ~15u) : 0u;
   if (F.issued[b]) {
     if (!mbar_wait_bounded(&F.bar[b], F.parity[b], WAIT_LIMIT)) {
@@ -181,25 +193,26 @@ __device__ __forceinline__ void feed_tile(const ParseParams& P, Feed& F, uint8_t
   w[4] = hi.x; w[5] = hi.y; w[6] = hi.z; w[7] = hi.w;
 }
 
-// After the last read of the current buffer (behind a block barrier):
-// refill it with the next tile and switch buffers.
+// After the last read of the current buffer (the caller's earlier block
+// barrier): switch to the other buffer.
 __device__ __forceinline__ void feed_next(const ParseParams& P, Feed& F, uint32_t* counter,
                                           bool aligned_in, uint8_t* lin0) {
   if (threadIdx.x == 0) {
     const uint32_t b = F.cur;
     if (F.issued[b]) F.parity[b] ^= 1u;
-    F.tile[b] = atomicAdd(counter, 1u);
-    F.issued[b] = issue_tile(P, F.tile[b], aligned_in, lin0 + b * TILE, &F.bar[b]);
-    F.cur = b ^ 1u;
+    const uint32_t o = b ^ 1u;
+    F.tile[o] = atomicAdd(counter, 1u);
+    F.issued[o] = issue_tile(P, F.tile[o], aligned_in, lin0 + o * TILE, &F.bar[o]);
+    F.cur = o;
   }
   __syncthreads();
 }
 
 __device__ __forceinline__ void feed_finish(Feed& F) {
   // never leave with a bulk copy in flight into this CTA's shared memory
-  if (threadIdx.x == 0)
-    for (int b = 0; b < 2; ++b)
-      if (F.issued[b]) mbar_wait_bounded(&F.bar[b], F.parity[b], WAIT_LIMIT);
+  // (only the current buffer can have one: a copy is started only for a
+  // tile that exists, and every such tile is waited for before it is used)
+  if (threadIdx.x == 0 && F.issued[F.cur]) mbar_wait_bounded(&F.bar[F.cur], F.parity[F.cur], WAIT_LIMIT);
 }
 
 // Multi-instance DFA over the chunk (back to front): G := G o delta_group(b).
@@ -374,13 +387,6 @@ __device__ __forceinline__ uint64_t tile_load8(const uint32_t* tile_w, uint32_t 
   return uint64_t(__funnelshift_r(w0, w1, sh)) | (uint64_t(__funnelshift_r(w1, w2, sh)) << 32);
 }
 
-// Copy the chunk's bytes selected by `seg` (runs of set bits) from the tile
-// to stage_s from dst on.
-__device__ __forceinline__ void stage_runs(uint32_t seg, uint32_t dst, const uint8_t* chunk,
-                                           uint8_t* stage_s) {
-  for (uint32_t m = seg; m; m &= m - 1) stage_s[dst++] = chunk[__ffs(m) - 1];
-}
-
 // ------------------------------------------------- numeric fast paths
 // Digit values of the low n bytes of x (1 <= n <= 8) left-aligned for the
 // combining steps, or false if one of them is not a digit.
@@ -400,43 +406,10 @@ __device__ __forceinline__ uint64_t swar_value(uint64_t d) {
   d = (d * 100 + (d >> 16)) & 0x0000FFFF0000FFFFull;
   return (d * 10000 + (d >> 32)) & 0xFFFFFFFFull;
 }
-// Plain [+-]?[0-9]{1,16} field [a, a+L) of the tile: magnitude and sign.
-__device__ __forceinline__ bool fast_int(const uint32_t* tile_w, uint32_t a, uint32_t L, uint64_t& mag,
-                                         bool& neg) {
-  uint64_t x = tile_load8(tile_w, a);
-  const uint32_t c0 = uint32_t(x & 0xFFu);
-  neg = c0 == '-';
-  uint32_t skip = (c0 == '-' || c0 == '+') ? 1u : 0u;
-  const uint32_t n = L - skip;
-  if (n == 0 || n > 16) return false;
-  if (skip) x = tile_load8(tile_w, a + 1);
-  uint64_t d;
-  if (n <= 8) {
-    if (!swar_digits(x, n, d)) return false;
-    mag = swar_value(d);
-    return true;
-  }
-  if (!swar_digits(x, 8, d)) return false;
-  const uint64_t hi = swar_value(d);
-  uint64_t d2;
-  if (!swar_digits(tile_load8(tile_w, a + skip + 8), n - 8, d2)) return false;
-  const uint32_t m = n - 8;
-  uint64_t p10 = 1;
-  for (uint32_t i = 0; i < m; ++i) p10 *= 10;
-  mag = hi * p10 + swar_value(d2);
-  return true;
-}
-// Plain [+-]?digits[.digits] field of at most 8 characters after the sign:
-// significand and decimal exponent.
-__device__ __forceinline__ bool fast_float(const uint32_t* tile_w, uint32_t a, uint32_t L,
-                                           uint64_t& mant, int& q, bool& neg) {
-  uint64_t x = tile_load8(tile_w, a);
-  const uint32_t c0 = uint32_t(x & 0xFFu);
-  neg = c0 == '-';
-  const uint32_t skip = (c0 == '-' || c0 == '+') ? 1u : 0u;
-  const uint32_t n = L - skip;
-  if (n == 0 || n > 8) return false;
-  if (skip) x = (x >> 8) | (uint64_t(tile_load8(tile_w, a + 8) & 0xFFu) << 56);
+// The n (1..8) characters in the low bytes of x as digits[.digits] (at
+// most one dot, at least one digit): significand (< 10^8) and decimal
+// exponent (-7..0).
+__device__ __forceinline__ bool fast_float_x(uint64_t x, uint32_t n, uint64_t& mant, int& q) {
   const uint64_t keep = n >= 8 ? ~0ull : ((1ull << (8 * n)) - 1);
   const uint64_t z = (x ^ 0x2E2E2E2E2E2E2E2Eull) & keep;  // zero bytes at '.'
   const uint64_t dots = ~(((z & 0x7F7F7F7F7F7F7F7Full) + 0x7F7F7F7F7F7F7F7Full) | z |
@@ -467,14 +440,32 @@ struct CtxShared {
   Feed F;
   uint32_t tile_stv;
   uint32_t warp_stv[NW];
-  uint32_t wv[NW][12];       // per warp: V2 for the four start states
-  uint32_t agg[12];          // tile aggregates per start state
-  uint64_t wcnt[NW][4][4];   // per warp, per state: packed string counts
-  uint32_t rel[4][PP_MAX_COLS];
+  uint32_t wv[NW][4][3];      // per warp, per start state: (records, column, last) of the warp
+  uint32_t wpre[NW][4][3];    // per warp, per start state: the same over the earlier warps
+  uint64_t wcnt[NW][4][4];    // per warp, per start state: packed value bytes per string column
+  uint32_t rel[4][PP_MAX_COLS];  // per start state: value bytes of relative field k
   int8_t stridx[PP_MAX_COLS];
 };
 constexpr size_t CTX_SMEM = LUT_BYTES + 2 * TILE + sizeof(CtxShared);
+constexpr int CTX_HDR = 52;  // transition vector + (records, column, last) per start state
 
+// Reduction over the warp in lane order (lane 0 receives lanes 0..31).
+__device__ __forceinline__ V2 warp_reduce_v2(V2 v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const V2 o = {__shfl_down_sync(FULL, v.rec, d), __shfl_down_sync(FULL, v.col, d),
+                  __shfl_down_sync(FULL, v.last, d)};
+    if (lane + d < 32) v = op2_32(v, o);
+  }
+  return v;
+}
+
+// Per tile: the transition vector and, for each of the four live start
+// states, the record count, column offset and last terminator of the tile
+// (ParPaRaw Sections 3.1-3.2), plus the value bytes per string column of
+// the fields whose column the tile fixes, and per relative field of the
+// tile's first, partial record (its column is only known from the scan).
 template <int NS>
 __global__ void __launch_bounds__(NT, 2) ctx_kernel(const __grid_constant__ ParseParams P) {
   constexpr int NSW = NS > 0 ? (NS + 3) / 4 : 1;
@@ -498,10 +489,10 @@ __global__ void __launch_bounds__(NT, 2) ctx_kernel(const __grid_constant__ Pars
     const uint64_t tile_base = uint64_t(tile) * TILE;
     const uint32_t tile_len = uint32_t(min(uint64_t(TILE), P.n - tile_base));
     uint32_t w[8];
-    feed_tile(P, S.F, tile_s, tile_base, tile_len, w);
+    feed_tile(P, S.F, counter, aligned_in, lin0, tile_base, tile_len, w);
     const uint32_t cstart = uint32_t(t) * CB;
-    const uint8_t* own = tile_s + cstart;
     const uint32_t clen = tile_len > cstart ? min(tile_len - cstart, uint32_t(CB)) : 0u;
+    const uint8_t* own = tile_s + cstart;
     if (NS > 0)
       for (int k = t; k < 4 * PP_MAX_COLS; k += NT) (&S.rel[0][0])[k] = 0;
 
@@ -530,139 +521,132 @@ __global__ void __launch_bounds__(NT, 2) ctx_kernel(const __grid_constant__ Pars
       }
     }
 
-    // block scan of (rec, col, last) for each start state
-    V2 vi[4], ve[4];
+    // per start state: (records, column, last) scanned over the warp; a
+    // state whose chunks all start like an earlier state's in this warp
+    // shares its scan
+    V2 ex[4];
 #pragma unroll
-    for (int s = 0; s < 4; ++s) vi[s] = chunk_v2(g[s]);
+    for (int s = 0; s < 4; ++s) {
+      int same = -1;
 #pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
+      for (int q = 0; q < s; ++q)
+        if (same < 0 && __all_sync(FULL, st[q] == st[s])) same = q;
+      if (same >= 0) {
 #pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        const V2 o = shfl_up_v2(vi[s], d);
-        if (lane >= d) vi[s] = op2_32(o, vi[s]);
+        for (int q = 0; q < 4; ++q)
+          if (q == same) ex[s] = ex[q];
+      } else {
+        V2 v = chunk_v2(g[s]);
+        if (__all_sync(FULL, (v.rec | v.col | v.last) == 0)) {
+          ex[s] = {0u, 0u, 0u};
+        } else {
+#pragma unroll
+          for (int d = 1; d < 32; d <<= 1) {
+            const V2 o = shfl_up_v2(v, d);
+            if (lane >= d) v = op2_32(o, v);
+          }
+          ex[s] = v;  // inclusive for now
+        }
       }
     }
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
-      ve[s] = shfl_up_v2(vi[s], 1);
-      if (lane == 0) ve[s] = {0u, 0u, 0u};
-    }
-    if (lane == 31) {
-#pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        S.wv[warp][3 * s] = vi[s].rec; S.wv[warp][3 * s + 1] = vi[s].col; S.wv[warp][3 * s + 2] = vi[s].last;
-      }
+      if (lane == 31) { S.wv[warp][s][0] = ex[s].rec; S.wv[warp][s][1] = ex[s].col; S.wv[warp][s][2] = ex[s].last; }
+      V2 e = shfl_up_v2(ex[s], 1);
+      if (lane == 0) e = {0u, 0u, 0u};
+      ex[s] = e;  // exclusive within the warp
     }
     __syncthreads();
-    if (warp == 0) {
+    // warp s (s < 4): prefix over the warps for start state s, and the
+    // tile's totals for the record
+    uint32_t* rec = reinterpret_cast<uint32_t*>(P.s.ctx + size_t(tile) * P.s.ctx_stride);
+    if (warp < 4) {
+      const int s = warp;
+      V2 x = lane < NW ? V2{S.wv[lane][s][0], S.wv[lane][s][1], S.wv[lane][s][2]} : V2{0u, 0u, 0u};
 #pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        V2 x = lane < NW ? V2{S.wv[lane][3 * s], S.wv[lane][3 * s + 1], S.wv[lane][3 * s + 2]}
-                         : V2{0u, 0u, 0u};
-#pragma unroll
-        for (int d = 1; d < NW; d <<= 1) {
-          const V2 o = shfl_up_v2(x, d);
-          if (lane >= d) x = op2_32(o, x);
-        }
-        V2 xe = shfl_up_v2(x, 1);
-        if (lane == 0) xe = {0u, 0u, 0u};
-        __syncwarp();
-        if (lane < NW) { S.wv[lane][3 * s] = xe.rec; S.wv[lane][3 * s + 1] = xe.col; S.wv[lane][3 * s + 2] = xe.last; }
-        if (lane == NW - 1) { S.agg[3 * s] = x.rec; S.agg[3 * s + 1] = x.col; S.agg[3 * s + 2] = x.last; }
+      for (int d = 1; d < NW; d <<= 1) {
+        const V2 o = shfl_up_v2(x, d);
+        if (lane >= d) x = op2_32(o, x);
       }
+      V2 xe = shfl_up_v2(x, 1);
+      if (lane == 0) xe = {0u, 0u, 0u};
+      if (lane < NW) { S.wpre[lane][s][0] = xe.rec; S.wpre[lane][s][1] = xe.col; S.wpre[lane][s][2] = xe.last; }
+      if (lane == NW - 1) { rec[1 + 3 * s] = x.rec; rec[2 + 3 * s] = x.col; rec[3 + 3 * s] = x.last; }
+      if (s == 0 && lane == 0) rec[0] = S.tile_stv;
     }
-    __syncthreads();
-
-    // value bytes per string column: absolute columns, or relative fields
-    // of the tile's first (partial) record
-    uint64_t cnt[4][NSW];
-#pragma unroll
-    for (int s = 0; s < 4; ++s)
-#pragma unroll
-      for (int k = 0; k < NSW; ++k) cnt[s][k] = 0;
     if (NS > 0) {
-      uint32_t s_k0[4], s_n0[4];
+      __syncthreads();
+      // value bytes per string column, per start state
+      uint32_t col0[4];
 #pragma unroll
       for (int s = 0; s < 4; ++s) {
-        const V2 pre = op2_32(V2{S.wv[warp][3 * s], S.wv[warp][3 * s + 1], S.wv[warp][3 * s + 2]}, ve[s]);
+        const V2 pre = op2_32(V2{S.wpre[warp][s][0], S.wpre[warp][s][1], S.wpre[warp][s][2]}, ex[s]);
+        col0[s] = pre.col;  // ABS32 | column, or a relative field index
+      }
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
         int same = -1;
 #pragma unroll
-        for (int q = 0; q < s; ++q) {
-          const V2 pq = op2_32(V2{S.wv[warp][3 * q], S.wv[warp][3 * q + 1], S.wv[warp][3 * q + 2]}, ve[q]);
-          if (same < 0 && st[q] == st[s] && (pq.col & ABS32) && pq.col == pre.col) same = q;
-        }
-        if (same >= 0) {
+        for (int q = 0; q < s; ++q)
+          if (same < 0 && __all_sync(FULL, st[q] == st[s] && ((col0[q] & ABS32) != 0) && col0[q] == col0[s]))
+            same = q;
+        uint64_t cnt[NSW];
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            if (q == same)
-#pragma unroll
-              for (int k = 0; k < NSW; ++k) cnt[s][k] = cnt[q][k];
-          s_k0[s] = 0xFFFFFFFFu;
-          s_n0[s] = 0;
-          continue;
-        }
+        for (int k = 0; k < NSW; ++k) cnt[k] = 0;
         const Tags& gs = g[s];
         const uint32_t valid = range_mask(0, min(clen, gs.inv_at));
         const uint32_t data = valid & ~(gs.fd | gs.rd | gs.ctrl);
-        bool abs = (pre.col & ABS32) != 0;
-        uint32_t col = pre.col & ~ABS32, term = gs.fd | gs.rd, start = 0;
-        uint32_t k0 = 0xFFFFFFFFu, n0 = 0;  // first relative segment, summed per warp below
-        for (;;) {
-          const uint32_t j = term ? uint32_t(__ffs(term) - 1) : 32u;
-          const uint32_t n = __popc(data & range_mask(start, j));
-          if (n && col < n_cols) {
-            if (abs) {
-              const int si = S.stridx[col];
-              if (si >= 0) add16(cnt[s], si, n);
-            } else if (start == 0) {
-              k0 = col;
-              n0 = n;
-            } else {
-              atomicAdd(&S.rel[s][col], n);
+        bool abs = (col0[s] & ABS32) != 0;
+        uint32_t col = col0[s] & ~ABS32, term = gs.fd | gs.rd, seg0 = 0;
+        uint32_t k0 = 0xFFFFFFFFu, n0 = 0;  // the first relative segment, summed per warp below
+        if (st[s] < 4 && same < 0) {  // (a shared state's fields are all absolute)
+          for (;;) {
+            const uint32_t j = term ? uint32_t(__ffs(term) - 1) : 32u;
+            const uint32_t n = __popc(data & range_mask(seg0, j));
+            if (n && col < n_cols) {
+              if (abs) {
+                const int si = S.stridx[col];
+                if (si >= 0) add16(cnt, si, n);
+              } else if (seg0 == 0) {
+                k0 = col;
+                n0 = n;
+              } else {
+                atomicAdd(&S.rel[s][col], n);
+              }
             }
+            if (j == 32) break;
+            if ((gs.rd >> j) & 1u) { abs = true; col = 0; }
+            else col = col < 0x7FFFFF00u ? col + 1 : col;
+            seg0 = j + 1;
+            term &= term - 1;
           }
-          if (j == 32) break;
-          if ((gs.rd >> j) & 1u) { abs = true; col = 0; }
-          else col = col < 0x7FFFFF00u ? col + 1 : col;
-          start = j + 1;
-          term &= term - 1;
         }
-        s_k0[s] = k0;
-        s_n0[s] = n0;
-      }
-      // relative first segments: one shared atomic per (warp, field index)
+        // relative first segments: one shared atomic per (warp, field index)
+        const uint32_t grp = __match_any_sync(FULL, k0);
+        const uint32_t sum = __reduce_add_sync(grp, n0);
+        if (k0 != 0xFFFFFFFFu && (grp & ((1u << lane) - 1)) == 0 && sum) atomicAdd(&S.rel[s][k0], sum);
+        // warp sums of the packed counters
+        if (same < 0) {
 #pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        const uint32_t grp = __match_any_sync(FULL, s_k0[s]);
-        const uint32_t sum = __reduce_add_sync(grp, s_n0[s]);
-        if (s_k0[s] != 0xFFFFFFFFu && (grp & ((1u << lane) - 1)) == 0 && sum)
-          atomicAdd(&S.rel[s][s_k0[s]], sum);
-      }
-      // block sums of the packed counters
+          for (int k = 0; k < NSW; ++k) {
+            uint64_t v = cnt[k];
 #pragma unroll
-      for (int s = 0; s < 4; ++s)
+            for (int d = 16; d; d >>= 1) v += __shfl_xor_sync(FULL, v, d);
+            if (lane == 0) S.wcnt[warp][s][k] = v;
+          }
+        } else if (lane == 0) {
 #pragma unroll
-        for (int k = 0; k < NSW; ++k) {
-          uint64_t v = cnt[s][k];
-#pragma unroll
-          for (int d = 16; d; d >>= 1) v += __shfl_xor_sync(FULL, v, d);
-          if (lane == 0) S.wcnt[warp][s][k] = v;
+          for (int k = 0; k < NSW; ++k) S.wcnt[warp][s][k] = S.wcnt[warp][same][k];
         }
-    }
-    __syncthreads();
-
-    // write the tile's context record
-    uint8_t* rec = P.s.ctx + size_t(tile) * P.s.ctx_stride;
-    if (t < 13) {
-      const uint32_t v = t == 0 ? S.tile_stv : S.agg[t - 1];
-      reinterpret_cast<uint32_t*>(rec)[t] = v;
-    }
-    if (NS > 0) {
-      uint16_t* cabs = reinterpret_cast<uint16_t*>(rec + CTX_HDR);
+      }
+      __syncthreads();
+      // the record's chars part, one word per thread
+      uint16_t* cabs = reinterpret_cast<uint16_t*>(rec) + CTX_HDR / 2;
       uint16_t* crel = cabs + 4 * P.n_str;
       if (t < 4 * P.n_str) {
         const int s = t / P.n_str, si = t - s * P.n_str;
         uint64_t sum = 0;
+#pragma unroll 4
         for (int q = 0; q < NW; ++q) sum += S.wcnt[q][s][si >> 2];
         cabs[t] = uint16_t((sum >> (16 * (si & 3))) & 0xFFFFu);
       }
@@ -671,7 +655,7 @@ __global__ void __launch_bounds__(NT, 2) ctx_kernel(const __grid_constant__ Pars
         crel[k] = uint16_t(S.rel[s][c]);
       }
     }
-    feed_next(P, S.F, counter, aligned_in, lin0);  // the tile was last read before the barrier above
+    feed_next(P, S.F, counter, aligned_in, lin0);  // the tile was last read before a barrier above
   }
   feed_finish(S.F);
 }
@@ -765,6 +749,8 @@ __device__ __forceinline__ SAgg sagg_of_tile(const uint8_t* rec, uint64_t tile_b
   return a;
 }
 
+// Per tile, written by the scan: the tile's context, followed by the
+// chars offset of the tile per string column (uint64 each).
 struct PreHdr {
   uint64_t rec0;     // record index at the tile start
   uint64_t last1;    // global position + 1 of the last terminator before the tile, 0 none
@@ -782,6 +768,10 @@ struct ScanShared {
   int8_t stridx[PP_MAX_COLS];
 };
 
+// Exclusive scan over tiles of the per-start-state aggregates; every tile
+// learns its true start state, record index, column and last terminator,
+// then, from those, its value bytes per string column, whose exclusive
+// scan gives the tile's chars offsets.
 template <int NS>
 __global__ void __launch_bounds__(SCAN_NT) scan_kernel(const __grid_constant__ ParseParams P) {
   constexpr int SW = SCAN_NT / 32;
@@ -794,9 +784,7 @@ __global__ void __launch_bounds__(SCAN_NT) scan_kernel(const __grid_constant__ P
   const uint32_t blk = S.block;
   const LookbackCfg cfg{P.st, P.spin_limit};
   const uint32_t t0 = blk * SCAN_TILES + uint32_t(t) * SCAN_TPT;
-  const uint32_t n_cols = uint32_t(P.n_cols);
 
-  // (A) per-start-state scan of (transition vector, records, column, last terminator)
   SAgg mine = sagg_identity(false);
   for (int i = 0; i < SCAN_TPT; ++i) {
     const uint32_t tile = t0 + i;
@@ -867,9 +855,7 @@ __global__ void __launch_bounds__(SCAN_NT) scan_kernel(const __grid_constant__ P
       col = blockpre.col[q] & ~ABS32;
       lst = blockpre.lst[q];
     }
-
-  // walk this thread's tiles with the true context; per tile, its value
-  // bytes per string column follow from its start state and column
+  const uint32_t n_cols = uint32_t(P.n_cols);
   uint64_t sum[K3];
 #pragma unroll
   for (int k = 0; k < K3; ++k) sum[k] = 0;
@@ -885,7 +871,7 @@ __global__ void __launch_bounds__(SCAN_NT) scan_kernel(const __grid_constant__ P
     h.state = s | (lst << 8);
     *reinterpret_cast<PreHdr*>(pr) = h;
     const uint32_t* hd = reinterpret_cast<const uint32_t*>(cr);
-    if (NS > 0) {
+    if (NS > 0) {  // the tile's value bytes per string column at its true context
       uint64_t* cb = reinterpret_cast<uint64_t*>(pr + PRE_HDR);
       const uint16_t* cabs = reinterpret_cast<const uint16_t*>(cr + CTX_HDR);
       const uint16_t* crel = cabs + 4 * P.n_str;
@@ -922,7 +908,7 @@ __global__ void __launch_bounds__(SCAN_NT) scan_kernel(const __grid_constant__ P
     }
   }
 
-  // (C) chars offsets: exclusive sum over tiles per string column
+  // chars offsets: exclusive sum over tiles per string column
   if (NS > 0) {
     uint64_t ci[K3];
 #pragma unroll
@@ -940,7 +926,7 @@ __global__ void __launch_bounds__(SCAN_NT) scan_kernel(const __grid_constant__ P
       for (int k = 0; k < K3; ++k) S.wsum[warp][k] = ci[k];
     __syncthreads();
     if (warp == 0) {
-      uint64_t v[K3], x[K3], agg[K3], zero[K3], ex[K3];
+      uint64_t v[K3], x[K3], agg[K3], zero[K3], exc[K3];
 #pragma unroll
       for (int k = 0; k < K3; ++k) { v[k] = lane < SW ? S.wsum[lane][k] : 0ull; x[k] = v[k]; zero[k] = 0; }
 #pragma unroll
@@ -957,10 +943,10 @@ __global__ void __launch_bounds__(SCAN_NT) scan_kernel(const __grid_constant__ P
         if (lane < SW) S.wsum[lane][k] = x[k] - v[k];
       }
       lookback_vec<K3>(P.s.scan_flag_c, P.s.scan_agg_c, P.s.scan_inc_c, blk, agg, zero, zero,
-                       AddOp<K3>{}, cfg, ex);
+                       AddOp<K3>{}, cfg, exc);
       if (lane == 0)
 #pragma unroll
-        for (int k = 0; k < K3; ++k) S.base[k] = ex[k];
+        for (int k = 0; k < K3; ++k) S.base[k] = exc[k];
     }
     __syncthreads();
     uint64_t run[K3];
@@ -981,62 +967,107 @@ __global__ void __launch_bounds__(SCAN_NT) scan_kernel(const __grid_constant__ P
   }
 }
 
+// Numeric field whose bytes are not all in the tile, contain control bytes
+// or need the full grammar: streaming accumulators over the value bytes.
+// Returns the error bits; *out receives the value (0 for an empty field).
+__device__ __noinline__ int convert_general(const ParseParams& P, uint32_t ty, uint64_t fs,
+                                            uint64_t fe, uint64_t tile_base,
+                                            const uint8_t* tile_s, const uint32_t* ctrl_s,
+                                            const uint32_t* my_lut, uint32_t fstate,
+                                            uint64_t* out) {
+  int err = 0;
+  uint64_t val = 0;
+  if (ty == PP_COL_FLOAT64) {
+    ppn::FloatAcc acc;
+    const uint32_t nd = feed_field(acc, P.in, fs, fe, tile_base, tile_s, ctrl_s, my_lut, fstate);
+    if (nd) err = acc.finish(&val);
+  } else {
+    ppn::IntAcc acc;
+    const uint32_t nd = feed_field(acc, P.in, fs, fe, tile_base, tile_s, ctrl_s, my_lut, fstate);
+    if (nd) {
+      int64_t x = 0;
+      if (ty == PP_COL_INT8) err = acc.finish(128ull, 127ull, &x);
+      else if (ty == PP_COL_INT32) err = acc.finish(2147483648ull, 2147483647ull, &x);
+      else err = acc.finish(9223372036854775808ull, 9223372036854775807ull, &x);
+      val = uint64_t(x);
+    }
+  }
+  *out = val;
+  return err;
+}
+
 // Convert the numeric field in slot value v (tile-relative start << 16 |
-// end; start 0xFFFF = the field began in an earlier tile) and store it at
-// row `rec` of column c of type ty; reports syntax / range errors.
-__device__ __forceinline__ void convert_slot(const ParseParams& P, uint32_t c, uint32_t ty,
-                                             uint32_t v, uint64_t rec, uint64_t tile_base,
-                                             uint64_t tile_fstart, uint32_t tile_fstate,
-                                             const uint8_t* tile_s, const uint32_t* tile_w,
-                                             const uint32_t* ctrl_s, const uint32_t* my_lut) {
+// end; start 0xFFFF = the field began in an earlier tile; SLOT_DEFAULT = a
+// missing field) and store it at row `rec` of column c of type ty.
+// Plain fields inside the tile take word-parallel fast paths: an integer
+// of at most 16 digits, or a decimal of at most 8 characters after the
+// sign converted by short_decimal_to_binary64; everything else streams
+// through the accumulators.
+__device__ __forceinline__ void convert_num(const ParseParams& P, uint32_t c, uint32_t ty,
+                                            uint32_t v, uint64_t rec, uint64_t tile_base,
+                                            uint64_t tile_fstart, uint32_t tile_fstate,
+                                            const uint8_t* tile_s, const uint32_t* tile_w,
+                                            const uint32_t* ctrl_s, const uint16_t* cpre,
+                                            const uint32_t* my_lut, bool any_ctrl) {
   uint64_t val = 0;
   int err = 0;
   uint64_t fs = 0;
   if (v != SLOT_DEFAULT) {
-    const uint32_t fsr = v >> 16;
-    const uint64_t fe = tile_base + (v & 0xFFFFu);
+    const uint32_t fsr = v >> 16, fe = v & 0xFFFFu;
     fs = fsr == 0xFFFFu ? tile_fstart : tile_base + fsr;
-    const uint32_t fl = (v & 0xFFFFu) - fsr;
     bool done = false;
-    if (fsr != 0xFFFFu && fl > 0 && popc_range(ctrl_s, fsr, fsr + fl) == 0) {
-      bool neg;
-      if (ty == PP_COL_FLOAT64) {
-        uint64_t mant;
-        int q;
-        if (fast_float(tile_w, fsr, fl, mant, q, neg)) {
-          val = (mant ? ppn::decimal_to_binary64(mant, q) : 0ull) | (neg ? (1ull << 63) : 0ull);
-          done = true;
-        }
+    if (fsr != 0xFFFFu && (!any_ctrl || ctrl_before(ctrl_s, cpre, fe) == ctrl_before(ctrl_s, cpre, fsr))) {
+      const uint32_t L = fe - fsr;
+      if (L == 0) {
+        done = true;  // empty field: the column default
       } else {
-        uint64_t mag;
-        if (fast_int(tile_w, fsr, fl, mag, neg)) {
-          const uint64_t lim = ty == PP_COL_INT8 ? (neg ? 128ull : 127ull)
-                             : ty == PP_COL_INT32 ? (neg ? 2147483648ull : 2147483647ull)
-                             : (neg ? 9223372036854775808ull : 9223372036854775807ull);
-          if (mag > lim) err = PP_ERR_NUM_OVERFLOW;
-          else val = neg ? (~mag + 1) : mag;
-          done = true;
+        uint64_t x = tile_load8(tile_w, fsr);
+        const uint32_t c0 = uint32_t(x) & 0xFFu;
+        const bool neg = c0 == '-';
+        const uint32_t sg = (c0 == '-' || c0 == '+') ? 1u : 0u;
+        const uint32_t n = L - sg;
+        if (sg) x = (x >> 8) | (uint64_t(tile_s[fsr + 8]) << 56);
+        if (ty == PP_COL_FLOAT64) {
+          uint64_t mant;
+          int q;
+          if (n >= 1 && n <= 8 && fast_float_x(x, n, mant, q)) {
+            val = (mant ? ppn::short_decimal_to_binary64(uint32_t(mant), q) : 0ull) |
+                  (neg ? (1ull << 63) : 0ull);
+            done = true;
+          }
+        } else {
+          uint64_t mag = 0;
+          bool ok = false;
+          if (n == 1) {
+            mag = (uint32_t(x) & 0xFFu) - 48u;
+            ok = mag <= 9;
+          } else if (n >= 2 && n <= 8) {
+            uint64_t d;
+            ok = swar_digits(x, n, d);
+            if (ok) mag = swar_value(d);
+          } else if (n > 8 && n <= 16) {
+            uint64_t d, d2;
+            ok = swar_digits(x, 8, d) && swar_digits(tile_load8(tile_w, fsr + sg + 8), n - 8, d2);
+            if (ok) {
+              uint64_t p10 = 1;
+              for (uint32_t i = 8; i < n; ++i) p10 *= 10;
+              mag = swar_value(d) * p10 + swar_value(d2);
+            }
+          }
+          if (ok) {
+            const uint64_t lim = ty == PP_COL_INT8 ? (neg ? 128ull : 127ull)
+                               : ty == PP_COL_INT32 ? (neg ? 2147483648ull : 2147483647ull)
+                               : (neg ? 9223372036854775808ull : 9223372036854775807ull);
+            if (mag > lim) err = PP_ERR_NUM_OVERFLOW;
+            else val = neg ? (~mag + 1) : mag;
+            done = true;
+          }
         }
       }
     }
-    if (done) {
-    } else if (ty == PP_COL_FLOAT64) {
-      ppn::FloatAcc acc;
-      const uint32_t nd = feed_field(acc, P.in, fs, fe, tile_base, tile_s, ctrl_s, my_lut,
-                                     tile_fstate);
-      if (nd) err = acc.finish(&val);
-    } else {
-      ppn::IntAcc acc;
-      const uint32_t nd = feed_field(acc, P.in, fs, fe, tile_base, tile_s, ctrl_s, my_lut,
-                                     tile_fstate);
-      if (nd) {
-        int64_t x = 0;
-        if (ty == PP_COL_INT8) err = acc.finish(128ull, 127ull, &x);
-        else if (ty == PP_COL_INT32) err = acc.finish(2147483648ull, 2147483647ull, &x);
-        else err = acc.finish(9223372036854775808ull, 9223372036854775807ull, &x);
-        val = uint64_t(x);
-      }
-    }
+    if (!done)
+      err = convert_general(P, ty, fs, tile_base + fe, tile_base, tile_s, ctrl_s, my_lut,
+                            tile_fstate, &val);
   }
   if (ty == PP_COL_FLOAT64) static_cast<uint64_t*>(P.typed[c])[rec] = val;
   else if (ty == PP_COL_INT8) static_cast<int8_t*>(P.typed[c])[rec] = int8_t(val);
@@ -1046,60 +1077,62 @@ __device__ __forceinline__ void convert_slot(const ParseParams& P, uint32_t c, u
 }
 
 // ================================================================ 3. main
+constexpr uint32_t SHORT_FIELD = 32;  // longer string fields are staged chunk-parallel
+constexpr uint16_t NO_FIELD = 0xFFFFu;
+
 struct MainShared {
   Feed F;
   uint32_t tile_stv;
-  uint32_t rows;             // records touched by the tile (#RD + 1)
   uint32_t warp_stv[NW];
   uint32_t warp_rec[NW], warp_col[NW], warp_last[NW];
-  uint64_t wcnt[NW][4];
-  uint64_t base[ppi::MAX_STR_COLS];
-  uint32_t total[ppi::MAX_STR_COLS];
-  uint32_t R[ppi::MAX_STR_COLS];
-  int8_t stridx[PP_MAX_COLS];
+  uint32_t rows;             // records touched by the tile (#RD + 1)
+  uint32_t col_end;          // fields of the last row closed in the tile
+  uint32_t item;             // next numeric work item
+  uint32_t wsum[NW];
+  uint32_t cstart[ppi::MAX_STR_COLS + 1];  // staging start per string column (this pass)
+  uint32_t carry[ppi::MAX_STR_COLS];       // chars of earlier passes per string column
+  uint64_t base[ppi::MAX_STR_COLS];        // chars offset of the tile per string column
   uint8_t coltype[PP_MAX_COLS];
-  uint8_t outcol[PP_MAX_COLS];  // columns that produce output, in order
-  uint8_t numcol[PP_MAX_COLS];  // numeric output columns, in order
-  uint32_t n_out, n_num;
-  uint32_t wnt[NW];          // per warp: terminators (then exclusive prefix)
-  uint32_t nterm;            // terminators in the tile
-  uint32_t wrd[NW], crd[NW]; // per warp range: record delimiters, carry in
-  int32_t wlast[NW], clast[NW], lastrd;
-  uint32_t cstart[ppi::MAX_STR_COLS + 1];
+  uint8_t numcol[PP_MAX_COLS];             // numeric output columns, in order
+  uint32_t n_num;
+  uint16_t cpre[NT + 1];     // control bytes before chunk t (exclusive scan)
+  uint16_t lk[2][NT];        // long string field (item) continuing in / starting in chunk t
 };
-constexpr int LIST_CAP = 4096;         // terminators per tile on the field-list path
 constexpr size_t MAIN_SMEM = LUT_BYTES + 2 * TILE + STAGE_BYTES + SLOT_CAP * 4 + NT * 4 +
-                             LIST_CAP * 2 + sizeof(MainShared);
+                             SLOT_CAP * 2 + sizeof(MainShared);
+
+
+// floor(x / d) for x * d < 2^32 (the magic number is ceil(2^32 / d))
+__device__ __forceinline__ uint32_t div_magic(uint32_t d) { return 0xFFFFFFFFu / d + 1u; }
+__device__ __forceinline__ uint32_t div_by(uint32_t x, uint32_t d, uint32_t magic) {
+  return d == 1 ? x : __umulhi(x, magic);
+}
 
 template <int NS>
 __global__ void __launch_bounds__(NT, 2) main_kernel(const __grid_constant__ ParseParams P) {
-  constexpr int NSW = NS > 0 ? (NS + 3) / 4 : 1;
   extern __shared__ __align__(128) uint8_t smem[];
   uint32_t* lut_s = reinterpret_cast<uint32_t*>(smem);
-  uint8_t* lin0 = smem + LUT_BYTES;             // two tile buffers
+  uint8_t* lin0 = smem + LUT_BYTES;  // two tile buffers
   uint8_t* stage_s = lin0 + 2 * TILE;
   uint32_t* slot_s = reinterpret_cast<uint32_t*>(stage_s + STAGE_BYTES);
   uint32_t* ctrl_s = slot_s + SLOT_CAP;
-  uint16_t* list_s = reinterpret_cast<uint16_t*>(ctrl_s + NT);  // field list, then chars ends
-  MainShared& S = *reinterpret_cast<MainShared*>(list_s + LIST_CAP);
+  uint16_t* pos_s = reinterpret_cast<uint16_t*>(ctrl_s + NT);  // chars end per string field
+  MainShared& S = *reinterpret_cast<MainShared*>(pos_s + SLOT_CAP);
 
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   load_lut(P, lut_s);
-  for (int k = t; k < PP_MAX_COLS; k += NT) {
-    S.stridx[k] = P.stridx[k];
-    S.coltype[k] = P.coltype[k];
-  }
+  for (int k = t; k < PP_MAX_COLS; k += NT) S.coltype[k] = P.coltype[k];
   if (t == 0) {
-    uint32_t k = 0, m = 0;
-    for (uint32_t c = 0; c < uint32_t(P.n_cols); ++c) {
-      if (P.coltype[c] != PP_COL_SKIP) S.outcol[k++] = uint8_t(c);
+    uint32_t m = 0;
+    for (uint32_t c = 0; c < uint32_t(P.n_cols); ++c)
       if (P.coltype[c] != PP_COL_SKIP && P.coltype[c] != PP_COL_STRING) S.numcol[m++] = uint8_t(c);
-    }
-    S.n_out = k;
-    S.n_num = m;
+    S.n_num = P.has_out ? m : 0u;
+    S.item = 0;
   }
+  for (int k = t; k < ppi::MAX_STR_COLS; k += NT) S.carry[k] = 0;
   const uint32_t* my_lut = lut_s + lane;
   const uint32_t n_cols = uint32_t(P.n_cols);
+  const uint32_t n_str = NS > 0 ? uint32_t(P.n_str) : 0u;
   const bool aligned_in = (reinterpret_cast<uintptr_t>(P.in) & 15) == 0;
   uint32_t* counter = &P.s.counters[1];
   feed_start(P, S.F, counter, aligned_in, lin0);
@@ -1114,25 +1147,24 @@ __global__ void __launch_bounds__(NT, 2) main_kernel(const __grid_constant__ Par
     const bool last_tile = tile + 1 == P.n_tiles;
     const uint8_t* pr = P.s.pre + size_t(tile) * P.s.pre_stride;
     const PreHdr ph = *reinterpret_cast<const PreHdr*>(pr);
+    if (NS > 0 && t < int(n_str)) S.base[t] = reinterpret_cast<const uint64_t*>(pr + PRE_HDR)[t];
     uint32_t w[8];
-    feed_tile(P, S.F, tile_s, tile_base, tile_len, w);
+    feed_tile(P, S.F, counter, aligned_in, lin0, tile_base, tile_len, w);
     const uint32_t cstart = uint32_t(t) * CB;
     const uint32_t clen = tile_len > cstart ? min(tile_len - cstart, uint32_t(CB)) : 0u;
     const uint8_t* own = tile_s + cstart;
 
-    // ---- context resolution: the tile's start state is known from the scan
+    // ---- the chunk's start state (the tile's is known from the scan)
     uint32_t G, special, special_x;
     stv_pass(w, clen, tile_s, cstart, my_lut, G, special, special_x);
     const uint32_t lane_ex = block_stv(G, S.warp_stv, &S.tile_stv);
     const uint32_t s_tile = ph.state & 0xFFu;
     const uint32_t s_chunk = stv_apply(lane_ex, stv_apply(S.warp_stv[warp], s_tile));
 
-    // ---- tagging
+    // ---- tags
     const Tags g = tag_chunk(s_chunk, special, special_x, P.sticky, clen, cstart, own, my_lut,
                              P.bg_next);
     const uint32_t fd = g.fd, rd = g.rd;
-    const uint32_t valid = range_mask(0, min(clen, g.inv_at));
-    const uint32_t data = valid & ~(fd | rd | g.ctrl);
     ctrl_s[t] = g.ctrl;
     if (g.inv_at < clen && s_chunk != 4)
       report(P.st, PP_ERR_INVALID_INPUT, tile_base + cstart + g.inv_at, true);
@@ -1142,7 +1174,7 @@ __global__ void __launch_bounds__(NT, 2) main_kernel(const __grid_constant__ Par
     const bool virt_rd = owns_end && g.end != 4 && ((P.accept_mask >> g.end) & 1u) &&
                          !((rd >> (clen - 1)) & 1u);
 
-    // ---- record and column indices across the block (tile prefix from the scan)
+    // ---- record, column and field start at the chunk start (block scan)
     V2 vi = chunk_v2(g);
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
@@ -1152,7 +1184,7 @@ __global__ void __launch_bounds__(NT, 2) main_kernel(const __grid_constant__ Par
     V2 lex = shfl_up_v2(vi, 1);
     if (lane == 0) lex = {0u, 0u, 0u};
     if (lane == 31) { S.warp_rec[warp] = vi.rec; S.warp_col[warp] = vi.col; S.warp_last[warp] = vi.last; }
-    __syncthreads();
+    const bool any_ctrl = __syncthreads_or(g.ctrl != 0) != 0;
     if (warp == 0) {
       V2 x = lane < NW ? V2{S.warp_rec[lane], S.warp_col[lane], S.warp_last[lane]} : V2{0u, 0u, 0u};
 #pragma unroll
@@ -1164,38 +1196,49 @@ __global__ void __launch_bounds__(NT, 2) main_kernel(const __grid_constant__ Par
       if (lane == 0) xe = {0u, 0u, 0u};
       __syncwarp();
       if (lane < NW) { S.warp_rec[lane] = xe.rec; S.warp_col[lane] = xe.col; S.warp_last[lane] = xe.last; }
-      if (lane == NW - 1) S.rows = x.rec + 1;
+      if (lane == NW - 1) {
+        S.rows = x.rec + 1;
+        if (x.col & ABS32) {
+          S.col_end = x.col & ~ABS32;
+        } else {
+          const uint64_t c = uint64_t(ph.col_in) + x.col;
+          S.col_end = c > 0x7FFFFF00ull ? 0x7FFFFF00u : uint32_t(c);
+        }
+      }
     }
-    __syncthreads();
+    const bool any_virt = __syncthreads_or(virt_rd) != 0;
     const V2 pre = op2_32(V2{S.warp_rec[warp], S.warp_col[warp], S.warp_last[warp]}, lex);
-    const uint64_t tile_rec0 = ph.rec0;
-    const uint64_t rec0 = tile_rec0 + pre.rec;
+    const uint64_t rec0 = ph.rec0;
+    const uint32_t rows = S.rows;
+    const uint32_t col_in = ph.col_in;
+    const uint32_t col_end = any_virt ? n_cols : S.col_end;
     uint32_t col0;
     if (pre.col & ABS32) {
       col0 = pre.col & ~ABS32;
     } else {
-      const uint64_t c = uint64_t(ph.col_in) + pre.col;
+      const uint64_t c = uint64_t(col_in) + pre.col;
       col0 = c > 0x7FFFFF00ull ? 0x7FFFFF00u : uint32_t(c);
     }
-    const uint64_t fstart0 = pre.last ? tile_base + (pre.last >> 8) : ph.last1;
-    // start (global) and DFA state of the field holding tile byte 0
+    // the field open at the tile start: global start and DFA state there
     const uint64_t tile_fstart = ph.last1;
     const uint32_t tile_fstate = ph.last1 ? (ph.state >> 8) & 0xFFu : uint32_t(P.start_state);
-
-    // ---- terminators of the tile (field ends): count and block scan
-    const uint32_t term_mask = fd | rd;
-    {
-      const uint32_t nt = __popc(term_mask) + (virt_rd ? 1u : 0u);
-      uint32_t ti = nt;
+    const uint32_t fs_tile = tile_fstart >= tile_base ? uint32_t(tile_fstart - tile_base) : 0xFFFFu;
+    const uint32_t fs0 = pre.last ? (pre.last >> 8) : fs_tile;  // field open at the chunk start
+    const uint32_t rl0 = pre.rec;
+    const uint32_t term_all = fd | rd;
+    const bool owns_tail = clen > 0 && cstart + clen == tile_len;
+    if (any_ctrl) {  // control bytes before each chunk: O(1) value-byte counts
+      const uint32_t nc = __popc(g.ctrl);
+      uint32_t xi = nc;
 #pragma unroll
       for (int d = 1; d < 32; d <<= 1) {
-        const uint32_t o = __shfl_up_sync(FULL, ti, d);
-        if (lane >= d) ti += o;
+        const uint32_t o = __shfl_up_sync(FULL, xi, d);
+        if (lane >= d) xi += o;
       }
-      if (lane == 31) S.wnt[warp] = ti;
+      if (lane == 31) S.wsum[warp] = xi;
       __syncthreads();
       if (warp == 0) {
-        const uint32_t v = lane < NW ? S.wnt[lane] : 0u;
+        const uint32_t v = lane < NW ? S.wsum[lane] : 0u;
         uint32_t x = v;
 #pragma unroll
         for (int d = 1; d < NW; d <<= 1) {
@@ -1203,433 +1246,255 @@ __global__ void __launch_bounds__(NT, 2) main_kernel(const __grid_constant__ Par
           if (lane >= d) x += o;
         }
         __syncwarp();
-        if (lane < NW) S.wnt[lane] = x - v;
-        if (lane == NW - 1) S.nterm = x;
+        if (lane < NW) S.wsum[lane] = x - v;
+        if (lane == NW - 1) S.cpre[NT] = uint16_t(x);
       }
       __syncthreads();
-      if (S.nterm <= LIST_CAP && n_cols * S.rows <= SLOT_CAP) {
-        uint32_t i = S.wnt[warp] + ti - nt;
-        uint32_t m = term_mask;
-        while (m) {
-          const uint32_t j = __ffs(m) - 1;
-          m &= m - 1;
-          list_s[i++] = uint16_t((cstart + j) | (((rd >> j) & 1u) << 15));
-        }
-        if (virt_rd) list_s[i] = uint16_t(tile_len | 0x8000u);
-      }
-      __syncthreads();  // the list is read across warps below
+      S.cpre[t] = uint16_t(S.wsum[warp] + xi - nc);
     }
-    const uint32_t T = S.nterm;
-    const uint32_t rows = S.rows;
-    uint64_t rec_end = rec0;
-    if (T <= LIST_CAP && n_cols * rows <= SLOT_CAP) {
-      // ======== field-list path: one lane per field, warp ranges with carries
-      for (uint32_t k = t; k < n_cols * rows; k += NT) slot_s[k] = SLOT_ABSENT;
-      const uint32_t R = (((T + NW - 1) / NW) + 31u) & ~31u;
-      const uint32_t r0 = min(T, uint32_t(warp) * R), r1 = min(T, r0 + R);
-      {
-        uint32_t nrd = 0;
-        int32_t last = -1;
-        for (uint32_t g0 = r0; g0 < r1; g0 += 32) {
-          const uint32_t f = g0 + lane;
-          const uint32_t b = __ballot_sync(FULL, f < r1 && (list_s[f] >> 15));
-          nrd += __popc(b);
-          if (b) last = int32_t(g0 + 31 - __clz(b));
-        }
-        if (lane == 0) { S.wrd[warp] = nrd; S.wlast[warp] = last; }
-      }
-      __syncthreads();
-      if (t == 0) {
-        uint32_t cnt = 0;
-        int32_t lst = -1;
-        for (int q = 0; q < NW; ++q) {
-          S.crd[q] = cnt;
-          S.clast[q] = lst;
-          cnt += S.wrd[q];
-          if (S.wlast[q] >= 0) lst = S.wlast[q];
-        }
-        S.lastrd = lst;
-      }
-      __syncthreads();
-      const uint32_t first_in = tile_fstart >= tile_base ? 0u : 0xFFFFu;  // start of field 0
-      {
-        uint32_t crd = S.crd[warp];
-        int32_t clast = S.clast[warp];
-        const uint32_t lt = (1u << lane) - 1u;
-        for (uint32_t g0 = r0; g0 < r1; g0 += 32) {
-          const uint32_t f = g0 + lane;
-          const bool ok = f < r1;
-          const uint32_t e = ok ? uint32_t(list_s[f]) : 0u;
-          const bool isrd = ok && (e >> 15);
-          const uint32_t b = __ballot_sync(FULL, isrd);
-          if (ok) {
-            const uint32_t below = b & lt;
-            const uint32_t rl = crd + __popc(below);
-            const int32_t lr = below ? int32_t(g0 + 31 - __clz(below)) : clast;
-            uint32_t col;
-            if (lr >= 0) {
-              col = f - uint32_t(lr) - 1u;
-            } else {
-              const uint64_t cc = uint64_t(ph.col_in) + f;
-              col = cc > 0x7FFFFF00ull ? 0x7FFFFF00u : uint32_t(cc);
-            }
-            const uint32_t pos = e & 0x7FFFu;
-            const uint32_t s0 = f ? (uint32_t(list_s[f - 1]) & 0x7FFFu) + 1u : first_in;
-            if (col < n_cols && S.coltype[col] != PP_COL_SKIP) slot_s[col * rows + rl] = (s0 << 16) | pos;
-            if (isrd && col != n_cols - 1) {
-              report(P.st, PP_ERR_COLCOUNT, tile_base + pos, true);
-              for (uint32_t c = col + 1; c < n_cols; ++c)
-                if (S.coltype[c] != PP_COL_SKIP) slot_s[c * rows + rl] = SLOT_DEFAULT;
-            }
-          }
-          crd += __popc(b);
-          if (b) clast = int32_t(g0 + 31 - __clz(b));
-        }
-      }
-      if (NS > 0 && t == 0) {  // the field still open at the tile end: value bytes only
-        const uint32_t s0 = T ? (uint32_t(list_s[T - 1]) & 0x7FFFu) + 1u : first_in;
-        const uint32_t s0in = s0 == 0xFFFFu ? 0u : s0;
-        if (s0in < tile_len) {
-          uint32_t col;
-          if (S.lastrd >= 0) {
-            col = T - uint32_t(S.lastrd) - 1u;
-          } else {
-            const uint64_t cc = uint64_t(ph.col_in) + T;
-            col = cc > 0x7FFFFF00ull ? 0x7FFFFF00u : uint32_t(cc);
-          }
-          if (col < n_cols && S.stridx[col] >= 0)
-            slot_s[col * rows + rows - 1] = (s0 << 16) | tile_len | 0x8000u;
-        }
-      }
-      __syncthreads();
-      // string columns: value bytes per field -> chars end offsets (a block
-      // scan over the column-major string slots), tile totals, staging layout
-      const uint32_t n_str = uint32_t(P.n_str);
-      if (NS > 0 && n_str) {
-        const uint32_t n = n_str * rows;
-        const uint32_t per = (n + NT - 1) / NT;
-        const uint32_t k0 = min(n, uint32_t(t) * per), k1 = min(n, k0 + per);
-        uint32_t lens[8];
-        uint32_t mysum = 0;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const uint32_t k = k0 + q;
-          uint32_t len = 0;
-          if (k < k1) {
-            const uint32_t si = k / rows, r = k - si * rows;
-            const uint32_t v = slot_s[P.strcol[si] * rows + r];
-            if (v != SLOT_ABSENT && v != SLOT_DEFAULT) {
-              const uint32_t a0 = (v >> 16) == 0xFFFFu ? 0u : (v >> 16), e = v & 0x7FFFu;
-              len = (e - a0) - popc_range(ctrl_s, a0, e);
-            }
-          }
-          lens[q] = len;
-          mysum += len;
-        }
-        uint32_t xi = mysum;
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-          const uint32_t o = __shfl_up_sync(FULL, xi, d);
-          if (lane >= d) xi += o;
-        }
-        if (lane == 31) S.wnt[warp] = xi;
-        __syncthreads();
-        if (warp == 0) {
-          const uint32_t v = lane < NW ? S.wnt[lane] : 0u;
-          uint32_t x = v;
-#pragma unroll
-          for (int d = 1; d < NW; d <<= 1) {
-            const uint32_t o = __shfl_up_sync(FULL, x, d);
-            if (lane >= d) x += o;
-          }
-          __syncwarp();
-          if (lane < NW) S.wnt[lane] = x - v;
-          if (lane == NW - 1) S.cstart[n_str] = x;
-        }
-        __syncthreads();
-        uint32_t run = S.wnt[warp] + xi - mysum;  // exclusive prefix of item k0
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const uint32_t k = k0 + q;
-          if (k < k1) {
-            if (k % rows == 0) S.cstart[k / rows] = run;
-            run += lens[q];
-            list_s[k] = uint16_t(run);  // inclusive: end of the field's chars in the tile
-          }
-        }
-        __syncthreads();
-        for (uint32_t k = t; k < n; k += NT) list_s[k] = uint16_t(list_s[k] - S.cstart[k / rows]);
-        if (t == 0) {
-          const uint64_t* cb = reinterpret_cast<const uint64_t*>(pr + PRE_HDR);
-          uint32_t Rr = 0;
-          for (uint32_t c = 0; c < n_str; ++c) {
-            const uint32_t a = S.cstart[c + 1] - S.cstart[c];
-            const uint64_t b = cb[c];
-            S.base[c] = b;
-            S.total[c] = a;
-            const uintptr_t gp = reinterpret_cast<uintptr_t>(P.chars[c]) + b;
-            Rr = ((Rr + 15u) & ~15u) + uint32_t(gp & 15u);
-            S.R[c] = Rr;
-            Rr += a;
-            if (last_tile) P.st->chars_len[P.strcol[c]] = b + a;
-          }
-        }
-        __syncthreads();
-        // Arrow offsets of closed string fields (coalesced per column)
-        for (uint32_t k = t; k < n; k += NT) {
-          const uint32_t si = k / rows, r = k - si * rows;
-          const uint32_t v = slot_s[P.strcol[si] * rows + r];
-          if (v == SLOT_ABSENT || (v != SLOT_DEFAULT && (v & 0x8000u))) continue;
-          const uint64_t rec = tile_rec0 + r;
-          if (!P.has_out) continue;
-          if (rec >= P.rec_cap) { report(P.st, PP_ERR_CAPACITY, 0, false); continue; }
-          const uint64_t off = S.base[si] + list_s[k];
-          if (off > 0x7FFFFFFFull || off > P.chars_cap[si]) report(P.st, PP_ERR_CAPACITY, 0, false);
-          else P.offsets[si][rec + 1] = int32_t(off);
-        }
-        // stage value bytes: a lane per short field, a warp per long one
-        for (uint32_t k = t; k < n; k += NT) {
-          const uint32_t si = k / rows, r = k - si * rows;
-          const uint32_t v = slot_s[P.strcol[si] * rows + r];
-          if (v == SLOT_ABSENT || v == SLOT_DEFAULT) continue;
-          const uint32_t a0 = (v >> 16) == 0xFFFFu ? 0u : (v >> 16), e = v & 0x7FFFu;
-          if (e - a0 > 64 || popc_range(ctrl_s, a0, e)) continue;
-          uint32_t dst = S.R[si] + list_s[k] - (e - a0);
-          for (uint32_t p = a0; p < e; ++p) stage_s[dst++] = uint8_t(tile_byte(tile_s, p));
-        }
-        for (uint32_t k = warp; k < n; k += NW) {
-          const uint32_t si = k / rows, r = k - si * rows;
-          const uint32_t v = slot_s[P.strcol[si] * rows + r];
-          if (v == SLOT_ABSENT || v == SLOT_DEFAULT) continue;
-          const uint32_t a0 = (v >> 16) == 0xFFFFu ? 0u : (v >> 16), e = v & 0x7FFFu;
-          const uint32_t nctrl = popc_range(ctrl_s, a0, e);
-          if (e - a0 <= 64 && !nctrl) continue;
-          const uint32_t len = (e - a0) - nctrl;
-          uint32_t dst = S.R[si] + list_s[k] - len;
-          for (uint32_t p0 = a0; p0 < e; p0 += 32) {
-            const uint32_t p = p0 + lane;
-            const bool isdata = p < e && !((ctrl_s[p >> 5] >> (p & 31)) & 1u);
-            const uint32_t bb = __ballot_sync(FULL, isdata);
-            if (isdata) stage_s[dst + __popc(bb & ((1u << lane) - 1u))] = uint8_t(tile_byte(tile_s, p));
-            dst += __popc(bb);
-          }
-        }
-      }
-      // numbers: a warp per 32 rows of one column
-      if (P.has_out && S.n_num) {
-        const uint32_t nch = (rows + 31) / 32;
-        const uint32_t total = S.n_num * nch;
-        for (uint32_t ci = warp; ci < total; ci += NW) {
-          const uint32_t oc = ci / nch;
-          const uint32_t r = (ci - oc * nch) * 32 + lane;
-          const uint32_t c = S.numcol[oc];
-          if (r >= rows) continue;
-          const uint32_t v = slot_s[c * rows + r];
-          if (v == SLOT_ABSENT) continue;
-          const uint64_t rec = tile_rec0 + r;
-          if (rec >= P.rec_cap) { report(P.st, PP_ERR_CAPACITY, 0, false); continue; }
-          convert_slot(P, c, S.coltype[c], v, rec, tile_base, tile_fstart, tile_fstate, tile_s,
-                       tile_w, ctrl_s, my_lut);
-        }
-      }
-      __syncthreads();
-      rec_end = tile_rec0 + (rows - 1) + (virt_rd ? 1u : 0u);
-    } else {
-      // ======== general path: per-thread walk over the chunk's fields
-      // ---- value bytes per string column: block scan, staging layout
-      uint64_t cex[NSW];
-  #pragma unroll
-      for (int k = 0; k < NSW; ++k) cex[k] = 0;
-      if (NS > 0) {
-        uint64_t cnt[NSW];
-  #pragma unroll
-        for (int k = 0; k < NSW; ++k) cnt[k] = 0;
-        {
-          uint32_t term = fd | rd, col = col0, start = 0;
-          for (;;) {
-            const uint32_t j = term ? uint32_t(__ffs(term) - 1) : 32u;
-            const uint32_t seg = data & range_mask(start, j);
-            if (col < n_cols) {
-              const int si = S.stridx[col];
-              if (si >= 0) add16(cnt, si, __popc(seg));
-            }
-            if (j == 32) break;
-            col = ((rd >> j) & 1u) ? 0u : col + 1;
-            start = j + 1;
-            term &= term - 1;
-          }
-        }
-        uint64_t ci[NSW];
-  #pragma unroll
-        for (int k = 0; k < NSW; ++k) ci[k] = cnt[k];
-  #pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-  #pragma unroll
-          for (int k = 0; k < NSW; ++k) {
-            const uint64_t o = __shfl_up_sync(FULL, ci[k], d);
-            if (lane >= d) ci[k] += o;
-          }
-        }
-        if (lane == 31) {
-  #pragma unroll
-          for (int k = 0; k < NSW; ++k) S.wcnt[warp][k] = ci[k];
-        }
-        __syncthreads();
-        if (warp == 0) {
-          uint64_t wv[NSW], wi2[NSW];
-  #pragma unroll
-          for (int k = 0; k < NSW; ++k) { wv[k] = lane < NW ? S.wcnt[lane][k] : 0ull; wi2[k] = wv[k]; }
-  #pragma unroll
-          for (int d = 1; d < NW; d <<= 1) {
-  #pragma unroll
-            for (int k = 0; k < NSW; ++k) {
-              const uint64_t o = __shfl_up_sync(FULL, wi2[k], d);
-              if (lane >= d) wi2[k] += o;
-            }
-          }
-          uint64_t tot[NSW];
-  #pragma unroll
-          for (int k = 0; k < NSW; ++k) {
-            tot[k] = __shfl_sync(FULL, wi2[k], NW - 1);
-            if (lane < NW) S.wcnt[lane][k] = wi2[k] - wv[k];
-          }
-          if (lane == 0) {
-            const uint64_t* cb = reinterpret_cast<const uint64_t*>(pr + PRE_HDR);
-            uint32_t R = 0;
-  #pragma unroll
-            for (int c = 0; c < NS; ++c) {
-              if (c < P.n_str) {
-                const uint32_t a = uint32_t((tot[c >> 2] >> (16 * (c & 3))) & 0xFFFFull);
-                const uint64_t b = cb[c];
-                S.base[c] = b;
-                S.total[c] = a;
-                const uintptr_t gp = reinterpret_cast<uintptr_t>(P.chars[c]) + b;
-                R = ((R + 15u) & ~15u) + uint32_t(gp & 15u);
-                S.R[c] = R;
-                R += a;
-                if (last_tile) P.st->chars_len[P.strcol[c]] = b + a;
-              }
-            }
-          }
-        }
-        __syncthreads();
-  #pragma unroll
-        for (int k = 0; k < NSW; ++k) cex[k] = S.wcnt[warp][k] + (ci[k] - cnt[k]);
-      }
 
-      // ---- fields: staging + (column, record) slots, then one lane per field
-      const uint32_t rows = S.rows;
-      const uint32_t n_out = S.n_out;
-      const uint32_t rpb = max(1u, uint32_t(SLOT_CAP) / n_cols);  // rows per pass
+    // ---- fields -> (column, row) slots, in passes of rows
+    const uint32_t rpb = max(1u, uint32_t(SLOT_CAP) / n_cols);
+    {
       for (uint32_t lo = 0; lo < rows; lo += rpb) {
-        const uint32_t hi = min(rows, lo + rpb);
-        const uint32_t nr = hi - lo;
-        for (uint32_t k = t; k < n_cols * nr; k += NT) slot_s[k] = SLOT_ABSENT;
-        __syncthreads();
-        {
-          uint32_t term = fd | rd, col = col0, start = 0;
-          uint64_t rec = rec0, fstart = fstart0;
-          uint64_t loc[NSW];
-  #pragma unroll
-          for (int k = 0; k < NSW; ++k) loc[k] = 0;
+        const uint32_t hi = min(rows, lo + rpb), nr = hi - lo;
+        if (NS > 0) { S.lk[0][t] = NO_FIELD; S.lk[1][t] = NO_FIELD; }
+        {  // walk this chunk's fields
+          uint32_t term = term_all, col = col0, rl = rl0, fs = fs0;
+          bool vrd = virt_rd;
           for (;;) {
-            const uint32_t j = term ? uint32_t(__ffs(term) - 1) : 32u;
-            const uint32_t seg = data & range_mask(start, j);
-            const int si = (NS > 0 && col < n_cols) ? int(S.stridx[col]) : -1;
-            if (si >= 0 && seg) {
-              if (lo == 0)  // stage this chunk's value bytes once
-                stage_runs(seg, S.R[si] + get16(cex, si) + get16(loc, si), own, stage_s);
-              add16(loc, si, __popc(seg));
+            uint32_t e;
+            bool isrd;
+            if (term) {
+              const uint32_t j = __ffs(term) - 1;
+              term &= term - 1;
+              e = cstart + j;
+              isrd = (rd >> j) & 1u;
+            } else if (vrd) {
+              e = tile_len;
+              isrd = true;
+              vrd = false;
+            } else {
+              break;
             }
-            uint64_t tpos;
-            bool is_rd;
-            if (j < 32) { tpos = tile_base + cstart + j; is_rd = (rd >> j) & 1u; }
-            else if (virt_rd) { tpos = P.n; is_rd = true; }
-            else break;
-            const uint64_t rl = rec - tile_rec0;
-            const bool in_pass = rl >= lo && rl < hi;
-            if (in_pass && col < n_cols && S.coltype[col] != PP_COL_SKIP) {
-              uint32_t v;
-              if (si >= 0) {
-                v = get16(cex, si) + get16(loc, si);
-              } else {
-                const uint32_t fs = fstart >= tile_base ? uint32_t(fstart - tile_base) : 0xFFFFu;
-                v = (fs << 16) | uint32_t(tpos - tile_base);
-              }
-              slot_s[col * nr + uint32_t(rl - lo)] = v;
-            }
-            if (is_rd) {
+            const bool in_pass = rl - lo < nr;
+            if (in_pass && col < n_cols) slot_s[col * nr + (rl - lo)] = (fs << 16) | e;
+            if (isrd) {
               if (col != n_cols - 1) {
-                if (lo == 0) report(P.st, PP_ERR_COLCOUNT, tpos, true);
-                if (in_pass) {  // missing fields take the column default
-                  for (uint32_t c = col + 1; c < n_cols; ++c) {
-                    const int sc = S.stridx[c];
-                    slot_s[c * nr + uint32_t(rl - lo)] =
-                        sc >= 0 ? get16(cex, sc) + get16(loc, sc) : SLOT_DEFAULT;
-                  }
-                }
+                if (lo == 0) report(P.st, PP_ERR_COLCOUNT, tile_base + e, true);
+                if (in_pass)  // missing fields take the column default
+                  for (uint32_t c = col + 1; c < n_cols; ++c) slot_s[c * nr + (rl - lo)] = SLOT_DEFAULT;
               }
-              ++rec;
+              ++rl;
               col = 0;
             } else {
               col = col < 0x7FFFFF00u ? col + 1 : col;
             }
-            fstart = tpos + 1;
-            if (j == 32) break;
-            start = j + 1;
-            term &= term - 1;
+            fs = e + 1;
           }
-          rec_end = rec;
+          // the field still open at the tile end (its value bytes are staged)
+          if (NS > 0 && owns_tail && !any_virt && rl - lo < nr && col < n_cols)
+            slot_s[col * nr + (rl - lo)] = (fs << 16) | tile_len;
         }
         __syncthreads();
-        if (P.has_out) {
-          const uint32_t items = n_out * nr;
-          for (uint32_t k = t; k < items; k += NT) {
-            const uint32_t oi = k / nr, r = k - oi * nr;
-            const uint32_t c = S.outcol[oi];
-            const uint32_t v = slot_s[c * nr + r];
-            if (v == SLOT_ABSENT) continue;
-            const uint64_t rec = tile_rec0 + lo + r;
-            if (rec >= P.rec_cap) { report(P.st, PP_ERR_CAPACITY, 0, false); continue; }
-            const uint32_t ty = S.coltype[c];
-            if (ty == PP_COL_STRING) {
-              const int si = S.stridx[c];
-              const uint64_t off = S.base[si] + v;
-              if (off > 0x7FFFFFFFull || off > P.chars_cap[si]) report(P.st, PP_ERR_CAPACITY, 0, false);
-              else P.offsets[si][rec + 1] = int32_t(off);
-              continue;
-            }
-            convert_slot(P, c, ty, v, rec, tile_base, tile_fstart, tile_fstate, tile_s, tile_w, ctrl_s,
-                         my_lut);
-          }
-        }
-        __syncthreads();
-      }
-    }
-    if (owns_end) P.st->n_records = rec_end;
+        const uint32_t ngr = (nr + 31) / 32;
+        const uint32_t mg = div_magic(ngr);
 
-    // ---- staged chars -> HBM
-    if (NS > 0 && P.has_out) {
-      for (int c = 0; c < P.n_str; ++c) {
-        uint32_t len = S.total[c];
-        if (!len) continue;
-        const uint64_t gb = S.base[c];
-        if (gb + len > P.chars_cap[c]) {
-          if (t == 0) report(P.st, PP_ERR_CAPACITY, 0, false);
-          len = gb >= P.chars_cap[c] ? 0u : uint32_t(P.chars_cap[c] - gb);
+        if (NS > 0 && n_str) {
+          // ---- string fields: value bytes -> chars positions (block scan
+          // over the column-major items), then staging copies
+          const uint32_t n_items = n_str * nr;
+          const uint32_t per = (n_items + NT - 1) / NT;  // <= SLOT_CAP / NT
+          const uint32_t k0 = min(n_items, uint32_t(t) * per), k1 = min(n_items, k0 + per);
+          // value bytes per field (into pos_s for now), long fields mark their chunks
+          uint32_t mysum = 0;
+          {
+            uint32_t si = k0 / nr, r = k0 - si * nr;
+            for (uint32_t k = k0; k < k1; ++k) {
+              uint32_t len = 0;
+              const uint32_t c = P.strcol[si];
+              const uint32_t row = lo + r;
+              const bool closed = (row > 0 || c >= col_in) && (row + 1 < rows || c < col_end);
+              const bool open = row + 1 == rows && c == col_end && !any_virt;
+              if (closed || open) {
+                const uint32_t v = slot_s[c * nr + r];
+                if (v != SLOT_DEFAULT) {
+                  const bool before = (v >> 16) == 0xFFFFu;
+                  const uint32_t a0 = before ? 0u : (v >> 16), e = v & 0xFFFFu;
+                  len = (e - a0) - (any_ctrl ? ctrl_before(ctrl_s, S.cpre, e) -
+                                                   ctrl_before(ctrl_s, S.cpre, a0) : 0u);
+                  if (len > SHORT_FIELD) {  // mark the chunks of a long field
+                    const uint32_t c0 = a0 >> 5, c1 = (e - 1) >> 5;
+                    S.lk[before ? 0 : 1][c0] = uint16_t(k);
+                    for (uint32_t cc = c0 + 1; cc <= c1; ++cc) S.lk[0][cc] = uint16_t(k);
+                  }
+                }
+              }
+              pos_s[k] = uint16_t(len);
+              mysum += len;
+              if (++r == nr) { r = 0; ++si; }
+            }
+          }
+          uint32_t xi = mysum;
+#pragma unroll
+          for (int d = 1; d < 32; d <<= 1) {
+            const uint32_t o = __shfl_up_sync(FULL, xi, d);
+            if (lane >= d) xi += o;
+          }
+          if (lane == 31) S.wsum[warp] = xi;
+          __syncthreads();
+          if (warp == 0) {
+            const uint32_t v = lane < NW ? S.wsum[lane] : 0u;
+            uint32_t x = v;
+#pragma unroll
+            for (int d = 1; d < NW; d <<= 1) {
+              const uint32_t o = __shfl_up_sync(FULL, x, d);
+              if (lane >= d) x += o;
+            }
+            __syncwarp();
+            if (lane < NW) S.wsum[lane] = x - v;
+            if (lane == NW - 1) S.cstart[n_str] = x;
+          }
+          __syncthreads();
+          {  // lengths -> chars end positions (inclusive prefix)
+            uint32_t run = S.wsum[warp] + xi - mysum;
+            uint32_t si = k0 / nr, r = k0 - si * nr;
+            for (uint32_t k = k0; k < k1; ++k) {
+              if (r == 0) S.cstart[si] = run;
+              run += pos_s[k];
+              pos_s[k] = uint16_t(run);
+              if (++r == nr) { r = 0; ++si; }
+            }
+          }
+          __syncthreads();
+          // staging: a lane per short field; long fields chunk-parallel,
+          // each thread copying its chunk's part of the (at most two) long
+          // fields that cover it
+          {
+            uint32_t si = k0 / nr, r = k0 - si * nr;
+            uint32_t prev = k0 ? pos_s[k0 - 1] : 0u;
+            if (r == 0) prev = S.cstart[si];
+            for (uint32_t k = k0; k < k1; ++k) {
+              const uint32_t pe = pos_s[k];
+              const uint32_t len = pe - prev;
+              prev = pe;
+              const uint32_t c = P.strcol[si];
+              const uint32_t rr = r;
+              if (++r == nr) { r = 0; ++si; prev = si < n_str ? S.cstart[si] : prev; }
+              if (len == 0 || len > SHORT_FIELD) continue;
+              const uint32_t v = slot_s[c * nr + rr];
+              const uint32_t a0 = (v >> 16) == 0xFFFFu ? 0u : (v >> 16), e = v & 0xFFFFu;
+              uint32_t dst = pe - len;
+              if (len == e - a0) {
+                for (uint32_t p = a0; p < e; ++p) stage_s[dst++] = tile_s[p];
+              } else {
+                for (uint32_t p = a0; p < e; ++p)
+                  if (!((ctrl_s[p >> 5] >> (p & 31)) & 1u)) stage_s[dst++] = tile_s[p];
+              }
+            }
+          }
+          {
+            const uint32_t mg_nr = div_magic(nr);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint32_t k = S.lk[h][t];
+              if (k == NO_FIELD) continue;
+              const uint32_t ksi = div_by(k, nr, mg_nr);
+              const uint32_t v = slot_s[P.strcol[ksi] * nr + (k - ksi * nr)];
+              const uint32_t a0 = (v >> 16) == 0xFFFFu ? 0u : (v >> 16), e = v & 0xFFFFu;
+              const uint32_t p0 = max(a0, cstart), p1 = min(e, cstart + clen);
+              const uint32_t c_a0 = any_ctrl ? ctrl_before(ctrl_s, S.cpre, a0) : 0u;
+              const uint32_t c_e = any_ctrl ? ctrl_before(ctrl_s, S.cpre, e) : 0u;
+              const uint32_t c_p0 = any_ctrl ? ctrl_before(ctrl_s, S.cpre, p0) : 0u;
+              const uint32_t len = (e - a0) - (c_e - c_a0);
+              uint32_t dst = pos_s[k] - len + (p0 - a0) - (c_p0 - c_a0);
+              const uint32_t cm = g.ctrl & range_mask(p0 - cstart, p1 - cstart);
+              if (!cm) {
+                for (uint32_t p = p0; p < p1; ++p) stage_s[dst++] = tile_s[p];
+              } else {
+                for (uint32_t p = p0; p < p1; ++p)
+                  if (!((cm >> (p - cstart)) & 1u)) stage_s[dst++] = tile_s[p];
+              }
+            }
+          }
         }
-        uint8_t* gp = P.chars[c] + gb;
-        const uint8_t* sp = stage_s + S.R[c];
-        const uint32_t head = min(len, uint32_t((16u - (reinterpret_cast<uintptr_t>(gp) & 15u)) & 15u));
-        const uint32_t nvec = (len - head) >> 4;
-        const uint32_t tail0 = head + (nvec << 4);
-        if (uint32_t(t) < head) gp[t] = sp[t];
-        uint4* gv = reinterpret_cast<uint4*>(gp + head);
-        const uint4* sv = reinterpret_cast<const uint4*>(sp + head);
-        for (uint32_t v = t; v < nvec; v += NT) __stcs(gv + v, sv[v]);
-        if (tail0 + t < len) gp[tail0 + t] = sp[tail0 + t];
+
+        // ---- numbers: a warp per 32 rows of one column
+        {
+          const uint32_t n_items = S.n_num * ngr;
+          for (;;) {
+            uint32_t it = 0;
+            if (lane == 0) it = atomicAdd(&S.item, 1u);
+            it = __shfl_sync(FULL, it, 0);
+            if (it >= n_items) break;
+            const uint32_t oc = div_by(it, ngr, mg);
+            const uint32_t r = lo + (it - oc * ngr) * 32 + lane;
+            const uint32_t c = S.numcol[oc];
+            if (r >= hi || (r == 0 && c < col_in) || (r + 1 == rows && c >= col_end)) continue;
+            const uint64_t rec = rec0 + r;
+            if (rec >= P.rec_cap) { report(P.st, PP_ERR_CAPACITY, 0, false); continue; }
+            convert_num(P, c, S.coltype[c], slot_s[c * nr + (r - lo)], rec, tile_base,
+                        tile_fstart, tile_fstate, tile_s, tile_w, ctrl_s, S.cpre, my_lut, any_ctrl);
+          }
+        }
+        __syncthreads();
+        if (NS > 0 && n_str && P.has_out) {
+          // Arrow offsets of the string fields closed in this pass
+          const uint32_t n_items = n_str * ngr;
+          for (uint32_t it = warp; it < n_items; it += NW) {
+            const uint32_t si = div_by(it, ngr, mg);
+            const uint32_t r = lo + (it - si * ngr) * 32 + lane;
+            const uint32_t c = P.strcol[si];
+            if (r >= hi || (r == 0 && c < col_in) || (r + 1 == rows && c >= col_end)) continue;
+            const uint64_t rec = rec0 + r;
+            if (rec >= P.rec_cap) { report(P.st, PP_ERR_CAPACITY, 0, false); continue; }
+            const uint64_t off = S.base[si] + S.carry[si] + (pos_s[si * nr + (r - lo)] - S.cstart[si]);
+            if (off > 0x7FFFFFFFull || off > P.chars_cap[si]) report(P.st, PP_ERR_CAPACITY, 0, false);
+            else P.offsets[si][rec + 1] = int32_t(off);
+          }
+          // staged chars -> HBM, 16-byte aligned stores
+          for (uint32_t si = 0; si < n_str; ++si) {
+            uint32_t len = S.cstart[si + 1] - S.cstart[si];
+            if (!len) continue;
+            const uint64_t gb = S.base[si] + S.carry[si];
+            if (gb + len > P.chars_cap[si]) {
+              if (t == 0) report(P.st, PP_ERR_CAPACITY, 0, false);
+              len = gb >= P.chars_cap[si] ? 0u : uint32_t(P.chars_cap[si] - gb);
+            }
+            uint8_t* gp = P.chars[si] + gb;
+            const uint32_t sp = S.cstart[si];
+            const uint32_t head = min(len, uint32_t((16u - (reinterpret_cast<uintptr_t>(gp) & 15u)) & 15u));
+            const uint32_t nvec = (len - head) >> 4;
+            const uint32_t tail0 = head + (nvec << 4);
+            if (uint32_t(t) < head) gp[t] = stage_s[sp + t];
+            const uint32_t src0 = sp + head;
+            const uint32_t sh = (src0 & 3u) * 8u;
+            const uint32_t* sw = reinterpret_cast<const uint32_t*>(stage_s + (src0 & ~3u));
+            uint4* gv = reinterpret_cast<uint4*>(gp + head);
+            for (uint32_t v = t; v < nvec; v += NT) {
+              const uint32_t* q = sw + 4 * v;
+              const uint32_t a0 = q[0], a1 = q[1], a2 = q[2], a3 = q[3], a4 = q[4];
+              uint4 o;
+              o.x = __funnelshift_r(a0, a1, sh);
+              o.y = __funnelshift_r(a1, a2, sh);
+              o.z = __funnelshift_r(a2, a3, sh);
+              o.w = __funnelshift_r(a3, a4, sh);
+              __stcs(gv + v, o);
+            }
+            if (tail0 + t < len) gp[tail0 + t] = stage_s[sp + tail0 + t];
+          }
+        }
+        __syncthreads();
+        if (NS > 0 && t < int(n_str)) S.carry[t] += S.cstart[t + 1] - S.cstart[t];
+        if (t == 0) S.item = 0;
       }
     }
+    __syncthreads();
+    if (t < int(n_str)) {
+      if (last_tile) P.st->chars_len[P.strcol[t]] = S.base[t] + S.carry[t];
+      S.carry[t] = 0;
+    }
+    if (owns_end) P.st->n_records = rec0 + (rows - 1) + (virt_rd ? 1u : 0u);
     feed_next(P, S.F, counter, aligned_in, lin0);  // the tile was last read before a barrier above
   }
   feed_finish(S.F);
@@ -1638,12 +1503,14 @@ __global__ void __launch_bounds__(NT, 2) main_kernel(const __grid_constant__ Par
 // ================================================================= launch
 // Zero the tile counters and the scan's look-back flags; initialise the
 // status and offsets[c][0] = 0 for every string column.
-__global__ void parse_init_kernel(uint32_t* counters, uint32_t* flag_a, uint32_t* flag_c,
-                                  uint32_t n_blocks, pp_status* st, ParseParams P) {
+__global__ void parse_init_kernel(ParseParams P) {
+  const ppi::ParseScratch& s = P.s;
   const uint32_t i0 = blockIdx.x * blockDim.x + threadIdx.x;
-  for (uint32_t i = i0; i < n_blocks; i += gridDim.x * blockDim.x) { flag_a[i] = 0; flag_c[i] = 0; }
-  if (i0 < 4) counters[i0] = 0;
+  const uint32_t stride = gridDim.x * blockDim.x;
+  for (uint32_t i = i0; i < s.n_scan_blocks; i += stride) { s.scan_flag_a[i] = 0; s.scan_flag_c[i] = 0; }
+  if (i0 < 4) s.counters[i0] = 0;
   if (i0 == 0) {
+    pp_status* st = P.st;
     st->error = 0;
     st->reserved = 0;
     st->first_error_offset = ~0ull;
@@ -1661,7 +1528,7 @@ template <int NS>
 cudaError_t launch_ns(const ParseParams& p, cudaStream_t stream) {
   static Occ occ;
   cudaError_t e;
-  if (occ.ctx < 0) {
+  if (occ.main < 0) {
     int dev;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&occ.n_sm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
@@ -1682,14 +1549,13 @@ cudaError_t launch_ns(const ParseParams& p, cudaStream_t stream) {
       return e;
     occ.main = b > 0 ? b : 1;
   }
-  const ppi::ParseScratch& s = p.s;
-  parse_init_kernel<<<std::max<uint32_t>(1, (s.n_scan_blocks + 255) / 256), 256, 0, stream>>>(
-      s.counters, s.scan_flag_a, s.scan_flag_c, s.n_scan_blocks, p.st, p);
+  parse_init_kernel<<<std::max<uint32_t>(1, std::min<uint32_t>((p.s.n_scan_blocks + 255) / 256, 1024)),
+                      256, 0, stream>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess || p.n_tiles == 0) return e;
   const uint32_t g1 = uint32_t(std::min<uint64_t>(p.n_tiles, uint64_t(occ.n_sm) * occ.ctx));
   ctx_kernel<NS><<<g1, NT, CTX_SMEM, stream>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  scan_kernel<NS><<<s.n_scan_blocks, SCAN_NT, 0, stream>>>(p);
+  scan_kernel<NS><<<p.s.n_scan_blocks, SCAN_NT, 0, stream>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const uint32_t g3 = uint32_t(std::min<uint64_t>(p.n_tiles, uint64_t(occ.n_sm) * occ.main));
   main_kernel<NS><<<g3, NT, MAIN_SMEM, stream>>>(p);
@@ -1697,11 +1563,11 @@ cudaError_t launch_ns(const ParseParams& p, cudaStream_t stream) {
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
-uint32_t ctx_stride_of(int n_str, int n_cols) {
-  const size_t b = CTX_HDR + (n_str > 0 ? 8 * size_t(n_str) + 8 * size_t(n_cols) : 0);
+uint32_t ctx_stride_of(int ns, int n_cols) {
+  const size_t b = CTX_HDR + (ns > 0 ? 8 * size_t(ns) + 8 * size_t(n_cols) : 0);
   return uint32_t((b + 15) & ~size_t(15));
 }
-uint32_t pre_stride_of(int n_str) { return uint32_t(PRE_HDR + 8 * (n_str > 0 ? n_str : 0)); }
+uint32_t pre_stride_of(int ns) { return uint32_t(PRE_HDR + 8 * (ns > 0 ? ns : 0)); }
 
 }  // namespace
 
@@ -1716,8 +1582,9 @@ int parse_ns_width(int n_str) {
   return 16;
 }
 
-// layout: counters (16 B) | scan flags a, c | scan payloads a (2 x 13 words
-// per block), c (2 x ns words per block) | ctx records | pre records
+// layout: counters | scan flags (records, chars) | scan payloads (2 x 13
+// words per scan block; 2 x ns words per scan block) | ctx records | pre
+// records
 size_t parse_scratch_bytes(uint32_t n, int ns, int n_cols) {
   const uint32_t nb = (n + SCAN_TILES - 1) / SCAN_TILES;
   const int k3 = ns > 0 ? ns : 1;

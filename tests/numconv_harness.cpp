@@ -18,4 +18,7 @@ void h_parse_floats(const unsigned char* buf, size_t n, uint64_t* bits, int* err
   }
 }
 uint64_t h_decimal_to_binary64(uint64_t w, int q) { return ppn::decimal_to_binary64(w, q); }
+uint64_t h_short_decimal_to_binary64(uint32_t w, int q) {
+  return ppn::short_decimal_to_binary64(w, q);
+}
 }

@@ -141,3 +141,43 @@ def test_syntax(harness):
     bad = ["", "+", ".", "e5", "1e", "1e+", "1.2.3", "inf", "nan", "0x1p3", "--1", "+.e1", "1a"]
     bits, err = _run(harness, bad)
     assert (err != 0).all()
+
+
+def _short(L, ws, qs):
+    L.h_short_decimal_to_binary64.restype = ctypes.c_uint64
+    L.h_short_decimal_to_binary64.argtypes = [ctypes.c_uint32, ctypes.c_int]
+    return np.array([L.h_short_decimal_to_binary64(w, q) for w, q in zip(ws, qs)], dtype=np.uint64)
+
+
+def _exact(ws, qs):
+    from fractions import Fraction
+    return np.array([struct.unpack("<Q", struct.pack("<d", float(Fraction(w) / 10 ** (-q))))[0]
+                     for w, q in zip(ws, qs)], dtype=np.uint64)
+
+
+def test_short_significand_edges(harness):
+    """The short path (w < 2^32, -22 <= q <= 0): dyadic values and the ends
+    of the range are exact."""
+    cases = [(1, 0), (9, 0), (4294967295, 0), (5, -1), (25, -2), (125, -3), (1, -1), (1, -22),
+             (4294967295, -22), (4294967295, -1), (46386, -2), (50000, -2), (3, -1),
+             (123456789, -7), (1, -8), (999999999, -9)]
+    ws, qs = zip(*cases)
+    assert (_short(harness, ws, qs) == _exact(ws, qs)).all()
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_short_significand_random(harness, seed):
+    """Random w < 2^32 and q in [-22, 0] against exact rational rounding:
+    correctly rounded."""
+    rng = random.Random(50 + seed)
+    ws = [rng.choice([rng.randrange(1, 1 << 32), rng.randrange(1, 100000)]) for _ in range(20000)]
+    qs = [rng.randint(-22, 0) for _ in ws]
+    assert (_short(harness, ws, qs) == _exact(ws, qs)).all()
+
+
+def test_short_significand_workload_shapes_exact(harness):
+    """%.2f in [0, 500] and the significands %.6g prints convert exactly."""
+    rng = random.Random(11)
+    ws = [rng.randint(1, 50000) for _ in range(20000)] + [rng.randint(1, 999999) for _ in range(20000)]
+    qs = [-2] * 20000 + [rng.randint(-6, 0) for _ in range(20000)]
+    assert (_short(harness, ws, qs) == _exact(ws, qs)).all()

@@ -85,7 +85,7 @@ def test_noalloc_rejects_input_larger_than_its_buffer():
     out = pp.CsvOutputs(col_types, 1, [1] * 64)
     with pytest.raises(RuntimeError, match=r"pp_parse_noalloc failed: .*\(4\)"):
         out.run_noalloc(d_in, n, pp.desc_csv())
-    # a smaller input with the same schema is accepted (empty records)
+    # a smaller input with the same schema is accepted
     small = d_in[: 1 << 20]
     out.run_noalloc(small, small.numel(), pp.desc_csv())
     torch.cuda.synchronize()
