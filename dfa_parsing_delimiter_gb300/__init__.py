@@ -84,6 +84,12 @@ def lib() -> ctypes.CDLL:
         L.pp_tile_bytes.argtypes = []
         L.pp_debug_set_spin_limit.restype = None
         L.pp_debug_set_spin_limit.argtypes = [_u32]
+        L.pp_debug_set_withhold.restype = None
+        L.pp_debug_set_withhold.argtypes = [ctypes.c_int]
+        L.pp_debug_stage_timing.restype = ctypes.c_int
+        L.pp_debug_stage_timing.argtypes = [ctypes.c_int]
+        L.pp_debug_stage_ms.restype = ctypes.c_int
+        L.pp_debug_stage_ms.argtypes = [_vp, ctypes.c_int]
         _lib = L
     return _lib
 
@@ -116,6 +122,29 @@ def tile_bytes() -> int:
 
 def debug_set_spin_limit(polls: int) -> None:
     lib().pp_debug_set_spin_limit(int(polls))
+
+
+def debug_set_withhold(on: bool) -> None:
+    """Test hook: the first cross-tile scan block posts nothing, so later
+    blocks time out (bounded) and report ERR_LOOKBACK_TIMEOUT."""
+    lib().pp_debug_set_withhold(1 if on else 0)
+
+
+def debug_stage_timing(n_calls: int) -> None:
+    """Record per-kernel CUDA events for the next n_calls pp_parse calls
+    (0: stop).  Benchmark hook."""
+    _check(lib().pp_debug_stage_timing(int(n_calls)), "pp_debug_stage_timing")
+
+
+def debug_stage_ms(max_calls: int):
+    """Per-call kernel durations (ms) recorded since debug_stage_timing:
+    rows of (init, context, scan, main)."""
+    import numpy as np
+    out = np.zeros((max(int(max_calls), 1), 4), dtype=np.float32)
+    n = lib().pp_debug_stage_ms(out.ctypes.data, int(max_calls))
+    if n < 0:
+        raise RuntimeError("pp_debug_stage_ms failed")
+    return out[:n]
 
 
 def new_status(device=None) -> torch.Tensor:

@@ -11,6 +11,20 @@
 
 namespace ppi {
 uint32_t g_spin_limit = 1u << 22;  // ~1 s of polling before a look-back gives up
+uint32_t g_withhold = 0;           // test hook, see pp_debug_set_withhold
+
+// Stage timing for benchmarks: events of the recorded calls, 5 per call.
+constexpr int STAGE_EVENTS = 5;
+cudaEvent_t* g_stage_ev = nullptr;
+int g_stage_cap = 0, g_stage_used = 0, g_stage_cur = -1;
+
+bool stage_begin() {
+  g_stage_cur = g_stage_used < g_stage_cap ? g_stage_used++ : -1;
+  return g_stage_cur >= 0;
+}
+void stage_mark(int k, cudaStream_t stream) {
+  if (g_stage_cur >= 0) cudaEventRecord(g_stage_ev[g_stage_cur * STAGE_EVENTS + k], stream);
+}
 }
 
 namespace {
@@ -193,6 +207,7 @@ pp_rc parse_prepare(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa,
   if (nt > 0xFFFFFFF0ull) return PP_EINVAL;
   p.n_tiles = uint32_t(nt);
   p.spin_limit = ppi::g_spin_limit;
+  p.dbg_withhold = ppi::g_withhold;
   const int x = sticky_state(dfa);
   p.sticky = uint32_t(x);
   for (int b = 0; b < 256; ++b) p.lut[b] = parse_lut_entry(dfa, dfa->byte_to_group[b], x);
@@ -402,5 +417,40 @@ pp_rc pp_count_byte(const uint8_t* d_in, size_t n_bytes, uint8_t value, uint64_t
 }
 
 void pp_debug_set_spin_limit(uint32_t polls) { ppi::g_spin_limit = polls ? polls : (1u << 22); }
+
+void pp_debug_set_withhold(int on) { ppi::g_withhold = on ? 1u : 0u; }
+
+pp_rc pp_debug_stage_timing(int n_calls) {
+  using namespace ppi;
+  for (int i = 0; i < g_stage_cap * STAGE_EVENTS; ++i) cudaEventDestroy(g_stage_ev[i]);
+  delete[] g_stage_ev;
+  g_stage_ev = nullptr;
+  g_stage_cap = g_stage_used = 0;
+  g_stage_cur = -1;
+  if (n_calls <= 0) return PP_OK;
+  g_stage_ev = new cudaEvent_t[size_t(n_calls) * STAGE_EVENTS];
+  for (int i = 0; i < n_calls * STAGE_EVENTS; ++i) {
+    if (cudaEventCreate(&g_stage_ev[i]) != cudaSuccess) {
+      for (int j = 0; j < i; ++j) cudaEventDestroy(g_stage_ev[j]);
+      delete[] g_stage_ev;
+      g_stage_ev = nullptr;
+      return PP_ECUDA;
+    }
+  }
+  g_stage_cap = n_calls;
+  return PP_OK;
+}
+
+int pp_debug_stage_ms(float* out, int max_calls) {
+  using namespace ppi;
+  const int n = g_stage_used < max_calls ? g_stage_used : max_calls;
+  for (int i = 0; i < n; ++i) {
+    cudaEvent_t* e = g_stage_ev + i * STAGE_EVENTS;
+    if (cudaEventSynchronize(e[STAGE_EVENTS - 1]) != cudaSuccess) return -1;
+    for (int k = 0; k + 1 < STAGE_EVENTS; ++k)
+      if (cudaEventElapsedTime(&out[4 * i + k], e[k], e[k + 1]) != cudaSuccess) return -1;
+  }
+  return n;
+}
 
 }  // extern "C"

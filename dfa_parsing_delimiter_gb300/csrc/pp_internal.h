@@ -36,6 +36,7 @@ struct ParseParams {
   uint64_t n;
   uint32_t n_tiles;
   uint32_t spin_limit;
+  uint32_t dbg_withhold;  // test hook: the first scan block posts nothing
   uint32_t lut[256];      // per byte: STV selector, next-state/tag fields, special bit
   uint32_t bg_next;       // nibble s = delta[background][s], s = 0..4
   uint32_t sticky;        // state whose non-inert groups set LUT bit 30 (4: none)
@@ -66,6 +67,11 @@ int parse_ns_width(int n_str);
 
 // init (counters, scan flags, status), context pass, scan, main pass
 cudaError_t launch_parse(const ParseParams& p, cudaStream_t stream);
+// Stage timing (benchmark hook): stage_begin() opens the record of one
+// call (false if recording is off or full); stage_mark(k) records its
+// event k (0: before the first kernel, k: after the k-th).
+bool stage_begin();
+void stage_mark(int k, cudaStream_t stream);
 // pp_parse's argument checks and kernel parameters (all but the scratch)
 pp_rc parse_prepare(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa, int n_cols,
                     const pp_coltype* col_types, int32_t* const out_offsets[],

@@ -828,8 +828,13 @@ __global__ void __launch_bounds__(SCAN_NT) scan_kernel(const __grid_constant__ P
     }
     sagg_pack(sagg_identity(true), seed);
     sagg_pack(sagg_identity(false), ident);
-    lookback_vec<13>(P.s.scan_flag_a, P.s.scan_agg_a, P.s.scan_inc_a, blk, agg, seed, ident,
-                     SAggOp{}, cfg, ex);
+    if (P.dbg_withhold && blk == 0) {  // test hook: post nothing, later blocks time out
+#pragma unroll
+      for (int k = 0; k < 13; ++k) ex[k] = seed[k];
+    } else {
+      lookback_vec<13>(P.s.scan_flag_a, P.s.scan_agg_a, P.s.scan_inc_a, blk, agg, seed, ident,
+                       SAggOp{}, cfg, ex);
+    }
     if (lane == 0)
 #pragma unroll
       for (int k = 0; k < 13; ++k) S.pre[k] = ex[k];
@@ -942,8 +947,13 @@ __global__ void __launch_bounds__(SCAN_NT) scan_kernel(const __grid_constant__ P
         agg[k] = __shfl_sync(FULL, x[k], SW - 1);
         if (lane < SW) S.wsum[lane][k] = x[k] - v[k];
       }
-      lookback_vec<K3>(P.s.scan_flag_c, P.s.scan_agg_c, P.s.scan_inc_c, blk, agg, zero, zero,
-                       AddOp<K3>{}, cfg, exc);
+      if (P.dbg_withhold && blk == 0) {
+#pragma unroll
+        for (int k = 0; k < K3; ++k) exc[k] = 0;
+      } else {
+        lookback_vec<K3>(P.s.scan_flag_c, P.s.scan_agg_c, P.s.scan_inc_c, blk, agg, zero, zero,
+                         AddOp<K3>{}, cfg, exc);
+      }
       if (lane == 0)
 #pragma unroll
         for (int k = 0; k < K3; ++k) S.base[k] = exc[k];
@@ -1549,16 +1559,24 @@ cudaError_t launch_ns(const ParseParams& p, cudaStream_t stream) {
       return e;
     occ.main = b > 0 ? b : 1;
   }
+  const bool timed = ppi::stage_begin();
+  if (timed) ppi::stage_mark(0, stream);
   parse_init_kernel<<<std::max<uint32_t>(1, std::min<uint32_t>((p.s.n_scan_blocks + 255) / 256, 1024)),
                       256, 0, stream>>>(p);
-  if ((e = cudaGetLastError()) != cudaSuccess || p.n_tiles == 0) return e;
-  const uint32_t g1 = uint32_t(std::min<uint64_t>(p.n_tiles, uint64_t(occ.n_sm) * occ.ctx));
-  ctx_kernel<NS><<<g1, NT, CTX_SMEM, stream>>>(p);
+  if (timed) ppi::stage_mark(1, stream);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  scan_kernel<NS><<<p.s.n_scan_blocks, SCAN_NT, 0, stream>>>(p);
+  const uint32_t g1 = uint32_t(std::min<uint64_t>(std::max<uint32_t>(p.n_tiles, 1),
+                                                  uint64_t(occ.n_sm) * occ.ctx));
+  if (p.n_tiles) ctx_kernel<NS><<<g1, NT, CTX_SMEM, stream>>>(p);
+  if (timed) ppi::stage_mark(2, stream);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const uint32_t g3 = uint32_t(std::min<uint64_t>(p.n_tiles, uint64_t(occ.n_sm) * occ.main));
-  main_kernel<NS><<<g3, NT, MAIN_SMEM, stream>>>(p);
+  if (p.n_tiles) scan_kernel<NS><<<p.s.n_scan_blocks, SCAN_NT, 0, stream>>>(p);
+  if (timed) ppi::stage_mark(3, stream);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const uint32_t g3 = uint32_t(std::min<uint64_t>(std::max<uint32_t>(p.n_tiles, 1),
+                                                  uint64_t(occ.n_sm) * occ.main));
+  if (p.n_tiles) main_kernel<NS><<<g3, NT, MAIN_SMEM, stream>>>(p);
+  if (timed) ppi::stage_mark(4, stream);
   return cudaGetLastError();
 }
 

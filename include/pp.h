@@ -257,6 +257,26 @@ size_t pp_tile_bytes(void);
  * second of polling).  Process-wide; affects calls made afterwards. */
 void pp_debug_set_spin_limit(uint32_t polls);
 
+/* Test hook for the bounded waits: while on, the first block of
+ * pp_parse's cross-tile scan posts nothing, so the waits of the later
+ * blocks run out after the spin limit and the call reports
+ * PP_ERR_LOOKBACK_TIMEOUT (fatal: outputs unspecified).  No wait is left
+ * unbounded; the device stays usable.  Process-wide. */
+void pp_debug_set_withhold(int on);
+
+/* Benchmark hook: with n_calls > 0, the next n_calls pp_parse calls record
+ * CUDA events on their stream around each of their four kernels (init,
+ * context pass, scan, main pass).  0 stops recording and frees the events.
+ * Process-wide; not thread-safe.  Returns PP_ECUDA if events cannot be
+ * created. */
+pp_rc pp_debug_stage_timing(int n_calls);
+
+/* Kernel durations of the recorded calls: out[4*i + k] = milliseconds of
+ * kernel k (0 init, 1 context, 2 scan, 3 main) of call i.  Waits for the
+ * events.  Returns the number of calls written (at most max_calls), or -1
+ * on a CUDA error. */
+int pp_debug_stage_ms(float* out, int max_calls);
+
 #ifdef __cplusplus
 }
 #endif

@@ -216,6 +216,25 @@ def test_parse_random_small_inputs():
         compare_csv(data, ["str", "i32", "f64"])
 
 
+def test_parse_lookback_timeout_is_reported_and_recoverable():
+    """A wait that runs out ends with an error status, not a hang: with the
+    first scan block withholding its prefix (a flag nothing sets) and a short
+    spin limit, the later blocks give up and report the timeout; the next
+    normal call on the same context is clean."""
+    data = b"ab,cd\n" * ((40 << 20) // 6)  # > 2048 tiles: several scan blocks
+    try:
+        pp.debug_set_spin_limit(2000)
+        pp.debug_set_withhold(True)
+        out, st = run_gpu_csv(data, ["str", "str"])
+        assert st["error"] & pp.ERR_LOOKBACK_TIMEOUT, st
+    finally:
+        pp.debug_set_withhold(False)
+        pp.debug_set_spin_limit(0)
+    out, st = run_gpu_csv(data, ["str", "str"])
+    assert st["error"] == 0 and st["n_records"] == len(data) // 6, st
+    torch.cuda.synchronize()
+
+
 def test_parse_capacity_too_small():
     data, info, _ = datagen.generate("csv18_2gib", target=2 * TILE)
     cols = datagen.WORKLOADS["csv18_2gib"]["cols"]
