@@ -295,9 +295,16 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
 }
 
+// x << n for 0 <= n <= 32 (PTX clamps shift amounts to the register width,
+// so n == 32 gives 0)
+__device__ __forceinline__ uint32_t shl32(uint32_t x, uint32_t n) {
+  uint32_t r;
+  asm("shl.b32 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(n));
+  return r;
+}
 // bits [a, b) of a 32-bit mask, 0 <= a <= b <= 32
 __device__ __forceinline__ uint32_t range_mask(uint32_t a, uint32_t b) {
-  return uint32_t(((1ull << b) - 1ull) & ~((1ull << a) - 1ull));
+  return shl32(0xFFFFFFFFu, a) & ~shl32(0xFFFFFFFFu, b);
 }
 
 }  // namespace ppd

@@ -388,47 +388,58 @@ __device__ __forceinline__ uint64_t tile_load8(const uint32_t* tile_w, uint32_t 
 }
 
 // ------------------------------------------------- numeric fast paths
-// Digit values of the low n bytes of x (1 <= n <= 8) left-aligned for the
-// combining steps, or false if one of them is not a digit.
-__device__ __forceinline__ bool swar_digits(uint64_t x, uint32_t n, uint64_t& d) {
-  const uint64_t keep = n >= 8 ? ~0ull : ((1ull << (8 * n)) - 1);
-  x &= keep;
-  const uint64_t hiok = (x & (0xF0F0F0F0F0F0F0F0ull & keep)) ^ (0x3030303030303030ull & keep);
-  const uint64_t lo = x & 0x0F0F0F0F0F0F0F0Full;
-  const uint64_t big = (lo + 0x0606060606060606ull) & 0xF0F0F0F0F0F0F0F0ull;
-  if (hiok | big) return false;
-  d = n >= 8 ? lo : lo << (8 * (8 - n));
+// Characters are handled four to a 32-bit word (character i in byte i);
+// y = chars ^ '0' maps digits to 0..9 and '.' to 0x1E.
+// 0x80 in each byte of y above 9
+__device__ __forceinline__ uint32_t nondigit_bytes(uint32_t y) {
+  return (((y & 0x7F7F7F7Fu) + 0x76767676u) | y) & 0x80808080u;
+}
+// 0x80 in each zero byte of v
+__device__ __forceinline__ uint32_t zero_bytes(uint32_t v) {
+  return ~(((v & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) | v | 0x7F7F7F7Fu);
+}
+// 0x80 in each of the first n (0..4) bytes
+__device__ __forceinline__ uint32_t first_bytes(int n) {
+  return n >= 4 ? 0x80808080u : (n <= 0 ? 0u : 0x80808080u & ((1u << (8 * n)) - 1u));
+}
+// value of the 4 digits in w, byte 0 the most significant
+__device__ __forceinline__ uint32_t val4(uint32_t w) {
+  w = (w * 10u + (w >> 8)) & 0x00FF00FFu;
+  return (w * 100u + (w >> 16)) & 0xFFFFu;
+}
+// Value of the n (1..8) digits in y0:y1 (chars ^ '0'), or false if one is
+// not a digit.
+__device__ __forceinline__ bool digits8(uint32_t y0, uint32_t y1, int n, uint32_t& v) {
+  if ((nondigit_bytes(y0) & first_bytes(n)) | (nondigit_bytes(y1) & first_bytes(n - 4))) return false;
+  // right-align: the last digit to byte 7, zeros before the first
+  const uint32_t sh = 8u * uint32_t(8 - n);
+  uint32_t z0, z1;
+  if (sh >= 32) { z1 = y0 << (sh - 32); z0 = 0; }
+  else { z1 = __funnelshift_l(y0, y1, sh); z0 = y0 << sh; }
+  v = val4(z0) * 10000u + val4(z1);
   return true;
 }
-// value of 8 left-aligned digits, most significant in the lowest byte
-__device__ __forceinline__ uint64_t swar_value(uint64_t d) {
-  d = (d * 10 + (d >> 8)) & 0x00FF00FF00FF00FFull;
-  d = (d * 100 + (d >> 16)) & 0x0000FFFF0000FFFFull;
-  return (d * 10000 + (d >> 32)) & 0xFFFFFFFFull;
-}
-// The n (1..8) characters in the low bytes of x as digits[.digits] (at
-// most one dot, at least one digit): significand (< 10^8) and decimal
-// exponent (-7..0).
-__device__ __forceinline__ bool fast_float_x(uint64_t x, uint32_t n, uint64_t& mant, int& q) {
-  const uint64_t keep = n >= 8 ? ~0ull : ((1ull << (8 * n)) - 1);
-  const uint64_t z = (x ^ 0x2E2E2E2E2E2E2E2Eull) & keep;  // zero bytes at '.'
-  const uint64_t dots = ~(((z & 0x7F7F7F7F7F7F7F7Full) + 0x7F7F7F7F7F7F7F7Full) | z |
-                          0x7F7F7F7F7F7F7F7Full) & keep;
-  uint32_t nd = n;
+// n (1..8) characters in x0:x1 as digits[.digits] (at most one dot, at
+// least one digit): significand (< 10^8) and decimal exponent (-7..0).
+__device__ __forceinline__ bool dec8(uint32_t x0, uint32_t x1, int n, uint32_t& mant, int& q) {
+  uint32_t y0 = x0 ^ 0x30303030u, y1 = x1 ^ 0x30303030u;
+  const uint32_t d0 = zero_bytes(y0 ^ 0x1E1E1E1Eu) & first_bytes(n);
+  const uint32_t d1 = zero_bytes(y1 ^ 0x1E1E1E1Eu) & first_bytes(n - 4);
   q = 0;
-  if (dots) {
-    if (dots & (dots - 1)) return false;                // two dots
-    const uint32_t k = (__ffsll(dots) - 1) >> 3;        // dot index
-    const uint64_t below = k ? ((1ull << (8 * k)) - 1) : 0ull;
-    x = (x & below) | ((x >> 8) & ~below);              // squeeze the dot out
-    nd = n - 1;
-    q = -int(nd - k);
-    if (nd == 0) return false;
+  if (d0 | d1) {
+    if (__popc(d0) + __popc(d1) > 1) return false;
+    const int p = d0 ? (__ffs(d0) - 1) >> 3 : 4 + ((__ffs(d1) - 1) >> 3);
+    // squeeze the dot out of the 8-byte string
+    uint64_t Y = (uint64_t(y1) << 32) | y0;
+    const uint64_t below = (1ull << (8 * p)) - 1ull;
+    Y = (Y & below) | ((Y >> 8) & ~below);
+    y0 = uint32_t(Y);
+    y1 = uint32_t(Y >> 32);
+    --n;
+    q = p - n;
+    if (n == 0) return false;
   }
-  uint64_t d;
-  if (!swar_digits(x, nd, d)) return false;
-  mant = swar_value(d);
-  return true;
+  return digits8(y0, y1, n, mant);
 }
 
 __device__ __forceinline__ void load_lut(const ParseParams& P, uint32_t* lut_s) {
@@ -575,6 +586,9 @@ __global__ void __launch_bounds__(NT, 2) ctx_kernel(const __grid_constant__ Pars
       if (s == 0 && lane == 0) rec[0] = S.tile_stv;
     }
     if (NS > 0) {
+      const uint64_t strmask = P.strmask;
+      const uint32_t cmax = 63u - __clzll(static_cast<long long>(strmask));  // last string column
+      const bool chain = cmax < 8;  // column masks when the string columns come early
       __syncthreads();
       // value bytes per string column, per start state
       uint32_t col0[4];
@@ -596,10 +610,15 @@ __global__ void __launch_bounds__(NT, 2) ctx_kernel(const __grid_constant__ Pars
         const Tags& gs = g[s];
         const uint32_t valid = range_mask(0, min(clen, gs.inv_at));
         const uint32_t data = valid & ~(gs.fd | gs.rd | gs.ctrl);
-        bool abs = (col0[s] & ABS32) != 0;
-        uint32_t col = col0[s] & ~ABS32, term = gs.fd | gs.rd, seg0 = 0;
+        const uint32_t T = gs.fd | gs.rd;
+        const bool abs0 = (col0[s] & ABS32) != 0;
+        const uint32_t c0 = col0[s] & ~ABS32;
         uint32_t k0 = 0xFFFFFFFFu, n0 = 0;  // the first relative segment, summed per warp below
-        if (st[s] < 4 && same < 0) {  // (a shared state's fields are all absolute)
+        if (st[s] < 4 && same < 0 && !chain) {
+          // a walk over the chunk's fields (string columns far from the
+          // record start: fewer steps than the column-by-column masks)
+          bool abs = abs0;
+          uint32_t col = c0, term = T, seg0 = 0;
           for (;;) {
             const uint32_t j = term ? uint32_t(__ffs(term) - 1) : 32u;
             const uint32_t n = __popc(data & range_mask(seg0, j));
@@ -620,19 +639,68 @@ __global__ void __launch_bounds__(NT, 2) ctx_kernel(const __grid_constant__ Pars
             seg0 = j + 1;
             term &= term - 1;
           }
+        } else if (st[s] < 4 && same < 0) {  // (a shared state's fields are all absolute)
+          if (!abs0) {
+            // fields of the tile's first, partial record: relative column
+            // indices, up to this chunk's first record delimiter
+            uint32_t col = c0, term = T, seg0 = 0;
+            for (;;) {
+              const uint32_t j = term ? uint32_t(__ffs(term) - 1) : 32u;
+              const uint32_t n = __popc(data & range_mask(seg0, j));
+              if (n && col < n_cols) {
+                if (seg0 == 0) { k0 = col; n0 = n; }
+                else atomicAdd(&S.rel[s][col], n);
+              }
+              if (j == 32 || ((gs.rd >> j) & 1u)) break;
+              col = col < 0x7FFFFF00u ? col + 1 : col;
+              seg0 = j + 1;
+              term &= term - 1;
+            }
+          }
+          // absolute columns, one column at a time: S holds the starts of
+          // the column's runs; T - S sets each run from its start up to its
+          // terminator (exclusive) and clears that terminator, so the
+          // terminators left out of T - S end the column's runs, and those
+          // that are field delimiters start the next column's runs
+          uint32_t Sc = (gs.rd << 1) | (abs0 && c0 == 0 ? 1u : 0u);
+          int si = 0;
+          for (uint32_t c = 0; c <= cmax; ++c) {
+            const uint32_t X = T - Sc;
+            if ((strmask >> c) & 1u) {
+              const uint32_t n = __popc(X & data);
+              if (n) add16(cnt, si, n);
+              ++si;
+            }
+            Sc = ((T & ~X & gs.fd) << 1) | (abs0 && c0 == c + 1 ? 1u : 0u);
+          }
         }
-        // relative first segments: one shared atomic per (warp, field index)
-        const uint32_t grp = __match_any_sync(FULL, k0);
-        const uint32_t sum = __reduce_add_sync(grp, n0);
-        if (k0 != 0xFFFFFFFFu && (grp & ((1u << lane) - 1)) == 0 && sum) atomicAdd(&S.rel[s][k0], sum);
+        // relative first segments (only the chunks before the tile's first
+        // record delimiter have them): one shared atomic per field index
+        if (__any_sync(FULL, k0 != 0xFFFFFFFFu)) {
+          const uint32_t k00 = __shfl_sync(FULL, k0, 0);
+          if (__all_sync(FULL, k0 == k00)) {  // the whole warp inside one field
+            const uint32_t sum = __reduce_add_sync(FULL, n0);
+            if (lane == 0 && sum) atomicAdd(&S.rel[s][k00], sum);
+          } else if (k0 != 0xFFFFFFFFu && n0) {
+            atomicAdd(&S.rel[s][k0], n0);
+          }
+        }
         // warp sums of the packed counters
         if (same < 0) {
+          bool any = false;
 #pragma unroll
-          for (int k = 0; k < NSW; ++k) {
-            uint64_t v = cnt[k];
+          for (int k = 0; k < NSW; ++k) any |= cnt[k] != 0;
+          if (__any_sync(FULL, any)) {
 #pragma unroll
-            for (int d = 16; d; d >>= 1) v += __shfl_xor_sync(FULL, v, d);
-            if (lane == 0) S.wcnt[warp][s][k] = v;
+            for (int k = 0; k < NSW; ++k) {
+              uint64_t v = cnt[k];
+#pragma unroll
+              for (int d = 16; d; d >>= 1) v += __shfl_xor_sync(FULL, v, d);
+              if (lane == 0) S.wcnt[warp][s][k] = v;
+            }
+          } else if (lane == 0) {
+#pragma unroll
+            for (int k = 0; k < NSW; ++k) S.wcnt[warp][s][k] = 0;
           }
         } else if (lane == 0) {
 #pragma unroll
@@ -980,7 +1048,7 @@ __global__ void __launch_bounds__(SCAN_NT) scan_kernel(const __grid_constant__ P
 // Numeric field whose bytes are not all in the tile, contain control bytes
 // or need the full grammar: streaming accumulators over the value bytes.
 // Returns the error bits; *out receives the value (0 for an empty field).
-__device__ __noinline__ int convert_general(const ParseParams& P, uint32_t ty, uint64_t fs,
+__device__ __forceinline__ int convert_general(const ParseParams& P, uint32_t ty, uint64_t fs,
                                             uint64_t fe, uint64_t tile_base,
                                             const uint8_t* tile_s, const uint32_t* ctrl_s,
                                             const uint32_t* my_lut, uint32_t fstate,
@@ -1008,82 +1076,71 @@ __device__ __noinline__ int convert_general(const ParseParams& P, uint32_t ty, u
 
 // Convert the numeric field in slot value v (tile-relative start << 16 |
 // end; start 0xFFFF = the field began in an earlier tile; SLOT_DEFAULT = a
-// missing field) and store it at row `rec` of column c of type ty.
-// Plain fields inside the tile take word-parallel fast paths: an integer
-// of at most 16 digits, or a decimal of at most 8 characters after the
-// sign converted by short_decimal_to_binary64; everything else streams
-// through the accumulators.
-__device__ __forceinline__ void convert_num(const ParseParams& P, uint32_t c, uint32_t ty,
-                                            uint32_t v, uint64_t rec, uint64_t tile_base,
-                                            uint64_t tile_fstart, uint32_t tile_fstate,
-                                            const uint8_t* tile_s, const uint32_t* tile_w,
-                                            const uint32_t* ctrl_s, const uint16_t* cpre,
-                                            const uint32_t* my_lut, bool any_ctrl) {
-  uint64_t val = 0;
-  int err = 0;
-  uint64_t fs = 0;
-  if (v != SLOT_DEFAULT) {
-    const uint32_t fsr = v >> 16, fe = v & 0xFFFFu;
-    fs = fsr == 0xFFFFu ? tile_fstart : tile_base + fsr;
-    bool done = false;
-    if (fsr != 0xFFFFu && (!any_ctrl || ctrl_before(ctrl_s, cpre, fe) == ctrl_before(ctrl_s, cpre, fsr))) {
-      const uint32_t L = fe - fsr;
-      if (L == 0) {
-        done = true;  // empty field: the column default
-      } else {
-        uint64_t x = tile_load8(tile_w, fsr);
-        const uint32_t c0 = uint32_t(x) & 0xFFu;
-        const bool neg = c0 == '-';
-        const uint32_t sg = (c0 == '-' || c0 == '+') ? 1u : 0u;
-        const uint32_t n = L - sg;
-        if (sg) x = (x >> 8) | (uint64_t(tile_s[fsr + 8]) << 56);
-        if (ty == PP_COL_FLOAT64) {
-          uint64_t mant;
-          int q;
-          if (n >= 1 && n <= 8 && fast_float_x(x, n, mant, q)) {
-            val = (mant ? ppn::short_decimal_to_binary64(uint32_t(mant), q) : 0ull) |
-                  (neg ? (1ull << 63) : 0ull);
-            done = true;
-          }
-        } else {
-          uint64_t mag = 0;
-          bool ok = false;
-          if (n == 1) {
-            mag = (uint32_t(x) & 0xFFu) - 48u;
-            ok = mag <= 9;
-          } else if (n >= 2 && n <= 8) {
-            uint64_t d;
-            ok = swar_digits(x, n, d);
-            if (ok) mag = swar_value(d);
-          } else if (n > 8 && n <= 16) {
-            uint64_t d, d2;
-            ok = swar_digits(x, 8, d) && swar_digits(tile_load8(tile_w, fsr + sg + 8), n - 8, d2);
-            if (ok) {
-              uint64_t p10 = 1;
-              for (uint32_t i = 8; i < n; ++i) p10 *= 10;
-              mag = swar_value(d) * p10 + swar_value(d2);
-            }
-          }
-          if (ok) {
-            const uint64_t lim = ty == PP_COL_INT8 ? (neg ? 128ull : 127ull)
-                               : ty == PP_COL_INT32 ? (neg ? 2147483648ull : 2147483647ull)
-                               : (neg ? 9223372036854775808ull : 9223372036854775807ull);
-            if (mag > lim) err = PP_ERR_NUM_OVERFLOW;
-            else val = neg ? (~mag + 1) : mag;
-            done = true;
-          }
+// missing field) of a column of type ty; lim_pos / lim_neg bound integer
+// magnitudes.  Plain fields inside the tile take word-parallel fast paths:
+// an integer of at most 16 digits, or a decimal of at most 8 characters
+// after the sign converted by short_decimal_to_binary64; everything else
+// streams through the accumulators.  Returns the error bits; *val gets the
+// value's bits (0 for an empty field or an error).
+__device__ __forceinline__ int convert_num(const ParseParams& P, uint32_t ty, uint64_t lim_pos,
+                                           uint64_t lim_neg, uint32_t v, uint64_t tile_base,
+                                           uint64_t tile_fstart, uint32_t tile_fstate,
+                                           const uint8_t* tile_s, const uint32_t* tile_w,
+                                           const uint32_t* ctrl_s, const uint16_t* cpre,
+                                           const uint32_t* my_lut, bool any_ctrl, uint64_t& val) {
+  val = 0;
+  if (v == SLOT_DEFAULT) return 0;
+  const uint32_t fsr = v >> 16, fe = v & 0xFFFFu;
+  if (fsr != 0xFFFFu && (!any_ctrl || ctrl_before(ctrl_s, cpre, fe) == ctrl_before(ctrl_s, cpre, fsr))) {
+    const uint32_t L = fe - fsr;
+    if (L == 0) return 0;  // empty field: the column default
+    const uint64_t x = tile_load8(tile_w, fsr);
+    uint32_t x0 = uint32_t(x), x1 = uint32_t(x >> 32);
+    const uint32_t c0 = x0 & 0xFFu;
+    const bool neg = c0 == '-';
+    const uint32_t sg = (c0 == '-' || c0 == '+') ? 1u : 0u;
+    const int n = int(L - sg);
+    if (sg) {
+      x0 = __funnelshift_r(x0, x1, 8);
+      x1 = (x1 >> 8) | (uint32_t(tile_s[fsr + 8]) << 24);
+    }
+    if (ty == PP_COL_FLOAT64) {
+      uint32_t mant;
+      int q;
+      if (n >= 1 && n <= 8 && dec8(x0, x1, n, mant, q)) {
+        val = (mant ? ppn::short_decimal_to_binary64(mant, q) : 0ull) | (neg ? (1ull << 63) : 0ull);
+        return 0;
+      }
+    } else {
+      uint64_t mag = 0;
+      bool ok = false;
+      if (n == 1) {
+        mag = (x0 & 0xFFu) - 48u;
+        ok = mag <= 9;
+      } else if (n >= 2 && n <= 8) {
+        uint32_t w;
+        ok = digits8(x0 ^ 0x30303030u, x1 ^ 0x30303030u, n, w);
+        mag = w;
+      } else if (n > 8 && n <= 16) {
+        const uint64_t x2 = tile_load8(tile_w, fsr + sg + 8);
+        uint32_t vh, vl;
+        ok = digits8(x0 ^ 0x30303030u, x1 ^ 0x30303030u, 8, vh) &&
+             digits8(uint32_t(x2) ^ 0x30303030u, uint32_t(x2 >> 32) ^ 0x30303030u, n - 8, vl);
+        if (ok) {
+          uint32_t p10 = 1;
+          for (int i = 8; i < n; ++i) p10 *= 10u;
+          mag = uint64_t(vh) * p10 + vl;
         }
       }
+      if (ok) {
+        if (mag > (neg ? lim_neg : lim_pos)) return PP_ERR_NUM_OVERFLOW;
+        val = neg ? (~mag + 1) : mag;
+        return 0;
+      }
     }
-    if (!done)
-      err = convert_general(P, ty, fs, tile_base + fe, tile_base, tile_s, ctrl_s, my_lut,
-                            tile_fstate, &val);
   }
-  if (ty == PP_COL_FLOAT64) static_cast<uint64_t*>(P.typed[c])[rec] = val;
-  else if (ty == PP_COL_INT8) static_cast<int8_t*>(P.typed[c])[rec] = int8_t(val);
-  else if (ty == PP_COL_INT32) static_cast<int32_t*>(P.typed[c])[rec] = int32_t(val);
-  else static_cast<int64_t*>(P.typed[c])[rec] = int64_t(val);
-  if (err) report(P.st, err, fs, true);
+  return convert_general(P, ty, fsr == 0xFFFFu ? tile_fstart : tile_base + fsr, tile_base + fe,
+                         tile_base, tile_s, ctrl_s, my_lut, tile_fstate, &val);
 }
 
 // ================================================================ 3. main
@@ -1097,7 +1154,6 @@ struct MainShared {
   uint32_t warp_rec[NW], warp_col[NW], warp_last[NW];
   uint32_t rows;             // records touched by the tile (#RD + 1)
   uint32_t col_end;          // fields of the last row closed in the tile
-  uint32_t item;             // next numeric work item
   uint32_t wsum[NW];
   uint32_t cstart[ppi::MAX_STR_COLS + 1];  // staging start per string column (this pass)
   uint32_t carry[ppi::MAX_STR_COLS];       // chars of earlier passes per string column
@@ -1112,11 +1168,6 @@ constexpr size_t MAIN_SMEM = LUT_BYTES + 2 * TILE + STAGE_BYTES + SLOT_CAP * 4 +
                              SLOT_CAP * 2 + sizeof(MainShared);
 
 
-// floor(x / d) for x * d < 2^32 (the magic number is ceil(2^32 / d))
-__device__ __forceinline__ uint32_t div_magic(uint32_t d) { return 0xFFFFFFFFu / d + 1u; }
-__device__ __forceinline__ uint32_t div_by(uint32_t x, uint32_t d, uint32_t magic) {
-  return d == 1 ? x : __umulhi(x, magic);
-}
 
 template <int NS>
 __global__ void __launch_bounds__(NT, 2) main_kernel(const __grid_constant__ ParseParams P) {
@@ -1137,12 +1188,12 @@ __global__ void __launch_bounds__(NT, 2) main_kernel(const __grid_constant__ Par
     for (uint32_t c = 0; c < uint32_t(P.n_cols); ++c)
       if (P.coltype[c] != PP_COL_SKIP && P.coltype[c] != PP_COL_STRING) S.numcol[m++] = uint8_t(c);
     S.n_num = P.has_out ? m : 0u;
-    S.item = 0;
   }
   for (int k = t; k < ppi::MAX_STR_COLS; k += NT) S.carry[k] = 0;
   const uint32_t* my_lut = lut_s + lane;
   const uint32_t n_cols = uint32_t(P.n_cols);
   const uint32_t n_str = NS > 0 ? uint32_t(P.n_str) : 0u;
+  const uint32_t rpb = max(1u, uint32_t(SLOT_CAP) / n_cols);  // rows per pass
   const bool aligned_in = (reinterpret_cast<uintptr_t>(P.in) & 15) == 0;
   uint32_t* counter = &P.s.counters[1];
   feed_start(P, S.F, counter, aligned_in, lin0);
@@ -1264,7 +1315,6 @@ __global__ void __launch_bounds__(NT, 2) main_kernel(const __grid_constant__ Par
     }
 
     // ---- fields -> (column, row) slots, in passes of rows
-    const uint32_t rpb = max(1u, uint32_t(SLOT_CAP) / n_cols);
     {
       for (uint32_t lo = 0; lo < rows; lo += rpb) {
         const uint32_t hi = min(rows, lo + rpb), nr = hi - lo;
@@ -1308,7 +1358,6 @@ __global__ void __launch_bounds__(NT, 2) main_kernel(const __grid_constant__ Par
         }
         __syncthreads();
         const uint32_t ngr = (nr + 31) / 32;
-        const uint32_t mg = div_magic(ngr);
 
         if (NS > 0 && n_str) {
           // ---- string fields: value bytes -> chars positions (block scan
@@ -1404,12 +1453,11 @@ __global__ void __launch_bounds__(NT, 2) main_kernel(const __grid_constant__ Par
             }
           }
           {
-            const uint32_t mg_nr = div_magic(nr);
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               const uint32_t k = S.lk[h][t];
               if (k == NO_FIELD) continue;
-              const uint32_t ksi = div_by(k, nr, mg_nr);
+              const uint32_t ksi = k / nr;
               const uint32_t v = slot_s[P.strcol[ksi] * nr + (k - ksi * nr)];
               const uint32_t a0 = (v >> 16) == 0xFFFFu ? 0u : (v >> 16), e = v & 0xFFFFu;
               const uint32_t p0 = max(a0, cstart), p1 = min(e, cstart + clen);
@@ -1430,30 +1478,52 @@ __global__ void __launch_bounds__(NT, 2) main_kernel(const __grid_constant__ Par
         }
 
         // ---- numbers: a warp per 32 rows of one column
-        {
-          const uint32_t n_items = S.n_num * ngr;
-          for (;;) {
-            uint32_t it = 0;
-            if (lane == 0) it = atomicAdd(&S.item, 1u);
-            it = __shfl_sync(FULL, it, 0);
-            if (it >= n_items) break;
-            const uint32_t oc = div_by(it, ngr, mg);
-            const uint32_t r = lo + (it - oc * ngr) * 32 + lane;
+        {  // items (numeric column oc, group gi of 32 rows), warp-strided
+          const uint32_t n_num = S.n_num;
+          uint32_t oc = 0, gi = uint32_t(warp);
+          while (gi >= ngr && oc < n_num) { gi -= ngr; ++oc; }
+          while (oc < n_num) {
             const uint32_t c = S.numcol[oc];
-            if (r >= hi || (r == 0 && c < col_in) || (r + 1 == rows && c >= col_end)) continue;
-            const uint64_t rec = rec0 + r;
-            if (rec >= P.rec_cap) { report(P.st, PP_ERR_CAPACITY, 0, false); continue; }
-            convert_num(P, c, S.coltype[c], slot_s[c * nr + (r - lo)], rec, tile_base,
-                        tile_fstart, tile_fstate, tile_s, tile_w, ctrl_s, S.cpre, my_lut, any_ctrl);
+            const uint32_t ty = S.coltype[c];
+            uint8_t* const out = static_cast<uint8_t*>(P.typed[c]);
+            const uint64_t lim_pos = ty == PP_COL_INT8 ? 127ull : ty == PP_COL_INT32 ? 2147483647ull
+                                                                 : 9223372036854775807ull;
+            const uint32_t r_first = c < col_in ? 1u : 0u;       // rows whose field c closes here
+            const uint32_t r_end = c < col_end ? rows : rows - 1u;
+            const uint32_t* col_slots = slot_s + c * nr;
+            for (; gi < ngr; gi += NW) {
+              const uint32_t r = lo + gi * 32 + lane;
+              if (r >= hi || r < r_first || r >= r_end) continue;
+              const uint64_t rec = rec0 + r;
+              if (rec >= P.rec_cap) { report(P.st, PP_ERR_CAPACITY, 0, false); continue; }
+              const uint32_t v = col_slots[r - lo];
+              uint64_t val;
+              const int err = convert_num(P, ty, lim_pos, lim_pos + 1, v, tile_base, tile_fstart,
+                                          tile_fstate, tile_s, tile_w, ctrl_s, S.cpre, my_lut,
+                                          any_ctrl, val);
+              if (ty == PP_COL_FLOAT64) reinterpret_cast<uint64_t*>(out)[rec] = val;
+              else if (ty == PP_COL_INT32) reinterpret_cast<int32_t*>(out)[rec] = int32_t(val);
+              else if (ty == PP_COL_INT64) reinterpret_cast<int64_t*>(out)[rec] = int64_t(val);
+              else reinterpret_cast<int8_t*>(out)[rec] = int8_t(val);
+              if (err) {
+                const uint32_t fsr = v >> 16;
+                report(P.st, err, fsr == 0xFFFFu ? tile_fstart : tile_base + fsr, true);
+              }
+            }
+            gi -= ngr;
+            ++oc;
+            while (gi >= ngr && oc < n_num) { gi -= ngr; ++oc; }
           }
         }
         __syncthreads();
         if (NS > 0 && n_str && P.has_out) {
           // Arrow offsets of the string fields closed in this pass
-          const uint32_t n_items = n_str * ngr;
-          for (uint32_t it = warp; it < n_items; it += NW) {
-            const uint32_t si = div_by(it, ngr, mg);
-            const uint32_t r = lo + (it - si * ngr) * 32 + lane;
+          uint32_t si = 0, gi = uint32_t(warp);
+          while (gi >= ngr && si < n_str) { gi -= ngr; ++si; }
+          for (; si < n_str; gi += NW) {
+            while (gi >= ngr && si < n_str) { gi -= ngr; ++si; }
+            if (si >= n_str) break;
+            const uint32_t r = lo + gi * 32 + lane;
             const uint32_t c = P.strcol[si];
             if (r >= hi || (r == 0 && c < col_in) || (r + 1 == rows && c >= col_end)) continue;
             const uint64_t rec = rec0 + r;
@@ -1496,7 +1566,6 @@ __global__ void __launch_bounds__(NT, 2) main_kernel(const __grid_constant__ Par
         }
         __syncthreads();
         if (NS > 0 && t < int(n_str)) S.carry[t] += S.cstart[t + 1] - S.cstart[t];
-        if (t == 0) S.item = 0;
       }
     }
     __syncthreads();
