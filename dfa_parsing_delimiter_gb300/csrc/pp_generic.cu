@@ -17,7 +17,9 @@
 // scanned (second look-back, which also carries the position of the last
 // token start) so each start knows its token index; the start of token k
 // closes token k-1 (its length and, from the state before the start, its
-// id).
+// id).  The token pass steps the DFA through a per-group row held in
+// registers, and a tile's triples are staged in shared memory and written
+// with coalesced stores (tiles with more than TOK_CAP tokens write directly).
 #include <cstdint>
 #include <cuda_runtime.h>
 #include <algorithm>
@@ -102,6 +104,7 @@ struct SharedG {
   uint64_t pre[2];
   Stv16 warp_stv[NW];
   uint64_t lb2[2];
+  uint32_t tile_cnt;
   uint32_t warp_cnt[NW];
   uint32_t warp_last[NW];
   GroupOps ops[PP_MAX_GROUPS];
@@ -185,7 +188,16 @@ __device__ uint32_t resolve_start_state(const GParams& P, SharedG& S, const uint
                                         const LookbackCfg& cfg) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   Stv16 G = stv16_id();
-  for (int j = int(clen) - 1; j >= 0; --j) G = stv16_step(G, S.ops[S.grp[tile_s[cstart + j]]]);
+  if (clen == CB) {  // full chunk: unrolled, so every load is issued ahead of the chain
+    const uint4* src = reinterpret_cast<const uint4*>(tile_s + cstart);
+    const uint4 a = src[0], b = src[1];
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int j = CB - 1; j >= 0; --j)
+      G = stv16_step(G, S.ops[S.grp[(w[j >> 2] >> (8 * (j & 3))) & 0xFFu]]);
+  } else {
+    for (int j = int(clen) - 1; j >= 0; --j) G = stv16_step(G, S.ops[S.grp[tile_s[cstart + j]]]);
+  }
   Stv16 inc = G;
 #pragma unroll
   for (int d = 1; d < 32; d <<= 1) {
@@ -268,11 +280,53 @@ __global__ void __launch_bounds__(NT, 2) tags_kernel(const __grid_constant__ GPa
   }
 }
 
+// Per symbol group, the whole transition row for the token pass: next
+// state of every state (4-bit lanes, states 0-7 in lo, 8-15 in hi), the
+// states in which the group begins a token, and those in which it leads
+// into the invalid state.  The state chain then needs no memory access.
+struct TokRow { uint32_t lo, hi, begin, to_inv; };
+
+constexpr uint32_t TOK_CAP = 4096;  // tokens per tile staged for coalesced stores
+
+__device__ __forceinline__ uint32_t row_next(const TokRow& r, uint32_t s) {
+  return ((s < 8 ? r.lo : r.hi) >> (4 * (s & 7))) & 0xFu;
+}
+
+// id of a token from the state after its last byte (or, for 0xFE, from its
+// first byte)
+__device__ __forceinline__ uint32_t token_id_of(const GParams& P, const SharedG& S,
+                                                const uint8_t* tile_s, uint64_t tile_base,
+                                                uint32_t s_after, uint64_t start) {
+  uint32_t id = S.token_id[s_after];
+  if (id == 0xFEu) {
+    const uint32_t fb = start >= tile_base ? tile_s[start - tile_base] : __ldg(P.in + start);
+    id = S.byte_token_id[fb];
+  }
+  return id;
+}
+
 __global__ void __launch_bounds__(NT, 2) tokenize_kernel(const __grid_constant__ GParams P) {
-  __shared__ __align__(16) uint8_t tile_s[TILE];
+  extern __shared__ __align__(16) uint8_t dyn[];
+  uint8_t* tile_s = dyn;                                            // TILE
+  uint8_t* sc_s = dyn + TILE;                                       // [32][NT]: state before each start
+  uint16_t* start_s = reinterpret_cast<uint16_t*>(dyn + 2 * TILE);  // [TOK_CAP]
+  uint32_t* len_s = reinterpret_cast<uint32_t*>(start_s + TOK_CAP); // [TOK_CAP + 1]
+  uint8_t* id_s = reinterpret_cast<uint8_t*>(len_s + TOK_CAP + 1);  // [TOK_CAP + 1]
   __shared__ SharedG S;
+  __shared__ TokRow rows[PP_MAX_GROUPS];
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   setup_tables(P, S);
+  if (t < PP_MAX_GROUPS) {
+    TokRow r = {0u, 0u, 0u, 0u};
+    for (uint32_t st = 0; st < uint32_t(P.dfa.n_states); ++st) {
+      const uint32_t nx = P.dfa.delta[t][st] & 0xFu;
+      if (st < 8) r.lo |= nx << (4 * st);
+      else r.hi |= nx << (4 * (st - 8));
+      if (P.dfa.tag[st][t] == PP_TAG_BEGIN) r.begin |= 1u << st;
+      if (nx == P.dfa.invalid_state && st != P.dfa.invalid_state) r.to_inv |= 1u << st;
+    }
+    rows[t] = r;
+  }
   const LookbackCfg cfg{P.st, P.spin_limit};
   const uint32_t inv = P.dfa.invalid_state;
   for (;;) {
@@ -290,22 +344,36 @@ __global__ void __launch_bounds__(NT, 2) tokenize_kernel(const __grid_constant__
     const uint32_t clen = tile_len > cstart ? min(tile_len - cstart, uint32_t(CB)) : 0u;
     const uint32_t s0 = resolve_start_state(P, S, tile_s, tile, cstart, clen, cfg);
 
-    // tag pass: token starts and the state before each byte's start
-    uint32_t begin = 0, s = s0, last_start = 0;
-    for (uint32_t j = 0; j < clen; ++j) {
-      const uint32_t g = S.grp[tile_s[cstart + j]];
-      const uint32_t nx = S.delta[g * PP_MAX_STATES + s];
-      const bool b = S.tag[s * PP_MAX_GROUPS + g] == PP_TAG_BEGIN || (tile_base + cstart + j == 0);
-      if (b) { begin |= 1u << j; last_start = cstart + j + 1; }
-      if (nx == inv && s != inv) report(P.st, PP_ERR_INVALID_INPUT, tile_base + cstart + j, true);
-      s = nx;
+    // token starts of the chunk; the state before each is kept for its id
+    uint32_t begin = 0, s = s0, last_start = 0, nb = 0, inv_at = 32;
+    auto step = [&](uint32_t j, uint32_t byte) {
+      const TokRow r = rows[S.grp[byte]];
+      if (((r.begin >> s) & 1u) || (tile_base + cstart + j == 0)) {
+        begin |= 1u << j;
+        sc_s[nb * NT + t] = uint8_t(s);
+        ++nb;
+      }
+      if (((r.to_inv >> s) & 1u) && inv_at == 32) inv_at = j;
+      s = row_next(r, s);
+    };
+    if (clen == CB) {  // full chunk: unrolled, loads ahead of the state chain
+      const uint4* src = reinterpret_cast<const uint4*>(tile_s + cstart);
+      const uint4 a = src[0], b = src[1];
+      const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (uint32_t j = 0; j < CB; ++j) step(j, (w[j >> 2] >> (8 * (j & 3))) & 0xFFu);
+    } else {
+      for (uint32_t j = 0; j < clen; ++j) step(j, tile_s[cstart + j]);
     }
+    if (begin) last_start = cstart + (31u - __clz(begin)) + 1u;
+    if (inv_at < 32) report(P.st, PP_ERR_INVALID_INPUT, tile_base + cstart + inv_at, true);
+    const uint32_t s_end = s;
     const bool owns_end = last_tile && clen > 0 && cstart + clen == tile_len;
-    if (owns_end && s != inv && !((P.dfa.accept_mask >> s) & 1u))
+    if (owns_end && s_end != inv && !((P.dfa.accept_mask >> s_end) & 1u))
       report(P.st, PP_ERR_BAD_END_STATE, P.n, true);
 
     // token index scan: (count, last start pos+1)
-    uint32_t cnt = __popc(begin), ci = cnt, li = last_start;
+    uint32_t ci = nb, li = last_start;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
       const uint32_t oc = __shfl_up_sync(FULL, ci, d), ol = __shfl_up_sync(FULL, li, d);
@@ -329,6 +397,7 @@ __global__ void __launch_bounds__(NT, 2) tokenize_kernel(const __grid_constant__
       uint32_t ex_l = __shfl_up_sync(FULL, wl, 1);
       if (lane == 0) ex_l = 0;
       if (lane < NW) S.warp_last[lane] = ex_l;
+      if (lane == 0) S.tile_cnt = tc;
       const uint64_t a2[2] = {tc, tl ? tile_base + tl : 0ull};
       const uint64_t z[2] = {0ull, 0ull};
       uint64_t ex[2];
@@ -341,51 +410,73 @@ __global__ void __launch_bounds__(NT, 2) tokenize_kernel(const __grid_constant__
       if (lane == 0) { S.lb2[0] = ex[0]; S.lb2[1] = ex[1]; }
     }
     __syncthreads();
-    uint64_t k = S.lb2[0] + S.warp_cnt[warp] + lc;
-    // global position (+1) of the start of the token open at this chunk's start
-    uint64_t prev_start1;
+    const uint64_t k0 = S.lb2[0];                 // first token starting in this tile
+    const uint32_t c = S.tile_cnt;                // tokens starting in this tile
+    const uint32_t i0 = S.warp_cnt[warp] + lc;    // this chunk's first start, tile-local
+    uint64_t prev_start1;                         // start (+1) of the token open at the chunk start
     if (ll) prev_start1 = tile_base + ll;
     else if (S.warp_last[warp]) prev_start1 = tile_base + S.warp_last[warp];
     else prev_start1 = S.lb2[1];
+    const bool staged = c <= TOK_CAP;
+    const bool sizing = P.cap == 0 && P.out_start == nullptr;
 
-    // emit: each start closes the previous token
-    s = s0;
-    for (uint32_t j = 0; j < clen; ++j) {
-      const uint32_t byte = tile_s[cstart + j];
-      const uint32_t g = S.grp[byte];
-      const uint64_t pos = tile_base + cstart + j;
-      if ((begin >> j) & 1u) {
-        if (prev_start1) {  // close token k-1
+    // emit: each start opens token k0 + i and closes token k0 + i - 1
+    {
+      uint32_t m = begin, b = 0;
+      while (m) {
+        const uint32_t j = __ffs(m) - 1;
+        m &= m - 1;
+        const uint32_t i = i0 + b;
+        const uint64_t pos = tile_base + cstart + j;
+        const uint32_t sb = sc_s[b * NT + t];
+        ++b;
+        uint32_t id = 0, len = 0;
+        const bool closes = prev_start1 != 0;
+        if (closes) {
           const uint64_t ps = prev_start1 - 1;
-          if (k - 1 < P.cap) {
-            uint32_t id = S.token_id[s];
-            if (id == 0xFEu) {
-              const uint32_t fb = ps >= tile_base ? tile_s[ps - tile_base] : __ldg(P.in + ps);
-              id = S.byte_token_id[fb];
-            }
-            P.out_id[k - 1] = uint8_t(id);
-            P.out_len[k - 1] = uint32_t(pos - ps);
-          }
+          id = token_id_of(P, S, tile_s, tile_base, sb, ps);
+          len = uint32_t(pos - ps);
         }
-        if (k < P.cap) P.out_start[k] = pos;
-        else if (P.cap || P.out_start) report(P.st, PP_ERR_CAPACITY, 0, false);
-        ++k;
+        if (staged) {
+          start_s[i] = uint16_t(cstart + j);
+          len_s[i] = len;
+          id_s[i] = uint8_t(id);
+        } else {
+          const uint64_t k = k0 + i;
+          if (closes && k - 1 < P.cap) { P.out_id[k - 1] = uint8_t(id); P.out_len[k - 1] = len; }
+          if (k < P.cap) P.out_start[k] = pos;
+          else if (!sizing) report(P.st, PP_ERR_CAPACITY, 0, false);
+        }
         prev_start1 = pos + 1;
       }
-      s = S.delta[g * PP_MAX_STATES + s];
-    }
-    if (owns_end) {
-      if (prev_start1 && k - 1 < P.cap) {  // close the last token
-        const uint64_t ps = prev_start1 - 1;
-        uint32_t id = S.token_id[s];
-        if (id == 0xFEu) {
-          const uint32_t fb = ps >= tile_base ? tile_s[ps - tile_base] : __ldg(P.in + ps);
-          id = S.byte_token_id[fb];
+      if (owns_end) {  // close the last token
+        const uint64_t k = k0 + i0 + b;  // tokens in total
+        if (prev_start1) {
+          const uint64_t ps = prev_start1 - 1;
+          const uint32_t id = token_id_of(P, S, tile_s, tile_base, s_end, ps);
+          const uint32_t len = uint32_t(P.n - ps);
+          if (staged) { len_s[c] = len; id_s[c] = uint8_t(id); }
+          else if (k - 1 < P.cap) { P.out_id[k - 1] = uint8_t(id); P.out_len[k - 1] = len; }
         }
-        P.out_id[k - 1] = uint8_t(id);
-        P.out_len[k - 1] = uint32_t(P.n - ps);
+        P.st->n_tokens = k;
       }
-      P.st->n_tokens = k;
+    }
+    if (staged) {
+      __syncthreads();
+      // starts of tokens k0 .. k0+c-1; ids and lengths of tokens k0-1 .. k0+c-2
+      // (and k0+c-1 in the last tile)
+      const uint32_t nclose = c + (last_tile ? 1u : 0u);
+      for (uint32_t i = t; i < nclose; i += NT) {
+        const uint64_t k = k0 + i;
+        if (i < c) {
+          if (k < P.cap) P.out_start[k] = tile_base + start_s[i];
+          else if (!sizing) report(P.st, PP_ERR_CAPACITY, 0, false);
+        }
+        if (k >= 1 && k - 1 < P.cap) {  // token k-1 exists (the first start closes none)
+          P.out_len[k - 1] = len_s[i];
+          P.out_id[k - 1] = id_s[i];
+        }
+      }
     }
   }
 }
@@ -515,7 +606,7 @@ cudaError_t launch_tokenize(const uint8_t* in, uint64_t n, const GenericDfa& dfa
   P.cap = cap;
   P.st = st;
   carve(scratch, P.n_tiles, P);
-  return run(tokenize_kernel, 0, P, scratch, stream);
+  return run(tokenize_kernel, 2 * TILE + TOK_CAP * 2 + (TOK_CAP + 1) * 5, P, scratch, stream);
 }
 
 cudaError_t launch_count_byte(const uint8_t* in, uint64_t n, uint8_t value, uint64_t* d_count,

@@ -297,6 +297,16 @@ def test_tokenize_random_including_invalid():
         compare_tokens(bytes(rng.choice(b' {"\\-+01.exa]:,E\t') for _ in range(n)))
 
 
+def test_tokenize_dense_and_long_tokens():
+    """Tiles with more tokens than are staged (a token per byte) and tokens
+    spanning several tiles (long strings and whitespace runs)."""
+    compare_tokens(b"1," * (3 * TILE // 2 + 7))
+    compare_tokens(b"[" * (2 * TILE + 5) + b"]" * (2 * TILE + 5))
+    long_str = b'"' + (b"ab" + b"\\" + b'"' + b"cd") * (TILE // 3) + b'"'  # escaped quotes
+    compare_tokens(b"[" + long_str + b", 12, " + long_str + b"]")
+    compare_tokens(b" " * (3 * TILE + 11) + b"1")
+
+
 def test_tokenize_capacity():
     data, info, _ = datagen.generate("json_2gib", target=3 * TILE)
     d_in = to_dev(data)
