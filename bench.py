@@ -60,7 +60,8 @@ def _traffic(workload):
     e = d.get(workload)
     if not e:
         return None
-    src = os.path.join(ROOT, "dfa_parsing_delimiter_gb300", "csrc", "pp_parse.cu")
+    src = os.path.join(ROOT, "dfa_parsing_delimiter_gb300", "csrc",
+                       e.get("kernel_source", "pp_parse.cu"))
     with open(src, "rb") as f:
         h = hashlib.sha256(f.read()).hexdigest()[:16]
     if e.get("kernel_source_sha256_prefix") != h:
@@ -276,7 +277,7 @@ def run_ours(args):
 
         def step():
             pp.pp_tokenize(d_in, n, desc, ids, starts, lens, T, status, stream)
-        launches_per_step = 2  # init, tokenize
+        launches_per_step = 6  # init, stv, state scan, count, count scan, emit
 
     for _ in range(args.warmup):
         step()
@@ -293,8 +294,8 @@ def run_ours(args):
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
-    if csv:  # per-kernel CUDA events of every timed call, on the launching stream
-        pp.debug_stage_timing(args.steps)
+    # per-kernel CUDA events of every timed call, on the launching stream
+    pp.debug_stage_timing(args.steps)
     with Clocks(local) as clk:
         _barrier(ws)
         torch.cuda.synchronize()
@@ -312,15 +313,14 @@ def run_ours(args):
     value = n * ws * args.steps / (tot_ms / 1e3) / 1e9
     peak, peak_src = _peaks()
     path_s = float(np.mean(step_ms)) / 1e3
-    stages = None
-    if csv:
-        st_ms = pp.debug_stage_ms(args.steps)
-        pp.debug_stage_timing(0)
-        stages = {k: float(st_ms[:, i].mean()) for i, k in
-                  enumerate(["init", "ctx_kernel", "scan_kernel", "main_kernel"])}
-        kern_s = stages["main_kernel"] / 1e3
-    else:
-        kern_s = path_s
+    st_ms = pp.debug_stage_ms(args.steps)
+    pp.debug_stage_timing(0)
+    names = (["init", "ctx_kernel", "scan_kernel", "main_kernel"] if csv else
+             ["init", "tok_stv_kernel", "tok_state_scan_kernel", "tok_count_kernel",
+              "tok_count_scan_kernel", "tok_emit_kernel"])
+    stages = {k: float(st_ms[:, i].mean()) for i, k in enumerate(names)}
+    kernel = "main_kernel" if csv else "tok_emit_kernel"
+    kern_s = stages[kernel] / 1e3
     # the dominant kernel reads the input once and writes every output
     achieved = (n + out_bytes) / kern_s / 1e9
 
@@ -360,7 +360,7 @@ def run_ours(args):
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": peak_src,
                      "algorithmic_bytes_per_launch": n + out_bytes,
-                     "kernel": "main_kernel" if csv else "tokenize_kernel",
+                     "kernel": kernel,
                      "timing": "CUDA events around the kernel on the launching stream, "
                                "every timed step"},
         "path": {"achieved_gbs": (n + out_bytes) / path_s / 1e9,

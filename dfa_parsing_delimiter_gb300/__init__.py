@@ -130,17 +130,21 @@ def debug_set_withhold(on: bool) -> None:
     lib().pp_debug_set_withhold(1 if on else 0)
 
 
+STAGES = 6  # PP_STAGES
+
+
 def debug_stage_timing(n_calls: int) -> None:
-    """Record per-kernel CUDA events for the next n_calls pp_parse calls
-    (0: stop).  Benchmark hook."""
+    """Record per-kernel CUDA events for the next n_calls pp_parse or
+    pp_tokenize calls (0: stop).  Benchmark hook."""
     _check(lib().pp_debug_stage_timing(int(n_calls)), "pp_debug_stage_timing")
 
 
 def debug_stage_ms(max_calls: int):
-    """Per-call kernel durations (ms) recorded since debug_stage_timing:
-    rows of (init, context, scan, main)."""
+    """Per-call kernel durations (ms) recorded since debug_stage_timing, one
+    row of STAGES per call: pp_parse (init, context, scan, main, 0, 0),
+    pp_tokenize (init, stv, state scan, count, count scan, emit)."""
     import numpy as np
-    out = np.zeros((max(int(max_calls), 1), 4), dtype=np.float32)
+    out = np.zeros((max(int(max_calls), 1), STAGES), dtype=np.float32)
     n = lib().pp_debug_stage_ms(out.ctypes.data, int(max_calls))
     if n < 0:
         raise RuntimeError("pp_debug_stage_ms failed")

@@ -13,9 +13,11 @@ namespace ppi {
 uint32_t g_spin_limit = 1u << 22;  // ~1 s of polling before a look-back gives up
 uint32_t g_withhold = 0;           // test hook, see pp_debug_set_withhold
 
-// Stage timing for benchmarks: events of the recorded calls, 5 per call.
-constexpr int STAGE_EVENTS = 5;
+// Stage timing for benchmarks: events of the recorded calls, up to
+// PP_STAGES + 1 per call, and how many of them each call recorded.
+constexpr int STAGE_EVENTS = PP_STAGES + 1;
 cudaEvent_t* g_stage_ev = nullptr;
+int* g_stage_n = nullptr;
 int g_stage_cap = 0, g_stage_used = 0, g_stage_cur = -1;
 
 bool stage_begin() {
@@ -23,7 +25,9 @@ bool stage_begin() {
   return g_stage_cur >= 0;
 }
 void stage_mark(int k, cudaStream_t stream) {
-  if (g_stage_cur >= 0) cudaEventRecord(g_stage_ev[g_stage_cur * STAGE_EVENTS + k], stream);
+  if (g_stage_cur < 0 || k >= STAGE_EVENTS) return;
+  cudaEventRecord(g_stage_ev[g_stage_cur * STAGE_EVENTS + k], stream);
+  if (k + 1 > g_stage_n[g_stage_cur]) g_stage_n[g_stage_cur] = k + 1;
 }
 }
 
@@ -424,16 +428,21 @@ pp_rc pp_debug_stage_timing(int n_calls) {
   using namespace ppi;
   for (int i = 0; i < g_stage_cap * STAGE_EVENTS; ++i) cudaEventDestroy(g_stage_ev[i]);
   delete[] g_stage_ev;
+  delete[] g_stage_n;
   g_stage_ev = nullptr;
+  g_stage_n = nullptr;
   g_stage_cap = g_stage_used = 0;
   g_stage_cur = -1;
   if (n_calls <= 0) return PP_OK;
+  g_stage_n = new int[n_calls]();
   g_stage_ev = new cudaEvent_t[size_t(n_calls) * STAGE_EVENTS];
   for (int i = 0; i < n_calls * STAGE_EVENTS; ++i) {
     if (cudaEventCreate(&g_stage_ev[i]) != cudaSuccess) {
       for (int j = 0; j < i; ++j) cudaEventDestroy(g_stage_ev[j]);
       delete[] g_stage_ev;
+      delete[] g_stage_n;
       g_stage_ev = nullptr;
+      g_stage_n = nullptr;
       return PP_ECUDA;
     }
   }
@@ -446,9 +455,12 @@ int pp_debug_stage_ms(float* out, int max_calls) {
   const int n = g_stage_used < max_calls ? g_stage_used : max_calls;
   for (int i = 0; i < n; ++i) {
     cudaEvent_t* e = g_stage_ev + i * STAGE_EVENTS;
-    if (cudaEventSynchronize(e[STAGE_EVENTS - 1]) != cudaSuccess) return -1;
-    for (int k = 0; k + 1 < STAGE_EVENTS; ++k)
-      if (cudaEventElapsedTime(&out[4 * i + k], e[k], e[k + 1]) != cudaSuccess) return -1;
+    const int marks = g_stage_n[i];
+    for (int k = 0; k < PP_STAGES; ++k) out[PP_STAGES * i + k] = 0.f;
+    if (marks < 2) continue;
+    if (cudaEventSynchronize(e[marks - 1]) != cudaSuccess) return -1;
+    for (int k = 0; k + 1 < marks; ++k)
+      if (cudaEventElapsedTime(&out[PP_STAGES * i + k], e[k], e[k + 1]) != cudaSuccess) return -1;
   }
   return n;
 }

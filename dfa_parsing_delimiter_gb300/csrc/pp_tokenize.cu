@@ -1,0 +1,660 @@
+// pp_tokenize on sm_103a: token triples (id, start, length) from a general
+// DFA with up to 16 states, in five passes that never wait on one another
+// inside a kernel's byte loop.
+//
+// The input is cut into pieces of 2 KiB, one per warp, 64 bytes per lane.
+//   1. stv    Per lane, the state-transition vector of its 64 bytes
+//             (ParPaRaw Section 3.1, Figure 2), built back to front two bytes
+//             at a time from a table of composed byte-pair transitions; a
+//             warp scan gives each lane the vector of the bytes before it in
+//             the piece, and lane 31 the piece's vector.
+//   2. scan   Exclusive composite scan of the piece vectors (decoupled
+//             look-back over tiles of 4096 pieces); applied to the DFA's
+//             start state it gives the state at every piece start.
+//   3. count  Each lane re-runs one DFA from its true start state and counts
+//             its token starts ("Lexing on the GPU: the scan is the easy
+//             part", section "A lexer is a prefix scan": a token starts at
+//             byte 0 and wherever a transition is tagged as a token begin).
+//   4. scan   Exclusive scan of (token count, position of the last token
+//             start) over pieces: the index of every piece's first token and
+//             the start of the token open at the piece start.
+//   5. emit   The DFA runs again and every token start k writes start[k] and
+//             closes token k-1 (its length, and its id from the state before
+//             the start).  A piece's triples are staged in shared memory and
+//             written with coalesced stores.
+// The byte passes read the input straight from HBM with 16-byte loads; all
+// per-byte lookups are one-byte tables in shared memory.
+#include <algorithm>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "pp.h"
+#include "pp_device.cuh"
+#include "pp_internal.h"
+#include "pp_stv16.cuh"
+
+namespace {
+using namespace ppd;
+using ppi::GenericDfa;
+
+constexpr int CB = 64;                   // bytes per lane
+constexpr int PIECE = 32 * CB;           // bytes per warp
+constexpr int WT = 256;                  // threads per block, byte passes
+constexpr int WW = WT / 32;
+constexpr int SCAN_T = 256, SCAN_E = 16; // scan passes: pieces per thread
+constexpr int SCAN_TILE = SCAN_T * SCAN_E;
+constexpr uint32_t CAPW = 512;           // tokens per piece staged for coalesced stores
+
+// transition-table entry bits (count and emit passes)
+constexpr uint32_t T_BEGIN = 0x10u, T_INV = 0x20u;
+
+struct TokParams {
+  const uint8_t* in;
+  uint64_t n;
+  uint32_t n_pieces;
+  uint32_t spin_limit;
+  bool aligned;  // in is 16-byte aligned
+  GenericDfa dfa;
+  uint8_t* out_id;
+  uint64_t* out_start;
+  uint32_t* out_len;
+  uint64_t cap;
+  pp_status* st;
+  // scratch
+  uint32_t* tickets;      // [0] state scan, [1] count scan
+  uint32_t* flag_s;       // look-back, state scan
+  uint64_t* agg_s;
+  uint64_t* inc_s;
+  uint32_t* flag_c;       // look-back, count scan
+  uint64_t* agg_c;
+  uint64_t* inc_c;
+  uint64_t* lane_pre;     // [pieces * 32] vector of the piece's bytes before the lane (nibbles)
+  uint64_t* piece_stv;    // [pieces] vector of the piece (nibbles)
+  uint8_t* piece_state;   // [pieces] state at the piece start
+  uint32_t* lane_info;    // [pieces * 32] start state | starts << 4 | (last start + 1) << 11
+  uint32_t* piece_cnt;    // [pieces] token starts in the piece
+  uint32_t* piece_last;   // [pieces] offset + 1 of the piece's last token start (0: none)
+  uint64_t* piece_k0;     // [pieces] index of the piece's first token start
+  uint64_t* piece_prev;   // [pieces] start + 1 of the token open at the piece start (0: none)
+};
+
+// ------------------------------------------------------------ input
+// The lane's 64 bytes as 16 little-endian words (zero past clen).
+__device__ __forceinline__ void load_chunk(const TokParams& P, uint64_t c0, uint32_t clen,
+                                           uint32_t (&w)[16]) {
+  if (clen == CB && P.aligned) {
+    const uint4* src = reinterpret_cast<const uint4*>(P.in + c0);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 v = __ldg(src + q);
+      w[4 * q] = v.x; w[4 * q + 1] = v.y; w[4 * q + 2] = v.z; w[4 * q + 3] = v.w;
+    }
+  } else {
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      uint32_t x = 0;
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (uint32_t(4 * q + k) < clen) x |= uint32_t(__ldg(P.in + c0 + 4 * q + k)) << (8 * k);
+      w[q] = x;
+    }
+  }
+}
+__device__ __forceinline__ uint32_t byte_of(const uint32_t (&w)[16], int j) {
+  return (w[j >> 2] >> (8 * (j & 3))) & 0xFFu;
+}
+__device__ __forceinline__ uint32_t chunk_len(uint64_t c0, uint64_t n) {
+  return c0 < n ? uint32_t(min(uint64_t(CB), n - c0)) : 0u;
+}
+
+// ------------------------------------------------------------ pass 1
+// pair_s[g1 * 16 + g2]: selectors of s -> delta_g2(delta_g1(s)) for the
+// two-byte step G'(s) = G(D(s)): word x holds states 0-7 (4 bits each), y
+// states 8-15.  single_s[g]: the same for one byte.
+struct StvTables {
+  uint8_t grp16[256];  // group * 16
+  uint8_t grp[256];
+  uint2 pair[256];
+  uint2 single[PP_MAX_GROUPS];
+};
+
+__device__ __forceinline__ Stv16 stv_step(const Stv16& G, uint2 e) {
+  const uint32_t xx = e.x ^ 0x88888888u, xy = e.y ^ 0x88888888u;
+  Stv16 r;
+  r.w[0] = stv16_gather(G, e.x, xx);
+  r.w[1] = stv16_gather(G, e.x >> 16, xx >> 16);
+  r.w[2] = stv16_gather(G, e.y, xy);
+  r.w[3] = stv16_gather(G, e.y >> 16, xy >> 16);
+  return r;
+}
+
+__global__ void __launch_bounds__(WT, 4) tok_stv_kernel(const __grid_constant__ TokParams P) {
+  __shared__ StvTables S;
+  const int t = threadIdx.x, lane = t & 31;
+  for (int k = t; k < 256; k += WT) {
+    const uint32_t g = P.dfa.byte_to_group[k] & 0xFu;
+    S.grp[k] = uint8_t(g);
+    S.grp16[k] = uint8_t(g << 4);
+    const uint32_t g1 = uint32_t(k) >> 4, g2 = uint32_t(k) & 0xFu;
+    uint32_t x = 0, y = 0;
+    for (uint32_t s = 0; s < 16; ++s) {
+      const uint32_t d = P.dfa.delta[g2][P.dfa.delta[g1][s] & 0xFu] & 0xFu;
+      if (s < 8) x |= d << (4 * s);
+      else y |= d << (4 * (s - 8));
+    }
+    S.pair[k] = make_uint2(x, y);
+    if (k < PP_MAX_GROUPS) {
+      x = y = 0;
+      for (uint32_t s = 0; s < 16; ++s) {
+        const uint32_t d = P.dfa.delta[k][s] & 0xFu;
+        if (s < 8) x |= d << (4 * s);
+        else y |= d << (4 * (s - 8));
+      }
+      S.single[k] = make_uint2(x, y);
+    }
+  }
+  __syncthreads();
+  const uint32_t n_warps = gridDim.x * WW;
+  for (uint32_t p = blockIdx.x * WW + (t >> 5); p < P.n_pieces; p += n_warps) {
+    const uint64_t c0 = uint64_t(p) * PIECE + uint64_t(lane) * CB;
+    const uint32_t clen = chunk_len(c0, P.n);
+    uint32_t w[16];
+    load_chunk(P, c0, clen, w);
+    Stv16 G = stv16_id();
+    if (clen == CB) {
+#pragma unroll
+      for (int j = CB - 2; j >= 0; j -= 2)
+        G = stv_step(G, S.pair[S.grp16[byte_of(w, j)] | S.grp[byte_of(w, j + 1)]]);
+    } else {
+      for (int j = int(clen) - 1; j >= 0; --j) G = stv_step(G, S.single[S.grp[P.in[c0 + j]]]);
+    }
+    Stv16 inc = G;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const Stv16 o = shfl_up16(inc, d);
+      if (lane >= d) inc = stv16_compose(o, inc);
+    }
+    Stv16 ex = shfl_up16(inc, 1);
+    if (lane == 0) ex = stv16_id();
+    P.lane_pre[size_t(p) * 32 + lane] = stv16_pack(ex);
+    if (lane == 31) P.piece_stv[p] = stv16_pack(inc);
+  }
+}
+
+// ------------------------------------------------------------ pass 2
+__global__ void __launch_bounds__(SCAN_T) tok_state_scan_kernel(const __grid_constant__ TokParams P) {
+  __shared__ uint32_t tile_s;
+  __shared__ Stv16 wv[SCAN_T / 32];
+  __shared__ uint64_t pre_s[2];
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  if (t == 0) tile_s = atomicAdd(&P.tickets[0], 1u);
+  __syncthreads();
+  const uint32_t tile = tile_s;
+  const uint64_t e0 = uint64_t(tile) * SCAN_TILE + uint64_t(t) * SCAN_E;
+  uint64_t v[SCAN_E];
+#pragma unroll
+  for (int e = 0; e < SCAN_E; ++e) v[e] = e0 + e < P.n_pieces ? P.piece_stv[e0 + e] : 0ull;
+  Stv16 acc = stv16_id();
+#pragma unroll
+  for (int e = 0; e < SCAN_E; ++e)
+    if (e0 + e < P.n_pieces) acc = stv16_compose(acc, stv16_unpack(v[e]));
+  Stv16 inc = acc;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const Stv16 o = shfl_up16(inc, d);
+    if (lane >= d) inc = stv16_compose(o, inc);
+  }
+  Stv16 lex = shfl_up16(inc, 1);
+  if (lane == 0) lex = stv16_id();
+  if (lane == 31) wv[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    constexpr int NWS = SCAN_T / 32;
+    Stv16 wi = lane < NWS ? wv[lane] : stv16_id();
+#pragma unroll
+    for (int d = 1; d < NWS; d <<= 1) {
+      const Stv16 o = shfl_up16(wi, d);
+      if (lane >= d) wi = stv16_compose(o, wi);
+    }
+    Stv16 wex = shfl_up16(wi, 1);
+    if (lane == 0) wex = stv16_id();
+    Stv16 agg;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) agg.w[k] = __shfl_sync(FULL, wi.w[k], NWS - 1);
+    __syncwarp();
+    if (lane < NWS) wv[lane] = wex;
+    uint64_t a2[2], id2[2], ex2[2];
+    stv16_to2(agg, a2);
+    stv16_to2(stv16_id(), id2);
+    lookback_vec<2>(P.flag_s, P.agg_s, P.inc_s, tile, a2, id2, id2, Stv16ComposeOp{},
+                    LookbackCfg{P.st, P.spin_limit}, ex2);
+    if (lane == 0) { pre_s[0] = ex2[0]; pre_s[1] = ex2[1]; }
+  }
+  __syncthreads();
+  const uint64_t pre2[2] = {pre_s[0], pre_s[1]};
+  uint32_t s = stv16_apply(stv16_from2(pre2), P.dfa.start_state);
+  s = stv16_apply(wv[warp], s);
+  s = stv16_apply(lex, s);
+#pragma unroll
+  for (int e = 0; e < SCAN_E; ++e) {
+    if (e0 + e < P.n_pieces) {
+      P.piece_state[e0 + e] = uint8_t(s);
+      s = nib_apply(v[e], s);
+    }
+  }
+}
+
+// ------------------------------------------------------------ passes 3, 5
+// trans_s[g * 16 + s] = next state | T_BEGIN | T_INV (a transition into the
+// invalid state from another state).
+struct DfaTables {
+  uint8_t grp16[256];
+  uint8_t trans[256];
+  uint8_t token_id[PP_MAX_STATES];
+  uint8_t byte_token_id[256];
+};
+
+__device__ void build_dfa_tables(const TokParams& P, DfaTables& S) {
+  const int t = threadIdx.x;
+  const uint32_t inv = P.dfa.invalid_state;
+  for (int k = t; k < 256; k += blockDim.x) {
+    S.grp16[k] = uint8_t((P.dfa.byte_to_group[k] & 0xFu) << 4);
+    const uint32_t g = uint32_t(k) >> 4, s = uint32_t(k) & 0xFu;
+    const uint32_t nx = P.dfa.delta[g][s] & 0xFu;
+    uint32_t e = nx;
+    if (P.dfa.tag[s][g] == PP_TAG_BEGIN) e |= T_BEGIN;
+    if (nx == inv && s != inv) e |= T_INV;
+    S.trans[k] = uint8_t(e);
+    S.byte_token_id[k] = P.dfa.byte_token_id[k];
+  }
+  if (t < PP_MAX_STATES) S.token_id[t] = P.dfa.token_id[t];
+}
+
+// One DFA over 32 bytes of the chunk (half h): begin mask, and (when
+// STATES) the state before every byte as nibbles in sn[4].  Bytes at or
+// past clen leave the state and the mask alone (PARTIAL only).
+template <bool PARTIAL, bool STATES>
+__device__ __forceinline__ uint32_t dfa_half(const DfaTables& S, const uint32_t (&w)[16], int h,
+                                             uint32_t clen, uint32_t& s, uint32_t& any,
+                                             uint32_t (&sn)[4]) {
+  uint32_t m = 0;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const int jj = 32 * h + j;
+    if (PARTIAL && uint32_t(jj) >= clen) break;
+    if (STATES) sn[j >> 3] |= s << (4 * (j & 7));
+    const uint32_t v = S.trans[S.grp16[byte_of(w, jj)] | s];
+    m |= ((v >> 4) & 1u) << j;
+    any |= v;
+    s = v & 0xFu;
+  }
+  return m;
+}
+
+// first invalid transition of the chunk (slow path: only when one exists)
+__device__ uint32_t first_invalid(const TokParams& P, const DfaTables& S, uint64_t c0,
+                                  uint32_t clen, uint32_t s) {
+  for (uint32_t j = 0; j < clen; ++j) {
+    const uint32_t v = S.trans[S.grp16[P.in[c0 + j]] | s];
+    if (v & T_INV) return j;
+    s = v & 0xFu;
+  }
+  return clen;
+}
+
+__global__ void __launch_bounds__(WT, 4) tok_count_kernel(const __grid_constant__ TokParams P) {
+  __shared__ DfaTables S;
+  build_dfa_tables(P, S);
+  __syncthreads();
+  const int t = threadIdx.x, lane = t & 31;
+  const uint32_t inv = P.dfa.invalid_state;
+  const uint32_t n_warps = gridDim.x * WW;
+  for (uint32_t p = blockIdx.x * WW + (t >> 5); p < P.n_pieces; p += n_warps) {
+    const uint64_t c0 = uint64_t(p) * PIECE + uint64_t(lane) * CB;
+    const uint32_t clen = chunk_len(c0, P.n);
+    const uint32_t s0 = nib_apply(P.lane_pre[size_t(p) * 32 + lane], P.piece_state[p]);
+    uint32_t w[16];
+    load_chunk(P, c0, clen, w);
+    uint32_t s = s0, any = 0, sn[4];
+    uint32_t m0, m1;
+    if (clen == CB) {
+      m0 = dfa_half<false, false>(S, w, 0, clen, s, any, sn);
+      m1 = dfa_half<false, false>(S, w, 1, clen, s, any, sn);
+    } else {
+      m0 = dfa_half<true, false>(S, w, 0, clen, s, any, sn);
+      m1 = dfa_half<true, false>(S, w, 1, clen, s, any, sn);
+    }
+    if (c0 == 0 && clen > 0) m0 |= 1u;  // the first token starts at byte 0
+    if (any & T_INV) report(P.st, PP_ERR_INVALID_INPUT, c0 + first_invalid(P, S, c0, clen, s0), true);
+    if (clen > 0 && c0 + clen == P.n && s != inv && !((P.dfa.accept_mask >> s) & 1u))
+      report(P.st, PP_ERR_BAD_END_STATE, P.n, true);
+    const uint32_t cnt = __popc(m0) + __popc(m1);
+    const uint32_t last = m1 ? 64u - __clz(m1) : m0 ? 32u - __clz(m0) : 0u;
+    P.lane_info[size_t(p) * 32 + lane] = s0 | (cnt << 4) | (last << 11);
+    const uint32_t total = __reduce_add_sync(FULL, cnt);
+    const uint32_t has = __ballot_sync(FULL, last != 0);
+    const int ll = has ? 31 - __clz(has) : 0;
+    const uint32_t l_last = __shfl_sync(FULL, last, ll);
+    if (lane == 0) {
+      P.piece_cnt[p] = total;
+      P.piece_last[p] = has ? uint32_t(ll) * CB + l_last : 0u;
+    }
+  }
+}
+
+// ------------------------------------------------------------ pass 4
+// (tokens, start + 1 of the last token start), combined earlier-then-later
+struct CountOp {
+  __device__ void operator()(const uint64_t (&a)[2], const uint64_t (&b)[2],
+                             uint64_t (&o)[2]) const {
+    o[0] = a[0] + b[0];
+    o[1] = b[1] ? b[1] : a[1];
+  }
+};
+
+__global__ void __launch_bounds__(SCAN_T) tok_count_scan_kernel(const __grid_constant__ TokParams P) {
+  __shared__ uint32_t tile_s;
+  __shared__ uint64_t wc[SCAN_T / 32], wl[SCAN_T / 32];
+  __shared__ uint64_t pre_s[2];
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  if (t == 0) tile_s = atomicAdd(&P.tickets[1], 1u);
+  __syncthreads();
+  const uint32_t tile = tile_s;
+  const uint64_t e0 = uint64_t(tile) * SCAN_TILE + uint64_t(t) * SCAN_E;
+  uint32_t c[SCAN_E];
+  uint64_t l[SCAN_E];
+  uint64_t ac = 0, al = 0;
+#pragma unroll
+  for (int e = 0; e < SCAN_E; ++e) {
+    const uint64_t idx = e0 + e;
+    c[e] = 0;
+    l[e] = 0;
+    if (idx < P.n_pieces) {
+      c[e] = P.piece_cnt[idx];
+      const uint32_t r = P.piece_last[idx];
+      l[e] = r ? idx * PIECE + r : 0ull;
+    }
+    ac += c[e];
+    if (l[e]) al = l[e];
+  }
+  // warp and block scans
+  uint64_t ic = ac, il = al;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const uint64_t oc = __shfl_up_sync(FULL, ic, d), ol = __shfl_up_sync(FULL, il, d);
+    if (lane >= d) { ic += oc; il = il ? il : ol; }
+  }
+  uint64_t xc = __shfl_up_sync(FULL, ic, 1), xl = __shfl_up_sync(FULL, il, 1);
+  if (lane == 0) { xc = 0; xl = 0; }
+  if (lane == 31) { wc[warp] = ic; wl[warp] = il; }
+  __syncthreads();
+  if (warp == 0) {
+    constexpr int NWS = SCAN_T / 32;
+    uint64_t vc = lane < NWS ? wc[lane] : 0ull, vl = lane < NWS ? wl[lane] : 0ull;
+    uint64_t sc = vc, sl = vl;
+#pragma unroll
+    for (int d = 1; d < NWS; d <<= 1) {
+      const uint64_t oc = __shfl_up_sync(FULL, sc, d), ol = __shfl_up_sync(FULL, sl, d);
+      if (lane >= d) { sc += oc; sl = sl ? sl : ol; }
+    }
+    uint64_t ec = __shfl_up_sync(FULL, sc, 1), el = __shfl_up_sync(FULL, sl, 1);
+    if (lane == 0) { ec = 0; el = 0; }
+    const uint64_t a2[2] = {__shfl_sync(FULL, sc, NWS - 1), __shfl_sync(FULL, sl, NWS - 1)};
+    __syncwarp();
+    if (lane < NWS) { wc[lane] = ec; wl[lane] = el; }
+    const uint64_t z[2] = {0ull, 0ull};
+    uint64_t ex2[2];
+    lookback_vec<2>(P.flag_c, P.agg_c, P.inc_c, tile, a2, z, z, CountOp{},
+                    LookbackCfg{P.st, P.spin_limit}, ex2);
+    if (lane == 0) { pre_s[0] = ex2[0]; pre_s[1] = ex2[1]; }
+  }
+  __syncthreads();
+  uint64_t k = pre_s[0] + wc[warp] + xc;
+  uint64_t pv = xl ? xl : wl[warp] ? wl[warp] : pre_s[1];
+#pragma unroll
+  for (int e = 0; e < SCAN_E; ++e) {
+    const uint64_t idx = e0 + e;
+    if (idx < P.n_pieces) {
+      P.piece_k0[idx] = k;
+      P.piece_prev[idx] = pv;
+      k += c[e];
+      if (l[e]) pv = l[e];
+      if (idx + 1 == P.n_pieces) P.st->n_tokens = k;
+    }
+  }
+}
+
+// ------------------------------------------------------------ pass 5
+struct EmitStage {
+  uint16_t start[WW][CAPW];     // offset in the piece of token k0 + i
+  uint32_t len[WW][CAPW + 1];   // length of token k0 + i - 1
+  uint8_t id[WW][CAPW + 1];     // id of token k0 + i - 1
+};
+
+__device__ __forceinline__ uint32_t nibble(const uint32_t (&sn)[4], uint32_t j) {
+  const uint32_t x = j < 16 ? (j < 8 ? sn[0] : sn[1]) : (j < 24 ? sn[2] : sn[3]);
+  return (x >> (4 * (j & 7))) & 0xFu;
+}
+
+__global__ void __launch_bounds__(WT, 4) tok_emit_kernel(const __grid_constant__ TokParams P) {
+  __shared__ DfaTables S;
+  __shared__ EmitStage E;
+  build_dfa_tables(P, S);
+  __syncthreads();
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const bool sizing = P.cap == 0 && P.out_start == nullptr;
+  const uint32_t n_warps = gridDim.x * WW;
+  for (uint32_t p = blockIdx.x * WW + warp; p < P.n_pieces; p += n_warps) {
+    const uint64_t pbase = uint64_t(p) * PIECE;
+    const uint64_t c0 = pbase + uint64_t(lane) * CB;
+    const uint32_t clen = chunk_len(c0, P.n);
+    const uint32_t info = P.lane_info[size_t(p) * 32 + lane];
+    const uint32_t cnt = (info >> 4) & 0x7Fu, last = (info >> 11) & 0x7Fu;
+    const uint64_t k0 = P.piece_k0[p];
+    // the lane's first token (piece-local index) and the token open at its start
+    uint32_t ib = cnt;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const uint32_t o = __shfl_up_sync(FULL, ib, d);
+      if (lane >= d) ib += o;
+    }
+    const uint32_t total = __shfl_sync(FULL, ib, 31);
+    ib -= cnt;
+    uint64_t lp = last ? c0 + last : 0ull;  // positions grow with the lane: max = latest
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const uint64_t o = __shfl_up_sync(FULL, lp, d);
+      if (lane >= d) lp = max(lp, o);
+    }
+    uint64_t prev = __shfl_up_sync(FULL, lp, 1);
+    if (lane == 0) prev = 0;
+    if (prev == 0) prev = P.piece_prev[p];
+    const bool staged = total <= CAPW;
+    const bool last_piece = p + 1 == P.n_pieces;
+
+    uint32_t w[16];
+    load_chunk(P, c0, clen, w);
+    uint32_t s = info & 0xFu, any = 0;
+    uint32_t i = ib;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t sn[4] = {0u, 0u, 0u, 0u};
+      uint32_t m = clen == CB ? dfa_half<false, true>(S, w, h, clen, s, any, sn)
+                              : dfa_half<true, true>(S, w, h, clen, s, any, sn);
+      if (h == 0 && c0 == 0 && clen > 0) m |= 1u;
+      while (m) {
+        const uint32_t j = __ffs(m) - 1;
+        m &= m - 1;
+        const uint64_t pos = c0 + 32 * h + j;
+        uint32_t id = 0, len = 0;
+        if (prev) {
+          const uint64_t ps = prev - 1;
+          id = S.token_id[nibble(sn, j)];
+          if (id == 0xFEu) id = S.byte_token_id[__ldg(P.in + ps)];
+          len = uint32_t(pos - ps);
+        }
+        if (staged) {
+          E.start[warp][i] = uint16_t(pos - pbase);
+          E.len[warp][i] = len;
+          E.id[warp][i] = uint8_t(id);
+        } else {
+          const uint64_t k = k0 + i;
+          if (prev && k - 1 < P.cap) { P.out_id[k - 1] = uint8_t(id); P.out_len[k - 1] = len; }
+          if (k < P.cap) P.out_start[k] = pos;
+          else if (!sizing) report(P.st, PP_ERR_CAPACITY, 0, false);
+        }
+        ++i;
+        prev = pos + 1;
+      }
+    }
+    if (clen > 0 && c0 + clen == P.n) {  // close the last token
+      const uint64_t k = k0 + i;  // tokens in total
+      if (prev) {
+        const uint64_t ps = prev - 1;
+        uint32_t id = S.token_id[s];
+        if (id == 0xFEu) id = S.byte_token_id[__ldg(P.in + ps)];
+        const uint32_t len = uint32_t(P.n - ps);
+        if (staged) { E.len[warp][i] = len; E.id[warp][i] = uint8_t(id); }
+        else if (k - 1 < P.cap) { P.out_id[k - 1] = uint8_t(id); P.out_len[k - 1] = len; }
+      }
+    }
+    if (staged) {
+      __syncwarp();
+      // starts of tokens k0 .. k0+total-1; ids and lengths of tokens
+      // k0-1 .. k0+total-2 (and k0+total-1 in the last piece)
+      const uint32_t nclose = total + (last_piece ? 1u : 0u);
+      for (uint32_t q = lane; q < nclose; q += 32) {
+        const uint64_t k = k0 + q;
+        if (q < total) {
+          if (k < P.cap) P.out_start[k] = pbase + E.start[warp][q];
+          else if (!sizing) report(P.st, PP_ERR_CAPACITY, 0, false);
+        }
+        if (k >= 1 && k - 1 < P.cap) {  // token k-1 exists (the first start closes none)
+          P.out_len[k - 1] = E.len[warp][q];
+          P.out_id[k - 1] = E.id[warp][q];
+        }
+      }
+      __syncwarp();
+    }
+  }
+}
+
+__global__ void tok_init_kernel(uint4* zero, size_t n16, pp_status* st) {
+  const size_t i0 = size_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (size_t i = i0; i < n16; i += size_t(gridDim.x) * blockDim.x) zero[i] = make_uint4(0, 0, 0, 0);
+  if (i0 == 0) {
+    st->error = 0;
+    st->reserved = 0;
+    st->first_error_offset = ~0ull;
+    st->n_records = 0;
+    st->n_tokens = 0;
+    for (int c = 0; c < PP_MAX_COLS; ++c) st->chars_len[c] = 0;
+  }
+}
+
+// ------------------------------------------------------------ host
+size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
+uint32_t pieces_of(uint64_t n) { return uint32_t((n + PIECE - 1) / PIECE); }
+uint32_t scan_tiles_of(uint32_t pieces) { return (pieces + SCAN_TILE - 1) / SCAN_TILE; }
+
+// [tickets 16][flag_s 4T][flag_c 4T] is zeroed by tok_init_kernel
+size_t zeroed_bytes(uint32_t tiles) { return (16 + size_t(tiles) * 8 + 15) & ~size_t(15); }
+
+struct Layout {
+  size_t agg_s, inc_s, agg_c, inc_c, lane_pre, piece_stv, piece_state, lane_info, piece_cnt,
+      piece_last, piece_k0, piece_prev, total;
+};
+Layout layout_of(uint64_t n) {
+  const uint32_t P = pieces_of(n), T = scan_tiles_of(P);
+  Layout L;
+  size_t o = al256(zeroed_bytes(T));
+  L.agg_s = o; o += al256(size_t(T) * 16);
+  L.inc_s = o; o += al256(size_t(T) * 16);
+  L.agg_c = o; o += al256(size_t(T) * 16);
+  L.inc_c = o; o += al256(size_t(T) * 16);
+  L.lane_pre = o; o += al256(size_t(P) * 32 * 8);
+  L.piece_stv = o; o += al256(size_t(P) * 8);
+  L.piece_state = o; o += al256(size_t(P));
+  L.lane_info = o; o += al256(size_t(P) * 32 * 4);
+  L.piece_cnt = o; o += al256(size_t(P) * 4);
+  L.piece_last = o; o += al256(size_t(P) * 4);
+  L.piece_k0 = o; o += al256(size_t(P) * 8);
+  L.piece_prev = o; o += al256(size_t(P) * 8);
+  L.total = o;
+  return L;
+}
+
+}  // namespace
+
+namespace ppi {
+
+extern uint32_t g_spin_limit;
+
+size_t tokenize_scratch_bytes(uint64_t n) { return layout_of(n).total; }
+
+cudaError_t launch_tokenize(const uint8_t* in, uint64_t n, const GenericDfa& dfa,
+                            uint8_t* out_id, uint64_t* out_start, uint32_t* out_len,
+                            uint64_t cap, pp_status* st, void* scratch, size_t,
+                            cudaStream_t stream) {
+  TokParams P{};
+  P.in = in;
+  P.n = n;
+  P.n_pieces = pieces_of(n);
+  P.spin_limit = g_spin_limit;
+  P.aligned = (reinterpret_cast<uintptr_t>(in) & 15) == 0;
+  P.dfa = dfa;
+  P.out_id = out_id;
+  P.out_start = out_start;
+  P.out_len = out_len;
+  P.cap = cap;
+  P.st = st;
+  const uint32_t T = scan_tiles_of(P.n_pieces);
+  const Layout L = layout_of(n);
+  uint8_t* b = static_cast<uint8_t*>(scratch);
+  P.tickets = reinterpret_cast<uint32_t*>(b);
+  P.flag_s = reinterpret_cast<uint32_t*>(b + 16);
+  P.flag_c = reinterpret_cast<uint32_t*>(b + 16 + size_t(T) * 4);
+  P.agg_s = reinterpret_cast<uint64_t*>(b + L.agg_s);
+  P.inc_s = reinterpret_cast<uint64_t*>(b + L.inc_s);
+  P.agg_c = reinterpret_cast<uint64_t*>(b + L.agg_c);
+  P.inc_c = reinterpret_cast<uint64_t*>(b + L.inc_c);
+  P.lane_pre = reinterpret_cast<uint64_t*>(b + L.lane_pre);
+  P.piece_stv = reinterpret_cast<uint64_t*>(b + L.piece_stv);
+  P.piece_state = b + L.piece_state;
+  P.lane_info = reinterpret_cast<uint32_t*>(b + L.lane_info);
+  P.piece_cnt = reinterpret_cast<uint32_t*>(b + L.piece_cnt);
+  P.piece_last = reinterpret_cast<uint32_t*>(b + L.piece_last);
+  P.piece_k0 = reinterpret_cast<uint64_t*>(b + L.piece_k0);
+  P.piece_prev = reinterpret_cast<uint64_t*>(b + L.piece_prev);
+
+  const bool timed = stage_begin();
+  if (timed) stage_mark(0, stream);
+  const size_t n16 = zeroed_bytes(T) / 16;
+  tok_init_kernel<<<int(std::min<size_t>((n16 + 255) / 256 + 1, 1024)), 256, 0, stream>>>(
+      reinterpret_cast<uint4*>(b), n16, st);
+  cudaError_t e = cudaGetLastError();
+  if (timed) stage_mark(1, stream);
+  if (e != cudaSuccess || P.n_pieces == 0) return e;
+  static int n_sm = 0;
+  if (!n_sm) {
+    int dev;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return e;
+  }
+  const uint32_t bgrid = std::min<uint32_t>((P.n_pieces + WW - 1) / WW, uint32_t(n_sm) * 4);
+  tok_stv_kernel<<<bgrid, WT, 0, stream>>>(P);
+  if (timed) stage_mark(2, stream);
+  tok_state_scan_kernel<<<T, SCAN_T, 0, stream>>>(P);
+  if (timed) stage_mark(3, stream);
+  tok_count_kernel<<<bgrid, WT, 0, stream>>>(P);
+  if (timed) stage_mark(4, stream);
+  tok_count_scan_kernel<<<T, SCAN_T, 0, stream>>>(P);
+  if (timed) stage_mark(5, stream);
+  const bool sizing = cap == 0 && out_start == nullptr;
+  if (!sizing) tok_emit_kernel<<<bgrid, WT, 0, stream>>>(P);
+  if (timed) stage_mark(6, stream);
+  return cudaGetLastError();
+}
+
+}  // namespace ppi

@@ -264,17 +264,20 @@ void pp_debug_set_spin_limit(uint32_t polls);
  * unbounded; the device stays usable.  Process-wide. */
 void pp_debug_set_withhold(int on);
 
-/* Benchmark hook: with n_calls > 0, the next n_calls pp_parse calls record
- * CUDA events on their stream around each of their four kernels (init,
- * context pass, scan, main pass).  0 stops recording and frees the events.
+/* Benchmark hook: with n_calls > 0, the next n_calls pp_parse or
+ * pp_tokenize calls record CUDA events on their stream around each of their
+ * kernels.  0 stops recording and frees the events.
  * Process-wide; not thread-safe.  Returns PP_ECUDA if events cannot be
  * created. */
 pp_rc pp_debug_stage_timing(int n_calls);
 
-/* Kernel durations of the recorded calls: out[4*i + k] = milliseconds of
- * kernel k (0 init, 1 context, 2 scan, 3 main) of call i.  Waits for the
- * events.  Returns the number of calls written (at most max_calls), or -1
- * on a CUDA error. */
+/* Kernel durations of the recorded calls: out[PP_STAGES*i + k] =
+ * milliseconds of kernel k of call i.  pp_parse: 0 init, 1 context pass,
+ * 2 scan, 3 main pass.  pp_tokenize: 0 init, 1 transition vectors, 2 state
+ * scan, 3 count pass, 4 count scan, 5 emit pass.  Entries a call does not
+ * use are 0.  Waits for the events.  Returns the number of calls written
+ * (at most max_calls), or -1 on a CUDA error. */
+#define PP_STAGES 6
 int pp_debug_stage_ms(float* out, int max_calls);
 
 #ifdef __cplusplus
