@@ -22,8 +22,9 @@
 //             closes token k-1 (its length, and its id from the state before
 //             the start).  A piece's triples are staged in shared memory and
 //             written with coalesced stores.
-// The byte passes read the input straight from HBM with 16-byte loads; all
-// per-byte lookups are one-byte tables in shared memory.
+// The byte passes read the input straight from HBM with 16-byte loads.  The
+// count pass looks up tables replicated per lane in shared memory (no bank
+// conflicts); the emit pass steps the DFA two bytes per lookup.
 #include <algorithm>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -39,14 +40,11 @@ using ppi::GenericDfa;
 
 constexpr int CB = 64;                   // bytes per lane
 constexpr int PIECE = 32 * CB;           // bytes per warp
-constexpr int WT = 256;                  // threads per block, byte passes
+constexpr int WT = 256;                  // threads per block, transition-vector pass
 constexpr int WW = WT / 32;
 constexpr int SCAN_T = 256, SCAN_E = 16; // scan passes: pieces per thread
 constexpr int SCAN_TILE = SCAN_T * SCAN_E;
 constexpr uint32_t CAPW = 512;           // tokens per piece staged for coalesced stores
-
-// transition-table entry bits (count and emit passes)
-constexpr uint32_t T_BEGIN = 0x10u, T_INV = 0x20u;
 
 struct TokParams {
   const uint8_t* in;
@@ -108,14 +106,17 @@ __device__ __forceinline__ uint32_t chunk_len(uint64_t c0, uint64_t n) {
 }
 
 // ------------------------------------------------------------ pass 1
-// pair_s[g1 * 16 + g2]: selectors of s -> delta_g2(delta_g1(s)) for the
-// two-byte step G'(s) = G(D(s)): word x holds states 0-7 (4 bits each), y
-// states 8-15.  single_s[g]: the same for one byte.
+// Steps of G'(s) = G(D(s)) take D as selector nibbles: word x holds
+// D(0..7) (4 bits each), y D(8..15).  tri[] holds D for three consecutive
+// bytes (groups g1, g2, g3: D = delta_g3 o delta_g2 o delta_g1), addressed
+// in bytes as ga[b1] | gb[b2] | gc[b3]; single[] one byte, at gc[b].
 struct StvTables {
-  uint8_t grp16[256];  // group * 16
-  uint8_t grp[256];
-  uint2 pair[256];
+  uint16_t ga[256];  // group * 2048
+  uint16_t gb[256];  // group * 128
+  uint16_t gc[256];  // group * 8
+  uint2 tri[16 * 16 * 16];
   uint2 single[PP_MAX_GROUPS];
+  Stv16 delta[PP_MAX_GROUPS];  // delta_g as a vector (table construction)
 };
 
 __device__ __forceinline__ Stv16 stv_step(const Stv16& G, uint2 e) {
@@ -127,32 +128,39 @@ __device__ __forceinline__ Stv16 stv_step(const Stv16& G, uint2 e) {
   r.w[3] = stv16_gather(G, e.y >> 16, xy >> 16);
   return r;
 }
+__device__ __forceinline__ uint2 as_sel(const Stv16& d) {
+  const uint64_t v = stv16_pack(d);
+  return make_uint2(uint32_t(v), uint32_t(v >> 32));
+}
+template <class T>
+__device__ __forceinline__ const T& at_byte(const T* base, uint32_t off) {
+  return *reinterpret_cast<const T*>(reinterpret_cast<const uint8_t*>(base) + off);
+}
 
 __global__ void __launch_bounds__(WT, 4) tok_stv_kernel(const __grid_constant__ TokParams P) {
   __shared__ StvTables S;
   const int t = threadIdx.x, lane = t & 31;
   for (int k = t; k < 256; k += WT) {
     const uint32_t g = P.dfa.byte_to_group[k] & 0xFu;
-    S.grp[k] = uint8_t(g);
-    S.grp16[k] = uint8_t(g << 4);
-    const uint32_t g1 = uint32_t(k) >> 4, g2 = uint32_t(k) & 0xFu;
-    uint32_t x = 0, y = 0;
-    for (uint32_t s = 0; s < 16; ++s) {
-      const uint32_t d = P.dfa.delta[g2][P.dfa.delta[g1][s] & 0xFu] & 0xFu;
-      if (s < 8) x |= d << (4 * s);
-      else y |= d << (4 * (s - 8));
-    }
-    S.pair[k] = make_uint2(x, y);
-    if (k < PP_MAX_GROUPS) {
-      x = y = 0;
-      for (uint32_t s = 0; s < 16; ++s) {
-        const uint32_t d = P.dfa.delta[k][s] & 0xFu;
-        if (s < 8) x |= d << (4 * s);
-        else y |= d << (4 * (s - 8));
-      }
-      S.single[k] = make_uint2(x, y);
-    }
+    S.ga[k] = uint16_t(g << 11);
+    S.gb[k] = uint16_t(g << 7);
+    S.gc[k] = uint16_t(g << 3);
   }
+  if (t < PP_MAX_GROUPS) {
+    Stv16 d;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint32_t x = 0;
+      for (int b = 0; b < 4; ++b) x |= uint32_t(P.dfa.delta[t][4 * k + b] & 0xFu) << (8 * b);
+      d.w[k] = x;
+    }
+    S.delta[t] = d;
+    S.single[t] = as_sel(d);
+  }
+  __syncthreads();
+  for (int k = t; k < 16 * 16 * 16; k += WT)
+    S.tri[k] = as_sel(stv16_compose(stv16_compose(S.delta[k >> 8], S.delta[(k >> 4) & 15]),
+                                    S.delta[k & 15]));
   __syncthreads();
   const uint32_t n_warps = gridDim.x * WW;
   for (uint32_t p = blockIdx.x * WW + (t >> 5); p < P.n_pieces; p += n_warps) {
@@ -161,12 +169,14 @@ __global__ void __launch_bounds__(WT, 4) tok_stv_kernel(const __grid_constant__ 
     uint32_t w[16];
     load_chunk(P, c0, clen, w);
     Stv16 G = stv16_id();
-    if (clen == CB) {
+    if (clen == CB) {  // back to front: bytes 61-63, 58-60, ..., 1-3, then byte 0
 #pragma unroll
-      for (int j = CB - 2; j >= 0; j -= 2)
-        G = stv_step(G, S.pair[S.grp16[byte_of(w, j)] | S.grp[byte_of(w, j + 1)]]);
+      for (int j = CB - 3; j >= 1; j -= 3)
+        G = stv_step(G, at_byte(S.tri, S.ga[byte_of(w, j)] | S.gb[byte_of(w, j + 1)] |
+                                           S.gc[byte_of(w, j + 2)]));
+      G = stv_step(G, at_byte(S.single, S.gc[byte_of(w, 0)]));
     } else {
-      for (int j = int(clen) - 1; j >= 0; --j) G = stv_step(G, S.single[S.grp[P.in[c0 + j]]]);
+      for (int j = int(clen) - 1; j >= 0; --j) G = stv_step(G, at_byte(S.single, S.gc[P.in[c0 + j]]));
     }
     Stv16 inc = G;
 #pragma unroll
@@ -244,88 +254,107 @@ __global__ void __launch_bounds__(SCAN_T) tok_state_scan_kernel(const __grid_con
   }
 }
 
-// ------------------------------------------------------------ passes 3, 5
-// trans_s[g * 16 + s] = next state | T_BEGIN | T_INV (a transition into the
-// invalid state from another state).
-struct DfaTables {
-  uint8_t grp16[256];
-  uint8_t trans[256];
+// ------------------------------------------------------------ pass 3
+// The count pass looks up two tables per byte, both replicated per lane:
+// entry e is stored 32 times, lane l's copy at word e * 32 + l, so the 32
+// lookups of a warp always fall in 32 different banks (one wavefront each,
+// whatever the bytes and states).  Values are pre-shifted to be byte
+// offsets: grp[b] = group * 2048, trans[g * 16 + s] = next * 128 | begin
+// flag; the lane's copy adds lane * 4.  The state is carried as
+// s * 128 | lane * 4.
+constexpr int DT = 512;  // threads per block, count pass
+constexpr int DW = DT / 32;
+constexpr uint32_t R_NEXT = 0x780u, R_BEGIN_BIT = 11;
+
+struct RepTables {
+  uint32_t grp[256 * 32];
+  uint32_t trans[256 * 32];
   uint8_t token_id[PP_MAX_STATES];
   uint8_t byte_token_id[256];
 };
 
-__device__ void build_dfa_tables(const TokParams& P, DfaTables& S) {
+__device__ void build_rep_tables(const TokParams& P, RepTables& R) {
   const int t = threadIdx.x;
-  const uint32_t inv = P.dfa.invalid_state;
-  for (int k = t; k < 256; k += blockDim.x) {
-    S.grp16[k] = uint8_t((P.dfa.byte_to_group[k] & 0xFu) << 4);
-    const uint32_t g = uint32_t(k) >> 4, s = uint32_t(k) & 0xFu;
-    const uint32_t nx = P.dfa.delta[g][s] & 0xFu;
-    uint32_t e = nx;
-    if (P.dfa.tag[s][g] == PP_TAG_BEGIN) e |= T_BEGIN;
-    if (nx == inv && s != inv) e |= T_INV;
-    S.trans[k] = uint8_t(e);
-    S.byte_token_id[k] = P.dfa.byte_token_id[k];
+  for (int k = t; k < 256 * 32; k += blockDim.x) {
+    const uint32_t e = uint32_t(k) >> 5;  // one entry per warp: uniform parameter reads
+    R.grp[k] = (P.dfa.byte_to_group[e] & 0xFu) << 11;
+    const uint32_t g = e >> 4, st = e & 0xFu;
+    R.trans[k] = ((P.dfa.delta[g][st] & 0xFu) << 7) |
+                 (P.dfa.tag[st][g] == PP_TAG_BEGIN ? 1u << R_BEGIN_BIT : 0u);
   }
-  if (t < PP_MAX_STATES) S.token_id[t] = P.dfa.token_id[t];
+  for (int k = t; k < 256; k += blockDim.x) R.byte_token_id[k] = P.dfa.byte_token_id[k];
+  if (t < PP_MAX_STATES) R.token_id[t] = P.dfa.token_id[t];
 }
 
-// One DFA over 32 bytes of the chunk (half h): begin mask, and (when
-// STATES) the state before every byte as nibbles in sn[4].  Bytes at or
-// past clen leave the state and the mask alone (PARTIAL only).
+__device__ __forceinline__ uint32_t lds_at(const uint32_t* base, uint32_t off) {
+  return *reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint8_t*>(base) + off);
+}
+// one DFA step on byte b; returns the begin flag
+__device__ __forceinline__ uint32_t dfa_step(const RepTables& R, uint32_t b, uint32_t lane4,
+                                             uint32_t& s) {
+  const uint32_t v = lds_at(R.trans, lds_at(R.grp, (b << 7) | lane4) | s);
+  s = (v & R_NEXT) | lane4;
+  return (v >> R_BEGIN_BIT) & 1u;
+}
+
+// The DFA over the 32 bytes of half h of the chunk: returns the begin mask.
+// With STATES, sn[4] gets the state before every byte as nibbles (byte j at
+// bits 4(j & 7) of sn[j >> 3]).  PARTIAL: bytes at or past clen are skipped.
 template <bool PARTIAL, bool STATES>
-__device__ __forceinline__ uint32_t dfa_half(const DfaTables& S, const uint32_t (&w)[16], int h,
-                                             uint32_t clen, uint32_t& s, uint32_t& any,
+__device__ __forceinline__ uint32_t dfa_half(const RepTables& R, const uint32_t (&w)[16], int h,
+                                             uint32_t clen, uint32_t lane4, uint32_t& s,
                                              uint32_t (&sn)[4]) {
   uint32_t m = 0;
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
     const int jj = 32 * h + j;
     if (PARTIAL && uint32_t(jj) >= clen) break;
-    if (STATES) sn[j >> 3] |= s << (4 * (j & 7));
-    const uint32_t v = S.trans[S.grp16[byte_of(w, jj)] | s];
-    m |= ((v >> 4) & 1u) << j;
-    any |= v;
-    s = v & 0xFu;
+    if (STATES) sn[j >> 3] |= (s >> 7) << (4 * (j & 7));
+    m |= dfa_step(R, byte_of(w, jj), lane4, s) << j;
   }
   return m;
 }
 
-// first invalid transition of the chunk (slow path: only when one exists)
-__device__ uint32_t first_invalid(const TokParams& P, const DfaTables& S, uint64_t c0,
-                                  uint32_t clen, uint32_t s) {
+// first transition into the invalid state in the chunk (slow path, only
+// when the chunk starts valid and ends invalid; the invalid state absorbs)
+__device__ uint32_t first_invalid(const TokParams& P, const RepTables& R, uint64_t c0,
+                                  uint32_t clen, uint32_t lane4, uint32_t s) {
+  const uint32_t inv = P.dfa.invalid_state;
   for (uint32_t j = 0; j < clen; ++j) {
-    const uint32_t v = S.trans[S.grp16[P.in[c0 + j]] | s];
-    if (v & T_INV) return j;
-    s = v & 0xFu;
+    dfa_step(R, P.in[c0 + j], lane4, s);
+    if ((s >> 7) == inv) return j;
   }
   return clen;
 }
 
-__global__ void __launch_bounds__(WT, 4) tok_count_kernel(const __grid_constant__ TokParams P) {
-  __shared__ DfaTables S;
-  build_dfa_tables(P, S);
+__global__ void __launch_bounds__(DT, 2) tok_count_kernel(const __grid_constant__ TokParams P) {
+  extern __shared__ __align__(16) uint8_t dsm[];
+  RepTables& R = *reinterpret_cast<RepTables*>(dsm);
+  build_rep_tables(P, R);
   __syncthreads();
   const int t = threadIdx.x, lane = t & 31;
+  const uint32_t lane4 = uint32_t(lane) * 4;
   const uint32_t inv = P.dfa.invalid_state;
-  const uint32_t n_warps = gridDim.x * WW;
-  for (uint32_t p = blockIdx.x * WW + (t >> 5); p < P.n_pieces; p += n_warps) {
+  const uint32_t n_warps = gridDim.x * DW;
+  for (uint32_t p = blockIdx.x * DW + (t >> 5); p < P.n_pieces; p += n_warps) {
     const uint64_t c0 = uint64_t(p) * PIECE + uint64_t(lane) * CB;
     const uint32_t clen = chunk_len(c0, P.n);
     const uint32_t s0 = nib_apply(P.lane_pre[size_t(p) * 32 + lane], P.piece_state[p]);
     uint32_t w[16];
     load_chunk(P, c0, clen, w);
-    uint32_t s = s0, any = 0, sn[4];
-    uint32_t m0, m1;
+    uint32_t s = (s0 << 7) | lane4, sn[4], m0, m1;
     if (clen == CB) {
-      m0 = dfa_half<false, false>(S, w, 0, clen, s, any, sn);
-      m1 = dfa_half<false, false>(S, w, 1, clen, s, any, sn);
+      m0 = dfa_half<false, false>(R, w, 0, clen, lane4, s, sn);
+      m1 = dfa_half<false, false>(R, w, 1, clen, lane4, s, sn);
     } else {
-      m0 = dfa_half<true, false>(S, w, 0, clen, s, any, sn);
-      m1 = dfa_half<true, false>(S, w, 1, clen, s, any, sn);
+      m0 = dfa_half<true, false>(R, w, 0, clen, lane4, s, sn);
+      m1 = dfa_half<true, false>(R, w, 1, clen, lane4, s, sn);
     }
+    s >>= 7;
     if (c0 == 0 && clen > 0) m0 |= 1u;  // the first token starts at byte 0
-    if (any & T_INV) report(P.st, PP_ERR_INVALID_INPUT, c0 + first_invalid(P, S, c0, clen, s0), true);
+    if (s == inv && s0 != inv)
+      report(P.st, PP_ERR_INVALID_INPUT, c0 + first_invalid(P, R, c0, clen, lane4, (s0 << 7) | lane4),
+             true);
     if (clen > 0 && c0 + clen == P.n && s != inv && !((P.dfa.accept_mask >> s) & 1u))
       report(P.st, PP_ERR_BAD_END_STATE, P.n, true);
     const uint32_t cnt = __popc(m0) + __popc(m1);
@@ -424,16 +453,137 @@ __global__ void __launch_bounds__(SCAN_T) tok_count_scan_kernel(const __grid_con
   }
 }
 
+// ------------------------------------------------------------ pass 5 tables
+// The DFA steps two bytes per lookup through composed pair transitions:
+// pair[(g1 * 16 + g2) * 16 + s], addressed in bytes as ga[b1] | gb[b2] | 2s,
+// holds 2 x the state after both bytes (P2_NEXT2), the state between them
+// (P2_MID), the token-begin flags of the two transitions (P2_BEGIN, first
+// byte in the low bit) and their invalid flags (P2_INV).  The last chunk of
+// the input steps one byte at a time through trans[g * 16 + s] = next state
+// | T_BEGIN | T_INV.  An invalid flag marks a transition into the invalid
+// state from another state.
+constexpr uint32_t P2_NEXT2 = 0x1Eu, P2_MID = 0x1E0u, P2_BEGIN_SHIFT = 9, P2_INV = 0x1800u;
+constexpr uint32_t T_BEGIN = 0x10u, T_INV = 0x20u;
+
+struct DfaTables {
+  uint16_t ga[256];     // group * 512
+  uint16_t gb[256];     // group * 32
+  uint16_t pair[16 * 16 * 16];
+  uint8_t grp16[256];   // group * 16
+  uint8_t trans[256];
+  uint8_t token_id[PP_MAX_STATES];
+  uint8_t byte_token_id[256];
+};
+
+// one transition: next state | T_BEGIN | T_INV
+__device__ __forceinline__ uint32_t trans_of(const TokParams& P, uint32_t g, uint32_t s) {
+  const uint32_t nx = P.dfa.delta[g][s] & 0xFu;
+  uint32_t e = nx;
+  if (P.dfa.tag[s][g] == PP_TAG_BEGIN) e |= T_BEGIN;
+  if (nx == P.dfa.invalid_state && s != P.dfa.invalid_state) e |= T_INV;
+  return e;
+}
+
+__device__ void build_dfa_tables(const TokParams& P, DfaTables& S) {
+  const int t = threadIdx.x;
+  for (int k = t; k < 256; k += blockDim.x) {
+    const uint32_t g = P.dfa.byte_to_group[k] & 0xFu;
+    S.ga[k] = uint16_t(g << 9);
+    S.gb[k] = uint16_t(g << 5);
+    S.grp16[k] = uint8_t(g << 4);
+    S.trans[k] = uint8_t(trans_of(P, uint32_t(k) >> 4, uint32_t(k) & 0xFu));
+    S.byte_token_id[k] = P.dfa.byte_token_id[k];
+  }
+  for (int k = t; k < 16 * 16 * 16; k += blockDim.x) {
+    const uint32_t g1 = uint32_t(k) >> 8, g2 = (uint32_t(k) >> 4) & 0xFu, s = uint32_t(k) & 0xFu;
+    const uint32_t e1 = trans_of(P, g1, s), s1 = e1 & 0xFu;
+    const uint32_t e2 = trans_of(P, g2, s1);
+    S.pair[k] = uint16_t(((e2 & 0xFu) << 1) | (s1 << 5) |
+                         ((e1 & T_BEGIN) ? 1u << P2_BEGIN_SHIFT : 0u) |
+                         ((e2 & T_BEGIN) ? 2u << P2_BEGIN_SHIFT : 0u) |
+                         (((e1 | e2) & T_INV) ? P2_INV : 0u));
+  }
+  if (t < PP_MAX_STATES) S.token_id[t] = P.dfa.token_id[t];
+}
+
+// One DFA over the 32 bytes of half h of a full chunk, two bytes a step:
+// returns the begin mask; s2 is 2 x the state.  With STATES, sn[4] gets the
+// state before every byte as nibbles (byte j at bits 4(j & 7) of sn[j >> 3]).
+template <bool STATES>
+__device__ __forceinline__ uint32_t dfa_pairs(const DfaTables& S, const uint32_t (&w)[16], int h,
+                                              uint32_t& s2, uint32_t& any, uint32_t (&sn)[4]) {
+  const uint8_t* tb = reinterpret_cast<const uint8_t*>(S.pair);
+  uint32_t m = 0;
+#pragma unroll
+  for (int q = 0; q < 16; ++q) {
+    const int j = 32 * h + 2 * q;
+    const uint32_t v =
+        *reinterpret_cast<const uint16_t*>(tb + (S.ga[byte_of(w, j)] | S.gb[byte_of(w, j + 1)] | s2));
+    if (STATES) sn[q >> 2] |= ((s2 | (v & P2_MID)) >> 1) << (8 * (q & 3));
+    m |= ((v >> P2_BEGIN_SHIFT) & 3u) << (2 * q);
+    any |= v;
+    s2 = v & P2_NEXT2;
+  }
+  return m;
+}
+
+// The same one byte at a time for the last, partial chunk (bytes at or past
+// clen leave the state and the mask alone); s is the state itself.
+template <bool STATES>
+__device__ __forceinline__ uint32_t dfa_bytes(const DfaTables& S, const uint32_t (&w)[16], int h,
+                                              uint32_t clen, uint32_t& s, uint32_t& any,
+                                              uint32_t (&sn)[4]) {
+  uint32_t m = 0;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const int jj = 32 * h + j;
+    if (uint32_t(jj) >= clen) break;
+    if (STATES) sn[j >> 3] |= s << (4 * (j & 7));
+    const uint32_t v = S.trans[S.grp16[byte_of(w, jj)] | s];
+    m |= ((v >> 4) & 1u) << j;
+    any |= v;
+    s = v & 0xFu;
+  }
+  return m;
+}
+
 // ------------------------------------------------------------ pass 5
+// A piece's token starts in order: offset in the piece and the state before
+// the start (which gives the id of the token it closes).  Entry `total`
+// holds the state after the last byte of the input, in the last piece.
 struct EmitStage {
-  uint16_t start[WW][CAPW];     // offset in the piece of token k0 + i
-  uint32_t len[WW][CAPW + 1];   // length of token k0 + i - 1
-  uint8_t id[WW][CAPW + 1];     // id of token k0 + i - 1
+  uint16_t start[WW][CAPW];
+  uint8_t state[WW][CAPW + 1];
 };
 
 __device__ __forceinline__ uint32_t nibble(const uint32_t (&sn)[4], uint32_t j) {
   const uint32_t x = j < 16 ? (j < 8 ? sn[0] : sn[1]) : (j < 24 ? sn[2] : sn[3]);
   return (x >> (4 * (j & 7))) & 0xFu;
+}
+
+// id of the token that starts at `start` and ends in state s_end
+__device__ __forceinline__ uint32_t token_id(const TokParams& P, const DfaTables& S,
+                                             uint32_t s_end, uint64_t start) {
+  const uint32_t id = S.token_id[s_end];
+  return id == 0xFEu ? S.byte_token_id[__ldg(P.in + start)] : id;
+}
+
+// One half of the chunk: run the DFA, return the begin mask and the states
+// before every byte.
+__device__ __forceinline__ uint32_t emit_half(const DfaTables& S, const uint32_t (&w)[16], int h,
+                                              bool full, uint32_t clen, uint32_t& s,
+                                              uint32_t (&sn)[4]) {
+  uint32_t any = 0, m;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) sn[k] = 0;
+  if (full) {
+    uint32_t s2 = 2 * s;
+    m = dfa_pairs<true>(S, w, h, s2, any, sn);
+    s = s2 >> 1;
+  } else {
+    m = dfa_bytes<true>(S, w, h, clen, s, any, sn);
+  }
+  return m;
 }
 
 __global__ void __launch_bounds__(WT, 4) tok_emit_kernel(const __grid_constant__ TokParams P) {
@@ -446,13 +596,15 @@ __global__ void __launch_bounds__(WT, 4) tok_emit_kernel(const __grid_constant__
   const uint32_t n_warps = gridDim.x * WW;
   for (uint32_t p = blockIdx.x * WW + warp; p < P.n_pieces; p += n_warps) {
     const uint64_t pbase = uint64_t(p) * PIECE;
-    const uint64_t c0 = pbase + uint64_t(lane) * CB;
+    const uint32_t off0 = uint32_t(lane) * CB;
+    const uint64_t c0 = pbase + off0;
     const uint32_t clen = chunk_len(c0, P.n);
+    const bool full = clen == CB;
+    const bool owns_end = clen > 0 && c0 + clen == P.n;
     const uint32_t info = P.lane_info[size_t(p) * 32 + lane];
-    const uint32_t cnt = (info >> 4) & 0x7Fu, last = (info >> 11) & 0x7Fu;
+    const uint32_t cnt = (info >> 4) & 0x7Fu;
     const uint64_t k0 = P.piece_k0[p];
-    // the lane's first token (piece-local index) and the token open at its start
-    uint32_t ib = cnt;
+    uint32_t ib = cnt;  // the lane's first token, piece-local
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
       const uint32_t o = __shfl_up_sync(FULL, ib, d);
@@ -460,81 +612,82 @@ __global__ void __launch_bounds__(WT, 4) tok_emit_kernel(const __grid_constant__
     }
     const uint32_t total = __shfl_sync(FULL, ib, 31);
     ib -= cnt;
-    uint64_t lp = last ? c0 + last : 0ull;  // positions grow with the lane: max = latest
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const uint64_t o = __shfl_up_sync(FULL, lp, d);
-      if (lane >= d) lp = max(lp, o);
-    }
-    uint64_t prev = __shfl_up_sync(FULL, lp, 1);
-    if (lane == 0) prev = 0;
-    if (prev == 0) prev = P.piece_prev[p];
-    const bool staged = total <= CAPW;
-    const bool last_piece = p + 1 == P.n_pieces;
-
     uint32_t w[16];
     load_chunk(P, c0, clen, w);
-    uint32_t s = info & 0xFu, any = 0;
-    uint32_t i = ib;
+    uint32_t s = info & 0xFu;
+
+    if (total <= CAPW) {
+      // ---- stage the starts, then write all three arrays coalesced
+      uint32_t i = ib;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      uint32_t sn[4] = {0u, 0u, 0u, 0u};
-      uint32_t m = clen == CB ? dfa_half<false, true>(S, w, h, clen, s, any, sn)
-                              : dfa_half<true, true>(S, w, h, clen, s, any, sn);
-      if (h == 0 && c0 == 0 && clen > 0) m |= 1u;
-      while (m) {
-        const uint32_t j = __ffs(m) - 1;
-        m &= m - 1;
-        const uint64_t pos = c0 + 32 * h + j;
-        uint32_t id = 0, len = 0;
-        if (prev) {
-          const uint64_t ps = prev - 1;
-          id = S.token_id[nibble(sn, j)];
-          if (id == 0xFEu) id = S.byte_token_id[__ldg(P.in + ps)];
-          len = uint32_t(pos - ps);
+      for (int h = 0; h < 2; ++h) {
+        uint32_t sn[4];
+        uint32_t m = emit_half(S, w, h, full, clen, s, sn);
+        if (h == 0 && c0 == 0 && clen > 0) m |= 1u;  // the first token starts at byte 0
+        while (m) {
+          const uint32_t j = __ffs(m) - 1;
+          m &= m - 1;
+          E.start[warp][i] = uint16_t(off0 + 32 * h + j);
+          E.state[warp][i] = uint8_t(nibble(sn, j));
+          ++i;
         }
-        if (staged) {
-          E.start[warp][i] = uint16_t(pos - pbase);
-          E.len[warp][i] = len;
-          E.id[warp][i] = uint8_t(id);
-        } else {
-          const uint64_t k = k0 + i;
-          if (prev && k - 1 < P.cap) { P.out_id[k - 1] = uint8_t(id); P.out_len[k - 1] = len; }
-          if (k < P.cap) P.out_start[k] = pos;
-          else if (!sizing) report(P.st, PP_ERR_CAPACITY, 0, false);
-        }
-        ++i;
-        prev = pos + 1;
       }
-    }
-    if (clen > 0 && c0 + clen == P.n) {  // close the last token
-      const uint64_t k = k0 + i;  // tokens in total
-      if (prev) {
-        const uint64_t ps = prev - 1;
-        uint32_t id = S.token_id[s];
-        if (id == 0xFEu) id = S.byte_token_id[__ldg(P.in + ps)];
-        const uint32_t len = uint32_t(P.n - ps);
-        if (staged) { E.len[warp][i] = len; E.id[warp][i] = uint8_t(id); }
-        else if (k - 1 < P.cap) { P.out_id[k - 1] = uint8_t(id); P.out_len[k - 1] = len; }
-      }
-    }
-    if (staged) {
+      if (owns_end) E.state[warp][i] = uint8_t(s);
       __syncwarp();
-      // starts of tokens k0 .. k0+total-1; ids and lengths of tokens
-      // k0-1 .. k0+total-2 (and k0+total-1 in the last piece)
-      const uint32_t nclose = total + (last_piece ? 1u : 0u);
+      // starts of tokens k0 .. k0+total-1; lengths and ids of the tokens
+      // they close, k0-1 .. k0+total-2, and of the last token in the last piece
+      const uint64_t prev = P.piece_prev[p];  // start + 1 of the token open at the piece start
+      const uint32_t nclose = total + (p + 1 == P.n_pieces ? 1u : 0u);
       for (uint32_t q = lane; q < nclose; q += 32) {
         const uint64_t k = k0 + q;
+        const uint64_t end = q < total ? pbase + E.start[warp][q] : P.n;
         if (q < total) {
-          if (k < P.cap) P.out_start[k] = pbase + E.start[warp][q];
+          if (k < P.cap) P.out_start[k] = end;
           else if (!sizing) report(P.st, PP_ERR_CAPACITY, 0, false);
         }
         if (k >= 1 && k - 1 < P.cap) {  // token k-1 exists (the first start closes none)
-          P.out_len[k - 1] = E.len[warp][q];
-          P.out_id[k - 1] = E.id[warp][q];
+          const uint64_t beg = q > 0 ? pbase + E.start[warp][q - 1] : prev - 1;
+          P.out_len[k - 1] = uint32_t(end - beg);
+          P.out_id[k - 1] = uint8_t(token_id(P, S, E.state[warp][q], beg));
         }
       }
       __syncwarp();
+    } else {
+      // ---- dense piece: every start writes its own triple entries
+      const uint32_t last = (info >> 11) & 0x7Fu;
+      uint64_t lp = last ? c0 + last : 0ull;  // positions grow with the lane: max = latest
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const uint64_t o = __shfl_up_sync(FULL, lp, d);
+        if (lane >= d) lp = max(lp, o);
+      }
+      uint64_t prev = __shfl_up_sync(FULL, lp, 1);  // start + 1 of the open token
+      if (lane == 0) prev = 0;
+      if (prev == 0) prev = P.piece_prev[p];
+      uint64_t k = k0 + ib;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t sn[4];
+        uint32_t m = emit_half(S, w, h, full, clen, s, sn);
+        if (h == 0 && c0 == 0 && clen > 0) m |= 1u;
+        while (m) {
+          const uint32_t j = __ffs(m) - 1;
+          m &= m - 1;
+          const uint64_t pos = c0 + 32 * h + j;
+          if (prev && k - 1 < P.cap) {
+            P.out_id[k - 1] = uint8_t(token_id(P, S, nibble(sn, j), prev - 1));
+            P.out_len[k - 1] = uint32_t(pos - (prev - 1));
+          }
+          if (k < P.cap) P.out_start[k] = pos;
+          else if (!sizing) report(P.st, PP_ERR_CAPACITY, 0, false);
+          ++k;
+          prev = pos + 1;
+        }
+      }
+      if (owns_end && prev && k - 1 < P.cap) {  // close the last token
+        P.out_id[k - 1] = uint8_t(token_id(P, S, s, prev - 1));
+        P.out_len[k - 1] = uint32_t(P.n - (prev - 1));
+      }
     }
   }
 }
@@ -642,12 +795,20 @@ cudaError_t launch_tokenize(const uint8_t* in, uint64_t n, const GenericDfa& dfa
     if ((e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
       return e;
   }
+  static bool attrs = false;
+  if (!attrs) {
+    if ((e = cudaFuncSetAttribute(tok_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  int(sizeof(RepTables)))) != cudaSuccess)
+      return e;
+    attrs = true;
+  }
   const uint32_t bgrid = std::min<uint32_t>((P.n_pieces + WW - 1) / WW, uint32_t(n_sm) * 4);
+  const uint32_t dgrid = std::min<uint32_t>((P.n_pieces + DW - 1) / DW, uint32_t(n_sm) * 2);
   tok_stv_kernel<<<bgrid, WT, 0, stream>>>(P);
   if (timed) stage_mark(2, stream);
   tok_state_scan_kernel<<<T, SCAN_T, 0, stream>>>(P);
   if (timed) stage_mark(3, stream);
-  tok_count_kernel<<<bgrid, WT, 0, stream>>>(P);
+  tok_count_kernel<<<dgrid, DT, sizeof(RepTables), stream>>>(P);
   if (timed) stage_mark(4, stream);
   tok_count_scan_kernel<<<T, SCAN_T, 0, stream>>>(P);
   if (timed) stage_mark(5, stream);
