@@ -24,7 +24,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libpp.so")
 
-PP_OK, PP_EINVAL, PP_ECUDA, PP_ENOMEM, PP_ETOOLARGE = 0, 1, 2, 3, 4
+PP_OK, PP_EINVAL, PP_ECUDA, PP_ENOMEM, PP_ETOOLARGE, PP_ECHUNK = 0, 1, 2, 3, 4, 5
 COL = {"str": 0, "i8": 1, "i32": 2, "i64": 3, "f64": 4, "skip": 5}
 DTYPE = {"i8": torch.int8, "i32": torch.int32, "i64": torch.int64, "f64": torch.float64}
 ERR_INVALID_INPUT, ERR_BAD_END_STATE, ERR_COLCOUNT = 1, 2, 4
@@ -68,6 +68,8 @@ def lib() -> ctypes.CDLL:
                                _sz, _vp, _vp, _vp]
         L.pp_parse_noalloc.restype = ctypes.c_int
         L.pp_parse_noalloc.argtypes = L.pp_parse.argtypes
+        L.pp_parse_host.restype = ctypes.c_int
+        L.pp_parse_host.argtypes = L.pp_parse.argtypes[:-1] + [_sz, _vp]
         L.pp_tokenize.restype = ctypes.c_int
         L.pp_tokenize.argtypes = [_vp, _sz, ctypes.POINTER(DfaDesc), _vp, _vp, _vp, _sz, _vp, _vp]
         L.pp_tags.restype = ctypes.c_int
@@ -226,8 +228,27 @@ def pp_count_byte(d_in, n_bytes, value: int, d_count, stream=None) -> None:
 
 
 # ------------------------------------------------------------- convenience
+def pp_parse_host(h_in: torch.Tensor, n_bytes: int, desc: DfaDesc, col_types, h_offsets,
+                  h_chars, h_typed, records_capacity: int, chars_capacity, h_status: torch.Tensor,
+                  chunk_bytes: int = 0, stream=None) -> None:
+    """Direct pp_parse_host call: input, outputs and status in host memory
+    (pinned for overlapped copies); returns when the results are there."""
+    n = len(col_types)
+    ct = (ctypes.c_int * n)(*[COL[c] if isinstance(c, str) else int(c) for c in col_types])
+    po = (_vp * n)(*[_ptr(x) for x in h_offsets])
+    pc = (_vp * n)(*[_ptr(x) for x in h_chars])
+    pt = (_vp * n)(*[_ptr(x) for x in h_typed])
+    cc = (_sz * n)(*[int(x) for x in chars_capacity])
+    rc = lib().pp_parse_host(_ptr(h_in), int(n_bytes), ctypes.byref(desc), n, ctypes.addressof(ct),
+                             ctypes.addressof(po), ctypes.addressof(pc), ctypes.addressof(pt),
+                             int(records_capacity), ctypes.addressof(cc), _ptr(h_status),
+                             int(chunk_bytes), _stream(stream))
+    _check(rc, "pp_parse_host")
+
+
 class CsvOutputs:
-    """Preallocated pp_parse outputs for one input size / schema."""
+    """Preallocated pp_parse outputs for one input size / schema: device
+    tensors, or pinned host tensors with device="cpu" (for pp_parse_host)."""
 
     def __init__(self, col_types, records_capacity: int, chars_capacity, device="cuda"):
         self.col_types = list(col_types)
@@ -235,20 +256,20 @@ class CsvOutputs:
         self.chars_capacity = [int(chars_capacity[i]) if t == "str" else 0
                                for i, t in enumerate(self.col_types)]
         self.offsets, self.chars, self.typed = [], [], []
+        host = torch.device(device).type == "cpu"
+        kw = dict(device=device, pin_memory=True) if host else dict(device=device)
         for i, t in enumerate(self.col_types):
             if t == "str":
-                self.offsets.append(torch.empty(self.records_capacity + 1, dtype=torch.int32,
-                                                device=device))
-                self.chars.append(torch.empty(max(self.chars_capacity[i], 1), dtype=torch.uint8,
-                                              device=device))
+                self.offsets.append(torch.empty(self.records_capacity + 1, dtype=torch.int32, **kw))
+                self.chars.append(torch.empty(max(self.chars_capacity[i], 1), dtype=torch.uint8, **kw))
                 self.typed.append(None)
             elif t == "skip":
                 self.offsets.append(None); self.chars.append(None); self.typed.append(None)
             else:
                 self.offsets.append(None); self.chars.append(None)
-                self.typed.append(torch.empty(max(self.records_capacity, 1), dtype=DTYPE[t],
-                                              device=device))
-        self.status = new_status(device)
+                self.typed.append(torch.empty(max(self.records_capacity, 1), dtype=DTYPE[t], **kw))
+        self.status = (torch.empty(STATUS_BYTES, dtype=torch.uint8, pin_memory=True) if host
+                       else new_status(device))
 
     def run(self, d_in: torch.Tensor, n_bytes: int, desc: DfaDesc, stream=None) -> None:
         pp_parse(d_in, n_bytes, desc, self.col_types, self.offsets, self.chars, self.typed,
@@ -258,6 +279,12 @@ class CsvOutputs:
         pp_parse_noalloc(d_in, n_bytes, desc, self.col_types, self.offsets, self.chars,
                          self.typed, self.records_capacity, self.chars_capacity, self.status,
                          stream)
+
+    def run_host(self, h_in: torch.Tensor, n_bytes: int, desc: DfaDesc, chunk_bytes: int = 0,
+                 stream=None) -> None:
+        """pp_parse_host of a host input into these (host) outputs."""
+        pp_parse_host(h_in, n_bytes, desc, self.col_types, self.offsets, self.chars, self.typed,
+                      self.records_capacity, self.chars_capacity, self.status, chunk_bytes, stream)
 
     def output_bytes(self, n_records: int, chars_len) -> int:
         """Bytes the parse writes: offsets, chars and typed values."""

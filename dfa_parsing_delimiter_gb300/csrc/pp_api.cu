@@ -243,6 +243,7 @@ const char* pp_strerror(int code) {
     case PP_ECUDA: return "CUDA error";
     case PP_ENOMEM: return "out of device memory";
     case PP_ETOOLARGE: return "input needs more scratch than the fixed buffer holds";
+    case PP_ECHUNK: return "a record is longer than the streaming chunk";
     default: return "unknown error";
   }
 }

@@ -56,6 +56,12 @@ struct ParseParams {
   void* typed[PP_MAX_COLS];
   uint64_t rec_cap;
   pp_status* st;
+  // Partial mode (streaming chunks), when not null: the input ends inside
+  // an unfinished record, which is neither closed nor checked for an
+  // accepting end state; st->n_records counts the complete records only,
+  // and *record_end receives 1 + the position of the last record delimiter
+  // (atomic maximum; the caller zeroes it).
+  unsigned long long* record_end;
   ParseScratch s;
 };
 

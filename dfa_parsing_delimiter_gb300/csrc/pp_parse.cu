@@ -1153,6 +1153,7 @@ struct MainShared {
   uint32_t warp_stv[NW];
   uint32_t warp_rec[NW], warp_col[NW], warp_last[NW];
   uint32_t rows;             // records touched by the tile (#RD + 1)
+  uint32_t wrd[NW];          // partial mode: per warp, 1 + its last record delimiter in the tile
   uint32_t col_end;          // fields of the last row closed in the tile
   uint32_t wsum[NW];
   uint32_t cstart[ppi::MAX_STR_COLS + 1];  // staging start per string column (this pass)
@@ -1230,10 +1231,16 @@ __global__ void __launch_bounds__(NT, 2) main_kernel(const __grid_constant__ Par
     if (g.inv_at < clen && s_chunk != 4)
       report(P.st, PP_ERR_INVALID_INPUT, tile_base + cstart + g.inv_at, true);
     const bool owns_end = last_tile && clen > 0 && cstart + clen == tile_len;
-    if (owns_end && g.end != 4 && !((P.accept_mask >> g.end) & 1u))
+    const bool partial = P.record_end != nullptr;
+    if (!partial && owns_end && g.end != 4 && !((P.accept_mask >> g.end) & 1u))
       report(P.st, PP_ERR_BAD_END_STATE, P.n, true);
-    const bool virt_rd = owns_end && g.end != 4 && ((P.accept_mask >> g.end) & 1u) &&
+    const bool virt_rd = !partial && owns_end && g.end != 4 && ((P.accept_mask >> g.end) & 1u) &&
                          !((rd >> (clen - 1)) & 1u);
+    if (partial) {
+      const uint32_t mine = rd ? cstart + 32u - __clz(rd) : 0u;
+      const uint32_t wm = __reduce_max_sync(FULL, mine);
+      if (lane == 0) S.wrd[warp] = wm;
+    }
 
     // ---- record, column and field start at the chunk start (block scan)
     V2 vi = chunk_v2(g);
@@ -1268,6 +1275,11 @@ __global__ void __launch_bounds__(NT, 2) main_kernel(const __grid_constant__ Par
       }
     }
     const bool any_virt = __syncthreads_or(virt_rd) != 0;
+    if (partial && t == 0) {
+      uint32_t m = 0;
+      for (int q = 0; q < NW; ++q) m = max(m, S.wrd[q]);
+      if (m) atomicMax(P.record_end, static_cast<unsigned long long>(tile_base + m));
+    }
     const V2 pre = op2_32(V2{S.warp_rec[warp], S.warp_col[warp], S.warp_last[warp]}, lex);
     const uint64_t rec0 = ph.rec0;
     const uint32_t rows = S.rows;

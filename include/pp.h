@@ -49,7 +49,10 @@ extern "C" {
 #define PP_MAX_GROUPS 16
 
 /* host return codes */
-typedef enum { PP_OK = 0, PP_EINVAL = 1, PP_ECUDA = 2, PP_ENOMEM = 3, PP_ETOOLARGE = 4 } pp_rc;
+typedef enum {
+  PP_OK = 0, PP_EINVAL = 1, PP_ECUDA = 2, PP_ENOMEM = 3, PP_ETOOLARGE = 4,
+  PP_ECHUNK = 5 /* pp_parse_host: a record longer than the streaming chunk */
+} pp_rc;
 
 /* column kinds for pp_parse */
 typedef enum {
@@ -153,6 +156,42 @@ pp_rc pp_parse(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa, int 
                uint8_t* const out_chars[], void* const out_typed[],
                size_t records_capacity, const size_t chars_capacity[],
                pp_status* d_status, cudaStream_t stream);
+
+/*
+ * pp_parse_host — pp_parse of an input in HOST memory into outputs in HOST
+ * memory, streamed through the device in chunks (the streaming set-up of
+ * ParPaRaw Section 4: partitions move to the device while earlier ones are
+ * parsed and their results move back).
+ *   h_in, h_offsets[], h_chars[], h_typed[], h_status: host memory, laid
+ *   out and filled exactly as pp_parse fills its device buffers (offsets
+ *   [records + 1] int32 per string column, chars, one typed array per
+ *   numeric column, and the status).  Page-locked (pinned) host memory lets
+ *   the copies run asynchronously and overlap the parse; pageable memory
+ *   works, with the copies staged by the driver.
+ *   records_capacity, chars_capacity[]: as in pp_parse, for the whole input.
+ *   chunk_bytes: bytes of new input per chunk (rounded up to a multiple of
+ *   pp_tile_bytes(); 0 = 128 MiB).  Each chunk after the first begins with
+ *   the bytes of the record left unfinished at the end of the one before,
+ *   so a record may be at most chunk_bytes long; a longer one stops the
+ *   call with PP_ECHUNK (h_status then holds the records emitted so far
+ *   and PP_ERR_CAPACITY at the offending record).
+ *   stream: parses run on it; the copies in each direction run on a
+ *   stream of their own that the call creates.  The call returns once
+ *   every result is in host memory.
+ *   Device memory: two input buffers of 2 x chunk_bytes, two staging
+ *   buffers of chunk_bytes and two sets of output buffers, each for
+ *   min(records_capacity, 2 x chunk_bytes) + 1 records (chars per string
+ *   column min(chars_capacity, 2 x chunk_bytes)), from the stream-ordered
+ *   allocator.  The call sets the device's default memory pool to keep
+ *   freed memory (release threshold: unlimited), so later calls reuse it.
+ * Returns PP_EINVAL for bad arguments, PP_ECHUNK as above, PP_ENOMEM /
+ * PP_ECUDA on CUDA errors.
+ */
+pp_rc pp_parse_host(const uint8_t* h_in, size_t n_bytes, const pp_dfa_desc* dfa, int n_cols,
+                    const pp_coltype* col_types, int32_t* const h_offsets[],
+                    uint8_t* const h_chars[], void* const h_typed[], size_t records_capacity,
+                    const size_t chars_capacity[], pp_status* h_status, size_t chunk_bytes,
+                    cudaStream_t stream);
 
 /* Size of pp_parse_noalloc's fixed scratch buffer (per device). */
 #define PP_NOALLOC_SCRATCH_BYTES (4u << 20)
