@@ -328,8 +328,9 @@ def run_ours(args):
     e2e_steps = 0 if args.no_e2e else max(1, min(args.steps, 3))
     e2e_t = []
     h2d = d2h = 0
-    if csv and e2e_steps:  # pinned host outputs, allocated once like the device ones
-        host_out = pp.CsvOutputs(w["cols"], R, chars_cap, device="cpu")
+    if e2e_steps:  # pinned host outputs, allocated once like the device ones
+        host_out = (pp.CsvOutputs(w["cols"], R, chars_cap, device="cpu") if csv
+                    else pp.TokenOutputs(T))
     for i in range(e2e_steps + 1 if e2e_steps else 0):
         torch.cuda.synchronize()
         t0 = time.perf_counter()
@@ -339,7 +340,9 @@ def run_ours(args):
             h2d = n
             d2h = host_out.output_bytes(est["n_records"], est["chars_len"]) + pp.STATUS_BYTES
         else:
-            _, est, h2d, d2h = pp.tokenize_host(h_in)
+            est = host_out.run_host(h_in, n, desc, stream=stream)
+            h2d = n
+            d2h = 13 * est["n_tokens"] + pp.STATUS_BYTES
         dt = time.perf_counter() - t0
         assert est["error"] == 0, est
         if i > 0:
@@ -377,7 +380,8 @@ def run_ours(args):
                 "d2h_bytes_per_step": d2h,
                 "api": "CsvOutputs.run_host (pp_parse_host: chunked host->device, parse, "
                        "device->host overlap) into pinned host outputs" if csv else
-                       "tokenize_host"},
+                       "TokenOutputs.run_host (pp_tokenize_host: chunked host->device, lexing, "
+                       "device->host overlap) into pinned host triples"},
         "clocks": clk.summary(),
         "gpu_launches": launches_per_step * args.steps,
         "wall_s_timed_region": wall,

@@ -70,6 +70,9 @@ def lib() -> ctypes.CDLL:
         L.pp_parse_noalloc.argtypes = L.pp_parse.argtypes
         L.pp_parse_host.restype = ctypes.c_int
         L.pp_parse_host.argtypes = L.pp_parse.argtypes[:-1] + [_sz, _vp]
+        L.pp_tokenize_host.restype = ctypes.c_int
+        L.pp_tokenize_host.argtypes = [_vp, _sz, ctypes.POINTER(DfaDesc), _vp, _vp, _vp, _sz, _vp,
+                                       _sz, _vp]
         L.pp_tokenize.restype = ctypes.c_int
         L.pp_tokenize.argtypes = [_vp, _sz, ctypes.POINTER(DfaDesc), _vp, _vp, _vp, _sz, _vp, _vp]
         L.pp_tags.restype = ctypes.c_int
@@ -244,6 +247,40 @@ def pp_parse_host(h_in: torch.Tensor, n_bytes: int, desc: DfaDesc, col_types, h_
                              int(records_capacity), ctypes.addressof(cc), _ptr(h_status),
                              int(chunk_bytes), _stream(stream))
     _check(rc, "pp_parse_host")
+
+
+def pp_tokenize_host(h_in: torch.Tensor, n_bytes: int, desc: DfaDesc, h_ids, h_starts, h_lens,
+                     capacity: int, h_status: torch.Tensor, chunk_bytes: int = 0,
+                     stream=None) -> None:
+    """Direct pp_tokenize_host call: input, triples and status in host memory
+    (pinned for overlapped copies); returns when the results are there."""
+    rc = lib().pp_tokenize_host(_ptr(h_in), int(n_bytes), ctypes.byref(desc), _ptr(h_ids),
+                                _ptr(h_starts), _ptr(h_lens), int(capacity), _ptr(h_status),
+                                int(chunk_bytes), _stream(stream))
+    _check(rc, "pp_tokenize_host")
+
+
+class TokenOutputs:
+    """Preallocated pinned host triples (ids u8, starts i64, lens i32) for
+    pp_tokenize_host."""
+
+    def __init__(self, capacity: int):
+        self.capacity = int(capacity)
+        n = max(self.capacity, 1)
+        self.ids = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+        self.starts = torch.empty(n, dtype=torch.int64, pin_memory=True)
+        self.lens = torch.empty(n, dtype=torch.int32, pin_memory=True)
+        self.status = torch.empty(STATUS_BYTES, dtype=torch.uint8, pin_memory=True)
+
+    def run_host(self, h_in: torch.Tensor, n_bytes: int, desc: DfaDesc, chunk_bytes: int = 0,
+                 stream=None) -> dict:
+        pp_tokenize_host(h_in, n_bytes, desc, self.ids, self.starts, self.lens, self.capacity,
+                         self.status, chunk_bytes, stream)
+        return read_status(self.status)
+
+    def results(self, status: dict):
+        T = min(status["n_tokens"], self.capacity)
+        return self.ids[:T], self.starts[:T], self.lens[:T]
 
 
 class CsvOutputs:

@@ -155,6 +155,9 @@ bool parse_dfa_ok(const pp_dfa_desc* d) {
 
 namespace ppi {
 
+bool generic_dfa_ok(const pp_dfa_desc* d) { return dfa_ok(d, PP_MAX_STATES); }
+GenericDfa to_generic_dfa(const pp_dfa_desc* d) { return to_generic(d); }
+
 // Host half of pp_parse: checks the arguments and fills the kernel
 // parameters (everything but the scratch carve).
 pp_rc parse_prepare(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa, int n_cols,

@@ -105,10 +105,14 @@ cudaError_t launch_tags(const uint8_t* in, uint64_t n, const GenericDfa& dfa,
                         size_t scratch_bytes, cudaStream_t stream);
 size_t tags_scratch_bytes(uint64_t n);
 
+// carry_out: partial mode (see TokParams in pp_tokenize.cu), or null
 cudaError_t launch_tokenize(const uint8_t* in, uint64_t n, const GenericDfa& dfa,
                             uint8_t* out_id, uint64_t* out_start, uint32_t* out_len,
                             uint64_t cap, pp_status* st, void* scratch, size_t scratch_bytes,
-                            cudaStream_t stream);
+                            cudaStream_t stream, unsigned long long* carry_out = nullptr);
+// pp_tokenize's checks of a descriptor, and its conversion
+bool generic_dfa_ok(const pp_dfa_desc* d);
+GenericDfa to_generic_dfa(const pp_dfa_desc* d);
 size_t tokenize_scratch_bytes(uint64_t n);
 
 cudaError_t launch_count_byte(const uint8_t* in, uint64_t n, uint8_t value, uint64_t* d_count,

@@ -74,6 +74,11 @@ struct TokParams {
   uint32_t* piece_last;   // [pieces] offset + 1 of the piece's last token start (0: none)
   uint64_t* piece_k0;     // [pieces] index of the piece's first token start
   uint64_t* piece_prev;   // [pieces] start + 1 of the token open at the piece start (0: none)
+  // Partial mode (streaming chunks), when not null: the input ends inside
+  // its last token, which is left open (no length, id or end-state check);
+  // carry_out[0] = 1 + the last token start, carry_out[1] = the DFA state
+  // before it.
+  unsigned long long* carry_out;
 };
 
 // ------------------------------------------------------------ input
@@ -355,7 +360,7 @@ __global__ void __launch_bounds__(DT, 2) tok_count_kernel(const __grid_constant_
     if (s == inv && s0 != inv)
       report(P.st, PP_ERR_INVALID_INPUT, c0 + first_invalid(P, R, c0, clen, lane4, (s0 << 7) | lane4),
              true);
-    if (clen > 0 && c0 + clen == P.n && s != inv && !((P.dfa.accept_mask >> s) & 1u))
+    if (!P.carry_out && clen > 0 && c0 + clen == P.n && s != inv && !((P.dfa.accept_mask >> s) & 1u))
       report(P.st, PP_ERR_BAD_END_STATE, P.n, true);
     const uint32_t cnt = __popc(m0) + __popc(m1);
     const uint32_t last = m1 ? 64u - __clz(m1) : m0 ? 32u - __clz(m0) : 0u;
@@ -448,9 +453,26 @@ __global__ void __launch_bounds__(SCAN_T) tok_count_scan_kernel(const __grid_con
       P.piece_prev[idx] = pv;
       k += c[e];
       if (l[e]) pv = l[e];
-      if (idx + 1 == P.n_pieces) P.st->n_tokens = k;
+      if (idx + 1 == P.n_pieces) {
+        P.st->n_tokens = k;
+        if (P.carry_out) P.carry_out[0] = pv;
+      }
     }
   }
+}
+
+// Partial mode: the DFA state before the last token start, re-run over the
+// bytes of its chunk before it from the chunk's start state (one thread).
+__global__ void tok_carry_kernel(const __grid_constant__ TokParams P) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  const uint64_t ls1 = P.carry_out[0];
+  if (ls1 == 0) { P.carry_out[1] = P.dfa.start_state; return; }
+  const uint64_t ls = ls1 - 1, p = ls / PIECE;
+  const uint32_t lane = uint32_t(ls % PIECE) / CB;
+  uint32_t s = P.lane_info[size_t(p) * 32 + lane] & 0xFu;
+  for (uint64_t j = p * PIECE + uint64_t(lane) * CB; j < ls; ++j)
+    s = P.dfa.delta[P.dfa.byte_to_group[P.in[j]] & 0xFu][s] & 0xFu;
+  P.carry_out[1] = s;
 }
 
 // ------------------------------------------------------------ pass 5 tables
@@ -637,7 +659,7 @@ __global__ void __launch_bounds__(WT, 4) tok_emit_kernel(const __grid_constant__
       // starts of tokens k0 .. k0+total-1; lengths and ids of the tokens
       // they close, k0-1 .. k0+total-2, and of the last token in the last piece
       const uint64_t prev = P.piece_prev[p];  // start + 1 of the token open at the piece start
-      const uint32_t nclose = total + (p + 1 == P.n_pieces ? 1u : 0u);
+      const uint32_t nclose = total + (p + 1 == P.n_pieces && !P.carry_out ? 1u : 0u);
       for (uint32_t q = lane; q < nclose; q += 32) {
         const uint64_t k = k0 + q;
         const uint64_t end = q < total ? pbase + E.start[warp][q] : P.n;
@@ -684,7 +706,7 @@ __global__ void __launch_bounds__(WT, 4) tok_emit_kernel(const __grid_constant__
           prev = pos + 1;
         }
       }
-      if (owns_end && prev && k - 1 < P.cap) {  // close the last token
+      if (!P.carry_out && owns_end && prev && k - 1 < P.cap) {  // close the last token
         P.out_id[k - 1] = uint8_t(token_id(P, S, s, prev - 1));
         P.out_len[k - 1] = uint32_t(P.n - (prev - 1));
       }
@@ -748,7 +770,7 @@ size_t tokenize_scratch_bytes(uint64_t n) { return layout_of(n).total; }
 cudaError_t launch_tokenize(const uint8_t* in, uint64_t n, const GenericDfa& dfa,
                             uint8_t* out_id, uint64_t* out_start, uint32_t* out_len,
                             uint64_t cap, pp_status* st, void* scratch, size_t,
-                            cudaStream_t stream) {
+                            cudaStream_t stream, unsigned long long* carry_out) {
   TokParams P{};
   P.in = in;
   P.n = n;
@@ -761,6 +783,7 @@ cudaError_t launch_tokenize(const uint8_t* in, uint64_t n, const GenericDfa& dfa
   P.out_len = out_len;
   P.cap = cap;
   P.st = st;
+  P.carry_out = carry_out;
   const uint32_t T = scan_tiles_of(P.n_pieces);
   const Layout L = layout_of(n);
   uint8_t* b = static_cast<uint8_t*>(scratch);
@@ -811,6 +834,7 @@ cudaError_t launch_tokenize(const uint8_t* in, uint64_t n, const GenericDfa& dfa
   tok_count_kernel<<<dgrid, DT, sizeof(RepTables), stream>>>(P);
   if (timed) stage_mark(4, stream);
   tok_count_scan_kernel<<<T, SCAN_T, 0, stream>>>(P);
+  if (carry_out) tok_carry_kernel<<<1, 32, 0, stream>>>(P);
   if (timed) stage_mark(5, stream);
   const bool sizing = cap == 0 && out_start == nullptr;
   if (!sizing) tok_emit_kernel<<<bgrid, WT, 0, stream>>>(P);

@@ -193,6 +193,26 @@ pp_rc pp_parse_host(const uint8_t* h_in, size_t n_bytes, const pp_dfa_desc* dfa,
                     const size_t chars_capacity[], pp_status* h_status, size_t chunk_bytes,
                     cudaStream_t stream);
 
+/*
+ * pp_tokenize_host — pp_tokenize of an input in HOST memory into triples in
+ * HOST memory, streamed through the device in chunks as pp_parse_host does.
+ *   h_in, h_token_id, h_start, h_len, h_status: host memory (pinned for
+ *   overlapped copies), filled as pp_tokenize fills its device buffers;
+ *   tokens_capacity = 0 with null outputs counts the tokens only.
+ *   chunk_bytes: as for pp_parse_host.  Each chunk after the first begins
+ *   at the start of the token left open at the end of the one before, in
+ *   the DFA state that token started from, so a token may be at most
+ *   chunk_bytes long; a longer one returns PP_ECHUNK.
+ *   Device memory: the input buffers of pp_parse_host, plus two sets of
+ *   triples for min(tokens_capacity, 2 x chunk_bytes) + 1 tokens.
+ * Returns PP_EINVAL for bad arguments, PP_ECHUNK as above, PP_ENOMEM /
+ * PP_ECUDA on CUDA errors.
+ */
+pp_rc pp_tokenize_host(const uint8_t* h_in, size_t n_bytes, const pp_dfa_desc* dfa,
+                       uint8_t* h_token_id, uint64_t* h_start, uint32_t* h_len,
+                       size_t tokens_capacity, pp_status* h_status, size_t chunk_bytes,
+                       cudaStream_t stream);
+
 /* Size of pp_parse_noalloc's fixed scratch buffer (per device). */
 #define PP_NOALLOC_SCRATCH_BYTES (4u << 20)
 

@@ -115,3 +115,64 @@ def test_host_stream_rejects_record_longer_than_chunk():
         host.run_host(h_in, arr.size, desc, chunk_bytes=16 << 10)
     st = pp.read_status(host.status, 2)
     assert st["error"] & pp.ERR_CAPACITY and st["n_records"] == 1
+
+
+# ---------------------------------------------------------------- tokens
+def _device_tokens(arr, desc):
+    n = arr.size
+    d_in = to_dev(arr)
+    st = pp.new_status()
+    pp.pp_tokenize(d_in, n, desc, None, None, None, 0, st)
+    T = pp.read_status(st)["n_tokens"]
+    ids = torch.empty(max(T, 1), dtype=torch.uint8, device="cuda")
+    starts = torch.empty(max(T, 1), dtype=torch.int64, device="cuda")
+    lens = torch.empty(max(T, 1), dtype=torch.int32, device="cuda")
+    pp.pp_tokenize(d_in, n, desc, ids, starts, lens, T, st)
+    s = pp.read_status(st)
+    return (ids[:T].cpu(), starts[:T].cpu(), lens[:T].cpu()), s
+
+
+def _host_tokens(arr, desc, cap, chunk):
+    h_in = torch.empty(max(arr.size, 1), dtype=torch.uint8, pin_memory=True)
+    if arr.size:
+        h_in[:arr.size].copy_(torch.from_numpy(arr))
+    out = pp.TokenOutputs(cap)
+    s = out.run_host(h_in, arr.size, desc, chunk_bytes=chunk)
+    return out.results(s), s, out
+
+
+@pytest.mark.parametrize("target,chunk", [(2 << 20, 16 << 10), (6 << 20, 1 << 20), (1 << 20, 0)])
+def test_host_tokens_match_device_tokens(target, chunk):
+    data, info, _ = datagen.generate("json_2gib", target=target)
+    desc = pp.desc_json_lexer()
+    (di, ds_, dl), sd = _device_tokens(data, desc)
+    assert sd["error"] == 0 and sd["n_tokens"] == info["n_tokens"]
+    (hi, hs, hl), sh, _ = _host_tokens(data, desc, sd["n_tokens"], chunk)
+    assert sh["error"] == 0 and sh["n_tokens"] == sd["n_tokens"]
+    assert torch.equal(hi, di) and torch.equal(hs, ds_) and torch.equal(hl, dl)
+
+
+def test_host_tokens_dense_long_and_errors():
+    desc = pp.desc_json_lexer()
+    # one-byte tokens everywhere, then a string token longer than a tile
+    dense = b"[" + b",".join(b"1" for _ in range(30000)) + b"]"
+    long_str = b'"' + b"ab\\\"cd" * 5000 + b'"'
+    arr = np.frombuffer(dense + b" " + long_str + b" " + dense, np.uint8)
+    (di, ds_, dl), sd = _device_tokens(arr, desc)
+    assert sd["error"] == 0
+    (hi, hs, hl), sh, _ = _host_tokens(arr, desc, sd["n_tokens"], 48 << 10)
+    assert sh["n_tokens"] == sd["n_tokens"] and sh["error"] == 0
+    assert torch.equal(hi, di) and torch.equal(hs, ds_) and torch.equal(hl, dl)
+    # a token longer than the chunk
+    with pytest.raises(RuntimeError, match=r"pp_tokenize_host failed: .*\(5\)"):
+        _host_tokens(arr, desc, sd["n_tokens"], 16 << 10)
+    # an invalid byte in a later chunk: same first error offset as on the device
+    bad = bytearray(dense * 3)
+    p = len(bad) * 2 // 3
+    bad[p] = 0x01
+    arr = np.frombuffer(bytes(bad), np.uint8)
+    _, sd = _device_tokens(arr, desc)
+    assert sd["error"] & pp.ERR_INVALID_INPUT
+    _, sh, _ = _host_tokens(arr, desc, max(sd["n_tokens"], 1), 16 << 10)
+    assert sh["error"] & pp.ERR_INVALID_INPUT
+    assert sh["first_error_offset"] == sd["first_error_offset"]
