@@ -4,8 +4,8 @@
 //
 // The input is cut into pieces of 2 KiB, one per warp, 64 bytes per lane.
 //   1. stv    Per lane, the state-transition vector of its 64 bytes
-//             (ParPaRaw Section 3.1, Figure 2), built back to front two bytes
-//             at a time from a table of composed byte-pair transitions; a
+//             (ParPaRaw Section 3.1, Figure 2), built back to front three
+//             bytes at a time from a table of composed transitions; a
 //             warp scan gives each lane the vector of the bytes before it in
 //             the piece, and lane 31 the piece's vector.
 //   2. scan   Exclusive composite scan of the piece vectors (decoupled
