@@ -266,7 +266,7 @@ def run_ours(args):
 
         def step():
             out.run(d_in, n, desc, stream)
-        launches_per_step = 4  # init, context pass, scan, main pass
+        launches_per_step = 6  # init, tile vectors, tile states, context pass, scan, main pass
     else:
         desc = pp.desc_json_lexer()
         T = info["n_tokens"]
@@ -315,7 +315,8 @@ def run_ours(args):
     path_s = float(np.mean(step_ms)) / 1e3
     st_ms = pp.debug_stage_ms(args.steps)
     pp.debug_stage_timing(0)
-    names = (["init", "ctx_kernel", "scan_kernel", "main_kernel"] if csv else
+    names = (["init", "tile_stv_kernel", "tile_state_kernel", "ctx_kernel", "scan_kernel",
+              "main_kernel"] if csv else
              ["init", "tok_stv_kernel", "tok_state_scan_kernel", "tok_count_kernel",
               "tok_count_scan_kernel", "tok_emit_kernel"])
     stages = {k: float(st_ms[:, i].mean()) for i, k in enumerate(names)}

@@ -146,7 +146,7 @@ def debug_stage_timing(n_calls: int) -> None:
 
 def debug_stage_ms(max_calls: int):
     """Per-call kernel durations (ms) recorded since debug_stage_timing, one
-    row of STAGES per call: pp_parse (init, context, scan, main, 0, 0),
+    row of STAGES per call: pp_parse (init, tile vectors, tile states, context, scan, main),
     pp_tokenize (init, stv, state scan, count, count scan, emit)."""
     import numpy as np
     out = np.zeros((max(int(max_calls), 1), STAGES), dtype=np.float32)

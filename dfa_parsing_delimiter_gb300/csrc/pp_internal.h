@@ -17,11 +17,18 @@ constexpr int MAX_STR_COLS = 16;  // string columns per pp_parse call
 //         last terminator before the tile, chars offset per string column.
 //   scan_*: cross-block look-back state of the scan kernel (a: contexts,
 //         c: chars offsets).
+//   tile_stv, tile_state: per tile, its transition vector and its true
+//         start state (from the tile-state scan, whose look-back words are
+//         tstate_words).
 struct ParseScratch {
   uint8_t* ctx;
   uint8_t* pre;
   uint32_t ctx_stride, pre_stride;
-  uint32_t* counters;       // [0] context pass, [1] main pass, [2] scan tickets
+  uint32_t* counters;       // [0] context pass, [1] main pass, [2] scan, [3] tile-state scan tickets
+  uint32_t* tile_stv;       // [n_tiles]
+  uint8_t* tile_state;      // [n_tiles]
+  unsigned long long* tstate_words;  // [n_tstate_blocks]
+  uint32_t n_tstate_blocks;
   uint32_t* scan_flag_a;    // [n_scan_blocks]
   uint64_t* scan_agg_a;     // [n_scan_blocks][13]
   uint64_t* scan_inc_a;

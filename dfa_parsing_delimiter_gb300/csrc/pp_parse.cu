@@ -446,37 +446,146 @@ __device__ __forceinline__ void load_lut(const ParseParams& P, uint32_t* lut_s) 
   for (int k = threadIdx.x; k < 256 * 32; k += NT) lut_s[k] = P.lut[k >> 5];
 }
 
+// ======================================================= 0. tile start states
+// The context pass works from each tile's true start state, found first by a
+// transition-vector pass (ParPaRaw Section 3.1) and an exclusive composite
+// scan over tiles.
+constexpr int TV_NT = 256;              // tile-vector pass: a warp per tile
+constexpr int TV_BYTES = TILE / 32;     // bytes per lane
+constexpr int TS_NT = 256, TS_TPT = 16; // tile-state scan: tiles per thread
+constexpr int TS_TILES = TS_NT * TS_TPT;
+
+// Transition vector of each tile: one warp per tile, each lane folding
+// TV_BYTES bytes back to front, a warp scan composing the lanes in order.
+__global__ void __launch_bounds__(TV_NT) tile_stv_kernel(const __grid_constant__ ParseParams P) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint32_t* lut_s = reinterpret_cast<uint32_t*>(smem);
+  for (int k = threadIdx.x; k < 256 * 32; k += TV_NT) lut_s[k] = P.lut[k >> 5];
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const uint32_t* my_lut = lut_s + lane;
+  const bool aligned = (reinterpret_cast<uintptr_t>(P.in) & 15) == 0;
+  const uint32_t warps = gridDim.x * (TV_NT / 32);
+  for (uint32_t tile = blockIdx.x * (TV_NT / 32) + (threadIdx.x >> 5); tile < P.n_tiles;
+       tile += warps) {
+    const uint64_t b0 = uint64_t(tile) * TILE + uint64_t(lane) * TV_BYTES;
+    const uint32_t len = b0 < P.n ? uint32_t(min(uint64_t(TV_BYTES), P.n - b0)) : 0u;
+    uint32_t G = STV_ID;
+    if (len == TV_BYTES && aligned) {
+      // back to front in steps of 64 bytes, the next step's loads in flight
+      // while the current one folds
+      constexpr int STEPS = TV_BYTES / 64;
+      const uint4* src = reinterpret_cast<const uint4*>(P.in + b0);
+      uint4 cur[4], nxt[4] = {};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) cur[k] = __ldg(src + 4 * (STEPS - 1) + k);
+      for (int step = STEPS - 1; step >= 0; --step) {
+        if (step > 0) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) nxt[k] = __ldg(src + 4 * (step - 1) + k);
+        }
+#pragma unroll
+        for (int k = 3; k >= 0; --k) {
+          const uint32_t wq[4] = {cur[k].x, cur[k].y, cur[k].z, cur[k].w};
+#pragma unroll
+          for (int j = 15; j >= 0; --j)
+            G = __byte_perm(G, STV_INV_POOL, my_lut[((wq[j >> 2] >> (8 * (j & 3))) & 0xFFu) << 5]);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) cur[k] = nxt[k];
+      }
+    } else {
+      for (int j = int(len) - 1; j >= 0; --j)
+        G = __byte_perm(G, STV_INV_POOL, my_lut[uint32_t(__ldg(P.in + b0 + j)) << 5]);
+    }
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const uint32_t o = __shfl_up_sync(FULL, G, d);
+      if (lane >= d) G = stv_compose(o, G);
+    }
+    if (lane == 31) P.s.tile_stv[tile] = G;
+  }
+}
+
+// Exclusive composite scan of the tile vectors (single-pass decoupled
+// look-back between blocks, bounded waits), applied to the start state.
+__global__ void __launch_bounds__(TS_NT) tile_state_kernel(const __grid_constant__ ParseParams P) {
+  __shared__ uint32_t blk_s, wv[TS_NT / 32], pre_s;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  if (t == 0) blk_s = atomicAdd(&P.s.counters[3], 1u);
+  __syncthreads();
+  const uint32_t blk = blk_s;
+  const uint32_t t0 = blk * TS_TILES + uint32_t(t) * TS_TPT;
+  uint32_t v[TS_TPT];
+  uint32_t acc = STV_ID;
+#pragma unroll
+  for (int e = 0; e < TS_TPT; ++e) {
+    v[e] = t0 + e < P.n_tiles ? P.s.tile_stv[t0 + e] : STV_ID;
+    acc = stv_compose(acc, v[e]);
+  }
+  uint32_t inc = acc;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const uint32_t o = __shfl_up_sync(FULL, inc, d);
+    if (lane >= d) inc = stv_compose(o, inc);
+  }
+  uint32_t lex = __shfl_up_sync(FULL, inc, 1);
+  if (lane == 0) lex = STV_ID;
+  if (lane == 31) wv[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    constexpr int W = TS_NT / 32;
+    const uint32_t x0 = lane < W ? wv[lane] : STV_ID;
+    uint32_t x = x0;
+#pragma unroll
+    for (int d = 1; d < W; d <<= 1) {
+      const uint32_t o = __shfl_up_sync(FULL, x, d);
+      if (lane >= d) x = stv_compose(o, x);
+    }
+    uint32_t xe = __shfl_up_sync(FULL, x, 1);
+    if (lane == 0) xe = STV_ID;
+    const uint32_t agg = __shfl_sync(FULL, x, W - 1);
+    __syncwarp();
+    if (lane < W) wv[lane] = xe;
+    const uint32_t pre = lookback_word(P.s.tstate_words, blk, agg, STV_ID, STV_ID,
+                                       [](uint32_t a, uint32_t b) { return stv_compose(a, b); },
+                                       LookbackCfg{P.st, P.spin_limit});
+    if (lane == 0) pre_s = pre;
+  }
+  __syncthreads();
+  uint32_t s = stv_apply(pre_s, P.start_state);
+  s = stv_apply(wv[warp], s);
+  s = stv_apply(lex, s);
+#pragma unroll
+  for (int e = 0; e < TS_TPT; ++e)
+    if (t0 + e < P.n_tiles) {
+      P.s.tile_state[t0 + e] = uint8_t(s);
+      s = stv_apply(v[e], s);
+    }
+}
+
 // ================================================================ 1. context
 struct CtxShared {
   Feed F;
   uint32_t tile_stv;
   uint32_t warp_stv[NW];
-  uint32_t wv[NW][4][3];      // per warp, per start state: (records, column, last) of the warp
-  uint32_t wpre[NW][4][3];    // per warp, per start state: the same over the earlier warps
-  uint64_t wcnt[NW][4][4];    // per warp, per start state: packed value bytes per string column
-  uint32_t rel[4][PP_MAX_COLS];  // per start state: value bytes of relative field k
+  uint32_t wv[NW][3];         // per warp: (records, column, last) of the warp
+  uint32_t wpre[NW][3];       // per warp: the same over the earlier warps
+  uint64_t wcnt[NW][4];       // per warp: packed value bytes per string column
+  uint32_t rel[PP_MAX_COLS];  // value bytes of relative field k
   int8_t stridx[PP_MAX_COLS];
 };
 constexpr size_t CTX_SMEM = LUT_BYTES + 2 * TILE + sizeof(CtxShared);
 constexpr int CTX_HDR = 52;  // transition vector + (records, column, last) per start state
 
-// Reduction over the warp in lane order (lane 0 receives lanes 0..31).
-__device__ __forceinline__ V2 warp_reduce_v2(V2 v) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    const V2 o = {__shfl_down_sync(FULL, v.rec, d), __shfl_down_sync(FULL, v.col, d),
-                  __shfl_down_sync(FULL, v.last, d)};
-    if (lane + d < 32) v = op2_32(v, o);
-  }
-  return v;
-}
-
-// Per tile: the transition vector and, for each of the four live start
-// states, the record count, column offset and last terminator of the tile
-// (ParPaRaw Sections 3.1-3.2), plus the value bytes per string column of
-// the fields whose column the tile fixes, and per relative field of the
-// tile's first, partial record (its column is only known from the scan).
+// Per tile, from the tile's true start state: the record count, column
+// offset and last terminator of the tile (ParPaRaw Sections 3.1-3.2), plus
+// the value bytes per string column of the fields whose column the tile
+// fixes, and per relative field of the tile's first, partial record (its
+// column is only known from the scan).  The record has a slot per start
+// state, as the scan composes them; only the true state's slot is filled
+// and the others are zero: the scan reads a tile's slots only along the path
+// from the input's start state, which enters every tile in its true state.
 template <int NS>
 __global__ void __launch_bounds__(NT, 2) ctx_kernel(const __grid_constant__ ParseParams P) {
   constexpr int NSW = NS > 0 ? (NS + 3) / 4 : 1;
@@ -505,75 +614,36 @@ __global__ void __launch_bounds__(NT, 2) ctx_kernel(const __grid_constant__ Pars
     const uint32_t clen = tile_len > cstart ? min(tile_len - cstart, uint32_t(CB)) : 0u;
     const uint8_t* own = tile_s + cstart;
     if (NS > 0)
-      for (int k = t; k < 4 * PP_MAX_COLS; k += NT) (&S.rel[0][0])[k] = 0;
+      for (int k = t; k < PP_MAX_COLS; k += NT) S.rel[k] = 0;
+    const uint32_t s_tile = P.s.tile_state[tile];
 
+    // the chunk's start state, and its tags
     uint32_t G, special, special_x;
     stv_pass(w, clen, tile_s, cstart, my_lut, G, special, special_x);
     const uint32_t lane_ex = block_stv(G, S.warp_stv, &S.tile_stv);
-    const uint32_t wex = S.warp_stv[warp];
+    const uint32_t st = stv_apply(lane_ex, stv_apply(S.warp_stv[warp], s_tile));
+    const Tags g = tag_chunk(st, special, special_x, P.sticky, clen, cstart, own, my_lut,
+                             P.bg_next);
 
-    // tag once per distinct start state of this chunk
-    uint32_t st[4];
-    Tags g[4];
+    // (records, column, last) scanned over the warp, then over the warps
+    V2 ex = chunk_v2(g);
+    if (__any_sync(FULL, (ex.rec | ex.col | ex.last) != 0)) {
 #pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      st[s] = stv_apply(lane_ex, stv_apply(wex, uint32_t(s)));
-      int same = -1;
-#pragma unroll
-      for (int q = 0; q < s; ++q)
-        if (same < 0 && st[q] == st[s]) same = q;
-      if (same >= 0) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          if (q == same) g[s] = g[q];
-      } else {
-        g[s] = tag_chunk(st[s], special, special_x, P.sticky, clen, cstart, own, my_lut,
-                         P.bg_next);
+      for (int d = 1; d < 32; d <<= 1) {
+        const V2 o = shfl_up_v2(ex, d);
+        if (lane >= d) ex = op2_32(o, ex);
       }
     }
-
-    // per start state: (records, column, last) scanned over the warp; a
-    // state whose chunks all start like an earlier state's in this warp
-    // shares its scan
-    V2 ex[4];
-#pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      int same = -1;
-#pragma unroll
-      for (int q = 0; q < s; ++q)
-        if (same < 0 && __all_sync(FULL, st[q] == st[s])) same = q;
-      if (same >= 0) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          if (q == same) ex[s] = ex[q];
-      } else {
-        V2 v = chunk_v2(g[s]);
-        if (__all_sync(FULL, (v.rec | v.col | v.last) == 0)) {
-          ex[s] = {0u, 0u, 0u};
-        } else {
-#pragma unroll
-          for (int d = 1; d < 32; d <<= 1) {
-            const V2 o = shfl_up_v2(v, d);
-            if (lane >= d) v = op2_32(o, v);
-          }
-          ex[s] = v;  // inclusive for now
-        }
-      }
-    }
-#pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      if (lane == 31) { S.wv[warp][s][0] = ex[s].rec; S.wv[warp][s][1] = ex[s].col; S.wv[warp][s][2] = ex[s].last; }
-      V2 e = shfl_up_v2(ex[s], 1);
+    if (lane == 31) { S.wv[warp][0] = ex.rec; S.wv[warp][1] = ex.col; S.wv[warp][2] = ex.last; }
+    {
+      V2 e = shfl_up_v2(ex, 1);
       if (lane == 0) e = {0u, 0u, 0u};
-      ex[s] = e;  // exclusive within the warp
+      ex = e;  // exclusive within the warp
     }
     __syncthreads();
-    // warp s (s < 4): prefix over the warps for start state s, and the
-    // tile's totals for the record
     uint32_t* rec = reinterpret_cast<uint32_t*>(P.s.ctx + size_t(tile) * P.s.ctx_stride);
-    if (warp < 4) {
-      const int s = warp;
-      V2 x = lane < NW ? V2{S.wv[lane][s][0], S.wv[lane][s][1], S.wv[lane][s][2]} : V2{0u, 0u, 0u};
+    if (warp == 0) {
+      V2 x = lane < NW ? V2{S.wv[lane][0], S.wv[lane][1], S.wv[lane][2]} : V2{0u, 0u, 0u};
 #pragma unroll
       for (int d = 1; d < NW; d <<= 1) {
         const V2 o = shfl_up_v2(x, d);
@@ -581,146 +651,137 @@ __global__ void __launch_bounds__(NT, 2) ctx_kernel(const __grid_constant__ Pars
       }
       V2 xe = shfl_up_v2(x, 1);
       if (lane == 0) xe = {0u, 0u, 0u};
-      if (lane < NW) { S.wpre[lane][s][0] = xe.rec; S.wpre[lane][s][1] = xe.col; S.wpre[lane][s][2] = xe.last; }
-      if (lane == NW - 1) { rec[1 + 3 * s] = x.rec; rec[2 + 3 * s] = x.col; rec[3 + 3 * s] = x.last; }
-      if (s == 0 && lane == 0) rec[0] = S.tile_stv;
+      if (lane < NW) { S.wpre[lane][0] = xe.rec; S.wpre[lane][1] = xe.col; S.wpre[lane][2] = xe.last; }
+      if (lane == NW - 1)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const bool mine = uint32_t(q) == s_tile;
+          rec[1 + 3 * q] = mine ? x.rec : 0u;
+          rec[2 + 3 * q] = mine ? x.col : 0u;
+          rec[3 + 3 * q] = mine ? x.last : 0u;
+        }
+      if (lane == 0) rec[0] = S.tile_stv;
     }
     if (NS > 0) {
       const uint64_t strmask = P.strmask;
       const uint32_t cmax = 63u - __clzll(static_cast<long long>(strmask));  // last string column
       const bool chain = cmax < 8;  // column masks when the string columns come early
       __syncthreads();
-      // value bytes per string column, per start state
-      uint32_t col0[4];
+      // value bytes per string column
+      const uint32_t col0 =
+          op2_32(V2{S.wpre[warp][0], S.wpre[warp][1], S.wpre[warp][2]}, ex).col;  // ABS32 | column, or a relative field index
+      uint64_t cnt[NSW];
 #pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        const V2 pre = op2_32(V2{S.wpre[warp][s][0], S.wpre[warp][s][1], S.wpre[warp][s][2]}, ex[s]);
-        col0[s] = pre.col;  // ABS32 | column, or a relative field index
-      }
-#pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        int same = -1;
-#pragma unroll
-        for (int q = 0; q < s; ++q)
-          if (same < 0 && __all_sync(FULL, st[q] == st[s] && ((col0[q] & ABS32) != 0) && col0[q] == col0[s]))
-            same = q;
-        uint64_t cnt[NSW];
-#pragma unroll
-        for (int k = 0; k < NSW; ++k) cnt[k] = 0;
-        const Tags& gs = g[s];
-        const uint32_t valid = range_mask(0, min(clen, gs.inv_at));
-        const uint32_t data = valid & ~(gs.fd | gs.rd | gs.ctrl);
-        const uint32_t T = gs.fd | gs.rd;
-        const bool abs0 = (col0[s] & ABS32) != 0;
-        const uint32_t c0 = col0[s] & ~ABS32;
-        uint32_t k0 = 0xFFFFFFFFu, n0 = 0;  // the first relative segment, summed per warp below
-        if (st[s] < 4 && same < 0 && !chain) {
-          // a walk over the chunk's fields (string columns far from the
-          // record start: fewer steps than the column-by-column masks)
-          bool abs = abs0;
+      for (int k = 0; k < NSW; ++k) cnt[k] = 0;
+      const uint32_t valid = range_mask(0, min(clen, g.inv_at));
+      const uint32_t data = valid & ~(g.fd | g.rd | g.ctrl);
+      const uint32_t T = g.fd | g.rd;
+      const bool abs0 = (col0 & ABS32) != 0;
+      const uint32_t c0 = col0 & ~ABS32;
+      uint32_t k0 = 0xFFFFFFFFu, n0 = 0;  // the first relative segment, summed per warp below
+      if (st < 4 && !chain) {
+        // a walk over the chunk's fields (string columns far from the
+        // record start: fewer steps than the column-by-column masks)
+        bool abs = abs0;
+        uint32_t col = c0, term = T, seg0 = 0;
+        for (;;) {
+          const uint32_t j = term ? uint32_t(__ffs(term) - 1) : 32u;
+          const uint32_t n = __popc(data & range_mask(seg0, j));
+          if (n && col < n_cols) {
+            if (abs) {
+              const int si = S.stridx[col];
+              if (si >= 0) add16(cnt, si, n);
+            } else if (seg0 == 0) {
+              k0 = col;
+              n0 = n;
+            } else {
+              atomicAdd(&S.rel[col], n);
+            }
+          }
+          if (j == 32) break;
+          if ((g.rd >> j) & 1u) { abs = true; col = 0; }
+          else col = col < 0x7FFFFF00u ? col + 1 : col;
+          seg0 = j + 1;
+          term &= term - 1;
+        }
+      } else if (st < 4) {
+        if (!abs0) {
+          // fields of the tile's first, partial record: relative column
+          // indices, up to this chunk's first record delimiter
           uint32_t col = c0, term = T, seg0 = 0;
           for (;;) {
             const uint32_t j = term ? uint32_t(__ffs(term) - 1) : 32u;
             const uint32_t n = __popc(data & range_mask(seg0, j));
             if (n && col < n_cols) {
-              if (abs) {
-                const int si = S.stridx[col];
-                if (si >= 0) add16(cnt, si, n);
-              } else if (seg0 == 0) {
-                k0 = col;
-                n0 = n;
-              } else {
-                atomicAdd(&S.rel[s][col], n);
-              }
+              if (seg0 == 0) { k0 = col; n0 = n; }
+              else atomicAdd(&S.rel[col], n);
             }
-            if (j == 32) break;
-            if ((gs.rd >> j) & 1u) { abs = true; col = 0; }
-            else col = col < 0x7FFFFF00u ? col + 1 : col;
+            if (j == 32 || ((g.rd >> j) & 1u)) break;
+            col = col < 0x7FFFFF00u ? col + 1 : col;
             seg0 = j + 1;
             term &= term - 1;
           }
-        } else if (st[s] < 4 && same < 0) {  // (a shared state's fields are all absolute)
-          if (!abs0) {
-            // fields of the tile's first, partial record: relative column
-            // indices, up to this chunk's first record delimiter
-            uint32_t col = c0, term = T, seg0 = 0;
-            for (;;) {
-              const uint32_t j = term ? uint32_t(__ffs(term) - 1) : 32u;
-              const uint32_t n = __popc(data & range_mask(seg0, j));
-              if (n && col < n_cols) {
-                if (seg0 == 0) { k0 = col; n0 = n; }
-                else atomicAdd(&S.rel[s][col], n);
-              }
-              if (j == 32 || ((gs.rd >> j) & 1u)) break;
-              col = col < 0x7FFFFF00u ? col + 1 : col;
-              seg0 = j + 1;
-              term &= term - 1;
-            }
-          }
-          // absolute columns, one column at a time: S holds the starts of
-          // the column's runs; T - S sets each run from its start up to its
-          // terminator (exclusive) and clears that terminator, so the
-          // terminators left out of T - S end the column's runs, and those
-          // that are field delimiters start the next column's runs
-          uint32_t Sc = (gs.rd << 1) | (abs0 && c0 == 0 ? 1u : 0u);
-          int si = 0;
-          for (uint32_t c = 0; c <= cmax; ++c) {
-            const uint32_t X = T - Sc;
-            if ((strmask >> c) & 1u) {
-              const uint32_t n = __popc(X & data);
-              if (n) add16(cnt, si, n);
-              ++si;
-            }
-            Sc = ((T & ~X & gs.fd) << 1) | (abs0 && c0 == c + 1 ? 1u : 0u);
-          }
         }
-        // relative first segments (only the chunks before the tile's first
-        // record delimiter have them): one shared atomic per field index
-        if (__any_sync(FULL, k0 != 0xFFFFFFFFu)) {
-          const uint32_t k00 = __shfl_sync(FULL, k0, 0);
-          if (__all_sync(FULL, k0 == k00)) {  // the whole warp inside one field
-            const uint32_t sum = __reduce_add_sync(FULL, n0);
-            if (lane == 0 && sum) atomicAdd(&S.rel[s][k00], sum);
-          } else if (k0 != 0xFFFFFFFFu && n0) {
-            atomicAdd(&S.rel[s][k0], n0);
+        // absolute columns, one column at a time: Sc holds the starts of
+        // the column's runs; T - Sc sets each run from its start up to its
+        // terminator (exclusive) and clears that terminator, so the
+        // terminators left out of T - Sc end the column's runs, and those
+        // that are field delimiters start the next column's runs
+        uint32_t Sc = (g.rd << 1) | (abs0 && c0 == 0 ? 1u : 0u);
+        int si = 0;
+        for (uint32_t c = 0; c <= cmax; ++c) {
+          const uint32_t X = T - Sc;
+          if ((strmask >> c) & 1u) {
+            const uint32_t n = __popc(X & data);
+            if (n) add16(cnt, si, n);
+            ++si;
           }
-        }
-        // warp sums of the packed counters
-        if (same < 0) {
-          bool any = false;
-#pragma unroll
-          for (int k = 0; k < NSW; ++k) any |= cnt[k] != 0;
-          if (__any_sync(FULL, any)) {
-#pragma unroll
-            for (int k = 0; k < NSW; ++k) {
-              uint64_t v = cnt[k];
-#pragma unroll
-              for (int d = 16; d; d >>= 1) v += __shfl_xor_sync(FULL, v, d);
-              if (lane == 0) S.wcnt[warp][s][k] = v;
-            }
-          } else if (lane == 0) {
-#pragma unroll
-            for (int k = 0; k < NSW; ++k) S.wcnt[warp][s][k] = 0;
-          }
-        } else if (lane == 0) {
-#pragma unroll
-          for (int k = 0; k < NSW; ++k) S.wcnt[warp][s][k] = S.wcnt[warp][same][k];
+          Sc = ((T & ~X & g.fd) << 1) | (abs0 && c0 == c + 1 ? 1u : 0u);
         }
       }
+      // relative first segments (only the chunks before the tile's first
+      // record delimiter have them): one shared atomic per field index
+      if (__any_sync(FULL, k0 != 0xFFFFFFFFu)) {
+        const uint32_t k00 = __shfl_sync(FULL, k0, 0);
+        if (__all_sync(FULL, k0 == k00)) {  // the whole warp inside one field
+          const uint32_t sum = __reduce_add_sync(FULL, n0);
+          if (lane == 0 && sum) atomicAdd(&S.rel[k00], sum);
+        } else if (k0 != 0xFFFFFFFFu && n0) {
+          atomicAdd(&S.rel[k0], n0);
+        }
+      }
+      // warp sums of the packed counters
+      bool any = false;
+#pragma unroll
+      for (int k = 0; k < NSW; ++k) any |= cnt[k] != 0;
+      if (__any_sync(FULL, any)) {
+#pragma unroll
+        for (int k = 0; k < NSW; ++k) {
+          uint64_t v = cnt[k];
+#pragma unroll
+          for (int d = 16; d; d >>= 1) v += __shfl_xor_sync(FULL, v, d);
+          if (lane == 0) S.wcnt[warp][k] = v;
+        }
+      } else if (lane == 0) {
+#pragma unroll
+        for (int k = 0; k < NSW; ++k) S.wcnt[warp][k] = 0;
+      }
       __syncthreads();
-      // the record's chars part, one word per thread
+      // the record's chars part: the true state's slot, zeros elsewhere
       uint16_t* cabs = reinterpret_cast<uint16_t*>(rec) + CTX_HDR / 2;
       uint16_t* crel = cabs + 4 * P.n_str;
       if (t < 4 * P.n_str) {
         const int s = t / P.n_str, si = t - s * P.n_str;
         uint64_t sum = 0;
+        if (uint32_t(s) == s_tile) {
 #pragma unroll 4
-        for (int q = 0; q < NW; ++q) sum += S.wcnt[q][s][si >> 2];
+          for (int q = 0; q < NW; ++q) sum += S.wcnt[q][si >> 2];
+        }
         cabs[t] = uint16_t((sum >> (16 * (si & 3))) & 0xFFFFu);
       }
       for (int k = t; k < 4 * int(n_cols); k += NT) {
         const int s = k / int(n_cols), c = k - s * int(n_cols);
-        crel[k] = uint16_t(S.rel[s][c]);
+        crel[k] = uint32_t(s) == s_tile ? uint16_t(S.rel[c]) : uint16_t(0);
       }
     }
     feed_next(P, S.F, counter, aligned_in, lin0);  // the tile was last read before a barrier above
@@ -1599,6 +1660,7 @@ __global__ void parse_init_kernel(ParseParams P) {
   const uint32_t i0 = blockIdx.x * blockDim.x + threadIdx.x;
   const uint32_t stride = gridDim.x * blockDim.x;
   for (uint32_t i = i0; i < s.n_scan_blocks; i += stride) { s.scan_flag_a[i] = 0; s.scan_flag_c[i] = 0; }
+  for (uint32_t i = i0; i < s.n_tstate_blocks; i += stride) s.tstate_words[i] = 0;
   if (i0 < 4) s.counters[i0] = 0;
   if (i0 == 0) {
     pp_status* st = P.st;
@@ -1646,18 +1708,28 @@ cudaError_t launch_ns(const ParseParams& p, cudaStream_t stream) {
                       256, 0, stream>>>(p);
   if (timed) ppi::stage_mark(1, stream);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (p.n_tiles) {
+    const uint32_t gv = uint32_t(std::min<uint64_t>((p.n_tiles + TV_NT / 32 - 1) / (TV_NT / 32),
+                                                    uint64_t(occ.n_sm) * 6));
+    tile_stv_kernel<<<gv, TV_NT, LUT_BYTES, stream>>>(p);
+  }
+  if (timed) ppi::stage_mark(2, stream);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (p.n_tiles) tile_state_kernel<<<p.s.n_tstate_blocks, TS_NT, 0, stream>>>(p);
+  if (timed) ppi::stage_mark(3, stream);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const uint32_t g1 = uint32_t(std::min<uint64_t>(std::max<uint32_t>(p.n_tiles, 1),
                                                   uint64_t(occ.n_sm) * occ.ctx));
   if (p.n_tiles) ctx_kernel<NS><<<g1, NT, CTX_SMEM, stream>>>(p);
-  if (timed) ppi::stage_mark(2, stream);
+  if (timed) ppi::stage_mark(4, stream);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (p.n_tiles) scan_kernel<NS><<<p.s.n_scan_blocks, SCAN_NT, 0, stream>>>(p);
-  if (timed) ppi::stage_mark(3, stream);
+  if (timed) ppi::stage_mark(5, stream);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const uint32_t g3 = uint32_t(std::min<uint64_t>(std::max<uint32_t>(p.n_tiles, 1),
                                                   uint64_t(occ.n_sm) * occ.main));
   if (p.n_tiles) main_kernel<NS><<<g3, NT, MAIN_SMEM, stream>>>(p);
-  if (timed) ppi::stage_mark(4, stream);
+  if (timed) ppi::stage_mark(6, stream);
   return cudaGetLastError();
 }
 
@@ -1686,10 +1758,12 @@ int parse_ns_width(int n_str) {
 // records
 size_t parse_scratch_bytes(uint32_t n, int ns, int n_cols) {
   const uint32_t nb = (n + SCAN_TILES - 1) / SCAN_TILES;
+  const uint32_t nt = (n + TS_TILES - 1) / TS_TILES;
   const int k3 = ns > 0 ? ns : 1;
   return 256 + 2 * align256(size_t(nb) * 4) + 2 * align256(size_t(nb) * 13 * 8) +
          2 * align256(size_t(nb) * k3 * 8) + align256(size_t(n) * ctx_stride_of(ns, n_cols)) +
-         align256(size_t(n) * pre_stride_of(ns));
+         align256(size_t(n) * pre_stride_of(ns)) + align256(size_t(n) * 4) + align256(n) +
+         align256(size_t(nt) * 8);
 }
 
 void parse_scratch_carve(void* base, uint32_t n, int ns, int n_cols, ParseScratch* o) {
@@ -1704,7 +1778,11 @@ void parse_scratch_carve(void* base, uint32_t n, int ns, int n_cols, ParseScratc
   o->scan_agg_c = reinterpret_cast<uint64_t*>(p); p += align256(size_t(nb) * k3 * 8);
   o->scan_inc_c = reinterpret_cast<uint64_t*>(p); p += align256(size_t(nb) * k3 * 8);
   o->ctx = p; p += align256(size_t(n) * ctx_stride_of(ns, n_cols));
-  o->pre = p;
+  o->pre = p; p += align256(size_t(n) * pre_stride_of(ns));
+  o->tile_stv = reinterpret_cast<uint32_t*>(p); p += align256(size_t(n) * 4);
+  o->tile_state = p; p += align256(n);
+  o->tstate_words = reinterpret_cast<unsigned long long*>(p);
+  o->n_tstate_blocks = (n + TS_TILES - 1) / TS_TILES;
   o->ctx_stride = ctx_stride_of(ns, n_cols);
   o->pre_stride = pre_stride_of(ns);
   o->n_scan_blocks = nb;

@@ -226,10 +226,10 @@ pp_rc pp_tokenize_host(const uint8_t* h_in, size_t n_bytes, const pp_dfa_desc* d
  * cudaMallocAsync fails; services whose device memory is fixed at
  * start-up).
  *   Arguments, semantics, outputs and d_status: exactly those of pp_parse.
- *   Limit: the scratch needed is about 88 bytes per 16 KiB tile of input
+ *   Limit: the scratch needed is about 93 bytes per 16 KiB tile of input
  *   with no string column, rising with the string and column counts to
- *   about 856 bytes per tile with 16 string columns of 64; so 4 MiB holds
- *   inputs up to about 740 MiB in the first case and about 76 MiB in the
+ *   about 861 bytes per tile with 16 string columns of 64; so 4 MiB holds
+ *   inputs up to about 700 MiB in the first case and about 76 MiB in the
  *   last.  A larger input returns PP_ETOOLARGE before any CUDA call.
  *   First call on each device: it looks up the buffer's address
  *   (cudaGetSymbolAddress; this can load the library's device code) and
@@ -331,8 +331,8 @@ void pp_debug_set_withhold(int on);
 pp_rc pp_debug_stage_timing(int n_calls);
 
 /* Kernel durations of the recorded calls: out[PP_STAGES*i + k] =
- * milliseconds of kernel k of call i.  pp_parse: 0 init, 1 context pass,
- * 2 scan, 3 main pass.  pp_tokenize: 0 init, 1 transition vectors, 2 state
+ * milliseconds of kernel k of call i.  pp_parse: 0 init, 1 tile transition
+ * vectors, 2 tile start states, 3 context pass, 4 scan, 5 main pass.  pp_tokenize: 0 init, 1 transition vectors, 2 state
  * scan, 3 count pass, 4 count scan, 5 emit pass.  Entries a call does not
  * use are 0.  Waits for the events.  Returns the number of calls written
  * (at most max_calls), or -1 on a CUDA error. */
