@@ -374,11 +374,11 @@ pp_rc pp_parse(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa, int 
                                       d_status, &p);
   if (rc != PP_OK) return rc;
   const int ns = ppi::parse_ns_width(p.n_str);
-  const size_t sb = ppi::parse_scratch_bytes(p.n_tiles, ns, n_cols);
+  const size_t sb = ppi::parse_scratch_bytes(p.n_tiles, ns, n_cols, true);
   void* scratch = nullptr;
   cudaError_t e = cudaMallocAsync(&scratch, sb, stream);
   if (e != cudaSuccess) return cuda_rc(e);
-  ppi::parse_scratch_carve(scratch, p.n_tiles, ns, n_cols, &p.s);
+  ppi::parse_scratch_carve(scratch, p.n_tiles, ns, n_cols, true, &p.s);
   e = ppi::launch_parse(p, stream);
   const cudaError_t ef = cudaFreeAsync(scratch, stream);
   if (e == cudaSuccess) e = ef;

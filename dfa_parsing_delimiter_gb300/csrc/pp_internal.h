@@ -29,6 +29,11 @@ struct ParseScratch {
   uint8_t* tile_state;      // [n_tiles]
   unsigned long long* tstate_words;  // [n_tstate_blocks]
   uint32_t n_tstate_blocks;
+  // [n_tiles * 512], per 32-byte chunk, written by the context pass for the
+  // main pass: FD, RD and control bitmaps, and (1 + the position in the tile
+  // of the chunk's last terminator) | end state << 16.  Null when the
+  // scratch has no room for them: the main pass then tags again.
+  uint4* tags;
   uint32_t* scan_flag_a;    // [n_scan_blocks]
   uint64_t* scan_agg_a;     // [n_scan_blocks][13]
   uint64_t* scan_inc_a;
@@ -74,8 +79,10 @@ struct ParseParams {
 
 // bytes of scratch for n_tiles tiles and ns string columns (ns rounded to the
 // kernel's instantiation width)
-size_t parse_scratch_bytes(uint32_t n_tiles, int ns, int n_cols);
-void parse_scratch_carve(void* base, uint32_t n_tiles, int ns, int n_cols, ParseScratch* out);
+// (tags: with room for the per-chunk tags, 8 KiB per tile)
+size_t parse_scratch_bytes(uint32_t n_tiles, int ns, int n_cols, bool tags);
+void parse_scratch_carve(void* base, uint32_t n_tiles, int ns, int n_cols, bool tags,
+                         ParseScratch* out);
 int parse_ns_width(int n_str);
 
 // init (counters, scan flags, status), context pass, scan, main pass

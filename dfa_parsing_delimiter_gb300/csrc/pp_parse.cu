@@ -624,6 +624,13 @@ __global__ void __launch_bounds__(NT, 2) ctx_kernel(const __grid_constant__ Pars
     const uint32_t st = stv_apply(lane_ex, stv_apply(S.warp_stv[warp], s_tile));
     const Tags g = tag_chunk(st, special, special_x, P.sticky, clen, cstart, own, my_lut,
                              P.bg_next);
+    if (g.inv_at < clen && st != 4)
+      report(P.st, PP_ERR_INVALID_INPUT, tile_base + cstart + g.inv_at, true);
+    if (!P.record_end && tile + 1 == P.n_tiles && clen > 0 && cstart + clen == tile_len &&
+        g.end != 4 && !((P.accept_mask >> g.end) & 1u))
+      report(P.st, PP_ERR_BAD_END_STATE, P.n, true);
+    if (P.s.tags)  // for the main pass: bitmaps, 1 + last terminator | end state << 16
+      P.s.tags[size_t(tile) * NT + t] = make_uint4(g.fd, g.rd, g.ctrl, (g.last >> 8) | (g.end << 16));
 
     // (records, column, last) scanned over the warp, then over the warps
     V2 ex = chunk_v2(g);
@@ -1277,24 +1284,26 @@ __global__ void __launch_bounds__(NT, 2) main_kernel(const __grid_constant__ Par
     const uint32_t clen = tile_len > cstart ? min(tile_len - cstart, uint32_t(CB)) : 0u;
     const uint8_t* own = tile_s + cstart;
 
-    // ---- the chunk's start state (the tile's is known from the scan)
-    uint32_t G, special, special_x;
-    stv_pass(w, clen, tile_s, cstart, my_lut, G, special, special_x);
-    const uint32_t lane_ex = block_stv(G, S.warp_stv, &S.tile_stv);
-    const uint32_t s_tile = ph.state & 0xFFu;
-    const uint32_t s_chunk = stv_apply(lane_ex, stv_apply(S.warp_stv[warp], s_tile));
-
-    // ---- tags
-    const Tags g = tag_chunk(s_chunk, special, special_x, P.sticky, clen, cstart, own, my_lut,
-                             P.bg_next);
+    // ---- the chunk's tags: stored by the context pass, or (without room
+    // for them in the scratch) re-run here from the chunk's start state, the
+    // tile's being known from the scan.  The context pass reports invalid
+    // input and a bad end state.
+    Tags g;
+    if (P.s.tags) {
+      const uint4 v = P.s.tags[size_t(tile) * NT + t];
+      g = {v.x, v.y, v.z, 32u, (v.w & 0xFFFFu) << 8, v.w >> 16};
+    } else {
+      uint32_t G, special, special_x;
+      stv_pass(w, clen, tile_s, cstart, my_lut, G, special, special_x);
+      const uint32_t lane_ex = block_stv(G, S.warp_stv, &S.tile_stv);
+      const uint32_t s_tile = ph.state & 0xFFu;
+      const uint32_t s_chunk = stv_apply(lane_ex, stv_apply(S.warp_stv[warp], s_tile));
+      g = tag_chunk(s_chunk, special, special_x, P.sticky, clen, cstart, own, my_lut, P.bg_next);
+    }
     const uint32_t fd = g.fd, rd = g.rd;
     ctrl_s[t] = g.ctrl;
-    if (g.inv_at < clen && s_chunk != 4)
-      report(P.st, PP_ERR_INVALID_INPUT, tile_base + cstart + g.inv_at, true);
     const bool owns_end = last_tile && clen > 0 && cstart + clen == tile_len;
     const bool partial = P.record_end != nullptr;
-    if (!partial && owns_end && g.end != 4 && !((P.accept_mask >> g.end) & 1u))
-      report(P.st, PP_ERR_BAD_END_STATE, P.n, true);
     const bool virt_rd = !partial && owns_end && g.end != 4 && ((P.accept_mask >> g.end) & 1u) &&
                          !((rd >> (clen - 1)) & 1u);
     if (partial) {
@@ -1756,17 +1765,17 @@ int parse_ns_width(int n_str) {
 // layout: counters | scan flags (records, chars) | scan payloads (2 x 13
 // words per scan block; 2 x ns words per scan block) | ctx records | pre
 // records
-size_t parse_scratch_bytes(uint32_t n, int ns, int n_cols) {
+size_t parse_scratch_bytes(uint32_t n, int ns, int n_cols, bool tags) {
   const uint32_t nb = (n + SCAN_TILES - 1) / SCAN_TILES;
   const uint32_t nt = (n + TS_TILES - 1) / TS_TILES;
   const int k3 = ns > 0 ? ns : 1;
   return 256 + 2 * align256(size_t(nb) * 4) + 2 * align256(size_t(nb) * 13 * 8) +
          2 * align256(size_t(nb) * k3 * 8) + align256(size_t(n) * ctx_stride_of(ns, n_cols)) +
          align256(size_t(n) * pre_stride_of(ns)) + align256(size_t(n) * 4) + align256(n) +
-         align256(size_t(nt) * 8);
+         align256(size_t(nt) * 8) + (tags ? align256(size_t(n) * NT * 16) : 0);
 }
 
-void parse_scratch_carve(void* base, uint32_t n, int ns, int n_cols, ParseScratch* o) {
+void parse_scratch_carve(void* base, uint32_t n, int ns, int n_cols, bool tags, ParseScratch* o) {
   const uint32_t nb = (n + SCAN_TILES - 1) / SCAN_TILES;
   const int k3 = ns > 0 ? ns : 1;
   uint8_t* p = static_cast<uint8_t*>(base);
@@ -1783,6 +1792,8 @@ void parse_scratch_carve(void* base, uint32_t n, int ns, int n_cols, ParseScratc
   o->tile_state = p; p += align256(n);
   o->tstate_words = reinterpret_cast<unsigned long long*>(p);
   o->n_tstate_blocks = (n + TS_TILES - 1) / TS_TILES;
+  p += align256(size_t(o->n_tstate_blocks) * 8);
+  o->tags = tags ? reinterpret_cast<uint4*>(p) : nullptr;
   o->ctx_stride = ctx_stride_of(ns, n_cols);
   o->pre_stride = pre_stride_of(ns);
   o->n_scan_blocks = nb;
