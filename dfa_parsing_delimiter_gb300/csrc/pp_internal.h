@@ -34,6 +34,11 @@ struct ParseScratch {
   // of the chunk's last terminator) | end state << 16.  Null when the
   // scratch has no room for them: the main pass then tags again.
   uint4* tags;
+  // [n_tiles * 512], with tags: the chunk's (records, column, last
+  // terminator) prefix in the tile: records | (1 + last position) << 16,
+  // column (15 bits) | 0x8000 if absolute.
+  uint2* vpre;
+  uint8_t* tile_flags;  // [n_tiles]: 1 if the tile has control bytes
   uint32_t* scan_flag_a;    // [n_scan_blocks]
   uint64_t* scan_agg_a;     // [n_scan_blocks][13]
   uint64_t* scan_inc_a;
@@ -79,7 +84,7 @@ struct ParseParams {
 
 // bytes of scratch for n_tiles tiles and ns string columns (ns rounded to the
 // kernel's instantiation width)
-// (tags: with room for the per-chunk tags, 8 KiB per tile)
+// (tags: with room for the per-chunk tags and prefixes, 12 KiB per tile)
 size_t parse_scratch_bytes(uint32_t n_tiles, int ns, int n_cols, bool tags);
 void parse_scratch_carve(void* base, uint32_t n_tiles, int ns, int n_cols, bool tags,
                          ParseScratch* out);

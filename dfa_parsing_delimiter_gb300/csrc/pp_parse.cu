@@ -573,6 +573,7 @@ struct CtxShared {
   uint32_t wpre[NW][3];       // per warp: the same over the earlier warps
   uint64_t wcnt[NW][4];       // per warp: packed value bytes per string column
   uint32_t rel[PP_MAX_COLS];  // value bytes of relative field k
+  uint32_t wrd[NW];           // partial mode: per warp, 1 + its last record delimiter in the tile
   int8_t stridx[PP_MAX_COLS];
 };
 constexpr size_t CTX_SMEM = LUT_BYTES + 2 * TILE + sizeof(CtxShared);
@@ -647,8 +648,17 @@ __global__ void __launch_bounds__(NT, 2) ctx_kernel(const __grid_constant__ Pars
       if (lane == 0) e = {0u, 0u, 0u};
       ex = e;  // exclusive within the warp
     }
+    if (P.record_end) {  // partial mode: 1 + the tile's last record delimiter
+      const uint32_t wm = __reduce_max_sync(FULL, g.rd ? cstart + 32u - __clz(g.rd) : 0u);
+      if (lane == 0) S.wrd[warp] = wm;
+    }
     __syncthreads();
     uint32_t* rec = reinterpret_cast<uint32_t*>(P.s.ctx + size_t(tile) * P.s.ctx_stride);
+    if (P.record_end && t == 0) {
+      uint32_t m = 0;
+      for (int q = 0; q < NW; ++q) m = max(m, S.wrd[q]);
+      if (m) atomicMax(P.record_end, static_cast<unsigned long long>(tile_base + m));
+    }
     if (warp == 0) {
       V2 x = lane < NW ? V2{S.wv[lane][0], S.wv[lane][1], S.wv[lane][2]} : V2{0u, 0u, 0u};
 #pragma unroll
@@ -669,14 +679,21 @@ __global__ void __launch_bounds__(NT, 2) ctx_kernel(const __grid_constant__ Pars
         }
       if (lane == 0) rec[0] = S.tile_stv;
     }
+    // the chunk's (records, column, last) prefix in the tile, and whether
+    // the tile has control bytes: stored for the main pass
+    const bool any_ctrl = __syncthreads_or(g.ctrl != 0) != 0;
+    const V2 pre = op2_32(V2{S.wpre[warp][0], S.wpre[warp][1], S.wpre[warp][2]}, ex);
+    if (P.s.vpre)
+      P.s.vpre[size_t(tile) * NT + t] =
+          make_uint2(pre.rec | ((pre.last >> 8) << 16),
+                     (pre.col & 0x7FFFu) | ((pre.col & ABS32) ? 0x8000u : 0u));
+    if (t == 0) P.s.tile_flags[tile] = any_ctrl ? 1u : 0u;
     if (NS > 0) {
       const uint64_t strmask = P.strmask;
       const uint32_t cmax = 63u - __clzll(static_cast<long long>(strmask));  // last string column
       const bool chain = cmax < 8;  // column masks when the string columns come early
-      __syncthreads();
       // value bytes per string column
-      const uint32_t col0 =
-          op2_32(V2{S.wpre[warp][0], S.wpre[warp][1], S.wpre[warp][2]}, ex).col;  // ABS32 | column, or a relative field index
+      const uint32_t col0 = pre.col;  // ABS32 | column, or a relative field index
       uint64_t cnt[NSW];
 #pragma unroll
       for (int k = 0; k < NSW; ++k) cnt[k] = 0;
@@ -1221,7 +1238,6 @@ struct MainShared {
   uint32_t warp_stv[NW];
   uint32_t warp_rec[NW], warp_col[NW], warp_last[NW];
   uint32_t rows;             // records touched by the tile (#RD + 1)
-  uint32_t wrd[NW];          // partial mode: per warp, 1 + its last record delimiter in the tile
   uint32_t col_end;          // fields of the last row closed in the tile
   uint32_t wsum[NW];
   uint32_t cstart[ppi::MAX_STR_COLS + 1];  // staging start per string column (this pass)
@@ -1306,55 +1322,77 @@ __global__ void __launch_bounds__(NT, 2) main_kernel(const __grid_constant__ Par
     const bool partial = P.record_end != nullptr;
     const bool virt_rd = !partial && owns_end && g.end != 4 && ((P.accept_mask >> g.end) & 1u) &&
                          !((rd >> (clen - 1)) & 1u);
-    if (partial) {
-      const uint32_t mine = rd ? cstart + 32u - __clz(rd) : 0u;
-      const uint32_t wm = __reduce_max_sync(FULL, mine);
-      if (lane == 0) S.wrd[warp] = wm;
-    }
 
-    // ---- record, column and field start at the chunk start (block scan)
-    V2 vi = chunk_v2(g);
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const V2 o = shfl_up_v2(vi, d);
-      if (lane >= d) vi = op2_32(o, vi);
-    }
-    V2 lex = shfl_up_v2(vi, 1);
-    if (lane == 0) lex = {0u, 0u, 0u};
-    if (lane == 31) { S.warp_rec[warp] = vi.rec; S.warp_col[warp] = vi.col; S.warp_last[warp] = vi.last; }
-    const bool any_ctrl = __syncthreads_or(g.ctrl != 0) != 0;
-    if (warp == 0) {
-      V2 x = lane < NW ? V2{S.warp_rec[lane], S.warp_col[lane], S.warp_last[lane]} : V2{0u, 0u, 0u};
-#pragma unroll
-      for (int d = 1; d < NW; d <<= 1) {
-        const V2 o = shfl_up_v2(x, d);
-        if (lane >= d) x = op2_32(o, x);
+    // ---- record, column and field start at the chunk start: stored by the
+    // context pass with the tags, or a block scan here
+    V2 pre;
+    bool any_ctrl, any_virt;
+    uint32_t rows, col_end_raw;  // records touched by the tile; fields of its last row
+    if (P.s.vpre) {
+      const uint2 pv = P.s.vpre[size_t(tile) * NT + t];
+      pre = {pv.x & 0xFFFFu, (pv.y & 0x7FFFu) | ((pv.y & 0x8000u) ? ABS32 : 0u), (pv.x >> 16) << 8};
+      any_ctrl = P.s.tile_flags[tile] != 0;
+      V2 x = {0u, 0u, 0u};  // the tile's totals: the record's slot of the true start state
+      const uint32_t s_tile = ph.state & 0xFFu;
+      if (s_tile < 4) {
+        const uint32_t* cr = reinterpret_cast<const uint32_t*>(P.s.ctx + size_t(tile) * P.s.ctx_stride);
+        x = {cr[1 + 3 * s_tile], cr[2 + 3 * s_tile], cr[3 + 3 * s_tile]};
       }
-      V2 xe = shfl_up_v2(x, 1);
-      if (lane == 0) xe = {0u, 0u, 0u};
-      __syncwarp();
-      if (lane < NW) { S.warp_rec[lane] = xe.rec; S.warp_col[lane] = xe.col; S.warp_last[lane] = xe.last; }
-      if (lane == NW - 1) {
-        S.rows = x.rec + 1;
-        if (x.col & ABS32) {
-          S.col_end = x.col & ~ABS32;
-        } else {
-          const uint64_t c = uint64_t(ph.col_in) + x.col;
-          S.col_end = c > 0x7FFFFF00ull ? 0x7FFFFF00u : uint32_t(c);
+      rows = x.rec + 1;
+      if (x.col & ABS32) {
+        col_end_raw = x.col & ~ABS32;
+      } else {
+        const uint64_t c = uint64_t(ph.col_in) + x.col;
+        col_end_raw = c > 0x7FFFFF00ull ? 0x7FFFFF00u : uint32_t(c);
+      }
+      any_virt = false;  // the chunk that owns the input's end closes a last record
+      if (last_tile && !partial) {
+        const uint32_t ot = (tile_len - 1) / CB;
+        const uint4 ov = P.s.tags[size_t(tile) * NT + ot];
+        const uint32_t oend = ov.w >> 16;
+        any_virt = oend != 4 && ((P.accept_mask >> oend) & 1u) &&
+                   !((ov.y >> (tile_len - 1 - ot * CB)) & 1u);
+      }
+    } else {
+      V2 vi = chunk_v2(g);
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const V2 o = shfl_up_v2(vi, d);
+        if (lane >= d) vi = op2_32(o, vi);
+      }
+      V2 lex = shfl_up_v2(vi, 1);
+      if (lane == 0) lex = {0u, 0u, 0u};
+      if (lane == 31) { S.warp_rec[warp] = vi.rec; S.warp_col[warp] = vi.col; S.warp_last[warp] = vi.last; }
+      any_ctrl = __syncthreads_or(g.ctrl != 0) != 0;
+      if (warp == 0) {
+        V2 x = lane < NW ? V2{S.warp_rec[lane], S.warp_col[lane], S.warp_last[lane]} : V2{0u, 0u, 0u};
+#pragma unroll
+        for (int d = 1; d < NW; d <<= 1) {
+          const V2 o = shfl_up_v2(x, d);
+          if (lane >= d) x = op2_32(o, x);
+        }
+        V2 xe = shfl_up_v2(x, 1);
+        if (lane == 0) xe = {0u, 0u, 0u};
+        __syncwarp();
+        if (lane < NW) { S.warp_rec[lane] = xe.rec; S.warp_col[lane] = xe.col; S.warp_last[lane] = xe.last; }
+        if (lane == NW - 1) {
+          S.rows = x.rec + 1;
+          if (x.col & ABS32) {
+            S.col_end = x.col & ~ABS32;
+          } else {
+            const uint64_t c = uint64_t(ph.col_in) + x.col;
+            S.col_end = c > 0x7FFFFF00ull ? 0x7FFFFF00u : uint32_t(c);
+          }
         }
       }
+      any_virt = __syncthreads_or(virt_rd) != 0;
+      pre = op2_32(V2{S.warp_rec[warp], S.warp_col[warp], S.warp_last[warp]}, lex);
+      rows = S.rows;
+      col_end_raw = S.col_end;
     }
-    const bool any_virt = __syncthreads_or(virt_rd) != 0;
-    if (partial && t == 0) {
-      uint32_t m = 0;
-      for (int q = 0; q < NW; ++q) m = max(m, S.wrd[q]);
-      if (m) atomicMax(P.record_end, static_cast<unsigned long long>(tile_base + m));
-    }
-    const V2 pre = op2_32(V2{S.warp_rec[warp], S.warp_col[warp], S.warp_last[warp]}, lex);
     const uint64_t rec0 = ph.rec0;
-    const uint32_t rows = S.rows;
     const uint32_t col_in = ph.col_in;
-    const uint32_t col_end = any_virt ? n_cols : S.col_end;
+    const uint32_t col_end = any_virt ? n_cols : col_end_raw;
     uint32_t col0;
     if (pre.col & ABS32) {
       col0 = pre.col & ~ABS32;
@@ -1772,7 +1810,7 @@ size_t parse_scratch_bytes(uint32_t n, int ns, int n_cols, bool tags) {
   return 256 + 2 * align256(size_t(nb) * 4) + 2 * align256(size_t(nb) * 13 * 8) +
          2 * align256(size_t(nb) * k3 * 8) + align256(size_t(n) * ctx_stride_of(ns, n_cols)) +
          align256(size_t(n) * pre_stride_of(ns)) + align256(size_t(n) * 4) + align256(n) +
-         align256(size_t(nt) * 8) + (tags ? align256(size_t(n) * NT * 16) : 0);
+         align256(size_t(nt) * 8) + align256(n) + (tags ? align256(size_t(n) * NT * 24) : 0);
 }
 
 void parse_scratch_carve(void* base, uint32_t n, int ns, int n_cols, bool tags, ParseScratch* o) {
@@ -1793,7 +1831,10 @@ void parse_scratch_carve(void* base, uint32_t n, int ns, int n_cols, bool tags, 
   o->tstate_words = reinterpret_cast<unsigned long long*>(p);
   o->n_tstate_blocks = (n + TS_TILES - 1) / TS_TILES;
   p += align256(size_t(o->n_tstate_blocks) * 8);
+  o->tile_flags = p; p += align256(n);
   o->tags = tags ? reinterpret_cast<uint4*>(p) : nullptr;
+  if (tags) p += size_t(n) * NT * 16;
+  o->vpre = tags ? reinterpret_cast<uint2*>(p) : nullptr;
   o->ctx_stride = ctx_stride_of(ns, n_cols);
   o->pre_stride = pre_stride_of(ns);
   o->n_scan_blocks = nb;

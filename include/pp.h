@@ -226,9 +226,9 @@ pp_rc pp_tokenize_host(const uint8_t* h_in, size_t n_bytes, const pp_dfa_desc* d
  * cudaMallocAsync fails; services whose device memory is fixed at
  * start-up).
  *   Arguments, semantics, outputs and d_status: exactly those of pp_parse.
- *   Limit: the scratch needed is about 93 bytes per 16 KiB tile of input
+ *   Limit: the scratch needed is about 94 bytes per 16 KiB tile of input
  *   with no string column, rising with the string and column counts to
- *   about 861 bytes per tile with 16 string columns of 64; so 4 MiB holds
+ *   about 862 bytes per tile with 16 string columns of 64; so 4 MiB holds
  *   inputs up to about 700 MiB in the first case and about 76 MiB in the
  *   last.  A larger input returns PP_ETOOLARGE before any CUDA call.
  *   First call on each device: it looks up the buffer's address
