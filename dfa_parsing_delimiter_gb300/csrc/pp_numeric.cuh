@@ -105,34 +105,130 @@ PP_FN uint64_t decimal_to_binary64(uint64_t w, int q) {
   return (uint64_t(be) << 52) | (m & ((1ull << 52) - 1));
 }
 
-// Bits of the binary64 nearest to w * 10^q for a short significand:
-// 0 < w < 2^32 and -22 <= q <= 0 (a plain decimal such as "463.86"), with
-// q == 0 the exact integer conversion.  w times the 128-bit table entry,
-// truncated to its top 96 bits, carries a relative error below 2^-94; the
-// value w / 10^-q is a rational whose distance from any rounding tie is
-// at least 2^-86 relative (its numerator against a 54-bit dyadic differs
-// by a nonzero integer), so the top 54 bits round correctly.
-PP_FN uint64_t short_decimal_to_binary64(uint32_t w, int q) {
-  const int lzw = clz64(uint64_t(w)) - 32;  // w != 0
-  if (q == 0)
-    return (uint64_t(1054 - lzw) << 52) | ((uint64_t(w) << (lzw + 21)) & ((1ull << 52) - 1));
-  const int k = q - PP_P5_MIN;
-  const uint64_t th = PP_LDG(&pp_p5_hi[k]);
-  const uint64_t tl = PP_LDG(&pp_p5_lo[k]);
-  const int e5 = PP_LDG(&pp_p5_e2[k]);
-  // (w * (th:tl)) >> 64 = hi * 2^32 + lo32, with hi >= 2^31
-  const uint64_t c1 = uint64_t(w) * uint32_t(tl);
-  const uint64_t c2 = uint64_t(w) * uint32_t(tl >> 32) + (c1 >> 32);
-  const uint64_t plo = uint64_t(w) * uint32_t(th) + (c2 >> 32);
-  const uint64_t hi = uint64_t(w) * uint32_t(th >> 32) + (plo >> 32);
-  const uint32_t lo32 = uint32_t(plo);
-  const int L = clz64(hi);                   // 0..32
-  const uint64_t top = L ? ((hi << L) | (uint64_t(lo32) >> (32 - L))) : hi;  // in [2^63, 2^64)
-  // w * 10^q ~= (hi * 2^32 + lo32) * 2^(q + e5 - 63) = top * 2^(32 - L + q + e5 - 63)
-  uint64_t m = (top >> 11) + ((top >> 10) & 1u);
-  int be = 32 - L + q + e5 - 63 + 11 + 52 + 1023;
-  if (m == (1ull << 53)) { m >>= 1; ++be; }
-  return (uint64_t(be) << 52) | (m & ((1ull << 52) - 1));
+PP_FN int clz32(uint32_t x) {
+#if defined(__CUDA_ARCH__)
+  return __clz(int(x));
+#else
+  return x ? __builtin_clz(x) : 32;
+#endif
+}
+PP_FN int ctz32(uint32_t x) {  // x != 0
+#if defined(__CUDA_ARCH__)
+  return __ffs(int(x)) - 1;
+#else
+  return __builtin_ctz(x);
+#endif
+}
+PP_FN int popc32(uint32_t x) {
+#if defined(__CUDA_ARCH__)
+  return __popc(x);
+#else
+  return __builtin_popcount(x);
+#endif
+}
+PP_FN uint32_t umulhi32(uint32_t a, uint32_t b) {
+#if defined(__CUDA_ARCH__)
+  return __umulhi(a, b);
+#else
+  return uint32_t((uint64_t(a) * b) >> 32);
+#endif
+}
+// Byte permute with PTX prmt semantics (default mode): result byte i is
+// byte (s >> 4i) & 7 of the eight bytes b:a (a the low word); when bit 3 of
+// that nibble is set, the chosen byte's sign bit is replicated instead.
+PP_FN uint32_t byte_perm(uint32_t a, uint32_t b, uint32_t s) {
+#if defined(__CUDA_ARCH__)
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(s));
+  return r;
+#else
+  const uint64_t v = (uint64_t(b) << 32) | a;
+  uint32_t r = 0;
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t n = (s >> (4 * i)) & 0xFu;
+    uint32_t x = uint32_t(v >> (8 * (n & 7u))) & 0xFFu;
+    if (n & 8u) x = (x & 0x80u) ? 0xFFu : 0u;
+    r |= x << (8 * i);
+  }
+  return r;
+#endif
+}
+
+// ------------------------------------------------ short plain decimals
+// Word-parallel decoding of a field of at most 8 characters, four to a
+// 32-bit word (character i in byte i).  With y = chars ^ '0', digits map
+// to 0..9 and '.' to 0x1E.
+
+// 0x80 in each byte of y that is not a digit
+PP_FN uint32_t nondigit_bytes(uint32_t y) {
+  return (((y & 0x7F7F7F7Fu) + 0x76767676u) | y) & 0x80808080u;
+}
+// value of the four digits in w, byte 0 the most significant
+PP_FN uint32_t val4(uint32_t w) {
+  w = (w * 10u + (w >> 8)) & 0x00FF00FFu;
+  return (w * 100u + (w >> 16)) & 0xFFFFu;
+}
+
+// The n (1..8) characters in x0:x1 as a plain decimal: digits only, or
+// (dot) digits with one '.' and at least one digit ("12", "4.5", "7.",
+// ".25").  Bytes past the n-th are ignored.  On success *w = the digits
+// as an integer (< 10^8) and *k = the number of digits after the '.', so
+// the value is w * 10^-k.
+PP_FN bool short_decimal(uint32_t x0, uint32_t x1, int n, bool dot, uint32_t* w, int* k) {
+  const uint32_t y0 = x0 ^ 0x30303030u, y1 = x1 ^ 0x30303030u;
+  const uint32_t m0 = n >= 4 ? 0x80808080u : 0x80808080u >> (32 - 8 * n);
+  const uint32_t m1 = n <= 4 ? 0u : 0x80808080u >> (64 - 8 * n);
+  const uint32_t d0 = nondigit_bytes(y0) & m0, d1 = nondigit_bytes(y1) & m1;
+  int p = 8, nd = n;  // position of the '.' (8: none), digit count
+  if (d0 | d1) {
+    const int b = d0 ? (ctz32(d0) >> 3) : 4 + (ctz32(d1) >> 3);
+    const uint32_t yb = ((b < 4 ? y0 : y1) >> (8 * (b & 3))) & 0xFFu;
+    if (!dot || popc32(d0) + popc32(d1) != 1 || yb != 0x1Eu || n == 1) return false;
+    p = b;
+    nd = n - 1;
+  }
+  // Right-align the digits, dropping the '.': byte i of z0:z1 takes digit
+  // i - a (a = 8 - nd leading zero bytes), i.e. character i - a, or
+  // i - a + 1 from the '.' on.  The leading bytes use selector 8, the sign
+  // of character 0, which is 0 for a digit or '.'.
+  const int a = 8 - nd;
+  uint32_t sel = (0x76543210u << (4 * a)) | (0x88888888u & ((1u << (4 * a)) - 1u));
+  if (a + p < 8) sel += 0x11111111u << (4 * (a + p));
+  const uint32_t z0 = byte_perm(y0, y1, sel), z1 = byte_perm(y0, y1, sel >> 16);
+  *w = val4(z0) * 10000u + val4(z1);
+  *k = p < 8 ? nd - p : 0;
+  return true;
+}
+
+// Bits of the binary64 nearest to w * 10^-k for 0 < w < 2^32 and
+// 0 <= k <= PP_R10_MAX (a plain decimal such as "463.86": w = 46386,
+// k = 2).  With W = w normalised to [2^31, 2^32) and R = the table's
+// 96-bit reciprocal ceil(2^(95 + e) / 10^k) (e = ceil(log2 10^k)), the top
+// 64 bits T of W * R are computed exactly with three 32x32 products; the
+// binary64 significand is T rounded to 53 bits.  Rounding R up keeps the
+// product at or above the exact value, by less than 2^-41 units of the
+// 54th bit; the exact value, a rational with denominator 5^k, is either
+// dyadic (and then ends in zeros there) or at least 5^-k >= 2^-40 such
+// units from a rounding point, so the rounding is always correct, and a
+// tie cannot occur (it would need 54 significant bits, w has at most 32).
+PP_FN uint64_t short_decimal_to_binary64(uint32_t w, int k) {
+  const int lz = clz32(w);
+  const uint32_t W = w << lz;
+#if defined(__CUDA_ARCH__)
+  const uint4 r = __ldg(reinterpret_cast<const uint4*>(pp_r10) + k);
+  const uint32_t r0 = r.x, r1 = r.y, r2 = r.z;
+  const int e = int(r.w);
+#else
+  const uint32_t r0 = pp_r10[4 * k], r1 = pp_r10[4 * k + 1], r2 = pp_r10[4 * k + 2];
+  const int e = int(pp_r10[4 * k + 3]);
+#endif
+  const uint64_t m1 = uint64_t(W) * r1 + umulhi32(W, r0);
+  const uint64_t T = uint64_t(W) * r2 + (m1 >> 32);  // in [2^62, 2^64)
+  const int h = int(T >> 63);
+  const uint64_t m = ((T >> (9 + h)) + 1u) >> 1;     // 53 bits (2^53 after a carry)
+  // value = m * 2^(E - 52) with E = 31 + h - lz - e; adding m carries its
+  // leading bit into the exponent field
+  return (uint64_t(31 + h - lz - e + 1022) << 52) + m;
 }
 
 struct FloatAcc {

@@ -387,61 +387,6 @@ __device__ __forceinline__ uint64_t tile_load8(const uint32_t* tile_w, uint32_t 
   return uint64_t(__funnelshift_r(w0, w1, sh)) | (uint64_t(__funnelshift_r(w1, w2, sh)) << 32);
 }
 
-// ------------------------------------------------- numeric fast paths
-// Characters are handled four to a 32-bit word (character i in byte i);
-// y = chars ^ '0' maps digits to 0..9 and '.' to 0x1E.
-// 0x80 in each byte of y above 9
-__device__ __forceinline__ uint32_t nondigit_bytes(uint32_t y) {
-  return (((y & 0x7F7F7F7Fu) + 0x76767676u) | y) & 0x80808080u;
-}
-// 0x80 in each zero byte of v
-__device__ __forceinline__ uint32_t zero_bytes(uint32_t v) {
-  return ~(((v & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) | v | 0x7F7F7F7Fu);
-}
-// 0x80 in each of the first n (0..4) bytes
-__device__ __forceinline__ uint32_t first_bytes(int n) {
-  return n >= 4 ? 0x80808080u : (n <= 0 ? 0u : 0x80808080u & ((1u << (8 * n)) - 1u));
-}
-// value of the 4 digits in w, byte 0 the most significant
-__device__ __forceinline__ uint32_t val4(uint32_t w) {
-  w = (w * 10u + (w >> 8)) & 0x00FF00FFu;
-  return (w * 100u + (w >> 16)) & 0xFFFFu;
-}
-// Value of the n (1..8) digits in y0:y1 (chars ^ '0'), or false if one is
-// not a digit.
-__device__ __forceinline__ bool digits8(uint32_t y0, uint32_t y1, int n, uint32_t& v) {
-  if ((nondigit_bytes(y0) & first_bytes(n)) | (nondigit_bytes(y1) & first_bytes(n - 4))) return false;
-  // right-align: the last digit to byte 7, zeros before the first
-  const uint32_t sh = 8u * uint32_t(8 - n);
-  uint32_t z0, z1;
-  if (sh >= 32) { z1 = y0 << (sh - 32); z0 = 0; }
-  else { z1 = __funnelshift_l(y0, y1, sh); z0 = y0 << sh; }
-  v = val4(z0) * 10000u + val4(z1);
-  return true;
-}
-// n (1..8) characters in x0:x1 as digits[.digits] (at most one dot, at
-// least one digit): significand (< 10^8) and decimal exponent (-7..0).
-__device__ __forceinline__ bool dec8(uint32_t x0, uint32_t x1, int n, uint32_t& mant, int& q) {
-  uint32_t y0 = x0 ^ 0x30303030u, y1 = x1 ^ 0x30303030u;
-  const uint32_t d0 = zero_bytes(y0 ^ 0x1E1E1E1Eu) & first_bytes(n);
-  const uint32_t d1 = zero_bytes(y1 ^ 0x1E1E1E1Eu) & first_bytes(n - 4);
-  q = 0;
-  if (d0 | d1) {
-    if (__popc(d0) + __popc(d1) > 1) return false;
-    const int p = d0 ? (__ffs(d0) - 1) >> 3 : 4 + ((__ffs(d1) - 1) >> 3);
-    // squeeze the dot out of the 8-byte string
-    uint64_t Y = (uint64_t(y1) << 32) | y0;
-    const uint64_t below = (1ull << (8 * p)) - 1ull;
-    Y = (Y & below) | ((Y >> 8) & ~below);
-    y0 = uint32_t(Y);
-    y1 = uint32_t(Y >> 32);
-    --n;
-    q = p - n;
-    if (n == 0) return false;
-  }
-  return digits8(y0, y1, n, mant);
-}
-
 __device__ __forceinline__ void load_lut(const ParseParams& P, uint32_t* lut_s) {
   for (int k = threadIdx.x; k < 256 * 32; k += NT) lut_s[k] = P.lut[k >> 5];
 }
@@ -588,7 +533,7 @@ constexpr int CTX_HDR = 52;  // transition vector + (records, column, last) per 
 // and the others are zero: the scan reads a tile's slots only along the path
 // from the input's start state, which enters every tile in its true state.
 template <int NS>
-__global__ void __launch_bounds__(NT, 2) ctx_kernel(const __grid_constant__ ParseParams P) {
+__global__ void __launch_bounds__(NT, 3) ctx_kernel(const __grid_constant__ ParseParams P) {
   constexpr int NSW = NS > 0 ? (NS + 3) / 4 : 1;
   extern __shared__ __align__(128) uint8_t smem[];
   uint32_t* lut_s = reinterpret_cast<uint32_t*>(smem);
@@ -1159,73 +1104,102 @@ __device__ __forceinline__ int convert_general(const ParseParams& P, uint32_t ty
   return err;
 }
 
+// The tile context a numeric field's conversion needs.
+struct NumCtx {
+  uint64_t tile_base, tile_fstart;  // the tile's first byte; start of the field open at it
+  uint32_t tile_fstate;             // DFA state at tile_fstart
+  const uint8_t* tile_s;
+  const uint32_t* tile_w;
+  const uint32_t* ctrl_s;
+  const uint16_t* cpre;
+  const uint32_t* my_lut;
+  bool any_ctrl;
+};
+
 // Convert the numeric field in slot value v (tile-relative start << 16 |
 // end; start 0xFFFF = the field began in an earlier tile; SLOT_DEFAULT = a
-// missing field) of a column of type ty; lim_pos / lim_neg bound integer
-// magnitudes.  Plain fields inside the tile take word-parallel fast paths:
-// an integer of at most 16 digits, or a decimal of at most 8 characters
-// after the sign converted by short_decimal_to_binary64; everything else
-// streams through the accumulators.  Returns the error bits; *val gets the
-// value's bits (0 for an empty field or an error).
-__device__ __forceinline__ int convert_num(const ParseParams& P, uint32_t ty, uint64_t lim_pos,
-                                           uint64_t lim_neg, uint32_t v, uint64_t tile_base,
-                                           uint64_t tile_fstart, uint32_t tile_fstate,
-                                           const uint8_t* tile_s, const uint32_t* tile_w,
-                                           const uint32_t* ctrl_s, const uint16_t* cpre,
-                                           const uint32_t* my_lut, bool any_ctrl, uint64_t& val) {
+// missing field) for a column of type TY.  A plain field inside the tile
+// and free of control bytes is decoded word-parallel: at most 8 characters
+// after the sign (an integer, or for floats a decimal with one '.'
+// converted by short_decimal_to_binary64), or an integer of 9 to 16 digits
+// in two such words.  Everything else streams through the accumulators.
+// Returns the error bits; val gets the value's bits (0 for an empty field
+// or an error).
+template <int TY>
+__device__ __forceinline__ int convert_field(const ParseParams& P, uint32_t v, const NumCtx& X,
+                                             uint64_t& val) {
   val = 0;
   if (v == SLOT_DEFAULT) return 0;
   const uint32_t fsr = v >> 16, fe = v & 0xFFFFu;
-  if (fsr != 0xFFFFu && (!any_ctrl || ctrl_before(ctrl_s, cpre, fe) == ctrl_before(ctrl_s, cpre, fsr))) {
+  if (fsr != 0xFFFFu &&
+      (!X.any_ctrl || ctrl_before(X.ctrl_s, X.cpre, fe) == ctrl_before(X.ctrl_s, X.cpre, fsr))) {
     const uint32_t L = fe - fsr;
     if (L == 0) return 0;  // empty field: the column default
-    const uint64_t x = tile_load8(tile_w, fsr);
-    uint32_t x0 = uint32_t(x), x1 = uint32_t(x >> 32);
-    const uint32_t c0 = x0 & 0xFFu;
-    const bool neg = c0 == '-';
+    const uint32_t c0 = X.tile_s[fsr];
     const uint32_t sg = (c0 == '-' || c0 == '+') ? 1u : 0u;
+    const bool neg = c0 == '-';
     const int n = int(L - sg);
-    if (sg) {
-      x0 = __funnelshift_r(x0, x1, 8);
-      x1 = (x1 >> 8) | (uint32_t(tile_s[fsr + 8]) << 24);
-    }
-    if (ty == PP_COL_FLOAT64) {
-      uint32_t mant;
-      int q;
-      if (n >= 1 && n <= 8 && dec8(x0, x1, n, mant, q)) {
-        val = (mant ? ppn::short_decimal_to_binary64(mant, q) : 0ull) | (neg ? (1ull << 63) : 0ull);
+    const uint32_t pv = fsr + sg, q = pv >> 2, sh = (pv & 3u) * 8u;
+    const uint32_t w0 = X.tile_w[q], w1 = X.tile_w[q + 1];
+    const uint32_t x0 = __funnelshift_r(w0, w1, sh);
+    uint32_t w;
+    if (TY != PP_COL_FLOAT64 && n >= 1 && n <= 4) {  // up to 4 digits: one word
+      const uint32_t y = x0 ^ 0x30303030u, a = 32u - 8u * uint32_t(n);
+      if (!(ppn::nondigit_bytes(y) & (0x80808080u >> a))) {
+        w = ppn::val4(y << a);
+        if (TY == PP_COL_INT8 && w > (neg ? 128u : 127u)) return PP_ERR_NUM_OVERFLOW;
+        val = neg ? uint64_t(0) - w : uint64_t(w);
         return 0;
       }
-    } else {
-      uint64_t mag = 0;
-      bool ok = false;
-      if (n == 1) {
-        mag = (x0 & 0xFFu) - 48u;
-        ok = mag <= 9;
-      } else if (n >= 2 && n <= 8) {
-        uint32_t w;
-        ok = digits8(x0 ^ 0x30303030u, x1 ^ 0x30303030u, n, w);
-        mag = w;
-      } else if (n > 8 && n <= 16) {
-        const uint64_t x2 = tile_load8(tile_w, fsr + sg + 8);
-        uint32_t vh, vl;
-        ok = digits8(x0 ^ 0x30303030u, x1 ^ 0x30303030u, 8, vh) &&
-             digits8(uint32_t(x2) ^ 0x30303030u, uint32_t(x2 >> 32) ^ 0x30303030u, n - 8, vl);
-        if (ok) {
-          uint32_t p10 = 1;
-          for (int i = 8; i < n; ++i) p10 *= 10u;
-          mag = uint64_t(vh) * p10 + vl;
-        }
+    }
+    const uint32_t x1 = __funnelshift_r(w1, X.tile_w[q + 2], sh);
+    const uint64_t x = (uint64_t(x1) << 32) | x0;
+    int k;
+    if (n >= 1 && n <= 8 &&
+        ppn::short_decimal(uint32_t(x), uint32_t(x >> 32), n, TY == PP_COL_FLOAT64, &w, &k)) {
+      if (TY == PP_COL_FLOAT64) {
+        val = (w ? ppn::short_decimal_to_binary64(w, k) : 0ull) | (neg ? (1ull << 63) : 0ull);
+        return 0;
       }
-      if (ok) {
-        if (mag > (neg ? lim_neg : lim_pos)) return PP_ERR_NUM_OVERFLOW;
-        val = neg ? (~mag + 1) : mag;
+      if (TY == PP_COL_INT8 && w > (neg ? 128u : 127u)) return PP_ERR_NUM_OVERFLOW;
+      val = neg ? uint64_t(0) - w : uint64_t(w);
+      return 0;
+    }
+    if (TY != PP_COL_FLOAT64 && n > 8 && n <= 16) {
+      const uint64_t x2 = tile_load8(X.tile_w, fsr + sg + 8);
+      uint32_t wl;
+      if (ppn::short_decimal(uint32_t(x), uint32_t(x >> 32), 8, false, &w, &k) &&
+          ppn::short_decimal(uint32_t(x2), uint32_t(x2 >> 32), n - 8, false, &wl, &k)) {
+        uint32_t p10 = 10u;  // 10^(n - 8)
+        for (int i = 9; i < n; ++i) p10 *= 10u;
+        const uint64_t mag = uint64_t(w) * p10 + wl;
+        const uint64_t lim = TY == PP_COL_INT8 ? 127ull : TY == PP_COL_INT32 ? 2147483647ull
+                                                                              : 9223372036854775807ull;
+        if (mag > lim + (neg ? 1u : 0u)) return PP_ERR_NUM_OVERFLOW;
+        val = neg ? ~mag + 1 : mag;
         return 0;
       }
     }
   }
-  return convert_general(P, ty, fsr == 0xFFFFu ? tile_fstart : tile_base + fsr, tile_base + fe,
-                         tile_base, tile_s, ctrl_s, my_lut, tile_fstate, &val);
+  return convert_general(P, TY, fsr == 0xFFFFu ? X.tile_fstart : X.tile_base + fsr,
+                         X.tile_base + fe, X.tile_base, X.tile_s, X.ctrl_s, X.my_lut,
+                         X.tile_fstate, &val);
+}
+
+// Convert one row's field of a column of type TY and store it at out[rec].
+template <int TY>
+__device__ __forceinline__ void convert_store(const ParseParams& P, const NumCtx& X, void* out,
+                                              uint64_t rec, uint32_t v) {
+  uint64_t val;
+  const int err = convert_field<TY>(P, v, X, val);
+  if (TY == PP_COL_FLOAT64) static_cast<uint64_t*>(out)[rec] = val;
+  else if (TY == PP_COL_INT64) static_cast<int64_t*>(out)[rec] = int64_t(val);
+  else if (TY == PP_COL_INT32) static_cast<int32_t*>(out)[rec] = int32_t(val);
+  else static_cast<int8_t*>(out)[rec] = int8_t(val);
+  if (err) {
+    const uint32_t fsr = v >> 16;
+    report(P.st, err, fsr == 0xFFFFu ? X.tile_fstart : X.tile_base + fsr, true);
+  }
 }
 
 // ================================================================ 3. main
@@ -1434,6 +1408,11 @@ __global__ void __launch_bounds__(NT, 2) main_kernel(const __grid_constant__ Par
       S.cpre[t] = uint16_t(S.wsum[warp] + xi - nc);
     }
 
+    const NumCtx X = {tile_base, tile_fstart, tile_fstate, tile_s, tile_w, ctrl_s, S.cpre, my_lut,
+                      any_ctrl};
+    const uint32_t rec_lim =  // records of the tile the outputs have room for
+        P.rec_cap > rec0 ? uint32_t(min(P.rec_cap - rec0, uint64_t(0xFFFFFFFFu))) : 0u;
+
     // ---- fields -> (column, row) slots, in passes of rows
     {
       for (uint32_t lo = 0; lo < rows; lo += rpb) {
@@ -1597,42 +1576,27 @@ __global__ void __launch_bounds__(NT, 2) main_kernel(const __grid_constant__ Par
           }
         }
 
-        // ---- numbers: a warp per 32 rows of one column
-        {  // items (numeric column oc, group gi of 32 rows), warp-strided
-          const uint32_t n_num = S.n_num;
-          uint32_t oc = 0, gi = uint32_t(warp);
-          while (gi >= ngr && oc < n_num) { gi -= ngr; ++oc; }
-          while (oc < n_num) {
+        // ---- numbers: a warp per item (numeric column, 32 rows), a lane per row
+        {
+          const uint32_t n_items = S.n_num * ngr;
+          const uint32_t magic = ngr > 1 ? 0xFFFFFFFFu / ngr + 1u : 0u;  // it / ngr, it < 2^16
+          for (uint32_t it = uint32_t(warp); it < n_items; it += NW) {
+            const uint32_t oc = ngr > 1 ? __umulhi(it, magic) : it;
             const uint32_t c = S.numcol[oc];
-            const uint32_t ty = S.coltype[c];
-            uint8_t* const out = static_cast<uint8_t*>(P.typed[c]);
-            const uint64_t lim_pos = ty == PP_COL_INT8 ? 127ull : ty == PP_COL_INT32 ? 2147483647ull
-                                                                 : 9223372036854775807ull;
-            const uint32_t r_first = c < col_in ? 1u : 0u;       // rows whose field c closes here
+            const uint32_t r = lo + (it - oc * ngr) * 32 + lane;
+            const uint32_t r_first = c < col_in ? 1u : 0u;  // rows whose field c closes here
             const uint32_t r_end = c < col_end ? rows : rows - 1u;
-            const uint32_t* col_slots = slot_s + c * nr;
-            for (; gi < ngr; gi += NW) {
-              const uint32_t r = lo + gi * 32 + lane;
-              if (r >= hi || r < r_first || r >= r_end) continue;
-              const uint64_t rec = rec0 + r;
-              if (rec >= P.rec_cap) { report(P.st, PP_ERR_CAPACITY, 0, false); continue; }
-              const uint32_t v = col_slots[r - lo];
-              uint64_t val;
-              const int err = convert_num(P, ty, lim_pos, lim_pos + 1, v, tile_base, tile_fstart,
-                                          tile_fstate, tile_s, tile_w, ctrl_s, S.cpre, my_lut,
-                                          any_ctrl, val);
-              if (ty == PP_COL_FLOAT64) reinterpret_cast<uint64_t*>(out)[rec] = val;
-              else if (ty == PP_COL_INT32) reinterpret_cast<int32_t*>(out)[rec] = int32_t(val);
-              else if (ty == PP_COL_INT64) reinterpret_cast<int64_t*>(out)[rec] = int64_t(val);
-              else reinterpret_cast<int8_t*>(out)[rec] = int8_t(val);
-              if (err) {
-                const uint32_t fsr = v >> 16;
-                report(P.st, err, fsr == 0xFFFFu ? tile_fstart : tile_base + fsr, true);
-              }
+            if (r >= hi || r < r_first || r >= r_end) continue;
+            if (r >= rec_lim) { report(P.st, PP_ERR_CAPACITY, 0, false); continue; }
+            const uint32_t v = slot_s[c * nr + (r - lo)];
+            void* const out = P.typed[c];
+            const uint64_t rec = rec0 + r;
+            switch (S.coltype[c]) {
+              case PP_COL_FLOAT64: convert_store<PP_COL_FLOAT64>(P, X, out, rec, v); break;
+              case PP_COL_INT64: convert_store<PP_COL_INT64>(P, X, out, rec, v); break;
+              case PP_COL_INT32: convert_store<PP_COL_INT32>(P, X, out, rec, v); break;
+              default: convert_store<PP_COL_INT8>(P, X, out, rec, v); break;
             }
-            gi -= ngr;
-            ++oc;
-            while (gi >= ngr && oc < n_num) { gi -= ngr; ++oc; }
           }
         }
         __syncthreads();

@@ -19,6 +19,13 @@ void h_parse_floats(const unsigned char* buf, size_t n, uint64_t* bits, int* err
 }
 uint64_t h_decimal_to_binary64(uint64_t w, int q) { return ppn::decimal_to_binary64(w, q); }
 uint64_t h_short_decimal_to_binary64(uint32_t w, int q) {
-  return ppn::short_decimal_to_binary64(w, q);
+  return ppn::short_decimal_to_binary64(w, -q);
+}
+// the 8 bytes at s as a short plain decimal of n characters
+int h_short_decimal(const unsigned char* s, int n, int dot, uint32_t* w, int* k) {
+  uint32_t x0 = 0, x1 = 0;
+  for (int i = 0; i < 4; ++i) x0 |= uint32_t(s[i]) << (8 * i);
+  for (int i = 0; i < 4; ++i) x1 |= uint32_t(s[4 + i]) << (8 * i);
+  return ppn::short_decimal(x0, x1, n, dot != 0, w, k) ? 1 : 0;
 }
 }

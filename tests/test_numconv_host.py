@@ -156,22 +156,23 @@ def _exact(ws, qs):
 
 
 def test_short_significand_edges(harness):
-    """The short path (w < 2^32, -22 <= q <= 0): dyadic values and the ends
+    """The short path (w < 2^32, -17 <= q <= 0): dyadic values and the ends
     of the range are exact."""
-    cases = [(1, 0), (9, 0), (4294967295, 0), (5, -1), (25, -2), (125, -3), (1, -1), (1, -22),
-             (4294967295, -22), (4294967295, -1), (46386, -2), (50000, -2), (3, -1),
-             (123456789, -7), (1, -8), (999999999, -9)]
+    cases = [(1, 0), (9, 0), (4294967295, 0), (5, -1), (25, -2), (125, -3), (1, -1), (1, -17),
+             (4294967295, -17), (4294967295, -1), (46386, -2), (50000, -2), (3, -1),
+             (123456789, -7), (1, -8), (999999999, -9), (2 ** 31, 0), (2 ** 31 - 1, -3),
+             (5 ** 13, -13), (99999999, -7), (10000000, -7)]
     ws, qs = zip(*cases)
     assert (_short(harness, ws, qs) == _exact(ws, qs)).all()
 
 
 @pytest.mark.parametrize("seed", range(3))
 def test_short_significand_random(harness, seed):
-    """Random w < 2^32 and q in [-22, 0] against exact rational rounding:
+    """Random w < 2^32 and q in [-17, 0] against exact rational rounding:
     correctly rounded."""
     rng = random.Random(50 + seed)
     ws = [rng.choice([rng.randrange(1, 1 << 32), rng.randrange(1, 100000)]) for _ in range(20000)]
-    qs = [rng.randint(-22, 0) for _ in ws]
+    qs = [rng.randint(-17, 0) for _ in ws]
     assert (_short(harness, ws, qs) == _exact(ws, qs)).all()
 
 
@@ -181,3 +182,59 @@ def test_short_significand_workload_shapes_exact(harness):
     ws = [rng.randint(1, 50000) for _ in range(20000)] + [rng.randint(1, 999999) for _ in range(20000)]
     qs = [-2] * 20000 + [rng.randint(-6, 0) for _ in range(20000)]
     assert (_short(harness, ws, qs) == _exact(ws, qs)).all()
+
+
+def _short_decimal(L, s, n, dot):
+    L.h_short_decimal.restype = ctypes.c_int
+    L.h_short_decimal.argtypes = [ctypes.c_char_p, ctypes.c_int, ctypes.c_int,
+                                  ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(ctypes.c_int)]
+    w, k = ctypes.c_uint32(0), ctypes.c_int(0)
+    ok = L.h_short_decimal(s, n, dot, ctypes.byref(w), ctypes.byref(k))
+    return (w.value, k.value) if ok else None
+
+
+def _short_decimal_want(s, n, dot):
+    """Plain reading: n digits, or (dot) digits with one '.' and at least one
+    digit; the value as (digits as an integer, digits after the '.')."""
+    t = s[:n]
+    digits = b"".join(bytes([c]) for c in t if 0x30 <= c <= 0x39)
+    dots = t.count(b".")
+    if len(digits) + dots != n or (dots and not dot) or dots > 1 or not digits:
+        return None
+    k = n - 1 - t.index(b".") if dots else 0
+    return int(digits), k
+
+
+def test_short_decimal_exhaustive_small(harness):
+    """Every string of 1..3 characters over digits, '.', signs, 'e' and
+    bytes that alias digits or '.' in their low bits, with garbage after."""
+    import itertools
+    alpha = [b"0", b"5", b"9", b".", b"+", b"e", b"/", b":", b"\x80", b"\xae", b"\xb5", b" ", b"\x00"]
+    for n in (1, 2, 3):
+        for tup in itertools.product(alpha, repeat=n):
+            s = b"".join(tup) + b"7.x\x00\xff9.1"[: 8 - n]
+            for dot in (0, 1):
+                assert _short_decimal(harness, s, n, dot) == _short_decimal_want(s, n, dot), (s, n, dot)
+
+
+@pytest.mark.parametrize("seed", range(2))
+def test_short_decimal_random(harness, seed):
+    """Random 1..8-character fields: mostly valid plain decimals (the
+    workloads' shapes), some with one character replaced."""
+    rng = random.Random(70 + seed)
+    for _ in range(20000):
+        n = rng.randint(1, 8)
+        kind = rng.random()
+        if kind < 0.4:
+            t = "".join(rng.choice("0123456789") for _ in range(n))
+        else:
+            t = "".join(rng.choice("0123456789") for _ in range(n))
+            if n > 1:
+                i = rng.randrange(n)
+                t = t[:i] + "." + t[i + 1:]
+        s = bytearray(t.encode() + bytes(rng.randrange(256) for _ in range(8 - n)))
+        if rng.random() < 0.2:
+            s[rng.randrange(n)] = rng.choice(b".-+e/:\x80\xae\xb0 0")
+        s = bytes(s)
+        for dot in (0, 1):
+            assert _short_decimal(harness, s, n, dot) == _short_decimal_want(s, n, dot), (s, n, dot)
