@@ -1204,6 +1204,7 @@ __device__ __forceinline__ void convert_store(const ParseParams& P, const NumCtx
 
 // ================================================================ 3. main
 constexpr uint32_t SHORT_FIELD = 32;  // longer string fields are staged chunk-parallel
+constexpr uint32_t WLIST_CAP = 512;   // terminators per warp listed in the staging buffer
 constexpr uint16_t NO_FIELD = 0xFFFFu;
 
 struct MainShared {
@@ -1382,6 +1383,16 @@ __global__ void __launch_bounds__(NT, 2) main_kernel(const __grid_constant__ Par
     const uint32_t rl0 = pre.rec;
     const uint32_t term_all = fd | rd;
     const bool owns_tail = clen > 0 && cstart + clen == tile_len;
+    // terminators per chunk (plus the virtual RD that closes the input),
+    // their prefix in the warp and the warp's count
+    const uint32_t nterm = __popc(term_all) + (virt_rd ? 1u : 0u);
+    uint32_t tincl = nterm;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const uint32_t o = __shfl_up_sync(FULL, tincl, d);
+      if (lane >= d) tincl += o;
+    }
+    const uint32_t tbase = tincl - nterm, wn = __shfl_sync(FULL, tincl, 31);
     if (any_ctrl) {  // control bytes before each chunk: O(1) value-byte counts
       const uint32_t nc = __popc(g.ctrl);
       uint32_t xi = nc;
@@ -1418,7 +1429,54 @@ __global__ void __launch_bounds__(NT, 2) main_kernel(const __grid_constant__ Par
       for (uint32_t lo = 0; lo < rows; lo += rpb) {
         const uint32_t hi = min(rows, lo + rpb), nr = hi - lo;
         if (NS > 0) { S.lk[0][t] = NO_FIELD; S.lk[1][t] = NO_FIELD; }
-        {  // walk this chunk's fields
+        if (wn <= WLIST_CAP) {
+          // the warp's terminators in input order (tile position | RD << 15),
+          // then a lane per field: row and column from a ballot of the RDs
+          uint16_t* const wl = reinterpret_cast<uint16_t*>(stage_s) + warp * WLIST_CAP;
+          {
+            uint32_t m = term_all, i = tbase;
+            while (m) {
+              const uint32_t j = __ffs(m) - 1;
+              m &= m - 1;
+              wl[i++] = uint16_t((cstart + j) | (((rd >> j) & 1u) << 15));
+            }
+            if (virt_rd) wl[i] = uint16_t(tile_len | 0x8000u);
+          }
+          __syncwarp();
+          // row, column and field start before the batch's first field
+          uint32_t crow = __shfl_sync(FULL, rl0, 0), ccol = __shfl_sync(FULL, col0, 0),
+                   cfs = __shfl_sync(FULL, fs0, 0);
+          const uint32_t lt = (1u << lane) - 1u;
+          for (uint32_t b0 = 0; b0 < wn; b0 += 32) {
+            const uint32_t k = b0 + uint32_t(lane);
+            const uint32_t ent = k < wn ? uint32_t(wl[k]) : 0u;
+            const uint32_t e = ent & 0x7FFFu;
+            const bool isrd = (ent >> 15) != 0;
+            const uint32_t pe = __shfl_up_sync(FULL, e, 1);
+            const uint32_t fs = lane == 0 ? cfs : pe + 1u;
+            const uint32_t rdm = __ballot_sync(FULL, isrd);
+            const uint32_t below = rdm & lt;
+            const uint32_t rl = crow + __popc(below);
+            const uint32_t col = below ? uint32_t(lane) - (32u - __clz(below))
+                                       : min(ccol + uint32_t(lane), 0x7FFFFF00u);
+            if (k < wn) {
+              const bool in_pass = rl - lo < nr;
+              if (in_pass && col < n_cols) slot_s[col * nr + (rl - lo)] = (fs << 16) | e;
+              if (isrd && col != n_cols - 1) {
+                if (lo == 0) report(P.st, PP_ERR_COLCOUNT, tile_base + e, true);
+                if (in_pass)  // missing fields take the column default
+                  for (uint32_t c = col + 1; c < n_cols; ++c) slot_s[c * nr + (rl - lo)] = SLOT_DEFAULT;
+              }
+            }
+            const uint32_t nin = min(32u, wn - b0);
+            crow += __popc(rdm);
+            ccol = rdm ? (nin - 1u) - (31u - __clz(rdm)) : min(ccol + nin, 0x7FFFFF00u);
+            cfs = __shfl_sync(FULL, e, nin - 1) + 1u;
+          }
+          // the field still open at the tile end (its value bytes are staged)
+          if (NS > 0 && owns_tail && !any_virt && crow - lo < nr && ccol < n_cols)
+            slot_s[ccol * nr + (crow - lo)] = (cfs << 16) | tile_len;
+        } else {  // each lane walks its chunk's fields
           uint32_t term = term_all, col = col0, rl = rl0, fs = fs0;
           bool vrd = virt_rd;
           for (;;) {
