@@ -86,13 +86,16 @@ def seed_of(name: str) -> int:
 
 def generate(name: str, target: int | None = None, seed: int | None = None,
              out_ptr: int | None = None, out_cap: int | None = None,
-             sidecar: bool = False, record_offsets: bool = False):
+             sidecar: bool = False, record_offsets: bool = False,
+             record_offsets_cap: int | None = None):
     """Generate workload `name`.
 
     Returns (data, info, side): `data` is a numpy uint8 array (a view of the
     caller's buffer when `out_ptr` is given), `info` a dict with n_bytes,
     n_records, n_fields, n_tokens, quoted_bytes, and `side` the ground-truth
-    sidecar bytes (or None).
+    sidecar bytes (or None).  With `record_offsets`, info["record_offsets"]
+    holds the start offset of each record (top-level value for the token
+    stream), the first `record_offsets_cap` of them (default: room for all).
     """
     w = WORKLOADS[name]
     target = w["target"] if target is None else int(target)
@@ -110,7 +113,8 @@ def generate(name: str, target: int | None = None, seed: int | None = None,
     info = _Info()
     roff = None
     if record_offsets:
-        roff = np.zeros(target // 2 + 2, dtype=np.uint64)
+        cap_r = target // 2 + 2 if record_offsets_cap is None else int(record_offsets_cap)
+        roff = np.zeros(max(cap_r, 1), dtype=np.uint64)
     rc = lib.dg_generate(w["index"], target, seed, ptr, cap,
                          side_buf.ctypes.data if sidecar else None, side_cap,
                          ctypes.byref(info), roff.ctypes.data if roff is not None else None,
