@@ -285,6 +285,10 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
   return mbar_try_wait(bar, parity);
 }
+// Start moving the 128-byte line at p towards L2 (a hint; no result).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
 // Global -> shared bulk copy completed on `bar` (dst, src 16-byte aligned,
 // bytes a multiple of 16).  Orders the CTA's earlier generic-proxy accesses
 // of dst before the asynchronous write.

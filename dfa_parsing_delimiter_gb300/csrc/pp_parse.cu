@@ -128,11 +128,12 @@ __device__ __forceinline__ uint32_t ctrl_before(const uint32_t* ctrl_s, const ui
 }
 
 // ------------------------------------------------- tile feeding (TMA)
-// Two linear landing buffers.  A block takes its first tile at start; when
-// it starts processing a tile it takes the next ticket and starts that
-// tile's bulk copy into the other buffer, which the previous tile has
-// released.  Tickets are thus taken in the order tiles start, and a tile's
-// predecessors have all started before it.
+// Two linear landing buffers.  A block takes its first tile at start; once
+// a tile has landed it takes the next ticket and starts that tile's bulk
+// copy into the other buffer, which the previous tile released at its last
+// block barrier, so the copy runs while the current tile is processed.
+// Neither pass waits on another tile, so the order in which tickets are
+// taken carries no constraint.
 struct Feed {
   uint64_t bar[2];
   uint32_t tile[2], issued[2], parity[2];
@@ -166,8 +167,8 @@ __device__ __forceinline__ void feed_start(const ParseParams& P, Feed& F, uint32
 }
 
 // Wait until the current tile is in its landing buffer (plain loads for a
-// ragged tail or unaligned input), start the next tile's copy into the
-// other buffer, and load this thread's chunk words.
+// ragged tail or unaligned input), take the next ticket and start that
+// tile's copy into the other buffer, and load this thread's chunk words.
 __device__ __forceinline__ void feed_tile(const ParseParams& P, Feed& F, uint32_t* counter,
                                           bool aligned_in, uint8_t* lin0, uint64_t tile_base,
                                           uint32_t tile_len, uint32_t (&w)[8]) {
@@ -185,6 +186,11 @@ __device__ __forceinline__ void feed_tile(const ParseParams& P, Feed& F, uint32_
     for (uint32_t k = bulk + t; k < tile_len; k += NT) lin_s[k] = P.in[tile_base + k];
     __syncthreads();
   }
+  if (t == 0) {
+    const uint32_t o = b ^ 1u;
+    F.tile[o] = atomicAdd(counter, 1u);
+    F.issued[o] = issue_tile(P, F.tile[o], aligned_in, lin0 + o * TILE, &F.bar[o]);
+  }
   const uint4* src = reinterpret_cast<const uint4*>(lin_s + uint32_t(t) * CB);
   const int sw = (t >> 2) & 1;  // alternate read order: conflict-free 16-byte reads
   const uint4 x = src[sw], y = src[sw ^ 1];
@@ -194,16 +200,12 @@ __device__ __forceinline__ void feed_tile(const ParseParams& P, Feed& F, uint32_
 }
 
 // After the last read of the current buffer (the caller's earlier block
-// barrier): switch to the other buffer.
-__device__ __forceinline__ void feed_next(const ParseParams& P, Feed& F, uint32_t* counter,
-                                          bool aligned_in, uint8_t* lin0) {
+// barrier): switch to the other buffer, whose tile is already on its way.
+__device__ __forceinline__ void feed_next(Feed& F) {
   if (threadIdx.x == 0) {
     const uint32_t b = F.cur;
     if (F.issued[b]) F.parity[b] ^= 1u;
-    const uint32_t o = b ^ 1u;
-    F.tile[o] = atomicAdd(counter, 1u);
-    F.issued[o] = issue_tile(P, F.tile[o], aligned_in, lin0 + o * TILE, &F.bar[o]);
-    F.cur = o;
+    F.cur = b ^ 1u;
   }
   __syncthreads();
 }
@@ -211,7 +213,8 @@ __device__ __forceinline__ void feed_next(const ParseParams& P, Feed& F, uint32_
 __device__ __forceinline__ void feed_finish(Feed& F) {
   // never leave with a bulk copy in flight into this CTA's shared memory
   // (only the current buffer can have one: a copy is started only for a
-  // tile that exists, and every such tile is waited for before it is used)
+  // tile that exists, and every such tile is processed, so waited for,
+  // before the loop ends)
   if (threadIdx.x == 0 && F.issued[F.cur]) mbar_wait_bounded(&F.bar[F.cur], F.parity[F.cur], WAIT_LIMIT);
 }
 
@@ -753,7 +756,7 @@ __global__ void __launch_bounds__(NT, 3) ctx_kernel(const __grid_constant__ Pars
         crel[k] = uint32_t(s) == s_tile ? uint16_t(S.rel[c]) : uint16_t(0);
       }
     }
-    feed_next(P, S.F, counter, aligned_in, lin0);  // the tile was last read before a barrier above
+    feed_next(S.F);  // the tile was last read before a barrier above
   }
   feed_finish(S.F);
 }
@@ -1515,6 +1518,13 @@ __global__ void __launch_bounds__(NT, 2) main_kernel(const __grid_constant__ Par
         }
         __syncthreads();
         const uint32_t ngr = (nr + 31) / 32;
+        if (lo == 0 && P.s.tags) {  // the next tile's stored tags and prefixes, towards L2
+          const uint32_t nt = S.F.tile[S.F.cur ^ 1u];  // taken before the barrier above
+          if (nt < P.n_tiles) {
+            if ((t & 7) == 0) prefetch_l2(P.s.tags + size_t(nt) * NT + t);
+            if ((t & 15) == 0) prefetch_l2(P.s.vpre + size_t(nt) * NT + t);
+          }
+        }
 
         if (NS > 0 && n_str) {
           // ---- string fields: value bytes -> chars positions (block scan
@@ -1716,7 +1726,7 @@ __global__ void __launch_bounds__(NT, 2) main_kernel(const __grid_constant__ Par
       S.carry[t] = 0;
     }
     if (owns_end) P.st->n_records = rec0 + (rows - 1) + (virt_rd ? 1u : 0u);
-    feed_next(P, S.F, counter, aligned_in, lin0);  // the tile was last read before a barrier above
+    feed_next(S.F);  // the tile was last read before a barrier above
   }
   feed_finish(S.F);
 }

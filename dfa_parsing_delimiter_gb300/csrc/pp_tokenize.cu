@@ -477,7 +477,9 @@ __global__ void tok_carry_kernel(const __grid_constant__ TokParams P) {
 
 // ------------------------------------------------------------ pass 5 tables
 // The DFA steps two bytes per lookup through composed pair transitions:
-// pair[(g1 * 16 + g2) * 16 + s], addressed in bytes as ga[b1] | gb[b2] | 2s,
+// pair[(g1 * 16 + g2) * 16 + s], addressed in bytes as g1 * 512 + g2 * 32 + 2s
+// (the groups come from a byte table, so the 32 lanes' lookups of ASCII
+// bytes fall in distinct banks),
 // holds 2 x the state after both bytes (P2_NEXT2), the state between them
 // (P2_MID), the token-begin flags of the two transitions (P2_BEGIN, first
 // byte in the low bit) and their invalid flags (P2_INV).  The last chunk of
@@ -488,8 +490,7 @@ constexpr uint32_t P2_NEXT2 = 0x1Eu, P2_MID = 0x1E0u, P2_BEGIN_SHIFT = 9, P2_INV
 constexpr uint32_t T_BEGIN = 0x10u, T_INV = 0x20u;
 
 struct DfaTables {
-  uint16_t ga[256];     // group * 512
-  uint16_t gb[256];     // group * 32
+  uint8_t g8[256];      // group
   uint16_t pair[16 * 16 * 16];
   uint8_t grp16[256];   // group * 16
   uint8_t trans[256];
@@ -510,8 +511,7 @@ __device__ void build_dfa_tables(const TokParams& P, DfaTables& S) {
   const int t = threadIdx.x;
   for (int k = t; k < 256; k += blockDim.x) {
     const uint32_t g = P.dfa.byte_to_group[k] & 0xFu;
-    S.ga[k] = uint16_t(g << 9);
-    S.gb[k] = uint16_t(g << 5);
+    S.g8[k] = uint8_t(g);
     S.grp16[k] = uint8_t(g << 4);
     S.trans[k] = uint8_t(trans_of(P, uint32_t(k) >> 4, uint32_t(k) & 0xFu));
     S.byte_token_id[k] = P.dfa.byte_token_id[k];
@@ -539,8 +539,8 @@ __device__ __forceinline__ uint32_t dfa_pairs(const DfaTables& S, const uint32_t
 #pragma unroll
   for (int q = 0; q < 16; ++q) {
     const int j = 32 * h + 2 * q;
-    const uint32_t v =
-        *reinterpret_cast<const uint16_t*>(tb + (S.ga[byte_of(w, j)] | S.gb[byte_of(w, j + 1)] | s2));
+    const uint32_t g1 = S.g8[byte_of(w, j)], g2 = S.g8[byte_of(w, j + 1)];
+    const uint32_t v = *reinterpret_cast<const uint16_t*>(tb + ((g1 << 9) | (g2 << 5) | s2));
     if (STATES) sn[q >> 2] |= ((s2 | (v & P2_MID)) >> 1) << (8 * (q & 3));
     m |= ((v >> P2_BEGIN_SHIFT) & 3u) << (2 * q);
     any |= v;
@@ -637,6 +637,10 @@ __global__ void __launch_bounds__(WT, 4) tok_emit_kernel(const __grid_constant__
     uint32_t w[16];
     load_chunk(P, c0, clen, w);
     uint32_t s = info & 0xFu;
+    {  // the warp's next piece: towards L2 while this one is processed
+      const uint64_t cn = c0 + uint64_t(n_warps) * PIECE;
+      if (cn < P.n) asm volatile("prefetch.global.L2 [%0];" ::"l"(P.in + cn));
+    }
 
     if (total <= CAPW) {
       // ---- stage the starts, then write all three arrays coalesced
@@ -660,17 +664,42 @@ __global__ void __launch_bounds__(WT, 4) tok_emit_kernel(const __grid_constant__
       // they close, k0-1 .. k0+total-2, and of the last token in the last piece
       const uint64_t prev = P.piece_prev[p];  // start + 1 of the token open at the piece start
       const uint32_t nclose = total + (p + 1 == P.n_pieces && !P.carry_out ? 1u : 0u);
-      for (uint32_t q = lane; q < nclose; q += 32) {
-        const uint64_t k = k0 + q;
-        const uint64_t end = q < total ? pbase + E.start[warp][q] : P.n;
-        if (q < total) {
-          if (k < P.cap) P.out_start[k] = end;
-          else if (!sizing) report(P.st, PP_ERR_CAPACITY, 0, false);
+      if (k0 + nclose <= P.cap) {
+        // every entry of the piece fits: piece offsets in 32 bits, the
+        // previous start from the neighbouring lane
+        const uint32_t n_rel = uint32_t(min(P.n - pbase, uint64_t(PIECE)));
+        uint32_t carry = 0;  // the previous batch's last start (lane 31's), for lane 0
+        for (uint32_t b = 0; b < nclose; b += 32) {
+          const uint32_t q = b + uint32_t(lane);
+          const uint32_t e = q < total ? uint32_t(E.start[warp][q]) : n_rel;
+          uint32_t pe = __shfl_up_sync(FULL, e, 1);
+          if (lane == 0) pe = carry;
+          carry = __shfl_sync(FULL, e, 31);
+          if (q < nclose) {
+            if (q < total) P.out_start[k0 + q] = pbase + e;
+            if (q > 0) {
+              P.out_len[k0 + q - 1] = e - pe;
+              P.out_id[k0 + q - 1] = uint8_t(token_id(P, S, E.state[warp][q], pbase + pe));
+            } else if (k0 > 0) {  // the token open at the piece start
+              const uint64_t beg = prev - 1;
+              P.out_len[k0 - 1] = uint32_t(pbase + e - beg);
+              P.out_id[k0 - 1] = uint8_t(token_id(P, S, E.state[warp][0], beg));
+            }
+          }
         }
-        if (k >= 1 && k - 1 < P.cap) {  // token k-1 exists (the first start closes none)
-          const uint64_t beg = q > 0 ? pbase + E.start[warp][q - 1] : prev - 1;
-          P.out_len[k - 1] = uint32_t(end - beg);
-          P.out_id[k - 1] = uint8_t(token_id(P, S, E.state[warp][q], beg));
+      } else {
+        for (uint32_t q = lane; q < nclose; q += 32) {
+          const uint64_t k = k0 + q;
+          const uint64_t end = q < total ? pbase + E.start[warp][q] : P.n;
+          if (q < total) {
+            if (k < P.cap) P.out_start[k] = end;
+            else if (!sizing) report(P.st, PP_ERR_CAPACITY, 0, false);
+          }
+          if (k >= 1 && k - 1 < P.cap) {  // token k-1 exists (the first start closes none)
+            const uint64_t beg = q > 0 ? pbase + E.start[warp][q - 1] : prev - 1;
+            P.out_len[k - 1] = uint32_t(end - beg);
+            P.out_id[k - 1] = uint8_t(token_id(P, S, E.state[warp][q], beg));
+          }
         }
       }
       __syncwarp();
