@@ -151,8 +151,11 @@ __device__ __forceinline__ uint32_t issue_tile(const ParseParams& P, uint32_t ti
   return 1;
 }
 
+// tk (thread 0 only) holds the ticket of the tile after the current one:
+// each ticket is taken one tile before it is used, so the atomic's round
+// trip never stalls the block.
 __device__ __forceinline__ void feed_start(const ParseParams& P, Feed& F, uint32_t* counter,
-                                           bool aligned_in, uint8_t* lin0) {
+                                           bool aligned_in, uint8_t* lin0, uint32_t& tk) {
   if (threadIdx.x == 0) {
     for (int b = 0; b < 2; ++b) {
       mbar_init(&F.bar[b], 1);
@@ -162,6 +165,7 @@ __device__ __forceinline__ void feed_start(const ParseParams& P, Feed& F, uint32
     F.tile[0] = atomicAdd(counter, 1u);
     F.issued[0] = issue_tile(P, F.tile[0], aligned_in, lin0, &F.bar[0]);
     F.cur = 0;
+    tk = atomicAdd(counter, 1u);
   }
   __syncthreads();
 }
@@ -171,7 +175,7 @@ __device__ __forceinline__ void feed_start(const ParseParams& P, Feed& F, uint32
 // tile's copy into the other buffer, and load this thread's chunk words.
 __device__ __forceinline__ void feed_tile(const ParseParams& P, Feed& F, uint32_t* counter,
                                           bool aligned_in, uint8_t* lin0, uint64_t tile_base,
-                                          uint32_t tile_len, uint32_t (&w)[8]) {
+                                          uint32_t tile_len, uint32_t (&w)[8], uint32_t& tk) {
   const int t = threadIdx.x;
   const uint32_t b = F.cur;
   uint8_t* lin_s = lin0 + b * TILE;
@@ -188,8 +192,9 @@ __device__ __forceinline__ void feed_tile(const ParseParams& P, Feed& F, uint32_
   }
   if (t == 0) {
     const uint32_t o = b ^ 1u;
-    F.tile[o] = atomicAdd(counter, 1u);
-    F.issued[o] = issue_tile(P, F.tile[o], aligned_in, lin0 + o * TILE, &F.bar[o]);
+    F.tile[o] = tk;
+    F.issued[o] = issue_tile(P, tk, aligned_in, lin0 + o * TILE, &F.bar[o]);
+    tk = atomicAdd(counter, 1u);
   }
   const uint4* src = reinterpret_cast<const uint4*>(lin_s + uint32_t(t) * CB);
   const int sw = (t >> 2) & 1;  // alternate read order: conflict-free 16-byte reads
@@ -549,7 +554,8 @@ __global__ void __launch_bounds__(NT, 3) ctx_kernel(const __grid_constant__ Pars
   const uint32_t n_cols = uint32_t(P.n_cols);
   const bool aligned_in = (reinterpret_cast<uintptr_t>(P.in) & 15) == 0;
   uint32_t* counter = &P.s.counters[0];
-  feed_start(P, S.F, counter, aligned_in, lin0);
+  uint32_t tk = 0;  // thread 0: the next ticket
+  feed_start(P, S.F, counter, aligned_in, lin0, tk);
 
   for (;;) {
     const uint32_t tile = S.F.tile[S.F.cur];
@@ -558,7 +564,7 @@ __global__ void __launch_bounds__(NT, 3) ctx_kernel(const __grid_constant__ Pars
     const uint64_t tile_base = uint64_t(tile) * TILE;
     const uint32_t tile_len = uint32_t(min(uint64_t(TILE), P.n - tile_base));
     uint32_t w[8];
-    feed_tile(P, S.F, counter, aligned_in, lin0, tile_base, tile_len, w);
+    feed_tile(P, S.F, counter, aligned_in, lin0, tile_base, tile_len, w, tk);
     const uint32_t cstart = uint32_t(t) * CB;
     const uint32_t clen = tile_len > cstart ? min(tile_len - cstart, uint32_t(CB)) : 0u;
     const uint8_t* own = tile_s + cstart;
@@ -1222,7 +1228,7 @@ struct MainShared {
   uint32_t carry[ppi::MAX_STR_COLS];       // chars of earlier passes per string column
   uint64_t base[ppi::MAX_STR_COLS];        // chars offset of the tile per string column
   uint8_t coltype[PP_MAX_COLS];
-  uint8_t numcol[PP_MAX_COLS];             // numeric output columns, in order
+  uint8_t numcol[PP_MAX_COLS];             // numeric output columns, floats first
   uint32_t n_num;
   uint16_t cpre[NT + 1];     // control bytes before chunk t (exclusive scan)
   uint16_t lk[2][NT];        // long string field (item) continuing in / starting in chunk t
@@ -1249,7 +1255,11 @@ __global__ void __launch_bounds__(NT, 2) main_kernel(const __grid_constant__ Par
   if (t == 0) {
     uint32_t m = 0;
     for (uint32_t c = 0; c < uint32_t(P.n_cols); ++c)
-      if (P.coltype[c] != PP_COL_SKIP && P.coltype[c] != PP_COL_STRING) S.numcol[m++] = uint8_t(c);
+      if (P.coltype[c] == PP_COL_FLOAT64) S.numcol[m++] = uint8_t(c);
+    for (uint32_t c = 0; c < uint32_t(P.n_cols); ++c)  // the integer columns after the floats
+      if (P.coltype[c] != PP_COL_SKIP && P.coltype[c] != PP_COL_STRING &&
+          P.coltype[c] != PP_COL_FLOAT64)
+        S.numcol[m++] = uint8_t(c);
     S.n_num = P.has_out ? m : 0u;
   }
   for (int k = t; k < ppi::MAX_STR_COLS; k += NT) S.carry[k] = 0;
@@ -1259,7 +1269,8 @@ __global__ void __launch_bounds__(NT, 2) main_kernel(const __grid_constant__ Par
   const uint32_t rpb = max(1u, uint32_t(SLOT_CAP) / n_cols);  // rows per pass
   const bool aligned_in = (reinterpret_cast<uintptr_t>(P.in) & 15) == 0;
   uint32_t* counter = &P.s.counters[1];
-  feed_start(P, S.F, counter, aligned_in, lin0);
+  uint32_t tk = 0;  // thread 0: the next ticket
+  feed_start(P, S.F, counter, aligned_in, lin0, tk);
 
   for (;;) {
     const uint32_t tile = S.F.tile[S.F.cur];
@@ -1273,7 +1284,7 @@ __global__ void __launch_bounds__(NT, 2) main_kernel(const __grid_constant__ Par
     const PreHdr ph = *reinterpret_cast<const PreHdr*>(pr);
     if (NS > 0 && t < int(n_str)) S.base[t] = reinterpret_cast<const uint64_t*>(pr + PRE_HDR)[t];
     uint32_t w[8];
-    feed_tile(P, S.F, counter, aligned_in, lin0, tile_base, tile_len, w);
+    feed_tile(P, S.F, counter, aligned_in, lin0, tile_base, tile_len, w, tk);
     const uint32_t cstart = uint32_t(t) * CB;
     const uint32_t clen = tile_len > cstart ? min(tile_len - cstart, uint32_t(CB)) : 0u;
     const uint8_t* own = tile_s + cstart;
@@ -1644,17 +1655,19 @@ __global__ void __launch_bounds__(NT, 2) main_kernel(const __grid_constant__ Par
           }
         }
 
-        // ---- numbers: a warp per item (numeric column, 32 rows), a lane per row
+        // ---- numbers: a lane per (numeric column, row) slot, the slots of
+        // the numeric columns taken column by column, 32 to a warp; columns
+        // of one type are adjacent, so a warp mostly runs one conversion
         {
-          const uint32_t n_items = S.n_num * ngr;
-          const uint32_t magic = ngr > 1 ? 0xFFFFFFFFu / ngr + 1u : 0u;  // it / ngr, it < 2^16
-          for (uint32_t it = uint32_t(warp); it < n_items; it += NW) {
-            const uint32_t oc = ngr > 1 ? __umulhi(it, magic) : it;
+          const uint32_t n_slots = S.n_num * nr;
+          const uint32_t magic = nr > 1 ? 0xFFFFFFFFu / nr + 1u : 0u;  // k / nr, exact for k < 2^13
+          for (uint32_t k = uint32_t(warp) * 32 + uint32_t(lane); k < n_slots; k += NT) {
+            const uint32_t oc = nr > 1 ? __umulhi(k, magic) : k;
             const uint32_t c = S.numcol[oc];
-            const uint32_t r = lo + (it - oc * ngr) * 32 + lane;
+            const uint32_t r = lo + (k - oc * nr);
             const uint32_t r_first = c < col_in ? 1u : 0u;  // rows whose field c closes here
             const uint32_t r_end = c < col_end ? rows : rows - 1u;
-            if (r >= hi || r < r_first || r >= r_end) continue;
+            if (r < r_first || r >= r_end) continue;
             if (r >= rec_lim) { report(P.st, PP_ERR_CAPACITY, 0, false); continue; }
             const uint32_t v = slot_s[c * nr + (r - lo)];
             void* const out = P.typed[c];
