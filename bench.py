@@ -47,11 +47,22 @@ def _peaks():
     return 6800.0, "fallback (6.8 TB/s earlier GB300 measurement)"
 
 
+def code_sha(path):
+    """sha256 prefix of a CUDA source's code: comments removed and whitespace
+    collapsed, so an edit of comments alone leaves it unchanged."""
+    import hashlib
+    import re
+    with open(path) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return hashlib.sha256(" ".join(text.split()).encode()).hexdigest()[:16]
+
+
 def _traffic(workload):
     """DRAM bytes per launch of the dominant kernel from a committed ncu
     capture (profiles/ncu_traffic.json), or None when there is none or the
-    kernel source has changed since it was taken."""
-    import hashlib
+    kernel's code has changed since it was taken."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(p):
         return None
@@ -62,9 +73,7 @@ def _traffic(workload):
         return None
     src = os.path.join(ROOT, "dfa_parsing_delimiter_gb300", "csrc",
                        e.get("kernel_source", "pp_parse.cu"))
-    with open(src, "rb") as f:
-        h = hashlib.sha256(f.read()).hexdigest()[:16]
-    if e.get("kernel_source_sha256_prefix") != h:
+    if e.get("kernel_code_sha256_prefix") != code_sha(src):
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -84,7 +93,7 @@ class Clocks:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -204,7 +213,7 @@ def run_reference(args):
     h_in, info = _generate_pinned(args.workload)
     import oracle
     arr = h_in.numpy()
-    # one bounded sample per step, sized for a few seconds of CPU work
+    # one bounded sample per step, sized so the whole run takes a few minutes
     probe = min(arr.size, 8 << 20)
     t0 = time.perf_counter()
     if w["kind"] == "csv":
@@ -212,7 +221,9 @@ def run_reference(args):
     else:
         oracle.tokenize(arr[:probe])
     rate = probe / max(time.perf_counter() - t0, 1e-9)
-    nb = int(min(arr.size, rate * 4.0))
+    # about 2.5 minutes of oracle work for the whole run, 0.5 to 4 s a step
+    per_step = max(0.5, min(4.0, 150.0 / (args.warmup + args.steps)))
+    nb = int(min(arr.size, rate * per_step))
     if w["kind"] == "csv":
         nl = np.flatnonzero(arr[:nb] == 10)
         nb = int(nl[-1]) + 1 if nl.size else nb
@@ -399,7 +410,7 @@ def run_ours(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(datagen.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])

@@ -1,43 +1,45 @@
 // pp_parse: DFA-based parsing of delimiter-separated input into Arrow-style
-// columns on sm_103a, in three kernels with no inter-tile waiting on the hot
-// path.
+// columns on sm_103a, in five kernels with no inter-tile waiting on the
+// byte-level hot path.
 //
-// The input is cut into 16 KiB tiles; each tile is one CTA of 512 threads
-// and each thread owns a 32-byte chunk (one bit per byte in the bitmap
-// indexes).  Tiles reach shared memory by a 1-D bulk copy (TMA engine)
-// into one of two linear buffers, the next tile landing in the other while
-// the current one is processed.
+// The input is cut into 16 KiB tiles.  In the two tile passes a tile is one
+// CTA of 512 threads and each thread owns a 32-byte chunk (one bit per byte
+// in the bitmap indexes).  Tiles reach shared memory by a 1-D bulk copy
+// (TMA engine) into one of two linear buffers, the next tile's copy running
+// while the current one is processed.
 //
-// 1. Context pass (ctx_kernel).  Each thread runs the multi-instance DFA
-//    over its chunk (ParPaRaw Section 3.1, Figure 2): the transition vector
-//    of the four live states sits in one register, one byte per state, and
-//    each byte composes it with its symbol group's row by one byte-permute
-//    (the row-per-group transition table of ParPaRaw Section 5, Table 1,
-//    read from a per-lane replicated shared-memory LUT).  Vectors compose
-//    across the warp (shuffles) and the block.  Because the tile's true
-//    start state is not known yet, the tile then tags its bytes once per
-//    possible start state (threads whose start state does not depend on it
-//    tag once) and records, per start state: record count, absolute or
-//    relative column offset (ParPaRaw Section 3.2, Figure 4), last
-//    terminator, value bytes per string column for fields whose column is
-//    known inside the tile, and value bytes per relative field of the
-//    tile's first, partial record.
-// 2. Scan (scan_kernel).  An exclusive scan over tiles with the composite
-//    operation on transition vectors (ParPaRaw Section 3.1) and the
-//    record-count / column-offset operators (Section 3.2), each applied per
-//    start state, resolves every tile's true start state, record index,
-//    column and last terminator; the tile's value bytes per string column
-//    then follow from its column, and a second scan turns them into chars
-//    offsets.  Blocks chain by a single-pass decoupled look-back.
-// 3. Main pass (main_kernel).  With its context known, each tile tags its
-//    bytes (re-running one DFA per thread over the non-background bytes
-//    only), scans record and column indices across the block, compacts
-//    string value bytes per column into shared memory (stream compaction in
-//    place of ParPaRaw's radix partitioning, Section 3.3) and writes them as
-//    16-byte stores, and enters every closed field in a column-major
-//    (column, record) slot table; one lane per field then writes the Arrow
-//    offset or converts the number (Section 3.3), so a warp handles one
-//    column, one type, with coalesced stores.
+// 0. Tile start states (tile_stv_kernel, tile_state_kernel).  A warp per
+//    tile folds the tile's transition vector (ParPaRaw Section 3.1, Figure
+//    2): the vector of the four live states sits in one register, one byte
+//    per state, and each byte composes it with its symbol group's row by
+//    one byte-permute (the row-per-group transition table of ParPaRaw
+//    Section 5, Table 1, read from a per-lane replicated shared-memory LUT).
+//    An exclusive composite scan over tiles gives every tile's true start
+//    state.
+// 1. Context pass (ctx_kernel).  Each thread folds its chunk's vector the
+//    same way; vectors compose across the warp (shuffles) and the block,
+//    which with the tile's start state gives every chunk's start state.
+//    The thread then tags its chunk (one DFA over the non-background bytes
+//    only) and the tile records, for its true start state: record count,
+//    absolute or relative column offset (ParPaRaw Section 3.2, Figure 4),
+//    last terminator, value bytes per string column for fields whose column
+//    is known inside the tile, and value bytes per relative field of the
+//    tile's first, partial record.  With room in the scratch it also stores
+//    every chunk's tag bitmaps and its (record, column, last terminator)
+//    prefix inside the tile for the main pass.
+// 2. Scan (scan_kernel).  An exclusive scan over tiles with the record-count
+//    / column-offset operators (Section 3.2) resolves every tile's record
+//    index, column and last terminator; the tile's value bytes per string
+//    column then follow from its column, and a second scan turns them into
+//    chars offsets.  Blocks chain by a single-pass decoupled look-back.
+// 3. Main pass (main_kernel).  With its context known, each tile loads its
+//    chunks' tags and prefixes (or, without them, tags again and scans the
+//    block), enters every closed field in a column-major (column, record)
+//    slot table, compacts string value bytes per column into shared memory
+//    (stream compaction in place of ParPaRaw's radix partitioning, Section
+//    3.3) and writes them as 16-byte stores; one lane per field then writes
+//    the Arrow offset or converts the number (Section 3.3), 32 consecutive
+//    rows of a column to a warp for coalesced stores.
 #include <cstdint>
 #include <cuda_runtime.h>
 #include <algorithm>
