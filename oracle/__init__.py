@@ -31,8 +31,8 @@ E_CAPACITY = 32
 FATAL = E_INVALID_INPUT | E_BAD_END_STATE | E_CAPACITY
 
 TAG_DATA, TAG_FD, TAG_RD, TAG_CTRL, TAG_INVALID, TAG_BEGIN = range(6)
-COL_CODES = {"str": 0, "i8": 1, "i32": 2, "i64": 3, "f64": 4, "skip": 5}
-NUMPY_OF = {"i8": np.int8, "i32": np.int32, "i64": np.int64, "f64": np.float64}
+COL_CODES = {"str": 0, "i8": 1, "i32": 2, "i64": 3, "f64": 4, "skip": 5, "ts": 6}
+NUMPY_OF = {"i8": np.int8, "i32": np.int32, "i64": np.int64, "f64": np.float64, "ts": np.int64}
 KIND_CSV, KIND_LEX = 0, 1
 U64MAX = (1 << 64) - 1
 

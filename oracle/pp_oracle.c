@@ -48,7 +48,7 @@
 #define E_CAPACITY 32
 
 enum { T_DATA = 0, T_FD = 1, T_RD = 2, T_CTRL = 3, T_INVALID = 4, T_BEGIN = 5 };
-enum { C_STR = 0, C_I8 = 1, C_I32 = 2, C_I64 = 3, C_F64 = 4, C_SKIP = 5 };
+enum { C_STR = 0, C_I8 = 1, C_I32 = 2, C_I64 = 3, C_F64 = 4, C_SKIP = 5, C_TS = 6 };
 
 typedef struct {
   int32_t error;
@@ -283,6 +283,46 @@ static int conv_f64(const uint8_t* v, size_t n, double* out) {
   return 0;
 }
 
+/* Temporal fields (ParPaRaw Section 3.3, field values of "numerical or
+ * temporal types"; the pages fix no format).  Reading: YYYY-MM-DD or
+ * YYYY-MM-DD HH:MM:SS, four- and two-digit fields, month 01-12, day within
+ * the month of the proleptic Gregorian calendar, hour 00-23, minute and
+ * second 00-59; the value is the signed count of seconds since 1970-01-01
+ * 00:00:00 (no time zone).  "" -> 0; anything else E_NUM_SYNTAX and 0.
+ * The days are counted one year and one month at a time, the plain way. */
+static int is_leap(int y) { return (y % 4 == 0 && y % 100 != 0) || y % 400 == 0; }
+static int month_days(int y, int m) {
+  static const int d[12] = {31, 28, 31, 30, 31, 30, 31, 31, 30, 31, 30, 31};
+  return m == 2 && is_leap(y) ? 29 : d[m - 1];
+}
+static int two(const uint8_t* v, size_t i, int* out) {
+  if (v[i] < '0' || v[i] > '9' || v[i + 1] < '0' || v[i + 1] > '9') return 0;
+  *out = (v[i] - '0') * 10 + (v[i + 1] - '0');
+  return 1;
+}
+static int conv_ts(const uint8_t* v, size_t n, int64_t* out) {
+  *out = 0;
+  if (n == 0) return 0;
+  if (n != 10 && n != 19) return E_NUM_SYNTAX;
+  int yh, yl, mo, d, h = 0, mi = 0, sec = 0;
+  if (!two(v, 0, &yh) || !two(v, 2, &yl) || v[4] != '-' || !two(v, 5, &mo) || v[7] != '-' ||
+      !two(v, 8, &d))
+    return E_NUM_SYNTAX;
+  if (n == 19 && (v[10] != ' ' || !two(v, 11, &h) || v[13] != ':' || !two(v, 14, &mi) ||
+                  v[16] != ':' || !two(v, 17, &sec)))
+    return E_NUM_SYNTAX;
+  const int y = yh * 100 + yl;
+  if (mo < 1 || mo > 12 || d < 1 || d > month_days(y, mo) || h > 23 || mi > 59 || sec > 59)
+    return E_NUM_SYNTAX;
+  int64_t days = 0;
+  for (int k = 1970; k < y; k++) days += is_leap(k) ? 366 : 365;
+  for (int k = y; k < 1970; k++) days -= is_leap(k) ? 366 : 365;
+  for (int k = 1; k < mo; k++) days += month_days(y, k);
+  days += d - 1;
+  *out = days * 86400 + (int64_t)h * 3600 + mi * 60 + sec;
+  return 0;
+}
+
 /* ------------------------------------------------------------ CSV parse */
 typedef struct {
   /* outputs */
@@ -330,6 +370,10 @@ static void close_field(csv_out* o, uint64_t rec, int col, uint64_t field_start)
     double d;
     rc = conv_f64(o->val, o->val_len, &d);
     ((double*)o->typed[col])[rec] = d;
+  } else if (t == C_TS) {
+    int64_t x;
+    rc = conv_ts(o->val, o->val_len, &x);
+    ((int64_t*)o->typed[col])[rec] = x;
   } else {
     int64_t lo = t == C_I8 ? -128 : t == C_I32 ? INT32_MIN : INT64_MIN;
     int64_t hi = t == C_I8 ? 127 : t == C_I32 ? INT32_MAX : INT64_MAX;

@@ -367,3 +367,56 @@ def test_edge_inputs():
     assert st["error"] == 0 and bytes(cols[0][1]) == b"a"
     cols, st = O.csv_parse(b'"a"x\n', ["str"])       # other after closing quote
     assert st["error"] == O.E_INVALID_INPUT and st["first_error_offset"] == 3
+
+
+# ------------------------------------------------------------ timestamps
+# Python's calendar.timegm (proleptic Gregorian, seconds since 1970-01-01
+# 00:00:00) is an independent implementation of the same day count.
+def _timegm(y, mo, d, h=0, mi=0, s=0):
+    import calendar
+    return calendar.timegm((y, mo, d, h, mi, s, 0, 0, 0))
+
+
+TS_OK = [
+    (b"1970-01-01 00:00:00", 0), (b"1970-01-01", 0), (b"1969-12-31 23:59:59", -1),
+    (b"2000-02-29 12:34:56", _timegm(2000, 2, 29, 12, 34, 56)),
+    (b"2024-02-29", _timegm(2024, 2, 29)), (b"2021-03-01 00:00:01", _timegm(2021, 3, 1, 0, 0, 1)),
+    (b"0001-01-01 00:00:00", _timegm(1, 1, 1)), (b"9999-12-31 23:59:59", _timegm(9999, 12, 31, 23, 59, 59)),
+    (b"1600-02-29", _timegm(1600, 2, 29)),
+    # year 0 (a leap year of the proleptic calendar) is 719528 days before 1970
+    (b"0000-01-01 00:00:00", -719528 * 86400), (b"0000-02-29", -719528 * 86400 + 59 * 86400),
+    (b'"2020-07-04 01:02:03"', _timegm(2020, 7, 4, 1, 2, 3)), (b"", 0),
+]
+TS_BAD = [b"1900-02-29", b"2023-02-29", b"2021-04-31", b"2021-13-01", b"2021-00-10",
+          b"2021-01-00", b"2021-01-01 24:00:00", b"2021-01-01 23:60:00", b"2021-01-01 23:59:60",
+          b"2021-1-01", b"2021/01/01", b"2021-01-01T00:00:00", b"2021-01-01 00:00", b" 2021-01-01",
+          b"2021-01-01 ", b"-021-01-01", b"2021-01-01 00:00:0x", b"20210101"]
+
+
+@pytest.mark.parametrize("text,val", TS_OK)
+def test_timestamp_conversion_matches_timegm(text, val):
+    cols, st = O.csv_parse(text + b"\n", ["ts"])
+    assert st["error"] == 0
+    assert int(cols[0][0]) == val
+
+
+@pytest.mark.parametrize("text", TS_BAD)
+def test_timestamp_syntax_errors(text):
+    cols, st = O.csv_parse(b"7," + text + b"\n", ["i32", "ts"])
+    assert st["error"] == O.E_NUM_SYNTAX and st["first_error_offset"] == 2
+    assert int(cols[1][0]) == 0
+
+
+def test_timestamps_random_days_match_timegm():
+    import random
+    rng = random.Random(7)
+    lines, want = [], []
+    for _ in range(3000):
+        y, mo = rng.randint(1, 9999), rng.randint(1, 12)
+        d = rng.randint(1, 28 if mo == 2 else 30)
+        h, mi, s = rng.randint(0, 23), rng.randint(0, 59), rng.randint(0, 59)
+        lines.append(b"%04d-%02d-%02d %02d:%02d:%02d" % (y, mo, d, h, mi, s))
+        want.append(_timegm(y, mo, d, h, mi, s))
+    cols, st = O.csv_parse(b"\n".join(lines) + b"\n", ["ts"])
+    assert st["error"] == 0
+    assert cols[0].tolist() == want
