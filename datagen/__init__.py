@@ -17,6 +17,8 @@ stays within the target, so CSV inputs end with '\\n'):
                    'YYYY-MM-DD HH:MM:SS', 10 int32 in 0..9, 6 float64 %.2f
   json_2gib        2 GiB JSON-like token stream (objects/arrays, strings
                    with backslash escapes, ints, floats, whitespace runs)
+  csv18ts_2gib     the csv18_2gib bytes with the two timestamp columns
+                   typed as timestamps (int64 seconds) instead of strings
 
 Seeds are 0x5EED0000 + the workload number (1..5); random numbers come from
 splitmix64.
@@ -44,6 +46,9 @@ WORKLOADS = {
     "csv18_2gib": dict(index=4, target=2 << 30, kind="csv",
                        cols=["str", "str"] + ["i32", "f64"] * 6 + ["i32"] * 4),
     "json_2gib": dict(index=5, target=2 << 30, kind="tokens", cols=None),
+    # the 2 GiB numeric input with its timestamps converted to int64 seconds
+    "csv18ts_2gib": dict(index=4, target=2 << 30, kind="csv",
+                         cols=["ts", "ts"] + ["i32", "f64"] * 6 + ["i32"] * 4),
 }
 TOKEN_KINDS = ["{", "}", "[", "]", ",", ":", "string", "int", "float", "ws"]
 

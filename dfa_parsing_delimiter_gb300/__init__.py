@@ -25,8 +25,9 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libpp.so")
 
 PP_OK, PP_EINVAL, PP_ECUDA, PP_ENOMEM, PP_ETOOLARGE, PP_ECHUNK = 0, 1, 2, 3, 4, 5
-COL = {"str": 0, "i8": 1, "i32": 2, "i64": 3, "f64": 4, "skip": 5}
-DTYPE = {"i8": torch.int8, "i32": torch.int32, "i64": torch.int64, "f64": torch.float64}
+COL = {"str": 0, "i8": 1, "i32": 2, "i64": 3, "f64": 4, "skip": 5, "ts": 6}
+DTYPE = {"i8": torch.int8, "i32": torch.int32, "i64": torch.int64, "f64": torch.float64,
+         "ts": torch.int64}
 ERR_INVALID_INPUT, ERR_BAD_END_STATE, ERR_COLCOUNT = 1, 2, 4
 ERR_NUM_SYNTAX, ERR_NUM_OVERFLOW, ERR_CAPACITY, ERR_LOOKBACK_TIMEOUT = 8, 16, 32, 64
 ERR_FATAL = ERR_INVALID_INPUT | ERR_BAD_END_STATE | ERR_CAPACITY | ERR_LOOKBACK_TIMEOUT

@@ -173,7 +173,7 @@ pp_rc parse_prepare(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa,
   bool any_out = false;
   for (int c = 0; c < n_cols; ++c) {
     const int ty = col_types[c];
-    if (ty < PP_COL_STRING || ty > PP_COL_SKIP) return PP_EINVAL;
+    if (ty < PP_COL_STRING || ty > PP_COL_TIMESTAMP) return PP_EINVAL;
     p.coltype[c] = uint8_t(ty);
     p.stridx[c] = -1;
     if (ty == PP_COL_STRING) {

@@ -315,4 +315,78 @@ struct IntAcc {
   }
 };
 
+// ------------------------------------------------------------ timestamps
+// Temporal fields (ParPaRaw Section 3.3, "numerical or temporal types"):
+// YYYY-MM-DD or YYYY-MM-DD HH:MM:SS (n = 10 or 19 characters) as int64
+// seconds since 1970-01-01 00:00:00, proleptic Gregorian calendar, no time
+// zone; month 01-12, day within the month, hour 00-23, minute and second
+// 00-59.  The characters come as five little-endian words x[0..4] (byte i
+// of the field in byte i % 4 of x[i / 4]; bytes past n are ignored).
+
+// Days from 1970-01-01 to y-m-d, by the closed form of H. Hinnant's
+// "chrono-Compatible Low-Level Date Algorithms" (days_from_civil): counting
+// years from March makes the leap day the last day of a year, so the day of
+// that year is (153 * month + 2) / 5 + day - 1 with March as month 0, and a
+// 400-year era holds 146097 days; 719468 is the day of 1970-01-01 counted
+// from 0000-03-01.
+PP_FN int64_t days_from_civil(int y, int m, int d) {
+  y -= m <= 2 ? 1 : 0;
+  const int era = (y >= 0 ? y : y - 399) / 400;
+  const int yoe = y - era * 400;                          // year of the era, 0..399
+  const int doy = (153 * (m > 2 ? m - 3 : m + 9) + 2) / 5 + d - 1;
+  const int doe = yoe * 365 + yoe / 4 - yoe / 100 + doy;  // day of the era
+  return int64_t(era) * 146097 + doe - 719468;
+}
+
+// digit pair at bytes i, i+1 of y (a field word xor '0' in every byte)
+PP_FN int digit_pair(uint32_t y, int i) {
+  return int((y >> (8 * i)) & 0xFFu) * 10 + int((y >> (8 * i + 8)) & 0xFFu);
+}
+
+PP_FN int parse_timestamp(const uint32_t (&x)[5], uint32_t n, int64_t* out) {
+  *out = 0;
+  if (n == 0) return 0;
+  if (n != 10 && n != 19) return PP_ERR_NUM_SYNTAX;
+  const uint32_t Z = 0x30303030u;
+  const uint32_t y0 = x[0] ^ Z, y1 = x[1] ^ Z, y2 = x[2] ^ Z, y3 = x[3] ^ Z, y4 = x[4] ^ Z;
+  // digits where the grammar puts them, separators in between
+  uint32_t bad = nondigit_bytes(y0) | (nondigit_bytes(y1) & 0x00808000u);
+  bool sep = (x[1] & 0xFF0000FFu) == 0x2D00002Du;  // '-' . . '-'
+  if (n == 19) {
+    bad |= (nondigit_bytes(y2) & 0x80008080u) | (nondigit_bytes(y3) & 0x80800080u) |
+            (nondigit_bytes(y4) & 0x00808000u);
+    sep = sep && (x[2] & 0x00FF0000u) == 0x00200000u && (x[3] & 0x0000FF00u) == 0x00003A00u &&
+          (x[4] & 0xFFu) == 0x3Au;  // ' ', ':', ':'
+  } else {
+    bad |= nondigit_bytes(y2) & 0x00008080u;
+  }
+  if (bad || !sep) return PP_ERR_NUM_SYNTAX;
+  const int yr = int(val4(y0)), mo = digit_pair(y1, 1), d = digit_pair(y2, 0);
+  int h = 0, mi = 0, sc = 0;
+  if (n == 19) {
+    h = int((y2 >> 24) & 0xFFu) * 10 + int(y3 & 0xFFu);
+    mi = digit_pair(y3, 2);
+    sc = digit_pair(y4, 1);
+  }
+  const bool leap = (yr % 4 == 0 && yr % 100 != 0) || yr % 400 == 0;
+  // days in month m: 30 + (m + m / 8) % 2 for m != 2
+  const int dim = mo == 2 ? (leap ? 29 : 28) : 30 + ((mo + mo / 8) & 1);
+  if (mo < 1 || mo > 12 || d < 1 || d > dim || h > 23 || mi > 59 || sc > 59)
+    return PP_ERR_NUM_SYNTAX;
+  *out = days_from_civil(yr, mo, d) * 86400 + int64_t(h * 3600 + mi * 60 + sc);
+  return 0;
+}
+
+// The same over a field fed byte by byte (fields that are not plain bytes
+// of the current tile).
+struct TsAcc {
+  uint32_t x[5] = {0u, 0u, 0u, 0u, 0u};
+  uint32_t n = 0;
+  PP_MFN void feed(uint32_t c) {
+    if (n < 20) x[n >> 2] |= (c & 0xFFu) << (8 * (n & 3));
+    ++n;
+  }
+  PP_MFN int finish(int64_t* out) const { return parse_timestamp(x, n, out); }
+};
+
 }  // namespace ppn

@@ -1100,6 +1100,12 @@ __device__ __forceinline__ int convert_general(const ParseParams& P, uint32_t ty
     ppn::FloatAcc acc;
     const uint32_t nd = feed_field(acc, P.in, fs, fe, tile_base, tile_s, ctrl_s, my_lut, fstate);
     if (nd) err = acc.finish(&val);
+  } else if (ty == PP_COL_TIMESTAMP) {
+    ppn::TsAcc acc;
+    feed_field(acc, P.in, fs, fe, tile_base, tile_s, ctrl_s, my_lut, fstate);
+    int64_t x = 0;
+    err = acc.finish(&x);
+    val = uint64_t(x);
   } else {
     ppn::IntAcc acc;
     const uint32_t nd = feed_field(acc, P.in, fs, fe, tile_base, tile_s, ctrl_s, my_lut, fstate);
@@ -1132,8 +1138,9 @@ struct NumCtx {
 // missing field) for a column of type TY.  A plain field inside the tile
 // and free of control bytes is decoded word-parallel: at most 8 characters
 // after the sign (an integer, or for floats a decimal with one '.'
-// converted by short_decimal_to_binary64), or an integer of 9 to 16 digits
-// in two such words.  Everything else streams through the accumulators.
+// converted by short_decimal_to_binary64), an integer of 9 to 16 digits
+// in two such words, or a timestamp from five words.  Everything else
+// streams through the accumulators.
 // Returns the error bits; val gets the value's bits (0 for an empty field
 // or an error).
 template <int TY>
@@ -1146,6 +1153,16 @@ __device__ __forceinline__ int convert_field(const ParseParams& P, uint32_t v, c
       (!X.any_ctrl || ctrl_before(X.ctrl_s, X.cpre, fe) == ctrl_before(X.ctrl_s, X.cpre, fsr))) {
     const uint32_t L = fe - fsr;
     if (L == 0) return 0;  // empty field: the column default
+    if (TY == PP_COL_TIMESTAMP) {  // five words of the tile from the field start
+      const uint32_t q = fsr >> 2, sh = (fsr & 3u) * 8u;
+      uint32_t x[5];
+#pragma unroll
+      for (int k = 0; k < 5; ++k) x[k] = __funnelshift_r(X.tile_w[q + k], X.tile_w[q + k + 1], sh);
+      int64_t t = 0;
+      const int err = ppn::parse_timestamp(x, L, &t);
+      val = uint64_t(t);
+      return err;
+    }
     const uint32_t c0 = X.tile_s[fsr];
     const uint32_t sg = (c0 == '-' || c0 == '+') ? 1u : 0u;
     const bool neg = c0 == '-';
@@ -1204,7 +1221,7 @@ __device__ __forceinline__ void convert_store(const ParseParams& P, const NumCtx
   uint64_t val;
   const int err = convert_field<TY>(P, v, X, val);
   if (TY == PP_COL_FLOAT64) static_cast<uint64_t*>(out)[rec] = val;
-  else if (TY == PP_COL_INT64) static_cast<int64_t*>(out)[rec] = int64_t(val);
+  else if (TY == PP_COL_INT64 || TY == PP_COL_TIMESTAMP) static_cast<int64_t*>(out)[rec] = int64_t(val);
   else if (TY == PP_COL_INT32) static_cast<int32_t*>(out)[rec] = int32_t(val);
   else static_cast<int8_t*>(out)[rec] = int8_t(val);
   if (err) {
@@ -1677,6 +1694,7 @@ __global__ void __launch_bounds__(NT, 2) main_kernel(const __grid_constant__ Par
             switch (S.coltype[c]) {
               case PP_COL_FLOAT64: convert_store<PP_COL_FLOAT64>(P, X, out, rec, v); break;
               case PP_COL_INT64: convert_store<PP_COL_INT64>(P, X, out, rec, v); break;
+              case PP_COL_TIMESTAMP: convert_store<PP_COL_TIMESTAMP>(P, X, out, rec, v); break;
               case PP_COL_INT32: convert_store<PP_COL_INT32>(P, X, out, rec, v); break;
               default: convert_store<PP_COL_INT8>(P, X, out, rec, v); break;
             }

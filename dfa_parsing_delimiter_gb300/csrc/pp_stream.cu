@@ -186,7 +186,7 @@ size_t width_of(int ty) {
   switch (ty) {
     case PP_COL_INT8: return 1;
     case PP_COL_INT32: return 4;
-    case PP_COL_INT64: case PP_COL_FLOAT64: return 8;
+    case PP_COL_INT64: case PP_COL_FLOAT64: case PP_COL_TIMESTAMP: return 8;
     default: return 0;
   }
 }

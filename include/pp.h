@@ -62,7 +62,14 @@ typedef enum {
   PP_COL_INT64 = 3,  /* int64[R]                                        */
   PP_COL_FLOAT64 = 4,/* double[R], decimal grammar, within 1 ulp of the
                         correctly rounded value                          */
-  PP_COL_SKIP = 5    /* parsed for structure, not emitted               */
+  PP_COL_SKIP = 5,   /* parsed for structure, not emitted               */
+  PP_COL_TIMESTAMP = 6 /* int64[R]: a temporal field (ParPaRaw Section 3.3,
+                        "numerical or temporal types") as seconds since
+                        1970-01-01 00:00:00, proleptic Gregorian calendar,
+                        no time zone.  Grammar YYYY-MM-DD or
+                        YYYY-MM-DD HH:MM:SS with month 01-12, day within
+                        the month, hour 00-23, minute and second 00-59;
+                        anything else is PP_ERR_NUM_SYNTAX with value 0  */
 } pp_coltype;
 
 /* per-byte tags (ParPaRaw Section 3.1: record delimiter, field delimiter,
@@ -137,7 +144,8 @@ typedef struct {
  *                   columns, else ignored (may be NULL).
  *   out_chars[c]    device uint8[chars_capacity[c]] for string columns.
  *   out_typed[c]    device array of records_capacity elements of the
- *                   column's type for numeric columns.
+ *                   column's type for numeric and timestamp columns (int64
+ *                   for PP_COL_TIMESTAMP).
  *   chars_capacity  host array of n_cols sizes (string columns only).
  *   d_status        device pp_status.
  * Passing NULL for every out_offsets/out_chars/out_typed pointer is allowed

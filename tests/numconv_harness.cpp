@@ -29,3 +29,18 @@ int h_short_decimal(const unsigned char* s, int n, int dot, uint32_t* w, int* k)
   return ppn::short_decimal(x0, x1, n, dot != 0, w, k) ? 1 : 0;
 }
 }
+
+extern "C" {
+// `buf` holds n fields, each terminated by one 0x00 byte, as timestamps:
+// out[i] = seconds since 1970, err[i] = 0 / PP_ERR_NUM_SYNTAX.
+void h_parse_timestamps(const unsigned char* buf, size_t n, int64_t* out, int* err) {
+  size_t p = 0;
+  for (size_t i = 0; i < n; ++i) {
+    ppn::TsAcc a;
+    while (buf[p]) a.feed(buf[p++]);
+    ++p;
+    err[i] = a.finish(&out[i]);
+  }
+}
+int64_t h_days_from_civil(int y, int m, int d) { return ppn::days_from_civil(y, m, d); }
+}

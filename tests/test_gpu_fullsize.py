@@ -60,7 +60,8 @@ def _to_device(data):
     return d_in
 
 
-@pytest.mark.parametrize("name", ["csv4_1mib", "csv16_256mib", "csv3_1gib", "csv18_2gib"])
+@pytest.mark.parametrize("name", ["csv4_1mib", "csv16_256mib", "csv3_1gib", "csv18_2gib",
+                                  "csv18ts_2gib"])
 def test_parse_full_size(name):
     w = datagen.WORKLOADS[name]
     cols = w["cols"]

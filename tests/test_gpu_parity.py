@@ -320,3 +320,37 @@ def test_tokenize_capacity():
     assert s["error"] & pp.ERR_CAPACITY and s["n_tokens"] == info["n_tokens"]
     (rids, rstarts, rlens), _ = O.tokenize(data)
     assert np.array_equal(starts.cpu().numpy().astype(np.uint64), rstarts[:cap])
+
+
+# ------------------------------------------------------------ timestamps
+def test_parse_timestamps_generated():
+    """The 2 GiB numeric workload's layout with its timestamp columns typed."""
+    cols = datagen.WORKLOADS["csv18ts_2gib"]["cols"]
+    for target in (2 << 20, 3 * TILE + 7):
+        data, info, _ = datagen.generate("csv18ts_2gib", target=target)
+        st = compare_csv(data, cols)
+        assert st["error"] == 0 and st["n_records"] == info["n_records"]
+
+
+def test_parse_timestamp_edge_cases():
+    good = [b"1970-01-01 00:00:00", b"1969-12-31 23:59:59", b"2000-02-29", b"0000-01-01",
+            b"9999-12-31 23:59:59", b'"2020-07-04 01:02:03"', b'"2021-""01-02"', b""]
+    bad = [b"1900-02-29", b"2021-04-31", b"2021-01-01 24:00:00", b"2021-1-01",
+           b"2021-01-01T00:00:00", b"2021-01-01 00:00", b"20210101", b'"2021-01-01 "']
+    rows = [b"%d,%s\n" % (i, t) for i, t in enumerate(good + bad)]
+    compare_csv(b"".join(rows), ["i32", "ts"])
+    compare_csv(b"".join(rows[: len(good)]), ["i32", "ts"])
+
+
+@pytest.mark.parametrize("shift", range(-21, 4, 3))
+def test_parse_timestamp_across_tile_boundary(shift):
+    """A timestamp field starting at every position around the first tile
+    edge, plain and quoted: a field that began in an earlier tile is re-read
+    from global memory by the tile that closes it."""
+    for ts in (b"2024-02-29 13:14:15", b'"2024-02-29 13:14:15"', b"1999-12-31"):
+        first = b"0,0000-01-01\n"
+        filler = b"x" * (TILE + shift - len(first) - 1)  # the timestamp starts at TILE + shift
+        rest = b"".join(b"%d,%s\n" % (i, ts) for i in range(50))
+        data = first + filler + b"," + ts + b"\n" + rest
+        assert data.index(ts, len(first)) == TILE + shift
+        compare_csv(data, ["str", "ts"])

@@ -238,3 +238,71 @@ def test_short_decimal_random(harness, seed):
         s = bytes(s)
         for dot in (0, 1):
             assert _short_decimal(harness, s, n, dot) == _short_decimal_want(s, n, dot), (s, n, dot)
+
+
+# ------------------------------------------------------------ timestamps
+def _ts(L, strs):
+    L.h_parse_timestamps.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
+                                     ctypes.c_void_p]
+    buf = b"".join(s + b"\x00" for s in strs)
+    a = np.frombuffer(buf, dtype=np.uint8)
+    out = np.zeros(len(strs), dtype=np.int64)
+    err = np.zeros(len(strs), dtype=np.int32)
+    L.h_parse_timestamps(a.ctypes.data, len(strs), out.ctypes.data, err.ctypes.data)
+    return out, err
+
+
+def test_days_from_civil_every_day_against_ordinal(harness):
+    """The closed-form day count against Python's date ordinals, every day of
+    years 1..9999 sampled every 7 days plus all days of leap-rule years."""
+    import datetime
+    L = harness
+    L.h_days_from_civil.restype = ctypes.c_int64
+    L.h_days_from_civil.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int]
+    epoch = datetime.date(1970, 1, 1).toordinal()
+    o = datetime.date(1, 1, 1).toordinal()
+    end = datetime.date(9999, 12, 31).toordinal()
+    days = list(range(o, end + 1, 7))
+    for y in (1, 4, 100, 400, 1600, 1700, 1900, 1969, 1970, 2000, 2024, 2100, 9999):
+        d0 = datetime.date(y, 1, 1).toordinal()
+        days += range(d0, d0 + 365 + (1 if (y % 4 == 0 and y % 100) or y % 400 == 0 else 0))
+    for k in days:
+        dt = datetime.date.fromordinal(k)
+        assert L.h_days_from_civil(dt.year, dt.month, dt.day) == k - epoch, dt
+    # year 0 of the proleptic calendar: 719528 days before 1970
+    assert L.h_days_from_civil(0, 1, 1) == -719528
+    assert L.h_days_from_civil(0, 3, 1) == -719468
+
+
+def test_timestamp_words_match_timegm_and_reject_bad_fields(harness):
+    import calendar
+    import random
+    rng = random.Random(11)
+    strs, want = [], []
+    for _ in range(5000):
+        y, mo = rng.randint(0, 9999), rng.randint(1, 12)
+        leap = (y % 4 == 0 and y % 100 != 0) or y % 400 == 0
+        dim = [31, 29 if leap else 28, 31, 30, 31, 30, 31, 31, 30, 31, 30, 31][mo - 1]
+        d, h, mi, s = rng.randint(1, dim), rng.randint(0, 23), rng.randint(0, 59), rng.randint(0, 59)
+        if rng.random() < 0.5:
+            strs.append(b"%04d-%02d-%02d %02d:%02d:%02d" % (y, mo, d, h, mi, s))
+        else:
+            strs.append(b"%04d-%02d-%02d" % (y, mo, d))
+            h = mi = s = 0
+        days = (calendar.timegm((max(y, 1), mo, d, 0, 0, 0, 0, 0, 0)) // 86400 if y else
+                -719528 + sum([31, 29, 31, 30, 31, 30, 31, 31, 30, 31, 30, 31][:mo - 1]) + d - 1)
+        want.append(days * 86400 + h * 3600 + mi * 60 + s)
+    bad = [b"1900-02-29", b"2023-02-29", b"2021-04-31", b"2021-13-01", b"2021-00-10",
+           b"2021-01-00", b"2021-01-01 24:00:00", b"2021-01-01 23:60:00",
+           b"2021-01-01 23:59:60", b"2021-1-01", b"2021/01/01", b"2021-01-01T00:00:00",
+           b"2021-01-01 00:00", b"2021-01-01 ", b"2021-01-01 00:00:0x", b"20210101",
+           b"2021-01-01 00:00:00 ", b"2021-01-0\x80", b"\xb021-01-01"]
+    out, err = _ts(harness, strs + bad + [b""])
+    assert err[:len(strs)].tolist() == [0] * len(strs)
+    assert out[:len(strs)].tolist() == want
+    assert err[len(strs):-1].tolist() == [PP_SYNTAX] * len(bad)
+    assert out[len(strs):].tolist() == [0] * (len(bad) + 1)
+    assert err[-1] == 0
+
+
+PP_SYNTAX = 8
