@@ -33,7 +33,7 @@ FATAL = E_INVALID_INPUT | E_BAD_END_STATE | E_CAPACITY
 TAG_DATA, TAG_FD, TAG_RD, TAG_CTRL, TAG_INVALID, TAG_BEGIN = range(6)
 COL_CODES = {"str": 0, "i8": 1, "i32": 2, "i64": 3, "f64": 4, "skip": 5, "ts": 6}
 NUMPY_OF = {"i8": np.int8, "i32": np.int32, "i64": np.int64, "f64": np.float64, "ts": np.int64}
-KIND_CSV, KIND_LEX = 0, 1
+KIND_CSV, KIND_LEX, KIND_CSV_CRLF = 0, 1, 2
 U64MAX = (1 << 64) - 1
 
 
@@ -65,8 +65,8 @@ def _load():
     if _lib is None:
         build()
         L = ctypes.CDLL(_SO)
-        L.or_csv_parse.argtypes = [_vp, _u64, _u8, _u8, _u8, ctypes.c_int, _vp, _vp, _vp,
-                                   _vp, _u64, _vp, ctypes.POINTER(Status)]
+        L.or_csv_parse.argtypes = [_vp, _u64, _u8, _u8, _u8, ctypes.c_int, ctypes.c_int, _vp,
+                                   _vp, _vp, _vp, _u64, _vp, ctypes.POINTER(Status)]
         L.or_tokenize.argtypes = [_vp, _u64, _vp, _vp, _vp, _u64, ctypes.POINTER(Status)]
         L.or_tags.argtypes = [ctypes.c_int, _u8, _u8, _u8, _vp, _u64, _vp, _vp]
         L.or_tags.restype = ctypes.c_int
@@ -87,8 +87,9 @@ def _arr(x) -> np.ndarray:
 
 
 def csv_parse(data, col_types, fd=b",", rd=b"\n", quote=b'"', records_capacity=None,
-              chars_capacity=None):
-    """Sequentially parse quoted CSV.
+              chars_capacity=None, crlf=False):
+    """Sequentially parse quoted CSV (crlf: carriage returns outside quotes
+    are dropped, so CRLF line ends work with rd = LF).
 
     Returns (columns, status): columns[c] is (offsets int32[R+1], chars uint8)
     for string columns, a numpy array of R values for numeric ones, None for
@@ -121,7 +122,8 @@ def csv_parse(data, col_types, fd=b",", rd=b"\n", quote=b'"', records_capacity=N
     codes = np.array([COL_CODES[t] for t in col_types] or [0], dtype=np.int32)
     ccap = np.array(list(chars_capacity) or [0], dtype=np.uint64)
     st = Status()
-    L.or_csv_parse(a.ctypes.data, n, fd[0], rd[0], quote[0], ncols, codes.ctypes.data,
+    L.or_csv_parse(a.ctypes.data, n, fd[0], rd[0], quote[0], int(bool(crlf)), ncols,
+                   codes.ctypes.data,
                    ctypes.addressof(ptr_off), ctypes.addressof(ptr_chr),
                    ctypes.addressof(ptr_typ), records_capacity, ccap.ctypes.data,
                    ctypes.byref(st))
@@ -165,7 +167,7 @@ def tags(data, kind=KIND_CSV, fd=b",", rd=b"\n", quote=b'"'):
 
 
 def nstates(kind):
-    return 5 if kind == KIND_CSV else 16
+    return 16 if kind == KIND_LEX else 5
 
 
 def stv(chunk, kind=KIND_CSV, fd=b",", rd=b"\n", quote=b'"'):

@@ -67,7 +67,8 @@ static void flag(or_status* st, int bit, uint64_t off, int with_offset) {
 /* ------------------------------------------------------------ CSV DFA */
 enum { EOR = 0, FLD = 1, ENC = 2, ESC = 3, INV = 4 };
 
-typedef struct { uint8_t fd, rd, q; } csv_syms;
+/* cr: a carriage return byte dropped outside quotes (CRLF line ends), or -1 */
+typedef struct { uint8_t fd, rd, q; int cr; } csv_syms;
 
 /* One transition of the quoted-CSV DFA.  Returns the next state and writes
  * the symbol's tag.  Cells (state, symbol) -> (next, tag):
@@ -76,19 +77,26 @@ typedef struct { uint8_t fd, rd, q; } csv_syms;
  *   ENC: quote -> ESC ctrl | anything else -> ENC data
  *   ESC: quote -> ENC data (second quote of a doubled pair)
  *        fd -> EOR fd | rd -> EOR rd | other -> INV
- *   INV: everything -> INV                                               */
+ *   INV: everything -> INV
+ * With a carriage return byte (CRLF line ends: the pages name no line-end
+ * convention, and ParPaRaw Section 4 notes that simulating the DFA allows
+ * more expressive parsing rules), a CR outside quotes is a control symbol,
+ * dropped from the value, that leaves the field open:
+ *   EOR, FLD, ESC: cr -> FLD ctrl     ENC: cr -> ENC data                */
 static int csv_step(const csv_syms* y, int s, uint8_t b, int* tag) {
-  int is_q = b == y->q, is_fd = b == y->fd, is_rd = b == y->rd;
+  int is_q = b == y->q, is_fd = b == y->fd, is_rd = b == y->rd, is_cr = (int)b == y->cr;
   switch (s) {
     case EOR:
       if (is_q) { *tag = T_CTRL; return ENC; }
       if (is_fd) { *tag = T_FD; return EOR; }
       if (is_rd) { *tag = T_RD; return EOR; }
+      if (is_cr) { *tag = T_CTRL; return FLD; }
       *tag = T_DATA; return FLD;
     case FLD:
       if (is_q) { *tag = T_INVALID; return INV; }
       if (is_fd) { *tag = T_FD; return EOR; }
       if (is_rd) { *tag = T_RD; return EOR; }
+      if (is_cr) { *tag = T_CTRL; return FLD; }
       *tag = T_DATA; return FLD;
     case ENC:
       if (is_q) { *tag = T_CTRL; return ESC; }
@@ -97,6 +105,7 @@ static int csv_step(const csv_syms* y, int s, uint8_t b, int* tag) {
       if (is_q) { *tag = T_DATA; return ENC; }
       if (is_fd) { *tag = T_FD; return EOR; }
       if (is_rd) { *tag = T_RD; return EOR; }
+      if (is_cr) { *tag = T_CTRL; return FLD; }
       *tag = T_INVALID; return INV;
     default:
       *tag = T_INVALID; return INV;
@@ -205,20 +214,26 @@ static int lex_token_id(int s, uint8_t first_byte) {
 }
 
 /* ------------------------------------------------- generic step by kind */
-/* kind 0 = quoted CSV (syms from y), kind 1 = JSON-like lexer             */
+/* kind 0 = quoted CSV (syms from y), kind 1 = JSON-like lexer, kind 2 =
+ * quoted CSV with CRLF line ends (CR dropped outside quotes)               */
+static int is_csv(int kind) { return kind == 0 || kind == 2; }
+static csv_syms syms_of(int kind, uint8_t fd, uint8_t rd, uint8_t q) {
+  csv_syms y = {fd, rd, q, kind == 2 ? '\r' : -1};
+  return y;
+}
 static int step_any(int kind, const csv_syms* y, int s, uint8_t b, int* tag) {
-  if (kind == 0) return csv_step(y, s, b, tag);
+  if (is_csv(kind)) return csv_step(y, s, b, tag);
   int begin, n = lex_step(s, b, &begin);
   *tag = n == L_INV ? T_INVALID : begin ? T_BEGIN : T_DATA;
   return n;
 }
-static int nstates(int kind) { return kind == 0 ? 5 : 16; }
+static int nstates(int kind) { return is_csv(kind) ? 5 : 16; }
 
 /* Per-byte state before and tag (the test hook's definition). */
 int or_tags(int kind, uint8_t fd, uint8_t rd, uint8_t q, const uint8_t* in, uint64_t n,
             uint8_t* state_before, uint8_t* tag) {
-  csv_syms y = {fd, rd, q};
-  int s = kind == 0 ? EOR : L_START;
+  csv_syms y = syms_of(kind, fd, rd, q);
+  int s = is_csv(kind) ? EOR : L_START;
   for (uint64_t i = 0; i < n; i++) {
     int t;
     state_before[i] = (uint8_t)s;
@@ -393,7 +408,7 @@ static void close_record(csv_out* o, uint64_t rec, int col, uint64_t off) {
   for (int c = col + 1; c < o->n_cols; c++) close_field(o, rec, c, off);  /* defaults */
 }
 
-int or_csv_parse(const uint8_t* in, uint64_t n, uint8_t fd, uint8_t rd, uint8_t q,
+int or_csv_parse(const uint8_t* in, uint64_t n, uint8_t fd, uint8_t rd, uint8_t q, int crlf,
                  int n_cols, const int32_t* col_types, int32_t** out_offsets,
                  uint8_t** out_chars, void** out_typed, uint64_t records_capacity,
                  const uint64_t* chars_capacity, or_status* st) {
@@ -403,7 +418,7 @@ int or_csv_parse(const uint8_t* in, uint64_t n, uint8_t fd, uint8_t rd, uint8_t 
                chars_capacity, st, NULL, 0, 0};
   for (int c = 0; c < n_cols; c++)
     if (col_types[c] == C_STR && out_offsets[c]) out_offsets[c][0] = 0;
-  csv_syms y = {fd, rd, q};
+  csv_syms y = syms_of(crlf ? 2 : 0, fd, rd, q);
   int s = EOR, tag = T_RD;
   uint64_t rec = 0, field_start = 0;
   int col = 0;
@@ -483,7 +498,7 @@ int or_tokenize(const uint8_t* in, uint64_t n, uint8_t* out_id, uint64_t* out_st
  * DFA instance that started the chunk in state i (Figure 2).              */
 void or_stv(int kind, uint8_t fd, uint8_t rd, uint8_t q, const uint8_t* chunk,
             uint64_t len, uint8_t* stv) {
-  csv_syms y = {fd, rd, q};
+  csv_syms y = syms_of(kind, fd, rd, q);
   for (int i = 0; i < nstates(kind); i++) {
     int s = i, t;
     for (uint64_t j = 0; j < len; j++) s = step_any(kind, &y, s, chunk[j], &t);
@@ -543,7 +558,7 @@ uint64_t or_bruteforce(int kind, uint8_t fd, uint8_t rd, uint8_t q, const uint8_
   *checked = 0;
   uint8_t str[16], seq_state[17], tags[16], starts[16];
   int idx[16];
-  csv_syms y = {fd, rd, q};
+  csv_syms y = syms_of(kind, fd, rd, q);
   for (int len = 1; len <= max_len; len++) {
     for (int i = 0; i < len; i++) idx[i] = 0;
     for (;;) {
@@ -557,7 +572,7 @@ uint64_t or_bruteforce(int kind, uint8_t fd, uint8_t rd, uint8_t q, const uint8_
         col_seq[i] = col;
         s = step_any(kind, &y, s, str[i], &t);
         tags[i] = (uint8_t)t;
-        if (kind == 0) { if (t == T_RD) col = 0; else if (t == T_FD) col++; }
+        if (is_csv(kind)) { if (t == T_RD) col = 0; else if (t == T_FD) col++; }
       }
       (*checked)++;
       for (int ch = 1; ch <= max_len; ch++) {
@@ -566,7 +581,7 @@ uint64_t or_bruteforce(int kind, uint8_t fd, uint8_t rd, uint8_t q, const uint8_
         int a_abs = 1; uint64_t a_o = 0;         /* seed: absolute column 0 */
         for (int c = 0; c < nch; c++) {
           if (starts[c] != seq_state[c * ch]) bad++;
-          if (kind == 0) {
+          if (is_csv(kind)) {
             if (!a_abs || a_o != col_seq[c * ch]) bad++;
             int b_abs; uint64_t b_o;
             int clen = len - c * ch < ch ? len - c * ch : ch;

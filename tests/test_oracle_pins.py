@@ -420,3 +420,68 @@ def test_timestamps_random_days_match_timegm():
     cols, st = O.csv_parse(b"\n".join(lines) + b"\n", ["ts"])
     assert st["error"] == 0
     assert cols[0].tolist() == want
+
+
+# ------------------------------------------------------------ CRLF line ends
+# Reading: with CRLF line ends, a carriage return outside quotes is a
+# control symbol (dropped from the value, the field stays open); inside
+# quotes it is data.  Record delimiter LF.
+CRLF_CASES = [
+    (b"a,b\r\nc,d\r\n", [[b"a", b"b"], [b"c", b"d"]], 0),
+    (b'"x",y\r\n', [[b"x", b"y"]], 0),
+    (b'"a\r\nb",c\r\n', [[b"a\r\nb", b"c"]], 0),            # CRLF inside quotes is data
+    (b"a,\r\n,\r\n", [[b"a", b""], [b"", b""]], 0),
+    (b"\r\n\r\n", [[b""], [b""]], 0),                       # empty lines
+    (b"a\rb,c\r\n", [[b"ab", b"c"]], 0),                    # a bare CR is dropped too
+    (b"a,b\r\nc,d", [[b"a", b"b"], [b"c", b"d"]], 0),       # no final line end
+    (b"a,b\r", [[b"a", b"b"]], 0),
+]
+
+
+@pytest.mark.parametrize("data,want,err", CRLF_CASES)
+def test_crlf_cases(data, want, err):
+    n = len(want[0])
+    cols, st = O.csv_parse(data, ["str"] * n, crlf=True)
+    assert st["error"] == err and st["n_records"] == len(want)
+    for c in range(n):
+        offs, chars = cols[c]
+        got = [bytes(chars[offs[r]:offs[r + 1]]) for r in range(len(want))]
+        assert got == [row[c] for row in want]
+
+
+def test_crlf_invalid_after_cr():
+    # a quote after a dropped CR is a quote inside an unquoted field
+    _, st = O.csv_parse(b'"a"\r"b"\r\n', ["str"], crlf=True)
+    assert st["error"] & O.E_INVALID_INPUT and st["first_error_offset"] == 4
+    # without CRLF handling the CR is plain data, so "a" followed by it is invalid at 3
+    _, st = O.csv_parse(b'"a"\r\n', ["str"])
+    assert st["error"] & O.E_INVALID_INPUT and st["first_error_offset"] == 3
+
+
+def test_crlf_equals_lf_after_removing_unquoted_cr():
+    """On generated quoted CSV, CRLF line ends parse to the same columns as
+    the LF original (quoted newlines keep their bytes in both)."""
+    data, info, _ = datagen.generate("csv4_1mib", target=64 * 1024)
+    lf = bytes(data)
+    # add a CR before every record delimiter only: walk the oracle's tags
+    _, tags, _ = O.tags(lf)
+    out = bytearray()
+    for b, t in zip(lf, tags):
+        if t == O.TAG_RD:
+            out += b"\r"
+        out.append(b)
+    cols = datagen.WORKLOADS["csv4_1mib"]["cols"]
+    a, sa = O.csv_parse(lf, cols)
+    b, sb = O.csv_parse(bytes(out), cols, crlf=True)
+    assert sa == sb and sa["error"] == 0
+    for (oa, ca), (ob, cb) in zip(a, b):
+        assert np.array_equal(oa, ob) and np.array_equal(ca, cb)
+
+
+def test_bruteforce_csv_crlf_len7():
+    """The CRLF variant's scan-derived chunk start states and column offsets
+    equal the sequential walk on every string of length 1..7 over one byte
+    per symbol group."""
+    bad, checked = O.bruteforce(O.KIND_CSV_CRLF, b'",\n\ra', 7)
+    assert checked == sum(5 ** k for k in range(1, 8))
+    assert bad == 0
