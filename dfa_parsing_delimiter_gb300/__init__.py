@@ -82,6 +82,8 @@ def lib() -> ctypes.CDLL:
         L.pp_count_byte.argtypes = [_vp, _sz, _u8, _vp, _vp]
         L.pp_desc_csv.restype = ctypes.c_int
         L.pp_desc_csv.argtypes = [ctypes.POINTER(DfaDesc), _u8, _u8, _u8]
+        L.pp_desc_csv_crlf.restype = ctypes.c_int
+        L.pp_desc_csv_crlf.argtypes = [ctypes.POINTER(DfaDesc), _u8, _u8]
         L.pp_desc_json_lexer.restype = ctypes.c_int
         L.pp_desc_json_lexer.argtypes = [ctypes.POINTER(DfaDesc)]
         L.pp_strerror.restype = ctypes.c_char_p
@@ -113,6 +115,13 @@ def _stream(stream) -> int:
 def desc_csv(fd: bytes = b",", rd: bytes = b"\n", quote: bytes = b'"') -> DfaDesc:
     d = DfaDesc()
     _check(lib().pp_desc_csv(ctypes.byref(d), fd[0], rd[0], quote[0]), "pp_desc_csv")
+    return d
+
+
+def desc_csv_crlf(fd: bytes = b",", quote: bytes = b'"') -> DfaDesc:
+    """The quoted-CSV DFA for CRLF line ends (CR outside quotes dropped)."""
+    d = DfaDesc()
+    _check(lib().pp_desc_csv_crlf(ctypes.byref(d), fd[0], quote[0]), "pp_desc_csv_crlf")
     return d
 
 

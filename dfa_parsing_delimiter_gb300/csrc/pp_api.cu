@@ -291,6 +291,27 @@ pp_rc pp_desc_csv(pp_dfa_desc* out, uint8_t fd, uint8_t rd, uint8_t quote) {
   return PP_OK;
 }
 
+pp_rc pp_desc_csv_crlf(pp_dfa_desc* out, uint8_t fd, uint8_t quote) {
+  const uint8_t lf = 0x0A, cr = 0x0D;
+  if (!out || fd == lf || fd == cr || quote == lf || quote == cr) return PP_EINVAL;
+  const pp_rc rc = pp_desc_csv(out, fd, lf, quote);
+  if (rc != PP_OK) return rc;
+  // a fifth symbol group for CR: a control symbol outside quotes that
+  // leaves the field open, data inside quotes
+  enum { EOR = 0, FLD = 1, ENC = 2, ESC = 3, INV = 4 };
+  const int GC = 4;
+  out->n_groups = 5;
+  out->byte_to_group[cr] = GC;
+  static const uint8_t next[5] = {FLD, FLD, ENC, FLD, INV};
+  static const uint8_t tags[5] = {PP_TAG_CTRL, PP_TAG_CTRL, PP_TAG_DATA, PP_TAG_CTRL,
+                                  PP_TAG_INVALID};
+  for (int s = 0; s < 5; ++s) {
+    out->delta[GC][s] = next[s];
+    out->tag[s][GC] = tags[s];
+  }
+  return PP_OK;
+}
+
 pp_rc pp_desc_json_lexer(pp_dfa_desc* out) {
   if (!out) return PP_EINVAL;
   std::memset(out, 0, sizeof *out);

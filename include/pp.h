@@ -304,6 +304,17 @@ pp_rc pp_count_byte(const uint8_t* d_in, size_t n_bytes, uint8_t value, uint64_t
 pp_rc pp_desc_csv(pp_dfa_desc* out, uint8_t fd, uint8_t rd, uint8_t quote);
 
 /*
+ * pp_desc_csv_crlf — the same DFA for CRLF line ends: the record delimiter
+ * is LF (0x0A), and a carriage return (0x0D) outside quotes is a control
+ * symbol, dropped from the value, after which the field stays open (EOR,
+ * FLD and ESC go to FLD on CR; inside quotes a CR is data).  The pages name
+ * no line-end convention; ParPaRaw Section 4 ("Validating format") notes
+ * that simulating the DFA allows such parsing rules.  fd and quote must be
+ * distinct and neither may be LF or CR.  Host only; PP_EINVAL otherwise.
+ */
+pp_rc pp_desc_csv_crlf(pp_dfa_desc* out, uint8_t fd, uint8_t quote);
+
+/*
  * pp_desc_json_lexer — build the 16-state JSON-like lexer DFA used by
  * pp_tokenize (whitespace runs, punctuation {}[],:, strings with backslash
  * escapes, integers, fractions and exponents).  Token ids: '{'0 '}'1 '['2

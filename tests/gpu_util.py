@@ -47,11 +47,12 @@ def desc_rd(desc):
     return 10
 
 
-def compare_csv(data, col_types, desc=None, offset=0, fd=b",", rd=b"\n", quote=b'"'):
+def compare_csv(data, col_types, desc=None, offset=0, fd=b",", rd=b"\n", quote=b'"',
+                crlf=False):
     """Parse with both; assert identical status and columns.  Returns status."""
-    desc = desc or pp.desc_csv(fd, rd, quote)
+    desc = desc or (pp.desc_csv_crlf(fd, quote) if crlf else pp.desc_csv(fd, rd, quote))
     out, st = run_gpu_csv(data, col_types, desc=desc, offset=offset)
-    ref, rst = O.csv_parse(data, col_types, fd=fd, rd=rd, quote=quote)
+    ref, rst = O.csv_parse(data, col_types, fd=fd, rd=rd, quote=quote, crlf=crlf)
     assert st["error"] == rst["error"], (st, rst)
     assert st["first_error_offset"] == rst["first_error_offset"], (st, rst)
     if st["error"] & O.FATAL:

@@ -53,9 +53,10 @@ def _reach(kind):
     return prefix
 
 
-@pytest.mark.parametrize("kind", [O.KIND_CSV, O.KIND_LEX])
+@pytest.mark.parametrize("kind", [O.KIND_CSV, O.KIND_LEX, O.KIND_CSV_CRLF])
 def test_desc_matches_oracle_cell_by_cell(kind):
-    d = pp.desc_csv() if kind == O.KIND_CSV else pp.desc_json_lexer()
+    d = {O.KIND_CSV: pp.desc_csv, O.KIND_LEX: pp.desc_json_lexer,
+         O.KIND_CSV_CRLF: pp.desc_csv_crlf}[kind]()
     ns = O.nstates(kind)
     assert d.n_states == ns
     prefix = _reach(kind)
@@ -83,6 +84,15 @@ def test_desc_accepting_states():
         if s == 15:
             continue
         assert bool((d.accept_mask >> s) & 1) == (not st["error"] & O.E_BAD_END_STATE), s
+
+
+def test_desc_csv_crlf_arguments():
+    L = pp.lib()
+    for fd, q in ((10, 34), (13, 34), (44, 10), (44, 13), (44, 44)):
+        assert L.pp_desc_csv_crlf(ctypes.byref(pp.DfaDesc()), fd, q) == pp.PP_EINVAL
+    d = pp.desc_csv_crlf(b";", b"'")
+    assert d.n_groups == 5 and d.byte_to_group[13] == 4 and d.byte_to_group[10] == 2
+    assert d.byte_to_group[ord(";")] == 1 and d.byte_to_group[ord("'")] == 0
 
 
 def test_desc_csv_custom_delimiters():

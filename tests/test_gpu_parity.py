@@ -354,3 +354,39 @@ def test_parse_timestamp_across_tile_boundary(shift):
         data = first + filler + b"," + ts + b"\n" + rest
         assert data.index(ts, len(first)) == TILE + shift
         compare_csv(data, ["str", "ts"])
+
+
+# ------------------------------------------------------------ CRLF line ends
+def _with_crlf(data):
+    """A CR before every record delimiter (found by the oracle's tags)."""
+    lf = bytes(data)
+    _, tags, _ = O.tags(lf)
+    out = bytearray()
+    for b, t in zip(lf, tags):
+        if t == O.TAG_RD:
+            out += b"\r"
+        out.append(b)
+    return bytes(out)
+
+
+@pytest.mark.parametrize("name,target", [("csv4_1mib", 3 * TILE + 101), ("csv16_256mib", 2 << 20),
+                                         ("csv18_2gib", 2 << 20), ("csv3_1gib", 4 << 20)])
+def test_parse_crlf_generated(name, target):
+    data, info, _ = datagen.generate(name, target=target)
+    st = compare_csv(_with_crlf(data), datagen.WORKLOADS[name]["cols"], crlf=True)
+    assert st["error"] == 0 and st["n_records"] == info["n_records"]
+
+
+@pytest.mark.parametrize("k", range(-3, 4))
+def test_parse_crlf_at_tile_boundary(k):
+    """CR and LF on either side of a tile edge, after plain, quoted and
+    numeric fields, and bare CRs inside fields."""
+    rows = []
+    n = 0
+    while n < TILE + 64:
+        r = b"%d,ab\rc,\"q\r\nx\"\r\n" % n
+        rows.append(r)
+        n += len(r)
+    data = b"z" * (TILE + k - 3) + b",,\r\n" + b"".join(rows)  # CR at TILE + k - 1, LF after it
+    compare_csv(data, ["str", "str", "str"], crlf=True)
+    compare_csv(data[: TILE + k + 40], ["i64", "str", "str"], crlf=True)
