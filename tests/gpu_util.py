@@ -9,7 +9,7 @@ import oracle as O
 
 def to_dev(a, offset=0):
     """Copy bytes to the GPU; offset > 0 yields a deliberately misaligned view."""
-    a = np.frombuffer(bytes(a), dtype=np.uint8) if isinstance(a, (bytes, bytearray)) else a
+    a = np.frombuffer(bytearray(a), dtype=np.uint8) if isinstance(a, (bytes, bytearray)) else a
     buf = torch.empty(a.size + offset + 16, dtype=torch.uint8, device="cuda")
     if a.size:
         buf[offset:offset + a.size].copy_(torch.from_numpy(np.ascontiguousarray(a)))
