@@ -67,6 +67,8 @@ def _load():
         L = ctypes.CDLL(_SO)
         L.or_csv_parse.argtypes = [_vp, _u64, _u8, _u8, _u8, ctypes.c_int, ctypes.c_int, _vp,
                                    _vp, _vp, _vp, _u64, _vp, ctypes.POINTER(Status)]
+        L.or_count_fields.argtypes = [_vp, _u64, _u8, _u8, _u8, ctypes.c_int, _vp,
+                                      ctypes.POINTER(Status)]
         L.or_tokenize.argtypes = [_vp, _u64, _vp, _vp, _vp, _u64, ctypes.POINTER(Status)]
         L.or_tags.argtypes = [ctypes.c_int, _u8, _u8, _u8, _vp, _u64, _vp, _vp]
         L.or_tags.restype = ctypes.c_int
@@ -137,6 +139,17 @@ def csv_parse(data, col_types, fd=b",", rd=b"\n", quote=b'"', records_capacity=N
         else:
             cols.append(typed[c][:R])
     return cols, st.as_dict(ncols)
+
+
+def count_fields(data, fd=b",", rd=b"\n", quote=b'"', crlf=False):
+    """(min, max) fields per record over the input, and the status."""
+    L = _load()
+    a = _arr(data)
+    out = np.zeros(2, dtype=np.uint64)
+    st = Status()
+    L.or_count_fields(a.ctypes.data, a.size, fd[0], rd[0], quote[0], int(bool(crlf)),
+                      out.ctypes.data, ctypes.byref(st))
+    return (int(out[0]), int(out[1])), st.as_dict()
 
 
 def tokenize(data, capacity=None):

@@ -496,6 +496,45 @@ int or_tokenize(const uint8_t* in, uint64_t n, uint8_t* out_id, uint64_t* out_st
 
 /* State-transition vector of one chunk: entry i = the final state of the
  * DFA instance that started the chunk in state i (Figure 2).              */
+/* Column-count inference (ParPaRaw Section 4, "Inferring or validating
+ * number of columns"; inputs may hold records with varying numbers of field
+ * delimiters): the fewest and the most fields of any record, walking the
+ * DFA byte by byte.  A record has one more field than
+ * field delimiters; a non-empty tail without a record delimiter is one more
+ * record.  out[0] = min, out[1] = max (both 0 without records); st gets
+ * n_records and the same data errors as the parse (invalid input, a
+ * non-accepting end state).                                              */
+void or_count_fields(const uint8_t* in, uint64_t n, uint8_t fd, uint8_t rd, uint8_t q, int crlf,
+                     uint64_t* out, or_status* st) {
+  memset(st, 0, sizeof *st);
+  st->first_error_offset = UINT64_MAX;
+  csv_syms y = syms_of(crlf ? 2 : 0, fd, rd, q);
+  int s = EOR, tag = T_RD;
+  uint64_t fields = 1, mn = UINT64_MAX, mx = 0, recs = 0;
+  for (uint64_t i = 0; i < n; i++) {
+    s = csv_step(&y, s, in[i], &tag);
+    if (tag == T_INVALID) { flag(st, E_INVALID_INPUT, i, 1); break; }
+    if (tag == T_FD) fields++;
+    if (tag == T_RD) {
+      if (fields < mn) mn = fields;
+      if (fields > mx) mx = fields;
+      recs++;
+      fields = 1;
+    }
+  }
+  if (!(st->error & E_INVALID_INPUT)) {
+    if (!csv_accepting(s)) flag(st, E_BAD_END_STATE, n, 1);
+    if (n > 0 && tag != T_RD) {  /* the open tail is one more record */
+      if (fields < mn) mn = fields;
+      if (fields > mx) mx = fields;
+      recs++;
+    }
+  }
+  out[0] = recs ? mn : 0;
+  out[1] = recs ? mx : 0;
+  st->n_records = recs;
+}
+
 void or_stv(int kind, uint8_t fd, uint8_t rd, uint8_t q, const uint8_t* chunk,
             uint64_t len, uint8_t* stv) {
   csv_syms y = syms_of(kind, fd, rd, q);

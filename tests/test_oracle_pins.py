@@ -485,3 +485,63 @@ def test_bruteforce_csv_crlf_len7():
     bad, checked = O.bruteforce(O.KIND_CSV_CRLF, b'",\n\ra', 7)
     assert checked == sum(5 ** k for k in range(1, 8))
     assert bad == 0
+
+
+# ------------------------------------------------- column-count inference
+COUNT_CASES = [
+    (b"", (0, 0), 0, 0),
+    (b"1,Apples\n2\n", (1, 2), 2, 0),                  # the pages' example of varying counts
+    (b"a,b,c\n", (3, 3), 1, 0),
+    (b"\n\n", (1, 1), 2, 0),                          # empty lines: one empty field each
+    (b"a,b\nc", (1, 2), 2, 0),                        # a tail without a delimiter
+    (b'a,"x,\ny",c\n,\n', (2, 3), 2, 0),              # delimiters inside quotes are data
+    (b",,,,\n", (5, 5), 1, 0),
+    (b'"ab', (0, 0), 0, O.E_BAD_END_STATE),           # ends inside quotes
+]
+
+
+@pytest.mark.parametrize("data,mm,recs,err", COUNT_CASES)
+def test_count_fields_cases(data, mm, recs, err):
+    got, st = O.count_fields(data)
+    assert st["error"] == err
+    if not err:
+        assert got == mm and st["n_records"] == recs
+
+
+def test_count_fields_invalid_offset():
+    _, st = O.count_fields(b'ab,c"d\n')
+    assert st["error"] == O.E_INVALID_INPUT and st["first_error_offset"] == 4
+
+
+@pytest.mark.parametrize("name", ["csv4_1mib", "csv16_256mib", "csv3_1gib", "csv18_2gib"])
+def test_count_fields_generated_schema(name):
+    """The generator writes a fixed number of columns per record, so the
+    inferred min and max are both that number, and the record count is the
+    generator's."""
+    data, info, _ = datagen.generate(name, target=1 << 20)
+    (mn, mx), st = O.count_fields(data)
+    n = len(datagen.WORKLOADS[name]["cols"])
+    assert st["error"] == 0 and (mn, mx) == (n, n) and st["n_records"] == info["n_records"]
+
+
+def test_count_fields_agrees_with_a_row_split():
+    """Min and max fields equal those of an independent split of each row on
+    its unquoted commas (rows whose quotes are balanced)."""
+    rng = random.Random(3)
+    rows = []
+    for _ in range(400):
+        k = rng.randint(1, 9)
+        rows.append(b",".join(rng.choice([b"x", b'"a,b"', b"", b'"\n"']) for _ in range(k)))
+    data = b"\n".join(rows) + b"\n"
+    (mn, mx), st = O.count_fields(data)
+    # recount independently: split each row on its unquoted commas
+    def nfields(r):
+        n, q = 1, False
+        for ch in r:
+            if ch == ord('"'):
+                q = not q
+            elif ch == ord(",") and not q:
+                n += 1
+        return n
+    counts = [nfields(r) for r in rows]
+    assert st["error"] == 0 and (mn, mx) == (min(counts), max(counts)) and st["n_records"] == 400
