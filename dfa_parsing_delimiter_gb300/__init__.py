@@ -82,6 +82,8 @@ def lib() -> ctypes.CDLL:
         L.pp_count_byte.argtypes = [_vp, _sz, _u8, _vp, _vp]
         L.pp_desc_csv.restype = ctypes.c_int
         L.pp_desc_csv.argtypes = [ctypes.POINTER(DfaDesc), _u8, _u8, _u8]
+        L.pp_count_fields.restype = ctypes.c_int
+        L.pp_count_fields.argtypes = [_vp, _sz, ctypes.POINTER(DfaDesc), _vp, _vp, _vp]
         L.pp_desc_csv_crlf.restype = ctypes.c_int
         L.pp_desc_csv_crlf.argtypes = [ctypes.POINTER(DfaDesc), _u8, _u8]
         L.pp_desc_json_lexer.restype = ctypes.c_int
@@ -355,6 +357,18 @@ class CsvOutputs:
             else:
                 cols.append(self.typed[i][:R])
         return cols
+
+
+def count_fields(d_in: torch.Tensor, desc: DfaDesc | None = None, stream=None):
+    """Fewest and most fields per record of a device uint8 tensor ->
+    ((min, max), status).  Synchronises to read the result."""
+    desc = desc or desc_csv()
+    out = torch.zeros(2, dtype=torch.int64, device=d_in.device)
+    st = new_status(d_in.device)
+    _check(lib().pp_count_fields(_ptr(d_in), d_in.numel(), ctypes.byref(desc), _ptr(out),
+                                 _ptr(st), _stream(stream)), "pp_count_fields")
+    mm = out.cpu().tolist()
+    return (int(mm[0]), int(mm[1])), read_status(st)
 
 
 def count_byte(d_in: torch.Tensor, value: int, stream=None) -> int:

@@ -406,6 +406,23 @@ pp_rc pp_parse(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa, int 
   return cuda_rc(e);
 }
 
+pp_rc pp_count_fields(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa,
+                      uint64_t* d_fields, pp_status* d_status, cudaStream_t stream) {
+  if (!d_fields) return PP_EINVAL;
+  const pp_coltype skip = PP_COL_SKIP;
+  ppi::ParseParams p;
+  const pp_rc rc = ppi::parse_prepare(d_in, n_bytes, dfa, 1, &skip, nullptr, nullptr, nullptr, 0,
+                                      nullptr, d_status, &p);
+  if (rc != PP_OK) return rc;
+  void* scratch = nullptr;
+  cudaError_t e = cudaMallocAsync(&scratch, ppi::fields_scratch_bytes(p.n_tiles), stream);
+  if (e != cudaSuccess) return cuda_rc(e);
+  e = ppi::launch_count_fields(p, scratch, d_fields, stream);
+  const cudaError_t ef = cudaFreeAsync(scratch, stream);
+  if (e == cudaSuccess) e = ef;
+  return cuda_rc(e);
+}
+
 pp_rc pp_tokenize(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa,
                   uint8_t* out_token_id, uint64_t* out_start, uint32_t* out_len,
                   size_t tokens_capacity, pp_status* d_status, cudaStream_t stream) {

@@ -104,6 +104,10 @@ pp_rc parse_prepare(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa,
                     size_t records_capacity, const size_t chars_capacity[],
                     pp_status* d_status, ParseParams* out);
 size_t parse_tile_bytes();
+// column-count inference (pp_count_fields): scratch bytes for n_tiles tiles,
+// and the launch (p from parse_prepare; its scratch is carved here)
+size_t fields_scratch_bytes(uint32_t n_tiles);
+cudaError_t launch_count_fields(ParseParams p, void* scratch, uint64_t* out, cudaStream_t stream);
 
 // ---------------------------------------------------------- pp_tags / tokenize
 struct GenericDfa {

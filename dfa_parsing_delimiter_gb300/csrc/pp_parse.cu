@@ -1764,6 +1764,169 @@ __global__ void __launch_bounds__(NT, 2) main_kernel(const __grid_constant__ Par
   feed_finish(S.F);
 }
 
+// ===================================================== column-count inference
+// ParPaRaw Section 4, "Inferring or validating number of columns": over a
+// byte range, the field delimiters before its first record delimiter (all
+// of them if it has none), those after its last, and the fewest and most
+// fields of the records lying wholly inside it.  Ranges combine in input
+// order: the records that span the seam have a.post + b.pre + 1 fields.
+struct FAgg { uint32_t rd, pre, post, mn, mx; };
+
+__device__ __forceinline__ FAgg fagg_identity() { return {0u, 0u, 0u, 0xFFFFFFFFu, 0u}; }
+__device__ __forceinline__ uint32_t sat_add(uint32_t a, uint32_t b) {
+  const uint32_t c = a + b;
+  return c < a ? 0xFFFFFFFFu : c;
+}
+__device__ __forceinline__ FAgg fagg_combine(const FAgg& a, const FAgg& b) {
+  if (!a.rd && !b.rd) {
+    const uint32_t f = sat_add(a.pre, b.pre);
+    return {0u, f, f, 0xFFFFFFFFu, 0u};
+  }
+  if (!a.rd) return {b.rd, sat_add(a.pre, b.pre), b.post, b.mn, b.mx};
+  if (!b.rd) return {a.rd, a.pre, sat_add(a.post, b.pre), a.mn, a.mx};
+  const uint32_t mid = sat_add(sat_add(a.post, b.pre), 1u);
+  return {sat_add(a.rd, b.rd), a.pre, b.post, min(min(a.mn, b.mn), mid),
+          max(max(a.mx, b.mx), mid)};
+}
+// one 32-byte chunk from its delimiter bitmaps
+__device__ __forceinline__ FAgg fagg_chunk(uint32_t fd, uint32_t rd) {
+  if (!rd) {
+    const uint32_t f = __popc(fd);
+    return {0u, f, f, 0xFFFFFFFFu, 0u};
+  }
+  const uint32_t first = __ffs(rd) - 1, last = 31 - __clz(rd);
+  FAgg a = {uint32_t(__popc(rd)), uint32_t(__popc(fd & range_mask(0, first))),
+            uint32_t(__popc(fd & range_mask(last + 1, 32))), 0xFFFFFFFFu, 0u};
+  uint32_t m = rd & (rd - 1), prev = first;
+  while (m) {
+    const uint32_t j = __ffs(m) - 1;
+    const uint32_t f = __popc(fd & range_mask(prev + 1, j)) + 1u;
+    a.mn = min(a.mn, f);
+    a.mx = max(a.mx, f);
+    prev = j;
+    m &= m - 1;
+  }
+  return a;
+}
+// ordered reduction over the warp: lane 0 gets lanes 0..31 combined in order
+__device__ __forceinline__ FAgg fagg_warp(FAgg a) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const FAgg o = {__shfl_down_sync(FULL, a.rd, d), __shfl_down_sync(FULL, a.pre, d),
+                    __shfl_down_sync(FULL, a.post, d), __shfl_down_sync(FULL, a.mn, d),
+                    __shfl_down_sync(FULL, a.mx, d)};
+    if (lane + d < 32) a = fagg_combine(a, o);
+  }
+  return a;
+}
+
+struct FieldsShared {
+  Feed F;
+  uint32_t tile_stv;
+  uint32_t warp_stv[NW];
+  FAgg wagg[NW];
+};
+constexpr size_t FIELDS_SMEM = LUT_BYTES + 2 * TILE + sizeof(FieldsShared);
+
+// Per tile, from its true start state: tag every chunk, then the tile's
+// aggregate; the thread that owns the input's last byte records whether the
+// input ends inside a record (counters[2]).
+__global__ void __launch_bounds__(NT, 3) fields_kernel(const __grid_constant__ ParseParams P,
+                                                       FAgg* agg) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint32_t* lut_s = reinterpret_cast<uint32_t*>(smem);
+  uint8_t* lin0 = smem + LUT_BYTES;  // two tile buffers
+  FieldsShared& S = *reinterpret_cast<FieldsShared*>(lin0 + 2 * TILE);
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  load_lut(P, lut_s);
+  const uint32_t* my_lut = lut_s + lane;
+  const bool aligned_in = (reinterpret_cast<uintptr_t>(P.in) & 15) == 0;
+  uint32_t* counter = &P.s.counters[0];
+  uint32_t tk = 0;  // thread 0: the next ticket
+  feed_start(P, S.F, counter, aligned_in, lin0, tk);
+  for (;;) {
+    const uint32_t tile = S.F.tile[S.F.cur];
+    if (tile >= P.n_tiles) break;
+    uint8_t* tile_s = lin0 + S.F.cur * TILE;
+    const uint64_t tile_base = uint64_t(tile) * TILE;
+    const uint32_t tile_len = uint32_t(min(uint64_t(TILE), P.n - tile_base));
+    uint32_t w[8];
+    feed_tile(P, S.F, counter, aligned_in, lin0, tile_base, tile_len, w, tk);
+    const uint32_t cstart = uint32_t(t) * CB;
+    const uint32_t clen = tile_len > cstart ? min(tile_len - cstart, uint32_t(CB)) : 0u;
+    const uint32_t s_tile = P.s.tile_state[tile];
+    uint32_t G, special, special_x;
+    stv_pass(w, clen, tile_s, cstart, my_lut, G, special, special_x);
+    const uint32_t lane_ex = block_stv(G, S.warp_stv, &S.tile_stv);
+    const uint32_t st = stv_apply(lane_ex, stv_apply(S.warp_stv[warp], s_tile));
+    const Tags g = tag_chunk(st, special, special_x, P.sticky, clen, cstart, tile_s + cstart,
+                             my_lut, P.bg_next);
+    if (g.inv_at < clen && st != 4)
+      report(P.st, PP_ERR_INVALID_INPUT, tile_base + cstart + g.inv_at, true);
+    if (tile + 1 == P.n_tiles && clen > 0 && cstart + clen == tile_len) {
+      if (g.end != 4 && !((P.accept_mask >> g.end) & 1u)) report(P.st, PP_ERR_BAD_END_STATE, P.n, true);
+      P.s.counters[2] = ((g.rd >> (clen - 1)) & 1u) ? 0u : 1u;
+    }
+    const FAgg a = fagg_warp(fagg_chunk(g.fd, g.rd));
+    if (lane == 0) S.wagg[warp] = a;
+    __syncthreads();
+    if (warp == 0) {
+      const FAgg b = fagg_warp(lane < NW ? S.wagg[lane] : fagg_identity());
+      if (lane == 0) agg[tile] = b;
+    }
+    feed_next(S.F);  // the tile was last read before the barrier above
+  }
+  feed_finish(S.F);
+}
+
+// The tiles' aggregates in input order (one block), then the records at the
+// input's two ends: the first record ends at the first record delimiter,
+// and an open tail is one more record.
+constexpr int FR_NT = 1024;
+__global__ void __launch_bounds__(FR_NT) fields_reduce_kernel(const __grid_constant__ ParseParams P,
+                                                              const FAgg* agg, uint64_t* out) {
+  __shared__ FAgg wa[FR_NT / 32];
+  __shared__ unsigned long long n_rd;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  if (t == 0) n_rd = 0;
+  __syncthreads();
+  const uint32_t n = P.n_tiles, per = (n + FR_NT - 1) / FR_NT;
+  const uint32_t i0 = min(n, uint32_t(t) * per), i1 = min(n, i0 + per);
+  FAgg a = fagg_identity();
+  unsigned long long rds = 0;
+  for (uint32_t i = i0; i < i1; ++i) {
+    const FAgg b = agg[i];
+    a = fagg_combine(a, b);
+    rds += b.rd;
+  }
+  if (rds) atomicAdd(&n_rd, rds);
+  a = fagg_warp(a);
+  if (lane == 0) wa[warp] = a;
+  __syncthreads();
+  if (warp == 0) {
+    a = fagg_warp(wa[lane]);
+    if (lane == 0) {
+      const bool tail = n > 0 && P.s.counters[2] != 0;
+      uint64_t mn = a.mn, mx = a.mx;
+      if (a.rd) {  // the first record, up to the first record delimiter
+        mn = min(mn, uint64_t(a.pre) + 1);
+        mx = max(mx, uint64_t(a.pre) + 1);
+        if (tail) {  // the open tail after the last one
+          mn = min(mn, uint64_t(a.post) + 1);
+          mx = max(mx, uint64_t(a.post) + 1);
+        }
+      } else if (tail) {  // one record, the whole input
+        mn = mx = uint64_t(a.pre) + 1;
+      }
+      const uint64_t recs = n_rd + (tail ? 1u : 0u);
+      out[0] = recs ? mn : 0;
+      out[1] = recs ? mx : 0;
+      P.st->n_records = recs;
+    }
+  }
+}
+
 // ================================================================= launch
 // Zero the tile counters and the scan's look-back flags; initialise the
 // status and offsets[c][0] = 0 for every string column.
@@ -1852,11 +2015,65 @@ uint32_t ctx_stride_of(int ns, int n_cols) {
 }
 uint32_t pre_stride_of(int ns) { return uint32_t(PRE_HDR + 8 * (ns > 0 ? ns : 0)); }
 
+cudaError_t launch_fields(const ParseParams& p, FAgg* agg, uint64_t* out, cudaStream_t stream) {
+  static int n_sm = 0, occ = 0;
+  cudaError_t e;
+  if (!occ) {
+    int dev;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return e;
+    if ((e = cudaFuncSetAttribute(fields_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  int(FIELDS_SMEM))) != cudaSuccess)
+      return e;
+    int b = 0;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fields_kernel, NT, FIELDS_SMEM)) !=
+        cudaSuccess)
+      return e;
+    occ = b > 0 ? b : 1;
+  }
+  parse_init_kernel<<<1, 256, 0, stream>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (p.n_tiles) {
+    const uint32_t gv = uint32_t(std::min<uint64_t>((p.n_tiles + TV_NT / 32 - 1) / (TV_NT / 32),
+                                                    uint64_t(n_sm) * 6));
+    tile_stv_kernel<<<gv, TV_NT, LUT_BYTES, stream>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    tile_state_kernel<<<p.s.n_tstate_blocks, TS_NT, 0, stream>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const uint32_t g = uint32_t(std::min<uint64_t>(p.n_tiles, uint64_t(n_sm) * occ));
+    fields_kernel<<<g, NT, FIELDS_SMEM, stream>>>(p, agg);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  fields_reduce_kernel<<<1, FR_NT, 0, stream>>>(p, agg, out);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 namespace ppi {
 
 size_t parse_tile_bytes() { return TILE; }
+
+// counters | tile vectors | tile states | tile-state look-back words | tile aggregates
+size_t fields_scratch_bytes(uint32_t n) {
+  const uint32_t nt = (n + TS_TILES - 1) / TS_TILES;
+  return 256 + align256(size_t(n) * 4) + align256(n) + align256(size_t(nt) * 8) +
+         align256(size_t(n) * sizeof(FAgg));
+}
+
+cudaError_t launch_count_fields(ParseParams p, void* scratch, uint64_t* out, cudaStream_t stream) {
+  uint8_t* b = static_cast<uint8_t*>(scratch);
+  const uint32_t n = p.n_tiles;
+  p.s = ParseScratch{};
+  p.s.counters = reinterpret_cast<uint32_t*>(b); b += 256;
+  p.s.tile_stv = reinterpret_cast<uint32_t*>(b); b += align256(size_t(n) * 4);
+  p.s.tile_state = b; b += align256(n);
+  p.s.n_tstate_blocks = (n + TS_TILES - 1) / TS_TILES;
+  p.s.tstate_words = reinterpret_cast<unsigned long long*>(b);
+  b += align256(size_t(p.s.n_tstate_blocks) * 8);
+  return launch_fields(p, reinterpret_cast<FAgg*>(b), out, stream);
+}
 
 int parse_ns_width(int n_str) {
   if (n_str <= 0) return 0;

@@ -294,6 +294,29 @@ pp_rc pp_count_byte(const uint8_t* d_in, size_t n_bytes, uint8_t value, uint64_t
                     cudaStream_t stream);
 
 /*
+ * pp_count_fields — column-count inference (ParPaRaw Section 4, "Inferring
+ * or validating number of columns"): the fewest and the most fields of any
+ * record of the input, for a caller without a schema or one that wants to
+ * validate it before pp_parse.  A record has one more field than field
+ * delimiters; a non-empty tail without a record delimiter is one more
+ * record (as in pp_parse).  Each tile reduces its chunks' (delimiters
+ * before the first record delimiter, after the last, fewest and most fields
+ * in between) in order, and one block combines the tiles.
+ *   d_in      device, n_bytes bytes (any alignment).
+ *   dfa       host; the same descriptors as pp_parse takes.
+ *   d_fields  device uint64[2]: [0] fewest, [1] most fields per record
+ *             (both 0 for an input without records).
+ *   d_status  device; error bits as pp_parse (invalid input, a
+ *             non-accepting end state; with a fatal bit d_fields is
+ *             unspecified) and n_records.
+ * Scratch about 25 bytes per 16 KiB tile, taken stream-ordered
+ * (cudaMallocAsync) and freed the same way; asynchronous on `stream`.
+ * Returns PP_EINVAL for bad arguments, PP_ENOMEM / PP_ECUDA on CUDA errors.
+ */
+pp_rc pp_count_fields(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa,
+                      uint64_t* d_fields, pp_status* d_status, cudaStream_t stream);
+
+/*
  * pp_desc_csv — build the quoted-CSV DFA (RFC-4180 style quoting) with
  * states EOR=0 (at a field/record boundary, the start state), FLD=1 (inside
  * an unquoted field), ENC=2 (inside quotes), ESC=3 (a quote seen inside

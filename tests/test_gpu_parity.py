@@ -390,3 +390,58 @@ def test_parse_crlf_at_tile_boundary(k):
     data = b"z" * (TILE + k - 3) + b",,\r\n" + b"".join(rows)  # CR at TILE + k - 1, LF after it
     compare_csv(data, ["str", "str", "str"], crlf=True)
     compare_csv(data[: TILE + k + 40], ["i64", "str", "str"], crlf=True)
+
+
+# ------------------------------------------------- column-count inference
+def compare_count_fields(data, crlf=False, offset=0):
+    desc = pp.desc_csv_crlf() if crlf else pp.desc_csv()
+    got, st = pp.count_fields(to_dev(data, offset), desc)
+    ref, rst = O.count_fields(data, crlf=crlf)
+    assert st["error"] == rst["error"], (st, rst)
+    assert st["first_error_offset"] == rst["first_error_offset"]
+    if st["error"] & O.FATAL:
+        return st
+    assert got == ref and st["n_records"] == rst["n_records"], (got, ref, st, rst)
+    return st
+
+
+@pytest.mark.parametrize("name,target", [("csv4_1mib", None), ("csv16_256mib", 5 * TILE + 3),
+                                         ("csv3_1gib", 4 << 20), ("csv18_2gib", 40 << 20)])
+def test_count_fields_generated(name, target):
+    data, info, _ = datagen.generate(name, target=target)
+    n = len(datagen.WORKLOADS[name]["cols"])
+    st = compare_count_fields(data)
+    assert st["n_records"] == info["n_records"]
+    assert pp.count_fields(to_dev(data))[0] == (n, n)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_count_fields_varying_rows(seed):
+    """Rows of 1..60 fields, some quoted with embedded delimiters, empty
+    lines and a few rows longer than a tile, over many tiles."""
+    rng = random.Random(seed)
+    rows = []
+    size = 0
+    while size < 6 * TILE:
+        if rng.random() < 0.02:
+            r = b",".join(b"y" * rng.randint(0, 900) for _ in range(rng.randint(20, 60)))
+        elif rng.random() < 0.05:
+            r = b""
+        else:
+            r = b",".join(rng.choice([b"ab", b"", b'"x,\ny"', b'"q""q"', b"123"])
+                          for _ in range(rng.randint(1, 12)))
+        rows.append(r)
+        size += len(r) + 1
+    data = b"\n".join(rows) + (b"\n" if seed % 2 else b"")
+    compare_count_fields(data)
+    compare_count_fields(data, offset=3)
+
+
+def test_count_fields_edges():
+    for data in (b"", b"\n", b"\n\n\n", b"a", b"a,b,c", b",", b"a,b\n" * 10000 + b"c",
+                 b"x" * (3 * TILE) + b",y\n", b"," * (2 * TILE + 5) + b"\n" + b"a\n"):
+        compare_count_fields(data)
+    compare_count_fields(b'a,"b')                        # ends inside quotes
+    compare_count_fields(b"a\n" * 9000 + b'x"y\n')         # a quote inside a field
+    crlf = b"\r\n".join(b",".join(b"v" for _ in range(k % 7 + 1)) for k in range(5000)) + b"\r\n"
+    compare_count_fields(crlf, crlf=True)
