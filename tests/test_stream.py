@@ -176,3 +176,22 @@ def test_host_tokens_dense_long_and_errors():
     _, sh, _ = _host_tokens(arr, desc, max(sd["n_tokens"], 1), 16 << 10)
     assert sh["error"] & pp.ERR_INVALID_INPUT
     assert sh["first_error_offset"] == sd["first_error_offset"]
+
+
+def test_host_stream_timestamps_and_crlf():
+    """Streamed timestamp columns (8 bytes a value) and CRLF line ends,
+    with chunk boundaries between a CR and its LF."""
+    data, info, _ = datagen.generate("csv18ts_2gib", target=3 << 20)
+    col_types = datagen.WORKLOADS["csv18ts_2gib"]["cols"]
+    desc = pp.desc_csv()
+    dev, sdev, R = _device_run(data, col_types, desc)
+    assert sdev["error"] == 0 and sdev["n_records"] == info["n_records"]
+    host, shost = _host_run(data, col_types, desc, R, 256 << 10)
+    _assert_same(col_types, dev, sdev, host, shost)
+    crlf = np.frombuffer(bytes(data).replace(b"\n", b"\r\n"), dtype=np.uint8)
+    cdesc = pp.desc_csv_crlf()
+    dev, sdev, R = _device_run(crlf, col_types, cdesc)
+    assert sdev["error"] == 0 and sdev["n_records"] == info["n_records"]
+    for chunk in (256 << 10, (256 << 10) + 1):
+        host, shost = _host_run(crlf, col_types, cdesc, R, chunk)
+        _assert_same(col_types, dev, sdev, host, shost)
