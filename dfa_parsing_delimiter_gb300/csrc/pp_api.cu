@@ -409,6 +409,7 @@ pp_rc pp_parse(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa, int 
 pp_rc pp_count_fields(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa,
                       uint64_t* d_fields, pp_status* d_status, cudaStream_t stream) {
   if (!d_fields) return PP_EINVAL;
+  if (n_bytes > (size_t(1) << 36)) return PP_ETOOLARGE;  // the tile reduction's 32-bit ranges
   const pp_coltype skip = PP_COL_SKIP;
   ppi::ParseParams p;
   const pp_rc rc = ppi::parse_prepare(d_in, n_bytes, dfa, 1, &skip, nullptr, nullptr, nullptr, 0,

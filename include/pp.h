@@ -311,6 +311,7 @@ pp_rc pp_count_byte(const uint8_t* d_in, size_t n_bytes, uint8_t value, uint64_t
  *             unspecified) and n_records.
  * Scratch about 25 bytes per 16 KiB tile, taken stream-ordered
  * (cudaMallocAsync) and freed the same way; asynchronous on `stream`.
+ * Inputs up to 64 GiB (2^36 bytes); larger ones return PP_ETOOLARGE.
  * Returns PP_EINVAL for bad arguments, PP_ENOMEM / PP_ECUDA on CUDA errors.
  */
 pp_rc pp_count_fields(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa,

@@ -136,6 +136,12 @@ def test_bad_arguments_rejected_without_gpu():
     # tokenize: outputs missing with a capacity
     assert L.pp_tokenize(1, 1, ctypes.byref(j), None, None, None, 5, 1, None) == pp.PP_EINVAL
     assert L.pp_count_byte(None, 3, 10, 1, None) == pp.PP_EINVAL
+    # count fields: no output, a bad descriptor, an input beyond 64 GiB
+    csv = pp.desc_csv()
+    assert L.pp_count_fields(1, 1, ctypes.byref(csv), None, 1, None) == pp.PP_EINVAL
+    assert L.pp_count_fields(1, 1, ctypes.byref(d2), 1, 1, None) == pp.PP_EINVAL
+    assert L.pp_count_fields(1, (1 << 36) + 1, ctypes.byref(csv), 1, 1, None) == pp.PP_ETOOLARGE
+    assert L.pp_count_fields(1, 1, ctypes.byref(csv), 1, None, None) == pp.PP_EINVAL
     assert pp.lib().pp_strerror(pp.PP_EINVAL) == b"invalid argument"
 
 
