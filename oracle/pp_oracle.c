@@ -586,11 +586,55 @@ void or_colofs_combine(int a_abs, uint64_t a_o, int b_abs, uint64_t b_o, int* ab
   else { *abs_out = a_abs; *o_out = a_o + b_o; }
 }
 
+/* Column-count inference per chunk (ParPaRaw Section 4, "Inferring or
+ * validating number of columns"): whether the chunk has a record delimiter,
+ * the field delimiters before its first one (the relative count, all of
+ * them without one), the fewest and most fields of the records that start
+ * after its first record delimiter and end at a later one, and the field
+ * delimiters after its last one.                                          */
+typedef struct { int has_rd; uint64_t pre, post, mn, mx; } or_fagg;
+static void or_fields_chunk(const uint8_t* tags, uint64_t len, or_fagg* a) {
+  uint64_t run = 0;
+  a->has_rd = 0; a->pre = a->post = 0; a->mn = UINT64_MAX; a->mx = 0;
+  for (uint64_t j = 0; j < len; j++) {
+    if (tags[j] == T_FD) { run++; continue; }
+    if (tags[j] != T_RD) continue;
+    if (!a->has_rd) a->pre = run;
+    else {
+      if (run + 1 < a->mn) a->mn = run + 1;
+      if (run + 1 > a->mx) a->mx = run + 1;
+    }
+    a->has_rd = 1;
+    run = 0;
+  }
+  if (a->has_rd) a->post = run; else a->pre = run;
+}
+/* Chunk a followed by chunk b: the record across the seam, when both sides
+ * close it, has a.post + b.pre + 1 fields.                               */
+static void or_fields_combine(const or_fagg* a, const or_fagg* b, or_fagg* o) {
+  or_fagg r;
+  if (!a->has_rd && !b->has_rd) {
+    r = *a; r.pre = a->pre + b->pre;
+  } else if (!a->has_rd) {
+    r = *b; r.pre = a->pre + b->pre;
+  } else if (!b->has_rd) {
+    r = *a; r.post = a->post + b->pre;
+  } else {
+    uint64_t mid = a->post + b->pre + 1;
+    r.has_rd = 1; r.pre = a->pre; r.post = b->post;
+    r.mn = a->mn < b->mn ? a->mn : b->mn; if (mid < r.mn) r.mn = mid;
+    r.mx = a->mx > b->mx ? a->mx : b->mx; if (mid > r.mx) r.mx = mid;
+  }
+  *o = r;
+}
+
 /* Brute force over every string of length 1..max_len on `alpha`: for every
  * chunk size 1..max_len, the scan-derived chunk start states must equal the
- * sequential walk's state at each chunk start, and the scanned column
- * offsets must equal the sequential column index.  Returns the number of
- * mismatches; *checked = strings visited.                                 */
+ * sequential walk's state at each chunk start, the scanned column offsets
+ * must equal the sequential column index, and (CSV, strings without an
+ * invalid byte) the chunks' column-count aggregates combined in order must
+ * give the sequential walk's fewest and most fields per record.  Returns
+ * the number of mismatches; *checked = strings visited.                   */
 uint64_t or_bruteforce(int kind, uint8_t fd, uint8_t rd, uint8_t q, const uint8_t* alpha,
                        int n_alpha, int max_len, uint64_t* checked) {
   uint64_t bad = 0;
@@ -614,10 +658,20 @@ uint64_t or_bruteforce(int kind, uint8_t fd, uint8_t rd, uint8_t q, const uint8_
         if (is_csv(kind)) { if (t == T_RD) col = 0; else if (t == T_FD) col++; }
       }
       (*checked)++;
+      /* sequential fewest / most fields per record (valid strings) */
+      int valid = 1;
+      uint64_t f = 1, smn = UINT64_MAX, smx = 0;
+      for (int i = 0; i < len; i++) {
+        if (tags[i] == T_INVALID) valid = 0;
+        if (tags[i] == T_FD) f++;
+        if (tags[i] == T_RD) { if (f < smn) smn = f; if (f > smx) smx = f; f = 1; }
+      }
+      if (tags[len - 1] != T_RD) { if (f < smn) smn = f; if (f > smx) smx = f; }
       for (int ch = 1; ch <= max_len; ch++) {
         or_chunk_start_states(kind, fd, rd, q, str, (uint64_t)len, (uint64_t)ch, starts);
         int nch = (len + ch - 1) / ch;
         int a_abs = 1; uint64_t a_o = 0;         /* seed: absolute column 0 */
+        or_fagg fa = {1, 0, 0, UINT64_MAX, 0};   /* seed: a record ends before the input */
         for (int c = 0; c < nch; c++) {
           if (starts[c] != seq_state[c * ch]) bad++;
           if (is_csv(kind)) {
@@ -626,7 +680,18 @@ uint64_t or_bruteforce(int kind, uint8_t fd, uint8_t rd, uint8_t q, const uint8_
             int clen = len - c * ch < ch ? len - c * ch : ch;
             or_colofs_chunk(tags + c * ch, (uint64_t)clen, &b_abs, &b_o);
             or_colofs_combine(a_abs, a_o, b_abs, b_o, &a_abs, &a_o);
+            or_fagg fb;
+            or_fields_chunk(tags + c * ch, (uint64_t)clen, &fb);
+            or_fields_combine(&fa, &fb, &fa);
           }
+        }
+        if (is_csv(kind) && valid) {
+          uint64_t mn = fa.mn, mx = fa.mx;
+          if (tags[len - 1] != T_RD) {         /* the open tail is one more record */
+            if (fa.post + 1 < mn) mn = fa.post + 1;
+            if (fa.post + 1 > mx) mx = fa.post + 1;
+          }
+          if (mn != smn || mx != smx) bad++;
         }
       }
       int p = len - 1;
