@@ -22,9 +22,14 @@
  * invalid state, "reading quotes in FLD state").
  *
  * The method's own steps (multi-instance DFA -> state-transition vector,
- * composite operation, exclusive scan; absolute/relative column offsets) are
- * stated separately below (or_stv_*, or_colofs_*) so the tests can check
- * them against the sequential walk on every short input.
+ * composite operation, exclusive scan; absolute/relative column offsets;
+ * the per-chunk column-count aggregate) are stated separately below
+ * (or_stv_*, or_colofs_*, or_fields_*) so the tests can check them against
+ * the sequential walk on every short input.
+ *
+ * Also stated plainly: timestamps (conv_ts: days counted a year and a month
+ * at a time), CRLF line ends (a CR symbol, kind 2) and the fewest and most
+ * fields per record (or_count_fields).
  *
  * The JSON-like lexer DFA (16 states) follows the prefix-scan lexing scheme
  * of "Lexing on the GPU: the scan is the easy part" (section "A lexer is a
