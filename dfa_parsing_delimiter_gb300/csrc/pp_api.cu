@@ -10,6 +10,26 @@
 #include "pp_internal.h"
 
 namespace ppi {
+
+cudaError_t current_device(int* dev) {
+  const cudaError_t e = cudaGetDevice(dev);
+  if (e != cudaSuccess) return e;
+  return (*dev >= 0 && *dev < MAX_DEVICES) ? cudaSuccess : cudaErrorInvalidDevice;
+}
+
+cudaError_t sm_count(int* out) {
+  static DeviceOnce once;
+  static int n_sm[MAX_DEVICES];
+  int dev;
+  cudaError_t e = current_device(&dev);
+  if (e != cudaSuccess) return e;
+  e = once.run(dev, [](int d) {
+    return cudaDeviceGetAttribute(&n_sm[d], cudaDevAttrMultiProcessorCount, d);
+  });
+  if (e == cudaSuccess) *out = n_sm[dev];
+  return e;
+}
+
 uint32_t g_spin_limit = 1u << 22;  // ~1 s of polling before a look-back gives up
 uint32_t g_withhold = 0;           // test hook, see pp_debug_set_withhold
 

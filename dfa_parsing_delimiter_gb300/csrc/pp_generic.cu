@@ -281,13 +281,8 @@ cudaError_t run(void (*kern)(GParams), size_t dyn_smem, const GParams& P, void* 
       static_cast<uint4*>(scratch), n16, P.st);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || P.n_tiles == 0) return e;
-  static int n_sm = 0;
-  if (!n_sm) {
-    int dev;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-      return e;
-  }
+  int n_sm = 0;
+  if ((e = ppi::sm_count(&n_sm)) != cudaSuccess) return e;
   if (dyn_smem > 0 &&
       (e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(dyn_smem))) !=
           cudaSuccess)
@@ -328,13 +323,8 @@ cudaError_t launch_count_byte(const uint8_t* in, uint64_t n, uint8_t value, uint
                               cudaStream_t stream) {
   cudaError_t e = cudaMemsetAsync(d_count, 0, sizeof(uint64_t), stream);
   if (e != cudaSuccess || n == 0) return e;
-  static int n_sm = 0;
-  if (!n_sm) {
-    int dev;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-      return e;
-  }
+  int n_sm = 0;
+  if ((e = ppi::sm_count(&n_sm)) != cudaSuccess) return e;
   const uint64_t want = (n / 16 + 255) / 256;
   const int blocks = int(std::min<uint64_t>(want ? want : 1, uint64_t(n_sm) * 8));
   count_byte_kernel<<<blocks, 256, 0, stream>>>(in, n, value, d_count);

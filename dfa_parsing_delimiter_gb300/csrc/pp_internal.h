@@ -1,10 +1,43 @@
 // Host/device shared definitions of libpp (not part of the public ABI).
 #pragma once
+#include <atomic>
 #include <cstdint>
+#include <mutex>
 #include <cuda_runtime_api.h>
 #include "pp.h"
 
 namespace ppi {
+
+// ------------------------------------------------------- per-device set-up
+// Kernel attributes (cudaFuncSetAttribute) and occupancy belong to a device
+// (its primary context, the one the runtime API uses), so every launcher
+// keeps its set-up per device ordinal.  DeviceOnce runs a set-up function
+// once per device, safely for concurrent host threads: the state it fills
+// is published by a release store and read after an acquire load.  A
+// set-up that fails is tried again by the next call.
+constexpr int MAX_DEVICES = 64;
+
+// The current device's ordinal (cudaErrorInvalidDevice beyond MAX_DEVICES).
+cudaError_t current_device(int* dev);
+// Streaming multiprocessors of the current device.
+cudaError_t sm_count(int* out);
+
+class DeviceOnce {
+ public:
+  template <class F>
+  cudaError_t run(int dev, F&& setup) {
+    if (done_[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    std::lock_guard<std::mutex> g(m_);
+    if (done_[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+    const cudaError_t e = setup(dev);
+    if (e == cudaSuccess) done_[dev].store(true, std::memory_order_release);
+    return e;
+  }
+
+ private:
+  std::mutex m_;
+  std::atomic<bool> done_[MAX_DEVICES] = {};
+};
 
 constexpr int MAX_STR_COLS = 16;  // string columns per pp_parse call
 

@@ -1950,33 +1950,49 @@ __global__ void parse_init_kernel(ParseParams P) {
   }
 }
 
-struct Occ { int ctx = -1, main = -1, n_sm = 0; };
+struct Occ { int ctx = 1, main = 1, n_sm = 0; };
+
+// Per device: the SM count, the dynamic shared-memory attributes of the two
+// big tile passes and their resident blocks per SM.
+template <int NS>
+cudaError_t parse_setup(Occ** out) {
+  static ppi::DeviceOnce once;
+  static Occ occ[ppi::MAX_DEVICES];
+  int dev;
+  cudaError_t e = ppi::current_device(&dev);
+  if (e != cudaSuccess) return e;
+  e = once.run(dev, [](int d) {
+    Occ o;
+    cudaError_t r;
+    if ((r = ppi::sm_count(&o.n_sm)) != cudaSuccess) return r;
+    if ((r = cudaFuncSetAttribute(ctx_kernel<NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  int(CTX_SMEM))) != cudaSuccess)
+      return r;
+    if ((r = cudaFuncSetAttribute(main_kernel<NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  int(MAIN_SMEM))) != cudaSuccess)
+      return r;
+    int b = 0;
+    if ((r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, ctx_kernel<NS>, NT, CTX_SMEM)) !=
+        cudaSuccess)
+      return r;
+    o.ctx = b > 0 ? b : 1;
+    if ((r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, main_kernel<NS>, NT, MAIN_SMEM)) !=
+        cudaSuccess)
+      return r;
+    o.main = b > 0 ? b : 1;
+    occ[d] = o;
+    return cudaSuccess;
+  });
+  *out = &occ[dev];
+  return e;
+}
 
 template <int NS>
 cudaError_t launch_ns(const ParseParams& p, cudaStream_t stream) {
-  static Occ occ;
-  cudaError_t e;
-  if (occ.main < 0) {
-    int dev;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&occ.n_sm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-      return e;
-    if ((e = cudaFuncSetAttribute(ctx_kernel<NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  int(CTX_SMEM))) != cudaSuccess)
-      return e;
-    if ((e = cudaFuncSetAttribute(main_kernel<NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  int(MAIN_SMEM))) != cudaSuccess)
-      return e;
-    int b = 0;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, ctx_kernel<NS>, NT, CTX_SMEM)) !=
-        cudaSuccess)
-      return e;
-    occ.ctx = b > 0 ? b : 1;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, main_kernel<NS>, NT, MAIN_SMEM)) !=
-        cudaSuccess)
-      return e;
-    occ.main = b > 0 ? b : 1;
-  }
+  Occ* po = nullptr;
+  cudaError_t e = parse_setup<NS>(&po);
+  if (e != cudaSuccess) return e;
+  const Occ& occ = *po;
   const bool timed = ppi::stage_begin();
   if (timed) ppi::stage_mark(0, stream);
   parse_init_kernel<<<std::max<uint32_t>(1, std::min<uint32_t>((p.s.n_scan_blocks + 255) / 256, 1024)),
@@ -2016,22 +2032,25 @@ uint32_t ctx_stride_of(int ns, int n_cols) {
 uint32_t pre_stride_of(int ns) { return uint32_t(PRE_HDR + 8 * (ns > 0 ? ns : 0)); }
 
 cudaError_t launch_fields(const ParseParams& p, FAgg* agg, uint64_t* out, cudaStream_t stream) {
-  static int n_sm = 0, occ = 0;
+  static ppi::DeviceOnce once;
+  static int occ_of[ppi::MAX_DEVICES];
+  int dev, n_sm = 0;
   cudaError_t e;
-  if (!occ) {
-    int dev;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-      return e;
-    if ((e = cudaFuncSetAttribute(fields_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  int(FIELDS_SMEM))) != cudaSuccess)
-      return e;
+  if ((e = ppi::current_device(&dev)) != cudaSuccess) return e;
+  if ((e = ppi::sm_count(&n_sm)) != cudaSuccess) return e;
+  e = once.run(dev, [](int d) {
+    cudaError_t r = cudaFuncSetAttribute(fields_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(FIELDS_SMEM));
+    if (r != cudaSuccess) return r;
     int b = 0;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fields_kernel, NT, FIELDS_SMEM)) !=
+    if ((r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fields_kernel, NT, FIELDS_SMEM)) !=
         cudaSuccess)
-      return e;
-    occ = b > 0 ? b : 1;
-  }
+      return r;
+    occ_of[d] = b > 0 ? b : 1;
+    return cudaSuccess;
+  });
+  if (e != cudaSuccess) return e;
+  const int occ = occ_of[dev];
   parse_init_kernel<<<1, 256, 0, stream>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (p.n_tiles) {

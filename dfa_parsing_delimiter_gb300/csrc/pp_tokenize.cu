@@ -840,20 +840,15 @@ cudaError_t launch_tokenize(const uint8_t* in, uint64_t n, const GenericDfa& dfa
   cudaError_t e = cudaGetLastError();
   if (timed) stage_mark(1, stream);
   if (e != cudaSuccess || P.n_pieces == 0) return e;
-  static int n_sm = 0;
-  if (!n_sm) {
-    int dev;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-      return e;
-  }
-  static bool attrs = false;
-  if (!attrs) {
-    if ((e = cudaFuncSetAttribute(tok_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  int(sizeof(RepTables)))) != cudaSuccess)
-      return e;
-    attrs = true;
-  }
+  int n_sm = 0, dev = 0;
+  if ((e = sm_count(&n_sm)) != cudaSuccess) return e;
+  if ((e = current_device(&dev)) != cudaSuccess) return e;
+  static DeviceOnce attrs;
+  e = attrs.run(dev, [](int) {
+    return cudaFuncSetAttribute(tok_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                int(sizeof(RepTables)));
+  });
+  if (e != cudaSuccess) return e;
   const uint32_t bgrid = std::min<uint32_t>((P.n_pieces + WW - 1) / WW, uint32_t(n_sm) * 4);
   const uint32_t dgrid = std::min<uint32_t>((P.n_pieces + DW - 1) / DW, uint32_t(n_sm) * 2);
   tok_stv_kernel<<<bgrid, WT, 0, stream>>>(P);

@@ -18,6 +18,10 @@
  * Section 4.3).
  *
  * Conventions for every entry point:
+ *  - Per-device set-up (kernel attributes, SM counts) is done once per
+ *    device ordinal, on the first call made with that device current, and
+ *    is safe to reach from several host threads at once.  It applies to
+ *    the device's primary context, the one the CUDA runtime API uses.
  *  - Pointers named d_* and out_* are DEVICE pointers; everything else
  *    (descriptors, column-type arrays, capacity arrays, pointer arrays) is
  *    HOST memory, read during the call only.
@@ -242,13 +246,17 @@ pp_rc pp_tokenize_host(const uint8_t* h_in, size_t n_bytes, const pp_dfa_desc* d
  *   First call on each device: it looks up the buffer's address
  *   (cudaGetSymbolAddress; this can load the library's device code) and
  *   sets kernel attributes.  Make that first call before any stream
- *   capture starts on the device.
+ *   capture starts on the device.  The address is kept per device ordinal
+ *   and belongs to the device's primary context, the one the CUDA runtime
+ *   API uses; a caller that switches the device to another context (driver
+ *   API) must not call this entry point from that context.
  *   Calls share the buffer: two calls in flight on one device at the same
  *   time (on different streams, or from host threads with no ordering
  *   between them) race on it and corrupt each other's results.  Issue the
  *   calls on one stream, or order them by events or synchronisation.
- * Returns PP_EINVAL for bad arguments, PP_ETOOLARGE as above, PP_ECUDA on
- * CUDA errors.
+ * Returns PP_EINVAL for bad arguments, PP_ETOOLARGE as above, PP_ENOMEM
+ * when a launch reports cudaErrorMemoryAllocation (the kernels' own
+ * resources; the call allocates no memory), PP_ECUDA on other CUDA errors.
  */
 pp_rc pp_parse_noalloc(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa, int n_cols,
                        const pp_coltype* col_types, int32_t* const out_offsets[],

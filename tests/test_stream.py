@@ -1,16 +1,22 @@
-"""pp_parse_host (host input and outputs, streamed through the device in
-chunks) against pp_parse on the same bytes: status and every output column
-equal, for chunk sizes that put chunk boundaries inside quoted fields,
-inside quoted newlines and inside records, and for the edge cases of the
-carry-over (no trailing newline, empty input, a record longer than the
-chunk, errors in later chunks)."""
+"""pp_parse_host and pp_tokenize_host (host input and outputs, streamed
+through the device in chunks) against the oracle on the same bytes, element
+by element (integers, offsets, chars and token triples bit-exact, floats
+within 1 ulp with the same sign), and against pp_parse / pp_tokenize: for
+chunk sizes that put chunk boundaries inside quoted fields, inside quoted
+newlines, between a CR and its LF and inside records, and for the edge cases
+of the carry-over (no trailing newline, empty input, a record or token
+longer than the chunk, errors in later chunks).  The streamed calls run
+kernel modes a single pp_parse never runs (a chunk whose last record stays
+open, the carried partial record, offsets rebased on the device), so the
+oracle, not the library, is the reference."""
 import numpy as np
 import pytest
 import torch
 
 import datagen
 import dfa_parsing_delimiter_gb300 as pp
-from gpu_util import to_dev
+import oracle as O
+from gpu_util import to_dev, ulp_diff
 
 pytestmark = pytest.mark.gpu
 
@@ -55,6 +61,29 @@ def _assert_same(col_types, dev, sdev, host, shost):
             assert torch.equal(rd[c].cpu(), rh[c]), f"col {c}"
 
 
+def _assert_oracle(arr, col_types, host, shost, crlf=False):
+    """Streamed outputs equal the oracle's for the same bytes."""
+    ref, rst = O.csv_parse(arr, col_types, crlf=crlf)
+    assert shost["error"] == rst["error"], (shost, rst)
+    assert shost["first_error_offset"] == rst["first_error_offset"], (shost, rst)
+    if rst["error"] & O.FATAL:
+        return
+    assert shost["n_records"] == rst["n_records"]
+    got = host.results(shost)
+    for c, t in enumerate(col_types):
+        if t == "str":
+            assert shost["chars_len"][c] == rst["chars_len"][c], c
+            assert np.array_equal(got[c][0].numpy(), ref[c][0]), f"offsets col {c}"
+            assert np.array_equal(got[c][1].numpy(), ref[c][1]), f"chars col {c}"
+        elif t == "f64":
+            g = got[c].numpy()
+            d = ulp_diff(g, ref[c])
+            assert d.size == 0 or int(d.max()) <= 1, f"f64 col {c}: {d.max()} ulp"
+            assert np.array_equal(np.signbit(g), np.signbit(ref[c]))
+        elif t != "skip":
+            assert np.array_equal(got[c].numpy(), ref[c]), f"col {c}"
+
+
 @pytest.mark.parametrize("name,target,chunk", [
     ("csv4_1mib", None, 16 << 10),       # quoted newlines across many boundaries
     ("csv4_1mib", None, 96 << 10),
@@ -70,6 +99,7 @@ def test_host_stream_matches_device_parse(name, target, chunk):
     dev, sdev, R = _device_run(data, col_types, desc)
     assert sdev["error"] == 0 and sdev["n_records"] == info["n_records"]
     host, shost = _host_run(data, col_types, desc, R, chunk)
+    _assert_oracle(data, col_types, host, shost)
     _assert_same(col_types, dev, sdev, host, shost)
 
 
@@ -82,6 +112,7 @@ def test_host_stream_without_trailing_newline_and_empty():
     dev, sdev, R = _device_run(arr, col_types, desc)
     assert sdev["error"] == 0 and sdev["n_records"] == 5000
     host, shost = _host_run(arr, col_types, desc, R, 16 << 10)
+    _assert_oracle(arr, col_types, host, shost)
     _assert_same(col_types, dev, sdev, host, shost)
     empty = np.zeros(0, np.uint8)
     host, shost = _host_run(empty, col_types, desc, 1, 16 << 10)
@@ -102,6 +133,7 @@ def test_host_stream_reports_errors_at_global_offsets():
     host, shost = _host_run(arr, col_types, desc, R, 32 << 10)
     assert shost["error"] & pp.ERR_INVALID_INPUT
     assert shost["first_error_offset"] == sdev["first_error_offset"] == p + 1
+    _assert_oracle(arr, col_types, host, shost)
 
 
 def test_host_stream_rejects_record_longer_than_chunk():
@@ -132,6 +164,15 @@ def _device_tokens(arr, desc):
     return (ids[:T].cpu(), starts[:T].cpu(), lens[:T].cpu()), s
 
 
+def _assert_tokens_oracle(arr, triples, sh):
+    (rids, rstarts, rlens), rst = O.tokenize(arr)
+    assert sh["error"] == rst["error"] and sh["n_tokens"] == rst["n_tokens"], (sh, rst)
+    hi, hs, hl = triples
+    assert np.array_equal(hi.numpy(), rids)
+    assert np.array_equal(hs.numpy().astype(np.uint64), rstarts)
+    assert np.array_equal(hl.numpy().astype(np.uint32), rlens)
+
+
 def _host_tokens(arr, desc, cap, chunk):
     h_in = torch.empty(max(arr.size, 1), dtype=torch.uint8, pin_memory=True)
     if arr.size:
@@ -149,6 +190,7 @@ def test_host_tokens_match_device_tokens(target, chunk):
     assert sd["error"] == 0 and sd["n_tokens"] == info["n_tokens"]
     (hi, hs, hl), sh, _ = _host_tokens(data, desc, sd["n_tokens"], chunk)
     assert sh["error"] == 0 and sh["n_tokens"] == sd["n_tokens"]
+    _assert_tokens_oracle(data, (hi, hs, hl), sh)
     assert torch.equal(hi, di) and torch.equal(hs, ds_) and torch.equal(hl, dl)
 
 
@@ -162,6 +204,7 @@ def test_host_tokens_dense_long_and_errors():
     assert sd["error"] == 0
     (hi, hs, hl), sh, _ = _host_tokens(arr, desc, sd["n_tokens"], 48 << 10)
     assert sh["n_tokens"] == sd["n_tokens"] and sh["error"] == 0
+    _assert_tokens_oracle(arr, (hi, hs, hl), sh)
     assert torch.equal(hi, di) and torch.equal(hs, ds_) and torch.equal(hl, dl)
     # a token longer than the chunk
     with pytest.raises(RuntimeError, match=r"pp_tokenize_host failed: .*\(5\)"):
@@ -176,6 +219,8 @@ def test_host_tokens_dense_long_and_errors():
     _, sh, _ = _host_tokens(arr, desc, max(sd["n_tokens"], 1), 16 << 10)
     assert sh["error"] & pp.ERR_INVALID_INPUT
     assert sh["first_error_offset"] == sd["first_error_offset"]
+    _, rst = O.tokenize(arr)
+    assert (sh["error"], sh["first_error_offset"]) == (rst["error"], rst["first_error_offset"])
 
 
 def test_host_stream_timestamps_and_crlf():
@@ -187,6 +232,7 @@ def test_host_stream_timestamps_and_crlf():
     dev, sdev, R = _device_run(data, col_types, desc)
     assert sdev["error"] == 0 and sdev["n_records"] == info["n_records"]
     host, shost = _host_run(data, col_types, desc, R, 256 << 10)
+    _assert_oracle(data, col_types, host, shost)
     _assert_same(col_types, dev, sdev, host, shost)
     crlf = np.frombuffer(bytes(data).replace(b"\n", b"\r\n"), dtype=np.uint8)
     cdesc = pp.desc_csv_crlf()
@@ -194,4 +240,5 @@ def test_host_stream_timestamps_and_crlf():
     assert sdev["error"] == 0 and sdev["n_records"] == info["n_records"]
     for chunk in (256 << 10, (256 << 10) + 1):
         host, shost = _host_run(crlf, col_types, cdesc, R, chunk)
+        _assert_oracle(crlf, col_types, host, shost, crlf=True)
         _assert_same(col_types, dev, sdev, host, shost)

@@ -1,7 +1,11 @@
 """pp_parse_noalloc (pp_parse with its scratch in a fixed buffer compiled
-into the library) against pp_parse on the same inputs: two calls in a row,
-each equal to pp_parse's result (integers, offsets and chars exactly,
-floats within 1 ulp), and inputs too large for the buffer rejected.
+into the library) against the oracle and against pp_parse on the same
+inputs: two calls in a row, each equal to the oracle's result and to
+pp_parse's (integers, offsets and chars exactly, floats within 1 ulp), and
+inputs too large for the buffer rejected.  The no-alloc call runs the
+parse's own kernels with scratch carved from the fixed buffer; comparing
+with the oracle as well keeps a fault the two calls share from passing
+unnoticed.
 
 Named to be collected last, so it also runs after every other test has used
 the library in the same process."""
@@ -11,6 +15,7 @@ import torch
 
 import datagen
 import dfa_parsing_delimiter_gb300 as pp
+import oracle as O
 from gpu_util import to_dev, ulp_diff
 
 pytestmark = pytest.mark.gpu
@@ -40,6 +45,25 @@ def _assert_same(a, sa, b, sb, col_types):
             assert torch.equal(ra[c], rb[c]), f"col {c}"
 
 
+def _assert_oracle(data, col_types, out, st):
+    ref, rst = O.csv_parse(data, col_types)
+    assert st["error"] == rst["error"] == 0, (st, rst)
+    assert st["n_records"] == rst["n_records"]
+    got = out.results(st)
+    for c, t in enumerate(col_types):
+        if t == "str":
+            assert st["chars_len"][c] == rst["chars_len"][c], c
+            assert np.array_equal(got[c][0].cpu().numpy(), ref[c][0]), f"offsets col {c}"
+            assert np.array_equal(got[c][1].cpu().numpy(), ref[c][1]), f"chars col {c}"
+        elif t == "f64":
+            g = got[c].cpu().numpy()
+            d = ulp_diff(g, ref[c])
+            assert d.size == 0 or int(d.max()) <= 1, f"f64 col {c}"
+            assert np.array_equal(np.signbit(g), np.signbit(ref[c]))
+        elif t != "skip":
+            assert np.array_equal(got[c].cpu().numpy(), ref[c]), f"col {c}"
+
+
 @pytest.mark.parametrize("name,target", [
     ("csv4_1mib", None),
     ("csv16_256mib", 3 << 20),
@@ -62,7 +86,9 @@ def test_noalloc_matches_pp_parse_on_two_calls_in_a_row(name, target):
     second.run_noalloc(d_in, n, desc)   # same stream, right after the first
     torch.cuda.synchronize()
     for out in (first, second):
-        _assert_same(ref, sref, out, pp.read_status(out.status, len(col_types)), col_types)
+        st = pp.read_status(out.status, len(col_types))
+        _assert_oracle(data, col_types, out, st)
+        _assert_same(ref, sref, out, st, col_types)
 
 
 def test_noalloc_sizing_pass_matches():
