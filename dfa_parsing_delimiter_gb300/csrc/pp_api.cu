@@ -229,6 +229,8 @@ pp_rc parse_prepare(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa,
   }
   p.in = d_in;
   p.n = n_bytes;
+  // positions and record counts travel in 40 bits through the tile pass's look-back
+  if (uint64_t(n_bytes) >= (1ull << 40)) return PP_ETOOLARGE;
   const uint64_t tile = ppi::parse_tile_bytes();
   const uint64_t nt = (uint64_t(n_bytes) + tile - 1) / tile;
   if (nt > 0xFFFFFFF0ull) return PP_EINVAL;
@@ -415,11 +417,11 @@ pp_rc pp_parse(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa, int 
                                       d_status, &p);
   if (rc != PP_OK) return rc;
   const int ns = ppi::parse_ns_width(p.n_str);
-  const size_t sb = ppi::parse_scratch_bytes(p.n_tiles, ns, n_cols, true);
+  const size_t sb = ppi::parse_scratch_bytes(p.n_tiles, ns);
   void* scratch = nullptr;
   cudaError_t e = cudaMallocAsync(&scratch, sb, stream);
   if (e != cudaSuccess) return cuda_rc(e);
-  ppi::parse_scratch_carve(scratch, p.n_tiles, ns, n_cols, true, &p.s);
+  ppi::parse_scratch_carve(scratch, p.n_tiles, ns, &p.s);
   e = ppi::launch_parse(p, stream);
   const cudaError_t ef = cudaFreeAsync(scratch, stream);
   if (e == cudaSuccess) e = ef;

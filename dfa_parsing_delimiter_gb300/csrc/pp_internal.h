@@ -42,43 +42,24 @@ class DeviceOnce {
 constexpr int MAX_STR_COLS = 16;  // string columns per pp_parse call
 
 // Scratch of one pp_parse call (device memory).
-//   ctx:  per tile, written by the context pass: transition vector and, for
-//         each of the 4 live start states, record count, column offset,
-//         last terminator, value bytes per string column (absolute
-//         columns) and per relative field of the first partial record.
-//   pre:  per tile, written by the scan: start state, record index, column,
-//         last terminator before the tile, chars offset per string column.
-//   scan_*: cross-block look-back state of the scan kernel (a: contexts,
-//         c: chars offsets).
-//   tile_stv, tile_state: per tile, its transition vector and its true
-//         start state (from the tile-state scan, whose look-back words are
+//   tile_stv, tile_state: per tile, its transition vector and its true start
+//         state (from the tile-state scan, whose look-back words are
 //         tstate_words).
+//   v2_desc: the tile pass's look-back over (record count, last
+//         terminator, column offset): a 16-byte descriptor per tile.
+//   c_*:  its look-back over the value bytes per string column: per tile a
+//         flag and ns-word aggregate / inclusive prefix (null without string
+//         columns).
 struct ParseScratch {
-  uint8_t* ctx;
-  uint8_t* pre;
-  uint32_t ctx_stride, pre_stride;
-  uint32_t* counters;       // [0] context pass, [1] main pass, [2] scan, [3] tile-state scan tickets
+  uint32_t* counters;       // [0] tile tickets, [2] column-count end flag, [3] tile-state scan tickets
   uint32_t* tile_stv;       // [n_tiles]
   uint8_t* tile_state;      // [n_tiles]
   unsigned long long* tstate_words;  // [n_tstate_blocks]
   uint32_t n_tstate_blocks;
-  // [n_tiles * 512], per 32-byte chunk, written by the context pass for the
-  // main pass: FD, RD and control bitmaps, and (1 + the position in the tile
-  // of the chunk's last terminator) | end state << 16.  Null when the
-  // scratch has no room for them: the main pass then tags again.
-  uint4* tags;
-  // [n_tiles * 512], with tags: the chunk's (records, column, last
-  // terminator) prefix in the tile: records | (1 + last position) << 16,
-  // column (15 bits) | 0x8000 if absolute.
-  uint2* vpre;
-  uint8_t* tile_flags;  // [n_tiles]: 1 if the tile has control bytes
-  uint32_t* scan_flag_a;    // [n_scan_blocks]
-  uint64_t* scan_agg_a;     // [n_scan_blocks][13]
-  uint64_t* scan_inc_a;
-  uint32_t* scan_flag_c;    // [n_scan_blocks]
-  uint64_t* scan_agg_c;     // [n_scan_blocks][ns]
-  uint64_t* scan_inc_c;
-  uint32_t n_scan_blocks;
+  uint64_t* v2_desc;        // [n_tiles][2]
+  uint32_t* c_flag;         // [n_tiles]
+  uint64_t* c_agg;          // [n_tiles][ns]
+  uint64_t* c_inc;
 };
 
 struct ParseParams {
@@ -86,7 +67,7 @@ struct ParseParams {
   uint64_t n;
   uint32_t n_tiles;
   uint32_t spin_limit;
-  uint32_t dbg_withhold;  // test hook: the first scan block posts nothing
+  uint32_t dbg_withhold;  // test hook: the first tile posts nothing to the look-backs
   uint32_t lut[256];      // per byte: STV selector, next-state/tag fields, special bit
   uint32_t bg_next;       // nibble s = delta[background][s], s = 0..4
   uint32_t sticky;        // state whose non-inert groups set LUT bit 30 (4: none)
@@ -117,13 +98,11 @@ struct ParseParams {
 
 // bytes of scratch for n_tiles tiles and ns string columns (ns rounded to the
 // kernel's instantiation width)
-// (tags: with room for the per-chunk tags and prefixes, 12 KiB per tile)
-size_t parse_scratch_bytes(uint32_t n_tiles, int ns, int n_cols, bool tags);
-void parse_scratch_carve(void* base, uint32_t n_tiles, int ns, int n_cols, bool tags,
-                         ParseScratch* out);
+size_t parse_scratch_bytes(uint32_t n_tiles, int ns);
+void parse_scratch_carve(void* base, uint32_t n_tiles, int ns, ParseScratch* out);
 int parse_ns_width(int n_str);
 
-// init (counters, scan flags, status), context pass, scan, main pass
+// init (counters, look-back flags, status), tile vectors, tile states, tile pass
 cudaError_t launch_parse(const ParseParams& p, cudaStream_t stream);
 // Stage timing (benchmark hook): stage_begin() opens the record of one
 // call (false if recording is off or full); stage_mark(k) records its

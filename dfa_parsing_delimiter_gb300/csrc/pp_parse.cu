@@ -1,12 +1,8 @@
 // pp_parse: DFA-based parsing of delimiter-separated input into Arrow-style
-// columns on sm_103a, in five kernels with no inter-tile waiting on the
-// byte-level hot path.
+// columns on sm_103a, in three kernels.
 //
-// The input is cut into 16 KiB tiles.  In the two tile passes a tile is one
-// CTA of 512 threads and each thread owns a 32-byte chunk (one bit per byte
-// in the bitmap indexes).  Tiles reach shared memory by a 1-D bulk copy
-// (TMA engine) into one of two linear buffers, the next tile's copy running
-// while the current one is processed.
+// The input is cut into 16 KiB tiles; each thread of the tile pass owns a
+// 32-byte chunk (one bit per byte in the bitmap indexes).
 //
 // 0. Tile start states (tile_stv_kernel, tile_state_kernel).  A warp per
 //    tile folds the tile's transition vector (ParPaRaw Section 3.1, Figure
@@ -16,30 +12,22 @@
 //    Section 5, Table 1, read from a per-lane replicated shared-memory LUT).
 //    An exclusive composite scan over tiles gives every tile's true start
 //    state.
-// 1. Context pass (ctx_kernel).  Each thread folds its chunk's vector the
-//    same way; vectors compose across the warp (shuffles) and the block,
-//    which with the tile's start state gives every chunk's start state.
-//    The thread then tags its chunk (one DFA over the non-background bytes
-//    only) and the tile records, for its true start state: record count,
-//    absolute or relative column offset (ParPaRaw Section 3.2, Figure 4),
-//    last terminator, value bytes per string column for fields whose column
-//    is known inside the tile, and value bytes per relative field of the
-//    tile's first, partial record.  With room in the scratch it also stores
-//    every chunk's tag bitmaps and its (record, column, last terminator)
-//    prefix inside the tile for the main pass.
-// 2. Scan (scan_kernel).  An exclusive scan over tiles with the record-count
-//    / column-offset operators (Section 3.2) resolves every tile's record
-//    index, column and last terminator; the tile's value bytes per string
-//    column then follow from its column, and a second scan turns them into
-//    chars offsets.  Blocks chain by a single-pass decoupled look-back.
-// 3. Main pass (main_kernel).  With its context known, each tile loads its
-//    chunks' tags and prefixes (or, without them, tags again and scans the
-//    block), enters every closed field in a column-major (column, record)
-//    slot table, compacts string value bytes per column into shared memory
-//    (stream compaction in place of ParPaRaw's radix partitioning, Section
-//    3.3) and writes them as 16-byte stores; one lane per field then writes
-//    the Arrow offset or converts the number (Section 3.3), 32 consecutive
-//    rows of a column to a warp for coalesced stores.
+// 1. Tile pass (parse_kernel).  Tiles reach shared memory by a 1-D bulk copy
+//    (TMA engine), the next tile's copy running while the current one is
+//    processed.  Per tile: chunk vectors composed across the block give every
+//    chunk's start state; one DFA per thread tags its chunk (the three bitmap
+//    indexes of Section 3.1); record counts and absolute/relative column
+//    offsets (Section 3.2, Figure 4) are scanned over the tile and then across
+//    tiles by a decoupled look-back run by a dedicated scan warp, as are the
+//    value bytes per string column; every closed field goes into a
+//    column-major (column, record) slot table in shared memory; string value
+//    bytes are compacted per column into shared memory (stream compaction in
+//    place of ParPaRaw's radix partitioning, Section 3.3) and written as
+//    16-byte stores, one lane per field writes the Arrow offset or converts
+//    the number (Section 3.3), 32 consecutive rows of a column to a warp for
+//    coalesced stores.  Each input byte is read twice from HBM (once per
+//    pass) and every output byte written once; no per-byte intermediate
+//    reaches HBM.
 #include <cstdint>
 #include <cuda_runtime.h>
 #include <algorithm>
@@ -63,9 +51,6 @@ constexpr int SLOT_CAP = 4096;         // (column, record) slots per pass
 constexpr uint32_t ABS32 = 1u << 31;
 constexpr uint32_t SLOT_DEFAULT = 0xFFFFFFFDu; // missing field: column default
 constexpr uint32_t WAIT_LIMIT = 1u << 24;      // bounded mbarrier polls
-constexpr int SCAN_NT = 256;           // scan kernel threads
-constexpr int SCAN_TPT = 8;            // tiles per scan thread
-constexpr int SCAN_TILES = SCAN_NT * SCAN_TPT;
 
 // ------------------------------------------------------------ helpers
 // (record count, column offset, last terminator) of a byte range; column
@@ -120,13 +105,6 @@ __device__ __forceinline__ uint32_t popc_range(const uint32_t* m, uint32_t a, ui
     a = (w + 1) << 5;
   }
   return n;
-}
-
-// control bytes before tile position p (p <= tile length)
-__device__ __forceinline__ uint32_t ctrl_before(const uint32_t* ctrl_s, const uint16_t* cpre,
-                                                uint32_t p) {
-  const uint32_t w = p >> 5, b = p & 31u;
-  return cpre[w] + (b ? uint32_t(__popc(ctrl_s[w] & ((1u << b) - 1u))) : 0u);
 }
 
 // ------------------------------------------------- tile feeding (TMA)
@@ -351,12 +329,13 @@ __device__ __forceinline__ V2 chunk_v2(const Tags& g) {
 // accumulator; returns the number of value bytes.  A field inside the tile
 // reads the tile copy (skipping control bytes by the control bitmap); a
 // field that began in an earlier tile is re-read from global memory and
-// re-tagged by running the DFA from the state at its first byte.
+// re-tagged by running the DFA from the state at its first byte (lut: one
+// LUT entry per byte value).
 template <class Acc>
 __device__ __forceinline__ uint32_t feed_field(Acc& acc, const uint8_t* in, uint64_t fs,
                                                uint64_t fe, uint64_t tile_base,
                                                const uint8_t* tile_s, const uint32_t* ctrl_s,
-                                               const uint32_t* my_lut, uint32_t fstate) {
+                                               const uint32_t* lut, uint32_t fstate) {
   uint32_t ndata = 0;
   if (fs >= tile_base) {
     const uint32_t a = uint32_t(fs - tile_base), e = uint32_t(fe - tile_base);
@@ -375,7 +354,7 @@ __device__ __forceinline__ uint32_t feed_field(Acc& acc, const uint8_t* in, uint
     for (uint64_t p = fs; p < fe; ++p) {
       const uint32_t b = p >= tile_base ? tile_byte(tile_s, uint32_t(p - tile_base))
                                         : uint32_t(__ldg(in + p));
-      const uint32_t e = my_lut[b << 5];
+      const uint32_t e = lut[b];
       const uint32_t tg = (e >> (20 + 2 * s)) & 3u;
       s = (e >> (4 * s)) & 0xFu;
       if (tg == uint32_t(PP_TAG_CTRL)) continue;
@@ -388,8 +367,8 @@ __device__ __forceinline__ uint32_t feed_field(Acc& acc, const uint8_t* in, uint
 
 // ---------------------------------------------- word access to the tile
 __device__ __forceinline__ uint32_t tile_word(const uint32_t* tile_w, uint32_t q) { return tile_w[q]; }
-// 8 bytes of the tile from position p (little-endian: byte p lowest); bytes
-// past the tile are unspecified but stay inside shared memory.
+// 8 bytes of a buffer from byte position p (little-endian: byte p lowest);
+// bytes past the tile are unspecified but stay inside shared memory.
 __device__ __forceinline__ uint64_t tile_load8(const uint32_t* tile_w, uint32_t p) {
   const uint32_t q = p >> 2, sh = (p & 3u) * 8u;
   const uint32_t w0 = tile_word(tile_w, q), w1 = tile_word(tile_w, q + 1),
@@ -519,573 +498,6 @@ __global__ void __launch_bounds__(TS_NT) tile_state_kernel(const __grid_constant
     }
 }
 
-// ================================================================ 1. context
-struct CtxShared {
-  Feed F;
-  uint32_t tile_stv;
-  uint32_t warp_stv[NW];
-  uint32_t wv[NW][3];         // per warp: (records, column, last) of the warp
-  uint32_t wpre[NW][3];       // per warp: the same over the earlier warps
-  uint64_t wcnt[NW][4];       // per warp: packed value bytes per string column
-  uint32_t rel[PP_MAX_COLS];  // value bytes of relative field k
-  uint32_t wrd[NW];           // partial mode: per warp, 1 + its last record delimiter in the tile
-  int8_t stridx[PP_MAX_COLS];
-};
-constexpr size_t CTX_SMEM = LUT_BYTES + 2 * TILE + sizeof(CtxShared);
-constexpr int CTX_HDR = 52;  // transition vector + (records, column, last) per start state
-
-// Per tile, from the tile's true start state: the record count, column
-// offset and last terminator of the tile (ParPaRaw Sections 3.1-3.2), plus
-// the value bytes per string column of the fields whose column the tile
-// fixes, and per relative field of the tile's first, partial record (its
-// column is only known from the scan).  The record has a slot per start
-// state, as the scan composes them; only the true state's slot is filled
-// and the others are zero: the scan reads a tile's slots only along the path
-// from the input's start state, which enters every tile in its true state.
-template <int NS>
-__global__ void __launch_bounds__(NT, 3) ctx_kernel(const __grid_constant__ ParseParams P) {
-  constexpr int NSW = NS > 0 ? (NS + 3) / 4 : 1;
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint32_t* lut_s = reinterpret_cast<uint32_t*>(smem);
-  uint8_t* lin0 = smem + LUT_BYTES;  // two tile buffers
-  CtxShared& S = *reinterpret_cast<CtxShared*>(lin0 + 2 * TILE);
-  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  load_lut(P, lut_s);
-  for (int k = t; k < PP_MAX_COLS; k += NT) S.stridx[k] = P.stridx[k];
-  const uint32_t* my_lut = lut_s + lane;
-  const uint32_t n_cols = uint32_t(P.n_cols);
-  const bool aligned_in = (reinterpret_cast<uintptr_t>(P.in) & 15) == 0;
-  uint32_t* counter = &P.s.counters[0];
-  uint32_t tk = 0;  // thread 0: the next ticket
-  feed_start(P, S.F, counter, aligned_in, lin0, tk);
-
-  for (;;) {
-    const uint32_t tile = S.F.tile[S.F.cur];
-    if (tile >= P.n_tiles) break;
-    uint8_t* tile_s = lin0 + S.F.cur * TILE;
-    const uint64_t tile_base = uint64_t(tile) * TILE;
-    const uint32_t tile_len = uint32_t(min(uint64_t(TILE), P.n - tile_base));
-    uint32_t w[8];
-    feed_tile(P, S.F, counter, aligned_in, lin0, tile_base, tile_len, w, tk);
-    const uint32_t cstart = uint32_t(t) * CB;
-    const uint32_t clen = tile_len > cstart ? min(tile_len - cstart, uint32_t(CB)) : 0u;
-    const uint8_t* own = tile_s + cstart;
-    if (NS > 0)
-      for (int k = t; k < PP_MAX_COLS; k += NT) S.rel[k] = 0;
-    const uint32_t s_tile = P.s.tile_state[tile];
-
-    // the chunk's start state, and its tags
-    uint32_t G, special, special_x;
-    stv_pass(w, clen, tile_s, cstart, my_lut, G, special, special_x);
-    const uint32_t lane_ex = block_stv(G, S.warp_stv, &S.tile_stv);
-    const uint32_t st = stv_apply(lane_ex, stv_apply(S.warp_stv[warp], s_tile));
-    const Tags g = tag_chunk(st, special, special_x, P.sticky, clen, cstart, own, my_lut,
-                             P.bg_next);
-    if (g.inv_at < clen && st != 4)
-      report(P.st, PP_ERR_INVALID_INPUT, tile_base + cstart + g.inv_at, true);
-    if (!P.record_end && tile + 1 == P.n_tiles && clen > 0 && cstart + clen == tile_len &&
-        g.end != 4 && !((P.accept_mask >> g.end) & 1u))
-      report(P.st, PP_ERR_BAD_END_STATE, P.n, true);
-    if (P.s.tags)  // for the main pass: bitmaps, 1 + last terminator | end state << 16
-      P.s.tags[size_t(tile) * NT + t] = make_uint4(g.fd, g.rd, g.ctrl, (g.last >> 8) | (g.end << 16));
-
-    // (records, column, last) scanned over the warp, then over the warps
-    V2 ex = chunk_v2(g);
-    if (__any_sync(FULL, (ex.rec | ex.col | ex.last) != 0)) {
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const V2 o = shfl_up_v2(ex, d);
-        if (lane >= d) ex = op2_32(o, ex);
-      }
-    }
-    if (lane == 31) { S.wv[warp][0] = ex.rec; S.wv[warp][1] = ex.col; S.wv[warp][2] = ex.last; }
-    {
-      V2 e = shfl_up_v2(ex, 1);
-      if (lane == 0) e = {0u, 0u, 0u};
-      ex = e;  // exclusive within the warp
-    }
-    if (P.record_end) {  // partial mode: 1 + the tile's last record delimiter
-      const uint32_t wm = __reduce_max_sync(FULL, g.rd ? cstart + 32u - __clz(g.rd) : 0u);
-      if (lane == 0) S.wrd[warp] = wm;
-    }
-    __syncthreads();
-    uint32_t* rec = reinterpret_cast<uint32_t*>(P.s.ctx + size_t(tile) * P.s.ctx_stride);
-    if (P.record_end && t == 0) {
-      uint32_t m = 0;
-      for (int q = 0; q < NW; ++q) m = max(m, S.wrd[q]);
-      if (m) atomicMax(P.record_end, static_cast<unsigned long long>(tile_base + m));
-    }
-    if (warp == 0) {
-      V2 x = lane < NW ? V2{S.wv[lane][0], S.wv[lane][1], S.wv[lane][2]} : V2{0u, 0u, 0u};
-#pragma unroll
-      for (int d = 1; d < NW; d <<= 1) {
-        const V2 o = shfl_up_v2(x, d);
-        if (lane >= d) x = op2_32(o, x);
-      }
-      V2 xe = shfl_up_v2(x, 1);
-      if (lane == 0) xe = {0u, 0u, 0u};
-      if (lane < NW) { S.wpre[lane][0] = xe.rec; S.wpre[lane][1] = xe.col; S.wpre[lane][2] = xe.last; }
-      if (lane == NW - 1)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const bool mine = uint32_t(q) == s_tile;
-          rec[1 + 3 * q] = mine ? x.rec : 0u;
-          rec[2 + 3 * q] = mine ? x.col : 0u;
-          rec[3 + 3 * q] = mine ? x.last : 0u;
-        }
-      if (lane == 0) rec[0] = S.tile_stv;
-    }
-    // the chunk's (records, column, last) prefix in the tile, and whether
-    // the tile has control bytes: stored for the main pass
-    const bool any_ctrl = __syncthreads_or(g.ctrl != 0) != 0;
-    const V2 pre = op2_32(V2{S.wpre[warp][0], S.wpre[warp][1], S.wpre[warp][2]}, ex);
-    if (P.s.vpre)
-      P.s.vpre[size_t(tile) * NT + t] =
-          make_uint2(pre.rec | ((pre.last >> 8) << 16),
-                     (pre.col & 0x7FFFu) | ((pre.col & ABS32) ? 0x8000u : 0u));
-    if (t == 0) P.s.tile_flags[tile] = any_ctrl ? 1u : 0u;
-    if (NS > 0) {
-      const uint64_t strmask = P.strmask;
-      const uint32_t cmax = 63u - __clzll(static_cast<long long>(strmask));  // last string column
-      const bool chain = cmax < 8;  // column masks when the string columns come early
-      // value bytes per string column
-      const uint32_t col0 = pre.col;  // ABS32 | column, or a relative field index
-      uint64_t cnt[NSW];
-#pragma unroll
-      for (int k = 0; k < NSW; ++k) cnt[k] = 0;
-      const uint32_t valid = range_mask(0, min(clen, g.inv_at));
-      const uint32_t data = valid & ~(g.fd | g.rd | g.ctrl);
-      const uint32_t T = g.fd | g.rd;
-      const bool abs0 = (col0 & ABS32) != 0;
-      const uint32_t c0 = col0 & ~ABS32;
-      uint32_t k0 = 0xFFFFFFFFu, n0 = 0;  // the first relative segment, summed per warp below
-      if (st < 4 && !chain) {
-        // a walk over the chunk's fields (string columns far from the
-        // record start: fewer steps than the column-by-column masks)
-        bool abs = abs0;
-        uint32_t col = c0, term = T, seg0 = 0;
-        for (;;) {
-          const uint32_t j = term ? uint32_t(__ffs(term) - 1) : 32u;
-          const uint32_t n = __popc(data & range_mask(seg0, j));
-          if (n && col < n_cols) {
-            if (abs) {
-              const int si = S.stridx[col];
-              if (si >= 0) add16(cnt, si, n);
-            } else if (seg0 == 0) {
-              k0 = col;
-              n0 = n;
-            } else {
-              atomicAdd(&S.rel[col], n);
-            }
-          }
-          if (j == 32) break;
-          if ((g.rd >> j) & 1u) { abs = true; col = 0; }
-          else col = col < 0x7FFFFF00u ? col + 1 : col;
-          seg0 = j + 1;
-          term &= term - 1;
-        }
-      } else if (st < 4) {
-        if (!abs0) {
-          // fields of the tile's first, partial record: relative column
-          // indices, up to this chunk's first record delimiter
-          uint32_t col = c0, term = T, seg0 = 0;
-          for (;;) {
-            const uint32_t j = term ? uint32_t(__ffs(term) - 1) : 32u;
-            const uint32_t n = __popc(data & range_mask(seg0, j));
-            if (n && col < n_cols) {
-              if (seg0 == 0) { k0 = col; n0 = n; }
-              else atomicAdd(&S.rel[col], n);
-            }
-            if (j == 32 || ((g.rd >> j) & 1u)) break;
-            col = col < 0x7FFFFF00u ? col + 1 : col;
-            seg0 = j + 1;
-            term &= term - 1;
-          }
-        }
-        // absolute columns, one column at a time: Sc holds the starts of
-        // the column's runs; T - Sc sets each run from its start up to its
-        // terminator (exclusive) and clears that terminator, so the
-        // terminators left out of T - Sc end the column's runs, and those
-        // that are field delimiters start the next column's runs
-        uint32_t Sc = (g.rd << 1) | (abs0 && c0 == 0 ? 1u : 0u);
-        int si = 0;
-        for (uint32_t c = 0; c <= cmax; ++c) {
-          const uint32_t X = T - Sc;
-          if ((strmask >> c) & 1u) {
-            const uint32_t n = __popc(X & data);
-            if (n) add16(cnt, si, n);
-            ++si;
-          }
-          Sc = ((T & ~X & g.fd) << 1) | (abs0 && c0 == c + 1 ? 1u : 0u);
-        }
-      }
-      // relative first segments (only the chunks before the tile's first
-      // record delimiter have them): one shared atomic per field index
-      if (__any_sync(FULL, k0 != 0xFFFFFFFFu)) {
-        const uint32_t k00 = __shfl_sync(FULL, k0, 0);
-        if (__all_sync(FULL, k0 == k00)) {  // the whole warp inside one field
-          const uint32_t sum = __reduce_add_sync(FULL, n0);
-          if (lane == 0 && sum) atomicAdd(&S.rel[k00], sum);
-        } else if (k0 != 0xFFFFFFFFu && n0) {
-          atomicAdd(&S.rel[k0], n0);
-        }
-      }
-      // warp sums of the packed counters
-      bool any = false;
-#pragma unroll
-      for (int k = 0; k < NSW; ++k) any |= cnt[k] != 0;
-      if (__any_sync(FULL, any)) {
-#pragma unroll
-        for (int k = 0; k < NSW; ++k) {
-          uint64_t v = cnt[k];
-#pragma unroll
-          for (int d = 16; d; d >>= 1) v += __shfl_xor_sync(FULL, v, d);
-          if (lane == 0) S.wcnt[warp][k] = v;
-        }
-      } else if (lane == 0) {
-#pragma unroll
-        for (int k = 0; k < NSW; ++k) S.wcnt[warp][k] = 0;
-      }
-      __syncthreads();
-      // the record's chars part: the true state's slot, zeros elsewhere
-      uint16_t* cabs = reinterpret_cast<uint16_t*>(rec) + CTX_HDR / 2;
-      uint16_t* crel = cabs + 4 * P.n_str;
-      if (t < 4 * P.n_str) {
-        const int s = t / P.n_str, si = t - s * P.n_str;
-        uint64_t sum = 0;
-        if (uint32_t(s) == s_tile) {
-#pragma unroll 4
-          for (int q = 0; q < NW; ++q) sum += S.wcnt[q][si >> 2];
-        }
-        cabs[t] = uint16_t((sum >> (16 * (si & 3))) & 0xFFFFu);
-      }
-      for (int k = t; k < 4 * int(n_cols); k += NT) {
-        const int s = k / int(n_cols), c = k - s * int(n_cols);
-        crel[k] = uint32_t(s) == s_tile ? uint16_t(S.rel[c]) : uint16_t(0);
-      }
-    }
-    feed_next(S.F);  // the tile was last read before a barrier above
-  }
-  feed_finish(S.F);
-}
-
-// ==================================================================== 2. scan
-// Per-start-state aggregate over a run of tiles.
-struct SAgg {
-  uint32_t T;
-  uint32_t col[4], lst[4];
-  uint64_t rec[4], last1[4];
-};
-
-__device__ __forceinline__ SAgg sagg_identity(bool seed) {
-  SAgg a;
-  a.T = STV_ID;
-#pragma unroll
-  for (int s = 0; s < 4; ++s) {
-    a.col[s] = seed ? ABS32 : 0u;
-    a.lst[s] = 0;
-    a.rec[s] = 0;
-    a.last1[s] = 0;
-  }
-  return a;
-}
-// a then b
-__device__ __forceinline__ SAgg sagg_combine(const SAgg& a, const SAgg& b) {
-  SAgg o;
-  o.T = stv_compose(a.T, b.T);
-#pragma unroll
-  for (int s = 0; s < 4; ++s) {
-    const uint32_t s2 = stv_apply(a.T, uint32_t(s));
-    uint32_t bc = 0, bl = 0;
-    uint64_t br = 0, bl1 = 0;
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-      if (uint32_t(q) == s2) { bc = b.col[q]; bl = b.lst[q]; br = b.rec[q]; bl1 = b.last1[q]; }
-    o.rec[s] = a.rec[s] + br;
-    o.col[s] = (bc & ABS32) ? bc : ((a.col[s] & ABS32) | ((a.col[s] + bc) & ~ABS32));
-    const bool hb = bl1 != 0;
-    o.last1[s] = hb ? bl1 : a.last1[s];
-    o.lst[s] = hb ? bl : a.lst[s];
-  }
-  return o;
-}
-__device__ __forceinline__ void sagg_pack(const SAgg& a, uint64_t (&w)[13]) {
-  w[0] = a.T;
-#pragma unroll
-  for (int s = 0; s < 4; ++s) {
-    w[1 + 3 * s] = a.rec[s];
-    w[2 + 3 * s] = a.last1[s];
-    w[3 + 3 * s] = uint64_t(a.col[s]) | (uint64_t(a.lst[s]) << 32);
-  }
-}
-__device__ __forceinline__ SAgg sagg_unpack(const uint64_t (&w)[13]) {
-  SAgg a;
-  a.T = uint32_t(w[0]);
-#pragma unroll
-  for (int s = 0; s < 4; ++s) {
-    a.rec[s] = w[1 + 3 * s];
-    a.last1[s] = w[2 + 3 * s];
-    a.col[s] = uint32_t(w[3 + 3 * s]);
-    a.lst[s] = uint32_t(w[3 + 3 * s] >> 32);
-  }
-  return a;
-}
-__device__ __forceinline__ SAgg sagg_shfl_up(const SAgg& a, int d) {
-  uint64_t w[13];
-  sagg_pack(a, w);
-#pragma unroll
-  for (int k = 0; k < 13; ++k) w[k] = __shfl_up_sync(FULL, w[k], d);
-  return sagg_unpack(w);
-}
-struct SAggOp {
-  __device__ void operator()(const uint64_t (&a)[13], const uint64_t (&b)[13],
-                             uint64_t (&o)[13]) const {
-    sagg_pack(sagg_combine(sagg_unpack(a), sagg_unpack(b)), o);
-  }
-};
-__device__ __forceinline__ SAgg sagg_of_tile(const uint8_t* rec, uint64_t tile_base) {
-  const uint32_t* h = reinterpret_cast<const uint32_t*>(rec);
-  SAgg a;
-  a.T = h[0];
-#pragma unroll
-  for (int s = 0; s < 4; ++s) {
-    a.rec[s] = h[1 + 3 * s];
-    a.col[s] = h[2 + 3 * s];
-    const uint32_t l = h[3 + 3 * s];
-    a.last1[s] = l ? tile_base + (l >> 8) : 0ull;
-    a.lst[s] = l & 0xFFu;
-  }
-  return a;
-}
-
-// Per tile, written by the scan: the tile's context, followed by the
-// chars offset of the tile per string column (uint64 each).
-struct PreHdr {
-  uint64_t rec0;     // record index at the tile start
-  uint64_t last1;    // global position + 1 of the last terminator before the tile, 0 none
-  uint32_t col_in;   // absolute column at the tile start (saturated)
-  uint32_t state;    // DFA state at the tile start | state after that terminator << 8
-};
-constexpr int PRE_HDR = sizeof(PreHdr);
-
-struct ScanShared {
-  uint32_t block;
-  uint64_t wagg[SCAN_NT / 32][13];
-  uint64_t pre[13];
-  uint64_t wsum[SCAN_NT / 32][ppi::MAX_STR_COLS];
-  uint64_t base[ppi::MAX_STR_COLS];
-  int8_t stridx[PP_MAX_COLS];
-};
-
-// Exclusive scan over tiles of the per-start-state aggregates; every tile
-// learns its true start state, record index, column and last terminator,
-// then, from those, its value bytes per string column, whose exclusive
-// scan gives the tile's chars offsets.
-template <int NS>
-__global__ void __launch_bounds__(SCAN_NT) scan_kernel(const __grid_constant__ ParseParams P) {
-  constexpr int SW = SCAN_NT / 32;
-  constexpr int K3 = NS > 0 ? NS : 1;
-  __shared__ ScanShared S;
-  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  for (int k = t; k < PP_MAX_COLS; k += SCAN_NT) S.stridx[k] = P.stridx[k];
-  if (t == 0) S.block = atomicAdd(&P.s.counters[2], 1u);
-  __syncthreads();
-  const uint32_t blk = S.block;
-  const LookbackCfg cfg{P.st, P.spin_limit};
-  const uint32_t t0 = blk * SCAN_TILES + uint32_t(t) * SCAN_TPT;
-
-  SAgg mine = sagg_identity(false);
-  for (int i = 0; i < SCAN_TPT; ++i) {
-    const uint32_t tile = t0 + i;
-    if (tile < P.n_tiles)
-      mine = sagg_combine(mine, sagg_of_tile(P.s.ctx + size_t(tile) * P.s.ctx_stride,
-                                             uint64_t(tile) * TILE));
-  }
-  SAgg inc = mine;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    const SAgg o = sagg_shfl_up(inc, d);
-    if (lane >= d) inc = sagg_combine(o, inc);
-  }
-  SAgg lex = sagg_shfl_up(inc, 1);
-  if (lane == 0) lex = sagg_identity(false);
-  if (lane == 31) sagg_pack(inc, S.wagg[warp]);
-  __syncthreads();
-  if (warp == 0) {
-    uint64_t wv[13];
-    SAgg x = sagg_identity(false);
-    if (lane < SW) {
-#pragma unroll
-      for (int k = 0; k < 13; ++k) wv[k] = S.wagg[lane][k];
-      x = sagg_unpack(wv);
-    }
-#pragma unroll
-    for (int d = 1; d < SW; d <<= 1) {
-      const SAgg o = sagg_shfl_up(x, d);
-      if (lane >= d) x = sagg_combine(o, x);
-    }
-    SAgg xe = sagg_shfl_up(x, 1);
-    if (lane == 0) xe = sagg_identity(false);
-    __syncwarp();
-    if (lane < SW) sagg_pack(xe, S.wagg[lane]);
-    uint64_t agg[13], seed[13], ident[13], ex[13];
-    {
-      uint64_t tw[13];
-      sagg_pack(x, tw);
-#pragma unroll
-      for (int k = 0; k < 13; ++k) agg[k] = __shfl_sync(FULL, tw[k], SW - 1);
-    }
-    sagg_pack(sagg_identity(true), seed);
-    sagg_pack(sagg_identity(false), ident);
-    if (P.dbg_withhold && blk == 0) {  // test hook: post nothing, later blocks time out
-#pragma unroll
-      for (int k = 0; k < 13; ++k) ex[k] = seed[k];
-    } else {
-      lookback_vec<13>(P.s.scan_flag_a, P.s.scan_agg_a, P.s.scan_inc_a, blk, agg, seed, ident,
-                       SAggOp{}, cfg, ex);
-    }
-    if (lane == 0)
-#pragma unroll
-      for (int k = 0; k < 13; ++k) S.pre[k] = ex[k];
-  }
-  __syncthreads();
-  // resolve this thread's first tile at the true start state
-  SAgg blockpre;
-  {
-    uint64_t pw[13], ww[13];
-#pragma unroll
-    for (int k = 0; k < 13; ++k) { pw[k] = S.pre[k]; ww[k] = S.wagg[warp][k]; }
-    blockpre = sagg_combine(sagg_unpack(pw), sagg_combine(sagg_unpack(ww), lex));
-  }
-  const uint32_t s0 = P.start_state;
-  uint32_t s = stv_apply(blockpre.T, s0);
-  uint64_t rec = 0, last1 = 0;
-  uint32_t col = 0, lst = 0;
-#pragma unroll
-  for (int q = 0; q < 4; ++q)
-    if (uint32_t(q) == s0) {
-      rec = blockpre.rec[q];
-      last1 = blockpre.last1[q];
-      col = blockpre.col[q] & ~ABS32;
-      lst = blockpre.lst[q];
-    }
-  const uint32_t n_cols = uint32_t(P.n_cols);
-  uint64_t sum[K3];
-#pragma unroll
-  for (int k = 0; k < K3; ++k) sum[k] = 0;
-  for (int i = 0; i < SCAN_TPT; ++i) {
-    const uint32_t tile = t0 + i;
-    if (tile >= P.n_tiles) break;
-    const uint8_t* cr = P.s.ctx + size_t(tile) * P.s.ctx_stride;
-    uint8_t* pr = P.s.pre + size_t(tile) * P.s.pre_stride;
-    PreHdr h;
-    h.rec0 = rec;
-    h.last1 = last1;
-    h.col_in = col;
-    h.state = s | (lst << 8);
-    *reinterpret_cast<PreHdr*>(pr) = h;
-    const uint32_t* hd = reinterpret_cast<const uint32_t*>(cr);
-    if (NS > 0) {  // the tile's value bytes per string column at its true context
-      uint64_t* cb = reinterpret_cast<uint64_t*>(pr + PRE_HDR);
-      const uint16_t* cabs = reinterpret_cast<const uint16_t*>(cr + CTX_HDR);
-      const uint16_t* crel = cabs + 4 * P.n_str;
-      uint64_t contrib[K3];
-#pragma unroll
-      for (int k = 0; k < K3; ++k) contrib[k] = 0;
-      if (s < 4) {
-#pragma unroll
-        for (int k = 0; k < K3; ++k)
-          if (k < P.n_str) contrib[k] = cabs[s * P.n_str + k];
-        for (uint32_t k = 0; col + k < n_cols; ++k) {
-          const int si = S.stridx[col + k];
-          const uint32_t v = crel[s * n_cols + k];
-          if (si >= 0 && v) {
-#pragma unroll
-            for (int q = 0; q < K3; ++q)
-              if (q == si) contrib[q] += v;
-          }
-        }
-      }
-#pragma unroll
-      for (int k = 0; k < K3; ++k) {
-        if (k < P.n_str) cb[k] = contrib[k];
-        sum[k] += contrib[k];
-      }
-    }
-    if (s < 4) {
-      const uint32_t trec = hd[1 + 3 * s], tcol = hd[2 + 3 * s], tl = hd[3 + 3 * s];
-      rec += trec;
-      if (tcol & ABS32) col = tcol & ~ABS32;
-      else col = (uint64_t(col) + tcol > 0x7FFFFF00ull) ? 0x7FFFFF00u : col + tcol;
-      if (tl) { last1 = uint64_t(tile) * TILE + (tl >> 8); lst = tl & 0xFFu; }
-      s = stv_apply(hd[0], s);
-    }
-  }
-
-  // chars offsets: exclusive sum over tiles per string column
-  if (NS > 0) {
-    uint64_t ci[K3];
-#pragma unroll
-    for (int k = 0; k < K3; ++k) ci[k] = sum[k];
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-#pragma unroll
-      for (int k = 0; k < K3; ++k) {
-        const uint64_t o = __shfl_up_sync(FULL, ci[k], d);
-        if (lane >= d) ci[k] += o;
-      }
-    }
-    if (lane == 31)
-#pragma unroll
-      for (int k = 0; k < K3; ++k) S.wsum[warp][k] = ci[k];
-    __syncthreads();
-    if (warp == 0) {
-      uint64_t v[K3], x[K3], agg[K3], zero[K3], exc[K3];
-#pragma unroll
-      for (int k = 0; k < K3; ++k) { v[k] = lane < SW ? S.wsum[lane][k] : 0ull; x[k] = v[k]; zero[k] = 0; }
-#pragma unroll
-      for (int d = 1; d < SW; d <<= 1) {
-#pragma unroll
-        for (int k = 0; k < K3; ++k) {
-          const uint64_t o = __shfl_up_sync(FULL, x[k], d);
-          if (lane >= d) x[k] += o;
-        }
-      }
-#pragma unroll
-      for (int k = 0; k < K3; ++k) {
-        agg[k] = __shfl_sync(FULL, x[k], SW - 1);
-        if (lane < SW) S.wsum[lane][k] = x[k] - v[k];
-      }
-      if (P.dbg_withhold && blk == 0) {
-#pragma unroll
-        for (int k = 0; k < K3; ++k) exc[k] = 0;
-      } else {
-        lookback_vec<K3>(P.s.scan_flag_c, P.s.scan_agg_c, P.s.scan_inc_c, blk, agg, zero, zero,
-                         AddOp<K3>{}, cfg, exc);
-      }
-      if (lane == 0)
-#pragma unroll
-        for (int k = 0; k < K3; ++k) S.base[k] = exc[k];
-    }
-    __syncthreads();
-    uint64_t run[K3];
-#pragma unroll
-    for (int k = 0; k < K3; ++k) run[k] = S.base[k] + S.wsum[warp][k] + (ci[k] - sum[k]);
-    for (int i = 0; i < SCAN_TPT; ++i) {
-      const uint32_t tile = t0 + i;
-      if (tile >= P.n_tiles) break;
-      uint64_t* cb = reinterpret_cast<uint64_t*>(P.s.pre + size_t(tile) * P.s.pre_stride + PRE_HDR);
-#pragma unroll
-      for (int k = 0; k < K3; ++k)
-        if (k < P.n_str) {
-          const uint64_t c = cb[k];
-          cb[k] = run[k];
-          run[k] += c;
-        }
-    }
-  }
-}
-
 // Numeric field whose bytes are not all in the tile, contain control bytes
 // or need the full grammar: streaming accumulators over the value bytes.
 // Returns the error bits; *out receives the value (0 for an empty field).
@@ -1125,13 +537,21 @@ __device__ __forceinline__ int convert_general(const ParseParams& P, uint32_t ty
 struct NumCtx {
   uint64_t tile_base, tile_fstart;  // the tile's first byte; start of the field open at it
   uint32_t tile_fstate;             // DFA state at tile_fstart
-  const uint8_t* tile_s;
-  const uint32_t* tile_w;
-  const uint32_t* ctrl_s;
-  const uint16_t* cpre;
-  const uint32_t* my_lut;
+  const uint8_t* tile_s;            // tile byte p at tile_s[p]
+  const uint32_t* raw_w;            // landing buffer as words: tile byte p at byte p + toff
+  uint32_t toff;
+  const uint32_t* ctrl_s;           // control bitmap per chunk
+  const uint32_t* wc;               // control bytes before each warp's chunks ([16]: total)
+  const uint16_t* cpl;              // control bytes before each chunk inside its warp
+  const uint32_t* lut;               // one LUT entry per byte value
   bool any_ctrl;
 };
+
+// control bytes of the tile before position p (p <= tile length)
+__device__ __forceinline__ uint32_t ctrl_x(const NumCtx& X, uint32_t p) {
+  const uint32_t c = p >> 5, b = p & 31u;
+  return X.wc[c >> 5] + X.cpl[c] + (b ? uint32_t(__popc(X.ctrl_s[c] & ((1u << b) - 1u))) : 0u);
+}
 
 // Convert the numeric field in slot value v (tile-relative start << 16 |
 // end; start 0xFFFF = the field began in an earlier tile; SLOT_DEFAULT = a
@@ -1150,14 +570,14 @@ __device__ __forceinline__ int convert_field(const ParseParams& P, uint32_t v, c
   if (v == SLOT_DEFAULT) return 0;
   const uint32_t fsr = v >> 16, fe = v & 0xFFFFu;
   if (fsr != 0xFFFFu &&
-      (!X.any_ctrl || ctrl_before(X.ctrl_s, X.cpre, fe) == ctrl_before(X.ctrl_s, X.cpre, fsr))) {
+      (!X.any_ctrl || ctrl_x(X, fe) == ctrl_x(X, fsr))) {
     const uint32_t L = fe - fsr;
     if (L == 0) return 0;  // empty field: the column default
     if (TY == PP_COL_TIMESTAMP) {  // five words of the tile from the field start
-      const uint32_t q = fsr >> 2, sh = (fsr & 3u) * 8u;
+      const uint32_t a = fsr + X.toff, q = a >> 2, sh = (a & 3u) * 8u;
       uint32_t x[5];
 #pragma unroll
-      for (int k = 0; k < 5; ++k) x[k] = __funnelshift_r(X.tile_w[q + k], X.tile_w[q + k + 1], sh);
+      for (int k = 0; k < 5; ++k) x[k] = __funnelshift_r(X.raw_w[q + k], X.raw_w[q + k + 1], sh);
       int64_t t = 0;
       const int err = ppn::parse_timestamp(x, L, &t);
       val = uint64_t(t);
@@ -1167,8 +587,8 @@ __device__ __forceinline__ int convert_field(const ParseParams& P, uint32_t v, c
     const uint32_t sg = (c0 == '-' || c0 == '+') ? 1u : 0u;
     const bool neg = c0 == '-';
     const int n = int(L - sg);
-    const uint32_t pv = fsr + sg, q = pv >> 2, sh = (pv & 3u) * 8u;
-    const uint32_t w0 = X.tile_w[q], w1 = X.tile_w[q + 1];
+    const uint32_t pv = fsr + sg + X.toff, q = pv >> 2, sh = (pv & 3u) * 8u;
+    const uint32_t w0 = X.raw_w[q], w1 = X.raw_w[q + 1];
     const uint32_t x0 = __funnelshift_r(w0, w1, sh);
     uint32_t w;
     if (TY != PP_COL_FLOAT64 && n >= 1 && n <= 4) {  // up to 4 digits: one word
@@ -1180,7 +600,7 @@ __device__ __forceinline__ int convert_field(const ParseParams& P, uint32_t v, c
         return 0;
       }
     }
-    const uint32_t x1 = __funnelshift_r(w1, X.tile_w[q + 2], sh);
+    const uint32_t x1 = __funnelshift_r(w1, X.raw_w[q + 2], sh);
     const uint64_t x = (uint64_t(x1) << 32) | x0;
     int k;
     if (n >= 1 && n <= 8 &&
@@ -1194,7 +614,7 @@ __device__ __forceinline__ int convert_field(const ParseParams& P, uint32_t v, c
       return 0;
     }
     if (TY != PP_COL_FLOAT64 && n > 8 && n <= 16) {
-      const uint64_t x2 = tile_load8(X.tile_w, fsr + sg + 8);
+      const uint64_t x2 = tile_load8(X.raw_w, fsr + sg + 8 + X.toff);
       uint32_t wl;
       if (ppn::short_decimal(uint32_t(x), uint32_t(x >> 32), 8, false, &w, &k) &&
           ppn::short_decimal(uint32_t(x2), uint32_t(x2 >> 32), n - 8, false, &wl, &k)) {
@@ -1210,67 +630,466 @@ __device__ __forceinline__ int convert_field(const ParseParams& P, uint32_t v, c
     }
   }
   return convert_general(P, TY, fsr == 0xFFFFu ? X.tile_fstart : X.tile_base + fsr,
-                         X.tile_base + fe, X.tile_base, X.tile_s, X.ctrl_s, X.my_lut,
+                         X.tile_base + fe, X.tile_base, X.tile_s, X.ctrl_s, X.lut,
                          X.tile_fstate, &val);
 }
 
-// Convert one row's field of a column of type TY and store it at out[rec].
-template <int TY>
-__device__ __forceinline__ void convert_store(const ParseParams& P, const NumCtx& X, void* out,
-                                              uint64_t rec, uint32_t v) {
+// Convert one row's field (slot value v) of a column of type ty, reporting
+// a number error at the field's first byte; returns the value's bits.
+__device__ __forceinline__ uint64_t convert_any(const ParseParams& P, const NumCtx& X, uint32_t ty,
+                                                uint32_t v) {
   uint64_t val;
-  const int err = convert_field<TY>(P, v, X, val);
-  if (TY == PP_COL_FLOAT64) static_cast<uint64_t*>(out)[rec] = val;
-  else if (TY == PP_COL_INT64 || TY == PP_COL_TIMESTAMP) static_cast<int64_t*>(out)[rec] = int64_t(val);
-  else if (TY == PP_COL_INT32) static_cast<int32_t*>(out)[rec] = int32_t(val);
-  else static_cast<int8_t*>(out)[rec] = int8_t(val);
+  int err;
+  switch (ty) {
+    case PP_COL_FLOAT64: err = convert_field<PP_COL_FLOAT64>(P, v, X, val); break;
+    case PP_COL_INT64: err = convert_field<PP_COL_INT64>(P, v, X, val); break;
+    case PP_COL_TIMESTAMP: err = convert_field<PP_COL_TIMESTAMP>(P, v, X, val); break;
+    case PP_COL_INT32: err = convert_field<PP_COL_INT32>(P, v, X, val); break;
+    default: err = convert_field<PP_COL_INT8>(P, v, X, val); break;
+  }
   if (err) {
     const uint32_t fsr = v >> 16;
     report(P.st, err, fsr == 0xFFFFu ? X.tile_fstart : X.tile_base + fsr, true);
   }
+  return val;
+}
+// Store a converted value at out[rec] in the column's width.
+__device__ __forceinline__ void store_typed(void* out, uint32_t ty, uint64_t rec, uint64_t val) {
+  if (ty == PP_COL_INT32) static_cast<int32_t*>(out)[rec] = int32_t(val);
+  else if (ty == PP_COL_INT8) static_cast<int8_t*>(out)[rec] = int8_t(val);
+  else static_cast<uint64_t*>(out)[rec] = val;
 }
 
-// ================================================================ 3. main
-constexpr uint32_t SHORT_FIELD = 32;  // longer string fields are staged chunk-parallel
-constexpr uint32_t WLIST_CAP = 512;   // terminators per warp listed in the staging buffer
+// ================================================================ 1. tile pass
+// Everything after the tile start states happens in one pass over the tiles.
+// A block has 16 worker warps (one 32-byte chunk per thread, as in the tile
+// states pass) and one scan warp.  The scan warp runs the two cross-tile
+// exclusive scans of ParPaRaw Section 3.2 as single-pass decoupled
+// look-backs — first (record count, column offset, last terminator), then
+// the value bytes per string column — while the workers go on with the
+// tile's own work; named barriers hand the aggregates and the prefixes
+// between the two roles:
+//
+//   workers                                   scan warp
+//   tag the tile, scan it        --BAR_AGG-->  post the tile's aggregate,
+//   list its fields (rows and                  look back: record index,
+//   columns inside the tile),                  column and last terminator
+//   value bytes per string                     at the tile start
+//   column                       --BAR_W2--->
+//   place the first record's     <--BAR_V2---  post the chars aggregate
+//   fields; stage strings,                     look back: chars offsets
+//   convert numbers (stored at                 of the tile
+//   their global rows)           <--BAR_CHR--
+//   write offsets and chars
+//
+// The first record of a tile (its row 0) is in general the tail of a record
+// that began earlier: its fields' columns are the tile's entry column plus
+// their index, known only from the look-back (ParPaRaw Section 3.2, the
+// "relative" column offset), so the workers keep them aside by index until
+// then.  Tiles are handed out by an atomic ticket, so a tile's predecessors
+// have always been started; a block takes its next ticket and starts that
+// tile's copy late in the current tile (after the number conversions), so
+// that tiles start in about ticket order and a tile's predecessors have
+// mostly posted their aggregates by the time it looks back.
+constexpr int BUF_BYTES = TILE + 64;      // landing buffer: the tile at toff, slack for word reads
+constexpr uint32_t SHORT_FIELD = 32;      // longer string fields are staged chunk-parallel
+constexpr uint32_t WLIST_CAP = 512;       // terminators per warp listed in the staging buffer
 constexpr uint16_t NO_FIELD = 0xFFFFu;
+constexpr uint32_t REL_START = 0xFFFFu;   // slot start: the field began before the tile
+constexpr uint32_t BAR_W = 1, BAR_AGG = 2, BAR_W2 = 3, BAR_V2 = 4, BAR_CHR = 5;
+constexpr uint64_t M40 = (1ull << 40) - 1;
+constexpr uint32_t COL_SAT = 0x1FFF00u;   // column counts saturate here (fit the look-back descriptor)
 
-struct MainShared {
-  Feed F;
-  uint32_t tile_stv;
+__device__ __forceinline__ void bar_sync(uint32_t id, uint32_t n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ void bar_arrive(uint32_t id, uint32_t n) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// The tile's bytes sit at buf[toff + p], toff = the input's address mod 16,
+// so the 16-byte aligned span [c0, c1) of the tile (tile coordinates, c0 may
+// be negative: bytes of the tile before) lands by one bulk copy at a 16-byte
+// aligned buffer address.  The span never leaves the input; plain loads fill
+// [0, c0) (the first tile of a misaligned input) and [c1, len) (the end of
+// the input).  c1 <= c0: no bulk copy.
+struct Span { int32_t c0, c1; };
+__device__ __forceinline__ Span bulk_span(const ParseParams& P, uint32_t tile, uint32_t toff) {
+  const uint64_t base = reinterpret_cast<uintptr_t>(P.in);
+  const uint64_t tb = uint64_t(tile) * TILE;
+  const uint32_t len = uint32_t(min(uint64_t(TILE), P.n - tb));
+  const uint64_t a = base + tb, end = base + P.n;
+  uint64_t lo = a - toff;
+  if (lo < base) lo += 16;
+  uint64_t hi = (a + len + 15) & ~uint64_t(15);
+  if (hi > end) hi = (a + len) & ~uint64_t(15);
+  if (hi <= lo) return {0, 0};
+  return {int32_t(int64_t(lo) - int64_t(a)), int32_t(int64_t(hi) - int64_t(a))};
+}
+
+// Start the bulk copy of `tile` into buf (one elected thread); 1 if started.
+__device__ __forceinline__ uint32_t issue_span(const ParseParams& P, uint32_t tile, uint32_t toff,
+                                               uint8_t* buf, uint64_t* bar) {
+  if (tile >= P.n_tiles) return 0;
+  const Span s = bulk_span(P, tile, toff);
+  if (s.c1 <= s.c0) return 0;
+  const uint32_t bytes = uint32_t(s.c1 - s.c0);
+  mbar_arrive_expect_tx(bar, bytes);
+  bulk_g2s(buf + int32_t(toff) + s.c0, P.in + int64_t(uint64_t(tile) * TILE) + s.c0, bytes, bar);
+  return 1;
+}
+
+// This thread's 32 bytes of the tile.
+__device__ __forceinline__ void load_chunk(const uint8_t* buf, uint32_t toff, uint32_t t,
+                                           uint32_t (&w)[8]) {
+  if (toff == 0) {
+    const uint4* src = reinterpret_cast<const uint4*>(buf + t * CB);
+    const int sw = (t >> 2) & 1;  // alternate read order: conflict-free 16-byte reads
+    const uint4 x = src[sw], y = src[sw ^ 1];
+    const uint4 lo = sw ? y : x, hi = sw ? x : y;
+    w[0] = lo.x; w[1] = lo.y; w[2] = lo.z; w[3] = lo.w;
+    w[4] = hi.x; w[5] = hi.y; w[6] = hi.z; w[7] = hi.w;
+  } else {
+    const uint32_t* rw = reinterpret_cast<const uint32_t*>(buf);
+    const uint32_t a = t * CB + toff, q = a >> 2, sh = (a & 3u) * 8u;
+    uint32_t r[9];
+#pragma unroll
+    for (int k = 0; k < 9; ++k) r[k] = rw[q + k];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) w[k] = __funnelshift_r(r[k], r[k + 1], sh);
+  }
+}
+
+// Chunk vectors composed over the worker warps (block_stv with the workers'
+// barrier).
+__device__ __forceinline__ uint32_t block_stv_w(uint32_t G, uint32_t* warp_stv) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t inc = G;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const uint32_t o = __shfl_up_sync(FULL, inc, d);
+    if (lane >= d) inc = stv_compose(o, inc);
+  }
+  uint32_t lane_ex = __shfl_up_sync(FULL, inc, 1);
+  if (lane == 0) lane_ex = STV_ID;
+  if (lane == 31) warp_stv[warp] = inc;
+  bar_sync(BAR_W, NT);
+  if (warp == 0) {
+    const uint32_t v = lane < NW ? warp_stv[lane] : STV_ID;
+    uint32_t wi = v;
+#pragma unroll
+    for (int d = 1; d < NW; d <<= 1) {
+      const uint32_t o = __shfl_up_sync(FULL, wi, d);
+      if (lane >= d) wi = stv_compose(o, wi);
+    }
+    uint32_t wex = __shfl_up_sync(FULL, wi, 1);
+    if (lane == 0) wex = STV_ID;
+    if (lane < NW) warp_stv[lane] = wex;
+  }
+  bar_sync(BAR_W, NT);
+  return lane_ex;
+}
+
+// (record count, last terminator as a global position + 1, column | state
+// after the last terminator << 32): the record-count and column-offset
+// operators of ParPaRaw Section 3.2, for the cross-tile look-back.
+struct V2Op {
+  __device__ void operator()(const uint64_t (&a)[3], const uint64_t (&b)[3],
+                             uint64_t (&o)[3]) const {
+    o[0] = a[0] + b[0];
+    const bool hb = b[1] != 0;
+    o[1] = hb ? b[1] : a[1];
+    const uint32_t ac = uint32_t(a[2]), bc = uint32_t(b[2]);
+    uint32_t col;
+    if (bc & ABS32) {
+      col = bc;
+    } else {
+      const uint64_t s = uint64_t(ac & ~ABS32) + bc;
+      col = (ac & ABS32) | uint32_t(s > COL_SAT ? uint64_t(COL_SAT) : s);
+    }
+    o[2] = uint64_t(col) | (uint64_t(hb ? uint32_t(b[2] >> 32) : uint32_t(a[2] >> 32)) << 32);
+  }
+};
+
+// The context look-back's per-tile descriptor: two 64-bit words, each
+// carrying the status in bits 0..1 (none / aggregate / inclusive prefix),
+// so that one 16-byte load reads a whole descriptor and a descriptor whose
+// two words show different statuses (read while being rewritten) counts as
+// not posted yet.
+//   word 0: status | records << 2 (40 bits) | state after the last terminator << 42
+//   word 1: status | (last terminator + 1) << 2 (40 bits) | column << 42
+// The column takes 22 bits: bit 21 absolute, 21 bits of count, saturated
+// (a record's fields beyond n_cols <= 64 are dropped anyway).  Positions and
+// record counts stay below 2^40 (inputs are limited to 2^40 bytes).
+__device__ __forceinline__ uint32_t col_pack(uint32_t c) {
+  return ((c & ABS32) ? (1u << 21) : 0u) | min(c & ~ABS32, COL_SAT);
+}
+__device__ __forceinline__ uint32_t col_unpack(uint32_t c) {
+  return ((c >> 21) & 1u ? ABS32 : 0u) | (c & 0x1FFFFFu);
+}
+__device__ __forceinline__ void v2_pack(uint32_t flag, const uint64_t (&v)[3], uint64_t& w0,
+                                        uint64_t& w1) {
+  w0 = flag | ((v[0] & M40) << 2) | (uint64_t(uint32_t(v[2] >> 32) & 0xFu) << 42);
+  w1 = flag | ((v[1] & M40) << 2) | (uint64_t(col_pack(uint32_t(v[2]))) << 42);
+}
+__device__ __forceinline__ void v2_unpack(uint64_t w0, uint64_t w1, uint64_t (&v)[3]) {
+  v[0] = (w0 >> 2) & M40;
+  v[1] = (w1 >> 2) & M40;
+  v[2] = uint64_t(col_unpack(uint32_t(w1 >> 42))) | (uint64_t((w0 >> 42) & 0xFu) << 32);
+}
+__device__ __forceinline__ void st_v2desc(uint64_t* d, uint64_t w0, uint64_t w1) {
+  asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %2};" ::"l"(d), "l"(w0), "l"(w1) : "memory");
+}
+__device__ __forceinline__ void ld_v2desc(const uint64_t* d, uint64_t& w0, uint64_t& w1) {
+  asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(w0), "=l"(w1) : "l"(d) : "memory");
+}
+
+// Decoupled look-back over the descriptors (one full warp): posts the
+// tile's aggregate, returns its exclusive prefix and posts its inclusive
+// prefix.  Every wait is bounded; a wait that runs out reports
+// PP_ERR_LOOKBACK_TIMEOUT and takes the missing tiles as empty.
+__device__ void v2_lookback(uint64_t* desc, uint32_t tile, const uint64_t (&agg)[3],
+                            const LookbackCfg& cfg, uint64_t (&out_excl)[3]) {
+  const int lane = threadIdx.x & 31;
+  const V2Op op;
+  const uint64_t seed[3] = {0ull, 0ull, uint64_t(ABS32)};
+  const uint64_t ident[3] = {0ull, 0ull, 0ull};
+  uint64_t w0, w1;
+  if (tile == 0) {
+    uint64_t inc[3];
+    op(seed, agg, inc);
+    v2_pack(LB_INC, inc, w0, w1);
+    if (lane == 0) st_v2desc(desc, w0, w1);
+#pragma unroll
+    for (int k = 0; k < 3; ++k) out_excl[k] = seed[k];
+    return;
+  }
+  v2_pack(LB_AGG, agg, w0, w1);
+  if (lane == 0) st_v2desc(desc + 2 * size_t(tile), w0, w1);
+  uint64_t acc[3] = {0ull, 0ull, 0ull};
+  int64_t base = int64_t(tile) - 1;
+  uint32_t spins = 0;
+  bool timed_out = false;
+  for (;;) {
+    const int64_t idx = base - lane;
+    uint32_t f;
+    uint64_t v[3];
+    for (;;) {
+      if (idx >= 0) {
+        ld_v2desc(desc + 2 * size_t(idx), w0, w1);
+        f = uint32_t(w0 & 3u) == uint32_t(w1 & 3u) ? uint32_t(w0 & 3u) : LB_NONE;
+      } else {
+        f = LB_INC;
+      }
+      if (lb_ready(f)) break;
+      if (!lb_backoff(spins, cfg.spin_limit)) { timed_out = true; break; }
+    }
+    if (idx < 0) {
+#pragma unroll
+      for (int k = 0; k < 3; ++k) v[k] = seed[k];
+    } else if (f == LB_NONE) {  // only after a timeout
+#pragma unroll
+      for (int k = 0; k < 3; ++k) v[k] = ident[k];
+      f = LB_INC;
+    } else {
+      v2_unpack(w0, w1, v);
+    }
+    const uint32_t pmask = __ballot_sync(FULL, f == LB_INC);
+    const int stop = pmask ? __ffs(pmask) - 1 : 31;
+    if (lane > stop) {
+#pragma unroll
+      for (int k = 0; k < 3; ++k) v[k] = ident[k];
+    }
+    // lane L combines with lane L+d, which holds an EARLIER tile
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      uint64_t o[3], t[3];
+#pragma unroll
+      for (int k = 0; k < 3; ++k) o[k] = __shfl_down_sync(FULL, v[k], d);
+      if (lane + d < 32) {
+        op(o, v, t);
+#pragma unroll
+        for (int k = 0; k < 3; ++k) v[k] = t[k];
+      }
+    }
+    uint64_t r[3], t[3];
+#pragma unroll
+    for (int k = 0; k < 3; ++k) r[k] = __shfl_sync(FULL, v[k], 0);
+    op(r, acc, t);
+#pragma unroll
+    for (int k = 0; k < 3; ++k) acc[k] = t[k];
+    if (pmask) break;
+    base -= 32;
+  }
+  if (timed_out && lane == 0) report(cfg.st, PP_ERR_LOOKBACK_TIMEOUT, 0, false);
+  uint64_t inc[3];
+  op(acc, agg, inc);
+  v2_pack(LB_INC, inc, w0, w1);
+  if (lane == 0) st_v2desc(desc + 2 * size_t(tile), w0, w1);
+#pragma unroll
+  for (int k = 0; k < 3; ++k) out_excl[k] = acc[k];
+}
+
+struct PShared {
+  uint64_t bar[2];               // landing buffers' mbarriers
+  uint32_t tile[2];              // ticket per buffer (written by the scan warp)
+  uint32_t issued[2], wpar[2];   // bulk copy started, phase parity to wait for
   uint32_t warp_stv[NW];
-  uint32_t warp_rec[NW], warp_col[NW], warp_last[NW];
-  uint32_t rows;             // records touched by the tile (#RD + 1)
-  uint32_t col_end;          // fields of the last row closed in the tile
+  uint32_t wv[NW][3];            // per warp (records, column, last), then exclusive
+  uint32_t wt[NW];               // terminators per warp, then exclusive
+  uint32_t wc[NW + 1];           // control bytes per warp, then exclusive; [NW] = tile total
+  uint32_t wrd[NW];              // partial mode: 1 + the warp's last record delimiter
+  uint32_t agg_rec, agg_col, agg_last, n_ctrl, virt;  // the tile's totals
+  uint32_t rel_slot[PP_MAX_COLS];  // row-0 field k: slot value
+  uint32_t rel_len[PP_MAX_COLS];   // row-0 field k: value bytes
+  uint32_t n_rel;                  // row-0 fields seen (k + 1 of the last)
+  uint32_t rd0_pos, rd0_k;         // the tile's first record delimiter: position + 1, field index
+  uint32_t ctot[ppi::MAX_STR_COLS];  // value bytes per string column of rows >= 1
+  uint64_t rec0, last1;            // from the look-back: record index, last terminator + 1
+  uint32_t col_in, lst;            // column at the tile start, state after that terminator
+  uint64_t base[ppi::MAX_STR_COLS];  // chars offset of the tile per string column
   uint32_t wsum[NW];
   uint32_t cstart[ppi::MAX_STR_COLS + 1];  // staging start per string column (this pass)
   uint32_t carry[ppi::MAX_STR_COLS];       // chars of earlier passes per string column
-  uint64_t base[ppi::MAX_STR_COLS];        // chars offset of the tile per string column
   uint8_t coltype[PP_MAX_COLS];
-  uint8_t numcol[PP_MAX_COLS];             // numeric output columns, floats first
+  uint8_t numcol[PP_MAX_COLS];     // numeric output columns, floats first
   uint32_t n_num;
-  uint16_t cpre[NT + 1];     // control bytes before chunk t (exclusive scan)
-  uint16_t lk[2][NT];        // long string field (item) continuing in / starting in chunk t
+  uint32_t lut1[256];              // the LUT, one entry per byte value
+  uint16_t cpl[NT + 1];            // control bytes before chunk t inside its warp
+  uint16_t lk[2][NT];              // long string field (item) continuing in / starting in chunk t
 };
-constexpr size_t MAIN_SMEM = LUT_BYTES + 2 * TILE + STAGE_BYTES + SLOT_CAP * 4 + NT * 4 +
-                             SLOT_CAP * 2 + sizeof(MainShared);
+constexpr size_t PARSE_SMEM = LUT_BYTES + 2 * BUF_BYTES + STAGE_BYTES + SLOT_CAP * 4 + NT * 4 +
+                              SLOT_CAP * 2 + sizeof(PShared);
 
+// control bytes of the tile before position p (p <= tile length)
+__device__ __forceinline__ uint32_t ctrl_bef(const uint32_t* ctrl_s, const PShared& S, uint32_t p) {
+  const uint32_t c = p >> 5, b = p & 31u;
+  return S.wc[c >> 5] + S.cpl[c] + (b ? uint32_t(__popc(ctrl_s[c] & ((1u << b) - 1u))) : 0u);
+}
+// value bytes of the field [fs, e) inside the tile (fs = REL_START: from 0)
+__device__ __forceinline__ uint32_t value_len(uint32_t fs, uint32_t e, bool any_ctrl,
+                                              const uint32_t* ctrl_s, const PShared& S) {
+  const uint32_t a0 = fs == REL_START ? 0u : fs;
+  return (e - a0) - (any_ctrl ? ctrl_bef(ctrl_s, S, e) - ctrl_bef(ctrl_s, S, a0) : 0u);
+}
 
-
+// ------------------------------------------------------------- scan warps
+// Block sizes: the workers, the context warp, and (with string columns) the
+// chars warp.
 template <int NS>
-__global__ void __launch_bounds__(NT, 2) main_kernel(const __grid_constant__ ParseParams P) {
+__host__ __device__ constexpr int ntf_of() { return NT + (NS > 0 ? 64 : 32); }
+
+// The context warp: per tile, the record/column look-back.
+template <int NS>
+__device__ void ctx_role(const ParseParams& P, PShared& S) {
+  constexpr uint32_t NTF_ = ntf_of<NS>();
+  const int lane = threadIdx.x & 31;
+  const LookbackCfg cfg{P.st, P.spin_limit};
+  for (uint32_t it = 0;; ++it) {
+    const uint32_t b = it & 1u;
+    bar_sync(BAR_AGG, NT + 32);  // the workers' tile aggregate (or their exit)
+    const uint32_t tile = S.tile[b];
+    if (tile >= P.n_tiles) break;
+    const uint64_t tile_base = uint64_t(tile) * TILE;
+    uint64_t agg[3], ex[3];
+    agg[0] = S.agg_rec;
+    agg[1] = S.agg_last ? tile_base + (S.agg_last >> 8) : 0ull;
+    agg[2] = uint64_t(S.agg_col) | (uint64_t(S.agg_last & 0xFFu) << 32);
+    if (P.dbg_withhold && tile == 0) {  // test hook: post nothing, later tiles time out
+      ex[0] = 0; ex[1] = 0; ex[2] = ABS32;
+    } else {
+      v2_lookback(P.s.v2_desc, tile, agg, cfg, ex);
+    }
+    if (lane == 0) {
+      S.rec0 = ex[0];
+      S.last1 = ex[1];
+      S.col_in = uint32_t(ex[2]) & ~ABS32;
+      S.lst = uint32_t(ex[2] >> 32);
+    }
+    __syncwarp();
+    bar_arrive(BAR_V2, NTF_);
+  }
+}
+
+// The chars warp: per tile, the chars aggregate (its first record's fields
+// placed by the entry column) and the chars look-back.
+template <int NS>
+__device__ void chars_role(const ParseParams& P, PShared& S) {
+  constexpr int K3 = NS > 0 ? NS : 1;
+  constexpr uint32_t NTF_ = ntf_of<NS>();
+  const int lane = threadIdx.x & 31;
+  const LookbackCfg cfg{P.st, P.spin_limit};
+  const uint32_t n_cols = uint32_t(P.n_cols);
+  for (uint32_t it = 0;; ++it) {
+    const uint32_t b = it & 1u;
+    bar_sync(BAR_W2, NT + 32);  // the workers' value-byte totals (or their exit)
+    const uint32_t tile = S.tile[b];
+    if (tile >= P.n_tiles) break;
+    bar_sync(BAR_V2, NTF_);     // the entry column
+    uint64_t cagg[K3];
+    const uint32_t col_in = S.col_in;
+    const uint32_t nrel = min(S.n_rel, n_cols);
+#pragma unroll
+    for (int k = 0; k < K3; ++k) cagg[k] = k < P.n_str ? S.ctot[k] : 0u;
+    // row-0 fields: column = entry column + index (at most n_cols of them,
+    // summed by one lane and broadcast)
+    uint32_t add[K3];
+#pragma unroll
+    for (int q = 0; q < K3; ++q) add[q] = 0;
+    if (lane == 0)
+      for (uint32_t k = 0; k < nrel && col_in + k < n_cols; ++k) {
+        const int si = P.stridx[col_in + k];
+        const uint32_t len = S.rel_len[k];
+#pragma unroll
+        for (int q = 0; q < K3; ++q)
+          if (q == si) add[q] += len;
+      }
+#pragma unroll
+    for (int q = 0; q < K3; ++q) cagg[q] += __shfl_sync(FULL, add[q], 0);
+    uint64_t zero[K3], ex[K3];
+#pragma unroll
+    for (int k = 0; k < K3; ++k) zero[k] = 0;
+    if (P.dbg_withhold && tile == 0) {
+#pragma unroll
+      for (int k = 0; k < K3; ++k) ex[k] = 0;
+    } else {
+      lookback_vec<K3>(P.s.c_flag, P.s.c_agg, P.s.c_inc, tile, cagg, zero, zero, AddOp<K3>{},
+                       cfg, ex);
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int k = 0; k < K3; ++k)
+        if (k < P.n_str) S.base[k] = ex[k];
+      if (tile + 1 == P.n_tiles)  // the input's chars per string column
+#pragma unroll
+        for (int k = 0; k < K3; ++k)
+          if (k < P.n_str) P.st->chars_len[P.strcol[k]] = ex[k] + cagg[k];
+    }
+    __syncwarp();
+    bar_arrive(BAR_CHR, NT + 32);
+  }
+}
+
+// ----------------------------------------------------------------- kernel
+template <int NS>
+__global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_constant__ ParseParams P) {
+  constexpr int NTF = ntf_of<NS>();
+  constexpr int NSW = NS > 0 ? (NS + 3) / 4 : 1;
   extern __shared__ __align__(128) uint8_t smem[];
   uint32_t* lut_s = reinterpret_cast<uint32_t*>(smem);
-  uint8_t* lin0 = smem + LUT_BYTES;  // two tile buffers
-  uint8_t* stage_s = lin0 + 2 * TILE;
+  uint8_t* lin0 = smem + LUT_BYTES;  // two landing buffers
+  uint8_t* stage_s = lin0 + 2 * BUF_BYTES;
   uint32_t* slot_s = reinterpret_cast<uint32_t*>(stage_s + STAGE_BYTES);
   uint32_t* ctrl_s = slot_s + SLOT_CAP;
   uint16_t* pos_s = reinterpret_cast<uint16_t*>(ctrl_s + NT);  // chars end per string field
-  MainShared& S = *reinterpret_cast<MainShared*>(pos_s + SLOT_CAP);
+  PShared& S = *reinterpret_cast<PShared*>(pos_s + SLOT_CAP);
 
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  load_lut(P, lut_s);
-  for (int k = t; k < PP_MAX_COLS; k += NT) S.coltype[k] = P.coltype[k];
+  const uint32_t toff = uint32_t(reinterpret_cast<uintptr_t>(P.in) & 15u);
+  for (int k = t; k < 256 * 32; k += NTF) lut_s[k] = P.lut[k >> 5];
+  for (int k = t; k < 256; k += NTF) S.lut1[k] = P.lut[k];
+  if (t < PP_MAX_COLS) S.coltype[t] = P.coltype[t];
+  if (t < ppi::MAX_STR_COLS) S.carry[t] = 0;
   if (t == 0) {
     uint32_t m = 0;
     for (uint32_t c = 0; c < uint32_t(P.n_cols); ++c)
@@ -1280,488 +1099,544 @@ __global__ void __launch_bounds__(NT, 2) main_kernel(const __grid_constant__ Par
           P.coltype[c] != PP_COL_FLOAT64)
         S.numcol[m++] = uint8_t(c);
     S.n_num = P.has_out ? m : 0u;
+    S.cpl[NT] = 0;
   }
-  for (int k = t; k < ppi::MAX_STR_COLS; k += NT) S.carry[k] = 0;
+  if (warp == NW && lane == 0) {  // the first ticket and its copy
+    mbar_init(&S.bar[0], 1);
+    mbar_init(&S.bar[1], 1);
+    const uint32_t first = atomicAdd(&P.s.counters[0], 1u);
+    S.tile[0] = first;
+    S.issued[0] = issue_span(P, first, toff, lin0, &S.bar[0]);
+    S.wpar[0] = 0;
+    S.tile[1] = 0xFFFFFFFFu;
+    S.issued[1] = 0;
+    S.wpar[1] = 0;
+  }
+  __syncthreads();
+  if (warp == NW) {
+    ctx_role<NS>(P, S);
+    return;
+  }
+  if (warp == NW + 1) {
+    chars_role<NS>(P, S);
+    return;
+  }
+
   const uint32_t* my_lut = lut_s + lane;
   const uint32_t n_cols = uint32_t(P.n_cols);
   const uint32_t n_str = NS > 0 ? uint32_t(P.n_str) : 0u;
-  const uint32_t rpb = max(1u, uint32_t(SLOT_CAP) / n_cols);  // rows per pass
-  const bool aligned_in = (reinterpret_cast<uintptr_t>(P.in) & 15) == 0;
-  uint32_t* counter = &P.s.counters[1];
-  uint32_t tk = 0;  // thread 0: the next ticket
-  feed_start(P, S.F, counter, aligned_in, lin0, tk);
+  const uint32_t rpb = max(1u, (uint32_t(SLOT_CAP) - n_cols) / n_cols);  // rows per pass
+  const bool partial = P.record_end != nullptr;
 
-  for (;;) {
-    const uint32_t tile = S.F.tile[S.F.cur];
-    if (tile >= P.n_tiles) break;
-    uint8_t* tile_s = lin0 + S.F.cur * TILE;
-    const uint32_t* tile_w = reinterpret_cast<const uint32_t*>(tile_s);
+  uint32_t nph[2] = {S.issued[0], 0u};  // thread 0: bulk copies started per buffer
+  // The next tile's ticket and bulk copy (thread 0), taken late in the
+  // current tile so that tiles start in ticket order and a tile's
+  // predecessors have posted their aggregates when it looks back; the copy
+  // goes to the buffer of the tile before, which is no longer read.
+  auto next_ticket = [&](uint32_t b) {
+    if (t != 0) return;
+    const uint32_t o = b ^ 1u;
+    const uint32_t nt = atomicAdd(&P.s.counters[0], 1u);
+    const uint32_t iss = issue_span(P, nt, toff, lin0 + o * BUF_BYTES, &S.bar[o]);
+    S.tile[o] = nt;
+    S.issued[o] = iss;
+    S.wpar[o] = nph[o] & 1u;
+    nph[o] += iss;
+  };
+
+  for (uint32_t it = 0;; ++it) {
+    const uint32_t b = it & 1u;
+    const uint32_t tile = S.tile[b];
+    if (tile >= P.n_tiles) {
+      bar_arrive(BAR_AGG, NT + 32);  // the scan warps see the end too
+      if (NS > 0) bar_arrive(BAR_W2, NT + 32);
+      break;
+    }
+    uint8_t* buf = lin0 + b * BUF_BYTES;
+    const uint8_t* tile_s = buf + toff;
+    const uint32_t* raw_w = reinterpret_cast<const uint32_t*>(buf);
     const uint64_t tile_base = uint64_t(tile) * TILE;
     const uint32_t tile_len = uint32_t(min(uint64_t(TILE), P.n - tile_base));
     const bool last_tile = tile + 1 == P.n_tiles;
-    const uint8_t* pr = P.s.pre + size_t(tile) * P.s.pre_stride;
-    const PreHdr ph = *reinterpret_cast<const PreHdr*>(pr);
-    if (NS > 0 && t < int(n_str)) S.base[t] = reinterpret_cast<const uint64_t*>(pr + PRE_HDR)[t];
+    const uint32_t s_tile = P.s.tile_state[tile];
+    if (t < ppi::MAX_STR_COLS) S.ctot[t] = 0;
+    if (t < PP_MAX_COLS) S.rel_len[t] = 0;
+    if (t == 0) { S.n_rel = 0; S.rd0_pos = 0; S.rd0_k = 0; S.virt = 0; }
+
+    // ---- the tile's bytes: bulk copy, plus plain loads at the input's ends
+    {
+      const uint32_t iss = S.issued[b];
+      const Span sp = iss ? bulk_span(P, tile, toff) : Span{0, 0};
+      if (iss && !mbar_wait_bounded(&S.bar[b], S.wpar[b], WAIT_LIMIT)) {
+        if (t == 0) report(P.st, PP_ERR_LOOKBACK_TIMEOUT, 0, false);
+        mbar_wait_bounded(&S.bar[b], S.wpar[b], WAIT_LIMIT);
+      }
+      const uint32_t h0 = iss ? uint32_t(max(sp.c0, 0)) : tile_len;  // [0, h0) plain
+      const uint32_t h1 = iss ? uint32_t(min(sp.c1, int32_t(tile_len))) : tile_len;
+      if (h0 > 0 || h1 < tile_len) {
+        for (uint32_t k = t; k < h0; k += NT) buf[toff + k] = P.in[tile_base + k];
+        for (uint32_t k = h1 + t; k < tile_len; k += NT) buf[toff + k] = P.in[tile_base + k];
+        bar_sync(BAR_W, NT);
+      }
+    }
     uint32_t w[8];
-    feed_tile(P, S.F, counter, aligned_in, lin0, tile_base, tile_len, w, tk);
+    load_chunk(buf, toff, uint32_t(t), w);
     const uint32_t cstart = uint32_t(t) * CB;
     const uint32_t clen = tile_len > cstart ? min(tile_len - cstart, uint32_t(CB)) : 0u;
     const uint8_t* own = tile_s + cstart;
 
-    // ---- the chunk's tags: stored by the context pass, or (without room
-    // for them in the scratch) re-run here from the chunk's start state, the
-    // tile's being known from the scan.  The context pass reports invalid
-    // input and a bad end state.
-    Tags g;
-    if (P.s.tags) {
-      const uint4 v = P.s.tags[size_t(tile) * NT + t];
-      g = {v.x, v.y, v.z, 32u, (v.w & 0xFFFFu) << 8, v.w >> 16};
-    } else {
-      uint32_t G, special, special_x;
-      stv_pass(w, clen, tile_s, cstart, my_lut, G, special, special_x);
-      const uint32_t lane_ex = block_stv(G, S.warp_stv, &S.tile_stv);
-      const uint32_t s_tile = ph.state & 0xFFu;
-      const uint32_t s_chunk = stv_apply(lane_ex, stv_apply(S.warp_stv[warp], s_tile));
-      g = tag_chunk(s_chunk, special, special_x, P.sticky, clen, cstart, own, my_lut, P.bg_next);
-    }
+    // ---- chunk start states and tags (ParPaRaw Section 3.1)
+    uint32_t G, special, special_x;
+    stv_pass(w, clen, tile_s, cstart, my_lut, G, special, special_x);
+    const uint32_t lane_ex = block_stv_w(G, S.warp_stv);
+    const uint32_t st = stv_apply(lane_ex, stv_apply(S.warp_stv[warp], s_tile));
+    const Tags g = tag_chunk(st, special, special_x, P.sticky, clen, cstart, own, my_lut,
+                             P.bg_next);
+    if (g.inv_at < clen && st != 4)
+      report(P.st, PP_ERR_INVALID_INPUT, tile_base + cstart + g.inv_at, true);
+    const bool owns_end = last_tile && clen > 0 && cstart + clen == tile_len;
+    const bool accepting = g.end != 4 && ((P.accept_mask >> g.end) & 1u);
+    if (!partial && owns_end && g.end != 4 && !accepting)  // an invalid end is reported where it began
+      report(P.st, PP_ERR_BAD_END_STATE, P.n, true);
+    const bool virt_rd = !partial && owns_end && accepting && !((g.rd >> (clen - 1)) & 1u);
     const uint32_t fd = g.fd, rd = g.rd;
     ctrl_s[t] = g.ctrl;
-    const bool owns_end = last_tile && clen > 0 && cstart + clen == tile_len;
-    const bool partial = P.record_end != nullptr;
-    const bool virt_rd = !partial && owns_end && g.end != 4 && ((P.accept_mask >> g.end) & 1u) &&
-                         !((rd >> (clen - 1)) & 1u);
 
-    // ---- record, column and field start at the chunk start: stored by the
-    // context pass with the tags, or a block scan here
-    V2 pre;
-    bool any_ctrl, any_virt;
-    uint32_t rows, col_end_raw;  // records touched by the tile; fields of its last row
-    if (P.s.vpre) {
-      const uint2 pv = P.s.vpre[size_t(tile) * NT + t];
-      pre = {pv.x & 0xFFFFu, (pv.y & 0x7FFFu) | ((pv.y & 0x8000u) ? ABS32 : 0u), (pv.x >> 16) << 8};
-      any_ctrl = P.s.tile_flags[tile] != 0;
-      V2 x = {0u, 0u, 0u};  // the tile's totals: the record's slot of the true start state
-      const uint32_t s_tile = ph.state & 0xFFu;
-      if (s_tile < 4) {
-        const uint32_t* cr = reinterpret_cast<const uint32_t*>(P.s.ctx + size_t(tile) * P.s.ctx_stride);
-        x = {cr[1 + 3 * s_tile], cr[2 + 3 * s_tile], cr[3 + 3 * s_tile]};
-      }
-      rows = x.rec + 1;
-      if (x.col & ABS32) {
-        col_end_raw = x.col & ~ABS32;
-      } else {
-        const uint64_t c = uint64_t(ph.col_in) + x.col;
-        col_end_raw = c > 0x7FFFFF00ull ? 0x7FFFFF00u : uint32_t(c);
-      }
-      any_virt = false;  // the chunk that owns the input's end closes a last record
-      if (last_tile && !partial) {
-        const uint32_t ot = (tile_len - 1) / CB;
-        const uint4 ov = P.s.tags[size_t(tile) * NT + ot];
-        const uint32_t oend = ov.w >> 16;
-        any_virt = oend != 4 && ((P.accept_mask >> oend) & 1u) &&
-                   !((ov.y >> (tile_len - 1 - ot * CB)) & 1u);
-      }
-    } else {
-      V2 vi = chunk_v2(g);
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const V2 o = shfl_up_v2(vi, d);
-        if (lane >= d) vi = op2_32(o, vi);
-      }
-      V2 lex = shfl_up_v2(vi, 1);
-      if (lane == 0) lex = {0u, 0u, 0u};
-      if (lane == 31) { S.warp_rec[warp] = vi.rec; S.warp_col[warp] = vi.col; S.warp_last[warp] = vi.last; }
-      any_ctrl = __syncthreads_or(g.ctrl != 0) != 0;
-      if (warp == 0) {
-        V2 x = lane < NW ? V2{S.warp_rec[lane], S.warp_col[lane], S.warp_last[lane]} : V2{0u, 0u, 0u};
-#pragma unroll
-        for (int d = 1; d < NW; d <<= 1) {
-          const V2 o = shfl_up_v2(x, d);
-          if (lane >= d) x = op2_32(o, x);
-        }
-        V2 xe = shfl_up_v2(x, 1);
-        if (lane == 0) xe = {0u, 0u, 0u};
-        __syncwarp();
-        if (lane < NW) { S.warp_rec[lane] = xe.rec; S.warp_col[lane] = xe.col; S.warp_last[lane] = xe.last; }
-        if (lane == NW - 1) {
-          S.rows = x.rec + 1;
-          if (x.col & ABS32) {
-            S.col_end = x.col & ~ABS32;
-          } else {
-            const uint64_t c = uint64_t(ph.col_in) + x.col;
-            S.col_end = c > 0x7FFFFF00ull ? 0x7FFFFF00u : uint32_t(c);
-          }
-        }
-      }
-      any_virt = __syncthreads_or(virt_rd) != 0;
-      pre = op2_32(V2{S.warp_rec[warp], S.warp_col[warp], S.warp_last[warp]}, lex);
-      rows = S.rows;
-      col_end_raw = S.col_end;
-    }
-    const uint64_t rec0 = ph.rec0;
-    const uint32_t col_in = ph.col_in;
-    const uint32_t col_end = any_virt ? n_cols : col_end_raw;
-    uint32_t col0;
-    if (pre.col & ABS32) {
-      col0 = pre.col & ~ABS32;
-    } else {
-      const uint64_t c = uint64_t(col_in) + pre.col;
-      col0 = c > 0x7FFFFF00ull ? 0x7FFFFF00u : uint32_t(c);
-    }
-    // the field open at the tile start: global start and DFA state there
-    const uint64_t tile_fstart = ph.last1;
-    const uint32_t tile_fstate = ph.last1 ? (ph.state >> 8) & 0xFFu : uint32_t(P.start_state);
-    const uint32_t fs_tile = tile_fstart >= tile_base ? uint32_t(tile_fstart - tile_base) : 0xFFFFu;
-    const uint32_t fs0 = pre.last ? (pre.last >> 8) : fs_tile;  // field open at the chunk start
-    const uint32_t rl0 = pre.rec;
-    const uint32_t term_all = fd | rd;
-    const bool owns_tail = clen > 0 && cstart + clen == tile_len;
-    // terminators per chunk (plus the virtual RD that closes the input),
-    // their prefix in the warp and the warp's count
-    const uint32_t nterm = __popc(term_all) + (virt_rd ? 1u : 0u);
-    uint32_t tincl = nterm;
+    // ---- (records, column, last), terminators and control bytes, scanned
+    // over the warp and then over the warps
+    V2 vi = chunk_v2(g);
+    const uint32_t t_own = __popc(fd | rd) + (virt_rd ? 1u : 0u), c_own = __popc(g.ctrl);
+    uint32_t ti = t_own, ci = c_own;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
-      const uint32_t o = __shfl_up_sync(FULL, tincl, d);
-      if (lane >= d) tincl += o;
-    }
-    const uint32_t tbase = tincl - nterm, wn = __shfl_sync(FULL, tincl, 31);
-    if (any_ctrl) {  // control bytes before each chunk: O(1) value-byte counts
-      const uint32_t nc = __popc(g.ctrl);
-      uint32_t xi = nc;
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const uint32_t o = __shfl_up_sync(FULL, xi, d);
-        if (lane >= d) xi += o;
+      const V2 o = shfl_up_v2(vi, d);
+      const uint32_t ot = __shfl_up_sync(FULL, ti, d), oc = __shfl_up_sync(FULL, ci, d);
+      if (lane >= d) {
+        vi = op2_32(o, vi);
+        ti += ot;
+        ci += oc;
       }
-      if (lane == 31) S.wsum[warp] = xi;
-      __syncthreads();
-      if (warp == 0) {
-        const uint32_t v = lane < NW ? S.wsum[lane] : 0u;
-        uint32_t x = v;
+    }
+    V2 vex = shfl_up_v2(vi, 1);
+    if (lane == 0) vex = {0u, 0u, 0u};
+    if (lane == 31) {
+      S.wv[warp][0] = vi.rec; S.wv[warp][1] = vi.col; S.wv[warp][2] = vi.last;
+      S.wt[warp] = ti;
+      S.wc[warp] = ci;
+    }
+    S.cpl[t] = uint16_t(ci - c_own);
+    if (partial) {
+      const uint32_t wm = __reduce_max_sync(FULL, rd ? cstart + 32u - __clz(rd) : 0u);
+      if (lane == 0) S.wrd[warp] = wm;
+    }
+    if (virt_rd) S.virt = 1;
+    bar_sync(BAR_W, NT);
+    if (warp == 0) {
+      V2 x = lane < NW ? V2{S.wv[lane][0], S.wv[lane][1], S.wv[lane][2]} : V2{0u, 0u, 0u};
+      const uint32_t t0 = lane < NW ? S.wt[lane] : 0u, c0 = lane < NW ? S.wc[lane] : 0u;
+      uint32_t xt = t0, xc = c0;
 #pragma unroll
-        for (int d = 1; d < NW; d <<= 1) {
-          const uint32_t o = __shfl_up_sync(FULL, x, d);
-          if (lane >= d) x += o;
+      for (int d = 1; d < NW; d <<= 1) {
+        const V2 o = shfl_up_v2(x, d);
+        const uint32_t ot = __shfl_up_sync(FULL, xt, d), oc = __shfl_up_sync(FULL, xc, d);
+        if (lane >= d) {
+          x = op2_32(o, x);
+          xt += ot;
+          xc += oc;
         }
-        __syncwarp();
-        if (lane < NW) S.wsum[lane] = x - v;
-        if (lane == NW - 1) S.cpre[NT] = uint16_t(x);
       }
-      __syncthreads();
-      S.cpre[t] = uint16_t(S.wsum[warp] + xi - nc);
+      V2 xe = shfl_up_v2(x, 1);
+      if (lane == 0) xe = {0u, 0u, 0u};
+      __syncwarp();
+      if (lane < NW) {
+        S.wv[lane][0] = xe.rec; S.wv[lane][1] = xe.col; S.wv[lane][2] = xe.last;
+        S.wt[lane] = xt - t0;
+        S.wc[lane] = xc - c0;
+      }
+      if (lane == NW - 1) {
+        S.agg_rec = x.rec;
+        S.agg_col = x.col;
+        S.agg_last = x.last;
+        S.n_ctrl = xc;
+        S.wc[NW] = xc;
+      }
+      if (partial && lane == 0) {  // 1 + the tile's last record delimiter
+        uint32_t m = 0;
+        for (int q = 0; q < NW; ++q) m = max(m, S.wrd[q]);
+        if (m) atomicMax(P.record_end, static_cast<unsigned long long>(tile_base + m));
+      }
     }
+    bar_sync(BAR_W, NT);
+    bar_arrive(BAR_AGG, NT + 32);  // the context warp may post the tile's aggregate
 
-    const NumCtx X = {tile_base, tile_fstart, tile_fstate, tile_s, tile_w, ctrl_s, S.cpre, my_lut,
-                      any_ctrl};
-    const uint32_t rec_lim =  // records of the tile the outputs have room for
-        P.rec_cap > rec0 ? uint32_t(min(P.rec_cap - rec0, uint64_t(0xFFFFFFFFu))) : 0u;
+    const V2 pre = op2_32(V2{S.wv[warp][0], S.wv[warp][1], S.wv[warp][2]}, vex);
+    const bool any_ctrl = S.n_ctrl != 0;
+    const bool any_virt = S.virt != 0;
+    const uint32_t rows = S.agg_rec + 1;   // records touched by the tile (row 0: the one open at its start)
+    const uint32_t rl0 = pre.rec;          // row at the chunk start
+    const uint32_t col0 = pre.col & ~ABS32;  // column there; for row 0, the index in the row
+    const uint32_t fs0 = pre.last ? (pre.last >> 8) : REL_START;  // start of the field open there
+    const uint32_t term_all = fd | rd;
+    const bool owns_tail = clen > 0 && cstart + clen == tile_len;
+    const uint32_t tbase = ti - t_own;
+    const uint32_t wn = __shfl_sync(FULL, ti, 31);
+
+    // filled after the look-back
+    uint64_t rec0 = 0;
+    uint32_t col_in = 0, col_end = 0;
+    // the conversion context; the field open at the tile start is known
+    // only after the look-back, and only row 0 needs it
+    NumCtx X{tile_base, 0ull, uint32_t(P.start_state), tile_s, raw_w, toff, ctrl_s, &S.wc[0],
+             &S.cpl[0], &S.lut1[0], any_ctrl};
+
 
     // ---- fields -> (column, row) slots, in passes of rows
-    {
-      for (uint32_t lo = 0; lo < rows; lo += rpb) {
-        const uint32_t hi = min(rows, lo + rpb), nr = hi - lo;
-        if (NS > 0) { S.lk[0][t] = NO_FIELD; S.lk[1][t] = NO_FIELD; }
-        if (wn <= WLIST_CAP) {
-          // the warp's terminators in input order (tile position | RD << 15),
-          // then a lane per field: row and column from a ballot of the RDs
-          uint16_t* const wl = reinterpret_cast<uint16_t*>(stage_s) + warp * WLIST_CAP;
-          {
-            uint32_t m = term_all, i = tbase;
-            while (m) {
-              const uint32_t j = __ffs(m) - 1;
-              m &= m - 1;
-              wl[i++] = uint16_t((cstart + j) | (((rd >> j) & 1u) << 15));
+    for (uint32_t lo = 0; lo < rows; lo += rpb) {
+      const uint32_t hi = min(rows, lo + rpb), nr = hi - lo;
+      const uint32_t nrp = nr | 1u;  // odd stride: a warp's column-wise writes hit distinct banks
+      const bool first = lo == 0;
+      uint64_t cnt[NSW];  // value bytes per string column of rows >= 1 (packed 16-bit)
+#pragma unroll
+      for (int k = 0; k < NSW; ++k) cnt[k] = 0;
+      if (NS > 0) { S.lk[0][t] = NO_FIELD; S.lk[1][t] = NO_FIELD; }
+      // One field: row rl, column (row 0: index) col, tile span [fs, e).
+      auto enter = [&](uint32_t rl, uint32_t col, uint32_t fs, uint32_t e, bool isrd, bool open) {
+        const bool in_pass = rl - lo < nr;
+        if (rl == 0) {
+          if (first) {
+            if (col < n_cols) {
+              S.rel_slot[col] = (fs << 16) | e;
+              const uint32_t L = value_len(fs, e, any_ctrl, ctrl_s, S);
+              if (L) atomicAdd(&S.rel_len[col], L);
+              atomicMax(&S.n_rel, col + 1);
             }
-            if (virt_rd) wl[i] = uint16_t(tile_len | 0x8000u);
+            if (isrd) { S.rd0_pos = e + 1; S.rd0_k = col; }
           }
-          __syncwarp();
-          // row, column and field start before the batch's first field
-          uint32_t crow = __shfl_sync(FULL, rl0, 0), ccol = __shfl_sync(FULL, col0, 0),
-                   cfs = __shfl_sync(FULL, fs0, 0);
-          const uint32_t lt = (1u << lane) - 1u;
-          for (uint32_t b0 = 0; b0 < wn; b0 += 32) {
-            const uint32_t k = b0 + uint32_t(lane);
-            const uint32_t ent = k < wn ? uint32_t(wl[k]) : 0u;
-            const uint32_t e = ent & 0x7FFFu;
-            const bool isrd = (ent >> 15) != 0;
-            const uint32_t pe = __shfl_up_sync(FULL, e, 1);
-            const uint32_t fs = lane == 0 ? cfs : pe + 1u;
-            const uint32_t rdm = __ballot_sync(FULL, isrd);
-            const uint32_t below = rdm & lt;
-            const uint32_t rl = crow + __popc(below);
-            const uint32_t col = below ? uint32_t(lane) - (32u - __clz(below))
-                                       : min(ccol + uint32_t(lane), 0x7FFFFF00u);
-            if (k < wn) {
-              const bool in_pass = rl - lo < nr;
-              if (in_pass && col < n_cols) slot_s[col * nr + (rl - lo)] = (fs << 16) | e;
-              if (isrd && col != n_cols - 1) {
-                if (lo == 0) report(P.st, PP_ERR_COLCOUNT, tile_base + e, true);
-                if (in_pass)  // missing fields take the column default
-                  for (uint32_t c = col + 1; c < n_cols; ++c) slot_s[c * nr + (rl - lo)] = SLOT_DEFAULT;
-              }
-            }
-            const uint32_t nin = min(32u, wn - b0);
-            crow += __popc(rdm);
-            ccol = rdm ? (nin - 1u) - (31u - __clz(rdm)) : min(ccol + nin, 0x7FFFFF00u);
-            cfs = __shfl_sync(FULL, e, nin - 1) + 1u;
-          }
-          // the field still open at the tile end (its value bytes are staged)
-          if (NS > 0 && owns_tail && !any_virt && crow - lo < nr && ccol < n_cols)
-            slot_s[ccol * nr + (crow - lo)] = (cfs << 16) | tile_len;
-        } else {  // each lane walks its chunk's fields
-          uint32_t term = term_all, col = col0, rl = rl0, fs = fs0;
-          bool vrd = virt_rd;
-          for (;;) {
-            uint32_t e;
-            bool isrd;
-            if (term) {
-              const uint32_t j = __ffs(term) - 1;
-              term &= term - 1;
-              e = cstart + j;
-              isrd = (rd >> j) & 1u;
-            } else if (vrd) {
-              e = tile_len;
-              isrd = true;
-              vrd = false;
-            } else {
-              break;
-            }
-            const bool in_pass = rl - lo < nr;
-            if (in_pass && col < n_cols) slot_s[col * nr + (rl - lo)] = (fs << 16) | e;
-            if (isrd) {
-              if (col != n_cols - 1) {
-                if (lo == 0) report(P.st, PP_ERR_COLCOUNT, tile_base + e, true);
-                if (in_pass)  // missing fields take the column default
-                  for (uint32_t c = col + 1; c < n_cols; ++c) slot_s[c * nr + (rl - lo)] = SLOT_DEFAULT;
-              }
-              ++rl;
-              col = 0;
-            } else {
-              col = col < 0x7FFFFF00u ? col + 1 : col;
-            }
-            fs = e + 1;
-          }
-          // the field still open at the tile end (its value bytes are staged)
-          if (NS > 0 && owns_tail && !any_virt && rl - lo < nr && col < n_cols)
-            slot_s[col * nr + (rl - lo)] = (fs << 16) | tile_len;
+          return;
         }
-        __syncthreads();
-        const uint32_t ngr = (nr + 31) / 32;
-        if (lo == 0 && P.s.tags) {  // the next tile's stored tags and prefixes, towards L2
-          const uint32_t nt = S.F.tile[S.F.cur ^ 1u];  // taken before the barrier above
-          if (nt < P.n_tiles) {
-            if ((t & 7) == 0) prefetch_l2(P.s.tags + size_t(nt) * NT + t);
-            if ((t & 15) == 0) prefetch_l2(P.s.vpre + size_t(nt) * NT + t);
+        if (in_pass && col < n_cols) slot_s[col * nrp + (rl - lo)] = (fs << 16) | e;
+        if (NS > 0 && first && col < n_cols && ((P.strmask >> col) & 1u)) {
+          const uint32_t L = value_len(fs, e, any_ctrl, ctrl_s, S);
+          if (L) add16(cnt, P.stridx[col], L);
+        }
+        if (isrd && !open && col != n_cols - 1) {
+          if (first) report(P.st, PP_ERR_COLCOUNT, tile_base + e, true);
+          if (in_pass)  // missing fields take the column default
+            for (uint32_t c = col + 1; c < n_cols; ++c) slot_s[c * nrp + (rl - lo)] = SLOT_DEFAULT;
+        }
+      };
+      if (wn <= WLIST_CAP) {
+        // the warp's terminators in input order (tile position | RD << 15),
+        // then a lane per field: row and column from a ballot of the RDs
+        uint16_t* const wl = reinterpret_cast<uint16_t*>(stage_s) + warp * WLIST_CAP;
+        {
+          uint32_t m = term_all, i = tbase;
+          while (m) {
+            const uint32_t j = __ffs(m) - 1;
+            m &= m - 1;
+            wl[i++] = uint16_t((cstart + j) | (((rd >> j) & 1u) << 15));
+          }
+          if (virt_rd) wl[i] = uint16_t(tile_len | 0x8000u);
+        }
+        __syncwarp();
+        uint32_t crow = __shfl_sync(FULL, rl0, 0), ccol = __shfl_sync(FULL, col0, 0),
+                 cfs = __shfl_sync(FULL, fs0, 0);
+        const uint32_t lt = (1u << lane) - 1u;
+        for (uint32_t b0 = 0; b0 < wn; b0 += 32) {
+          const uint32_t k = b0 + uint32_t(lane);
+          const uint32_t ent = k < wn ? uint32_t(wl[k]) : 0u;
+          const uint32_t e = ent & 0x7FFFu;
+          const bool isrd = (ent >> 15) != 0;
+          const uint32_t pe = __shfl_up_sync(FULL, e, 1);
+          const uint32_t fs = lane == 0 ? cfs : pe + 1u;
+          const uint32_t rdm = __ballot_sync(FULL, k < wn && isrd);
+          const uint32_t below = rdm & lt;
+          const uint32_t rl = crow + __popc(below);
+          const uint32_t col = below ? uint32_t(lane) - (32u - __clz(below))
+                                     : min(ccol + uint32_t(lane), 0x7FFFFF00u);
+          if (k < wn) enter(rl, col, fs, e, isrd, false);
+          const uint32_t nin = min(32u, wn - b0);
+          crow += __popc(rdm);
+          ccol = rdm ? (nin - 1u) - (31u - __clz(rdm)) : min(ccol + nin, 0x7FFFFF00u);
+          cfs = __shfl_sync(FULL, e, nin - 1) + 1u;
+        }
+        // the field still open at the tile end (its value bytes are counted
+        // and staged here)
+        if (owns_tail && !any_virt) enter(crow, ccol, cfs, tile_len, false, true);
+      } else {  // each lane walks its chunk's fields
+        uint32_t term = term_all, col = col0, rl = rl0, fs = fs0;
+        bool vrd = virt_rd;
+        for (;;) {
+          uint32_t e;
+          bool isrd;
+          if (term) {
+            const uint32_t j = __ffs(term) - 1;
+            term &= term - 1;
+            e = cstart + j;
+            isrd = (rd >> j) & 1u;
+          } else if (vrd) {
+            e = tile_len;
+            isrd = true;
+            vrd = false;
+          } else {
+            break;
+          }
+          enter(rl, col, fs, e, isrd, false);
+          if (isrd) { ++rl; col = 0; }
+          else col = col < 0x7FFFFF00u ? col + 1 : col;
+          fs = e + 1;
+        }
+        if (owns_tail && !any_virt) enter(rl, col, fs, tile_len, false, true);
+      }
+      if (NS > 0 && first) {  // warp sums of the packed counters -> tile totals
+        bool any = false;
+#pragma unroll
+        for (int k = 0; k < NSW; ++k) any |= cnt[k] != 0;
+        if (__any_sync(FULL, any)) {
+#pragma unroll
+          for (int k = 0; k < NSW; ++k) {
+            uint64_t v = cnt[k];
+#pragma unroll
+            for (int d = 16; d; d >>= 1) v += __shfl_xor_sync(FULL, v, d);
+            if (lane < 4 && 4 * k + lane < int(n_str)) {
+              const uint32_t x = uint32_t(v >> (16 * lane)) & 0xFFFFu;
+              if (x) atomicAdd(&S.ctot[4 * k + lane], x);
+            }
           }
         }
+      }
+      if (first) {
+        if (NS > 0) bar_arrive(BAR_W2, NT + 32);
+        // ---- the tile's context from the look-back
+        bar_sync(BAR_V2, NTF);
+        rec0 = S.rec0;
+        X.tile_fstart = S.last1;
+        X.tile_fstate = S.last1 ? (S.lst & 0xFFu) : uint32_t(P.start_state);
+        col_in = S.col_in;
+        {
+          const uint32_t ac = S.agg_col;
+          if (ac & ABS32) {
+            col_end = ac & ~ABS32;
+          } else {
+            const uint64_t c = uint64_t(col_in) + ac;
+            col_end = c > 0x7FFFFF00ull ? 0x7FFFFF00u : uint32_t(c);
+          }
+          if (any_virt) col_end = n_cols;
+        }
+        // row 0: its fields' columns follow the entry column
+        const uint32_t nrel = S.n_rel;
+        if (uint32_t(t) < nrel && col_in + t < n_cols) slot_s[(col_in + t) * nrp] = S.rel_slot[t];
+        if (S.rd0_pos) {
+          const uint32_t nf = col_in + S.rd0_k + 1;  // fields of the record
+          if (nf != n_cols) {
+            if (t == 0) report(P.st, PP_ERR_COLCOUNT, tile_base + S.rd0_pos - 1, true);
+            for (uint32_t c = nf + t; c < n_cols; c += NT) slot_s[c * nrp] = SLOT_DEFAULT;
+          }
+        }
+      }
+      bar_sync(BAR_W, NT);
+      if (!P.has_out) {  // a sizing pass: counts only
+        next_ticket(b);
+        if (NS > 0 && n_str) bar_sync(BAR_CHR, NT + 32);
+        break;
+      }
+      const uint32_t ngr = (nr + 31) / 32;
+      const uint32_t rec_lim =  // records of the tile the outputs have room for
+          P.rec_cap > rec0 ? uint32_t(min(P.rec_cap - rec0, uint64_t(0xFFFFFFFFu))) : 0u;
 
-        if (NS > 0 && n_str) {
-          // ---- string fields: value bytes -> chars positions (block scan
-          // over the column-major items), then staging copies
-          const uint32_t n_items = n_str * nr;
-          const uint32_t per = (n_items + NT - 1) / NT;  // <= SLOT_CAP / NT
-          const uint32_t k0 = min(n_items, uint32_t(t) * per), k1 = min(n_items, k0 + per);
-          // value bytes per field (into pos_s for now), long fields mark their chunks
-          uint32_t mysum = 0;
-          {
-            uint32_t si = k0 / nr, r = k0 - si * nr;
-            for (uint32_t k = k0; k < k1; ++k) {
-              uint32_t len = 0;
-              const uint32_t c = P.strcol[si];
-              const uint32_t row = lo + r;
-              const bool closed = (row > 0 || c >= col_in) && (row + 1 < rows || c < col_end);
-              const bool open = row + 1 == rows && c == col_end && !any_virt;
-              if (closed || open) {
-                const uint32_t v = slot_s[c * nr + r];
-                if (v != SLOT_DEFAULT) {
-                  const bool before = (v >> 16) == 0xFFFFu;
-                  const uint32_t a0 = before ? 0u : (v >> 16), e = v & 0xFFFFu;
-                  len = (e - a0) - (any_ctrl ? ctrl_before(ctrl_s, S.cpre, e) -
-                                                   ctrl_before(ctrl_s, S.cpre, a0) : 0u);
-                  if (len > SHORT_FIELD) {  // mark the chunks of a long field
-                    const uint32_t c0 = a0 >> 5, c1 = (e - 1) >> 5;
-                    S.lk[before ? 0 : 1][c0] = uint16_t(k);
-                    for (uint32_t cc = c0 + 1; cc <= c1; ++cc) S.lk[0][cc] = uint16_t(k);
-                  }
+      if (NS > 0 && n_str) {
+        // ---- string fields: value bytes -> chars positions (block scan
+        // over the column-major items), then staging copies
+        const uint32_t n_items = n_str * nr;
+        const uint32_t per = (n_items + NT - 1) / NT;  // <= SLOT_CAP / NT
+        const uint32_t k0 = min(n_items, uint32_t(t) * per), k1 = min(n_items, k0 + per);
+        uint32_t mysum = 0;
+        {
+          uint32_t si = k0 / nr, r = k0 - si * nr;
+          for (uint32_t k = k0; k < k1; ++k) {
+            uint32_t len = 0;
+            const uint32_t c = P.strcol[si];
+            const uint32_t row = lo + r;
+            const bool closed = (row > 0 || c >= col_in) && (row + 1 < rows || c < col_end);
+            const bool open = row + 1 == rows && c == col_end && !any_virt;
+            if (closed || open) {
+              const uint32_t v = slot_s[c * nrp + r];
+              if (v != SLOT_DEFAULT) {
+                const bool before = (v >> 16) == REL_START;
+                const uint32_t a0 = before ? 0u : (v >> 16), e = v & 0xFFFFu;
+                len = value_len(v >> 16, e, any_ctrl, ctrl_s, S);
+                if (len > SHORT_FIELD) {  // mark the chunks of a long field
+                  const uint32_t c0 = a0 >> 5, c1 = (e - 1) >> 5;
+                  S.lk[before ? 0 : 1][c0] = uint16_t(k);
+                  for (uint32_t cc = c0 + 1; cc <= c1; ++cc) S.lk[0][cc] = uint16_t(k);
                 }
               }
-              pos_s[k] = uint16_t(len);
-              mysum += len;
-              if (++r == nr) { r = 0; ++si; }
             }
-          }
-          uint32_t xi = mysum;
-#pragma unroll
-          for (int d = 1; d < 32; d <<= 1) {
-            const uint32_t o = __shfl_up_sync(FULL, xi, d);
-            if (lane >= d) xi += o;
-          }
-          if (lane == 31) S.wsum[warp] = xi;
-          __syncthreads();
-          if (warp == 0) {
-            const uint32_t v = lane < NW ? S.wsum[lane] : 0u;
-            uint32_t x = v;
-#pragma unroll
-            for (int d = 1; d < NW; d <<= 1) {
-              const uint32_t o = __shfl_up_sync(FULL, x, d);
-              if (lane >= d) x += o;
-            }
-            __syncwarp();
-            if (lane < NW) S.wsum[lane] = x - v;
-            if (lane == NW - 1) S.cstart[n_str] = x;
-          }
-          __syncthreads();
-          {  // lengths -> chars end positions (inclusive prefix)
-            uint32_t run = S.wsum[warp] + xi - mysum;
-            uint32_t si = k0 / nr, r = k0 - si * nr;
-            for (uint32_t k = k0; k < k1; ++k) {
-              if (r == 0) S.cstart[si] = run;
-              run += pos_s[k];
-              pos_s[k] = uint16_t(run);
-              if (++r == nr) { r = 0; ++si; }
-            }
-          }
-          __syncthreads();
-          // staging: a lane per short field; long fields chunk-parallel,
-          // each thread copying its chunk's part of the (at most two) long
-          // fields that cover it
-          {
-            uint32_t si = k0 / nr, r = k0 - si * nr;
-            uint32_t prev = k0 ? pos_s[k0 - 1] : 0u;
-            if (r == 0) prev = S.cstart[si];
-            for (uint32_t k = k0; k < k1; ++k) {
-              const uint32_t pe = pos_s[k];
-              const uint32_t len = pe - prev;
-              prev = pe;
-              const uint32_t c = P.strcol[si];
-              const uint32_t rr = r;
-              if (++r == nr) { r = 0; ++si; prev = si < n_str ? S.cstart[si] : prev; }
-              if (len == 0 || len > SHORT_FIELD) continue;
-              const uint32_t v = slot_s[c * nr + rr];
-              const uint32_t a0 = (v >> 16) == 0xFFFFu ? 0u : (v >> 16), e = v & 0xFFFFu;
-              uint32_t dst = pe - len;
-              if (len == e - a0) {
-                for (uint32_t p = a0; p < e; ++p) stage_s[dst++] = tile_s[p];
-              } else {
-                for (uint32_t p = a0; p < e; ++p)
-                  if (!((ctrl_s[p >> 5] >> (p & 31)) & 1u)) stage_s[dst++] = tile_s[p];
-              }
-            }
-          }
-          {
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const uint32_t k = S.lk[h][t];
-              if (k == NO_FIELD) continue;
-              const uint32_t ksi = k / nr;
-              const uint32_t v = slot_s[P.strcol[ksi] * nr + (k - ksi * nr)];
-              const uint32_t a0 = (v >> 16) == 0xFFFFu ? 0u : (v >> 16), e = v & 0xFFFFu;
-              const uint32_t p0 = max(a0, cstart), p1 = min(e, cstart + clen);
-              const uint32_t c_a0 = any_ctrl ? ctrl_before(ctrl_s, S.cpre, a0) : 0u;
-              const uint32_t c_e = any_ctrl ? ctrl_before(ctrl_s, S.cpre, e) : 0u;
-              const uint32_t c_p0 = any_ctrl ? ctrl_before(ctrl_s, S.cpre, p0) : 0u;
-              const uint32_t len = (e - a0) - (c_e - c_a0);
-              uint32_t dst = pos_s[k] - len + (p0 - a0) - (c_p0 - c_a0);
-              const uint32_t cm = g.ctrl & range_mask(p0 - cstart, p1 - cstart);
-              if (!cm) {
-                for (uint32_t p = p0; p < p1; ++p) stage_s[dst++] = tile_s[p];
-              } else {
-                for (uint32_t p = p0; p < p1; ++p)
-                  if (!((cm >> (p - cstart)) & 1u)) stage_s[dst++] = tile_s[p];
-              }
-            }
+            pos_s[k] = uint16_t(len);
+            mysum += len;
+            if (++r == nr) { r = 0; ++si; }
           }
         }
-
-        // ---- numbers: a lane per (numeric column, row) slot, the slots of
-        // the numeric columns taken column by column, 32 to a warp; columns
-        // of one type are adjacent, so a warp mostly runs one conversion
+        uint32_t xi = mysum;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+          const uint32_t o = __shfl_up_sync(FULL, xi, d);
+          if (lane >= d) xi += o;
+        }
+        if (lane == 31) S.wsum[warp] = xi;
+        bar_sync(BAR_W, NT);
+        if (warp == 0) {
+          const uint32_t v = lane < NW ? S.wsum[lane] : 0u;
+          uint32_t x = v;
+#pragma unroll
+          for (int d = 1; d < NW; d <<= 1) {
+            const uint32_t o = __shfl_up_sync(FULL, x, d);
+            if (lane >= d) x += o;
+          }
+          __syncwarp();
+          if (lane < NW) S.wsum[lane] = x - v;
+          if (lane == NW - 1) S.cstart[n_str] = x;
+        }
+        bar_sync(BAR_W, NT);
+        {  // lengths -> chars end positions (inclusive prefix)
+          uint32_t run = S.wsum[warp] + xi - mysum;
+          uint32_t si = k0 / nr, r = k0 - si * nr;
+          for (uint32_t k = k0; k < k1; ++k) {
+            if (r == 0) S.cstart[si] = run;
+            run += pos_s[k];
+            pos_s[k] = uint16_t(run);
+            if (++r == nr) { r = 0; ++si; }
+          }
+        }
+        bar_sync(BAR_W, NT);
+        // staging: a lane per short field; long fields chunk-parallel, each
+        // thread copying its chunk's part of the (at most two) long fields
+        // that cover it
         {
-          const uint32_t n_slots = S.n_num * nr;
-          const uint32_t magic = nr > 1 ? 0xFFFFFFFFu / nr + 1u : 0u;  // k / nr, exact for k < 2^13
-          for (uint32_t k = uint32_t(warp) * 32 + uint32_t(lane); k < n_slots; k += NT) {
-            const uint32_t oc = nr > 1 ? __umulhi(k, magic) : k;
-            const uint32_t c = S.numcol[oc];
-            const uint32_t r = lo + (k - oc * nr);
-            const uint32_t r_first = c < col_in ? 1u : 0u;  // rows whose field c closes here
-            const uint32_t r_end = c < col_end ? rows : rows - 1u;
-            if (r < r_first || r >= r_end) continue;
-            if (r >= rec_lim) { report(P.st, PP_ERR_CAPACITY, 0, false); continue; }
-            const uint32_t v = slot_s[c * nr + (r - lo)];
-            void* const out = P.typed[c];
-            const uint64_t rec = rec0 + r;
-            switch (S.coltype[c]) {
-              case PP_COL_FLOAT64: convert_store<PP_COL_FLOAT64>(P, X, out, rec, v); break;
-              case PP_COL_INT64: convert_store<PP_COL_INT64>(P, X, out, rec, v); break;
-              case PP_COL_TIMESTAMP: convert_store<PP_COL_TIMESTAMP>(P, X, out, rec, v); break;
-              case PP_COL_INT32: convert_store<PP_COL_INT32>(P, X, out, rec, v); break;
-              default: convert_store<PP_COL_INT8>(P, X, out, rec, v); break;
-            }
-          }
-        }
-        __syncthreads();
-        if (NS > 0 && n_str && P.has_out) {
-          // Arrow offsets of the string fields closed in this pass
-          uint32_t si = 0, gi = uint32_t(warp);
-          while (gi >= ngr && si < n_str) { gi -= ngr; ++si; }
-          for (; si < n_str; gi += NW) {
-            while (gi >= ngr && si < n_str) { gi -= ngr; ++si; }
-            if (si >= n_str) break;
-            const uint32_t r = lo + gi * 32 + lane;
+          uint32_t si = k0 / nr, r = k0 - si * nr;
+          uint32_t prev = k0 ? pos_s[k0 - 1] : 0u;
+          if (r == 0) prev = S.cstart[si];
+          for (uint32_t k = k0; k < k1; ++k) {
+            const uint32_t pe = pos_s[k];
+            const uint32_t len = pe - prev;
+            prev = pe;
             const uint32_t c = P.strcol[si];
-            if (r >= hi || (r == 0 && c < col_in) || (r + 1 == rows && c >= col_end)) continue;
-            const uint64_t rec = rec0 + r;
-            if (rec >= P.rec_cap) { report(P.st, PP_ERR_CAPACITY, 0, false); continue; }
-            const uint64_t off = S.base[si] + S.carry[si] + (pos_s[si * nr + (r - lo)] - S.cstart[si]);
-            if (off > 0x7FFFFFFFull || off > P.chars_cap[si]) report(P.st, PP_ERR_CAPACITY, 0, false);
-            else P.offsets[si][rec + 1] = int32_t(off);
-          }
-          // staged chars -> HBM, 16-byte aligned stores
-          for (uint32_t si = 0; si < n_str; ++si) {
-            uint32_t len = S.cstart[si + 1] - S.cstart[si];
-            if (!len) continue;
-            const uint64_t gb = S.base[si] + S.carry[si];
-            if (gb + len > P.chars_cap[si]) {
-              if (t == 0) report(P.st, PP_ERR_CAPACITY, 0, false);
-              len = gb >= P.chars_cap[si] ? 0u : uint32_t(P.chars_cap[si] - gb);
+            const uint32_t rr = r;
+            if (++r == nr) { r = 0; ++si; prev = si < n_str ? S.cstart[si] : prev; }
+            if (len == 0 || len > SHORT_FIELD) continue;
+            const uint32_t v = slot_s[c * nrp + rr];
+            const uint32_t a0 = (v >> 16) == REL_START ? 0u : (v >> 16), e = v & 0xFFFFu;
+            uint32_t dst = pe - len;
+            if (len == e - a0) {
+              for (uint32_t p = a0; p < e; ++p) stage_s[dst++] = tile_s[p];
+            } else {
+              for (uint32_t p = a0; p < e; ++p)
+                if (!((ctrl_s[p >> 5] >> (p & 31)) & 1u)) stage_s[dst++] = tile_s[p];
             }
-            uint8_t* gp = P.chars[si] + gb;
-            const uint32_t sp = S.cstart[si];
-            const uint32_t head = min(len, uint32_t((16u - (reinterpret_cast<uintptr_t>(gp) & 15u)) & 15u));
-            const uint32_t nvec = (len - head) >> 4;
-            const uint32_t tail0 = head + (nvec << 4);
-            if (uint32_t(t) < head) gp[t] = stage_s[sp + t];
-            const uint32_t src0 = sp + head;
-            const uint32_t sh = (src0 & 3u) * 8u;
-            const uint32_t* sw = reinterpret_cast<const uint32_t*>(stage_s + (src0 & ~3u));
-            uint4* gv = reinterpret_cast<uint4*>(gp + head);
-            for (uint32_t v = t; v < nvec; v += NT) {
-              const uint32_t* q = sw + 4 * v;
-              const uint32_t a0 = q[0], a1 = q[1], a2 = q[2], a3 = q[3], a4 = q[4];
-              uint4 o;
-              o.x = __funnelshift_r(a0, a1, sh);
-              o.y = __funnelshift_r(a1, a2, sh);
-              o.z = __funnelshift_r(a2, a3, sh);
-              o.w = __funnelshift_r(a3, a4, sh);
-              __stcs(gv + v, o);
-            }
-            if (tail0 + t < len) gp[tail0 + t] = stage_s[sp + tail0 + t];
           }
         }
-        __syncthreads();
-        if (NS > 0 && t < int(n_str)) S.carry[t] += S.cstart[t + 1] - S.cstart[t];
+        {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t k = S.lk[h][t];
+            if (k == NO_FIELD) continue;
+            const uint32_t ksi = k / nr;
+            const uint32_t v = slot_s[P.strcol[ksi] * nrp + (k - ksi * nr)];
+            const uint32_t a0 = (v >> 16) == REL_START ? 0u : (v >> 16), e = v & 0xFFFFu;
+            const uint32_t p0 = max(a0, cstart), p1 = min(e, cstart + clen);
+            const uint32_t c_a0 = any_ctrl ? ctrl_bef(ctrl_s, S, a0) : 0u;
+            const uint32_t c_e = any_ctrl ? ctrl_bef(ctrl_s, S, e) : 0u;
+            const uint32_t c_p0 = any_ctrl ? ctrl_bef(ctrl_s, S, p0) : 0u;
+            const uint32_t len = (e - a0) - (c_e - c_a0);
+            uint32_t dst = pos_s[k] - len + (p0 - a0) - (c_p0 - c_a0);
+            const uint32_t cm = g.ctrl & range_mask(p0 - cstart, p1 - cstart);
+            if (!cm) {
+              for (uint32_t p = p0; p < p1; ++p) stage_s[dst++] = tile_s[p];
+            } else {
+              for (uint32_t p = p0; p < p1; ++p)
+                if (!((cm >> (p - cstart)) & 1u)) stage_s[dst++] = tile_s[p];
+            }
+          }
+        }
       }
+
+      // ---- numbers: a lane per (numeric column, row) slot, the slots of
+      // the numeric columns taken column by column, 32 to a warp; columns of
+      // one type are adjacent, so a warp mostly runs one conversion
+      {
+        const uint32_t n_slots = S.n_num * nr;
+        const uint32_t magic = nr > 1 ? 0xFFFFFFFFu / nr + 1u : 0u;  // k / nr, exact for k < 2^13
+        for (uint32_t k = uint32_t(warp) * 32 + uint32_t(lane); k < n_slots; k += NT) {
+          const uint32_t oc = nr > 1 ? __umulhi(k, magic) : k;
+          const uint32_t c = S.numcol[oc];
+          const uint32_t r = lo + (k - oc * nr);
+          const uint32_t r_first = c < col_in ? 1u : 0u;  // rows whose field c closes here
+          const uint32_t r_end = c < col_end ? rows : rows - 1u;
+          if (r < r_first || r >= r_end) continue;
+          if (r >= rec_lim) { report(P.st, PP_ERR_CAPACITY, 0, false); continue; }
+          const uint32_t ty = S.coltype[c];
+          store_typed(P.typed[c], ty, rec0 + r, convert_any(P, X, ty, slot_s[c * nrp + (r - lo)]));
+        }
+      }
+      if (first) next_ticket(b);
+      bar_sync(BAR_W, NT);
+      if (NS > 0 && n_str) {
+        if (first) bar_sync(BAR_CHR, NT + 32);  // the tile's chars offsets
+        // Arrow offsets of the string fields closed in this pass
+        uint32_t si = 0, gi = uint32_t(warp);
+        while (gi >= ngr && si < n_str) { gi -= ngr; ++si; }
+        for (; si < n_str; gi += NW) {
+          while (gi >= ngr && si < n_str) { gi -= ngr; ++si; }
+          if (si >= n_str) break;
+          const uint32_t r = lo + gi * 32 + lane;
+          const uint32_t c = P.strcol[si];
+          if (r >= hi || (r == 0 && c < col_in) || (r + 1 == rows && c >= col_end)) continue;
+          const uint64_t rec = rec0 + r;
+          if (rec >= P.rec_cap) { report(P.st, PP_ERR_CAPACITY, 0, false); continue; }
+          const uint64_t off = S.base[si] + S.carry[si] + (pos_s[si * nr + (r - lo)] - S.cstart[si]);
+          if (off > 0x7FFFFFFFull || off > P.chars_cap[si]) report(P.st, PP_ERR_CAPACITY, 0, false);
+          else P.offsets[si][rec + 1] = int32_t(off);
+        }
+        // staged chars -> HBM, 16-byte aligned stores
+        for (uint32_t si = 0; si < n_str; ++si) {
+          uint32_t len = S.cstart[si + 1] - S.cstart[si];
+          if (!len) continue;
+          const uint64_t gb = S.base[si] + S.carry[si];
+          if (gb + len > P.chars_cap[si]) {
+            if (t == 0) report(P.st, PP_ERR_CAPACITY, 0, false);
+            len = gb >= P.chars_cap[si] ? 0u : uint32_t(P.chars_cap[si] - gb);
+          }
+          uint8_t* gp = P.chars[si] + gb;
+          const uint32_t sp = S.cstart[si];
+          const uint32_t head = min(len, uint32_t((16u - (reinterpret_cast<uintptr_t>(gp) & 15u)) & 15u));
+          const uint32_t nvec = (len - head) >> 4;
+          const uint32_t tail0 = head + (nvec << 4);
+          if (uint32_t(t) < head) gp[t] = stage_s[sp + t];
+          const uint32_t src0 = sp + head;
+          const uint32_t sh = (src0 & 3u) * 8u;
+          const uint32_t* sw = reinterpret_cast<const uint32_t*>(stage_s + (src0 & ~3u));
+          uint4* gv = reinterpret_cast<uint4*>(gp + head);
+          for (uint32_t v = t; v < nvec; v += NT) {
+            const uint32_t* q = sw + 4 * v;
+            const uint32_t a0 = q[0], a1 = q[1], a2 = q[2], a3 = q[3], a4 = q[4];
+            uint4 o;
+            o.x = __funnelshift_r(a0, a1, sh);
+            o.y = __funnelshift_r(a1, a2, sh);
+            o.z = __funnelshift_r(a2, a3, sh);
+            o.w = __funnelshift_r(a3, a4, sh);
+            __stcs(gv + v, o);
+          }
+          if (tail0 + t < len) gp[tail0 + t] = stage_s[sp + tail0 + t];
+        }
+        bar_sync(BAR_W, NT);
+        if (t < int(n_str)) S.carry[t] += S.cstart[t + 1] - S.cstart[t];
+      }
+      bar_sync(BAR_W, NT);
     }
-    __syncthreads();
-    if (t < int(n_str)) {
-      if (last_tile) P.st->chars_len[P.strcol[t]] = S.base[t] + S.carry[t];
-      S.carry[t] = 0;
-    }
+    if (t < int(n_str)) S.carry[t] = 0;
     if (owns_end) P.st->n_records = rec0 + (rows - 1) + (virt_rd ? 1u : 0u);
-    feed_next(S.F);  // the tile was last read before a barrier above
+    bar_sync(BAR_W, NT);
   }
-  feed_finish(S.F);
 }
 
 // ===================================================== column-count inference
@@ -1928,13 +1803,19 @@ __global__ void __launch_bounds__(FR_NT) fields_reduce_kernel(const __grid_const
 }
 
 // ================================================================= launch
-// Zero the tile counters and the scan's look-back flags; initialise the
-// status and offsets[c][0] = 0 for every string column.
+// Zero the tile counters and the look-back flags; initialise the status and
+// offsets[c][0] = 0 for every string column.
 __global__ void parse_init_kernel(ParseParams P) {
   const ppi::ParseScratch& s = P.s;
   const uint32_t i0 = blockIdx.x * blockDim.x + threadIdx.x;
   const uint32_t stride = gridDim.x * blockDim.x;
-  for (uint32_t i = i0; i < s.n_scan_blocks; i += stride) { s.scan_flag_a[i] = 0; s.scan_flag_c[i] = 0; }
+  if (s.v2_desc)
+    for (uint32_t i = i0; i < P.n_tiles; i += stride) {
+      s.v2_desc[2 * size_t(i)] = 0;
+      s.v2_desc[2 * size_t(i) + 1] = 0;
+    }
+  if (s.c_flag)
+    for (uint32_t i = i0; i < P.n_tiles; i += stride) s.c_flag[i] = 0;
   for (uint32_t i = i0; i < s.n_tstate_blocks; i += stride) s.tstate_words[i] = 0;
   if (i0 < 4) s.counters[i0] = 0;
   if (i0 == 0) {
@@ -1950,10 +1831,14 @@ __global__ void parse_init_kernel(ParseParams P) {
   }
 }
 
-struct Occ { int ctx = 1, main = 1, n_sm = 0; };
+uint32_t init_grid(uint32_t n) {
+  return std::max<uint32_t>(1, std::min<uint32_t>((n + 255) / 256, 1024));
+}
 
-// Per device: the SM count, the dynamic shared-memory attributes of the two
-// big tile passes and their resident blocks per SM.
+// Per device: the SM count, the tile pass's dynamic shared-memory attribute
+// and its resident blocks per SM.
+struct Occ { int blocks = 1, n_sm = 0; };
+
 template <int NS>
 cudaError_t parse_setup(Occ** out) {
   static ppi::DeviceOnce once;
@@ -1965,21 +1850,14 @@ cudaError_t parse_setup(Occ** out) {
     Occ o;
     cudaError_t r;
     if ((r = ppi::sm_count(&o.n_sm)) != cudaSuccess) return r;
-    if ((r = cudaFuncSetAttribute(ctx_kernel<NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  int(CTX_SMEM))) != cudaSuccess)
-      return r;
-    if ((r = cudaFuncSetAttribute(main_kernel<NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  int(MAIN_SMEM))) != cudaSuccess)
+    if ((r = cudaFuncSetAttribute(parse_kernel<NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  int(PARSE_SMEM))) != cudaSuccess)
       return r;
     int b = 0;
-    if ((r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, ctx_kernel<NS>, NT, CTX_SMEM)) !=
-        cudaSuccess)
+    if ((r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, parse_kernel<NS>, ntf_of<NS>(),
+                                                           PARSE_SMEM)) != cudaSuccess)
       return r;
-    o.ctx = b > 0 ? b : 1;
-    if ((r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, main_kernel<NS>, NT, MAIN_SMEM)) !=
-        cudaSuccess)
-      return r;
-    o.main = b > 0 ? b : 1;
+    o.blocks = b > 0 ? b : 1;
     occ[d] = o;
     return cudaSuccess;
   });
@@ -1995,8 +1873,7 @@ cudaError_t launch_ns(const ParseParams& p, cudaStream_t stream) {
   const Occ& occ = *po;
   const bool timed = ppi::stage_begin();
   if (timed) ppi::stage_mark(0, stream);
-  parse_init_kernel<<<std::max<uint32_t>(1, std::min<uint32_t>((p.s.n_scan_blocks + 255) / 256, 1024)),
-                      256, 0, stream>>>(p);
+  parse_init_kernel<<<init_grid(std::max(p.n_tiles, p.s.n_tstate_blocks)), 256, 0, stream>>>(p);
   if (timed) ppi::stage_mark(1, stream);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (p.n_tiles) {
@@ -2009,27 +1886,14 @@ cudaError_t launch_ns(const ParseParams& p, cudaStream_t stream) {
   if (p.n_tiles) tile_state_kernel<<<p.s.n_tstate_blocks, TS_NT, 0, stream>>>(p);
   if (timed) ppi::stage_mark(3, stream);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const uint32_t g1 = uint32_t(std::min<uint64_t>(std::max<uint32_t>(p.n_tiles, 1),
-                                                  uint64_t(occ.n_sm) * occ.ctx));
-  if (p.n_tiles) ctx_kernel<NS><<<g1, NT, CTX_SMEM, stream>>>(p);
+  const uint32_t g = uint32_t(std::min<uint64_t>(std::max<uint32_t>(p.n_tiles, 1),
+                                                 uint64_t(occ.n_sm) * occ.blocks));
+  if (p.n_tiles) parse_kernel<NS><<<g, ntf_of<NS>(), PARSE_SMEM, stream>>>(p);
   if (timed) ppi::stage_mark(4, stream);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if (p.n_tiles) scan_kernel<NS><<<p.s.n_scan_blocks, SCAN_NT, 0, stream>>>(p);
-  if (timed) ppi::stage_mark(5, stream);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const uint32_t g3 = uint32_t(std::min<uint64_t>(std::max<uint32_t>(p.n_tiles, 1),
-                                                  uint64_t(occ.n_sm) * occ.main));
-  if (p.n_tiles) main_kernel<NS><<<g3, NT, MAIN_SMEM, stream>>>(p);
-  if (timed) ppi::stage_mark(6, stream);
   return cudaGetLastError();
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
-uint32_t ctx_stride_of(int ns, int n_cols) {
-  const size_t b = CTX_HDR + (ns > 0 ? 8 * size_t(ns) + 8 * size_t(n_cols) : 0);
-  return uint32_t((b + 15) & ~size_t(15));
-}
-uint32_t pre_stride_of(int ns) { return uint32_t(PRE_HDR + 8 * (ns > 0 ? ns : 0)); }
 
 cudaError_t launch_fields(const ParseParams& p, FAgg* agg, uint64_t* out, cudaStream_t stream) {
   static ppi::DeviceOnce once;
@@ -2051,7 +1915,7 @@ cudaError_t launch_fields(const ParseParams& p, FAgg* agg, uint64_t* out, cudaSt
   });
   if (e != cudaSuccess) return e;
   const int occ = occ_of[dev];
-  parse_init_kernel<<<1, 256, 0, stream>>>(p);
+  parse_init_kernel<<<init_grid(p.s.n_tstate_blocks), 256, 0, stream>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (p.n_tiles) {
     const uint32_t gv = uint32_t(std::min<uint64_t>((p.n_tiles + TV_NT / 32 - 1) / (TV_NT / 32),
@@ -2101,44 +1965,33 @@ int parse_ns_width(int n_str) {
   return 16;
 }
 
-// layout: counters | scan flags (records, chars) | scan payloads (2 x 13
-// words per scan block; 2 x ns words per scan block) | ctx records | pre
-// records
-size_t parse_scratch_bytes(uint32_t n, int ns, int n_cols, bool tags) {
-  const uint32_t nb = (n + SCAN_TILES - 1) / SCAN_TILES;
+// layout: counters | tile vectors | tile states | tile-state look-back words |
+// context look-back descriptors (16 bytes a tile) | chars look-back (flags,
+// aggregates, inclusive prefixes: ns words a tile)
+size_t parse_scratch_bytes(uint32_t n, int ns) {
   const uint32_t nt = (n + TS_TILES - 1) / TS_TILES;
   const int k3 = ns > 0 ? ns : 1;
-  return 256 + 2 * align256(size_t(nb) * 4) + 2 * align256(size_t(nb) * 13 * 8) +
-         2 * align256(size_t(nb) * k3 * 8) + align256(size_t(n) * ctx_stride_of(ns, n_cols)) +
-         align256(size_t(n) * pre_stride_of(ns)) + align256(size_t(n) * 4) + align256(n) +
-         align256(size_t(nt) * 8) + align256(n) + (tags ? align256(size_t(n) * NT * 24) : 0);
+  return 256 + align256(size_t(n) * 4) + align256(n) + align256(size_t(nt) * 8) +
+         align256(size_t(n) * 16) +
+         (ns > 0 ? align256(size_t(n) * 4) + 2 * align256(size_t(n) * k3 * 8) : 0);
 }
 
-void parse_scratch_carve(void* base, uint32_t n, int ns, int n_cols, bool tags, ParseScratch* o) {
-  const uint32_t nb = (n + SCAN_TILES - 1) / SCAN_TILES;
+void parse_scratch_carve(void* base, uint32_t n, int ns, ParseScratch* o) {
   const int k3 = ns > 0 ? ns : 1;
   uint8_t* p = static_cast<uint8_t*>(base);
+  *o = ParseScratch{};
   o->counters = reinterpret_cast<uint32_t*>(p); p += 256;
-  o->scan_flag_a = reinterpret_cast<uint32_t*>(p); p += align256(size_t(nb) * 4);
-  o->scan_flag_c = reinterpret_cast<uint32_t*>(p); p += align256(size_t(nb) * 4);
-  o->scan_agg_a = reinterpret_cast<uint64_t*>(p); p += align256(size_t(nb) * 13 * 8);
-  o->scan_inc_a = reinterpret_cast<uint64_t*>(p); p += align256(size_t(nb) * 13 * 8);
-  o->scan_agg_c = reinterpret_cast<uint64_t*>(p); p += align256(size_t(nb) * k3 * 8);
-  o->scan_inc_c = reinterpret_cast<uint64_t*>(p); p += align256(size_t(nb) * k3 * 8);
-  o->ctx = p; p += align256(size_t(n) * ctx_stride_of(ns, n_cols));
-  o->pre = p; p += align256(size_t(n) * pre_stride_of(ns));
   o->tile_stv = reinterpret_cast<uint32_t*>(p); p += align256(size_t(n) * 4);
   o->tile_state = p; p += align256(n);
-  o->tstate_words = reinterpret_cast<unsigned long long*>(p);
   o->n_tstate_blocks = (n + TS_TILES - 1) / TS_TILES;
+  o->tstate_words = reinterpret_cast<unsigned long long*>(p);
   p += align256(size_t(o->n_tstate_blocks) * 8);
-  o->tile_flags = p; p += align256(n);
-  o->tags = tags ? reinterpret_cast<uint4*>(p) : nullptr;
-  if (tags) p += size_t(n) * NT * 16;
-  o->vpre = tags ? reinterpret_cast<uint2*>(p) : nullptr;
-  o->ctx_stride = ctx_stride_of(ns, n_cols);
-  o->pre_stride = pre_stride_of(ns);
-  o->n_scan_blocks = nb;
+  o->v2_desc = reinterpret_cast<uint64_t*>(p); p += align256(size_t(n) * 16);
+  if (ns > 0) {
+    o->c_flag = reinterpret_cast<uint32_t*>(p); p += align256(size_t(n) * 4);
+    o->c_agg = reinterpret_cast<uint64_t*>(p); p += align256(size_t(n) * k3 * 8);
+    o->c_inc = reinterpret_cast<uint64_t*>(p); p += align256(size_t(n) * k3 * 8);
+  }
 }
 
 cudaError_t launch_parse(const ParseParams& p, cudaStream_t stream) {

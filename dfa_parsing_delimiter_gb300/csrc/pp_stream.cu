@@ -253,7 +253,7 @@ pp_rc pp_parse_host(const uint8_t* h_in, size_t n_bytes, const pp_dfa_desc* dfa,
     }
   void* scratch = nullptr;
   if (e == cudaSuccess)
-    e = B.alloc(&scratch, ppi::parse_scratch_bytes(uint32_t((in_cap + tile - 1) / tile), ns, n_cols, true));
+    e = B.alloc(&scratch, ppi::parse_scratch_bytes(uint32_t((in_cap + tile - 1) / tile), ns));
   if (e != cudaSuccess) return rc_of(e);
 
   int32_t merged_err = 0;
@@ -278,7 +278,7 @@ pp_rc pp_parse_host(const uint8_t* h_in, size_t n_bytes, const pp_dfa_desc* dfa,
     if (rc != PP_OK) return rc;
     if ((e = cudaMemsetAsync(di, 0, sizeof(ParseInfo), B.cs)) != cudaSuccess) return rc_of(e);
     p.record_end = last ? nullptr : &di->record_end;
-    ppi::parse_scratch_carve(scratch, p.n_tiles, ns, n_cols, true, &p.s);
+    ppi::parse_scratch_carve(scratch, p.n_tiles, ns, &p.s);
     if ((e = ppi::launch_parse(p, B.cs)) != cudaSuccess) return rc_of(e);
     if (out && n_str) {
       RebaseArgs a{};

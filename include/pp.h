@@ -161,6 +161,7 @@ typedef struct {
  * PP_ERR_COLCOUNT, extra fields are dropped and missing ones take the
  * default (empty string / 0).  String values are the value bytes only
  * (enclosing quotes dropped, a doubled quote yields one quote).
+ * Inputs of 2^40 bytes (1 TiB) or more return PP_ETOOLARGE.
  * Returns PP_EINVAL for bad arguments, PP_ENOMEM / PP_ECUDA on CUDA errors.
  */
 pp_rc pp_parse(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa, int n_cols,
@@ -230,7 +231,7 @@ pp_rc pp_tokenize_host(const uint8_t* h_in, size_t n_bytes, const pp_dfa_desc* d
 
 /*
  * pp_parse_noalloc — pp_parse without allocation: its cross-tile scratch
- * (tile contexts, scan flags and aggregates) lives in a buffer of
+ * (tile vectors and states, look-back flags and aggregates) lives in a buffer of
  * PP_NOALLOC_SCRATCH_BYTES compiled into the library, one per device.  The
  * ParPaRaw paper has no counterpart; this is an integration entry point
  * for callers that cannot allocate device memory per call (devices or
@@ -238,11 +239,12 @@ pp_rc pp_tokenize_host(const uint8_t* h_in, size_t n_bytes, const pp_dfa_desc* d
  * cudaMallocAsync fails; services whose device memory is fixed at
  * start-up).
  *   Arguments, semantics, outputs and d_status: exactly those of pp_parse.
- *   Limit: the scratch needed is about 94 bytes per 16 KiB tile of input
- *   with no string column, rising with the string and column counts to
- *   about 862 bytes per tile with 16 string columns of 64; so 4 MiB holds
- *   inputs up to about 700 MiB in the first case and about 76 MiB in the
- *   last.  A larger input returns PP_ETOOLARGE before any CUDA call.
+ *   Limit: the scratch needed is about 22 bytes per 16 KiB tile of input
+ *   without string columns and 4 + 16 x w bytes more with them, w being the
+ *   string-column count rounded up to 4, 8 or 16; 4 MiB therefore holds
+ *   inputs up to about 3 GiB without string columns, 730 MiB with 1 to 4,
+ *   420 MiB with 5 to 8 and 230 MiB with 9 to 16 string columns.  A larger
+ *   input returns PP_ETOOLARGE before any CUDA call.
  *   First call on each device: it looks up the buffer's address
  *   (cudaGetSymbolAddress; this can load the library's device code) and
  *   sets kernel attributes.  Make that first call before any stream
@@ -367,9 +369,9 @@ size_t pp_tile_bytes(void);
  * second of polling).  Process-wide; affects calls made afterwards. */
 void pp_debug_set_spin_limit(uint32_t polls);
 
-/* Test hook for the bounded waits: while on, the first block of
- * pp_parse's cross-tile scan posts nothing, so the waits of the later
- * blocks run out after the spin limit and the call reports
+/* Test hook for the bounded waits: while on, the first tile of pp_parse's
+ * tile pass posts nothing to its cross-tile look-backs, so the waits of the
+ * tiles after it run out after the spin limit and the call reports
  * PP_ERR_LOOKBACK_TIMEOUT (fatal: outputs unspecified).  No wait is left
  * unbounded; the device stays usable.  Process-wide. */
 void pp_debug_set_withhold(int on);
@@ -383,10 +385,11 @@ pp_rc pp_debug_stage_timing(int n_calls);
 
 /* Kernel durations of the recorded calls: out[PP_STAGES*i + k] =
  * milliseconds of kernel k of call i.  pp_parse: 0 init, 1 tile transition
- * vectors, 2 tile start states, 3 context pass, 4 scan, 5 main pass.  pp_tokenize: 0 init, 1 transition vectors, 2 state
- * scan, 3 count pass, 4 count scan, 5 emit pass.  Entries a call does not
- * use are 0.  Waits for the events.  Returns the number of calls written
- * (at most max_calls), or -1 on a CUDA error. */
+ * vectors, 2 tile start states, 3 tile pass (tagging, indices, columns and
+ * conversion).  pp_tokenize: 0 init, 1 transition vectors, 2 state scan,
+ * 3 count pass, 4 count scan, 5 emit pass.  Entries a call does not use
+ * are 0.  Waits for the events.  Returns the number of calls written (at
+ * most max_calls), or -1 on a CUDA error. */
 #define PP_STAGES 6
 int pp_debug_stage_ms(float* out, int max_calls);
 

@@ -218,9 +218,9 @@ def test_parse_random_small_inputs():
 
 def test_parse_lookback_timeout_is_reported_and_recoverable():
     """A wait that runs out ends with an error status, not a hang: with the
-    first scan block withholding its prefix (a flag nothing sets) and a short
-    spin limit, the later blocks give up and report the timeout; the next
-    normal call on the same context is clean."""
+    first tile withholding its look-back posts (flags nothing sets) and a
+    short spin limit, the tiles after it give up and report the timeout;
+    the next normal call on the same context is clean."""
     data = b"ab,cd\n" * ((40 << 20) // 6)  # > 2048 tiles: several scan blocks
     try:
         pp.debug_set_spin_limit(2000)
