@@ -634,30 +634,20 @@ __device__ __forceinline__ int convert_field(const ParseParams& P, uint32_t v, c
                          X.tile_fstate, &val);
 }
 
-// Convert one row's field (slot value v) of a column of type ty, reporting
-// a number error at the field's first byte; returns the value's bits.
-__device__ __forceinline__ uint64_t convert_any(const ParseParams& P, const NumCtx& X, uint32_t ty,
-                                                uint32_t v) {
+// Convert one row's field (slot value v) of a column of type TY, store it
+// at out[rec] and report a number error at the field's first byte.
+template <int TY>
+__device__ __forceinline__ void convert_store(const ParseParams& P, const NumCtx& X, void* out,
+                                              uint64_t rec, uint32_t v) {
   uint64_t val;
-  int err;
-  switch (ty) {
-    case PP_COL_FLOAT64: err = convert_field<PP_COL_FLOAT64>(P, v, X, val); break;
-    case PP_COL_INT64: err = convert_field<PP_COL_INT64>(P, v, X, val); break;
-    case PP_COL_TIMESTAMP: err = convert_field<PP_COL_TIMESTAMP>(P, v, X, val); break;
-    case PP_COL_INT32: err = convert_field<PP_COL_INT32>(P, v, X, val); break;
-    default: err = convert_field<PP_COL_INT8>(P, v, X, val); break;
-  }
+  const int err = convert_field<TY>(P, v, X, val);
+  if (TY == PP_COL_INT32) static_cast<int32_t*>(out)[rec] = int32_t(val);
+  else if (TY == PP_COL_INT8) static_cast<int8_t*>(out)[rec] = int8_t(val);
+  else static_cast<uint64_t*>(out)[rec] = val;
   if (err) {
     const uint32_t fsr = v >> 16;
     report(P.st, err, fsr == 0xFFFFu ? X.tile_fstart : X.tile_base + fsr, true);
   }
-  return val;
-}
-// Store a converted value at out[rec] in the column's width.
-__device__ __forceinline__ void store_typed(void* out, uint32_t ty, uint64_t rec, uint64_t val) {
-  if (ty == PP_COL_INT32) static_cast<int32_t*>(out)[rec] = int32_t(val);
-  else if (ty == PP_COL_INT8) static_cast<int8_t*>(out)[rec] = int8_t(val);
-  else static_cast<uint64_t*>(out)[rec] = val;
 }
 
 // ================================================================ 1. tile pass
@@ -1574,8 +1564,16 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
           const uint32_t r_end = c < col_end ? rows : rows - 1u;
           if (r < r_first || r >= r_end) continue;
           if (r >= rec_lim) { report(P.st, PP_ERR_CAPACITY, 0, false); continue; }
-          const uint32_t ty = S.coltype[c];
-          store_typed(P.typed[c], ty, rec0 + r, convert_any(P, X, ty, slot_s[c * nrp + (r - lo)]));
+          const uint32_t v = slot_s[c * nrp + (r - lo)];
+          void* const out = P.typed[c];
+          const uint64_t rec = rec0 + r;
+          switch (S.coltype[c]) {
+            case PP_COL_FLOAT64: convert_store<PP_COL_FLOAT64>(P, X, out, rec, v); break;
+            case PP_COL_INT64: convert_store<PP_COL_INT64>(P, X, out, rec, v); break;
+            case PP_COL_TIMESTAMP: convert_store<PP_COL_TIMESTAMP>(P, X, out, rec, v); break;
+            case PP_COL_INT32: convert_store<PP_COL_INT32>(P, X, out, rec, v); break;
+            default: convert_store<PP_COL_INT8>(P, X, out, rec, v); break;
+          }
         }
       }
       if (first) next_ticket(b);

@@ -40,12 +40,14 @@ U64MAX = (1 << 64) - 1
 class Status(ctypes.Structure):
     _fields_ = [("error", ctypes.c_int32), ("pad", ctypes.c_int32),
                 ("first_error_offset", ctypes.c_uint64), ("n_records", ctypes.c_uint64),
-                ("n_tokens", ctypes.c_uint64), ("chars_len", ctypes.c_uint64 * 64)]
+                ("n_tokens", ctypes.c_uint64), ("chars_len", ctypes.c_uint64 * 64),
+                ("n_dropped", ctypes.c_uint64)]
 
     def as_dict(self, n_cols=0):
         return dict(error=int(self.error), first_error_offset=int(self.first_error_offset),
                     n_records=int(self.n_records), n_tokens=int(self.n_tokens),
-                    chars_len=[int(self.chars_len[i]) for i in range(n_cols)])
+                    chars_len=[int(self.chars_len[i]) for i in range(n_cols)],
+                    n_dropped=int(self.n_dropped))
 
 
 def build(force: bool = False) -> str:
@@ -67,6 +69,11 @@ def _load():
         L = ctypes.CDLL(_SO)
         L.or_csv_parse.argtypes = [_vp, _u64, _u8, _u8, _u8, ctypes.c_int, ctypes.c_int, _vp,
                                    _vp, _vp, _vp, _u64, _vp, ctypes.POINTER(Status)]
+        L.or_csv_parse_ex.argtypes = [_vp, _u64, _u8, _u8, _u8, ctypes.c_int, ctypes.c_int, _vp,
+                                      _vp, ctypes.c_int, _vp, _u64, _vp, _vp, _vp, _u64, _vp,
+                                      ctypes.POINTER(Status)]
+        L.or_skip_rows.argtypes = [_vp, _u64, _u8, _vp, _u64, _vp]
+        L.or_skip_rows.restype = _u64
         L.or_count_fields.argtypes = [_vp, _u64, _u8, _u8, _u8, ctypes.c_int, _vp,
                                       ctypes.POINTER(Status)]
         L.or_tokenize.argtypes = [_vp, _u64, _vp, _vp, _vp, _u64, ctypes.POINTER(Status)]
@@ -88,16 +95,37 @@ def _arr(x) -> np.ndarray:
     return np.ascontiguousarray(x, dtype=np.uint8)
 
 
+def skip_rows(data, rows, rd=b"\n"):
+    """The input without the listed rows (lines ended by rd; ParPaRaw
+    Section 4, "Skipping rows")."""
+    L = _load()
+    a = _arr(data)
+    r = np.ascontiguousarray(sorted(set(int(x) for x in rows)), dtype=np.uint64)
+    out = np.zeros(max(a.size, 1), dtype=np.uint8)
+    w = L.or_skip_rows(a.ctypes.data, a.size, rd[0], r.ctypes.data if r.size else None, r.size,
+                       out.ctypes.data)
+    return out[:w]
+
+
 def csv_parse(data, col_types, fd=b",", rd=b"\n", quote=b'"', records_capacity=None,
-              chars_capacity=None, crlf=False):
+              chars_capacity=None, crlf=False, defaults=None, reject=False,
+              skip_records=None, skip_rows_=None):
     """Sequentially parse quoted CSV (crlf: carriage returns outside quotes
     are dropped, so CRLF line ends work with rd = LF).
+
+    Options (ParPaRaw Section 4): `defaults` (n_cols integer bit patterns)
+    are stored for empty or missing numeric fields instead of 0; with
+    `reject`, records whose field count is not len(col_types) are not
+    emitted; `skip_records` lists record indices not to emit; `skip_rows_`
+    lists rows (lines) removed from the input before parsing.
 
     Returns (columns, status): columns[c] is (offsets int32[R+1], chars uint8)
     for string columns, a numpy array of R values for numeric ones, None for
     'skip'.  Output arrays are trimmed to the record / chars counts.
     """
     L = _load()
+    if skip_rows_ is not None:
+        data = skip_rows(data, skip_rows_, rd)
     a = _arr(data)
     n = a.size
     ncols = len(col_types)
@@ -124,11 +152,15 @@ def csv_parse(data, col_types, fd=b",", rd=b"\n", quote=b'"', records_capacity=N
     codes = np.array([COL_CODES[t] for t in col_types] or [0], dtype=np.int32)
     ccap = np.array(list(chars_capacity) or [0], dtype=np.uint64)
     st = Status()
-    L.or_csv_parse(a.ctypes.data, n, fd[0], rd[0], quote[0], int(bool(crlf)), ncols,
-                   codes.ctypes.data,
-                   ctypes.addressof(ptr_off), ctypes.addressof(ptr_chr),
-                   ctypes.addressof(ptr_typ), records_capacity, ccap.ctypes.data,
-                   ctypes.byref(st))
+    dflt = None if defaults is None else np.ascontiguousarray(
+        [int(x) & 0xFFFFFFFFFFFFFFFF for x in defaults], dtype=np.uint64)
+    skr = np.ascontiguousarray(sorted(set(int(x) for x in (skip_records or []))), dtype=np.uint64)
+    L.or_csv_parse_ex(a.ctypes.data, n, fd[0], rd[0], quote[0], int(bool(crlf)), ncols,
+                      codes.ctypes.data, dflt.ctypes.data if dflt is not None else None,
+                      int(bool(reject)), skr.ctypes.data if skr.size else None, skr.size,
+                      ctypes.addressof(ptr_off), ctypes.addressof(ptr_chr),
+                      ctypes.addressof(ptr_typ), records_capacity, ccap.ctypes.data,
+                      ctypes.byref(st))
     R = min(int(st.n_records), records_capacity)
     cols = []
     for c, t in enumerate(col_types):

@@ -62,6 +62,7 @@ typedef struct {
   uint64_t n_records;
   uint64_t n_tokens;
   uint64_t chars_len[64];
+  uint64_t n_dropped;          /* records not emitted (skipped or rejected) */
 } or_status;
 
 static void flag(or_status* st, int bit, uint64_t off, int with_offset) {
@@ -348,6 +349,7 @@ typedef struct {
   /* outputs */
   int n_cols;
   const int32_t* types;
+  const uint64_t* defaults;     /* bits stored for an empty or missing numeric field, or NULL */
   int32_t** offsets;
   uint8_t** chars;
   void** typed;
@@ -386,6 +388,13 @@ static void close_field(csv_out* o, uint64_t rec, int col, uint64_t field_start)
     return;
   }
   int rc;
+  if (o->val_len == 0 && o->defaults) {       /* empty or missing: the column default */
+    const uint64_t d = o->defaults[col];
+    if (t == C_I8) ((int8_t*)o->typed[col])[rec] = (int8_t)d;
+    else if (t == C_I32) ((int32_t*)o->typed[col])[rec] = (int32_t)d;
+    else ((uint64_t*)o->typed[col])[rec] = d;
+    return;
+  }
   if (t == C_F64) {
     double d;
     rc = conv_f64(o->val, o->val_len, &d);
@@ -413,33 +422,87 @@ static void close_record(csv_out* o, uint64_t rec, int col, uint64_t off) {
   for (int c = col + 1; c < o->n_cols; c++) close_field(o, rec, c, off);  /* defaults */
 }
 
-int or_csv_parse(const uint8_t* in, uint64_t n, uint8_t fd, uint8_t rd, uint8_t q, int crlf,
-                 int n_cols, const int32_t* col_types, int32_t** out_offsets,
-                 uint8_t** out_chars, void** out_typed, uint64_t records_capacity,
-                 const uint64_t* chars_capacity, or_status* st) {
+/* One parsed field of the record being collected (the records are buffered
+ * whole so that a record can be dropped once its field count is known). */
+typedef struct { uint64_t start, vbeg, vlen; } or_field;
+
+int or_csv_parse_ex(const uint8_t* in, uint64_t n, uint8_t fd, uint8_t rd, uint8_t q, int crlf,
+                    int n_cols, const int32_t* col_types, const uint64_t* defaults, int reject,
+                    const uint64_t* skip_records, uint64_t n_skip_records,
+                    int32_t** out_offsets, uint8_t** out_chars, void** out_typed,
+                    uint64_t records_capacity, const uint64_t* chars_capacity, or_status* st) {
   memset(st, 0, sizeof *st);
   st->first_error_offset = UINT64_MAX;
-  csv_out o = {n_cols, col_types, out_offsets, out_chars, out_typed, records_capacity,
+  csv_out o = {n_cols, col_types, defaults, out_offsets, out_chars, out_typed, records_capacity,
                chars_capacity, st, NULL, 0, 0};
   for (int c = 0; c < n_cols; c++)
     if (col_types[c] == C_STR && out_offsets[c]) out_offsets[c][0] = 0;
   csv_syms y = syms_of(crlf ? 2 : 0, fd, rd, q);
+  /* the current record: its value bytes in one buffer, a list of fields */
+  uint8_t* rbytes = NULL;
+  size_t rb_len = 0, rb_cap = 0;
+  or_field* fields = NULL;
+  size_t nf = 0, nf_cap = 0;
+  uint64_t rec_in = 0;   /* records read (index in the input) */
+  uint64_t rec_out = 0;  /* records emitted */
+  uint64_t skip_i = 0;   /* next entry of skip_records */
   int s = EOR, tag = T_RD;
-  uint64_t rec = 0, field_start = 0;
-  int col = 0;
+  uint64_t field_start = 0;
+#define PUSH_FIELD()                                                          \
+  do {                                                                        \
+    if (nf == nf_cap) {                                                       \
+      nf_cap = nf_cap ? 2 * nf_cap : 16;                                      \
+      fields = (or_field*)realloc(fields, nf_cap * sizeof *fields);           \
+    }                                                                         \
+    fields[nf].start = field_start;                                           \
+    fields[nf].vbeg = vbeg;                                                   \
+    fields[nf].vlen = rb_len - vbeg;                                          \
+    nf++;                                                                     \
+  } while (0)
+  uint64_t vbeg = 0;
+  /* emit (or drop) the collected record whose terminator is at off */
+#define CLOSE_RECORD(off)                                                     \
+  do {                                                                        \
+    while (skip_i < n_skip_records && skip_records[skip_i] < rec_in) skip_i++; \
+    const int skipped = skip_i < n_skip_records && skip_records[skip_i] == rec_in; \
+    const int bad = (int)nf != n_cols;                                        \
+    if (skipped) {                                                            \
+      st->n_dropped++;                                                        \
+    } else if (bad && reject) {                                               \
+      flag(st, E_COLCOUNT, (off), 1);                                         \
+      st->n_dropped++;                                                        \
+    } else {                                                                  \
+      for (size_t f = 0; f < nf; f++) {                                       \
+        o.val_len = 0;                                                        \
+        for (uint64_t k = 0; k < fields[f].vlen; k++)                         \
+          field_value_push(&o, rbytes[fields[f].vbeg + k]);                   \
+        close_field(&o, rec_out, (int)f, fields[f].start);                    \
+      }                                                                       \
+      close_record(&o, rec_out, (int)nf - 1, (off));                          \
+      rec_out++;                                                              \
+    }                                                                         \
+    rec_in++;                                                                 \
+    nf = 0; rb_len = 0; vbeg = 0;                                             \
+  } while (0)
   for (uint64_t i = 0; i < n; i++) {
     s = csv_step(&y, s, in[i], &tag);
     switch (tag) {
-      case T_DATA: field_value_push(&o, in[i]); break;
+      case T_DATA:
+        if (rb_len == rb_cap) {
+          rb_cap = rb_cap ? 2 * rb_cap : 256;
+          rbytes = (uint8_t*)realloc(rbytes, rb_cap);
+        }
+        rbytes[rb_len++] = in[i];
+        break;
       case T_CTRL: break;
       case T_FD:
-        close_field(&o, rec, col, field_start);
-        o.val_len = 0; col++; field_start = i + 1;
+        PUSH_FIELD();
+        vbeg = rb_len; field_start = i + 1;
         break;
       case T_RD:
-        close_field(&o, rec, col, field_start);
-        close_record(&o, rec, col, i);
-        rec++; col = 0; field_start = i + 1;
+        PUSH_FIELD();
+        CLOSE_RECORD(i);
+        field_start = i + 1;
         break;
       default:
         flag(st, E_INVALID_INPUT, i, 1);
@@ -451,13 +514,40 @@ int or_csv_parse(const uint8_t* in, uint64_t n, uint8_t fd, uint8_t rd, uint8_t 
   } else if (!csv_accepting(s)) {
     flag(st, E_BAD_END_STATE, n, 1);
   } else if (n > 0 && tag != T_RD) {            /* unterminated last record */
-    close_field(&o, rec, col, field_start);
-    close_record(&o, rec, col, n);
-    rec++;
+    PUSH_FIELD();
+    CLOSE_RECORD(n);
   }
-  st->n_records = rec;
+#undef PUSH_FIELD
+#undef CLOSE_RECORD
+  st->n_records = rec_out;
   free(o.val);
+  free(rbytes);
+  free(fields);
   return 0;
+}
+
+int or_csv_parse(const uint8_t* in, uint64_t n, uint8_t fd, uint8_t rd, uint8_t q, int crlf,
+                 int n_cols, const int32_t* col_types, int32_t** out_offsets,
+                 uint8_t** out_chars, void** out_typed, uint64_t records_capacity,
+                 const uint64_t* chars_capacity, or_status* st) {
+  return or_csv_parse_ex(in, n, fd, rd, q, crlf, n_cols, col_types, NULL, 0, NULL, 0,
+                         out_offsets, out_chars, out_typed, records_capacity, chars_capacity, st);
+}
+
+/* Rows are lines: the bytes up to and including each record-delimiter byte
+ * (rd), whatever the quoting (ParPaRaw Section 4, "Skipping rows": a record
+ * may span several rows), plus a last line without one.  Copies the input
+ * without the rows listed in skip_rows (sorted ascending) to out; returns
+ * the bytes written. */
+uint64_t or_skip_rows(const uint8_t* in, uint64_t n, uint8_t rd, const uint64_t* skip_rows,
+                      uint64_t n_skip_rows, uint8_t* out) {
+  uint64_t row = 0, w = 0, k = 0;
+  for (uint64_t i = 0; i < n; i++) {
+    while (k < n_skip_rows && skip_rows[k] < row) k++;
+    if (!(k < n_skip_rows && skip_rows[k] == row)) out[w++] = in[i];
+    if (in[i] == rd) row++;
+  }
+  return w;
 }
 
 /* ------------------------------------------------------------ tokenize */
