@@ -19,6 +19,7 @@ from __future__ import annotations
 import ctypes
 import os
 
+import numpy as np
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -50,7 +51,17 @@ class Status(ctypes.Structure):
     """pp_status (lives in device memory; this is its host image)."""
     _fields_ = [("error", ctypes.c_int32), ("reserved", ctypes.c_int32),
                 ("first_error_offset", _u64), ("n_records", _u64), ("n_tokens", _u64),
-                ("chars_len", _u64 * MAX_COLS)]
+                ("chars_len", _u64 * MAX_COLS), ("n_dropped", _u64)]
+
+
+class ParseOpts(ctypes.Structure):
+    """pp_parse_opts (host memory)."""
+    _fields_ = [("flags", ctypes.c_uint32), ("reserved", ctypes.c_uint32),
+                ("col_default", ctypes.c_void_p), ("skip_records", ctypes.c_void_p),
+                ("n_skip_records", _u64), ("skip_rows", ctypes.c_void_p), ("n_skip_rows", _u64)]
+
+
+PARSE_REJECT = 1
 
 
 STATUS_BYTES = ctypes.sizeof(Status)
@@ -69,6 +80,12 @@ def lib() -> ctypes.CDLL:
                                _sz, _vp, _vp, _vp]
         L.pp_parse_noalloc.restype = ctypes.c_int
         L.pp_parse_noalloc.argtypes = L.pp_parse.argtypes
+        L.pp_infer_types.restype = ctypes.c_int
+        L.pp_infer_types.argtypes = [_vp, _sz, ctypes.POINTER(DfaDesc), ctypes.c_int, _vp, _vp,
+                                     _vp]
+        L.pp_parse_ex.restype = ctypes.c_int
+        L.pp_parse_ex.argtypes = [_vp, _sz, ctypes.POINTER(DfaDesc), ctypes.c_int, _vp,
+                                  ctypes.POINTER(ParseOpts), _vp, _vp, _vp, _sz, _vp, _vp, _vp]
         L.pp_parse_host.restype = ctypes.c_int
         L.pp_parse_host.argtypes = L.pp_parse.argtypes[:-1] + [_sz, _vp]
         L.pp_tokenize_host.restype = ctypes.c_int
@@ -178,7 +195,8 @@ def read_status(st: torch.Tensor, n_cols: int = 0) -> dict:
     s = Status.from_buffer_copy(raw)
     return dict(error=int(s.error), first_error_offset=int(s.first_error_offset),
                 n_records=int(s.n_records), n_tokens=int(s.n_tokens),
-                chars_len=[int(s.chars_len[i]) for i in range(n_cols)])
+                chars_len=[int(s.chars_len[i]) for i in range(n_cols)],
+                n_dropped=int(s.n_dropped))
 
 
 def _ptr(t) -> int:
@@ -203,6 +221,59 @@ def pp_parse(d_in: torch.Tensor, n_bytes: int, desc: DfaDesc, col_types, out_off
                         int(records_capacity), ctypes.addressof(cc) if cc is not None else None,
                         _ptr(status), _stream(stream))
     _check(rc, "pp_parse")
+
+
+def parse_opts(defaults=None, reject=False, skip_records=None, skip_rows=None):
+    """A ParseOpts plus the host arrays it points to (keep both alive for
+    the call)."""
+    keep = []
+    o = ParseOpts()
+    o.flags = PARSE_REJECT if reject else 0
+    if defaults is not None:
+        a = np.ascontiguousarray([int(x) & 0xFFFFFFFFFFFFFFFF for x in defaults], dtype=np.uint64)
+        keep.append(a)
+        o.col_default = a.ctypes.data
+    for name, lst in (("skip_records", skip_records), ("skip_rows", skip_rows)):
+        if lst is not None and len(lst):
+            a = np.ascontiguousarray(sorted(int(x) for x in lst), dtype=np.uint64)
+            keep.append(a)
+            setattr(o, name, a.ctypes.data)
+            setattr(o, "n_" + name, a.size)
+    return o, keep
+
+
+def pp_parse_ex(d_in: torch.Tensor, n_bytes: int, desc: DfaDesc, col_types, opts, out_offsets,
+                out_chars, out_typed, records_capacity: int, chars_capacity, status: torch.Tensor,
+                stream=None) -> None:
+    """Direct pp_parse_ex call (opts: a ParseOpts, or None)."""
+    n = len(col_types)
+    ct = (ctypes.c_int * n)(*[COL[c] if isinstance(c, str) else int(c) for c in col_types])
+    arrs = [None if a is None else (_vp * n)(*[_ptr(x) for x in a])
+            for a in (out_offsets, out_chars, out_typed)]
+    cc = (_sz * n)(*[int(x) for x in chars_capacity]) if chars_capacity is not None else None
+    rc = lib().pp_parse_ex(
+        _ptr(d_in), int(n_bytes), ctypes.byref(desc), n, ctypes.addressof(ct),
+        ctypes.byref(opts) if opts is not None else None,
+        *[ctypes.addressof(a) if a is not None else None for a in arrs],
+        int(records_capacity), ctypes.addressof(cc) if cc is not None else None,
+        _ptr(status), _stream(stream))
+    _check(rc, "pp_parse_ex")
+
+
+TYPE_NAMES = {v: k for k, v in COL.items()}
+
+
+def infer_types(d_in: torch.Tensor, n_cols: int, desc: DfaDesc = None, n_bytes: int = None,
+                stream=None):
+    """pp_infer_types: per column the smallest type backing every field, as
+    column names ('i8', 'i32', 'i64', 'f64', 'str'), and the status."""
+    desc = desc or desc_csv()
+    n = d_in.numel() if n_bytes is None else n_bytes
+    types = torch.empty(max(n_cols, 1), dtype=torch.int32, device=d_in.device)
+    st = new_status(d_in.device)
+    _check(lib().pp_infer_types(_ptr(d_in), int(n), ctypes.byref(desc), int(n_cols),
+                                _ptr(types), _ptr(st), _stream(stream)), "pp_infer_types")
+    return [TYPE_NAMES[int(x)] for x in types[:n_cols].cpu()], read_status(st)
 
 
 def pp_parse_noalloc(d_in: torch.Tensor, n_bytes: int, desc: DfaDesc, col_types, out_offsets,
@@ -323,6 +394,14 @@ class CsvOutputs:
     def run(self, d_in: torch.Tensor, n_bytes: int, desc: DfaDesc, stream=None) -> None:
         pp_parse(d_in, n_bytes, desc, self.col_types, self.offsets, self.chars, self.typed,
                  self.records_capacity, self.chars_capacity, self.status, stream)
+
+    def run_ex(self, d_in: torch.Tensor, n_bytes: int, desc: DfaDesc, stream=None,
+               **options) -> None:
+        """pp_parse_ex with options (defaults, reject, skip_records, skip_rows)."""
+        opts, keep = parse_opts(**options)
+        pp_parse_ex(d_in, n_bytes, desc, self.col_types, opts, self.offsets, self.chars,
+                    self.typed, self.records_capacity, self.chars_capacity, self.status, stream)
+        del keep
 
     def run_noalloc(self, d_in: torch.Tensor, n_bytes: int, desc: DfaDesc, stream=None) -> None:
         pp_parse_noalloc(d_in, n_bytes, desc, self.col_types, self.offsets, self.chars,

@@ -12,7 +12,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpp.so")
 SOURCES = ["pp_api.cu", "pp_parse.cu", "pp_tokenize.cu", "pp_generic.cu", "pp_noalloc.cu",
-           "pp_stream.cu"]
+           "pp_stream.cu", "pp_options.cu"]
 HEADERS = ["pp_device.cuh", "pp_numeric.cuh", "pp_stv16.cuh", "pp_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC",

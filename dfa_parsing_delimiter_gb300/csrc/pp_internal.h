@@ -40,6 +40,7 @@ class DeviceOnce {
 };
 
 constexpr int MAX_STR_COLS = 16;  // string columns per pp_parse call
+constexpr uint8_t COL_INFER = 7;  // internal column kind: type inference only
 
 // Scratch of one pp_parse call (device memory).
 //   tile_stv, tile_state: per tile, its transition vector and its true start
@@ -87,6 +88,21 @@ struct ParseParams {
   void* typed[PP_MAX_COLS];
   uint64_t rec_cap;
   pp_status* st;
+  uint64_t defval[PP_MAX_COLS];  // bits stored for an empty or missing numeric field
+  // pp_parse_ex with dropped records (skipped or rejected), else null:
+  // bit r of drop_bits = record r of the input is not emitted; drop_pre[g]
+  // = dropped records before group g (256 records, 8 words); skip_list[0,
+  // n_skip) = the caller's sorted skipped records (no column-count check).
+  const uint32_t* drop_bits;
+  const uint64_t* drop_pre;
+  const uint64_t* skip_list;
+  uint64_t n_skip;
+  // Status pass of PP_PARSE_REJECT (no outputs), else null: bit r is set
+  // for every record r whose field count is not n_cols.
+  uint32_t* mark_bits;
+  // Type inference (pp_infer_types), else null: per column the largest
+  // type code of its fields (columns of kind COL_INFER).
+  uint32_t* infer_out;
   // Partial mode (streaming chunks), when not null: the input ends inside
   // an unfinished record, which is neither closed nor checked for an
   // accepting end state; st->n_records counts the complete records only,
@@ -120,6 +136,8 @@ size_t parse_tile_bytes();
 // and the launch (p from parse_prepare; its scratch is carved here)
 size_t fields_scratch_bytes(uint32_t n_tiles);
 cudaError_t launch_count_fields(ParseParams p, void* scratch, uint64_t* out, cudaStream_t stream);
+// codes (0 empty .. 5 string) -> pp_coltype, n entries (type inference)
+cudaError_t launch_infer_finish(const uint32_t* codes, int32_t* types, int n, cudaStream_t stream);
 
 // ---------------------------------------------------------- pp_tags / tokenize
 struct GenericDfa {

@@ -500,24 +500,27 @@ __global__ void __launch_bounds__(TS_NT) tile_state_kernel(const __grid_constant
 
 // Numeric field whose bytes are not all in the tile, contain control bytes
 // or need the full grammar: streaming accumulators over the value bytes.
-// Returns the error bits; *out receives the value (0 for an empty field).
+// Returns the error bits; *out receives the value (dflt, the column's
+// default, for a field without value bytes; 0 after an error).
 __device__ __forceinline__ int convert_general(const ParseParams& P, uint32_t ty, uint64_t fs,
                                             uint64_t fe, uint64_t tile_base,
                                             const uint8_t* tile_s, const uint32_t* ctrl_s,
                                             const uint32_t* my_lut, uint32_t fstate,
-                                            uint64_t* out) {
+                                            uint64_t dflt, uint64_t* out) {
   int err = 0;
-  uint64_t val = 0;
+  uint64_t val = dflt;
   if (ty == PP_COL_FLOAT64) {
     ppn::FloatAcc acc;
     const uint32_t nd = feed_field(acc, P.in, fs, fe, tile_base, tile_s, ctrl_s, my_lut, fstate);
     if (nd) err = acc.finish(&val);
   } else if (ty == PP_COL_TIMESTAMP) {
     ppn::TsAcc acc;
-    feed_field(acc, P.in, fs, fe, tile_base, tile_s, ctrl_s, my_lut, fstate);
-    int64_t x = 0;
-    err = acc.finish(&x);
-    val = uint64_t(x);
+    const uint32_t nd = feed_field(acc, P.in, fs, fe, tile_base, tile_s, ctrl_s, my_lut, fstate);
+    if (nd) {
+      int64_t x = 0;
+      err = acc.finish(&x);
+      val = uint64_t(x);
+    }
   } else {
     ppn::IntAcc acc;
     const uint32_t nd = feed_field(acc, P.in, fs, fe, tile_base, tile_s, ctrl_s, my_lut, fstate);
@@ -565,14 +568,14 @@ __device__ __forceinline__ uint32_t ctrl_x(const NumCtx& X, uint32_t p) {
 // or an error).
 template <int TY>
 __device__ __forceinline__ int convert_field(const ParseParams& P, uint32_t v, const NumCtx& X,
-                                             uint64_t& val) {
+                                             uint64_t dflt, uint64_t& val) {
   val = 0;
-  if (v == SLOT_DEFAULT) return 0;
+  if (v == SLOT_DEFAULT) { val = dflt; return 0; }  // a missing field: the column default
   const uint32_t fsr = v >> 16, fe = v & 0xFFFFu;
   if (fsr != 0xFFFFu &&
       (!X.any_ctrl || ctrl_x(X, fe) == ctrl_x(X, fsr))) {
     const uint32_t L = fe - fsr;
-    if (L == 0) return 0;  // empty field: the column default
+    if (L == 0) { val = dflt; return 0; }  // an empty field: the column default
     if (TY == PP_COL_TIMESTAMP) {  // five words of the tile from the field start
       const uint32_t a = fsr + X.toff, q = a >> 2, sh = (a & 3u) * 8u;
       uint32_t x[5];
@@ -631,16 +634,16 @@ __device__ __forceinline__ int convert_field(const ParseParams& P, uint32_t v, c
   }
   return convert_general(P, TY, fsr == 0xFFFFu ? X.tile_fstart : X.tile_base + fsr,
                          X.tile_base + fe, X.tile_base, X.tile_s, X.ctrl_s, X.lut,
-                         X.tile_fstate, &val);
+                         X.tile_fstate, dflt, &val);
 }
 
 // Convert one row's field (slot value v) of a column of type TY, store it
 // at out[rec] and report a number error at the field's first byte.
 template <int TY>
 __device__ __forceinline__ void convert_store(const ParseParams& P, const NumCtx& X, void* out,
-                                              uint64_t rec, uint32_t v) {
+                                              uint64_t rec, uint32_t v, uint64_t dflt) {
   uint64_t val;
-  const int err = convert_field<TY>(P, v, X, val);
+  const int err = convert_field<TY>(P, v, X, dflt, val);
   if (TY == PP_COL_INT32) static_cast<int32_t*>(out)[rec] = int32_t(val);
   else if (TY == PP_COL_INT8) static_cast<int8_t*>(out)[rec] = int8_t(val);
   else static_cast<uint64_t*>(out)[rec] = val;
@@ -648,6 +651,68 @@ __device__ __forceinline__ void convert_store(const ParseParams& P, const NumCtx
     const uint32_t fsr = v >> 16;
     report(P.st, err, fsr == 0xFFFFu ? X.tile_fstart : X.tile_base + fsr, true);
   }
+}
+
+// ------------------------------------------------------ type inference
+// The smallest type backing a field's value (ParPaRaw Section 4, "Type
+// inference"): 1 int8, 2 int32, 3 int64, 4 float64 (also an integer beyond
+// int64), 5 string; 0 for an empty or missing field.  Both number grammars
+// read the value bytes at once.
+struct TypeAcc {
+  ppn::IntAcc i;
+  ppn::FloatAcc f;
+  __device__ __forceinline__ void feed(uint32_t c) { i.feed(c); f.feed(c); }
+};
+__device__ __forceinline__ uint32_t infer_field(const ParseParams& P, uint32_t v, const NumCtx& X) {
+  if (v == SLOT_DEFAULT) return 0;
+  const uint32_t fsr = v >> 16, fe = v & 0xFFFFu;
+  TypeAcc acc;
+  const uint32_t nd = feed_field(acc, P.in, fsr == 0xFFFFu ? X.tile_fstart : X.tile_base + fsr,
+                                 X.tile_base + fe, X.tile_base, X.tile_s, X.ctrl_s, X.lut,
+                                 X.tile_fstate);
+  if (!nd) return 0;
+  int64_t x;
+  const int rc = acc.i.finish(128ull, 127ull, &x);
+  if (rc == 0) return 1;
+  if (rc == PP_ERR_NUM_OVERFLOW) {
+    if (acc.i.finish(2147483648ull, 2147483647ull, &x) == 0) return 2;
+    if (acc.i.finish(9223372036854775808ull, 9223372036854775807ull, &x) == 0) return 3;
+    return 4;
+  }
+  uint64_t b;
+  return acc.f.finish(&b) == 0 ? 4u : 5u;
+}
+
+__global__ void infer_finish_kernel(const uint32_t* codes, int32_t* types, int n) {
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= n) return;
+  static constexpr int32_t kind[6] = {PP_COL_INT8, PP_COL_INT8, PP_COL_INT32, PP_COL_INT64,
+                                      PP_COL_FLOAT64, PP_COL_STRING};
+  types[c] = kind[min(codes[c], 5u)];
+}
+
+// ------------------------------------------------ dropped records (pp_parse_ex)
+__device__ __forceinline__ bool rec_dropped(const ParseParams& P, uint64_t rec) {
+  return (P.drop_bits[rec >> 5] >> (rec & 31u)) & 1u;
+}
+// dropped records before record `rec`
+__device__ __forceinline__ uint64_t dropped_before(const ParseParams& P, uint64_t rec) {
+  const uint64_t g = rec >> 8, w = rec >> 5;
+  uint64_t d = P.drop_pre[g];
+  for (uint64_t k = g << 3; k < w; ++k) d += __popc(P.drop_bits[k]);
+  const uint32_t b = uint32_t(rec & 31u);
+  if (b) d += __popc(P.drop_bits[w] & ((1u << b) - 1u));
+  return d;
+}
+// record `rec` is on the caller's skip list (skipped records are not checked)
+__device__ __forceinline__ bool rec_skip_listed(const ParseParams& P, uint64_t rec) {
+  uint64_t lo = 0, hi = P.n_skip;
+  while (lo < hi) {
+    const uint64_t mid = (lo + hi) >> 1;
+    if (P.skip_list[mid] < rec) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo < P.n_skip && P.skip_list[lo] == rec;
 }
 
 // ================================================================ 1. tile pass
@@ -945,6 +1010,7 @@ struct PShared {
   uint8_t numcol[PP_MAX_COLS];     // numeric output columns, floats first
   uint32_t n_num;
   uint32_t lut1[256];              // the LUT, one entry per byte value
+  uint32_t inf[PP_MAX_COLS];       // type inference: largest type code per column
   uint16_t cpl[NT + 1];            // control bytes before chunk t inside its warp
   uint16_t lk[2][NT];              // long string field (item) continuing in / starting in chunk t
 };
@@ -979,7 +1045,10 @@ __device__ void ctx_role(const ParseParams& P, PShared& S) {
     const uint32_t b = it & 1u;
     bar_sync(BAR_AGG, NT + 32);  // the workers' tile aggregate (or their exit)
     const uint32_t tile = S.tile[b];
-    if (tile >= P.n_tiles) break;
+    if (tile >= P.n_tiles) {
+      bar_arrive(BAR_V2, NTF_);  // the last barrier the other roles wait on
+      break;
+    }
     const uint64_t tile_base = uint64_t(tile) * TILE;
     uint64_t agg[3], ex[3];
     agg[0] = S.agg_rec;
@@ -1012,10 +1081,10 @@ __device__ void chars_role(const ParseParams& P, PShared& S) {
   const uint32_t n_cols = uint32_t(P.n_cols);
   for (uint32_t it = 0;; ++it) {
     const uint32_t b = it & 1u;
-    bar_sync(BAR_W2, NT + 32);  // the workers' value-byte totals (or their exit)
+    bar_sync(BAR_V2, NTF_);     // the entry column (or the workers' exit)
     const uint32_t tile = S.tile[b];
     if (tile >= P.n_tiles) break;
-    bar_sync(BAR_V2, NTF_);     // the entry column
+    bar_sync(BAR_W2, NT + 32);  // the workers' value-byte totals
     uint64_t cagg[K3];
     const uint32_t col_in = S.col_in;
     const uint32_t nrel = min(S.n_rel, n_cols);
@@ -1078,7 +1147,7 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
   const uint32_t toff = uint32_t(reinterpret_cast<uintptr_t>(P.in) & 15u);
   for (int k = t; k < 256 * 32; k += NTF) lut_s[k] = P.lut[k >> 5];
   for (int k = t; k < 256; k += NTF) S.lut1[k] = P.lut[k];
-  if (t < PP_MAX_COLS) S.coltype[t] = P.coltype[t];
+  if (t < PP_MAX_COLS) { S.coltype[t] = P.coltype[t]; S.inf[t] = 0; }
   if (t < ppi::MAX_STR_COLS) S.carry[t] = 0;
   if (t == 0) {
     uint32_t m = 0;
@@ -1117,6 +1186,11 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
   const uint32_t n_str = NS > 0 ? uint32_t(P.n_str) : 0u;
   const uint32_t rpb = max(1u, (uint32_t(SLOT_CAP) - n_cols) / n_cols);  // rows per pass
   const bool partial = P.record_end != nullptr;
+  const bool emit = P.drop_bits != nullptr;    // some records are not emitted
+  const bool status = P.mark_bits != nullptr;  // the status pass of rejection
+  // status pass: rows of the tile with a wrong field count (pos_s's space,
+  // which only string staging uses)
+  uint32_t* const flags_s = reinterpret_cast<uint32_t*>(pos_s);
 
   uint32_t nph[2] = {S.issued[0], 0u};  // thread 0: bulk copies started per buffer
   // The next tile's ticket and bulk copy (thread 0), taken late in the
@@ -1139,7 +1213,7 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
     const uint32_t tile = S.tile[b];
     if (tile >= P.n_tiles) {
       bar_arrive(BAR_AGG, NT + 32);  // the scan warps see the end too
-      if (NS > 0) bar_arrive(BAR_W2, NT + 32);
+      bar_sync(BAR_V2, NTF);
       break;
     }
     uint8_t* buf = lin0 + b * BUF_BYTES;
@@ -1151,6 +1225,8 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
     const uint32_t s_tile = P.s.tile_state[tile];
     if (t < ppi::MAX_STR_COLS) S.ctot[t] = 0;
     if (t < PP_MAX_COLS) S.rel_len[t] = 0;
+    if (status)
+      for (int q = t; q < (TILE + 32) / 32 + 1; q += NT) flags_s[q] = 0;
     if (t == 0) { S.n_rel = 0; S.rd0_pos = 0; S.rd0_k = 0; S.virt = 0; }
 
     // ---- the tile's bytes: bulk copy, plus plain loads at the input's ends
@@ -1296,8 +1372,10 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
           if (first) {
             if (col < n_cols) {
               S.rel_slot[col] = (fs << 16) | e;
-              const uint32_t L = value_len(fs, e, any_ctrl, ctrl_s, S);
-              if (L) atomicAdd(&S.rel_len[col], L);
+              if (!emit) {
+                const uint32_t L = value_len(fs, e, any_ctrl, ctrl_s, S);
+                if (L) atomicAdd(&S.rel_len[col], L);
+              }
               atomicMax(&S.n_rel, col + 1);
             }
             if (isrd) { S.rd0_pos = e + 1; S.rd0_k = col; }
@@ -1305,80 +1383,87 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
           return;
         }
         if (in_pass && col < n_cols) slot_s[col * nrp + (rl - lo)] = (fs << 16) | e;
-        if (NS > 0 && first && col < n_cols && ((P.strmask >> col) & 1u)) {
+        if (NS > 0 && first && !emit && col < n_cols && ((P.strmask >> col) & 1u)) {
           const uint32_t L = value_len(fs, e, any_ctrl, ctrl_s, S);
           if (L) add16(cnt, P.stridx[col], L);
         }
         if (isrd && !open && col != n_cols - 1) {
-          if (first) report(P.st, PP_ERR_COLCOUNT, tile_base + e, true);
+          if (first && !emit && !P.infer_out) report(P.st, PP_ERR_COLCOUNT, tile_base + e, true);
+          if (first && status) atomicOr(&flags_s[rl >> 5], 1u << (rl & 31u));
           if (in_pass)  // missing fields take the column default
             for (uint32_t c = col + 1; c < n_cols; ++c) slot_s[c * nrp + (rl - lo)] = SLOT_DEFAULT;
         }
       };
-      if (wn <= WLIST_CAP) {
-        // the warp's terminators in input order (tile position | RD << 15),
-        // then a lane per field: row and column from a ballot of the RDs
-        uint16_t* const wl = reinterpret_cast<uint16_t*>(stage_s) + warp * WLIST_CAP;
-        {
-          uint32_t m = term_all, i = tbase;
-          while (m) {
-            const uint32_t j = __ffs(m) - 1;
-            m &= m - 1;
-            wl[i++] = uint16_t((cstart + j) | (((rd >> j) & 1u) << 15));
-          }
-          if (virt_rd) wl[i] = uint16_t(tile_len | 0x8000u);
+      // The warp's fields in input order, each passed to act(row, column
+      // (row 0: index), start, end, ends a record, still open).
+      const bool listed = wn <= WLIST_CAP;
+      uint16_t* const wl = reinterpret_cast<uint16_t*>(stage_s) + warp * WLIST_CAP;
+      if (listed) {
+        // the warp's terminators in input order (tile position | RD << 15)
+        uint32_t m = term_all, i = tbase;
+        while (m) {
+          const uint32_t j = __ffs(m) - 1;
+          m &= m - 1;
+          wl[i++] = uint16_t((cstart + j) | (((rd >> j) & 1u) << 15));
         }
+        if (virt_rd) wl[i] = uint16_t(tile_len | 0x8000u);
         __syncwarp();
-        uint32_t crow = __shfl_sync(FULL, rl0, 0), ccol = __shfl_sync(FULL, col0, 0),
-                 cfs = __shfl_sync(FULL, fs0, 0);
-        const uint32_t lt = (1u << lane) - 1u;
-        for (uint32_t b0 = 0; b0 < wn; b0 += 32) {
-          const uint32_t k = b0 + uint32_t(lane);
-          const uint32_t ent = k < wn ? uint32_t(wl[k]) : 0u;
-          const uint32_t e = ent & 0x7FFFu;
-          const bool isrd = (ent >> 15) != 0;
-          const uint32_t pe = __shfl_up_sync(FULL, e, 1);
-          const uint32_t fs = lane == 0 ? cfs : pe + 1u;
-          const uint32_t rdm = __ballot_sync(FULL, k < wn && isrd);
-          const uint32_t below = rdm & lt;
-          const uint32_t rl = crow + __popc(below);
-          const uint32_t col = below ? uint32_t(lane) - (32u - __clz(below))
-                                     : min(ccol + uint32_t(lane), 0x7FFFFF00u);
-          if (k < wn) enter(rl, col, fs, e, isrd, false);
-          const uint32_t nin = min(32u, wn - b0);
-          crow += __popc(rdm);
-          ccol = rdm ? (nin - 1u) - (31u - __clz(rdm)) : min(ccol + nin, 0x7FFFFF00u);
-          cfs = __shfl_sync(FULL, e, nin - 1) + 1u;
-        }
-        // the field still open at the tile end (its value bytes are counted
-        // and staged here)
-        if (owns_tail && !any_virt) enter(crow, ccol, cfs, tile_len, false, true);
-      } else {  // each lane walks its chunk's fields
-        uint32_t term = term_all, col = col0, rl = rl0, fs = fs0;
-        bool vrd = virt_rd;
-        for (;;) {
-          uint32_t e;
-          bool isrd;
-          if (term) {
-            const uint32_t j = __ffs(term) - 1;
-            term &= term - 1;
-            e = cstart + j;
-            isrd = (rd >> j) & 1u;
-          } else if (vrd) {
-            e = tile_len;
-            isrd = true;
-            vrd = false;
-          } else {
-            break;
-          }
-          enter(rl, col, fs, e, isrd, false);
-          if (isrd) { ++rl; col = 0; }
-          else col = col < 0x7FFFFF00u ? col + 1 : col;
-          fs = e + 1;
-        }
-        if (owns_tail && !any_virt) enter(rl, col, fs, tile_len, false, true);
       }
-      if (NS > 0 && first) {  // warp sums of the packed counters -> tile totals
+      auto walk = [&](auto&& act) {
+        if (listed) {
+          // a lane per field: row and column from a ballot of the RDs
+          uint32_t crow = __shfl_sync(FULL, rl0, 0), ccol = __shfl_sync(FULL, col0, 0),
+                   cfs = __shfl_sync(FULL, fs0, 0);
+          const uint32_t lt = (1u << lane) - 1u;
+          for (uint32_t b0 = 0; b0 < wn; b0 += 32) {
+            const uint32_t k = b0 + uint32_t(lane);
+            const uint32_t ent = k < wn ? uint32_t(wl[k]) : 0u;
+            const uint32_t e = ent & 0x7FFFu;
+            const bool isrd = (ent >> 15) != 0;
+            const uint32_t pe = __shfl_up_sync(FULL, e, 1);
+            const uint32_t fs = lane == 0 ? cfs : pe + 1u;
+            const uint32_t rdm = __ballot_sync(FULL, k < wn && isrd);
+            const uint32_t below = rdm & lt;
+            const uint32_t rl = crow + __popc(below);
+            const uint32_t col = below ? uint32_t(lane) - (32u - __clz(below))
+                                       : min(ccol + uint32_t(lane), 0x7FFFFF00u);
+            if (k < wn) act(rl, col, fs, e, isrd, false);
+            const uint32_t nin = min(32u, wn - b0);
+            crow += __popc(rdm);
+            ccol = rdm ? (nin - 1u) - (31u - __clz(rdm)) : min(ccol + nin, 0x7FFFFF00u);
+            cfs = __shfl_sync(FULL, e, nin - 1) + 1u;
+          }
+          // the field still open at the tile end (its value bytes are counted
+          // and staged here)
+          if (owns_tail && !any_virt) act(crow, ccol, cfs, tile_len, false, true);
+        } else {  // each lane walks its chunk's fields
+          uint32_t term = term_all, col = col0, rl = rl0, fs = fs0;
+          bool vrd = virt_rd;
+          for (;;) {
+            uint32_t e;
+            bool isrd;
+            if (term) {
+              const uint32_t j = __ffs(term) - 1;
+              term &= term - 1;
+              e = cstart + j;
+              isrd = (rd >> j) & 1u;
+            } else if (vrd) {
+              e = tile_len;
+              isrd = true;
+              vrd = false;
+            } else {
+              break;
+            }
+            act(rl, col, fs, e, isrd, false);
+            if (isrd) { ++rl; col = 0; }
+            else col = col < 0x7FFFFF00u ? col + 1 : col;
+            fs = e + 1;
+          }
+          if (owns_tail && !any_virt) act(rl, col, fs, tile_len, false, true);
+        }
+      };
+      walk(enter);
+      if (NS > 0 && first && !emit) {  // warp sums of the packed counters -> tile totals
         bool any = false;
 #pragma unroll
         for (int k = 0; k < NSW; ++k) any |= cnt[k] != 0;
@@ -1396,7 +1481,7 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
         }
       }
       if (first) {
-        if (NS > 0) bar_arrive(BAR_W2, NT + 32);
+        if (NS > 0 && !emit) bar_arrive(BAR_W2, NT + 32);
         // ---- the tile's context from the look-back
         bar_sync(BAR_V2, NTF);
         rec0 = S.rec0;
@@ -1413,16 +1498,43 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
           }
           if (any_virt) col_end = n_cols;
         }
+        if (emit) {
+          // dropped records known: the emitted value bytes per string
+          // column, and the column-count check of every record closed here
+          // that is not on the skip list
+          walk([&](uint32_t rl, uint32_t col, uint32_t fs, uint32_t e, bool isrd, bool open) {
+            const uint64_t rec = rec0 + rl;
+            if (rl > 0 && isrd && !open && col != n_cols - 1 && !rec_skip_listed(P, rec))
+              report(P.st, PP_ERR_COLCOUNT, tile_base + e, true);
+            const uint32_t c = rl == 0 ? col_in + col : col;
+            if (NS > 0 && c < n_cols && ((P.strmask >> c) & 1u) && !rec_dropped(P, rec)) {
+              const uint32_t L = value_len(fs, e, any_ctrl, ctrl_s, S);
+              if (L) atomicAdd(&S.ctot[P.stridx[c]], L);
+            }
+          });
+          if (NS > 0) bar_arrive(BAR_W2, NT + 32);
+        }
         // row 0: its fields' columns follow the entry column
         const uint32_t nrel = S.n_rel;
         if (uint32_t(t) < nrel && col_in + t < n_cols) slot_s[(col_in + t) * nrp] = S.rel_slot[t];
         if (S.rd0_pos) {
           const uint32_t nf = col_in + S.rd0_k + 1;  // fields of the record
           if (nf != n_cols) {
-            if (t == 0) report(P.st, PP_ERR_COLCOUNT, tile_base + S.rd0_pos - 1, true);
+            if (t == 0 && !(emit && rec_skip_listed(P, rec0)) && !P.infer_out)
+              report(P.st, PP_ERR_COLCOUNT, tile_base + S.rd0_pos - 1, true);
+            if (t == 0 && status) atomicOr(&P.mark_bits[rec0 >> 5], 1u << (rec0 & 31u));
             for (uint32_t c = nf + t; c < n_cols; c += NT) slot_s[c * nrp] = SLOT_DEFAULT;
           }
         }
+        if (status)  // the records of rows >= 1 with a wrong field count, to the input's bitmap
+          for (uint32_t q = t; q < (rows + 31) / 32; q += NT) {
+            uint32_t m = flags_s[q];
+            while (m) {
+              const uint64_t rec = rec0 + 32u * q + uint32_t(__ffs(m) - 1);
+              m &= m - 1;
+              atomicOr(&P.mark_bits[rec >> 5], 1u << (rec & 31u));
+            }
+          }
       }
       bar_sync(BAR_W, NT);
       if (!P.has_out) {  // a sizing pass: counts only
@@ -1431,8 +1543,6 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
         break;
       }
       const uint32_t ngr = (nr + 31) / 32;
-      const uint32_t rec_lim =  // records of the tile the outputs have room for
-          P.rec_cap > rec0 ? uint32_t(min(P.rec_cap - rec0, uint64_t(0xFFFFFFFFu))) : 0u;
 
       if (NS > 0 && n_str) {
         // ---- string fields: value bytes -> chars positions (block scan
@@ -1449,7 +1559,7 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
             const uint32_t row = lo + r;
             const bool closed = (row > 0 || c >= col_in) && (row + 1 < rows || c < col_end);
             const bool open = row + 1 == rows && c == col_end && !any_virt;
-            if (closed || open) {
+            if ((closed || open) && !(emit && rec_dropped(P, rec0 + row))) {
               const uint32_t v = slot_s[c * nrp + r];
               if (v != SLOT_DEFAULT) {
                 const bool before = (v >> 16) == REL_START;
@@ -1563,16 +1673,26 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
           const uint32_t r_first = c < col_in ? 1u : 0u;  // rows whose field c closes here
           const uint32_t r_end = c < col_end ? rows : rows - 1u;
           if (r < r_first || r >= r_end) continue;
-          if (r >= rec_lim) { report(P.st, PP_ERR_CAPACITY, 0, false); continue; }
+          uint64_t rec = rec0 + r;
+          if (emit) {
+            if (rec_dropped(P, rec)) continue;
+            rec -= dropped_before(P, rec);
+          }
+          if (rec >= P.rec_cap) { report(P.st, PP_ERR_CAPACITY, 0, false); continue; }
           const uint32_t v = slot_s[c * nrp + (r - lo)];
           void* const out = P.typed[c];
-          const uint64_t rec = rec0 + r;
+          const uint64_t dflt = P.defval[c];
           switch (S.coltype[c]) {
-            case PP_COL_FLOAT64: convert_store<PP_COL_FLOAT64>(P, X, out, rec, v); break;
-            case PP_COL_INT64: convert_store<PP_COL_INT64>(P, X, out, rec, v); break;
-            case PP_COL_TIMESTAMP: convert_store<PP_COL_TIMESTAMP>(P, X, out, rec, v); break;
-            case PP_COL_INT32: convert_store<PP_COL_INT32>(P, X, out, rec, v); break;
-            default: convert_store<PP_COL_INT8>(P, X, out, rec, v); break;
+            case PP_COL_FLOAT64: convert_store<PP_COL_FLOAT64>(P, X, out, rec, v, dflt); break;
+            case PP_COL_INT64: convert_store<PP_COL_INT64>(P, X, out, rec, v, dflt); break;
+            case PP_COL_TIMESTAMP: convert_store<PP_COL_TIMESTAMP>(P, X, out, rec, v, dflt); break;
+            case PP_COL_INT32: convert_store<PP_COL_INT32>(P, X, out, rec, v, dflt); break;
+            case ppi::COL_INFER: {
+              const uint32_t code = infer_field(P, v, X);
+              if (code) atomicMax(&S.inf[c], code);
+              break;
+            }
+            default: convert_store<PP_COL_INT8>(P, X, out, rec, v, dflt); break;
           }
         }
       }
@@ -1589,7 +1709,11 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
           const uint32_t r = lo + gi * 32 + lane;
           const uint32_t c = P.strcol[si];
           if (r >= hi || (r == 0 && c < col_in) || (r + 1 == rows && c >= col_end)) continue;
-          const uint64_t rec = rec0 + r;
+          uint64_t rec = rec0 + r;
+          if (emit) {
+            if (rec_dropped(P, rec)) continue;
+            rec -= dropped_before(P, rec);
+          }
           if (rec >= P.rec_cap) { report(P.st, PP_ERR_CAPACITY, 0, false); continue; }
           const uint64_t off = S.base[si] + S.carry[si] + (pos_s[si * nr + (r - lo)] - S.cstart[si]);
           if (off > 0x7FFFFFFFull || off > P.chars_cap[si]) report(P.st, PP_ERR_CAPACITY, 0, false);
@@ -1632,7 +1756,16 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
       bar_sync(BAR_W, NT);
     }
     if (t < int(n_str)) S.carry[t] = 0;
-    if (owns_end) P.st->n_records = rec0 + (rows - 1) + (virt_rd ? 1u : 0u);
+    if (P.infer_out && t < int(n_cols) && S.inf[t]) {  // this tile's types, to the input's
+      atomicMax(&P.infer_out[t], S.inf[t]);
+      S.inf[t] = 0;
+    }
+    if (owns_end) {
+      const uint64_t total = rec0 + (rows - 1) + (virt_rd ? 1u : 0u);  // records of the input
+      const uint64_t dropped = emit ? dropped_before(P, total) : 0ull;
+      P.st->n_records = total - dropped;
+      P.st->n_dropped = dropped;
+    }
     bar_sync(BAR_W, NT);
   }
 }
@@ -1824,6 +1957,7 @@ __global__ void parse_init_kernel(ParseParams P) {
     st->n_records = 0;
     st->n_tokens = 0;
     for (int c = 0; c < PP_MAX_COLS; ++c) st->chars_len[c] = 0;
+    st->n_dropped = 0;
     if (P.has_out)
       for (int c = 0; c < P.n_str; ++c) P.offsets[c][0] = 0;
   }
@@ -1954,6 +2088,11 @@ cudaError_t launch_count_fields(ParseParams p, void* scratch, uint64_t* out, cud
   p.s.tstate_words = reinterpret_cast<unsigned long long*>(b);
   b += align256(size_t(p.s.n_tstate_blocks) * 8);
   return launch_fields(p, reinterpret_cast<FAgg*>(b), out, stream);
+}
+
+cudaError_t launch_infer_finish(const uint32_t* codes, int32_t* types, int n, cudaStream_t stream) {
+  infer_finish_kernel<<<1, 64, 0, stream>>>(codes, types, n);
+  return cudaGetLastError();
 }
 
 int parse_ns_width(int n_str) {

@@ -753,6 +753,7 @@ __global__ void tok_init_kernel(uint4* zero, size_t n16, pp_status* st) {
     st->n_records = 0;
     st->n_tokens = 0;
     for (int c = 0; c < PP_MAX_COLS; ++c) st->chars_len[c] = 0;
+    st->n_dropped = 0;
   }
 }
 

@@ -135,6 +135,8 @@ typedef struct {
   uint64_t n_tokens;             /* pp_tokenize                            */
   uint64_t chars_len[PP_MAX_COLS]; /* pp_parse: chars of column c (string
                                     columns; 0 for the others)             */
+  uint64_t n_dropped;            /* pp_parse_ex: records of the input not
+                                    emitted (skipped or rejected)          */
 } pp_status;
 
 /*
@@ -169,6 +171,56 @@ pp_rc pp_parse(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa, int 
                uint8_t* const out_chars[], void* const out_typed[],
                size_t records_capacity, const size_t chars_capacity[],
                pp_status* d_status, cudaStream_t stream);
+
+/* pp_parse_ex options (ParPaRaw Section 4).  A zero-initialised struct (or
+ * a NULL pointer) gives pp_parse's behaviour. */
+#define PP_PARSE_REJECT 1u  /* records whose field count is not n_cols are not
+                               emitted (they still set PP_ERR_COLCOUNT)     */
+typedef struct {
+  uint32_t flags;               /* PP_PARSE_* bits                            */
+  uint32_t reserved;            /* 0                                          */
+  const uint64_t* col_default;  /* host, n_cols entries, or NULL: the bits
+                                   stored for an empty or missing field of a
+                                   numeric or timestamp column (int64 two's
+                                   complement, binary64 bits or seconds;
+                                   truncated to int8/int32 columns) instead of
+                                   0.  Section 4, "Default values for empty
+                                   strings".  String columns keep the empty
+                                   string.                                    */
+  const uint64_t* skip_records; /* host, ascending indices of records not to
+                                   emit (counted in the input after skipped
+                                   rows), or NULL.  Section 4, "Skipping
+                                   records and selecting columns": their
+                                   fields are irrelevant (not converted, no
+                                   column-count check).                       */
+  uint64_t n_skip_records;
+  const uint64_t* skip_rows;    /* host, ascending indices of rows (lines:
+                                   bytes up to and including each record-
+                                   delimiter byte, whatever the quoting, plus
+                                   a last line without one) removed before
+                                   parsing, or NULL.  Section 4, "Skipping
+                                   rows".  Error offsets then refer to the
+                                   input without those rows.                  */
+  uint64_t n_skip_rows;
+} pp_parse_opts;
+
+/*
+ * pp_parse_ex — pp_parse with the options above.  Emitted records are
+ * numbered 0.. in input order without the dropped ones; n_records counts
+ * the emitted records and n_dropped the others.
+ *   Extra device memory (stream-ordered): with skip_rows, a copy of the
+ *   input without those rows (n_bytes); with PP_PARSE_REJECT or
+ *   skip_records, a dropped-record bitmap and its prefix sums (about
+ *   n_bytes / 6) and one more pass over the input for PP_PARSE_REJECT.
+ *   skip_rows needs the record delimiter to be the byte the descriptor's
+ *   PP_TAG_RD transitions read (as for pp_desc_csv / pp_desc_csv_crlf).
+ * Returns as pp_parse; PP_EINVAL also for unsorted skip lists.
+ */
+pp_rc pp_parse_ex(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa, int n_cols,
+                  const pp_coltype* col_types, const pp_parse_opts* opts,
+                  int32_t* const out_offsets[], uint8_t* const out_chars[],
+                  void* const out_typed[], size_t records_capacity,
+                  const size_t chars_capacity[], pp_status* d_status, cudaStream_t stream);
 
 /*
  * pp_parse_host — pp_parse of an input in HOST memory into outputs in HOST
@@ -326,6 +378,31 @@ pp_rc pp_count_byte(const uint8_t* d_in, size_t n_bytes, uint8_t value, uint64_t
  */
 pp_rc pp_count_fields(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa,
                       uint64_t* d_fields, pp_status* d_status, cudaStream_t stream);
+
+/*
+ * pp_infer_types — numeric type inference (ParPaRaw Section 4, "Type
+ * inference"): for each of the first n_cols columns, the smallest of
+ * PP_COL_INT8 < PP_COL_INT32 < PP_COL_INT64 < PP_COL_FLOAT64 <
+ * PP_COL_STRING that backs every field of the column.  A field's value
+ * bytes (quotes dropped, as pp_parse reads them) take int8/int32/int64 when
+ * they match [+-]?[0-9]+ within that range, float64 when they match the
+ * float grammar of PP_COL_FLOAT64 or are an integer beyond int64, and
+ * string otherwise; empty and missing fields constrain nothing, so a
+ * column without a non-empty field is PP_COL_INT8.  Fields past n_cols
+ * are ignored.  Each tile classifies its fields and reduces them per
+ * column; the tiles combine by an atomic maximum.
+ *   d_in      device, n_bytes bytes (any alignment); dfa as for pp_parse.
+ *   n_cols    1..PP_MAX_COLS (for instance the most fields per record from
+ *             pp_count_fields).
+ *   d_types   device int32[n_cols]: pp_coltype values.
+ *   d_status  device; PP_ERR_INVALID_INPUT and PP_ERR_BAD_END_STATE as
+ *             pp_parse (records need not have n_cols fields: no
+ *             PP_ERR_COLCOUNT; no PP_ERR_NUM_*), and n_records.
+ * Scratch as pp_parse, stream-ordered; asynchronous on `stream`.
+ * Returns PP_EINVAL for bad arguments, PP_ENOMEM / PP_ECUDA on CUDA errors.
+ */
+pp_rc pp_infer_types(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa, int n_cols,
+                     int32_t* d_types, pp_status* d_status, cudaStream_t stream);
 
 /*
  * pp_desc_csv — build the quoted-CSV DFA (RFC-4180 style quoting) with

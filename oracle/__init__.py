@@ -73,6 +73,8 @@ def _load():
                                       _vp, ctypes.c_int, _vp, _u64, _vp, _vp, _vp, _u64, _vp,
                                       ctypes.POINTER(Status)]
         L.or_skip_rows.argtypes = [_vp, _u64, _u8, _vp, _u64, _vp]
+        L.or_infer_types.argtypes = [_vp, _u64, _u8, _u8, _u8, ctypes.c_int, ctypes.c_int, _vp,
+                                     ctypes.POINTER(Status)]
         L.or_skip_rows.restype = _u64
         L.or_count_fields.argtypes = [_vp, _u64, _u8, _u8, _u8, ctypes.c_int, _vp,
                                       ctypes.POINTER(Status)]
@@ -171,6 +173,22 @@ def csv_parse(data, col_types, fd=b",", rd=b"\n", quote=b'"', records_capacity=N
         else:
             cols.append(typed[c][:R])
     return cols, st.as_dict(ncols)
+
+
+INFER_NAMES = {1: "i8", 2: "i32", 3: "i64", 4: "f64", 0: "str"}
+
+
+def infer_types(data, n_cols, fd=b",", rd=b"\n", quote=b'"', crlf=False):
+    """Per column the smallest of int8 < int32 < int64 < float64 < string
+    that backs every field (ParPaRaw Section 4, "Type inference"), as the
+    library's column names, and the status."""
+    L = _load()
+    a = _arr(data)
+    out = np.zeros(max(n_cols, 1), dtype=np.int32)
+    st = Status()
+    L.or_infer_types(a.ctypes.data, a.size, fd[0], rd[0], quote[0], int(bool(crlf)), n_cols,
+                     out.ctypes.data, ctypes.byref(st))
+    return [INFER_NAMES[int(x)] for x in out[:n_cols]], st.as_dict()
 
 
 def count_fields(data, fd=b",", rd=b"\n", quote=b'"', crlf=False):

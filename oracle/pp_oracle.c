@@ -509,10 +509,19 @@ int or_csv_parse_ex(const uint8_t* in, uint64_t n, uint8_t fd, uint8_t rd, uint8
         break;
     }
   }
-  if (s == INV) {
-    /* the automaton died; nothing after the invalid byte forms a field */
-  } else if (!csv_accepting(s)) {
-    flag(st, E_BAD_END_STATE, n, 1);
+  if (s == INV || !csv_accepting(s)) {
+    /* the input ends inside a record that never closes (the automaton
+     * died, or ended in a non-accepting state): the fields the record
+     * closed are converted as they closed (unless the record is skipped);
+     * nothing else of it forms a field */
+    if (s != INV) flag(st, E_BAD_END_STATE, n, 1);
+    while (skip_i < n_skip_records && skip_records[skip_i] < rec_in) skip_i++;
+    if (!(skip_i < n_skip_records && skip_records[skip_i] == rec_in))
+      for (size_t f = 0; f < nf; f++) {
+        o.val_len = 0;
+        for (uint64_t k = 0; k < fields[f].vlen; k++) field_value_push(&o, rbytes[fields[f].vbeg + k]);
+        close_field(&o, rec_out, (int)f, fields[f].start);
+      }
   } else if (n > 0 && tag != T_RD) {            /* unterminated last record */
     PUSH_FIELD();
     CLOSE_RECORD(n);
@@ -532,6 +541,68 @@ int or_csv_parse(const uint8_t* in, uint64_t n, uint8_t fd, uint8_t rd, uint8_t 
                  const uint64_t* chars_capacity, or_status* st) {
   return or_csv_parse_ex(in, n, fd, rd, q, crlf, n_cols, col_types, NULL, 0, NULL, 0,
                          out_offsets, out_chars, out_typed, records_capacity, chars_capacity, st);
+}
+
+/* Numeric type inference (ParPaRaw Section 4, "Type inference"): the
+ * smallest type that backs a field's value, in the order int8 < int32 <
+ * int64 < float64 < string (codes 1..5; 0: an empty field, which constrains
+ * nothing).  An integer beyond int64 is backed by float64. */
+static int field_type(const uint8_t* v, size_t n) {
+  if (n == 0) return 0;
+  int64_t x;
+  int rc = conv_int(v, n, -128, 127, &x);
+  if (rc == 0) return 1;
+  if (rc == E_NUM_OVERFLOW) {
+    if (conv_int(v, n, INT32_MIN, INT32_MAX, &x) == 0) return 2;
+    if (conv_int(v, n, INT64_MIN, INT64_MAX, &x) == 0) return 3;
+    return 4;
+  }
+  double d;
+  if (conv_f64(v, n, &d) == 0) return 4;
+  return 5;
+}
+
+/* Per column c < n_cols, the largest field_type over the input's records
+ * (fields past n_cols are ignored, a missing field is empty); a column
+ * whose fields are all empty gets int8.  out[c] holds the library's column
+ * codes: 1 int8, 2 int32, 3 int64, 4 float64, 0 string. */
+void or_infer_types(const uint8_t* in, uint64_t n, uint8_t fd, uint8_t rd, uint8_t q, int crlf,
+                    int n_cols, int32_t* out, or_status* st) {
+  memset(st, 0, sizeof *st);
+  st->first_error_offset = UINT64_MAX;
+  int best[64];
+  for (int c = 0; c < n_cols; c++) best[c] = 0;
+  csv_syms y = syms_of(crlf ? 2 : 0, fd, rd, q);
+  uint8_t* val = NULL;
+  size_t len = 0, cap = 0;
+  int s = EOR, tag = T_RD, col = 0;
+  uint64_t rec = 0;
+  for (uint64_t i = 0; i <= n; i++) {
+    const int end = i == n;
+    if (!end) {
+      s = csv_step(&y, s, in[i], &tag);
+      if (tag == T_DATA) {
+        if (len == cap) { cap = cap ? 2 * cap : 256; val = (uint8_t*)realloc(val, cap); }
+        val[len++] = in[i];
+        continue;
+      }
+      if (tag == T_CTRL) continue;
+      if (tag != T_FD && tag != T_RD) { flag(st, E_INVALID_INPUT, i, 1); continue; }
+    } else if (s == INV || !csv_accepting(s) || n == 0 || tag == T_RD) {
+      if (s != INV && !csv_accepting(s)) flag(st, E_BAD_END_STATE, n, 1);
+      break;
+    }
+    if (col < n_cols) {
+      const int t = field_type(val, len);
+      if (t > best[col]) best[col] = t;
+    }
+    len = 0;
+    if (end || tag == T_RD) { rec++; col = 0; } else col++;
+  }
+  static const int32_t code[6] = {1, 1, 2, 3, 4, 0};
+  for (int c = 0; c < n_cols; c++) out[c] = code[best[c]];
+  st->n_records = rec;
+  free(val);
 }
 
 /* Rows are lines: the bytes up to and including each record-delimiter byte

@@ -33,7 +33,7 @@ def test_exports_every_declared_symbol():
 
 def test_struct_sizes():
     assert ctypes.sizeof(pp.DfaDesc) == 8 + 256 + 256 + 256 + 16 + 256
-    assert pp.STATUS_BYTES == 32 + 8 * 64
+    assert pp.STATUS_BYTES == 32 + 8 * 64 + 8  # + n_dropped
 
 
 def _reach(kind):

@@ -157,3 +157,49 @@ def test_skip_rows_matches_line_filter(seed):
     cols, st = O.csv_parse(data, ["str"] * 3, skip_rows_=skip)
     ref_cols, ref_st = O.csv_parse(want, ["str"] * 3)
     assert st == ref_st
+
+
+# ------------------------------------------------------------ type inference
+@pytest.mark.parametrize("text,want", [
+    (b"0", "i8"), (b"127", "i8"), (b"-128", "i8"), (b"+5", "i8"),
+    (b"128", "i32"), (b"-129", "i32"), (b"2147483647", "i32"), (b"-2147483648", "i32"),
+    (b"2147483648", "i64"), (b"-2147483649", "i64"), (b"9223372036854775807", "i64"),
+    (b"-9223372036854775808", "i64"),
+    (b"9223372036854775808", "f64"), (b"-9223372036854775809", "f64"),
+    (b"1.0", "f64"), (b".5", "f64"), (b"7.", "f64"), (b"1e5", "f64"), (b"-2.5E-3", "f64"),
+    (b"abc", "str"), (b"1,5", None), (b"1.2.3", "str"), (b"--1", "str"), (b"1e", "str"),
+    (b"0x10", "str"), (b"inf", "str"), (b"", "i8"), (b'"12"', "i8"), (b'"1""2"', "str"),
+])
+def test_infer_single_values(text, want):
+    """The smallest type backing one value (ParPaRaw Section 4, "Type
+    inference"): integer ranges at their exact edges, the float grammar,
+    quoted values read without their quotes."""
+    if want is None:  # a field delimiter: two one-digit columns
+        assert O.infer_types(text + b"\n", 2)[0] == ["i8", "i8"]
+        return
+    types, st = O.infer_types(text + b"\n", 1)
+    assert st["error"] == 0 and types == [want]
+
+
+def test_infer_takes_the_largest_per_column():
+    data = b"1,2.5,x,,\n-200,3,,\n99999999999,1e5,\"\"\n"
+    types, st = O.infer_types(data, 5)
+    assert types == ["i64", "f64", "str", "i8", "i8"] and st["n_records"] == 3
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_infer_of_concatenation_is_the_maximum(seed):
+    """Inference is a reduction with the maximum over a total order: the
+    type of a column over two inputs is the larger of the two types."""
+    rng = random.Random(300 + seed)
+    order = ["i8", "i32", "i64", "f64", "str"]
+    pool = [b"1", b"-7", b"300", b"-40000", b"5000000000", b"2.5", b"1e9", b"", b"ab", b'"9"']
+
+    def part():
+        return b"".join(b",".join(rng.choice(pool) for _ in range(3)) + b"\n"
+                        for _ in range(rng.randint(1, 20)))
+    a, b = part(), part()
+    ta, _ = O.infer_types(a, 3)
+    tb, _ = O.infer_types(b, 3)
+    tab, _ = O.infer_types(a + b, 3)
+    assert tab == [max(x, y, key=order.index) for x, y in zip(ta, tb)]
