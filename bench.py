@@ -259,7 +259,8 @@ def measure(pp, workload, args, dev, ws, clock_index):
     w = datagen.WORKLOADS[workload]
     h_in, info = _generate_pinned(workload, target=args.target)
     n = int(h_in.numel())
-    d_in = torch.empty(n + 16, dtype=torch.uint8, device=dev)[:n]
+    off = getattr(args, "in_offset", 0)  # bytes past a 256-byte aligned allocation
+    d_in = torch.empty(n + 16 + off, dtype=torch.uint8, device=dev)[off:off + n]
     d_in.copy_(h_in)
     stream = torch.cuda.current_stream(dev)
     csv = w["kind"] == "csv"
@@ -273,7 +274,9 @@ def measure(pp, workload, args, dev, ws, clock_index):
 
         def step():
             out.run(d_in, n, desc, stream)
-        launches_per_step = 4  # init, tile vectors, tile states, tile pass
+        # init, tile vectors, tile states, tile pass, and with numeric columns
+        # the long-field pass
+        launches_per_step = 4 + (1 if any(t in ("i8", "i32", "i64", "f64") for t in w["cols"]) else 0)
     else:
         desc = pp.desc_json_lexer()
         T = info["n_tokens"]
@@ -322,7 +325,8 @@ def measure(pp, workload, args, dev, ws, clock_index):
     path_s = float(np.mean(step_ms)) / 1e3
     st_ms = pp.debug_stage_ms(args.steps)
     pp.debug_stage_timing(0)
-    names = (["init", "tile_stv_kernel", "tile_state_kernel", "parse_kernel", "-", "-"] if csv else
+    names = (["init", "tile_stv_kernel", "tile_state_kernel", "parse_kernel", "long_field_kernel",
+              "-"] if csv else
              ["init", "tok_stv_kernel", "tok_state_scan_kernel", "tok_count_kernel",
               "tok_count_scan_kernel", "tok_emit_kernel"])
     stages = {k: float(st_ms[:, i].mean()) for i, k in enumerate(names) if k != "-"}
@@ -369,7 +373,8 @@ def measure(pp, workload, args, dev, ws, clock_index):
                    "n_tokens": info["n_tokens"] if not csv else None,
                    "columns": w["cols"], "output_bytes": out_bytes,
                    "l2": "input (and output) larger than the 129 MB L2; no flush",
-                   "parallelism": "replicas" if ws > 1 else "single GPU"},
+                   "parallelism": "replicas" if ws > 1 else "single GPU",
+                   "input_offset": off},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": peak_src,
@@ -447,6 +452,9 @@ def main():
                     help="input byte target (default: the workload's size); smaller "
                          "values give the small case used for ncu captures")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--in-offset", type=int, default=0,
+                    help="place the device input this many bytes past an aligned "
+                         "allocation (0-15: times the unaligned-input path)")
     ap.add_argument("--no-others", action="store_true",
                     help="time the headline workload only (not the second 2 GiB workload)")
     args = ap.parse_args()

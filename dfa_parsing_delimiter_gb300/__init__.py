@@ -117,6 +117,8 @@ def lib() -> ctypes.CDLL:
         L.pp_debug_stage_timing.argtypes = [ctypes.c_int]
         L.pp_debug_stage_ms.restype = ctypes.c_int
         L.pp_debug_stage_ms.argtypes = [_vp, ctypes.c_int]
+        L.pp_debug_long_fields.restype = ctypes.c_int
+        L.pp_debug_long_fields.argtypes = [ctypes.POINTER(ctypes.c_uint64), ctypes.c_int]
         _lib = L
     return _lib
 
@@ -175,7 +177,7 @@ def debug_stage_timing(n_calls: int) -> None:
 
 def debug_stage_ms(max_calls: int):
     """Per-call kernel durations (ms) recorded since debug_stage_timing, one
-    row of STAGES per call: pp_parse (init, tile vectors, tile states, context, scan, main),
+    row of STAGES per call: pp_parse (init, tile vectors, tile states, tile pass, long fields),
     pp_tokenize (init, stv, state scan, count, count scan, emit)."""
     import numpy as np
     out = np.zeros((max(int(max_calls), 1), STAGES), dtype=np.float32)
@@ -183,6 +185,14 @@ def debug_stage_ms(max_calls: int):
     if n < 0:
         raise RuntimeError("pp_debug_stage_ms failed")
     return out[:n]
+
+
+def debug_long_fields(reset: bool = False) -> int:
+    """Numeric fields converted by the long-field pass (a warp per field)
+    on the current device since the last reset; reset=True zeroes it."""
+    v = ctypes.c_uint64(0)
+    _check(lib().pp_debug_long_fields(ctypes.byref(v), int(reset)), "pp_debug_long_fields")
+    return int(v.value)
 
 
 def new_status(device=None) -> torch.Tensor:

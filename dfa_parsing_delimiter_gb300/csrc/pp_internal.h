@@ -51,8 +51,16 @@ constexpr uint8_t COL_INFER = 7;  // internal column kind: type inference only
 //   c_*:  its look-back over the value bytes per string column: per tile a
 //         flag and ns-word aggregate / inclusive prefix (null without string
 //         columns).
+// A numeric field queued for conversion by a warp (long fields): output row,
+// input byte range, column | type << 8.
+struct LongField { uint64_t rec, start, end; uint32_t col, pad; };
+constexpr uint32_t LONG_CAP = 4096;  // queued fields per call, at most
+
 struct ParseScratch {
-  uint32_t* counters;       // [0] tile tickets, [2] column-count end flag, [3] tile-state scan tickets
+  uint32_t* counters;       // [0] tile tickets, [2] column-count end flag, [3] tile-state scan
+                            // tickets, [4] queued long fields
+  LongField* long_q;        // [long_cap] (null: no queue, every field converted by its lane)
+  uint32_t long_cap;
   uint32_t* tile_stv;       // [n_tiles]
   uint8_t* tile_state;      // [n_tiles]
   unsigned long long* tstate_words;  // [n_tstate_blocks]

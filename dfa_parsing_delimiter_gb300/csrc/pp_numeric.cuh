@@ -236,12 +236,12 @@ struct FloatAcc {
   int32_t d10 = 0;     // decimal exponent adjustment from digit positions
   int32_t ex = 0;      // explicit exponent magnitude (saturating)
   uint16_t nsig = 0;   // digits accumulated into mant
-  uint16_t ndig = 0;   // digits in int + frac parts
+  bool dig = false;    // a digit of the int or frac part seen
   uint8_t phase = 0;   // 0 start, 1 int, 2 frac, 3 'e' seen, 4 exp sign, 5 exp digits, 6 error
   bool neg = false, eneg = false;
 
   PP_MFN void digit(uint32_t d, bool frac) {
-    ++ndig;
+    dig = true;
     if (nsig == 0 && d == 0) { if (frac) --d10; return; }
     if (nsig < 19) { mant = mant * 10 + d; ++nsig; if (frac) --d10; return; }
     if (!frac) ++d10;
@@ -285,7 +285,7 @@ struct FloatAcc {
   // returns 0 or PP_ERR_NUM_SYNTAX; *bits gets the binary64 bits (0 on error)
   PP_MFN int finish(uint64_t* bits) const {
     *bits = 0;
-    if (phase == 6 || phase == 3 || phase == 4 || ndig == 0) return PP_ERR_NUM_SYNTAX;
+    if (phase == 6 || phase == 3 || phase == 4 || !dig) return PP_ERR_NUM_SYNTAX;
     const uint64_t mag = mant == 0 ? 0 : decimal_to_binary64(mant, d10 + (eneg ? -ex : ex));
     *bits = mag | (neg ? (1ull << 63) : 0);
     return 0;

@@ -36,6 +36,7 @@
 #include "pp_device.cuh"
 #include "pp_internal.h"
 #include "pp_numeric.cuh"
+#include "pp_stv16.cuh"
 
 namespace {
 using namespace ppd;
@@ -398,36 +399,50 @@ __global__ void __launch_bounds__(TV_NT) tile_stv_kernel(const __grid_constant__
   __syncthreads();
   const int lane = threadIdx.x & 31;
   const uint32_t* my_lut = lut_s + lane;
-  const bool aligned = (reinterpret_cast<uintptr_t>(P.in) & 15) == 0;
+  // A lane's bytes split into a head up to the first 16-byte boundary, whole
+  // 16-byte blocks and a tail; with the input 16-byte aligned there is no
+  // head or tail.  The split is the same for every lane (lanes start at
+  // multiples of TV_BYTES).
+  const uint32_t h = uint32_t(16u - (reinterpret_cast<uintptr_t>(P.in) & 15u)) & 15u;
+  const uint32_t nb = (TV_BYTES - h) >> 4;          // TV_BYTES / 16, or one less
+  const uint32_t tl = TV_BYTES - h - 16u * nb;      // 0, or 16 - h
   const uint32_t warps = gridDim.x * (TV_NT / 32);
+  auto fold16 = [&](uint32_t G, const uint4 v) {
+    const uint32_t wq[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 15; j >= 0; --j)
+      G = __byte_perm(G, STV_INV_POOL, my_lut[((wq[j >> 2] >> (8 * (j & 3))) & 0xFFu) << 5]);
+    return G;
+  };
   for (uint32_t tile = blockIdx.x * (TV_NT / 32) + (threadIdx.x >> 5); tile < P.n_tiles;
        tile += warps) {
     const uint64_t b0 = uint64_t(tile) * TILE + uint64_t(lane) * TV_BYTES;
     const uint32_t len = b0 < P.n ? uint32_t(min(uint64_t(TV_BYTES), P.n - b0)) : 0u;
     uint32_t G = STV_ID;
-    if (len == TV_BYTES && aligned) {
-      // back to front in steps of 64 bytes, the next step's loads in flight
-      // while the current one folds
-      constexpr int STEPS = TV_BYTES / 64;
-      const uint4* src = reinterpret_cast<const uint4*>(P.in + b0);
+    if (len == TV_BYTES) {
+      const uint8_t* p = P.in + b0;
+      for (int j = int(tl) - 1; j >= 0; --j)  // the tail
+        G = __byte_perm(G, STV_INV_POOL, my_lut[uint32_t(__ldg(p + h + 16u * nb + j)) << 5]);
+      const uint4* src = reinterpret_cast<const uint4*>(p + h);
+      const uint32_t ng = nb >> 2;  // groups of four blocks; the rest first, back to front
+      for (int k = int(nb) - 1; k >= int(4 * ng); --k) G = fold16(G, __ldg(src + k));
+      // groups back to front, the next group's loads in flight while the
+      // current one folds
       uint4 cur[4], nxt[4] = {};
 #pragma unroll
-      for (int k = 0; k < 4; ++k) cur[k] = __ldg(src + 4 * (STEPS - 1) + k);
-      for (int step = STEPS - 1; step >= 0; --step) {
+      for (int k = 0; k < 4; ++k) cur[k] = __ldg(src + 4 * (ng - 1) + k);
+      for (int step = int(ng) - 1; step >= 0; --step) {
         if (step > 0) {
 #pragma unroll
           for (int k = 0; k < 4; ++k) nxt[k] = __ldg(src + 4 * (step - 1) + k);
         }
 #pragma unroll
-        for (int k = 3; k >= 0; --k) {
-          const uint32_t wq[4] = {cur[k].x, cur[k].y, cur[k].z, cur[k].w};
-#pragma unroll
-          for (int j = 15; j >= 0; --j)
-            G = __byte_perm(G, STV_INV_POOL, my_lut[((wq[j >> 2] >> (8 * (j & 3))) & 0xFFu) << 5]);
-        }
+        for (int k = 3; k >= 0; --k) G = fold16(G, cur[k]);
 #pragma unroll
         for (int k = 0; k < 4; ++k) cur[k] = nxt[k];
       }
+      for (int j = int(h) - 1; j >= 0; --j)  // the head
+        G = __byte_perm(G, STV_INV_POOL, my_lut[uint32_t(__ldg(p + j)) << 5]);
     } else {
       for (int j = int(len) - 1; j >= 0; --j)
         G = __byte_perm(G, STV_INV_POOL, my_lut[uint32_t(__ldg(P.in + b0 + j)) << 5]);
@@ -651,6 +666,275 @@ __device__ __forceinline__ void convert_store(const ParseParams& P, const NumCtx
     const uint32_t fsr = v >> 16;
     report(P.st, err, fsr == 0xFFFFu ? X.tile_fstart : X.tile_base + fsr, true);
   }
+}
+
+// ------------------------------------------- long numeric fields (a warp)
+// Collaboration on long fields (ParPaRaw Section 3.3): a number field whose
+// bytes span more than LONG_NUM bytes is not converted by its lane in the
+// tile pass.  The lane queues it (up to LONG_CAP fields per call; fields
+// beyond that are converted by their lane), and long_field_kernel converts
+// each queued field with a whole warp, by the data-parallel method of the
+// parse itself:
+//  1. the warp takes the bytes from the start of the field's tile, whose DFA
+//     state the tile-state scan gave, to the field's end, in rounds of
+//     32 x LONG_SEG bytes, a segment per lane; a warp scan of the segments'
+//     transition vectors gives each segment its CSV state (Section 3.1), and
+//     with it which of its bytes are control bytes;
+//  2. the field's value bytes run through the number grammar as a second DFA
+//     (9 states), again by transition vectors and a warp scan, which gives
+//     each segment its grammar state; each lane then counts its integer- and
+//     fraction-part digits and finds its first non-zero digits;
+//  3. warp sums and minima combine the segments and rounds, and one lane
+//     reads at most 19 significant digits (and at most 7 of the exponent)
+//     and finishes the conversion.
+// The value is the one the per-lane conversion gives (the first 19
+// significant digits, the exponent saturated the same way).
+constexpr uint32_t LONG_NUM = 256;
+constexpr uint32_t LONG_SEG = 16;
+constexpr int LF_NT = 128;
+
+namespace numg {
+// Number grammar [+-]?([0-9]+(\.[0-9]*)?|\.[0-9]+)([eE][+-]?[0-9]+)?:
+// G0 start, G1 after the sign, G2 integer digits, G3 a point with no digit
+// before, G4 fraction (after at least one mantissa digit), G5 after the
+// exponent mark, G6 after its sign, G7 exponent digits, GX error.  Accepting:
+// G2, G4, G7 (integers: G2 alone).  Symbol classes: digit, sign, point,
+// exponent mark, other.  A vector holds the next state of every state, one
+// nibble per state (states 9-15 unused, mapped to themselves).
+constexpr uint32_t G0 = 0, G1 = 1, G2 = 2, G3 = 3, G4 = 4, G5 = 5, G6 = 6, G7 = 7, GX = 8;
+constexpr uint64_t vec9(uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t a4,
+                        uint32_t a5, uint32_t a6, uint32_t a7) {
+  const uint32_t a[9] = {a0, a1, a2, a3, a4, a5, a6, a7, GX};
+  uint64_t v = 0;
+  for (int s = 0; s < 16; ++s) v |= uint64_t(s < 9 ? a[s] : uint32_t(s)) << (4 * s);
+  return v;
+}
+constexpr uint64_t K_DIGIT = vec9(G2, G2, G2, G4, G4, G7, G7, G7);
+constexpr uint64_t K_SIGN = vec9(G1, GX, GX, GX, GX, G6, GX, GX);
+constexpr uint64_t K_POINT = vec9(G3, G3, G4, GX, GX, GX, GX, GX);
+constexpr uint64_t K_EXP = vec9(GX, GX, G5, GX, G5, GX, GX, GX);
+constexpr uint64_t K_OTHER = vec9(GX, GX, GX, GX, GX, GX, GX, GX);
+__device__ __forceinline__ uint32_t sym_class(uint32_t b) {
+  return b - '0' <= 9u ? 0u : (b == '+' || b == '-') ? 1u : b == '.' ? 2u
+                                                      : (b | 0x20u) == 'e' ? 3u : 4u;
+}
+__device__ __forceinline__ uint64_t class_vec(uint32_t c) {
+  return c == 0 ? K_DIGIT : c == 1 ? K_SIGN : c == 2 ? K_POINT : c == 3 ? K_EXP : K_OTHER;
+}
+}  // namespace numg
+
+// Byte b, whose DFA state before it is s, is a control byte; s advances past it.
+__device__ __forceinline__ bool step_ctrl(const uint32_t* lut, uint32_t b, uint32_t& s) {
+  const uint32_t e = lut[b];
+  const uint32_t tg = (e >> (20 + 2 * s)) & 3u;
+  s = (e >> (4 * s)) & 0xFu;
+  return tg == uint32_t(PP_TAG_CTRL);
+}
+__device__ __forceinline__ uint64_t warp_min64(uint64_t v) {
+#pragma unroll
+  for (int d = 16; d; d >>= 1) v = min(v, __shfl_xor_sync(FULL, v, d));
+  return v;
+}
+
+// Convert queued field f with the calling warp; lane 0 stores the value and
+// reports an error at the field's first byte.  lut: one entry per byte value.
+__device__ void convert_long(const ParseParams& P, const uint32_t* lut, const ppi::LongField f) {
+  using namespace numg;
+  constexpr uint64_t NONE = ~0ull;
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint32_t ty = f.col >> 8, col = f.col & 0xFFu;
+  const uint64_t gs = f.start, ge = f.end;
+  const uint64_t t0 = (gs / TILE) * TILE;  // the DFA state there is known
+  uint32_t cs = P.s.tile_state[gs / TILE];  // CSV state at the round start
+  uint32_t gq = G0;                         // grammar state at the round start
+  uint64_t n_int = 0, n_frac = 0, n_val = 0;
+  uint64_t z = NONE, pz = NONE, pez = NONE;  // first non-zero mantissa digit (index, position), exponent digit
+  uint32_t sz = 0, sez = 0;                   // CSV states before them
+  bool mneg = false, eneg = false;
+  for (uint64_t r0 = t0; r0 < ge; r0 += 32 * LONG_SEG) {
+    const uint64_t a = r0 + uint64_t(lane) * LONG_SEG;
+    const uint32_t len = a < ge ? uint32_t(min(uint64_t(LONG_SEG), ge - a)) : 0u;
+    uint32_t bw[LONG_SEG / 4] = {};  // the segment's bytes, four to a word
+#pragma unroll
+    for (uint32_t j = 0; j < LONG_SEG; ++j)
+      if (j < len) bw[j >> 2] |= uint32_t(__ldg(P.in + a + j)) << (8 * (j & 3));
+    // CSV states: a warp scan of the segments' transition vectors
+    uint32_t cv = STV_ID;
+#pragma unroll
+    for (int j = int(LONG_SEG) - 1; j >= 0; --j)
+      if (uint32_t(j) < len) cv = __byte_perm(cv, STV_INV_POOL, lut[(bw[j >> 2] >> (8 * (j & 3))) & 0xFFu]);
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const uint32_t o = __shfl_up_sync(FULL, cv, d);
+      if (int(lane) >= d) cv = stv_compose(o, cv);
+    }
+    uint32_t cx = __shfl_up_sync(FULL, cv, 1);
+    if (lane == 0) cx = STV_ID;
+    const uint32_t s_lane = stv_apply(cx, cs);
+    cs = stv_apply(__shfl_sync(FULL, cv, 31), cs);
+    uint32_t val_m = 0;  // bit j: byte j is a value byte of the field
+    {
+      uint32_t s = s_lane;
+#pragma unroll
+      for (uint32_t j = 0; j < LONG_SEG; ++j)
+        if (j < len && !step_ctrl(lut, (bw[j >> 2] >> (8 * (j & 3))) & 0xFFu, s) && a + j >= gs)
+          val_m |= 1u << j;
+    }
+    // grammar: the segment's transition vector (runs of digits compose once)
+    Stv16 gv = stv16_id();
+    {
+      uint32_t last = 5;
+#pragma unroll
+      for (uint32_t j = 0; j < LONG_SEG; ++j) {
+        if (!((val_m >> j) & 1u)) continue;
+        const uint32_t c = sym_class((bw[j >> 2] >> (8 * (j & 3))) & 0xFFu);
+        if (!(c == 0 && last == 0)) gv = stv16_compose(gv, stv16_unpack(class_vec(c)));
+        last = c;
+      }
+    }
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const Stv16 o = shfl_up16(gv, d);
+      if (int(lane) >= d) gv = stv16_compose(o, gv);
+    }
+    Stv16 gx = shfl_up16(gv, 1);
+    if (lane == 0) gx = stv16_id();
+    uint32_t g = stv16_apply(gx, gq);
+    gq = __shfl_sync(FULL, stv16_apply(gv, gq), 31);
+    // the segment's digits and signs, its states known
+    uint32_t ni = 0, nf = 0, zl = 0xFFFFFFFFu, pzl = 0, szl = 0, pel = 0xFFFFFFFFu, sel = 0;
+    bool mn = false, en = false;
+    {
+      uint32_t s = s_lane;
+#pragma unroll
+      for (uint32_t j = 0; j < LONG_SEG; ++j) {
+        if (j >= len) continue;
+        const uint32_t s_before = s;
+        const uint32_t b = (bw[j >> 2] >> (8 * (j & 3))) & 0xFFu;
+        step_ctrl(lut, b, s);
+        if (!((val_m >> j) & 1u)) continue;
+        const uint32_t c = sym_class(b);
+        const uint32_t ns = nib_apply(class_vec(c), g);
+        if (c == 0) {
+          if (ns == G2 || ns == G4) {
+            if (b != '0' && zl == 0xFFFFFFFFu) { zl = ni + nf; pzl = j; szl = s_before; }
+            if (ns == G2) ++ni; else ++nf;
+          } else if (ns == G7 && b != '0' && pel == 0xFFFFFFFFu) {
+            pel = j; sel = s_before;
+          }
+        } else if (c == 1 && b == '-') {
+          if (ns == G1) mn = true;
+          else if (ns == G6) en = true;
+        }
+        g = ns;
+      }
+    }
+    // combine the lanes: digit indexes, first non-zero digits, counts
+    uint32_t md = ni + nf;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const uint32_t o = __shfl_up_sync(FULL, md, d);
+      if (int(lane) >= d) md += o;
+    }
+    const uint32_t md_before = md - (ni + nf);
+    if (z == NONE) {
+      const uint64_t cand = zl != 0xFFFFFFFFu ? n_int + n_frac + md_before + zl : NONE;
+      const uint64_t m = warp_min64(cand);
+      if (m != NONE) {
+        const uint32_t src = __ffs(__ballot_sync(FULL, cand == m)) - 1;
+        z = m;
+        pz = __shfl_sync(FULL, a + pzl, src);
+        sz = __shfl_sync(FULL, szl, src);
+      }
+    }
+    if (pez == NONE) {
+      const uint64_t cand = pel != 0xFFFFFFFFu ? a + pel : NONE;
+      const uint64_t m = warp_min64(cand);
+      if (m != NONE) {
+        const uint32_t src = __ffs(__ballot_sync(FULL, cand == m)) - 1;
+        pez = m;
+        sez = __shfl_sync(FULL, sel, src);
+      }
+    }
+    n_int += __reduce_add_sync(FULL, ni);
+    n_frac += __reduce_add_sync(FULL, nf);
+    n_val += __reduce_add_sync(FULL, uint32_t(__popc(val_m)));
+    mneg |= __any_sync(FULL, mn);
+    eneg |= __any_sync(FULL, en);
+  }
+  if (lane != 0) return;
+  uint64_t val = P.defval[col];
+  int err = 0;
+  if (n_val) {
+    const bool accept = ty == PP_COL_FLOAT64 ? (gq == G2 || gq == G4 || gq == G7) : gq == G2;
+    const uint64_t L = n_int + n_frac;
+    val = 0;
+    if (!accept) {
+      err = PP_ERR_NUM_SYNTAX;
+    } else if (ty != PP_COL_FLOAT64 && z != NONE && L - z > 19) {
+      err = PP_ERR_NUM_OVERFLOW;  // 20 or more significant digits
+    } else {
+      // the significant digits, at most 19, from the first non-zero one
+      uint64_t m = 0;
+      if (z != NONE) {
+        const uint64_t want = min(L - z, uint64_t(19));
+        uint64_t got = 0;
+        uint32_t s = sz;
+        for (uint64_t p = pz; p < ge && got < want; ++p) {
+          const uint32_t b = __ldg(P.in + p);
+          if (step_ctrl(lut, b, s)) continue;
+          if (b - '0' <= 9u) { m = m * 10 + (b - '0'); ++got; }
+        }
+      }
+      if (ty == PP_COL_FLOAT64) {
+        uint64_t mag = 0;
+        if (z != NONE) {
+          // the exponent: at most 7 significant digits, saturated above 100000
+          int64_t ex = 0;
+          if (pez != NONE) {
+            uint32_t s = sez;
+            for (uint64_t p = pez; p < ge && ex <= 100000; ++p) {
+              const uint32_t b = __ldg(P.in + p);
+              if (step_ctrl(lut, b, s)) continue;
+              ex = ex * 10 + int64_t(b - '0');
+            }
+          }
+          const uint64_t q = min(z + 19, L);
+          const int64_t d10 = -int64_t(q > n_int ? q - n_int : 0) +
+                              int64_t(n_int > z + 19 ? n_int - z - 19 : 0);
+          int64_t e10 = d10 + (eneg ? -ex : ex);
+          e10 = max(int64_t(-0x40000000), min(int64_t(0x40000000), e10));
+          mag = ppn::decimal_to_binary64(m, int(e10));
+        }
+        val = mag | (mneg ? (1ull << 63) : 0ull);
+      } else {
+        const uint64_t lim = ty == PP_COL_INT8 ? 127ull : ty == PP_COL_INT32 ? 2147483647ull
+                                                                             : 9223372036854775807ull;
+        if (m > lim + (mneg ? 1u : 0u)) err = PP_ERR_NUM_OVERFLOW;
+        else val = mneg ? ~m + 1 : m;
+      }
+    }
+  }
+  void* const out = P.typed[col];
+  if (ty == PP_COL_INT32) static_cast<int32_t*>(out)[f.rec] = int32_t(val);
+  else if (ty == PP_COL_INT8) static_cast<int8_t*>(out)[f.rec] = int8_t(val);
+  else static_cast<uint64_t*>(out)[f.rec] = val;
+  if (err) report(P.st, err, gs, true);
+}
+
+// Fields converted by long_field_kernel on this device (a test hook's count).
+__device__ unsigned long long g_long_fields;
+
+// The queued long fields, a warp each.
+__global__ void __launch_bounds__(LF_NT) long_field_kernel(const __grid_constant__ ParseParams P) {
+  __shared__ uint32_t lut[256];
+  for (int k = threadIdx.x; k < 256; k += LF_NT) lut[k] = P.lut[k];
+  __syncthreads();
+  const uint32_t n = min(P.s.counters[4], P.s.long_cap);
+  if (blockIdx.x == 0 && threadIdx.x == 0 && n) atomicAdd(&g_long_fields, n);
+  const uint32_t warps = gridDim.x * (LF_NT / 32);
+  for (uint32_t q = blockIdx.x * (LF_NT / 32) + (threadIdx.x >> 5); q < n; q += warps)
+    convert_long(P, lut, P.s.long_q[q]);
 }
 
 // ------------------------------------------------------ type inference
@@ -1680,9 +1964,24 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
           }
           if (rec >= P.rec_cap) { report(P.st, PP_ERR_CAPACITY, 0, false); continue; }
           const uint32_t v = slot_s[c * nrp + (r - lo)];
+          const uint32_t ty = S.coltype[c];
+          if ((v >> 16) == REL_START || (v & 0xFFFFu) - (v >> 16) > LONG_NUM) {
+            // a long field goes to a warp (the queue permitting)
+            const uint32_t fsr = v >> 16, fe = v & 0xFFFFu;
+            const uint64_t span = fsr == REL_START ? X.tile_base + fe - X.tile_fstart : fe - fsr;
+            if (v != SLOT_DEFAULT && span > LONG_NUM && ty != PP_COL_TIMESTAMP &&
+                ty != ppi::COL_INFER && P.s.long_q) {
+              const uint32_t q = atomicAdd(&P.s.counters[4], 1u);
+              if (q < P.s.long_cap) {
+                P.s.long_q[q] = ppi::LongField{rec, fsr == REL_START ? X.tile_fstart : X.tile_base + fsr,
+                                               X.tile_base + fe, c | (ty << 8)};
+                continue;
+              }
+            }
+          }
           void* const out = P.typed[c];
           const uint64_t dflt = P.defval[c];
-          switch (S.coltype[c]) {
+          switch (ty) {
             case PP_COL_FLOAT64: convert_store<PP_COL_FLOAT64>(P, X, out, rec, v, dflt); break;
             case PP_COL_INT64: convert_store<PP_COL_INT64>(P, X, out, rec, v, dflt); break;
             case PP_COL_TIMESTAMP: convert_store<PP_COL_TIMESTAMP>(P, X, out, rec, v, dflt); break;
@@ -1948,7 +2247,7 @@ __global__ void parse_init_kernel(ParseParams P) {
   if (s.c_flag)
     for (uint32_t i = i0; i < P.n_tiles; i += stride) s.c_flag[i] = 0;
   for (uint32_t i = i0; i < s.n_tstate_blocks; i += stride) s.tstate_words[i] = 0;
-  if (i0 < 4) s.counters[i0] = 0;
+  if (i0 < 5) s.counters[i0] = 0;
   if (i0 == 0) {
     pp_status* st = P.st;
     st->error = 0;
@@ -2022,6 +2321,16 @@ cudaError_t launch_ns(const ParseParams& p, cudaStream_t stream) {
                                                  uint64_t(occ.n_sm) * occ.blocks));
   if (p.n_tiles) parse_kernel<NS><<<g, ntf_of<NS>(), PARSE_SMEM, stream>>>(p);
   if (timed) ppi::stage_mark(4, stream);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // the long numeric fields the tile pass queued (an empty queue costs a
+  // launch that returns at once)
+  bool any_num = false;
+  for (int c = 0; c < p.n_cols; ++c)
+    any_num |= p.coltype[c] == PP_COL_INT8 || p.coltype[c] == PP_COL_INT32 ||
+               p.coltype[c] == PP_COL_INT64 || p.coltype[c] == PP_COL_FLOAT64;
+  if (p.n_tiles && p.has_out && any_num && p.s.long_q)
+    long_field_kernel<<<std::max(1, occ.n_sm), LF_NT, 0, stream>>>(p);
+  if (timed) ppi::stage_mark(5, stream);
   return cudaGetLastError();
 }
 
@@ -2105,11 +2414,17 @@ int parse_ns_width(int n_str) {
 // layout: counters | tile vectors | tile states | tile-state look-back words |
 // context look-back descriptors (16 bytes a tile) | chars look-back (flags,
 // aggregates, inclusive prefixes: ns words a tile)
+// Long numeric fields queued per call: a tile starts at most TILE / LONG_NUM
+// of them, plus the one open at its start.
+uint32_t long_cap(uint32_t n) {
+  return uint32_t(std::min<uint64_t>(ppi::LONG_CAP, uint64_t(n) * (TILE / LONG_NUM + 1)));
+}
+
 size_t parse_scratch_bytes(uint32_t n, int ns) {
   const uint32_t nt = (n + TS_TILES - 1) / TS_TILES;
   const int k3 = ns > 0 ? ns : 1;
   return 256 + align256(size_t(n) * 4) + align256(n) + align256(size_t(nt) * 8) +
-         align256(size_t(n) * 16) +
+         align256(size_t(n) * 16) + align256(size_t(long_cap(n)) * sizeof(ppi::LongField)) +
          (ns > 0 ? align256(size_t(n) * 4) + 2 * align256(size_t(n) * k3 * 8) : 0);
 }
 
@@ -2124,6 +2439,9 @@ void parse_scratch_carve(void* base, uint32_t n, int ns, ParseScratch* o) {
   o->tstate_words = reinterpret_cast<unsigned long long*>(p);
   p += align256(size_t(o->n_tstate_blocks) * 8);
   o->v2_desc = reinterpret_cast<uint64_t*>(p); p += align256(size_t(n) * 16);
+  o->long_cap = long_cap(n);
+  o->long_q = reinterpret_cast<ppi::LongField*>(p);
+  p += align256(size_t(o->long_cap) * sizeof(ppi::LongField));
   if (ns > 0) {
     o->c_flag = reinterpret_cast<uint32_t*>(p); p += align256(size_t(n) * 4);
     o->c_agg = reinterpret_cast<uint64_t*>(p); p += align256(size_t(n) * k3 * 8);
@@ -2141,3 +2459,14 @@ cudaError_t launch_parse(const ParseParams& p, cudaStream_t stream) {
 }
 
 }  // namespace ppi
+
+extern "C" pp_rc pp_debug_long_fields(uint64_t* out, int reset) {
+  unsigned long long v = 0;
+  if (out && cudaMemcpyFromSymbol(&v, g_long_fields, sizeof(v)) != cudaSuccess) return PP_ECUDA;
+  if (out) *out = v;
+  if (reset) {
+    v = 0;
+    if (cudaMemcpyToSymbol(g_long_fields, &v, sizeof(v)) != cudaSuccess) return PP_ECUDA;
+  }
+  return PP_OK;
+}

@@ -82,15 +82,43 @@ struct TokParams {
 };
 
 // ------------------------------------------------------------ input
-// The lane's 64 bytes as 16 little-endian words (zero past clen).
+// 16 words of r from word WS on, shifted right by sh bits (0, 8, 16, 24).
+template <int WS>
+__device__ __forceinline__ void shift_words(const uint32_t (&r)[20], uint32_t sh,
+                                            uint32_t (&w)[16]) {
+#pragma unroll
+  for (int q = 0; q < 16; ++q) w[q] = __funnelshift_r(r[WS + q], r[WS + q + 1], sh);
+}
+// The lane's 64 bytes as 16 little-endian words (zero past clen).  A full
+// chunk is read with 16-byte loads: four of them on a 16-byte aligned input;
+// otherwise five aligned loads around the chunk, shifted into place, as long
+// as they stay inside the input (every chunk but the input's first and
+// last).  The misalignment is the same for every chunk (chunks start at
+// multiples of 64).
 __device__ __forceinline__ void load_chunk(const TokParams& P, uint64_t c0, uint32_t clen,
                                            uint32_t (&w)[16]) {
+  const uint32_t m = uint32_t(reinterpret_cast<uintptr_t>(P.in) & 15u);
   if (clen == CB && P.aligned) {
     const uint4* src = reinterpret_cast<const uint4*>(P.in + c0);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const uint4 v = __ldg(src + q);
       w[4 * q] = v.x; w[4 * q + 1] = v.y; w[4 * q + 2] = v.z; w[4 * q + 3] = v.w;
+    }
+  } else if (clen == CB && c0 >= 16 && c0 + CB + 16 <= P.n) {
+    const uint4* src = reinterpret_cast<const uint4*>(P.in + c0 - m);
+    uint32_t r[20];
+#pragma unroll
+    for (int q = 0; q < 5; ++q) {
+      const uint4 v = __ldg(src + q);
+      r[4 * q] = v.x; r[4 * q + 1] = v.y; r[4 * q + 2] = v.z; r[4 * q + 3] = v.w;
+    }
+    const uint32_t sh = (m & 3u) * 8u;
+    switch (m >> 2) {
+      case 0: shift_words<0>(r, sh, w); break;
+      case 1: shift_words<1>(r, sh, w); break;
+      case 2: shift_words<2>(r, sh, w); break;
+      default: shift_words<3>(r, sh, w); break;
     }
   } else {
 #pragma unroll

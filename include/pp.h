@@ -430,7 +430,10 @@ pp_rc pp_desc_csv_crlf(pp_dfa_desc* out, uint8_t fd, uint8_t quote);
  * pp_tokenize (whitespace runs, punctuation {}[],:, strings with backslash
  * escapes, integers, fractions and exponents).  Token ids: '{'0 '}'1 '['2
  * ']'3 ','4 ':'5 string 6 integer 7 float 8 whitespace 9, 255 invalid.
- * Host only.
+ * Host only.  Source: "Lexing on the GPU: the scan is the easy part",
+ * section "A lexer is a prefix scan" (a lexer as one DFA whose transitions
+ * mark token starts); the state table is this library's own, since the page
+ * gives the scheme and not a table.
  */
 pp_rc pp_desc_json_lexer(pp_dfa_desc* out);
 
@@ -463,12 +466,18 @@ pp_rc pp_debug_stage_timing(int n_calls);
 /* Kernel durations of the recorded calls: out[PP_STAGES*i + k] =
  * milliseconds of kernel k of call i.  pp_parse: 0 init, 1 tile transition
  * vectors, 2 tile start states, 3 tile pass (tagging, indices, columns and
- * conversion).  pp_tokenize: 0 init, 1 transition vectors, 2 state scan,
+ * conversion), 4 long numeric fields (a warp per queued field).  pp_tokenize: 0 init, 1 transition vectors, 2 state scan,
  * 3 count pass, 4 count scan, 5 emit pass.  Entries a call does not use
  * are 0.  Waits for the events.  Returns the number of calls written (at
  * most max_calls), or -1 on a CUDA error. */
 #define PP_STAGES 6
 int pp_debug_stage_ms(float* out, int max_calls);
+
+/* Test hook: *out (if not NULL) = the number of numeric fields converted by
+ * the long-field pass (a warp per field longer than 256 bytes) on the
+ * current device since the last reset; reset != 0 then sets it to 0.
+ * Synchronous (waits for the device).  Returns PP_ECUDA on a CUDA error. */
+pp_rc pp_debug_long_fields(uint64_t* out, int reset);
 
 #ifdef __cplusplus
 }

@@ -239,9 +239,13 @@ def test_parse_capacity_too_small():
     data, info, _ = datagen.generate("csv18_2gib", target=2 * TILE)
     cols = datagen.WORKLOADS["csv18_2gib"]["cols"]
     out, st = run_gpu_csv(data, cols, records_capacity=info["n_records"] - 3)
-    assert st["error"] & pp.ERR_CAPACITY
+    _, ost = O.csv_parse(data, cols, records_capacity=info["n_records"] - 3)
+    assert ost["error"] == O.E_CAPACITY
+    assert st["error"] == ost["error"] and st["n_records"] == ost["n_records"]
     out, st = run_gpu_csv(data, cols, chars_capacity=[100] * len(cols))
-    assert st["error"] & pp.ERR_CAPACITY
+    _, ost = O.csv_parse(data, cols, chars_capacity=[100] * len(cols))
+    assert ost["error"] == O.E_CAPACITY
+    assert st["error"] == ost["error"] and st["n_records"] == ost["n_records"]
 
 
 def test_parse_sizing_pass():
