@@ -293,10 +293,11 @@ pp_rc pp_tokenize_host(const uint8_t* h_in, size_t n_bytes, const pp_dfa_desc* d
  *   Arguments, semantics, outputs and d_status: exactly those of pp_parse.
  *   Limit: the scratch needed is about 22 bytes per 16 KiB tile of input
  *   without string columns and 4 + 16 x w bytes more with them, w being the
- *   string-column count rounded up to 4, 8 or 16; 4 MiB therefore holds
- *   inputs up to about 3 GiB without string columns, 730 MiB with 1 to 4,
- *   420 MiB with 5 to 8 and 230 MiB with 9 to 16 string columns.  A larger
- *   input returns PP_ETOOLARGE before any CUDA call.
+ *   string-column count rounded up to 4, 8 or 16, plus up to 128 KiB for
+ *   the queue of long numeric fields; 4 MiB therefore holds inputs up to
+ *   about 2.9 GiB without string columns, 710 MiB with 1 to 4, 410 MiB with
+ *   5 to 8 and 225 MiB with 9 to 16 string columns.  A larger input returns
+ *   PP_ETOOLARGE before any CUDA call.
  *   First call on each device: it looks up the buffer's address
  *   (cudaGetSymbolAddress; this can load the library's device code) and
  *   sets kernel attributes.  Make that first call before any stream

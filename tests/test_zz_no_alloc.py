@@ -104,7 +104,7 @@ def test_noalloc_sizing_pass_matches():
 
 
 def test_noalloc_rejects_input_larger_than_its_buffer():
-    # 64 columns, 16 of them strings: the buffer holds about 233 MiB of input
+    # 64 columns, 16 of them strings: the buffer holds about 225 MiB of input
     col_types = ["str"] * 16 + ["i32"] * 48
     n = 240 << 20
     d_in = torch.zeros(n, dtype=torch.uint8, device="cuda")
