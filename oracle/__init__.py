@@ -72,6 +72,9 @@ def _load():
         L.or_csv_parse_ex.argtypes = [_vp, _u64, _u8, _u8, _u8, ctypes.c_int, ctypes.c_int, _vp,
                                       _vp, ctypes.c_int, _vp, _u64, _vp, _vp, _vp, _u64, _vp,
                                       ctypes.POINTER(Status)]
+        L.or_csv_parse_enc.argtypes = [_vp, _u64, ctypes.c_int, ctypes.c_uint32, ctypes.c_uint32,
+                                       ctypes.c_uint32, ctypes.c_int, _vp, _vp, ctypes.c_int, _vp,
+                                       _u64, _vp, _vp, _vp, _u64, _vp, ctypes.POINTER(Status)]
         L.or_skip_rows.argtypes = [_vp, _u64, _u8, _vp, _u64, _vp]
         L.or_infer_types.argtypes = [_vp, _u64, _u8, _u8, _u8, ctypes.c_int, ctypes.c_int, _vp,
                                      ctypes.POINTER(Status)]
@@ -109,11 +112,22 @@ def skip_rows(data, rows, rd=b"\n"):
     return out[:w]
 
 
+ENCODINGS = {"utf-8": 1, "utf-16-le": 2}
+
+
+def _cp(x):
+    return x if isinstance(x, int) else ord(x.decode() if isinstance(x, bytes) else x)
+
+
 def csv_parse(data, col_types, fd=b",", rd=b"\n", quote=b'"', records_capacity=None,
               chars_capacity=None, crlf=False, defaults=None, reject=False,
-              skip_records=None, skip_rows_=None):
+              skip_records=None, skip_rows_=None, encoding=None):
     """Sequentially parse quoted CSV (crlf: carriage returns outside quotes
     are dropped, so CRLF line ends work with rd = LF).
+
+    With `encoding` ("utf-8" or "utf-16-le", ParPaRaw Section 3.4) the DFA
+    reads symbols of that encoding and fd, rd and quote are characters (or
+    code points); values keep all bytes of their symbols.
 
     Options (ParPaRaw Section 4): `defaults` (n_cols integer bit patterns)
     are stored for empty or missing numeric fields instead of 0; with
@@ -132,7 +146,7 @@ def csv_parse(data, col_types, fd=b",", rd=b"\n", quote=b'"', records_capacity=N
     n = a.size
     ncols = len(col_types)
     if records_capacity is None:
-        records_capacity = int(np.count_nonzero(a == rd[0])) + 1
+        records_capacity = (n + 1) if encoding else int(np.count_nonzero(a == rd[0])) + 1
     if chars_capacity is None:
         chars_capacity = [n] * ncols
     offs, chars, typed = [], [], []
@@ -157,12 +171,16 @@ def csv_parse(data, col_types, fd=b",", rd=b"\n", quote=b'"', records_capacity=N
     dflt = None if defaults is None else np.ascontiguousarray(
         [int(x) & 0xFFFFFFFFFFFFFFFF for x in defaults], dtype=np.uint64)
     skr = np.ascontiguousarray(sorted(set(int(x) for x in (skip_records or []))), dtype=np.uint64)
-    L.or_csv_parse_ex(a.ctypes.data, n, fd[0], rd[0], quote[0], int(bool(crlf)), ncols,
-                      codes.ctypes.data, dflt.ctypes.data if dflt is not None else None,
-                      int(bool(reject)), skr.ctypes.data if skr.size else None, skr.size,
-                      ctypes.addressof(ptr_off), ctypes.addressof(ptr_chr),
-                      ctypes.addressof(ptr_typ), records_capacity, ccap.ctypes.data,
-                      ctypes.byref(st))
+    common = (ncols, codes.ctypes.data, dflt.ctypes.data if dflt is not None else None,
+              int(bool(reject)), skr.ctypes.data if skr.size else None, skr.size,
+              ctypes.addressof(ptr_off), ctypes.addressof(ptr_chr), ctypes.addressof(ptr_typ),
+              records_capacity, ccap.ctypes.data, ctypes.byref(st))
+    if encoding:
+        assert not crlf and skip_rows_ is None
+        L.or_csv_parse_enc(a.ctypes.data, n, ENCODINGS[encoding], _cp(fd), _cp(rd), _cp(quote),
+                           *common)
+    else:
+        L.or_csv_parse_ex(a.ctypes.data, n, fd[0], rd[0], quote[0], int(bool(crlf)), *common)
     R = min(int(st.n_records), records_capacity)
     cols = []
     for c, t in enumerate(col_types):

@@ -28,8 +28,10 @@
  * the sequential walk on every short input.
  *
  * Also stated plainly: timestamps (conv_ts: days counted a year and a month
- * at a time), CRLF line ends (a CR symbol, kind 2) and the fewest and most
- * fields per record (or_count_fields).
+ * at a time), CRLF line ends (a CR symbol, kind 2), the fewest and most
+ * fields per record (or_count_fields), and symbols of several bytes in
+ * UTF-8 and UTF-16 inputs (sym_at, or_csv_parse_enc: the DFA steps once per
+ * symbol, decoded front to back).
  *
  * The JSON-like lexer DFA (16 states) follows the prefix-scan lexing scheme
  * of "Lexing on the GPU: the scan is the easy part" (section "A lexer is a
@@ -73,8 +75,10 @@ static void flag(or_status* st, int bit, uint64_t off, int with_offset) {
 /* ------------------------------------------------------------ CSV DFA */
 enum { EOR = 0, FLD = 1, ENC = 2, ESC = 3, INV = 4 };
 
-/* cr: a carriage return byte dropped outside quotes (CRLF line ends), or -1 */
-typedef struct { uint8_t fd, rd, q; int cr; } csv_syms;
+/* The symbols the CSV DFA tells apart, as byte values or, for the
+ * encodings below, code points; cr: a carriage return dropped outside
+ * quotes (CRLF line ends), or -1 */
+typedef struct { uint32_t fd, rd, q; int64_t cr; } csv_syms;
 
 /* One transition of the quoted-CSV DFA.  Returns the next state and writes
  * the symbol's tag.  Cells (state, symbol) -> (next, tag):
@@ -89,8 +93,8 @@ typedef struct { uint8_t fd, rd, q; int cr; } csv_syms;
  * more expressive parsing rules), a CR outside quotes is a control symbol,
  * dropped from the value, that leaves the field open:
  *   EOR, FLD, ESC: cr -> FLD ctrl     ENC: cr -> ENC data                */
-static int csv_step(const csv_syms* y, int s, uint8_t b, int* tag) {
-  int is_q = b == y->q, is_fd = b == y->fd, is_rd = b == y->rd, is_cr = (int)b == y->cr;
+static int csv_step(const csv_syms* y, int s, uint32_t b, int* tag) {
+  int is_q = b == y->q, is_fd = b == y->fd, is_rd = b == y->rd, is_cr = (int64_t)b == y->cr;
   switch (s) {
     case EOR:
       if (is_q) { *tag = T_CTRL; return ENC; }
@@ -422,22 +426,75 @@ static void close_record(csv_out* o, uint64_t rec, int col, uint64_t off) {
   for (int c = col + 1; c < o->n_cols; c++) close_field(o, rec, c, off);  /* defaults */
 }
 
+/* ------------------------------------------------- symbols of an encoding */
+/* ParPaRaw Section 3.4: with a variable-length encoding a symbol spans
+ * several bytes; the DFA takes one transition per symbol.
+ *   bytes (0): every byte is a symbol, its value the byte.
+ *   UTF-8 (1): a symbol is a byte that is not a continuation byte
+ *     (0b10xxxxxx) together with all the continuation bytes after it (so a
+ *     chunk's leading continuation bytes belong to the symbol before).  It
+ *     is well formed if it has the length its first byte announces (1 for
+ *     0xxxxxxx, 2, 3, 4 for 110xxxxx, 1110xxxx, 11110xxx), is no overlong
+ *     form and is at most 0x10FFFF; its value is then the code point.
+ *     Continuation bytes at the input's start form one ill-formed symbol.
+ *   UTF-16LE (2): 2-byte little-endian units counted from the input's first
+ *     byte; a high surrogate (0xD800-0xDBFF) followed by a low surrogate
+ *     (0xDC00-0xDFFF) is one 4-byte symbol, any other unit a 2-byte one
+ *     whose value is the unit; an odd last byte is an ill-formed symbol.
+ * sym_at returns the end of the symbol starting at i and its value in
+ * *cp (OR_BAD_CP when ill formed).                                      */
+#define OR_BAD_CP 0xFFFFFFFFu
+static int is_cont(uint8_t b) { return (b & 0xC0) == 0x80; }
+static uint64_t sym_at(const uint8_t* in, uint64_t n, int enc, uint64_t i, uint32_t* cp) {
+  if (enc == 0) { *cp = in[i]; return i + 1; }
+  if (enc == 1) {
+    uint64_t j = i + 1;
+    while (j < n && is_cont(in[j])) j++;
+    const uint64_t len = j - i;
+    const uint8_t b = in[i];
+    uint64_t want;
+    uint32_t v;
+    if (b < 0x80) { want = 1; v = b; }
+    else if ((b & 0xE0) == 0xC0) { want = 2; v = b & 0x1F; }
+    else if ((b & 0xF0) == 0xE0) { want = 3; v = b & 0x0F; }
+    else if ((b & 0xF8) == 0xF0) { want = 4; v = b & 0x07; }
+    else { *cp = OR_BAD_CP; return j; }          /* a continuation byte or 0xF8-0xFF */
+    if (len != want) { *cp = OR_BAD_CP; return j; }
+    for (uint64_t k = i + 1; k < j; k++) v = (v << 6) | (in[k] & 0x3F);
+    static const uint32_t min_of_len[5] = {0, 0, 0x80, 0x800, 0x10000};
+    *cp = (v < min_of_len[len] || v > 0x10FFFF) ? OR_BAD_CP : v;
+    return j;
+  }
+  /* UTF-16LE */
+  if (i + 1 >= n) { *cp = OR_BAD_CP; return n; }
+  const uint32_t u = in[i] | (uint32_t)in[i + 1] << 8;
+  if (u >= 0xD800 && u <= 0xDBFF && i + 3 < n) {
+    const uint32_t w = in[i + 2] | (uint32_t)in[i + 3] << 8;
+    if (w >= 0xDC00 && w <= 0xDFFF) {
+      *cp = 0x10000 + ((u - 0xD800) << 10) + (w - 0xDC00);
+      return i + 4;
+    }
+  }
+  *cp = u;
+  return i + 2;
+}
+
 /* One parsed field of the record being collected (the records are buffered
  * whole so that a record can be dropped once its field count is known). */
 typedef struct { uint64_t start, vbeg, vlen; } or_field;
 
-int or_csv_parse_ex(const uint8_t* in, uint64_t n, uint8_t fd, uint8_t rd, uint8_t q, int crlf,
-                    int n_cols, const int32_t* col_types, const uint64_t* defaults, int reject,
-                    const uint64_t* skip_records, uint64_t n_skip_records,
-                    int32_t** out_offsets, uint8_t** out_chars, void** out_typed,
-                    uint64_t records_capacity, const uint64_t* chars_capacity, or_status* st) {
+static int csv_parse_core(const uint8_t* in, uint64_t n, int enc, csv_syms y,
+                          int n_cols, const int32_t* col_types, const uint64_t* defaults,
+                          int reject, const uint64_t* skip_records, uint64_t n_skip_records,
+                          int32_t** out_offsets, uint8_t** out_chars, void** out_typed,
+                          uint64_t records_capacity, const uint64_t* chars_capacity,
+                          or_status* st) {
   memset(st, 0, sizeof *st);
   st->first_error_offset = UINT64_MAX;
   csv_out o = {n_cols, col_types, defaults, out_offsets, out_chars, out_typed, records_capacity,
                chars_capacity, st, NULL, 0, 0};
   for (int c = 0; c < n_cols; c++)
     if (col_types[c] == C_STR && out_offsets[c]) out_offsets[c][0] = 0;
-  csv_syms y = syms_of(crlf ? 2 : 0, fd, rd, q);
   /* the current record: its value bytes in one buffer, a list of fields */
   uint8_t* rbytes = NULL;
   size_t rb_len = 0, rb_cap = 0;
@@ -484,28 +541,34 @@ int or_csv_parse_ex(const uint8_t* in, uint64_t n, uint8_t fd, uint8_t rd, uint8
     rec_in++;                                                                 \
     nf = 0; rb_len = 0; vbeg = 0;                                             \
   } while (0)
-  for (uint64_t i = 0; i < n; i++) {
-    s = csv_step(&y, s, in[i], &tag);
+  /* one symbol [i, j) at a time; a symbol's offsets (terminator, invalid
+   * transition) are those of its last byte */
+  for (uint64_t i = 0, j; i < n; i = j) {
+    uint32_t sym;
+    j = sym_at(in, n, enc, i, &sym);
+    s = csv_step(&y, s, sym, &tag);
     switch (tag) {
       case T_DATA:
-        if (rb_len == rb_cap) {
-          rb_cap = rb_cap ? 2 * rb_cap : 256;
-          rbytes = (uint8_t*)realloc(rbytes, rb_cap);
+        for (uint64_t k = i; k < j; k++) {
+          if (rb_len == rb_cap) {
+            rb_cap = rb_cap ? 2 * rb_cap : 256;
+            rbytes = (uint8_t*)realloc(rbytes, rb_cap);
+          }
+          rbytes[rb_len++] = in[k];
         }
-        rbytes[rb_len++] = in[i];
         break;
       case T_CTRL: break;
       case T_FD:
         PUSH_FIELD();
-        vbeg = rb_len; field_start = i + 1;
+        vbeg = rb_len; field_start = j;
         break;
       case T_RD:
         PUSH_FIELD();
-        CLOSE_RECORD(i);
-        field_start = i + 1;
+        CLOSE_RECORD(j - 1);
+        field_start = j;
         break;
       default:
-        flag(st, E_INVALID_INPUT, i, 1);
+        flag(st, E_INVALID_INPUT, j - 1, 1);
         break;
     }
   }
@@ -533,6 +596,30 @@ int or_csv_parse_ex(const uint8_t* in, uint64_t n, uint8_t fd, uint8_t rd, uint8
   free(rbytes);
   free(fields);
   return 0;
+}
+
+int or_csv_parse_ex(const uint8_t* in, uint64_t n, uint8_t fd, uint8_t rd, uint8_t q, int crlf,
+                    int n_cols, const int32_t* col_types, const uint64_t* defaults, int reject,
+                    const uint64_t* skip_records, uint64_t n_skip_records,
+                    int32_t** out_offsets, uint8_t** out_chars, void** out_typed,
+                    uint64_t records_capacity, const uint64_t* chars_capacity, or_status* st) {
+  return csv_parse_core(in, n, 0, syms_of(crlf ? 2 : 0, fd, rd, q), n_cols, col_types, defaults,
+                        reject, skip_records, n_skip_records, out_offsets, out_chars, out_typed,
+                        records_capacity, chars_capacity, st);
+}
+
+/* The quoted-CSV parse of an input in a variable-length encoding (enc 1
+ * UTF-8, 2 UTF-16LE; ParPaRaw Section 3.4): the DFA reads symbols, with
+ * field delimiter, record delimiter and quote given as code points. */
+int or_csv_parse_enc(const uint8_t* in, uint64_t n, int enc, uint32_t fd, uint32_t rd, uint32_t q,
+                     int n_cols, const int32_t* col_types, const uint64_t* defaults, int reject,
+                     const uint64_t* skip_records, uint64_t n_skip_records,
+                     int32_t** out_offsets, uint8_t** out_chars, void** out_typed,
+                     uint64_t records_capacity, const uint64_t* chars_capacity, or_status* st) {
+  const csv_syms y = {fd, rd, q, -1};
+  return csv_parse_core(in, n, enc, y, n_cols, col_types, defaults, reject, skip_records,
+                        n_skip_records, out_offsets, out_chars, out_typed, records_capacity,
+                        chars_capacity, st);
 }
 
 int or_csv_parse(const uint8_t* in, uint64_t n, uint8_t fd, uint8_t rd, uint8_t q, int crlf,
