@@ -43,8 +43,10 @@ class DfaDesc(ctypes.Structure):
     """pp_dfa_desc (host memory)."""
     _fields_ = [("n_states", _u8), ("n_groups", _u8), ("start_state", _u8),
                 ("invalid_state", _u8), ("accept_mask", _u16), ("background_group", _u8),
-                ("reserved", _u8), ("byte_to_group", _u8 * 256), ("delta", (_u8 * 16) * 16),
-                ("tag", (_u8 * 16) * 16), ("token_id", _u8 * 16), ("byte_token_id", _u8 * 256)]
+                ("encoding", _u8), ("byte_to_group", _u8 * 256), ("delta", (_u8 * 16) * 16),
+                ("tag", (_u8 * 16) * 16), ("token_id", _u8 * 16), ("byte_token_id", _u8 * 256),
+                ("n_syms", _u8), ("sym_group", _u8 * 8), ("reserved2", _u8 * 3),
+                ("sym_cp", ctypes.c_uint32 * 8)]
 
 
 class Status(ctypes.Structure):
@@ -97,6 +99,9 @@ def lib() -> ctypes.CDLL:
         L.pp_tags.argtypes = [_vp, _sz, ctypes.POINTER(DfaDesc), _vp, _vp, _vp, _vp]
         L.pp_count_byte.restype = ctypes.c_int
         L.pp_count_byte.argtypes = [_vp, _sz, _u8, _vp, _vp]
+        L.pp_desc_csv_enc.restype = ctypes.c_int
+        L.pp_desc_csv_enc.argtypes = [ctypes.POINTER(DfaDesc), ctypes.c_int, ctypes.c_uint32,
+                                      ctypes.c_uint32, ctypes.c_uint32]
         L.pp_desc_csv.restype = ctypes.c_int
         L.pp_desc_csv.argtypes = [ctypes.POINTER(DfaDesc), _u8, _u8, _u8]
         L.pp_count_fields.restype = ctypes.c_int
@@ -136,6 +141,21 @@ def _stream(stream) -> int:
 def desc_csv(fd: bytes = b",", rd: bytes = b"\n", quote: bytes = b'"') -> DfaDesc:
     d = DfaDesc()
     _check(lib().pp_desc_csv(ctypes.byref(d), fd[0], rd[0], quote[0]), "pp_desc_csv")
+    return d
+
+
+ENC_UTF8, ENC_UTF16LE = 1, 2
+ENCODINGS = {"utf-8": ENC_UTF8, "utf-16-le": ENC_UTF16LE}
+
+
+def desc_csv_enc(encoding: str, fd: str = ",", rd: str = "\n", quote: str = '"') -> DfaDesc:
+    """The quoted-CSV DFA over the symbols of an encoding ("utf-8" or
+    "utf-16-le"); fd, rd and quote are characters (or code points)."""
+    def cp(x):
+        return x if isinstance(x, int) else ord(x)
+    d = DfaDesc()
+    _check(lib().pp_desc_csv_enc(ctypes.byref(d), ENCODINGS[encoding], cp(fd), cp(rd), cp(quote)),
+           "pp_desc_csv_enc")
     return d
 
 

@@ -71,6 +71,14 @@ bool dfa_ok(const pp_dfa_desc* d, int max_states) {
   if (d->start_state == d->invalid_state) return false;
   for (int b = 0; b < 256; ++b)
     if (d->byte_to_group[b] >= d->n_groups) return false;
+  if (d->encoding > PP_ENC_UTF16LE || d->n_syms > PP_MAX_SYMS) return false;
+  for (int k = 0; k < d->n_syms; ++k) {
+    const uint32_t cp = d->sym_cp[k];
+    if (cp < 0x80 || cp > 0x10FFFF || (cp >= 0xD800 && cp <= 0xDFFF)) return false;
+    if (d->sym_group[k] >= d->n_groups) return false;
+    for (int j = 0; j < k; ++j)
+      if (d->sym_cp[j] == cp) return false;
+  }
   for (int g = 0; g < d->n_groups; ++g)
     for (int s = 0; s < d->n_states; ++s) {
       if (d->delta[g][s] >= d->n_states) return false;
@@ -126,6 +134,23 @@ uint32_t parse_lut_entry(const pp_dfa_desc* d, int g, int x) {
   return e;
 }
 
+// LUT entry of a byte of a multi-byte symbol of group g other than its
+// last: it keeps the state and is tagged CTRL where the symbol is a
+// delimiter or control symbol, else DATA; never background.
+uint32_t parse_lut_mid_entry(const pp_dfa_desc* d, int g, int x) {
+  uint32_t e = 4u << 16 | 3u << 28 | 1u << 31;
+  for (int s = 0; s < 4; ++s) {
+    e |= uint32_t(s) << (4 * s);
+    const int t = s < d->n_states ? d->tag[s][g] : PP_TAG_DATA;
+    if (t == PP_TAG_FD || t == PP_TAG_RD || t == PP_TAG_CTRL) e |= 3u << (20 + 2 * s);
+  }
+  if (x < 4) {
+    const int t = d->tag[x][g];
+    if (t == PP_TAG_FD || t == PP_TAG_RD || t == PP_TAG_CTRL) e |= 1u << 30;
+  }
+  return e;
+}
+
 // The live state with the fewest non-inert symbol groups (a group is inert
 // in s if it keeps s and tags the byte DATA); runs of inert bytes in that
 // state need no DFA steps.  4 when no state has an inert group.
@@ -175,7 +200,9 @@ bool parse_dfa_ok(const pp_dfa_desc* d) {
 
 namespace ppi {
 
-bool generic_dfa_ok(const pp_dfa_desc* d) { return dfa_ok(d, PP_MAX_STATES); }
+bool generic_dfa_ok(const pp_dfa_desc* d) {
+  return dfa_ok(d, PP_MAX_STATES) && d->encoding == PP_ENC_BYTES;
+}
 GenericDfa to_generic_dfa(const pp_dfa_desc* d) { return to_generic(d); }
 
 // Host half of pp_parse: checks the arguments and fills the kernel
@@ -194,6 +221,7 @@ pp_rc parse_prepare(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa,
   for (int c = 0; c < n_cols; ++c) {
     const int ty = col_types[c];
     if (ty < PP_COL_STRING || ty > PP_COL_TIMESTAMP) return PP_EINVAL;
+    if (ty == PP_COL_TIMESTAMP && dfa->encoding != PP_ENC_BYTES) return PP_EINVAL;
     p.coltype[c] = uint8_t(ty);
     p.stridx[c] = -1;
     if (ty == PP_COL_STRING) {
@@ -239,7 +267,28 @@ pp_rc parse_prepare(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa,
   p.dbg_withhold = ppi::g_withhold;
   const int x = sticky_state(dfa);
   p.sticky = uint32_t(x);
-  for (int b = 0; b < 256; ++b) p.lut[b] = parse_lut_entry(dfa, dfa->byte_to_group[b], x);
+  if (dfa->encoding == PP_ENC_BYTES) {
+    for (int b = 0; b < 256; ++b) p.lut[b] = parse_lut_entry(dfa, dfa->byte_to_group[b], x);
+  } else {
+    // LUT rows by symbol code: a one-byte symbol below 0x80 is its own code,
+    // SYM_LAST + g the last byte of a longer symbol of group g, SYM_MID + g
+    // its other bytes
+    const int dflt = dfa->byte_to_group[0x80];
+    for (int b = 0; b < 256; ++b) p.lut[b] = parse_lut_entry(dfa, dflt, x);
+    for (int b = 0; b < 0x80; ++b) p.lut[b] = parse_lut_entry(dfa, dfa->byte_to_group[b], x);
+    for (int g = 0; g < dfa->n_groups; ++g) {
+      p.lut[SYM_LAST + g] = parse_lut_entry(dfa, g, x);
+      p.lut[SYM_MID + g] = parse_lut_mid_entry(dfa, g, x);
+    }
+    p.enc = dfa->encoding;
+    p.sym_n = dfa->n_syms;
+    p.sym_dflt = uint8_t(dflt);
+    for (int b = 0; b < 0x80; ++b) p.sym_b2g[b] = dfa->byte_to_group[b];
+    for (int k = 0; k < dfa->n_syms; ++k) {
+      p.sym_cp[k] = dfa->sym_cp[k];
+      p.sym_g[k] = dfa->sym_group[k];
+    }
+  }
   p.bg_next = 0;
   if (dfa->background_group != 0xFF) {
     for (int s = 0; s < 4; ++s)
@@ -310,6 +359,29 @@ pp_rc pp_desc_csv(pp_dfa_desc* out, uint8_t fd, uint8_t rd, uint8_t quote) {
     }
   for (int s = 0; s < PP_MAX_STATES; ++s) out->token_id[s] = 255;
   for (int b = 0; b < 256; ++b) out->byte_token_id[b] = 255;
+  return PP_OK;
+}
+
+pp_rc pp_desc_csv_enc(pp_dfa_desc* out, int encoding, uint32_t fd, uint32_t rd, uint32_t quote) {
+  if (!out || (encoding != PP_ENC_UTF8 && encoding != PP_ENC_UTF16LE)) return PP_EINVAL;
+  const uint32_t cps[3] = {quote, fd, rd};  // groups 0, 1, 2 as in pp_desc_csv
+  for (int k = 0; k < 3; ++k)
+    if (cps[k] > 0x10FFFF || (cps[k] >= 0xD800 && cps[k] <= 0xDFFF)) return PP_EINVAL;
+  if (fd == rd || fd == quote || rd == quote) return PP_EINVAL;
+  // the byte descriptor with placeholder symbols, then the real ones
+  pp_rc rc = pp_desc_csv(out, 0, 1, 2);
+  if (rc != PP_OK) return rc;
+  for (int b = 0; b < 3; ++b) out->byte_to_group[b] = 3;  // the catch-all group
+  out->encoding = uint8_t(encoding);
+  for (int k = 0; k < 3; ++k) {
+    if (cps[k] < 0x80) {
+      out->byte_to_group[cps[k]] = uint8_t(k);
+    } else {
+      out->sym_cp[out->n_syms] = cps[k];
+      out->sym_group[out->n_syms] = uint8_t(k);
+      ++out->n_syms;
+    }
+  }
   return PP_OK;
 }
 
@@ -417,11 +489,11 @@ pp_rc pp_parse(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa, int 
                                       d_status, &p);
   if (rc != PP_OK) return rc;
   const int ns = ppi::parse_ns_width(p.n_str);
-  const size_t sb = ppi::parse_scratch_bytes(p.n_tiles, ns);
+  const size_t sb = ppi::parse_scratch_bytes(p.n_tiles, ns, p.enc != 0);
   void* scratch = nullptr;
   cudaError_t e = cudaMallocAsync(&scratch, sb, stream);
   if (e != cudaSuccess) return cuda_rc(e);
-  ppi::parse_scratch_carve(scratch, p.n_tiles, ns, &p.s);
+  ppi::parse_scratch_carve(scratch, p.n_tiles, ns, &p.s, p.enc != 0);
   e = ppi::launch_parse(p, stream);
   const cudaError_t ef = cudaFreeAsync(scratch, stream);
   if (e == cudaSuccess) e = ef;
@@ -430,7 +502,7 @@ pp_rc pp_parse(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa, int 
 
 pp_rc pp_count_fields(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa,
                       uint64_t* d_fields, pp_status* d_status, cudaStream_t stream) {
-  if (!d_fields) return PP_EINVAL;
+  if (!d_fields || (dfa && dfa->encoding != PP_ENC_BYTES)) return PP_EINVAL;
   if (n_bytes > (size_t(1) << 36)) return PP_ETOOLARGE;  // the tile reduction's 32-bit ranges
   const pp_coltype skip = PP_COL_SKIP;
   ppi::ParseParams p;
@@ -449,7 +521,7 @@ pp_rc pp_count_fields(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* df
 pp_rc pp_tokenize(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa,
                   uint8_t* out_token_id, uint64_t* out_start, uint32_t* out_len,
                   size_t tokens_capacity, pp_status* d_status, cudaStream_t stream) {
-  if (!d_status || (n_bytes && !d_in) || !dfa_ok(dfa, PP_MAX_STATES)) return PP_EINVAL;
+  if (!d_status || (n_bytes && !d_in) || !ppi::generic_dfa_ok(dfa)) return PP_EINVAL;
   if (tokens_capacity && (!out_token_id || !out_start || !out_len)) return PP_EINVAL;
   const GenericDfa g = to_generic(dfa);
   const size_t sb = ppi::tokenize_scratch_bytes(n_bytes);
@@ -466,7 +538,7 @@ pp_rc pp_tokenize(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa,
 pp_rc pp_tags(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa, uint8_t* d_state_before,
               uint8_t* d_tag, pp_status* d_status, cudaStream_t stream) {
   if (!d_status || (n_bytes && (!d_in || !d_state_before || !d_tag)) ||
-      !dfa_ok(dfa, PP_MAX_STATES))
+      !ppi::generic_dfa_ok(dfa))
     return PP_EINVAL;
   const GenericDfa g = to_generic(dfa);
   const size_t sb = ppi::tags_scratch_bytes(n_bytes);

@@ -55,10 +55,12 @@ constexpr uint8_t COL_INFER = 7;  // internal column kind: type inference only
 // input byte range, column | type << 8.
 struct LongField { uint64_t rec, start, end; uint32_t col, pad; };
 constexpr uint32_t LONG_CAP = 4096;  // queued fields per call, at most
+constexpr uint32_t SYM_LAST = 128, SYM_MID = 144;  // symbol codes (see ParseParams::enc)
 
 struct ParseScratch {
   uint32_t* counters;       // [0] tile tickets, [2] column-count end flag, [3] tile-state scan
-                            // tickets, [4] queued long fields
+                            // tickets, [4] queued long fields, [5] queued fields begun in an
+                            // earlier tile (encodings; at long_q[long_cap ...])
   LongField* long_q;        // [long_cap] (null: no queue, every field converted by its lane)
   uint32_t long_cap;
   uint32_t* tile_stv;       // [n_tiles]
@@ -77,7 +79,16 @@ struct ParseParams {
   uint32_t n_tiles;
   uint32_t spin_limit;
   uint32_t dbg_withhold;  // test hook: the first tile posts nothing to the look-backs
-  uint32_t lut[256];      // per byte: STV selector, next-state/tag fields, special bit
+  uint32_t lut[256];      // per byte (or symbol code): STV selector, next-state/tag fields, special bit
+  // Inputs in an encoding (PP_ENC_UTF8, PP_ENC_UTF16LE): lut is indexed by
+  // symbol code (a one-byte symbol below 0x80: the byte; SYM_LAST + group:
+  // the last byte of a longer symbol; SYM_MID + group: its other bytes).
+  uint8_t enc;            // PP_ENC_*
+  uint8_t sym_n;          // code points with a group of their own
+  uint8_t sym_dflt;       // group of every other symbol of 0x80 and above
+  uint8_t sym_b2g[0x80];  // group of the code points below 0x80
+  uint8_t sym_g[PP_MAX_SYMS];
+  uint32_t sym_cp[PP_MAX_SYMS];
   uint32_t bg_next;       // nibble s = delta[background][s], s = 0..4
   uint32_t sticky;        // state whose non-inert groups set LUT bit 30 (4: none)
   uint16_t accept_mask;
@@ -122,8 +133,10 @@ struct ParseParams {
 
 // bytes of scratch for n_tiles tiles and ns string columns (ns rounded to the
 // kernel's instantiation width)
-size_t parse_scratch_bytes(uint32_t n_tiles, int ns);
-void parse_scratch_carve(void* base, uint32_t n_tiles, int ns, ParseScratch* out);
+// sym: an input in an encoding (room in the long-field queue for one field
+// per tile begun in an earlier tile)
+size_t parse_scratch_bytes(uint32_t n_tiles, int ns, bool sym = false);
+void parse_scratch_carve(void* base, uint32_t n_tiles, int ns, ParseScratch* out, bool sym = false);
 int parse_ns_width(int n_str);
 
 // init (counters, look-back flags, status), tile vectors, tile states, tile pass

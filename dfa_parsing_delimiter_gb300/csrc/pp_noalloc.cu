@@ -59,14 +59,14 @@ pp_rc pp_parse_noalloc(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* d
                                 out_typed, records_capacity, chars_capacity, d_status, &p);
   if (rc != PP_OK) return rc;
   const int ns = ppi::parse_ns_width(p.n_str);
-  const size_t sb = ppi::parse_scratch_bytes(p.n_tiles, ns);
+  const size_t sb = ppi::parse_scratch_bytes(p.n_tiles, ns, p.enc != 0);
   if (sb > PP_NOALLOC_SCRATCH_BYTES) return PP_ETOOLARGE;  // before any CUDA call
   void* scratch = nullptr;
   if ((rc = scratch_address(&scratch)) != PP_OK) return rc;
   // The tile counters and look-back flags, the only parts of the buffer
   // that must start at zero, are zeroed by the first kernel launch_parse
   // enqueues; every other byte is written before it is read.
-  ppi::parse_scratch_carve(scratch, p.n_tiles, ns, &p.s);
+  ppi::parse_scratch_carve(scratch, p.n_tiles, ns, &p.s, p.enc != 0);
   const cudaError_t e = ppi::launch_parse(p, stream);
   if (e == cudaSuccess) return PP_OK;
   return e == cudaErrorMemoryAllocation ? PP_ENOMEM : PP_ECUDA;

@@ -200,6 +200,8 @@ extern "C" pp_rc pp_parse_ex(const uint8_t* d_in, size_t n_bytes, const pp_dfa_d
   std::memset(&o, 0, sizeof o);
   if (opts) o = *opts;
   if (o.flags & ~PP_PARSE_REJECT) return PP_EINVAL;
+  // rows are cut at record-delimiter bytes: byte inputs only
+  if (o.n_skip_rows && dfa && dfa->encoding != PP_ENC_BYTES) return PP_EINVAL;
   if ((o.n_skip_records && !o.skip_records) || (o.n_skip_rows && !o.skip_rows)) return PP_EINVAL;
   if (!ascending(o.skip_records, o.n_skip_records) || !ascending(o.skip_rows, o.n_skip_rows))
     return PP_EINVAL;
@@ -312,16 +314,16 @@ extern "C" pp_rc pp_parse_ex(const uint8_t* d_in, size_t n_bytes, const pp_dfa_d
   // ---- the parse
   const int ns = ppi::parse_ns_width(p.n_str);
   void* scratch;
-  if ((e = A.get(&scratch, ppi::parse_scratch_bytes(p.n_tiles, ns))) != cudaSuccess)
+  if ((e = A.get(&scratch, ppi::parse_scratch_bytes(p.n_tiles, ns, p.enc != 0))) != cudaSuccess)
     return rc_of(e);
-  ppi::parse_scratch_carve(scratch, p.n_tiles, ns, &p.s);
+  ppi::parse_scratch_carve(scratch, p.n_tiles, ns, &p.s, p.enc != 0);
   return rc_of(ppi::launch_parse(p, stream));
 }
 
 extern "C" pp_rc pp_infer_types(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa,
                                 int n_cols, int32_t* d_types, pp_status* d_status,
                                 cudaStream_t stream) {
-  if (!d_types) return PP_EINVAL;
+  if (!d_types || (dfa && dfa->encoding != PP_ENC_BYTES)) return PP_EINVAL;
   std::vector<pp_coltype> skip(size_t(n_cols > 0 ? n_cols : 1), PP_COL_SKIP);
   ppi::ParseParams p;
   const pp_rc rc = ppi::parse_prepare(d_in, n_bytes, dfa, n_cols, skip.data(), nullptr, nullptr,

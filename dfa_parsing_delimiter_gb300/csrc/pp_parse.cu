@@ -108,6 +108,107 @@ __device__ __forceinline__ uint32_t popc_range(const uint32_t* m, uint32_t a, ui
   return n;
 }
 
+// ------------------------------------------------ symbols of an encoding
+// Inputs in UTF-8 or UTF-16LE (ParPaRaw Section 3.4): a symbol may span
+// several bytes and cross chunk and tile boundaries.  Every byte gets a code
+// that indexes the LUT in place of the byte: the symbol's transition is
+// taken at its last byte (code: the byte for a one-byte symbol below 0x80,
+// else SYM_LAST + its group); its other bytes keep the state and take the
+// symbol's tag as DATA or CTRL (code SYM_MID + group).  So the bytes at a
+// chunk's start that continue a symbol begun before it change nothing, as
+// the page asks, and a multi-byte delimiter's other bytes drop out of the
+// values like control bytes.  Symbol boundaries: in UTF-8 a byte that is
+// not 0b10xxxxxx with the 0b10xxxxxx bytes after it; in UTF-16LE 2-byte
+// units from the input's first byte, a high surrogate and the low
+// surrogate after it forming one symbol.  B(q) reads input byte q (q < n).
+using ppi::SYM_LAST;
+using ppi::SYM_MID;
+
+__device__ __forceinline__ uint32_t sym_group(const ParseParams& P, const uint8_t* b2g,
+                                              uint32_t cp) {
+  if (cp < 0x80) return b2g[cp];
+  for (uint32_t k = 0; k < P.sym_n; ++k)
+    if (P.sym_cp[k] == cp) return P.sym_g[k];
+  return P.sym_dflt;
+}
+__device__ __forceinline__ bool is_cont(uint32_t b) { return (b & 0xC0u) == 0x80u; }
+
+// UTF-8: the group of the symbol whose last byte is r.
+template <class ByteAt>
+__device__ uint32_t utf8_group(const ParseParams& P, const uint8_t* b2g, uint64_t r, ByteAt B) {
+  uint64_t q = r;
+  for (int k = 0; k < 4 && q > 0 && is_cont(B(q)); ++k) --q;
+  const uint32_t lead = B(q);
+  if (is_cont(lead)) return P.sym_dflt;  // no first byte in reach (or at the input start)
+  const uint32_t len = uint32_t(r - q) + 1;
+  uint32_t want, v;
+  if (lead < 0x80) { want = 1; v = lead; }
+  else if ((lead & 0xE0u) == 0xC0u) { want = 2; v = lead & 0x1Fu; }
+  else if ((lead & 0xF0u) == 0xE0u) { want = 3; v = lead & 0x0Fu; }
+  else if ((lead & 0xF8u) == 0xF0u) { want = 4; v = lead & 0x07u; }
+  else return P.sym_dflt;
+  if (len != want) return P.sym_dflt;
+  for (uint64_t i = q + 1; i <= r; ++i) v = (v << 6) | (B(i) & 0x3Fu);
+  const uint32_t lo = len == 2 ? 0x80u : len == 3 ? 0x800u : len == 4 ? 0x10000u : 0u;
+  if (v < lo || v > 0x10FFFFu) return P.sym_dflt;
+  return sym_group(P, b2g, v);
+}
+
+// The code of input byte p.
+template <class ByteAt>
+__device__ uint32_t sym_code(const ParseParams& P, const uint8_t* b2g, uint64_t p, ByteAt B) {
+  const uint64_t n = P.n;
+  if (P.enc == PP_ENC_UTF8) {
+    const uint32_t b = B(p);
+    if (!(p + 1 < n && is_cont(B(p + 1))))  // the symbol's last byte
+      return b < 0x80 ? b : SYM_LAST + utf8_group(P, b2g, p, B);
+    uint64_t r = p + 1;  // its last byte, when at most four bytes on
+    for (int k = 1; k < 4 && r + 1 < n && is_cont(B(r + 1)); ++k) ++r;
+    const bool longer = r + 1 < n && is_cont(B(r + 1));
+    return SYM_MID + (longer ? uint32_t(P.sym_dflt) : utf8_group(P, b2g, r, B));
+  }
+  // UTF-16LE
+  const uint64_t u = p >> 1;
+  if (2 * u + 1 >= n) return SYM_LAST + P.sym_dflt;  // an odd last byte
+  auto unit = [&](uint64_t v) { return B(2 * v) | (B(2 * v + 1) << 8); };
+  const uint32_t x = unit(u);
+  uint64_t last = 2 * u + 1;
+  uint32_t cp = x;
+  if (x >= 0xDC00u && x <= 0xDFFFu && u > 0) {
+    const uint32_t y = unit(u - 1);
+    if (y >= 0xD800u && y <= 0xDBFFu) cp = 0x10000u + ((y - 0xD800u) << 10) + (x - 0xDC00u);
+  } else if (x >= 0xD800u && x <= 0xDBFFu && 2 * u + 3 < n) {
+    const uint32_t y = unit(u + 1);
+    if (y >= 0xDC00u && y <= 0xDFFFu) {
+      cp = 0x10000u + ((x - 0xD800u) << 10) + (y - 0xDC00u);
+      last = 2 * u + 3;
+    }
+  }
+  if (p == last) return cp < 0x80 ? cp : SYM_LAST + sym_group(P, b2g, cp);
+  return SYM_MID + sym_group(P, b2g, cp);
+}
+
+// The code of input byte p, read from HBM (the paths outside the tile pass's
+// hot loops).
+__device__ __noinline__ uint32_t sym_code_global(const ParseParams& P, uint64_t p) {
+  auto B = [&](uint64_t q) -> uint32_t { return __ldg(P.in + q); };
+  return sym_code(P, P.sym_b2g, p, B);
+}
+
+// Symbol codes of tile bytes [c0, c0 + clen) into codes_s[c0 ...]; bytes
+// outside the tile (a symbol crossing the tile's ends) are read from HBM.
+__device__ __noinline__ void chunk_codes(const ParseParams& P, const uint8_t* b2g,
+                                         const uint8_t* tile_s, uint64_t tile_base,
+                                         uint32_t tile_len, uint32_t c0, uint32_t clen,
+                                         uint8_t* codes_s) {
+  auto B = [&](uint64_t q) -> uint32_t {
+    const uint64_t l = q - tile_base;
+    return l < tile_len ? uint32_t(tile_s[l]) : uint32_t(__ldg(P.in + q));
+  };
+  for (uint32_t j = 0; j < clen; ++j)
+    codes_s[c0 + j] = uint8_t(sym_code(P, b2g, tile_base + c0 + j, B));
+}
+
 // ------------------------------------------------- tile feeding (TMA)
 // Two linear landing buffers.  A block takes its first tile at start; once
 // a tile has landed it takes the next ticket and starts that tile's bulk
@@ -333,7 +434,7 @@ __device__ __forceinline__ V2 chunk_v2(const Tags& g) {
 // re-tagged by running the DFA from the state at its first byte (lut: one
 // LUT entry per byte value).
 template <class Acc>
-__device__ __forceinline__ uint32_t feed_field(Acc& acc, const uint8_t* in, uint64_t fs,
+__device__ __forceinline__ uint32_t feed_field(Acc& acc, const ParseParams& P, uint64_t fs,
                                                uint64_t fe, uint64_t tile_base,
                                                const uint8_t* tile_s, const uint32_t* ctrl_s,
                                                const uint32_t* lut, uint32_t fstate) {
@@ -354,8 +455,8 @@ __device__ __forceinline__ uint32_t feed_field(Acc& acc, const uint8_t* in, uint
     uint32_t s = fstate;
     for (uint64_t p = fs; p < fe; ++p) {
       const uint32_t b = p >= tile_base ? tile_byte(tile_s, uint32_t(p - tile_base))
-                                        : uint32_t(__ldg(in + p));
-      const uint32_t e = lut[b];
+                                        : uint32_t(__ldg(P.in + p));
+      const uint32_t e = lut[b];  // byte inputs only: with an encoding such fields go to a warp
       const uint32_t tg = (e >> (20 + 2 * s)) & 3u;
       s = (e >> (4 * s)) & 0xFu;
       if (tg == uint32_t(PP_TAG_CTRL)) continue;
@@ -394,8 +495,10 @@ constexpr int TS_TILES = TS_NT * TS_TPT;
 // TV_BYTES bytes back to front, a warp scan composing the lanes in order.
 __global__ void __launch_bounds__(TV_NT) tile_stv_kernel(const __grid_constant__ ParseParams P) {
   extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ uint8_t b2g_s[0x80];
   uint32_t* lut_s = reinterpret_cast<uint32_t*>(smem);
   for (int k = threadIdx.x; k < 256 * 32; k += TV_NT) lut_s[k] = P.lut[k >> 5];
+  for (int k = threadIdx.x; k < 0x80; k += TV_NT) b2g_s[k] = P.sym_b2g[k];
   __syncthreads();
   const int lane = threadIdx.x & 31;
   const uint32_t* my_lut = lut_s + lane;
@@ -419,7 +522,11 @@ __global__ void __launch_bounds__(TV_NT) tile_stv_kernel(const __grid_constant__
     const uint64_t b0 = uint64_t(tile) * TILE + uint64_t(lane) * TV_BYTES;
     const uint32_t len = b0 < P.n ? uint32_t(min(uint64_t(TV_BYTES), P.n - b0)) : 0u;
     uint32_t G = STV_ID;
-    if (len == TV_BYTES) {
+    if (P.enc) {  // symbols of an encoding: one code per byte
+      auto B = [&](uint64_t q) -> uint32_t { return __ldg(P.in + q); };
+      for (int j = int(len) - 1; j >= 0; --j)
+        G = __byte_perm(G, STV_INV_POOL, my_lut[sym_code(P, b2g_s, b0 + j, B) << 5]);
+    } else if (len == TV_BYTES) {
       const uint8_t* p = P.in + b0;
       for (int j = int(tl) - 1; j >= 0; --j)  // the tail
         G = __byte_perm(G, STV_INV_POOL, my_lut[uint32_t(__ldg(p + h + 16u * nb + j)) << 5]);
@@ -526,11 +633,11 @@ __device__ __forceinline__ int convert_general(const ParseParams& P, uint32_t ty
   uint64_t val = dflt;
   if (ty == PP_COL_FLOAT64) {
     ppn::FloatAcc acc;
-    const uint32_t nd = feed_field(acc, P.in, fs, fe, tile_base, tile_s, ctrl_s, my_lut, fstate);
+    const uint32_t nd = feed_field(acc, P, fs, fe, tile_base, tile_s, ctrl_s, my_lut, fstate);
     if (nd) err = acc.finish(&val);
   } else if (ty == PP_COL_TIMESTAMP) {
     ppn::TsAcc acc;
-    const uint32_t nd = feed_field(acc, P.in, fs, fe, tile_base, tile_s, ctrl_s, my_lut, fstate);
+    const uint32_t nd = feed_field(acc, P, fs, fe, tile_base, tile_s, ctrl_s, my_lut, fstate);
     if (nd) {
       int64_t x = 0;
       err = acc.finish(&x);
@@ -538,7 +645,7 @@ __device__ __forceinline__ int convert_general(const ParseParams& P, uint32_t ty
     }
   } else {
     ppn::IntAcc acc;
-    const uint32_t nd = feed_field(acc, P.in, fs, fe, tile_base, tile_s, ctrl_s, my_lut, fstate);
+    const uint32_t nd = feed_field(acc, P, fs, fe, tile_base, tile_s, ctrl_s, my_lut, fstate);
     if (nd) {
       int64_t x = 0;
       if (ty == PP_COL_INT8) err = acc.finish(128ull, 127ull, &x);
@@ -744,6 +851,9 @@ __device__ void convert_long(const ParseParams& P, const uint32_t* lut, const pp
   const uint32_t lane = threadIdx.x & 31u;
   const uint32_t ty = f.col >> 8, col = f.col & 0xFFu;
   const uint64_t gs = f.start, ge = f.end;
+  auto code_at = [&](uint64_t q, uint32_t b) -> uint32_t {  // the LUT index of byte q (value b)
+    return P.enc ? sym_code_global(P, q) : b;
+  };
   const uint64_t t0 = (gs / TILE) * TILE;  // the DFA state there is known
   uint32_t cs = P.s.tile_state[gs / TILE];  // CSV state at the round start
   uint32_t gq = G0;                         // grammar state at the round start
@@ -762,7 +872,7 @@ __device__ void convert_long(const ParseParams& P, const uint32_t* lut, const pp
     uint32_t cv = STV_ID;
 #pragma unroll
     for (int j = int(LONG_SEG) - 1; j >= 0; --j)
-      if (uint32_t(j) < len) cv = __byte_perm(cv, STV_INV_POOL, lut[(bw[j >> 2] >> (8 * (j & 3))) & 0xFFu]);
+      if (uint32_t(j) < len) cv = __byte_perm(cv, STV_INV_POOL, lut[code_at(a + j, (bw[j >> 2] >> (8 * (j & 3))) & 0xFFu)]);
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
       const uint32_t o = __shfl_up_sync(FULL, cv, d);
@@ -777,7 +887,8 @@ __device__ void convert_long(const ParseParams& P, const uint32_t* lut, const pp
       uint32_t s = s_lane;
 #pragma unroll
       for (uint32_t j = 0; j < LONG_SEG; ++j)
-        if (j < len && !step_ctrl(lut, (bw[j >> 2] >> (8 * (j & 3))) & 0xFFu, s) && a + j >= gs)
+        if (j < len && !step_ctrl(lut, code_at(a + j, (bw[j >> 2] >> (8 * (j & 3))) & 0xFFu), s) &&
+            a + j >= gs)
           val_m |= 1u << j;
     }
     // grammar: the segment's transition vector (runs of digits compose once)
@@ -811,7 +922,7 @@ __device__ void convert_long(const ParseParams& P, const uint32_t* lut, const pp
         if (j >= len) continue;
         const uint32_t s_before = s;
         const uint32_t b = (bw[j >> 2] >> (8 * (j & 3))) & 0xFFu;
-        step_ctrl(lut, b, s);
+        step_ctrl(lut, code_at(a + j, b), s);
         if (!((val_m >> j) & 1u)) continue;
         const uint32_t c = sym_class(b);
         const uint32_t ns = nib_apply(class_vec(c), g);
@@ -882,7 +993,7 @@ __device__ void convert_long(const ParseParams& P, const uint32_t* lut, const pp
         uint32_t s = sz;
         for (uint64_t p = pz; p < ge && got < want; ++p) {
           const uint32_t b = __ldg(P.in + p);
-          if (step_ctrl(lut, b, s)) continue;
+          if (step_ctrl(lut, code_at(p, b), s)) continue;
           if (b - '0' <= 9u) { m = m * 10 + (b - '0'); ++got; }
         }
       }
@@ -895,7 +1006,7 @@ __device__ void convert_long(const ParseParams& P, const uint32_t* lut, const pp
             uint32_t s = sez;
             for (uint64_t p = pez; p < ge && ex <= 100000; ++p) {
               const uint32_t b = __ldg(P.in + p);
-              if (step_ctrl(lut, b, s)) continue;
+              if (step_ctrl(lut, code_at(p, b), s)) continue;
               ex = ex * 10 + int64_t(b - '0');
             }
           }
@@ -930,11 +1041,12 @@ __global__ void __launch_bounds__(LF_NT) long_field_kernel(const __grid_constant
   __shared__ uint32_t lut[256];
   for (int k = threadIdx.x; k < 256; k += LF_NT) lut[k] = P.lut[k];
   __syncthreads();
-  const uint32_t n = min(P.s.counters[4], P.s.long_cap);
+  // the queue proper, then (with an encoding) the fields begun in an earlier tile
+  const uint32_t n1 = min(P.s.counters[4], P.s.long_cap), n = n1 + P.s.counters[5];
   if (blockIdx.x == 0 && threadIdx.x == 0 && n) atomicAdd(&g_long_fields, n);
   const uint32_t warps = gridDim.x * (LF_NT / 32);
   for (uint32_t q = blockIdx.x * (LF_NT / 32) + (threadIdx.x >> 5); q < n; q += warps)
-    convert_long(P, lut, P.s.long_q[q]);
+    convert_long(P, lut, P.s.long_q[q < n1 ? q : P.s.long_cap + (q - n1)]);
 }
 
 // ------------------------------------------------------ type inference
@@ -951,7 +1063,7 @@ __device__ __forceinline__ uint32_t infer_field(const ParseParams& P, uint32_t v
   if (v == SLOT_DEFAULT) return 0;
   const uint32_t fsr = v >> 16, fe = v & 0xFFFFu;
   TypeAcc acc;
-  const uint32_t nd = feed_field(acc, P.in, fsr == 0xFFFFu ? X.tile_fstart : X.tile_base + fsr,
+  const uint32_t nd = feed_field(acc, P, fsr == 0xFFFFu ? X.tile_fstart : X.tile_base + fsr,
                                  X.tile_base + fe, X.tile_base, X.tile_s, X.ctrl_s, X.lut,
                                  X.tile_fstate);
   if (!nd) return 0;
@@ -1294,6 +1406,7 @@ struct PShared {
   uint8_t numcol[PP_MAX_COLS];     // numeric output columns, floats first
   uint32_t n_num;
   uint32_t lut1[256];              // the LUT, one entry per byte value
+  uint8_t sym_b2g[0x80];           // encodings: groups of the code points below 0x80
   uint32_t inf[PP_MAX_COLS];       // type inference: largest type code per column
   uint16_t cpl[NT + 1];            // control bytes before chunk t inside its warp
   uint16_t lk[2][NT];              // long string field (item) continuing in / starting in chunk t
@@ -1431,6 +1544,7 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
   const uint32_t toff = uint32_t(reinterpret_cast<uintptr_t>(P.in) & 15u);
   for (int k = t; k < 256 * 32; k += NTF) lut_s[k] = P.lut[k >> 5];
   for (int k = t; k < 256; k += NTF) S.lut1[k] = P.lut[k];
+  for (int k = t; k < 0x80; k += NTF) S.sym_b2g[k] = P.sym_b2g[k];
   if (t < PP_MAX_COLS) { S.coltype[t] = P.coltype[t]; S.inf[t] = 0; }
   if (t < ppi::MAX_STR_COLS) S.carry[t] = 0;
   if (t == 0) {
@@ -1534,10 +1648,34 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
     const uint32_t cstart = uint32_t(t) * CB;
     const uint32_t clen = tile_len > cstart ? min(tile_len - cstart, uint32_t(CB)) : 0u;
     const uint8_t* own = tile_s + cstart;
+    const uint8_t* dfa_s = tile_s;  // what the DFA reads: the bytes, or their symbol codes
+    if (P.enc) {
+      // a chunk of one-byte UTF-8 symbols is its own codes
+      bool plain = P.enc == PP_ENC_UTF8 && clen == CB;
+      if (plain) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) plain &= (w[k] & 0x80808080u) == 0;
+        const uint64_t nx = tile_base + cstart + CB;
+        if (plain && nx < P.n)
+          plain = !is_cont(cstart + CB < tile_len ? uint32_t(tile_s[cstart + CB]) : uint32_t(__ldg(P.in + nx)));
+      }
+      if (!plain) {
+        uint8_t* codes_s = stage_s;  // free until the warps list their terminators
+        chunk_codes(P, S.sym_b2g, tile_s, tile_base, tile_len, cstart, clen, codes_s);
+        if (clen == CB) {
+          const uint4* c4 = reinterpret_cast<const uint4*>(codes_s + cstart);
+          const uint4 x = c4[0], y = c4[1];
+          w[0] = x.x; w[1] = x.y; w[2] = x.z; w[3] = x.w;
+          w[4] = y.x; w[5] = y.y; w[6] = y.z; w[7] = y.w;
+        }
+        own = codes_s + cstart;
+        dfa_s = codes_s;
+      }
+    }
 
     // ---- chunk start states and tags (ParPaRaw Section 3.1)
     uint32_t G, special, special_x;
-    stv_pass(w, clen, tile_s, cstart, my_lut, G, special, special_x);
+    stv_pass(w, clen, dfa_s, cstart, my_lut, G, special, special_x);
     const uint32_t lane_ex = block_stv_w(G, S.warp_stv);
     const uint32_t st = stv_apply(lane_ex, stv_apply(S.warp_stv[warp], s_tile));
     const Tags g = tag_chunk(st, special, special_x, P.sticky, clen, cstart, own, my_lut,
@@ -1966,9 +2104,17 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
           const uint32_t v = slot_s[c * nrp + (r - lo)];
           const uint32_t ty = S.coltype[c];
           if ((v >> 16) == REL_START || (v & 0xFFFFu) - (v >> 16) > LONG_NUM) {
-            // a long field goes to a warp (the queue permitting)
+            // a long field goes to a warp (the queue permitting); so does,
+            // with an encoding, a field begun in an earlier tile (its bytes
+            // before the tile need symbol decoding)
             const uint32_t fsr = v >> 16, fe = v & 0xFFFFu;
             const uint64_t span = fsr == REL_START ? X.tile_base + fe - X.tile_fstart : fe - fsr;
+            if (P.enc && v != SLOT_DEFAULT && fsr == REL_START) {
+              const uint32_t q = atomicAdd(&P.s.counters[5], 1u);  // at most one per tile
+              P.s.long_q[P.s.long_cap + q] = ppi::LongField{rec, X.tile_fstart, X.tile_base + fe,
+                                                            c | (ty << 8)};
+              continue;
+            }
             if (v != SLOT_DEFAULT && span > LONG_NUM && ty != PP_COL_TIMESTAMP &&
                 ty != ppi::COL_INFER && P.s.long_q) {
               const uint32_t q = atomicAdd(&P.s.counters[4], 1u);
@@ -2247,7 +2393,7 @@ __global__ void parse_init_kernel(ParseParams P) {
   if (s.c_flag)
     for (uint32_t i = i0; i < P.n_tiles; i += stride) s.c_flag[i] = 0;
   for (uint32_t i = i0; i < s.n_tstate_blocks; i += stride) s.tstate_words[i] = 0;
-  if (i0 < 5) s.counters[i0] = 0;
+  if (i0 < 6) s.counters[i0] = 0;
   if (i0 == 0) {
     pp_status* st = P.st;
     st->error = 0;
@@ -2420,15 +2566,16 @@ uint32_t long_cap(uint32_t n) {
   return uint32_t(std::min<uint64_t>(ppi::LONG_CAP, uint64_t(n) * (TILE / LONG_NUM + 1)));
 }
 
-size_t parse_scratch_bytes(uint32_t n, int ns) {
+size_t parse_scratch_bytes(uint32_t n, int ns, bool sym) {
   const uint32_t nt = (n + TS_TILES - 1) / TS_TILES;
   const int k3 = ns > 0 ? ns : 1;
+  const size_t nq = size_t(long_cap(n)) + (sym ? n : 0u);
   return 256 + align256(size_t(n) * 4) + align256(n) + align256(size_t(nt) * 8) +
-         align256(size_t(n) * 16) + align256(size_t(long_cap(n)) * sizeof(ppi::LongField)) +
+         align256(size_t(n) * 16) + align256(nq * sizeof(ppi::LongField)) +
          (ns > 0 ? align256(size_t(n) * 4) + 2 * align256(size_t(n) * k3 * 8) : 0);
 }
 
-void parse_scratch_carve(void* base, uint32_t n, int ns, ParseScratch* o) {
+void parse_scratch_carve(void* base, uint32_t n, int ns, ParseScratch* o, bool sym) {
   const int k3 = ns > 0 ? ns : 1;
   uint8_t* p = static_cast<uint8_t*>(base);
   *o = ParseScratch{};
@@ -2441,7 +2588,7 @@ void parse_scratch_carve(void* base, uint32_t n, int ns, ParseScratch* o) {
   o->v2_desc = reinterpret_cast<uint64_t*>(p); p += align256(size_t(n) * 16);
   o->long_cap = long_cap(n);
   o->long_q = reinterpret_cast<ppi::LongField*>(p);
-  p += align256(size_t(o->long_cap) * sizeof(ppi::LongField));
+  p += align256((size_t(o->long_cap) + (sym ? n : 0u)) * sizeof(ppi::LongField));
   if (ns > 0) {
     o->c_flag = reinterpret_cast<uint32_t*>(p); p += align256(size_t(n) * 4);
     o->c_agg = reinterpret_cast<uint64_t*>(p); p += align256(size_t(n) * k3 * 8);

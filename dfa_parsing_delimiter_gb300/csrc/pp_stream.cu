@@ -218,7 +218,9 @@ pp_rc pp_parse_host(const uint8_t* h_in, size_t n_bytes, const pp_dfa_desc* dfa,
                     const size_t chars_capacity[], pp_status* h_status, size_t chunk_bytes,
                     cudaStream_t stream) {
   // the arguments are checked as pp_parse checks them (host pointers stand
-  // in for the device ones)
+  // in for the device ones); inputs in a multi-byte encoding are not
+  // streamed (a chunk could end inside a symbol)
+  if (dfa && dfa->encoding != PP_ENC_BYTES) return PP_EINVAL;
   ppi::ParseParams p0;
   pp_rc rc = ppi::parse_prepare(h_in, n_bytes, dfa, n_cols, col_types, h_offsets, h_chars, h_typed,
                                 records_capacity, chars_capacity, h_status, &p0);

@@ -99,9 +99,33 @@ typedef enum {
 #define PP_ERR_FATAL (PP_ERR_INVALID_INPUT | PP_ERR_BAD_END_STATE | \
                       PP_ERR_CAPACITY | PP_ERR_LOOKBACK_TIMEOUT)
 
-/* Description of a DFA over bytes (ParPaRaw Section 5, Table 1: symbols
- * with identical transitions are collapsed into symbol groups, and the
- * transition table is stored with one row per symbol group).             */
+/* Symbol encodings of the input (ParPaRaw Section 3.4: with a
+ * variable-length encoding a symbol spans several bytes and may cross chunk
+ * boundaries).
+ *   PP_ENC_BYTES    every byte is a symbol (the default).
+ *   PP_ENC_UTF8     a symbol is a byte that is not 0b10xxxxxx together with
+ *                   the 0b10xxxxxx bytes after it; it is well formed if it
+ *                   has the length its first byte announces, is not an
+ *                   overlong form and is at most 0x10FFFF.
+ *   PP_ENC_UTF16LE  2-byte little-endian units from the input's first byte;
+ *                   a high surrogate followed by a low surrogate is one
+ *                   4-byte symbol; an odd last byte is a symbol of its own.
+ * With an encoding the DFA takes one transition per symbol, at the symbol's
+ * last byte, so every offset the library reports for a symbol (a record
+ * delimiter, an invalid transition) is that of its last byte.  A value
+ * keeps all bytes of its value symbols; the other bytes of a multi-byte
+ * delimiter or control symbol are dropped like a control symbol.
+ * Symbol groups: a code point below 0x80 takes byte_to_group[code point],
+ * the code points listed in sym_cp take sym_group, and every other symbol
+ * (ill-formed ones too) takes byte_to_group[0x80].                        */
+#define PP_ENC_BYTES 0
+#define PP_ENC_UTF8 1
+#define PP_ENC_UTF16LE 2
+#define PP_MAX_SYMS 8
+
+/* Description of a DFA over bytes or symbols (ParPaRaw Section 5, Table 1:
+ * symbols with identical transitions are collapsed into symbol groups, and
+ * the transition table is stored with one row per symbol group).          */
 typedef struct {
   uint8_t n_states;       /* |S|, 1..16                                    */
   uint8_t n_groups;       /* symbol groups, 1..16                          */
@@ -111,7 +135,12 @@ typedef struct {
   uint8_t background_group; /* a group whose transition is idempotent and
                                whose bytes are never delimiters/controls, or
                                0xFF; lets the tagger skip runs of it        */
-  uint8_t reserved;
+  uint8_t encoding;       /* PP_ENC_*: pp_parse, pp_parse_ex (without
+                             skipped rows) and pp_parse_noalloc take every
+                             encoding, with string, integer, float and skip
+                             columns; the other entry points, and timestamp
+                             columns, take PP_ENC_BYTES only (else
+                             PP_EINVAL)                                    */
   uint8_t byte_to_group[256];
   uint8_t delta[PP_MAX_GROUPS][PP_MAX_STATES]; /* delta[group][state]       */
   uint8_t tag[PP_MAX_STATES][PP_MAX_GROUPS];   /* tag[state_before][group]  */
@@ -119,6 +148,12 @@ typedef struct {
    * 0xFE means "take byte_token_id[first byte of the token]"             */
   uint8_t token_id[PP_MAX_STATES];
   uint8_t byte_token_id[256];
+  /* encodings other than PP_ENC_BYTES: code points of at least 0x80 with a
+   * group of their own (distinct, at most 0x10FFFF, no surrogates)        */
+  uint8_t n_syms;
+  uint8_t sym_group[PP_MAX_SYMS];
+  uint8_t reserved2[3];
+  uint32_t sym_cp[PP_MAX_SYMS];
 } pp_dfa_desc;
 
 /* Device-resident result status.  The caller allocates it; every call
@@ -414,6 +449,14 @@ pp_rc pp_infer_types(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa
  * Accepting end states: EOR, FLD, ESC.  Host only.
  */
 pp_rc pp_desc_csv(pp_dfa_desc* out, uint8_t fd, uint8_t rd, uint8_t quote);
+
+/*
+ * pp_desc_csv_enc — the same quoted-CSV DFA over the symbols of a
+ * variable-length encoding (encoding PP_ENC_UTF8 or PP_ENC_UTF16LE; ParPaRaw
+ * Section 3.4): fd, rd and quote are code points (distinct, at most
+ * 0x10FFFF, no surrogates), any of them may take several bytes.  Host only.
+ */
+pp_rc pp_desc_csv_enc(pp_dfa_desc* out, int encoding, uint32_t fd, uint32_t rd, uint32_t quote);
 
 /*
  * pp_desc_csv_crlf — the same DFA for CRLF line ends: the record delimiter

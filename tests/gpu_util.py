@@ -48,11 +48,18 @@ def desc_rd(desc):
 
 
 def compare_csv(data, col_types, desc=None, offset=0, fd=b",", rd=b"\n", quote=b'"',
-                crlf=False):
-    """Parse with both; assert identical status and columns.  Returns status."""
-    desc = desc or (pp.desc_csv_crlf(fd, quote) if crlf else pp.desc_csv(fd, rd, quote))
-    out, st = run_gpu_csv(data, col_types, desc=desc, offset=offset)
-    ref, rst = O.csv_parse(data, col_types, fd=fd, rd=rd, quote=quote, crlf=crlf)
+                crlf=False, encoding=None):
+    """Parse with both; assert identical status and columns.  Returns status.
+    With `encoding` ("utf-8", "utf-16-le") fd, rd and quote are characters."""
+    if encoding:
+        desc = pp.desc_csv_enc(encoding, fd, rd, quote)
+        out, st = run_gpu_csv(data, col_types, desc=desc, offset=offset,
+                              records_capacity=len(data) + 1)
+        ref, rst = O.csv_parse(data, col_types, fd=fd, rd=rd, quote=quote, encoding=encoding)
+    else:
+        desc = desc or (pp.desc_csv_crlf(fd, quote) if crlf else pp.desc_csv(fd, rd, quote))
+        out, st = run_gpu_csv(data, col_types, desc=desc, offset=offset)
+        ref, rst = O.csv_parse(data, col_types, fd=fd, rd=rd, quote=quote, crlf=crlf)
     assert st["error"] == rst["error"], (st, rst)
     assert st["first_error_offset"] == rst["first_error_offset"], (st, rst)
     if st["error"] & O.FATAL:

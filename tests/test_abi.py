@@ -32,7 +32,7 @@ def test_exports_every_declared_symbol():
 
 
 def test_struct_sizes():
-    assert ctypes.sizeof(pp.DfaDesc) == 8 + 256 + 256 + 256 + 16 + 256
+    assert ctypes.sizeof(pp.DfaDesc) == 8 + 256 + 256 + 256 + 16 + 256 + 12 + 4 * 8
     assert pp.STATUS_BYTES == 32 + 8 * 64 + 8  # + n_dropped
 
 
@@ -152,3 +152,23 @@ def test_oracle_package_is_not_imported_by_library():
     for f in os.listdir(os.path.join(ROOT, "dfa_parsing_delimiter_gb300", "csrc")):
         text = open(os.path.join(ROOT, "dfa_parsing_delimiter_gb300", "csrc", f)).read()
         assert "pp_oracle" not in text and "or_csv_parse" not in text
+
+
+def test_encoded_csv_descriptor():
+    """pp_desc_csv_enc: the byte CSV DFA's table, with quote, field and
+    record delimiter as code points (ASCII ones through byte_to_group, the
+    others through the symbol table); bad code points are refused."""
+    b = pp.desc_csv()
+    d = pp.desc_csv_enc("utf-8", "\u00a7", "\u2028", '"')
+    assert d.encoding == pp.ENC_UTF8 and d.n_syms == 2
+    assert [(d.sym_cp[k], d.sym_group[k]) for k in range(2)] == [(0xA7, 1), (0x2028, 2)]
+    assert d.byte_to_group[ord('"')] == 0 and d.byte_to_group[ord(",")] == 3
+    assert d.byte_to_group[0x80] == 3 and d.byte_to_group[10] == 3
+    for g in range(4):
+        for st in range(5):
+            assert d.delta[g][st] == b.delta[g][st] and d.tag[st][g] == b.tag[st][g]
+    u = pp.desc_csv_enc("utf-16-le")
+    assert u.encoding == pp.ENC_UTF16LE and u.n_syms == 0 and u.byte_to_group[ord(",")] == 1
+    for bad in ((0xD800, 10, 34), (44, 44, 34), (0x110000, 10, 34)):
+        with pytest.raises(RuntimeError):
+            pp.desc_csv_enc("utf-8", *bad)
