@@ -1527,7 +1527,8 @@ __device__ void chars_role(const ParseParams& P, PShared& S) {
 }
 
 // ----------------------------------------------------------------- kernel
-template <int NS>
+// SYM: an input in an encoding (symbol codes; see sym_code)
+template <int NS, bool SYM>
 __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_constant__ ParseParams P) {
   constexpr int NTF = ntf_of<NS>();
   constexpr int NSW = NS > 0 ? (NS + 3) / 4 : 1;
@@ -1649,7 +1650,7 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
     const uint32_t clen = tile_len > cstart ? min(tile_len - cstart, uint32_t(CB)) : 0u;
     const uint8_t* own = tile_s + cstart;
     const uint8_t* dfa_s = tile_s;  // what the DFA reads: the bytes, or their symbol codes
-    if (P.enc) {
+    if (SYM) {
       // a chunk of one-byte UTF-8 symbols is its own codes
       bool plain = P.enc == PP_ENC_UTF8 && clen == CB;
       if (plain) {
@@ -2103,13 +2104,13 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
           if (rec >= P.rec_cap) { report(P.st, PP_ERR_CAPACITY, 0, false); continue; }
           const uint32_t v = slot_s[c * nrp + (r - lo)];
           const uint32_t ty = S.coltype[c];
-          if ((v >> 16) == REL_START || (v & 0xFFFFu) - (v >> 16) > LONG_NUM) {
+          if ((v & 0xFFFFu) - (v >> 16) > LONG_NUM) {  // (wraps for REL_START and SLOT_DEFAULT)
             // a long field goes to a warp (the queue permitting); so does,
             // with an encoding, a field begun in an earlier tile (its bytes
             // before the tile need symbol decoding)
             const uint32_t fsr = v >> 16, fe = v & 0xFFFFu;
             const uint64_t span = fsr == REL_START ? X.tile_base + fe - X.tile_fstart : fe - fsr;
-            if (P.enc && v != SLOT_DEFAULT && fsr == REL_START) {
+            if (SYM && v != SLOT_DEFAULT && fsr == REL_START) {
               const uint32_t q = atomicAdd(&P.s.counters[5], 1u);  // at most one per tile
               P.s.long_q[P.s.long_cap + q] = ppi::LongField{rec, X.tile_fstart, X.tile_base + fe,
                                                             c | (ty << 8)};
@@ -2416,7 +2417,7 @@ uint32_t init_grid(uint32_t n) {
 // and its resident blocks per SM.
 struct Occ { int blocks = 1, n_sm = 0; };
 
-template <int NS>
+template <int NS, bool SYM>
 cudaError_t parse_setup(Occ** out) {
   static ppi::DeviceOnce once;
   static Occ occ[ppi::MAX_DEVICES];
@@ -2427,11 +2428,11 @@ cudaError_t parse_setup(Occ** out) {
     Occ o;
     cudaError_t r;
     if ((r = ppi::sm_count(&o.n_sm)) != cudaSuccess) return r;
-    if ((r = cudaFuncSetAttribute(parse_kernel<NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if ((r = cudaFuncSetAttribute(parse_kernel<NS, SYM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   int(PARSE_SMEM))) != cudaSuccess)
       return r;
     int b = 0;
-    if ((r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, parse_kernel<NS>, ntf_of<NS>(),
+    if ((r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, parse_kernel<NS, SYM>, ntf_of<NS>(),
                                                            PARSE_SMEM)) != cudaSuccess)
       return r;
     o.blocks = b > 0 ? b : 1;
@@ -2442,10 +2443,10 @@ cudaError_t parse_setup(Occ** out) {
   return e;
 }
 
-template <int NS>
+template <int NS, bool SYM>
 cudaError_t launch_ns(const ParseParams& p, cudaStream_t stream) {
   Occ* po = nullptr;
-  cudaError_t e = parse_setup<NS>(&po);
+  cudaError_t e = parse_setup<NS, SYM>(&po);
   if (e != cudaSuccess) return e;
   const Occ& occ = *po;
   const bool timed = ppi::stage_begin();
@@ -2465,7 +2466,7 @@ cudaError_t launch_ns(const ParseParams& p, cudaStream_t stream) {
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const uint32_t g = uint32_t(std::min<uint64_t>(std::max<uint32_t>(p.n_tiles, 1),
                                                  uint64_t(occ.n_sm) * occ.blocks));
-  if (p.n_tiles) parse_kernel<NS><<<g, ntf_of<NS>(), PARSE_SMEM, stream>>>(p);
+  if (p.n_tiles) parse_kernel<NS, SYM><<<g, ntf_of<NS>(), PARSE_SMEM, stream>>>(p);
   if (timed) ppi::stage_mark(4, stream);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // the long numeric fields the tile pass queued (an empty queue costs a
@@ -2598,10 +2599,10 @@ void parse_scratch_carve(void* base, uint32_t n, int ns, ParseScratch* o, bool s
 
 cudaError_t launch_parse(const ParseParams& p, cudaStream_t stream) {
   switch (parse_ns_width(p.n_str)) {
-    case 0: return launch_ns<0>(p, stream);
-    case 4: return launch_ns<4>(p, stream);
-    case 8: return launch_ns<8>(p, stream);
-    default: return launch_ns<16>(p, stream);
+    case 0: return p.enc ? launch_ns<0, true>(p, stream) : launch_ns<0, false>(p, stream);
+    case 4: return p.enc ? launch_ns<4, true>(p, stream) : launch_ns<4, false>(p, stream);
+    case 8: return p.enc ? launch_ns<8, true>(p, stream) : launch_ns<8, false>(p, stream);
+    default: return p.enc ? launch_ns<16, true>(p, stream) : launch_ns<16, false>(p, stream);
   }
 }
 

@@ -449,3 +449,23 @@ def test_count_fields_edges():
     compare_count_fields(b"a\n" * 9000 + b'x"y\n')         # a quote inside a field
     crlf = b"\r\n".join(b",".join(b"v" for _ in range(k % 7 + 1)) for k in range(5000)) + b"\r\n"
     compare_count_fields(crlf, crlf=True)
+
+
+@pytest.mark.parametrize("skew", [0, 1, 2])
+def test_parse_field_walk_both_ways(skew):
+    """A warp (1 KiB of input) lists its fields and takes a lane per field,
+    unless it has more than 512 of them (runs of empty fields), when it
+    walks a chunk per lane.  Both against the oracle, on inputs mixing the
+    two within and across tiles."""
+    rng = random.Random(40 + skew)
+    parts = []
+    for i in range(4000):
+        r = rng.random()
+        if r < 0.02 * (skew + 1):
+            parts.append("," * rng.randint(600, 1500))                          # > 512 fields per warp
+        elif r < 0.1 * (skew + 1):
+            parts.append(",".join("x" * rng.randint(0, 2) for _ in range(40)))   # a crowd of fields
+        else:
+            parts.append("y" * rng.randint(100, 400) + "," + str(i))            # few, long fields
+    data = ("\n".join(parts) + "\n").encode()
+    compare_csv(data, ["str", "str", "str"])
