@@ -52,8 +52,10 @@ constexpr uint8_t COL_INFER = 7;  // internal column kind: type inference only
 //         flag and ns-word aggregate / inclusive prefix (null without string
 //         columns).
 // A numeric field queued for conversion by a warp (long fields): output row,
-// input byte range, column | type << 8.
-struct LongField { uint64_t rec, start, end; uint32_t col, pad; };
+// input byte range, column | type << 8, and the DFA state at its start
+// (LONG_STATE | state) when known, else 0 (found from its tile's start).
+struct LongField { uint64_t rec, start, end; uint32_t col, state; };
+constexpr uint32_t LONG_STATE = 0x80000000u;
 constexpr uint32_t LONG_CAP = 4096;  // queued fields per call, at most
 constexpr uint32_t SYM_LAST = 128, SYM_MID = 144;  // symbol codes (see ParseParams::enc)
 

@@ -522,10 +522,35 @@ __global__ void __launch_bounds__(TV_NT) tile_stv_kernel(const __grid_constant__
     const uint64_t b0 = uint64_t(tile) * TILE + uint64_t(lane) * TV_BYTES;
     const uint32_t len = b0 < P.n ? uint32_t(min(uint64_t(TV_BYTES), P.n - b0)) : 0u;
     uint32_t G = STV_ID;
-    if (P.enc) {  // symbols of an encoding: one code per byte
+    if (P.enc) {
+      // Symbols of an encoding: only a symbol's last byte moves the state
+      // (its other bytes have identity rows), so only last bytes are
+      // decoded.  UTF-8 blocks of 16 bytes below 0x80, not followed by a
+      // continuation byte, are their own codes and fold like bytes.
       auto B = [&](uint64_t q) -> uint32_t { return __ldg(P.in + q); };
-      for (int j = int(len) - 1; j >= 0; --j)
-        G = __byte_perm(G, STV_INV_POOL, my_lut[sym_code(P, b2g_s, b0 + j, B) << 5]);
+      auto fold_sym = [&](uint32_t G, uint64_t p) {
+        if (P.enc == PP_ENC_UTF8 ? (p + 1 < P.n && is_cont(B(p + 1)))
+                                 : ((p & 1u) == 0 && p + 1 < P.n))
+          return G;  // not the symbol's last byte
+        return __byte_perm(G, STV_INV_POOL, my_lut[sym_code(P, b2g_s, p, B) << 5]);
+      };
+      const bool vec = P.enc == PP_ENC_UTF8 && len == TV_BYTES &&
+                       (reinterpret_cast<uintptr_t>(P.in + b0) & 15u) == 0;
+      if (vec) {
+        const uint4* src = reinterpret_cast<const uint4*>(P.in + b0);
+        uint32_t next = b0 + TV_BYTES < P.n ? B(b0 + TV_BYTES) : 0u;  // the byte after the block
+        for (int k = TV_BYTES / 16 - 1; k >= 0; --k) {
+          const uint4 v = __ldg(src + k);
+          if ((((v.x | v.y | v.z | v.w) & 0x80808080u) == 0) && !is_cont(next)) {
+            G = fold16(G, v);
+          } else {
+            for (int j = 15; j >= 0; --j) G = fold_sym(G, b0 + 16u * uint32_t(k) + uint32_t(j));
+          }
+          next = v.x & 0xFFu;
+        }
+      } else {
+        for (int j = int(len) - 1; j >= 0; --j) G = fold_sym(G, b0 + uint32_t(j));
+      }
     } else if (len == TV_BYTES) {
       const uint8_t* p = P.in + b0;
       for (int j = int(tl) - 1; j >= 0; --j)  // the tail
@@ -854,8 +879,11 @@ __device__ void convert_long(const ParseParams& P, const uint32_t* lut, const pp
   auto code_at = [&](uint64_t q, uint32_t b) -> uint32_t {  // the LUT index of byte q (value b)
     return P.enc ? sym_code_global(P, q) : b;
   };
-  const uint64_t t0 = (gs / TILE) * TILE;  // the DFA state there is known
-  uint32_t cs = P.s.tile_state[gs / TILE];  // CSV state at the round start
+  // where the walk starts: the field's start when its DFA state is known,
+  // else the start of its tile (whose state the tile-state scan gave)
+  const bool known = (f.state & ppi::LONG_STATE) != 0;
+  const uint64_t t0 = known ? gs : (gs / TILE) * TILE;
+  uint32_t cs = known ? (f.state & 0xFFu) : P.s.tile_state[gs / TILE];  // CSV state at the round start
   uint32_t gq = G0;                         // grammar state at the round start
   uint64_t n_int = 0, n_frac = 0, n_val = 0;
   uint64_t z = NONE, pz = NONE, pez = NONE;  // first non-zero mantissa digit (index, position), exponent digit
@@ -2113,15 +2141,18 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
             if (SYM && v != SLOT_DEFAULT && fsr == REL_START) {
               const uint32_t q = atomicAdd(&P.s.counters[5], 1u);  // at most one per tile
               P.s.long_q[P.s.long_cap + q] = ppi::LongField{rec, X.tile_fstart, X.tile_base + fe,
-                                                            c | (ty << 8)};
+                                                            c | (ty << 8),
+                                                            ppi::LONG_STATE | X.tile_fstate};
               continue;
             }
             if (v != SLOT_DEFAULT && span > LONG_NUM && ty != PP_COL_TIMESTAMP &&
                 ty != ppi::COL_INFER && P.s.long_q) {
               const uint32_t q = atomicAdd(&P.s.counters[4], 1u);
               if (q < P.s.long_cap) {
-                P.s.long_q[q] = ppi::LongField{rec, fsr == REL_START ? X.tile_fstart : X.tile_base + fsr,
-                                               X.tile_base + fe, c | (ty << 8)};
+                P.s.long_q[q] = fsr == REL_START
+                    ? ppi::LongField{rec, X.tile_fstart, X.tile_base + fe, c | (ty << 8),
+                                     ppi::LONG_STATE | X.tile_fstate}
+                    : ppi::LongField{rec, X.tile_base + fsr, X.tile_base + fe, c | (ty << 8), 0u};
                 continue;
               }
             }
