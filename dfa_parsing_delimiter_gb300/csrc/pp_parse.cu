@@ -1447,6 +1447,33 @@ __device__ __forceinline__ uint32_t ctrl_bef(const uint32_t* ctrl_s, const PShar
   const uint32_t c = p >> 5, b = p & 31u;
   return S.wc[c >> 5] + S.cpl[c] + (b ? uint32_t(__popc(ctrl_s[c] & ((1u << b) - 1u))) : 0u);
 }
+// Copy tile bytes [p, p + len) to dst[d ...] (staging): bytes up to the
+// next 4-byte boundary of the destination, then whole words built from two
+// source words by a funnel shift (raw_w: the landing buffer as words, tile
+// byte p at byte p + toff; it has slack for the word after the last), then
+// the last bytes.
+__device__ __forceinline__ void copy_run(uint8_t* dst, uint32_t d, const uint8_t* tile_s,
+                                         const uint32_t* raw_w, uint32_t toff, uint32_t p,
+                                         uint32_t len) {
+  for (; len && (d & 3u); --len) dst[d++] = tile_s[p++];
+  const uint32_t nw = len >> 2;
+  if (nw) {
+    uint32_t* dw = reinterpret_cast<uint32_t*>(dst + d);
+    const uint32_t a = p + toff, sh = (a & 3u) * 8u;
+    const uint32_t* sw = raw_w + (a >> 2);
+    uint32_t lo = sw[0];
+    for (uint32_t i = 0; i < nw; ++i) {
+      const uint32_t hi = sw[i + 1];
+      dw[i] = __funnelshift_r(lo, hi, sh);
+      lo = hi;
+    }
+    d += 4 * nw;
+    p += 4 * nw;
+    len -= 4 * nw;
+  }
+  for (; len; --len) dst[d++] = tile_s[p++];
+}
+
 // value bytes of the field [fs, e) inside the tile (fs = REL_START: from 0)
 __device__ __forceinline__ uint32_t value_len(uint32_t fs, uint32_t e, bool any_ctrl,
                                               const uint32_t* ctrl_s, const PShared& S) {
@@ -2101,11 +2128,17 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
             const uint32_t len = (e - a0) - (c_e - c_a0);
             uint32_t dst = pos_s[k] - len + (p0 - a0) - (c_p0 - c_a0);
             const uint32_t cm = g.ctrl & range_mask(p0 - cstart, p1 - cstart);
-            if (!cm) {
-              for (uint32_t p = p0; p < p1; ++p) stage_s[dst++] = tile_s[p];
-            } else {
-              for (uint32_t p = p0; p < p1; ++p)
-                if (!((cm >> (p - cstart)) & 1u)) stage_s[dst++] = tile_s[p];
+            // the runs between control bytes
+            uint32_t q = p0, mm = cm;
+            while (q < p1) {
+              const uint32_t nx = mm ? cstart + uint32_t(__ffs(mm)) - 1u : p1;  // next control byte
+              if (nx > q) {
+                copy_run(stage_s, dst, tile_s, raw_w, toff, q, nx - q);
+                dst += nx - q;
+              }
+              if (!mm) break;
+              mm &= mm - 1u;
+              q = nx + 1u;
             }
           }
         }
