@@ -1172,7 +1172,6 @@ __device__ __forceinline__ bool rec_skip_listed(const ParseParams& P, uint64_t r
 // mostly posted their aggregates by the time it looks back.
 constexpr int BUF_BYTES = TILE + 64;      // landing buffer: the tile at toff, slack for word reads
 constexpr uint32_t SHORT_FIELD = 32;      // longer string fields are staged chunk-parallel
-constexpr uint32_t WLIST_CAP = 512;       // terminators per warp listed in the staging buffer
 constexpr uint16_t NO_FIELD = 0xFFFFu;
 constexpr uint32_t REL_START = 0xFFFFu;   // slot start: the field began before the tile
 constexpr uint32_t BAR_W = 1, BAR_AGG = 2, BAR_W2 = 3, BAR_V2 = 4, BAR_CHR = 5;
@@ -1415,7 +1414,6 @@ struct PShared {
   uint32_t issued[2], wpar[2];   // bulk copy started, phase parity to wait for
   uint32_t warp_stv[NW];
   uint32_t wv[NW][3];            // per warp (records, column, last), then exclusive
-  uint32_t wt[NW];               // terminators per warp, then exclusive
   uint32_t wc[NW + 1];           // control bytes per warp, then exclusive; [NW] = tile total
   uint32_t wrd[NW];              // partial mode: 1 + the warp's last record delimiter
   uint32_t agg_rec, agg_col, agg_last, n_ctrl, virt;  // the tile's totals
@@ -1716,7 +1714,7 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
           plain = !is_cont(cstart + CB < tile_len ? uint32_t(tile_s[cstart + CB]) : uint32_t(__ldg(P.in + nx)));
       }
       if (!plain) {
-        uint8_t* codes_s = stage_s;  // free until the warps list their terminators
+        uint8_t* codes_s = stage_s;  // free until the strings are staged
         chunk_codes(P, S.sym_b2g, tile_s, tile_base, tile_len, cstart, clen, codes_s);
         if (clen == CB) {
           const uint4* c4 = reinterpret_cast<const uint4*>(codes_s + cstart);
@@ -1746,18 +1744,17 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
     const uint32_t fd = g.fd, rd = g.rd;
     ctrl_s[t] = g.ctrl;
 
-    // ---- (records, column, last), terminators and control bytes, scanned
-    // over the warp and then over the warps
+    // ---- (records, column, last) and control bytes, scanned over the warp
+    // and then over the warps
     V2 vi = chunk_v2(g);
-    const uint32_t t_own = __popc(fd | rd) + (virt_rd ? 1u : 0u), c_own = __popc(g.ctrl);
-    uint32_t ti = t_own, ci = c_own;
+    const uint32_t c_own = __popc(g.ctrl);
+    uint32_t ci = c_own;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
       const V2 o = shfl_up_v2(vi, d);
-      const uint32_t ot = __shfl_up_sync(FULL, ti, d), oc = __shfl_up_sync(FULL, ci, d);
+      const uint32_t oc = __shfl_up_sync(FULL, ci, d);
       if (lane >= d) {
         vi = op2_32(o, vi);
-        ti += ot;
         ci += oc;
       }
     }
@@ -1765,7 +1762,6 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
     if (lane == 0) vex = {0u, 0u, 0u};
     if (lane == 31) {
       S.wv[warp][0] = vi.rec; S.wv[warp][1] = vi.col; S.wv[warp][2] = vi.last;
-      S.wt[warp] = ti;
       S.wc[warp] = ci;
     }
     S.cpl[t] = uint16_t(ci - c_own);
@@ -1777,15 +1773,14 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
     bar_sync(BAR_W, NT);
     if (warp == 0) {
       V2 x = lane < NW ? V2{S.wv[lane][0], S.wv[lane][1], S.wv[lane][2]} : V2{0u, 0u, 0u};
-      const uint32_t t0 = lane < NW ? S.wt[lane] : 0u, c0 = lane < NW ? S.wc[lane] : 0u;
-      uint32_t xt = t0, xc = c0;
+      const uint32_t c0 = lane < NW ? S.wc[lane] : 0u;
+      uint32_t xc = c0;
 #pragma unroll
       for (int d = 1; d < NW; d <<= 1) {
         const V2 o = shfl_up_v2(x, d);
-        const uint32_t ot = __shfl_up_sync(FULL, xt, d), oc = __shfl_up_sync(FULL, xc, d);
+        const uint32_t oc = __shfl_up_sync(FULL, xc, d);
         if (lane >= d) {
           x = op2_32(o, x);
-          xt += ot;
           xc += oc;
         }
       }
@@ -1794,7 +1789,6 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
       __syncwarp();
       if (lane < NW) {
         S.wv[lane][0] = xe.rec; S.wv[lane][1] = xe.col; S.wv[lane][2] = xe.last;
-        S.wt[lane] = xt - t0;
         S.wc[lane] = xc - c0;
       }
       if (lane == NW - 1) {
@@ -1822,8 +1816,6 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
     const uint32_t fs0 = pre.last ? (pre.last >> 8) : REL_START;  // start of the field open there
     const uint32_t term_all = fd | rd;
     const bool owns_tail = clen > 0 && cstart + clen == tile_len;
-    const uint32_t tbase = ti - t_own;
-    const uint32_t wn = __shfl_sync(FULL, ti, 31);
 
     // filled after the look-back
     uint64_t rec0 = 0;
@@ -1872,49 +1864,13 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
             for (uint32_t c = col + 1; c < n_cols; ++c) slot_s[c * nrp + (rl - lo)] = SLOT_DEFAULT;
         }
       };
-      // The warp's fields in input order, each passed to act(row, column
-      // (row 0: index), start, end, ends a record, still open).
-      const bool listed = wn <= WLIST_CAP;
-      uint16_t* const wl = reinterpret_cast<uint16_t*>(stage_s) + warp * WLIST_CAP;
-      if (listed) {
-        // the warp's terminators in input order (tile position | RD << 15)
-        uint32_t m = term_all, i = tbase;
-        while (m) {
-          const uint32_t j = __ffs(m) - 1;
-          m &= m - 1;
-          wl[i++] = uint16_t((cstart + j) | (((rd >> j) & 1u) << 15));
-        }
-        if (virt_rd) wl[i] = uint16_t(tile_len | 0x8000u);
-        __syncwarp();
-      }
+      // The fields of the lane's chunk in input order, each passed to
+      // act(row, column (row 0: index), start, end, ends a record, still
+      // open): a lane per chunk walks its terminators.  (A lane per field,
+      // from a list of the warp's terminators, was measured 1-3 % slower:
+      // fields spread evenly enough over the chunks.)
       auto walk = [&](auto&& act) {
-        if (listed) {
-          // a lane per field: row and column from a ballot of the RDs
-          uint32_t crow = __shfl_sync(FULL, rl0, 0), ccol = __shfl_sync(FULL, col0, 0),
-                   cfs = __shfl_sync(FULL, fs0, 0);
-          const uint32_t lt = (1u << lane) - 1u;
-          for (uint32_t b0 = 0; b0 < wn; b0 += 32) {
-            const uint32_t k = b0 + uint32_t(lane);
-            const uint32_t ent = k < wn ? uint32_t(wl[k]) : 0u;
-            const uint32_t e = ent & 0x7FFFu;
-            const bool isrd = (ent >> 15) != 0;
-            const uint32_t pe = __shfl_up_sync(FULL, e, 1);
-            const uint32_t fs = lane == 0 ? cfs : pe + 1u;
-            const uint32_t rdm = __ballot_sync(FULL, k < wn && isrd);
-            const uint32_t below = rdm & lt;
-            const uint32_t rl = crow + __popc(below);
-            const uint32_t col = below ? uint32_t(lane) - (32u - __clz(below))
-                                       : min(ccol + uint32_t(lane), 0x7FFFFF00u);
-            if (k < wn) act(rl, col, fs, e, isrd, false);
-            const uint32_t nin = min(32u, wn - b0);
-            crow += __popc(rdm);
-            ccol = rdm ? (nin - 1u) - (31u - __clz(rdm)) : min(ccol + nin, 0x7FFFFF00u);
-            cfs = __shfl_sync(FULL, e, nin - 1) + 1u;
-          }
-          // the field still open at the tile end (its value bytes are counted
-          // and staged here)
-          if (owns_tail && !any_virt) act(crow, ccol, cfs, tile_len, false, true);
-        } else {  // each lane walks its chunk's fields
+        {
           uint32_t term = term_all, col = col0, rl = rl0, fs = fs0;
           bool vrd = virt_rd;
           for (;;) {

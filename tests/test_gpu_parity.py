@@ -452,11 +452,10 @@ def test_count_fields_edges():
 
 
 @pytest.mark.parametrize("skew", [0, 1, 2])
-def test_parse_field_walk_both_ways(skew):
-    """A warp (1 KiB of input) lists its fields and takes a lane per field,
-    unless it has more than 512 of them (runs of empty fields), when it
-    walks a chunk per lane.  Both against the oracle, on inputs mixing the
-    two within and across tiles."""
+def test_parse_crowded_and_sparse_fields(skew):
+    """Chunks crowded with fields (runs of empty fields, 32 terminators in a
+    chunk) next to chunks inside long fields, within and across tiles: each
+    lane walks its chunk's terminators, however unevenly they are spread."""
     rng = random.Random(40 + skew)
     parts = []
     for i in range(4000):
