@@ -1240,7 +1240,9 @@ __device__ __forceinline__ void load_chunk(const uint8_t* buf, uint32_t toff, ui
 
 // Chunk vectors composed over the worker warps (block_stv with the workers'
 // barrier).
-__device__ __forceinline__ uint32_t block_stv_w(uint32_t G, uint32_t* warp_stv) {
+// wex: the composition of the warps before this one, which every warp
+// computes itself after the one barrier.
+__device__ __forceinline__ uint32_t block_stv_w(uint32_t G, uint32_t* warp_stv, uint32_t& wex) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t inc = G;
 #pragma unroll
@@ -1252,19 +1254,14 @@ __device__ __forceinline__ uint32_t block_stv_w(uint32_t G, uint32_t* warp_stv) 
   if (lane == 0) lane_ex = STV_ID;
   if (lane == 31) warp_stv[warp] = inc;
   bar_sync(BAR_W, NT);
-  if (warp == 0) {
-    const uint32_t v = lane < NW ? warp_stv[lane] : STV_ID;
-    uint32_t wi = v;
+  uint32_t wi = lane < warp ? warp_stv[lane] : STV_ID;
 #pragma unroll
-    for (int d = 1; d < NW; d <<= 1) {
-      const uint32_t o = __shfl_up_sync(FULL, wi, d);
-      if (lane >= d) wi = stv_compose(o, wi);
-    }
-    uint32_t wex = __shfl_up_sync(FULL, wi, 1);
-    if (lane == 0) wex = STV_ID;
-    if (lane < NW) warp_stv[lane] = wex;
+  for (int d = 1; d < NW; d <<= 1) {
+    const uint32_t o = __shfl_up_sync(FULL, wi, d);
+    if (lane >= d) wi = stv_compose(o, wi);
   }
-  bar_sync(BAR_W, NT);
+  wex = __shfl_sync(FULL, wi, warp > 0 ? warp - 1 : 0);
+  if (warp == 0) wex = STV_ID;
   return lane_ex;
 }
 
@@ -1730,8 +1727,9 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
     // ---- chunk start states and tags (ParPaRaw Section 3.1)
     uint32_t G, special, special_x;
     stv_pass(w, clen, dfa_s, cstart, my_lut, G, special, special_x);
-    const uint32_t lane_ex = block_stv_w(G, S.warp_stv);
-    const uint32_t st = stv_apply(lane_ex, stv_apply(S.warp_stv[warp], s_tile));
+    uint32_t warp_ex;
+    const uint32_t lane_ex = block_stv_w(G, S.warp_stv, warp_ex);
+    const uint32_t st = stv_apply(lane_ex, stv_apply(warp_ex, s_tile));
     const Tags g = tag_chunk(st, special, special_x, P.sticky, clen, cstart, own, my_lut,
                              P.bg_next);
     if (g.inv_at < clen && st != 4)
@@ -2019,21 +2017,11 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
         }
         if (lane == 31) S.wsum[warp] = xi;
         bar_sync(BAR_W, NT);
-        if (warp == 0) {
-          const uint32_t v = lane < NW ? S.wsum[lane] : 0u;
-          uint32_t x = v;
-#pragma unroll
-          for (int d = 1; d < NW; d <<= 1) {
-            const uint32_t o = __shfl_up_sync(FULL, x, d);
-            if (lane >= d) x += o;
-          }
-          __syncwarp();
-          if (lane < NW) S.wsum[lane] = x - v;
-          if (lane == NW - 1) S.cstart[n_str] = x;
-        }
-        bar_sync(BAR_W, NT);
-        {  // lengths -> chars end positions (inclusive prefix)
-          uint32_t run = S.wsum[warp] + xi - mysum;
+        {  // lengths -> chars end positions (inclusive prefix); every warp
+           // sums the warps before it itself
+          const uint32_t before = __reduce_add_sync(FULL, lane < warp ? S.wsum[lane] : 0u);
+          if (warp == NW - 1 && lane == 31) S.cstart[n_str] = before + xi;
+          uint32_t run = before + xi - mysum;
           uint32_t si = k0 / nr, r = k0 - si * nr;
           for (uint32_t k = k0; k < k1; ++k) {
             if (r == 0) S.cstart[si] = run;
