@@ -1577,8 +1577,10 @@ __device__ void chars_role(const ParseParams& P, PShared& S) {
 }
 
 // ----------------------------------------------------------------- kernel
-// SYM: an input in an encoding (symbol codes; see sym_code)
-template <int NS, bool SYM>
+// GEN: the general kernel, for inputs in an encoding (symbol codes; see
+// sym_code), the options of pp_parse_ex and type inference; the plain
+// kernel (byte inputs, every record emitted) carries none of that code.
+template <int NS, bool GEN>
 __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_constant__ ParseParams P) {
   constexpr int NTF = ntf_of<NS>();
   constexpr int NSW = NS > 0 ? (NS + 3) / 4 : 1;
@@ -1635,8 +1637,9 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
   const uint32_t n_str = NS > 0 ? uint32_t(P.n_str) : 0u;
   const uint32_t rpb = max(1u, (uint32_t(SLOT_CAP) - n_cols) / n_cols);  // rows per pass
   const bool partial = P.record_end != nullptr;
-  const bool emit = P.drop_bits != nullptr;    // some records are not emitted
-  const bool status = P.mark_bits != nullptr;  // the status pass of rejection
+  const bool emit = GEN && P.drop_bits != nullptr;    // some records are not emitted
+  const bool status = GEN && P.mark_bits != nullptr;  // the status pass of rejection
+  const bool infer = GEN && P.infer_out != nullptr;   // type inference
   // status pass: rows of the tile with a wrong field count (pos_s's space,
   // which only string staging uses)
   uint32_t* const flags_s = reinterpret_cast<uint32_t*>(pos_s);
@@ -1700,7 +1703,7 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
     const uint32_t clen = tile_len > cstart ? min(tile_len - cstart, uint32_t(CB)) : 0u;
     const uint8_t* own = tile_s + cstart;
     const uint8_t* dfa_s = tile_s;  // what the DFA reads: the bytes, or their symbol codes
-    if (SYM) {
+    if (GEN && P.enc) {
       // a chunk of one-byte UTF-8 symbols is its own codes
       bool plain = P.enc == PP_ENC_UTF8 && clen == CB;
       if (plain) {
@@ -1856,7 +1859,7 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
           if (L) add16(cnt, P.stridx[col], L);
         }
         if (isrd && !open && col != n_cols - 1) {
-          if (first && !emit && !P.infer_out) report(P.st, PP_ERR_COLCOUNT, tile_base + e, true);
+          if (first && !emit && !infer) report(P.st, PP_ERR_COLCOUNT, tile_base + e, true);
           if (first && status) atomicOr(&flags_s[rl >> 5], 1u << (rl & 31u));
           if (in_pass)  // missing fields take the column default
             for (uint32_t c = col + 1; c < n_cols; ++c) slot_s[c * nrp + (rl - lo)] = SLOT_DEFAULT;
@@ -1952,7 +1955,7 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
         if (S.rd0_pos) {
           const uint32_t nf = col_in + S.rd0_k + 1;  // fields of the record
           if (nf != n_cols) {
-            if (t == 0 && !(emit && rec_skip_listed(P, rec0)) && !P.infer_out)
+            if (t == 0 && !(emit && rec_skip_listed(P, rec0)) && !infer)
               report(P.st, PP_ERR_COLCOUNT, tile_base + S.rd0_pos - 1, true);
             if (t == 0 && status) atomicOr(&P.mark_bits[rec0 >> 5], 1u << (rec0 & 31u));
             for (uint32_t c = nf + t; c < n_cols; c += NT) slot_s[c * nrp] = SLOT_DEFAULT;
@@ -2115,7 +2118,7 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
             // before the tile need symbol decoding)
             const uint32_t fsr = v >> 16, fe = v & 0xFFFFu;
             const uint64_t span = fsr == REL_START ? X.tile_base + fe - X.tile_fstart : fe - fsr;
-            if (SYM && v != SLOT_DEFAULT && fsr == REL_START) {
+            if (GEN && P.enc && v != SLOT_DEFAULT && fsr == REL_START) {
               const uint32_t q = atomicAdd(&P.s.counters[5], 1u);  // at most one per tile
               P.s.long_q[P.s.long_cap + q] = ppi::LongField{rec, X.tile_fstart, X.tile_base + fe,
                                                             c | (ty << 8),
@@ -2142,8 +2145,10 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
             case PP_COL_TIMESTAMP: convert_store<PP_COL_TIMESTAMP>(P, X, out, rec, v, dflt); break;
             case PP_COL_INT32: convert_store<PP_COL_INT32>(P, X, out, rec, v, dflt); break;
             case ppi::COL_INFER: {
-              const uint32_t code = infer_field(P, v, X);
-              if (code) atomicMax(&S.inf[c], code);
+              if constexpr (GEN) {
+                const uint32_t code = infer_field(P, v, X);
+                if (code) atomicMax(&S.inf[c], code);
+              }
               break;
             }
             default: convert_store<PP_COL_INT8>(P, X, out, rec, v, dflt); break;
@@ -2210,7 +2215,7 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
       bar_sync(BAR_W, NT);
     }
     if (t < int(n_str)) S.carry[t] = 0;
-    if (P.infer_out && t < int(n_cols) && S.inf[t]) {  // this tile's types, to the input's
+    if (infer && t < int(n_cols) && S.inf[t]) {  // this tile's types, to the input's
       atomicMax(&P.infer_out[t], S.inf[t]);
       S.inf[t] = 0;
     }
@@ -2425,7 +2430,7 @@ uint32_t init_grid(uint32_t n) {
 // and its resident blocks per SM.
 struct Occ { int blocks = 1, n_sm = 0; };
 
-template <int NS, bool SYM>
+template <int NS, bool GEN>
 cudaError_t parse_setup(Occ** out) {
   static ppi::DeviceOnce once;
   static Occ occ[ppi::MAX_DEVICES];
@@ -2436,11 +2441,11 @@ cudaError_t parse_setup(Occ** out) {
     Occ o;
     cudaError_t r;
     if ((r = ppi::sm_count(&o.n_sm)) != cudaSuccess) return r;
-    if ((r = cudaFuncSetAttribute(parse_kernel<NS, SYM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if ((r = cudaFuncSetAttribute(parse_kernel<NS, GEN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   int(PARSE_SMEM))) != cudaSuccess)
       return r;
     int b = 0;
-    if ((r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, parse_kernel<NS, SYM>, ntf_of<NS>(),
+    if ((r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, parse_kernel<NS, GEN>, ntf_of<NS>(),
                                                            PARSE_SMEM)) != cudaSuccess)
       return r;
     o.blocks = b > 0 ? b : 1;
@@ -2451,10 +2456,10 @@ cudaError_t parse_setup(Occ** out) {
   return e;
 }
 
-template <int NS, bool SYM>
+template <int NS, bool GEN>
 cudaError_t launch_ns(const ParseParams& p, cudaStream_t stream) {
   Occ* po = nullptr;
-  cudaError_t e = parse_setup<NS, SYM>(&po);
+  cudaError_t e = parse_setup<NS, GEN>(&po);
   if (e != cudaSuccess) return e;
   const Occ& occ = *po;
   const bool timed = ppi::stage_begin();
@@ -2474,7 +2479,7 @@ cudaError_t launch_ns(const ParseParams& p, cudaStream_t stream) {
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const uint32_t g = uint32_t(std::min<uint64_t>(std::max<uint32_t>(p.n_tiles, 1),
                                                  uint64_t(occ.n_sm) * occ.blocks));
-  if (p.n_tiles) parse_kernel<NS, SYM><<<g, ntf_of<NS>(), PARSE_SMEM, stream>>>(p);
+  if (p.n_tiles) parse_kernel<NS, GEN><<<g, ntf_of<NS>(), PARSE_SMEM, stream>>>(p);
   if (timed) ppi::stage_mark(4, stream);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // the long numeric fields the tile pass queued (an empty queue costs a
@@ -2606,11 +2611,13 @@ void parse_scratch_carve(void* base, uint32_t n, int ns, ParseScratch* o, bool s
 }
 
 cudaError_t launch_parse(const ParseParams& p, cudaStream_t stream) {
+  // the general kernel for encodings, the options and type inference
+  const bool gen = p.enc || p.drop_bits || p.mark_bits || p.infer_out;
   switch (parse_ns_width(p.n_str)) {
-    case 0: return p.enc ? launch_ns<0, true>(p, stream) : launch_ns<0, false>(p, stream);
-    case 4: return p.enc ? launch_ns<4, true>(p, stream) : launch_ns<4, false>(p, stream);
-    case 8: return p.enc ? launch_ns<8, true>(p, stream) : launch_ns<8, false>(p, stream);
-    default: return p.enc ? launch_ns<16, true>(p, stream) : launch_ns<16, false>(p, stream);
+    case 0: return gen ? launch_ns<0, true>(p, stream) : launch_ns<0, false>(p, stream);
+    case 4: return gen ? launch_ns<4, true>(p, stream) : launch_ns<4, false>(p, stream);
+    case 8: return gen ? launch_ns<8, true>(p, stream) : launch_ns<8, false>(p, stream);
+    default: return gen ? launch_ns<16, true>(p, stream) : launch_ns<16, false>(p, stream);
   }
 }
 
