@@ -141,16 +141,21 @@ __device__ __forceinline__ uint32_t chunk_len(uint64_t c0, uint64_t n) {
 // ------------------------------------------------------------ pass 1
 // Steps of G'(s) = G(D(s)) take D as selector nibbles: word x holds
 // D(0..7) (4 bits each), y D(8..15).  tri[] holds D for three consecutive
-// bytes (groups g1, g2, g3: D = delta_g3 o delta_g2 o delta_g1), addressed
-// in bytes as ga[b1] | gb[b2] | gc[b3]; single[] one byte, at gc[b].
+// bytes (groups g1, g2, g3: D = delta_g3 o delta_g2 o delta_g1) at entry
+// g1 * 256 + g2 * 16 + (g3 ^ g1 ^ rot(g2)), addressed in bytes as
+// ga[b1] ^ gb[b2] ^ gc[b3]: the first two groups move the entry's bank, so
+// a warp's lanes spread over the banks whatever their third byte.
+// single[] holds one byte's D, at gc[b].
 struct StvTables {
-  uint16_t ga[256];  // group * 2048
-  uint16_t gb[256];  // group * 128
+  uint16_t ga[256];  // group * 2048, and the bank move
+  uint16_t gb[256];  // group * 128, and the bank move
   uint16_t gc[256];  // group * 8
   uint2 tri[16 * 16 * 16];
   uint2 single[PP_MAX_GROUPS];
   Stv16 delta[PP_MAX_GROUPS];  // delta_g as a vector (table construction)
 };
+
+__device__ __forceinline__ uint32_t tri_rot(uint32_t g) { return ((g >> 2) | (g << 2)) & 15u; }
 
 __device__ __forceinline__ Stv16 stv_step(const Stv16& G, uint2 e) {
   const uint32_t xx = e.x ^ 0x88888888u, xy = e.y ^ 0x88888888u;
@@ -175,8 +180,8 @@ __global__ void __launch_bounds__(WT, 4) tok_stv_kernel(const __grid_constant__ 
   const int t = threadIdx.x, lane = t & 31;
   for (int k = t; k < 256; k += WT) {
     const uint32_t g = P.dfa.byte_to_group[k] & 0xFu;
-    S.ga[k] = uint16_t(g << 11);
-    S.gb[k] = uint16_t(g << 7);
+    S.ga[k] = uint16_t((g << 11) ^ (g << 3));
+    S.gb[k] = uint16_t((g << 7) ^ (tri_rot(g) << 3));
     S.gc[k] = uint16_t(g << 3);
   }
   if (t < PP_MAX_GROUPS) {
@@ -191,9 +196,11 @@ __global__ void __launch_bounds__(WT, 4) tok_stv_kernel(const __grid_constant__ 
     S.single[t] = as_sel(d);
   }
   __syncthreads();
-  for (int k = t; k < 16 * 16 * 16; k += WT)
-    S.tri[k] = as_sel(stv16_compose(stv16_compose(S.delta[k >> 8], S.delta[(k >> 4) & 15]),
-                                    S.delta[k & 15]));
+  for (int k = t; k < 16 * 16 * 16; k += WT) {
+    const uint32_t g1 = uint32_t(k) >> 8, g2 = (uint32_t(k) >> 4) & 15u, g3 = uint32_t(k) & 15u;
+    S.tri[(k & ~15) | (g3 ^ g1 ^ tri_rot(g2))] =
+        as_sel(stv16_compose(stv16_compose(S.delta[g1], S.delta[g2]), S.delta[g3]));
+  }
   __syncthreads();
   const uint32_t n_warps = gridDim.x * WW;
   for (uint32_t p = blockIdx.x * WW + (t >> 5); p < P.n_pieces; p += n_warps) {
@@ -205,7 +212,7 @@ __global__ void __launch_bounds__(WT, 4) tok_stv_kernel(const __grid_constant__ 
     if (clen == CB) {  // back to front: bytes 61-63, 58-60, ..., 1-3, then byte 0
 #pragma unroll
       for (int j = CB - 3; j >= 1; j -= 3)
-        G = stv_step(G, at_byte(S.tri, S.ga[byte_of(w, j)] | S.gb[byte_of(w, j + 1)] |
+        G = stv_step(G, at_byte(S.tri, S.ga[byte_of(w, j)] ^ S.gb[byte_of(w, j + 1)] ^
                                            S.gc[byte_of(w, j + 2)]));
       G = stv_step(G, at_byte(S.single, S.gc[byte_of(w, 0)]));
     } else {
