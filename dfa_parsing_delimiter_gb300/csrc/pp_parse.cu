@@ -1578,8 +1578,9 @@ __device__ void chars_role(const ParseParams& P, PShared& S) {
 
 // ----------------------------------------------------------------- kernel
 // GEN: the general kernel, for inputs in an encoding (symbol codes; see
-// sym_code), the options of pp_parse_ex and type inference; the plain
-// kernel (byte inputs, every record emitted) carries none of that code.
+// sym_code), the options of pp_parse_ex, type inference and streamed chunks
+// (partial mode); the plain kernel (a whole byte input, every record
+// emitted) carries none of that code.
 template <int NS, bool GEN>
 __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_constant__ ParseParams P) {
   constexpr int NTF = ntf_of<NS>();
@@ -1636,7 +1637,7 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
   const uint32_t n_cols = uint32_t(P.n_cols);
   const uint32_t n_str = NS > 0 ? uint32_t(P.n_str) : 0u;
   const uint32_t rpb = max(1u, (uint32_t(SLOT_CAP) - n_cols) / n_cols);  // rows per pass
-  const bool partial = P.record_end != nullptr;
+  const bool partial = GEN && P.record_end != nullptr;  // a streamed chunk
   const bool emit = GEN && P.drop_bits != nullptr;    // some records are not emitted
   const bool status = GEN && P.mark_bits != nullptr;  // the status pass of rejection
   const bool infer = GEN && P.infer_out != nullptr;   // type inference
@@ -2611,8 +2612,9 @@ void parse_scratch_carve(void* base, uint32_t n, int ns, ParseScratch* o, bool s
 }
 
 cudaError_t launch_parse(const ParseParams& p, cudaStream_t stream) {
-  // the general kernel for encodings, the options and type inference
-  const bool gen = p.enc || p.drop_bits || p.mark_bits || p.infer_out;
+  // the general kernel for encodings, the options, type inference and
+  // streamed chunks
+  const bool gen = p.enc || p.drop_bits || p.mark_bits || p.infer_out || p.record_end;
   switch (parse_ns_width(p.n_str)) {
     case 0: return gen ? launch_ns<0, true>(p, stream) : launch_ns<0, false>(p, stream);
     case 4: return gen ? launch_ns<4, true>(p, stream) : launch_ns<4, false>(p, stream);

@@ -510,10 +510,11 @@ pp_rc pp_debug_stage_timing(int n_calls);
 /* Kernel durations of the recorded calls: out[PP_STAGES*i + k] =
  * milliseconds of kernel k of call i.  pp_parse: 0 init, 1 tile transition
  * vectors, 2 tile start states, 3 tile pass (tagging, indices, columns and
- * conversion), 4 long numeric fields (a warp per queued field).  pp_tokenize: 0 init, 1 transition vectors, 2 state scan,
- * 3 count pass, 4 count scan, 5 emit pass.  Entries a call does not use
- * are 0.  Waits for the events.  Returns the number of calls written (at
- * most max_calls), or -1 on a CUDA error. */
+ * conversion), 4 long numeric fields (a warp per queued field).
+ * pp_tokenize: 0 init, 1 transition vectors, 2 state scan, 3 count pass,
+ * 4 count scan, 5 emit pass.  Entries a call does not use are 0.  Waits for
+ * the events.  Returns the number of calls written (at most max_calls), or
+ * -1 on a CUDA error. */
 #define PP_STAGES 6
 int pp_debug_stage_ms(float* out, int max_calls);
 
