@@ -2429,7 +2429,7 @@ uint32_t init_grid(uint32_t n) {
 
 // Per device: the SM count, the tile pass's dynamic shared-memory attribute
 // and its resident blocks per SM.
-struct Occ { int blocks = 1, n_sm = 0; };
+struct Occ { int blocks = 1, n_sm = 0, tv_blocks = 1; };  // tile pass and tile-vector blocks per SM
 
 template <int NS, bool GEN>
 cudaError_t parse_setup(Occ** out) {
@@ -2450,6 +2450,12 @@ cudaError_t parse_setup(Occ** out) {
                                                            PARSE_SMEM)) != cudaSuccess)
       return r;
     o.blocks = b > 0 ? b : 1;
+    // the tile-vector pass: a grid of exactly the resident blocks (a second,
+    // partial wave would leave most SMs idle at its end)
+    if ((r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, tile_stv_kernel, TV_NT,
+                                                           LUT_BYTES)) != cudaSuccess)
+      return r;
+    o.tv_blocks = b > 0 ? b : 1;
     occ[d] = o;
     return cudaSuccess;
   });
@@ -2470,7 +2476,7 @@ cudaError_t launch_ns(const ParseParams& p, cudaStream_t stream) {
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (p.n_tiles) {
     const uint32_t gv = uint32_t(std::min<uint64_t>((p.n_tiles + TV_NT / 32 - 1) / (TV_NT / 32),
-                                                    uint64_t(occ.n_sm) * 6));
+                                                    uint64_t(occ.n_sm) * occ.tv_blocks));
     tile_stv_kernel<<<gv, TV_NT, LUT_BYTES, stream>>>(p);
   }
   if (timed) ppi::stage_mark(2, stream);
