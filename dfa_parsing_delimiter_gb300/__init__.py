@@ -122,6 +122,8 @@ def lib() -> ctypes.CDLL:
         L.pp_debug_stage_timing.argtypes = [ctypes.c_int]
         L.pp_debug_stage_ms.restype = ctypes.c_int
         L.pp_debug_stage_ms.argtypes = [_vp, ctypes.c_int]
+        L.pp_debug_parse_tags.restype = ctypes.c_int
+        L.pp_debug_parse_tags.argtypes = [_vp, _sz, ctypes.POINTER(DfaDesc), _vp, _vp, _vp]
         L.pp_debug_long_fields.restype = ctypes.c_int
         L.pp_debug_long_fields.argtypes = [ctypes.POINTER(ctypes.c_uint64), ctypes.c_int]
         _lib = L
@@ -205,6 +207,22 @@ def debug_stage_ms(max_calls: int):
     if n < 0:
         raise RuntimeError("pp_debug_stage_ms failed")
     return out[:n]
+
+
+def debug_parse_tags(d_in: torch.Tensor, desc: DfaDesc, n_bytes: int = None, stream=None):
+    """The tile pass's tag bitmaps (pp_debug_parse_tags) as three boolean
+    numpy arrays over the input bytes: field delimiter, record delimiter,
+    control symbol; and the status."""
+    import numpy as np
+    n = int(d_in.numel()) if n_bytes is None else int(n_bytes)
+    words = torch.zeros(max(3 * ((n + 31) // 32), 3), dtype=torch.int32, device=d_in.device)
+    st = new_status(d_in.device)
+    _check(lib().pp_debug_parse_tags(_ptr(d_in), n, ctypes.byref(desc), _ptr(words), _ptr(st),
+                                     _stream(stream)), "pp_debug_parse_tags")
+    w = words.cpu().numpy().view(np.uint32).reshape(-1, 3)
+    bits = [np.unpackbits(w[:, k].copy().view(np.uint8), bitorder="little")[:n].astype(bool)
+            for k in range(3)]
+    return bits[0], bits[1], bits[2], read_status(st)
 
 
 def debug_long_fields(reset: bool = False) -> int:

@@ -500,6 +500,27 @@ pp_rc pp_parse(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa, int 
   return cuda_rc(e);
 }
 
+pp_rc pp_debug_parse_tags(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa,
+                          uint32_t* d_bits, pp_status* d_status, cudaStream_t stream) {
+  if (!d_bits && n_bytes) return PP_EINVAL;
+  const pp_coltype skip = PP_COL_SKIP;
+  ppi::ParseParams p;
+  const pp_rc rc = ppi::parse_prepare(d_in, n_bytes, dfa, 1, &skip, nullptr, nullptr, nullptr, 0,
+                                      nullptr, d_status, &p);
+  if (rc != PP_OK) return rc;
+  p.dbg_tags = d_bits;
+  const int ns = ppi::parse_ns_width(p.n_str);
+  void* scratch = nullptr;
+  cudaError_t e = cudaMallocAsync(&scratch, ppi::parse_scratch_bytes(p.n_tiles, ns, p.enc != 0),
+                                  stream);
+  if (e != cudaSuccess) return cuda_rc(e);
+  ppi::parse_scratch_carve(scratch, p.n_tiles, ns, &p.s, p.enc != 0);
+  e = ppi::launch_parse(p, stream);
+  const cudaError_t ef = cudaFreeAsync(scratch, stream);
+  if (e == cudaSuccess) e = ef;
+  return cuda_rc(e);
+}
+
 pp_rc pp_count_fields(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa,
                       uint64_t* d_fields, pp_status* d_status, cudaStream_t stream) {
   if (!d_fields || (dfa && dfa->encoding != PP_ENC_BYTES)) return PP_EINVAL;

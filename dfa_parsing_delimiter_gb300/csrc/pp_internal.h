@@ -81,6 +81,8 @@ struct ParseParams {
   uint32_t n_tiles;
   uint32_t spin_limit;
   uint32_t dbg_withhold;  // test hook: the first tile posts nothing to the look-backs
+  uint32_t* dbg_tags;     // test hook, or null: per 32-byte chunk the tile pass's
+                          // field-delimiter, record-delimiter and control bitmaps
   uint32_t lut[256];      // per byte (or symbol code): STV selector, next-state/tag fields, special bit
   // Inputs in an encoding (PP_ENC_UTF8, PP_ENC_UTF16LE): lut is indexed by
   // symbol code (a one-byte symbol below 0x80: the byte; SYM_LAST + group:

@@ -1578,9 +1578,9 @@ __device__ void chars_role(const ParseParams& P, PShared& S) {
 
 // ----------------------------------------------------------------- kernel
 // GEN: the general kernel, for inputs in an encoding (symbol codes; see
-// sym_code), the options of pp_parse_ex, type inference and streamed chunks
-// (partial mode); the plain kernel (a whole byte input, every record
-// emitted) carries none of that code.
+// sym_code), the options of pp_parse_ex, type inference, streamed chunks
+// (partial mode) and the tag test hook; the plain kernel (a whole byte
+// input, every record emitted) carries none of that code.
 template <int NS, bool GEN>
 __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_constant__ ParseParams P) {
   constexpr int NTF = ntf_of<NS>();
@@ -1745,6 +1745,12 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
     const bool virt_rd = !partial && owns_end && accepting && !((g.rd >> (clen - 1)) & 1u);
     const uint32_t fd = g.fd, rd = g.rd;
     ctrl_s[t] = g.ctrl;
+    if (GEN && P.dbg_tags && clen) {  // test hook: the chunk's bitmaps
+      uint32_t* o = P.dbg_tags + 3 * ((tile_base + cstart) / CB);
+      o[0] = fd;
+      o[1] = rd;
+      o[2] = g.ctrl;
+    }
 
     // ---- (records, column, last) and control bytes, scanned over the warp
     // and then over the warps
@@ -2620,7 +2626,8 @@ void parse_scratch_carve(void* base, uint32_t n, int ns, ParseScratch* o, bool s
 cudaError_t launch_parse(const ParseParams& p, cudaStream_t stream) {
   // the general kernel for encodings, the options, type inference and
   // streamed chunks
-  const bool gen = p.enc || p.drop_bits || p.mark_bits || p.infer_out || p.record_end;
+  const bool gen = p.enc || p.drop_bits || p.mark_bits || p.infer_out || p.record_end ||
+                   p.dbg_tags;
   switch (parse_ns_width(p.n_str)) {
     case 0: return gen ? launch_ns<0, true>(p, stream) : launch_ns<0, false>(p, stream);
     case 4: return gen ? launch_ns<4, true>(p, stream) : launch_ns<4, false>(p, stream);

@@ -518,6 +518,16 @@ pp_rc pp_debug_stage_timing(int n_calls);
 #define PP_STAGES 6
 int pp_debug_stage_ms(float* out, int max_calls);
 
+/* Test hook: the tag bitmaps the tile pass of pp_parse computes (ParPaRaw
+ * Section 3.1, the bitmap indexes): for the 32-byte chunk k of the input,
+ * d_bits[3k] has bit j set if byte 32k + j is a field delimiter, d_bits[3k+1]
+ * a record delimiter, d_bits[3k+2] a control symbol.  d_bits: device,
+ * 3 * ceil(n_bytes / 32) words, written for every chunk.  Runs the parse's
+ * kernels with no outputs; data errors go to d_status as for pp_parse.
+ * Returns PP_EINVAL on a bad argument, PP_ENOMEM / PP_ECUDA on CUDA errors. */
+pp_rc pp_debug_parse_tags(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa,
+                          uint32_t* d_bits, pp_status* d_status, cudaStream_t stream);
+
 /* Test hook: *out (if not NULL) = the number of numeric fields converted by
  * the long-field pass (a warp per field longer than 256 bytes) on the
  * current device since the last reset; reset != 0 then sets it to 0.
