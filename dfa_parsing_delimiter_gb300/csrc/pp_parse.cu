@@ -1,8 +1,8 @@
 // pp_parse: DFA-based parsing of delimiter-separated input into Arrow-style
-// columns on sm_103a, in three kernels.
+// columns on sm_103a.
 //
-// The input is cut into 16 KiB tiles; each thread of the tile pass owns a
-// 32-byte chunk (one bit per byte in the bitmap indexes).
+// The input is cut into 16 KiB tiles; each worker thread of the tile pass
+// owns a 32-byte chunk (one bit per byte in the bitmap indexes).
 //
 // 0. Tile start states (tile_stv_kernel, tile_state_kernel).  A warp per
 //    tile folds the tile's transition vector (ParPaRaw Section 3.1, Figure
@@ -18,16 +18,23 @@
 //    chunk's start state; one DFA per thread tags its chunk (the three bitmap
 //    indexes of Section 3.1); record counts and absolute/relative column
 //    offsets (Section 3.2, Figure 4) are scanned over the tile and then across
-//    tiles by a decoupled look-back run by a dedicated scan warp, as are the
-//    value bytes per string column; every closed field goes into a
-//    column-major (column, record) slot table in shared memory; string value
-//    bytes are compacted per column into shared memory (stream compaction in
-//    place of ParPaRaw's radix partitioning, Section 3.3) and written as
-//    16-byte stores, one lane per field writes the Arrow offset or converts
-//    the number (Section 3.3), 32 consecutive rows of a column to a warp for
-//    coalesced stores.  Each input byte is read twice from HBM (once per
-//    pass) and every output byte written once; no per-byte intermediate
-//    reaches HBM.
+//    tiles by a decoupled look-back run by a dedicated context warp, and the
+//    value bytes per string column by a chars warp; each lane walks its
+//    chunk's fields into a column-major (column, record) slot table in shared
+//    memory; string value bytes are compacted per column into shared memory
+//    (stream compaction in place of ParPaRaw's radix partitioning, Section
+//    3.3) and written as 16-byte stores, and one lane per field writes the
+//    Arrow offset or converts the number (Section 3.3), 32 consecutive rows
+//    of a column to a warp for coalesced stores.  Each input byte is read
+//    twice from HBM (once per pass) and every output byte written once; no
+//    per-byte intermediate reaches HBM.  The kernel is instantiated plain
+//    (byte inputs, every record emitted) and general (encodings, the options
+//    of pp_parse_ex, type inference, streamed chunks).
+// 2. Long numeric fields (long_field_kernel): fields over 256 bytes, queued
+//    by the tile pass, converted by a warp each (Section 3.3's collaboration
+//    on long fields).
+// Column-count inference (fields_kernel, fields_reduce_kernel) reuses the
+// tile start states.
 #include <cstdint>
 #include <cuda_runtime.h>
 #include <algorithm>
