@@ -14,7 +14,7 @@ import torch
 
 import dfa_parsing_delimiter_gb300 as pp
 import oracle as O
-from gpu_util import compare_csv
+from gpu_util import compare_csv, to_dev
 from test_gpu_options import compare_ex
 
 pytestmark = pytest.mark.gpu
@@ -172,3 +172,29 @@ def test_long_fields_with_dropped_records():
     data = ("\n".join(rows) + "\n").encode()
     compare_ex(data, ["i64", "f64"], skip_records=sorted(rng.sample(range(200), 30)))
     compare_ex(data, ["i64", "f64"], reject=True)
+
+
+def test_long_field_last_record_without_newline():
+    """The input ends inside a long field of a record with no record
+    delimiter: the field still closes (the virtual delimiter at the end),
+    also when it spans tiles."""
+    for n in (300, 3 * TILE):
+        compare_csv(("1,2\n3," + "0" * n + "4.5").encode(), ["i32", "f64"])
+        compare_csv(("1,2\n3," + "0" * n + "-77").encode(), ["i32", "i64"])
+
+
+def test_long_fields_fixed_scratch():
+    """pp_parse_noalloc queues long fields in its fixed buffer too."""
+    rng = random.Random(31)
+    rows = ["0" * rng.randint(300, 2000) + str(i) + ".25," + str(i) for i in range(300)]
+    data = ("\n".join(rows) + "\n").encode()
+    n = len(data)
+    out = pp.CsvOutputs(["f64", "i32"], n + 1, [0, 0])
+    pp.debug_long_fields(reset=True)
+    out.run_noalloc(to_dev(data), n, pp.desc_csv())
+    st = pp.read_status(out.status, 2)
+    ref, rst = O.csv_parse(data, ["f64", "i32"])
+    assert st["error"] == rst["error"] == 0 and st["n_records"] == rst["n_records"] == 300
+    got = out.results(st)
+    assert np.array_equal(got[0].cpu().numpy(), ref[0]) and np.array_equal(got[1].cpu().numpy(), ref[1])
+    assert pp.debug_long_fields() == 300
