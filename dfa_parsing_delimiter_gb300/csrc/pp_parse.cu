@@ -1432,6 +1432,8 @@ struct PShared {
   uint32_t wsum[NW];
   uint32_t cstart[ppi::MAX_STR_COLS + 1];  // staging start per string column (this pass)
   uint32_t carry[ppi::MAX_STR_COLS];       // chars of earlier passes per string column
+  uint64_t pd_rec0;                // deferred write-out: the tile's first record,
+  uint32_t pd_rows, pd_col_in, pd_col_end;  // its rows, entry and end columns
   uint8_t coltype[PP_MAX_COLS];
   uint8_t numcol[PP_MAX_COLS];     // numeric output columns, floats first
   uint32_t n_num;
@@ -1668,10 +1670,81 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
     nph[o] += iss;
   };
 
+  // Arrow offsets and chars of the string fields of rows [lo, hi) of a tile
+  // with `rows` rows, first record rec0, entry column col_in and end column
+  // col_end, from the chars positions (pos_s), the column starts (S.cstart)
+  // and the staged bytes; the column's chars begin at S.base + S.carry.
+  auto write_out = [&](uint32_t lo, uint32_t hi, uint32_t rows, uint64_t rec0, uint32_t col_in,
+                       uint32_t col_end) {
+    const uint32_t nr = hi - lo, ngr = (nr + 31) / 32;
+    const uint32_t n_str = NS > 0 ? uint32_t(P.n_str) : 0u;
+    // Arrow offsets of the string fields closed in this pass
+    uint32_t si = 0, gi = uint32_t(warp);
+    while (gi >= ngr && si < n_str) { gi -= ngr; ++si; }
+    for (; si < n_str; gi += NW) {
+      while (gi >= ngr && si < n_str) { gi -= ngr; ++si; }
+      if (si >= n_str) break;
+      const uint32_t r = lo + gi * 32 + lane;
+      const uint32_t c = P.strcol[si];
+      if (r >= hi || (r == 0 && c < col_in) || (r + 1 == rows && c >= col_end)) continue;
+      uint64_t rec = rec0 + r;
+      if (emit) {
+        if (rec_dropped(P, rec)) continue;
+        rec -= dropped_before(P, rec);
+      }
+      if (rec >= P.rec_cap) { report(P.st, PP_ERR_CAPACITY, 0, false); continue; }
+      const uint64_t off = S.base[si] + S.carry[si] + (pos_s[si * nr + (r - lo)] - S.cstart[si]);
+      if (off > 0x7FFFFFFFull || off > P.chars_cap[si]) report(P.st, PP_ERR_CAPACITY, 0, false);
+      else P.offsets[si][rec + 1] = int32_t(off);
+    }
+    // staged chars -> HBM, 16-byte aligned stores
+    for (uint32_t si = 0; si < n_str; ++si) {
+      uint32_t len = S.cstart[si + 1] - S.cstart[si];
+      if (!len) continue;
+      const uint64_t gb = S.base[si] + S.carry[si];
+      if (gb + len > P.chars_cap[si]) {
+        if (t == 0) report(P.st, PP_ERR_CAPACITY, 0, false);
+        len = gb >= P.chars_cap[si] ? 0u : uint32_t(P.chars_cap[si] - gb);
+      }
+      uint8_t* gp = P.chars[si] + gb;
+      const uint32_t sp = S.cstart[si];
+      const uint32_t head = min(len, uint32_t((16u - (reinterpret_cast<uintptr_t>(gp) & 15u)) & 15u));
+      const uint32_t nvec = (len - head) >> 4;
+      const uint32_t tail0 = head + (nvec << 4);
+      if (uint32_t(t) < head) gp[t] = stage_s[sp + t];
+      const uint32_t src0 = sp + head;
+      const uint32_t sh = (src0 & 3u) * 8u;
+      const uint32_t* sw = reinterpret_cast<const uint32_t*>(stage_s + (src0 & ~3u));
+      uint4* gv = reinterpret_cast<uint4*>(gp + head);
+      for (uint32_t v = t; v < nvec; v += NT) {
+        const uint32_t* q = sw + 4 * v;
+        const uint32_t a0 = q[0], a1 = q[1], a2 = q[2], a3 = q[3], a4 = q[4];
+        uint4 o;
+        o.x = __funnelshift_r(a0, a1, sh);
+        o.y = __funnelshift_r(a1, a2, sh);
+        o.z = __funnelshift_r(a2, a3, sh);
+        o.w = __funnelshift_r(a3, a4, sh);
+        __stcs(gv + v, o);
+      }
+      if (tail0 + t < len) gp[tail0 + t] = stage_s[sp + tail0 + t];
+    }
+  };
+  // A tile of one pass in the plain kernel leaves its write-out pending
+  // (pend) until the next tile has walked its fields: by then the chars
+  // warp's look-back for it has long finished, where an immediate write-out
+  // would wait for it.  The bytes stay staged meanwhile: the next tile
+  // overwrites the staging area, the chars positions and the column starts
+  // only after that.
+  bool pend = false;
+
   for (uint32_t it = 0;; ++it) {
     const uint32_t b = it & 1u;
     const uint32_t tile = S.tile[b];
     if (tile >= P.n_tiles) {
+      if (NS > 0 && pend) {  // the last tile's write-out
+        bar_sync(BAR_CHR, NT + 32);
+        write_out(0u, S.pd_rows, S.pd_rows, S.pd_rec0, S.pd_col_in, S.pd_col_end);
+      }
       bar_arrive(BAR_AGG, NT + 32);  // the scan warps see the end too
       bar_sync(BAR_V2, NTF);
       break;
@@ -1841,6 +1914,7 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
              &S.cpl[0], &S.lut1[0], any_ctrl};
 
 
+    const bool defer = !GEN && rows <= rpb;  // one pass: its write-out may wait
     // ---- fields -> (column, row) slots, in passes of rows
     for (uint32_t lo = 0; lo < rows; lo += rpb) {
       const uint32_t hi = min(rows, lo + rpb), nr = hi - lo;
@@ -1930,6 +2004,11 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
         }
       }
       if (first) {
+        if (NS > 0 && pend) {  // the previous tile's write-out, its chars offsets known
+          bar_sync(BAR_CHR, NT + 32);
+          write_out(0u, S.pd_rows, S.pd_rows, S.pd_rec0, S.pd_col_in, S.pd_col_end);
+          pend = false;
+        }
         if (NS > 0 && !emit) bar_arrive(BAR_W2, NT + 32);
         // ---- the tile's context from the look-back
         bar_sync(BAR_V2, NTF);
@@ -2172,59 +2251,15 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
       if (first) next_ticket(b);
       bar_sync(BAR_W, NT);
       if (NS > 0 && n_str) {
-        if (first) bar_sync(BAR_CHR, NT + 32);  // the tile's chars offsets
-        // Arrow offsets of the string fields closed in this pass
-        uint32_t si = 0, gi = uint32_t(warp);
-        while (gi >= ngr && si < n_str) { gi -= ngr; ++si; }
-        for (; si < n_str; gi += NW) {
-          while (gi >= ngr && si < n_str) { gi -= ngr; ++si; }
-          if (si >= n_str) break;
-          const uint32_t r = lo + gi * 32 + lane;
-          const uint32_t c = P.strcol[si];
-          if (r >= hi || (r == 0 && c < col_in) || (r + 1 == rows && c >= col_end)) continue;
-          uint64_t rec = rec0 + r;
-          if (emit) {
-            if (rec_dropped(P, rec)) continue;
-            rec -= dropped_before(P, rec);
-          }
-          if (rec >= P.rec_cap) { report(P.st, PP_ERR_CAPACITY, 0, false); continue; }
-          const uint64_t off = S.base[si] + S.carry[si] + (pos_s[si * nr + (r - lo)] - S.cstart[si]);
-          if (off > 0x7FFFFFFFull || off > P.chars_cap[si]) report(P.st, PP_ERR_CAPACITY, 0, false);
-          else P.offsets[si][rec + 1] = int32_t(off);
+        if (defer) {  // written during the next tile, once its fields are walked
+          if (t == 0) { S.pd_rec0 = rec0; S.pd_rows = rows; S.pd_col_in = col_in; S.pd_col_end = col_end; }
+          pend = true;
+        } else {
+          if (first) bar_sync(BAR_CHR, NT + 32);  // the tile's chars offsets
+          write_out(lo, hi, rows, rec0, col_in, col_end);
+          bar_sync(BAR_W, NT);
+          if (t < int(n_str)) S.carry[t] += S.cstart[t + 1] - S.cstart[t];
         }
-        // staged chars -> HBM, 16-byte aligned stores
-        for (uint32_t si = 0; si < n_str; ++si) {
-          uint32_t len = S.cstart[si + 1] - S.cstart[si];
-          if (!len) continue;
-          const uint64_t gb = S.base[si] + S.carry[si];
-          if (gb + len > P.chars_cap[si]) {
-            if (t == 0) report(P.st, PP_ERR_CAPACITY, 0, false);
-            len = gb >= P.chars_cap[si] ? 0u : uint32_t(P.chars_cap[si] - gb);
-          }
-          uint8_t* gp = P.chars[si] + gb;
-          const uint32_t sp = S.cstart[si];
-          const uint32_t head = min(len, uint32_t((16u - (reinterpret_cast<uintptr_t>(gp) & 15u)) & 15u));
-          const uint32_t nvec = (len - head) >> 4;
-          const uint32_t tail0 = head + (nvec << 4);
-          if (uint32_t(t) < head) gp[t] = stage_s[sp + t];
-          const uint32_t src0 = sp + head;
-          const uint32_t sh = (src0 & 3u) * 8u;
-          const uint32_t* sw = reinterpret_cast<const uint32_t*>(stage_s + (src0 & ~3u));
-          uint4* gv = reinterpret_cast<uint4*>(gp + head);
-          for (uint32_t v = t; v < nvec; v += NT) {
-            const uint32_t* q = sw + 4 * v;
-            const uint32_t a0 = q[0], a1 = q[1], a2 = q[2], a3 = q[3], a4 = q[4];
-            uint4 o;
-            o.x = __funnelshift_r(a0, a1, sh);
-            o.y = __funnelshift_r(a1, a2, sh);
-            o.z = __funnelshift_r(a2, a3, sh);
-            o.w = __funnelshift_r(a3, a4, sh);
-            __stcs(gv + v, o);
-          }
-          if (tail0 + t < len) gp[tail0 + t] = stage_s[sp + tail0 + t];
-        }
-        bar_sync(BAR_W, NT);
-        if (t < int(n_str)) S.carry[t] += S.cstart[t + 1] - S.cstart[t];
       }
       bar_sync(BAR_W, NT);
     }
