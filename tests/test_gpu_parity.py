@@ -468,3 +468,32 @@ def test_parse_crowded_and_sparse_fields(skew):
             parts.append("y" * rng.randint(100, 400) + "," + str(i))            # few, long fields
     data = ("\n".join(parts) + "\n").encode()
     compare_csv(data, ["str", "str", "str"])
+
+
+@pytest.mark.parametrize("last", ["short", "long", "one"])
+def test_parse_write_out_across_tiles(last):
+    """Tiles of one pass of rows leave their offsets and chars to be written
+    during the next tile; tiles with more rows than a pass holds (short
+    records, several passes) write theirs at once.  Regions of each kind
+    alternate, a few tiles long and at ragged offsets, and the input ends
+    in either kind of tile, or in a single tile, so that every hand-over
+    between the two, and the last tile's write-out at the end of a block's
+    tiles, meets the oracle."""
+    rng = random.Random({"short": 71, "long": 72, "one": 73}[last])
+    parts = []
+    kinds = ["short", "long"] * 6 + [last]
+    if last == "one":
+        kinds = ["long"]
+    size = 0
+    for kind in kinds:
+        target = size + (rng.randint(2000, 15000) if last == "one" else rng.randint(20000, 70000))
+        while size < target:
+            if kind == "short":  # six bytes a record: 2730 rows a tile, three passes
+                rec = "%s,%s,%d\n" % (rng.choice("abc"), rng.choice(["", "d"]), rng.randint(0, 9))
+            else:
+                rec = "%s,%s,%d\n" % ("x" * rng.randint(100, 900), "y" * rng.randint(0, 40),
+                                       rng.randint(-99999, 99999))
+            parts.append(rec)
+            size += len(rec)
+    data = "".join(parts).encode()
+    compare_csv(data, ["str", "str", "i64"])
