@@ -1432,6 +1432,8 @@ struct PShared {
   uint32_t wsum[NW];
   uint32_t cstart[ppi::MAX_STR_COLS + 1];  // staging start per string column (this pass)
   uint32_t carry[ppi::MAX_STR_COLS];       // chars of earlier passes per string column
+  uint32_t wo_len[ppi::MAX_STR_COLS], wo_head[ppi::MAX_STR_COLS];  // chars write-out per column:
+  uint32_t wo_vpre[ppi::MAX_STR_COLS + 1];  // bytes, head bytes, 16-byte middles before it
   uint64_t pd_rec0;                // deferred write-out: the tile's first record,
   uint32_t pd_rows, pd_col_in, pd_col_end;  // its rows, entry and end columns
   uint8_t coltype[PP_MAX_COLS];
@@ -1697,36 +1699,60 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
       if (off > 0x7FFFFFFFull || off > P.chars_cap[si]) report(P.st, PP_ERR_CAPACITY, 0, false);
       else P.offsets[si][rec + 1] = int32_t(off);
     }
-    // staged chars -> HBM, 16-byte aligned stores
-    for (uint32_t si = 0; si < n_str; ++si) {
-      uint32_t len = S.cstart[si + 1] - S.cstart[si];
-      if (!len) continue;
-      const uint64_t gb = S.base[si] + S.carry[si];
-      if (gb + len > P.chars_cap[si]) {
-        if (t == 0) report(P.st, PP_ERR_CAPACITY, 0, false);
-        len = gb >= P.chars_cap[si] ? 0u : uint32_t(P.chars_cap[si] - gb);
+    // staged chars -> HBM, the string columns together: each column's
+    // bytes up to a 16-byte boundary of its destination (head) and after its
+    // last whole 16 bytes (tail) by a warp per column, and the 16-byte
+    // middles of all columns as one index space (wo_vpre: middles before
+    // each column), realigned by funnel shifts
+    static_assert(ppi::MAX_STR_COLS <= NW, "a warp per string column");
+    if (warp == 0) {
+      uint32_t nv = 0;
+      if (uint32_t(lane) < n_str) {
+        const uint32_t si = uint32_t(lane);
+        uint32_t len = S.cstart[si + 1] - S.cstart[si];
+        const uint64_t gb = S.base[si] + S.carry[si];
+        if (len && gb + len > P.chars_cap[si]) {
+          report(P.st, PP_ERR_CAPACITY, 0, false);
+          len = gb >= P.chars_cap[si] ? 0u : uint32_t(P.chars_cap[si] - gb);
+        }
+        const uint32_t head =
+            min(len, uint32_t((16u - (reinterpret_cast<uintptr_t>(P.chars[si] + gb) & 15u)) & 15u));
+        S.wo_len[si] = len;
+        S.wo_head[si] = head;
+        nv = (len - head) >> 4;
       }
-      uint8_t* gp = P.chars[si] + gb;
-      const uint32_t sp = S.cstart[si];
-      const uint32_t head = min(len, uint32_t((16u - (reinterpret_cast<uintptr_t>(gp) & 15u)) & 15u));
-      const uint32_t nvec = (len - head) >> 4;
-      const uint32_t tail0 = head + (nvec << 4);
-      if (uint32_t(t) < head) gp[t] = stage_s[sp + t];
-      const uint32_t src0 = sp + head;
-      const uint32_t sh = (src0 & 3u) * 8u;
-      const uint32_t* sw = reinterpret_cast<const uint32_t*>(stage_s + (src0 & ~3u));
-      uint4* gv = reinterpret_cast<uint4*>(gp + head);
-      for (uint32_t v = t; v < nvec; v += NT) {
-        const uint32_t* q = sw + 4 * v;
-        const uint32_t a0 = q[0], a1 = q[1], a2 = q[2], a3 = q[3], a4 = q[4];
-        uint4 o;
-        o.x = __funnelshift_r(a0, a1, sh);
-        o.y = __funnelshift_r(a1, a2, sh);
-        o.z = __funnelshift_r(a2, a3, sh);
-        o.w = __funnelshift_r(a3, a4, sh);
-        __stcs(gv + v, o);
+      uint32_t inc = nv;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t o = __shfl_up_sync(FULL, inc, d);
+        if (lane >= d) inc += o;
       }
-      if (tail0 + t < len) gp[tail0 + t] = stage_s[sp + tail0 + t];
+      if (uint32_t(lane) < n_str) S.wo_vpre[lane + 1] = inc;
+      if (lane == 0) S.wo_vpre[0] = 0;
+    }
+    bar_sync(BAR_W, NT);
+    if (uint32_t(warp) < n_str) {
+      const uint32_t si = uint32_t(warp), len = S.wo_len[si], head = S.wo_head[si];
+      const uint32_t tail0 = head + (((len - head) >> 4) << 4), sp = S.cstart[si];
+      uint8_t* gp = P.chars[si] + (S.base[si] + S.carry[si]);
+      const uint32_t k = uint32_t(lane) & 15u;
+      const uint32_t p = lane < 16 ? (k < head ? k : len) : tail0 + k;
+      if (p < len) gp[p] = stage_s[sp + p];
+    }
+    const uint32_t vtot = S.wo_vpre[n_str];
+    uint32_t vc = 0;  // the column of middle v
+    for (uint32_t v = uint32_t(t); v < vtot; v += NT) {
+      while (v >= S.wo_vpre[vc + 1]) ++vc;
+      const uint32_t vi = v - S.wo_vpre[vc], head = S.wo_head[vc];
+      const uint32_t src0 = S.cstart[vc] + head, sh = (src0 & 3u) * 8u;
+      const uint32_t* q = reinterpret_cast<const uint32_t*>(stage_s + (src0 & ~3u)) + 4 * vi;
+      const uint32_t a0 = q[0], a1 = q[1], a2 = q[2], a3 = q[3], a4 = q[4];
+      uint4 o;
+      o.x = __funnelshift_r(a0, a1, sh);
+      o.y = __funnelshift_r(a1, a2, sh);
+      o.z = __funnelshift_r(a2, a3, sh);
+      o.w = __funnelshift_r(a3, a4, sh);
+      __stcs(reinterpret_cast<uint4*>(P.chars[vc] + (S.base[vc] + S.carry[vc]) + head) + vi, o);
     }
   };
   // A tile of one pass in the plain kernel leaves its write-out pending
