@@ -42,6 +42,7 @@ constexpr int CB = 64;                   // bytes per lane
 constexpr int PIECE = 32 * CB;           // bytes per warp
 constexpr int WT = 256;                  // threads per block, transition-vector pass
 constexpr int WW = WT / 32;
+constexpr int EMIT_BPS = 5;              // emit pass: blocks per SM (48 registers a thread)
 constexpr int SCAN_T = 256, SCAN_E = 16; // scan passes: pieces per thread
 constexpr int SCAN_TILE = SCAN_T * SCAN_E;
 constexpr uint32_t CAPW = 512;           // tokens per piece staged for coalesced stores
@@ -643,7 +644,7 @@ __device__ __forceinline__ uint32_t emit_half(const DfaTables& S, const uint32_t
   return m;
 }
 
-__global__ void __launch_bounds__(WT, 4) tok_emit_kernel(const __grid_constant__ TokParams P) {
+__global__ void __launch_bounds__(WT, EMIT_BPS) tok_emit_kernel(const __grid_constant__ TokParams P) {
   __shared__ DfaTables S;
   __shared__ EmitStage E;
   build_dfa_tables(P, S);
@@ -886,6 +887,7 @@ cudaError_t launch_tokenize(const uint8_t* in, uint64_t n, const GenericDfa& dfa
   });
   if (e != cudaSuccess) return e;
   const uint32_t bgrid = std::min<uint32_t>((P.n_pieces + WW - 1) / WW, uint32_t(n_sm) * 4);
+  const uint32_t egrid = std::min<uint32_t>((P.n_pieces + WW - 1) / WW, uint32_t(n_sm) * EMIT_BPS);
   const uint32_t dgrid = std::min<uint32_t>((P.n_pieces + DW - 1) / DW, uint32_t(n_sm) * 2);
   tok_stv_kernel<<<bgrid, WT, 0, stream>>>(P);
   if (timed) stage_mark(2, stream);
@@ -897,7 +899,7 @@ cudaError_t launch_tokenize(const uint8_t* in, uint64_t n, const GenericDfa& dfa
   if (carry_out) tok_carry_kernel<<<1, 32, 0, stream>>>(P);
   if (timed) stage_mark(5, stream);
   const bool sizing = cap == 0 && out_start == nullptr;
-  if (!sizing) tok_emit_kernel<<<bgrid, WT, 0, stream>>>(P);
+  if (!sizing) tok_emit_kernel<<<egrid, WT, 0, stream>>>(P);
   if (timed) stage_mark(6, stream);
   return cudaGetLastError();
 }
