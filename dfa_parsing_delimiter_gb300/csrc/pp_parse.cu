@@ -1149,25 +1149,29 @@ __device__ __forceinline__ bool rec_skip_listed(const ParseParams& P, uint64_t r
 // ================================================================ 1. tile pass
 // Everything after the tile start states happens in one pass over the tiles.
 // A block has 16 worker warps (one 32-byte chunk per thread, as in the tile
-// states pass) and one scan warp.  The scan warp runs the two cross-tile
-// exclusive scans of ParPaRaw Section 3.2 as single-pass decoupled
-// look-backs — first (record count, column offset, last terminator), then
-// the value bytes per string column — while the workers go on with the
-// tile's own work; named barriers hand the aggregates and the prefixes
-// between the two roles:
+// states pass), a context warp and, with string columns, a chars warp.  The
+// two run the cross-tile exclusive scans of ParPaRaw Section 3.2 as
+// single-pass decoupled look-backs, the context warp (record count, column
+// offset, last terminator) and the chars warp the value bytes per string
+// column, while the workers go on with the tile's own work; named barriers
+// hand the aggregates and the prefixes between the roles:
 //
-//   workers                                   scan warp
+//   workers                                   context / chars warp
 //   tag the tile, scan it        --BAR_AGG-->  post the tile's aggregate,
 //   list its fields (rows and                  look back: record index,
 //   columns inside the tile),                  column and last terminator
 //   value bytes per string                     at the tile start
 //   column                       --BAR_W2--->
-//   place the first record's     <--BAR_V2---  post the chars aggregate
+//   place the first record's     <--BAR_V2---  post the chars aggregate,
 //   fields; stage strings,                     look back: chars offsets
 //   convert numbers (stored at                 of the tile
 //   their global rows)           <--BAR_CHR--
 //   write offsets and chars
 //
+// A tile of one pass of rows (the plain kernel) writes its offsets and chars
+// during the next tile instead, after that tile's field walk: its chars
+// look-back has finished by then.
+
 // The first record of a tile (its row 0) is in general the tail of a record
 // that began earlier: its fields' columns are the tile's entry column plus
 // their index, known only from the look-back (ParPaRaw Section 3.2, the
