@@ -1430,6 +1430,8 @@ struct PShared {
   uint32_t n_rel;                  // row-0 fields seen (k + 1 of the last)
   uint32_t rd0_pos, rd0_k;         // the tile's first record delimiter: position + 1, field index
   uint32_t ctot[ppi::MAX_STR_COLS];  // value bytes per string column of rows >= 1
+  uint32_t cmode[2];               // per landing buffer: 1 = the chars aggregate is the
+                                   // items scan's column totals (a one-pass tile)
   uint64_t rec0, last1;            // from the look-back: record index, last terminator + 1
   uint32_t col_in, lst;            // column at the tile start, state after that terminator
   uint64_t base[ppi::MAX_STR_COLS];  // chars offset of the tile per string column
@@ -1548,25 +1550,30 @@ __device__ void chars_role(const ParseParams& P, PShared& S) {
     if (tile >= P.n_tiles) break;
     bar_sync(BAR_W2, NT + 32);  // the workers' value-byte totals
     uint64_t cagg[K3];
-    const uint32_t col_in = S.col_in;
-    const uint32_t nrel = min(S.n_rel, n_cols);
+    if (S.cmode[b]) {  // a one-pass tile: the column totals of its items scan
 #pragma unroll
-    for (int k = 0; k < K3; ++k) cagg[k] = k < P.n_str ? S.ctot[k] : 0u;
-    // row-0 fields: column = entry column + index (at most n_cols of them,
-    // summed by one lane and broadcast)
-    uint32_t add[K3];
+      for (int k = 0; k < K3; ++k) cagg[k] = k < P.n_str ? uint64_t(S.cstart[k + 1] - S.cstart[k]) : 0u;
+    } else {  // the field walk's totals of rows >= 1, and row 0's fields
+      const uint32_t col_in = S.col_in;
+      const uint32_t nrel = min(S.n_rel, n_cols);
 #pragma unroll
-    for (int q = 0; q < K3; ++q) add[q] = 0;
-    if (lane == 0)
-      for (uint32_t k = 0; k < nrel && col_in + k < n_cols; ++k) {
-        const int si = P.stridx[col_in + k];
-        const uint32_t len = S.rel_len[k];
+      for (int k = 0; k < K3; ++k) cagg[k] = k < P.n_str ? S.ctot[k] : 0u;
+      // row-0 fields: column = entry column + index (at most n_cols of them,
+      // summed by one lane and broadcast)
+      uint32_t add[K3];
 #pragma unroll
-        for (int q = 0; q < K3; ++q)
-          if (q == si) add[q] += len;
-      }
+      for (int q = 0; q < K3; ++q) add[q] = 0;
+      if (lane == 0)
+        for (uint32_t k = 0; k < nrel && col_in + k < n_cols; ++k) {
+          const int si = P.stridx[col_in + k];
+          const uint32_t len = S.rel_len[k];
 #pragma unroll
-    for (int q = 0; q < K3; ++q) cagg[q] += __shfl_sync(FULL, add[q], 0);
+          for (int q = 0; q < K3; ++q)
+            if (q == si) add[q] += len;
+        }
+#pragma unroll
+      for (int q = 0; q < K3; ++q) cagg[q] += __shfl_sync(FULL, add[q], 0);
+    }
     uint64_t zero[K3], ex[K3];
 #pragma unroll
     for (int k = 0; k < K3; ++k) zero[k] = 0;
@@ -1944,7 +1951,11 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
              &S.cpl[0], &S.lut1[0], any_ctrl};
 
 
-    const bool defer = !GEN && rows <= rpb;  // one pass: its write-out may wait
+    // One pass of rows in the plain kernel: the write-out waits for the next
+    // tile, and the chars aggregate is the items scan's column totals (the
+    // field walk counts no value bytes)
+    const bool defer = !GEN && P.has_out && rows <= rpb;
+    if (t == 0) S.cmode[b] = defer ? 1u : 0u;
     // ---- fields -> (column, row) slots, in passes of rows
     for (uint32_t lo = 0; lo < rows; lo += rpb) {
       const uint32_t hi = min(rows, lo + rpb), nr = hi - lo;
@@ -1961,7 +1972,7 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
           if (first) {
             if (col < n_cols) {
               S.rel_slot[col] = (fs << 16) | e;
-              if (!emit) {
+              if (!emit && !defer) {
                 const uint32_t L = value_len(fs, e, any_ctrl, ctrl_s, S);
                 if (L) atomicAdd(&S.rel_len[col], L);
               }
@@ -1972,7 +1983,7 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
           return;
         }
         if (in_pass && col < n_cols) slot_s[col * nrp + (rl - lo)] = (fs << 16) | e;
-        if (NS > 0 && first && !emit && col < n_cols && ((P.strmask >> col) & 1u)) {
+        if (NS > 0 && first && !emit && !defer && col < n_cols && ((P.strmask >> col) & 1u)) {
           const uint32_t L = value_len(fs, e, any_ctrl, ctrl_s, S);
           if (L) add16(cnt, P.stridx[col], L);
         }
@@ -2016,7 +2027,7 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
         }
       };
       walk(enter);
-      if (NS > 0 && first && !emit) {  // warp sums of the packed counters -> tile totals
+      if (NS > 0 && first && !emit && !defer) {  // warp sums of the packed counters -> tile totals
         bool any = false;
 #pragma unroll
         for (int k = 0; k < NSW; ++k) any |= cnt[k] != 0;
@@ -2039,7 +2050,7 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
           write_out(0u, S.pd_rows, S.pd_rows, S.pd_rec0, S.pd_col_in, S.pd_col_end);
           pend = false;
         }
-        if (NS > 0 && !emit) bar_arrive(BAR_W2, NT + 32);
+        if (NS > 0 && !emit && !defer) bar_arrive(BAR_W2, NT + 32);
         // ---- the tile's context from the look-back
         bar_sync(BAR_V2, NTF);
         rec0 = S.rec0;
@@ -2157,6 +2168,7 @@ __global__ void __launch_bounds__(ntf_of<NS>(), 2) parse_kernel(const __grid_con
           }
         }
         bar_sync(BAR_W, NT);
+        if (defer) bar_arrive(BAR_W2, NT + 32);  // the column totals (S.cstart) for the chars warp
         // staging: a lane per short field; long fields chunk-parallel, each
         // thread copying its chunk's part of the (at most two) long fields
         // that cover it
