@@ -1170,7 +1170,9 @@ __device__ __forceinline__ bool rec_skip_listed(const ParseParams& P, uint64_t r
 //
 // A tile of one pass of rows (the plain kernel) writes its offsets and chars
 // during the next tile instead, after that tile's field walk: its chars
-// look-back has finished by then.
+// look-back has finished by then.  Such a tile also hands the chars warp its
+// value bytes per string column only after the string items scan (the
+// column totals of that scan), so its field walk counts none.
 
 // The first record of a tile (its row 0) is in general the tail of a record
 // that began earlier: its fields' columns are the tile's entry column plus
