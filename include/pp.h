@@ -267,7 +267,7 @@ pp_rc pp_parse_ex(const uint8_t* d_in, size_t n_bytes, const pp_dfa_desc* dfa, i
  *   [records + 1] int32 per string column, chars, one typed array per
  *   numeric column, and the status).  Page-locked (pinned) host memory lets
  *   the copies run asynchronously and overlap the parse; pageable memory
- *   works, with the copies staged by the driver.
+ *   works, with the copies staged by the CUDA driver.
  *   records_capacity, chars_capacity[]: as in pp_parse, for the whole input.
  *   chunk_bytes: bytes of new input per chunk (rounded up to a multiple of
  *   pp_tile_bytes(); 0 = 128 MiB).  Each chunk after the first begins with

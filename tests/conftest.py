@@ -10,7 +10,7 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
-    config.addinivalue_line("markers", "fullsize: full-size workload (GPU box only)")
+    config.addinivalue_line("markers", "fullsize: full-size workload (needs a GPU with tens of GB free)")
 
 
 @pytest.fixture(scope="session")
