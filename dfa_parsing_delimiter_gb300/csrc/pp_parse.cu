@@ -495,15 +495,26 @@ __device__ __forceinline__ void load_lut(const ParseParams& P, uint32_t* lut_s) 
 // scan over tiles.
 constexpr int TV_NT = 256;              // tile-vector pass: a warp per tile
 constexpr int TV_BYTES = TILE / 32;     // bytes per lane
+constexpr int TV_STEP = 128;            // staged path: bytes per lane per step
+constexpr int TV_ROW = TV_STEP + 16;    // a lane's staging row (padded: conflict-free reads)
+constexpr int TV_SMEM = LUT_BYTES + (TV_NT / 32) * 32 * TV_ROW;
 constexpr int TS_NT = 256, TS_TPT = 16; // tile-state scan: tiles per thread
 constexpr int TS_TILES = TS_NT * TS_TPT;
 
 // Transition vector of each tile: one warp per tile, each lane folding
 // TV_BYTES bytes back to front, a warp scan composing the lanes in order.
+// A whole tile of a 16-byte aligned byte input goes through shared memory
+// in steps of TV_STEP bytes per lane: a lane's bytes are TV_BYTES from its
+// neighbour's, so reading them straight from global memory would touch a
+// sector per lane in every load; the warp instead loads the step's rows
+// 128 contiguous bytes per 8 lanes, stores them to per-lane rows padded to
+// TV_ROW bytes, and each lane folds its own row.  Launched with TV_SMEM
+// bytes of dynamic shared memory.
 __global__ void __launch_bounds__(TV_NT) tile_stv_kernel(const __grid_constant__ ParseParams P) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint8_t b2g_s[0x80];
   uint32_t* lut_s = reinterpret_cast<uint32_t*>(smem);
+  uint8_t* const stage = smem + LUT_BYTES + (threadIdx.x >> 5) * (32 * TV_ROW);  // the warp's rows
   for (int k = threadIdx.x; k < 256 * 32; k += TV_NT) lut_s[k] = P.lut[k >> 5];
   for (int k = threadIdx.x; k < 0x80; k += TV_NT) b2g_s[k] = P.sym_b2g[k];
   __syncthreads();
@@ -557,6 +568,22 @@ __global__ void __launch_bounds__(TV_NT) tile_stv_kernel(const __grid_constant__
         }
       } else {
         for (int j = int(len) - 1; j >= 0; --j) G = fold_sym(G, b0 + uint32_t(j));
+      }
+    } else if (h == 0 && uint64_t(tile + 1) * TILE <= P.n) {  // staged (uniform in the warp)
+      const uint8_t* tb = P.in + uint64_t(tile) * TILE;
+      const uint32_t r4 = uint32_t(lane) >> 3, c16 = uint32_t(lane) & 7u;
+      for (int st = TV_BYTES / TV_STEP - 1; st >= 0; --st) {
+        __syncwarp();  // the rows of the step after are read
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint32_t row = 4u * uint32_t(q) + r4;
+          const uint4 v = __ldg(reinterpret_cast<const uint4*>(tb + row * TV_BYTES + uint32_t(st) * TV_STEP) + c16);
+          *reinterpret_cast<uint4*>(stage + row * TV_ROW + c16 * 16u) = v;
+        }
+        __syncwarp();
+        const uint4* mine = reinterpret_cast<const uint4*>(stage + uint32_t(lane) * TV_ROW);
+#pragma unroll
+        for (int k = TV_STEP / 16 - 1; k >= 0; --k) G = fold16(G, mine[k]);
       }
     } else if (len == TV_BYTES) {
       const uint8_t* p = P.in + b0;
@@ -2544,8 +2571,11 @@ cudaError_t parse_setup(Occ** out) {
     o.blocks = b > 0 ? b : 1;
     // the tile-vector pass: a grid of exactly the resident blocks (a second,
     // partial wave would leave most SMs idle at its end)
+    if ((r = cudaFuncSetAttribute(tile_stv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  TV_SMEM)) != cudaSuccess)
+      return r;
     if ((r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, tile_stv_kernel, TV_NT,
-                                                           LUT_BYTES)) != cudaSuccess)
+                                                           TV_SMEM)) != cudaSuccess)
       return r;
     o.tv_blocks = b > 0 ? b : 1;
     occ[d] = o;
@@ -2569,7 +2599,7 @@ cudaError_t launch_ns(const ParseParams& p, cudaStream_t stream) {
   if (p.n_tiles) {
     const uint32_t gv = uint32_t(std::min<uint64_t>((p.n_tiles + TV_NT / 32 - 1) / (TV_NT / 32),
                                                     uint64_t(occ.n_sm) * occ.tv_blocks));
-    tile_stv_kernel<<<gv, TV_NT, LUT_BYTES, stream>>>(p);
+    tile_stv_kernel<<<gv, TV_NT, TV_SMEM, stream>>>(p);
   }
   if (timed) ppi::stage_mark(2, stream);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -2606,6 +2636,9 @@ cudaError_t launch_fields(const ParseParams& p, FAgg* agg, uint64_t* out, cudaSt
     cudaError_t r = cudaFuncSetAttribute(fields_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(FIELDS_SMEM));
     if (r != cudaSuccess) return r;
+    if ((r = cudaFuncSetAttribute(tile_stv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  TV_SMEM)) != cudaSuccess)
+      return r;
     int b = 0;
     if ((r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fields_kernel, NT, FIELDS_SMEM)) !=
         cudaSuccess)
@@ -2619,8 +2652,8 @@ cudaError_t launch_fields(const ParseParams& p, FAgg* agg, uint64_t* out, cudaSt
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (p.n_tiles) {
     const uint32_t gv = uint32_t(std::min<uint64_t>((p.n_tiles + TV_NT / 32 - 1) / (TV_NT / 32),
-                                                    uint64_t(n_sm) * 6));
-    tile_stv_kernel<<<gv, TV_NT, LUT_BYTES, stream>>>(p);
+                                                    uint64_t(n_sm) * 3));
+    tile_stv_kernel<<<gv, TV_NT, TV_SMEM, stream>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     tile_state_kernel<<<p.s.n_tstate_blocks, TS_NT, 0, stream>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
